@@ -1,0 +1,362 @@
+// libkvc C ABI: argument validation, workspace planning and dispatch onto the caller's
+// stream.  Every entry point validates on the host before enqueuing anything and reports
+// failures as kvc_status codes; no exception crosses the boundary.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+namespace {
+thread_local char t_err[512] = {0};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kvc_status fail(kvc_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+kvc_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return KVC_OK;
+  return fail(KVC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+kvc_status check_desc(const kvc_kv_desc* kv, const char* name) {
+  if (!kv) return fail(KVC_ERR_INVALID_ARG, "%s: descriptor is NULL", name);
+  if (kv->B < 1 || kv->H < 1 || kv->KVH < 1 || kv->S < 1)
+    return fail(KVC_ERR_INVALID_ARG, "%s: B, H, KVH and S must be >= 1", name);
+  if (kv->H % kv->KVH != 0) return fail(KVC_ERR_INVALID_ARG, "%s: H %% KVH != 0", name);
+  if (kv->D != 64 && kv->D != 128) return fail(KVC_ERR_UNSUPPORTED, "%s: head_dim must be 64 or 128", name);
+  if (kv->S > (int64_t)INT32_MAX - 64) return fail(KVC_ERR_UNSUPPORTED, "%s: S too large", name);
+  if (kv->stride_b % 8 || kv->stride_h % 8 || kv->stride_s % 8)
+    return fail(KVC_ERR_INVALID_ARG, "%s: strides must be multiples of 8 elements", name);
+  if (kv->stride_s < kv->D) return fail(KVC_ERR_INVALID_ARG, "%s: stride_s < D", name);
+  if (kv->stride_b < 0 || kv->stride_h < 0) return fail(KVC_ERR_INVALID_ARG, "%s: negative stride", name);
+  return KVC_OK;
+}
+
+// byte range [lo, hi) touched by a strided cache
+void cache_range(const void* base, const kvc_kv_desc& kv, uintptr_t* lo, uintptr_t* hi) {
+  const uintptr_t b = reinterpret_cast<uintptr_t>(base);
+  const int64_t last = (kv.B - 1) * kv.stride_b + (kv.KVH - 1) * kv.stride_h + (kv.S - 1) * kv.stride_s + kv.D;
+  *lo = b;
+  *hi = b + (uintptr_t)last * 2;
+}
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+kvc_status check_ptr(const void* p, const char* what) {
+  if (!p) return fail(KVC_ERR_INVALID_ARG, "%s is NULL", what);
+  if (!aligned16(p)) return fail(KVC_ERR_INVALID_ARG, "%s is not 16-byte aligned", what);
+  return KVC_OK;
+}
+
+kvc_status check_ws(void* ws, size_t have, size_t need, const char* what) {
+  if (need == 0) return KVC_OK;
+  if (!ws || have < need)
+    return fail(KVC_ERR_WORKSPACE, "%s: workspace of %zu bytes needed (%zu given)", what, need, ws ? have : 0);
+  if (!aligned16(ws)) return fail(KVC_ERR_INVALID_ARG, "%s: workspace not 16-byte aligned", what);
+  return KVC_OK;
+}
+
+#define KVC_TRY(x)                  \
+  do {                              \
+    const kvc_status _s = (x);      \
+    if (_s != KVC_OK) return _s;    \
+  } while (0)
+
+kvc_status check_window(const kvc_kv_desc* kv, int32_t w, const char* name) {
+  if (w < 1 || (int64_t)w > kv->S) return fail(KVC_ERR_INVALID_ARG, "%s: need 1 <= w <= S", name);
+  if ((int64_t)w * (kv->H / kv->KVH) > 512)
+    return fail(KVC_ERR_UNSUPPORTED, "%s: w * H / KVH must be <= 512", name);
+  return KVC_OK;
+}
+
+kvc_status check_sh(const kvc_sh_state* st) {
+  if (!st) return fail(KVC_ERR_INVALID_ARG, "scissorhands state is NULL");
+  if (st->B < 1 || st->KVH < 1 || st->cap < 32 || st->cap % 32)
+    return fail(KVC_ERR_INVALID_ARG, "scissorhands: B, KVH >= 1 and cap a positive multiple of 32");
+  if (st->history < 1 || st->history > 4096) return fail(KVC_ERR_INVALID_ARG, "scissorhands: history in [1, 4096]");
+  if (!st->hist || !st->low_count || !st->insert_step || !st->live || !st->slot)
+    return fail(KVC_ERR_INVALID_ARG, "scissorhands: a state buffer is NULL");
+  if (st->t < 0 || st->t > INT32_MAX) return fail(KVC_ERR_INVALID_ARG, "scissorhands: step counter out of range");
+  return KVC_OK;
+}
+
+}  // namespace
+
+void set_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+}  // namespace kvc
+
+using namespace kvc;
+
+extern "C" {
+
+int32_t kvc_version(void) { return 10000; }
+
+const char* kvc_status_string(kvc_status s) {
+  switch (s) {
+    case KVC_OK: return "ok";
+    case KVC_ERR_INVALID_ARG: return "invalid argument";
+    case KVC_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVC_ERR_CUDA: return "CUDA error";
+    case KVC_ERR_TIMEOUT: return "device wait timed out";
+    case KVC_ERR_DEVICE_BOUNDS: return "device index out of range";
+    case KVC_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+const char* kvc_last_error_message(void) { return t_err; }
+
+size_t kvc_workspace_size(kvc_op op, const kvc_kv_desc* kv, int32_t w, int32_t k) {
+  if (op == KVC_OP_TOPK_SELECT || op == KVC_OP_SCISSORHANDS_EVICT) return 0;
+  if (!kv || check_desc(kv, "kvc_workspace_size") != KVC_OK) return (size_t)-1;
+  switch (op) {
+    case KVC_OP_WINDOW_SCORES:
+      if (check_window(kv, w, "kvc_workspace_size") != KVC_OK) return (size_t)-1;
+      return scores_workspace(*kv, w, KVC_REDUCE_ALL_HEADS);
+    case KVC_OP_COMPRESS_PREFILL:
+      if (check_window(kv, w, "kvc_workspace_size") != KVC_OK) return (size_t)-1;
+      return scores_workspace(*kv, w, KVC_REDUCE_ALL_HEADS);
+    case KVC_OP_TOVA_DECODE_STEP:
+    case KVC_OP_SCISSORHANDS_UPDATE:
+      return scores_workspace(*kv, 1, KVC_REDUCE_ALL_HEADS);
+    case KVC_OP_CHANNEL_SCORE:
+      return channel_score_workspace(*kv, k, k > 0);
+    default:
+      return (size_t)-1;
+  }
+}
+
+kvc_status kvc_window_scores(const kvc_bf16* q_win, const kvc_bf16* K, const kvc_kv_desc* kv,
+                             int32_t w, float scale, int32_t causal, const uint32_t* live_mask,
+                             kvc_head_reduce reduce, float* scores, void* ws, size_t ws_bytes,
+                             kvc_stream_t stream) {
+  KVC_TRY(check_desc(kv, "kvc_window_scores"));
+  KVC_TRY(check_window(kv, w, "kvc_window_scores"));
+  KVC_TRY(check_ptr(q_win, "q_win"));
+  KVC_TRY(check_ptr(K, "K"));
+  KVC_TRY(check_ptr(scores, "scores"));
+  if (live_mask && !aligned16(live_mask)) return fail(KVC_ERR_INVALID_ARG, "live_mask not 16-byte aligned");
+  if (reduce != KVC_REDUCE_GQA_GROUP && reduce != KVC_REDUCE_ALL_HEADS)
+    return fail(KVC_ERR_INVALID_ARG, "unknown head reduction");
+  if (!(scale > 0.f) || scale != scale) return fail(KVC_ERR_INVALID_ARG, "scale must be > 0");
+  KVC_TRY(check_ws(ws, ws_bytes, scores_workspace(*kv, w, reduce), "kvc_window_scores"));
+  return cuda_status(launch_window_scores(q_win, K, *kv, w, scale, causal ? 1 : 0, live_mask, reduce,
+                                          scores, ws, (cudaStream_t)stream),
+                     "kvc_window_scores launch");
+}
+
+kvc_status kvc_topk_select(const float* scores, int32_t B, int32_t KVH, int64_t S, int32_t k,
+                           int32_t protect_tail, const uint32_t* live_mask, int32_t largest,
+                           int32_t* idx, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (B < 1 || KVH < 1 || S < 1 || k < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select: B, KVH, S, k must be >= 1");
+  if (S > (int64_t)INT32_MAX - 64) return fail(KVC_ERR_UNSUPPORTED, "kvc_topk_select: S too large");
+  if ((int64_t)B * KVH > 2147483647LL) return fail(KVC_ERR_UNSUPPORTED, "kvc_topk_select: too many rows");
+  if (protect_tail < 0 || protect_tail > k || (int64_t)protect_tail > S)
+    return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select: need 0 <= protect_tail <= min(k, S)");
+  if (protect_tail && !largest) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select: protect_tail needs largest=1");
+  KVC_TRY(check_ptr(scores, "scores"));
+  if (!idx) return fail(KVC_ERR_INVALID_ARG, "idx is NULL");
+  if (live_mask && !aligned16(live_mask)) return fail(KVC_ERR_INVALID_ARG, "live_mask not 16-byte aligned");
+  return cuda_status(launch_topk(scores, B, KVH, S, k, protect_tail, live_mask, largest ? 1 : 0, idx,
+                                 (cudaStream_t)stream),
+                     "kvc_topk_select launch");
+}
+
+kvc_status kvc_compact_kv(const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_desc* kv,
+                          const int32_t* idx, int32_t k, kvc_bf16* K_out, kvc_bf16* V_out,
+                          kvc_stream_t stream) {
+  KVC_TRY(check_desc(kv, "kvc_compact_kv"));
+  if (k < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_compact_kv: k must be >= 1");
+  KVC_TRY(check_ptr(K, "K"));
+  KVC_TRY(check_ptr(K_out, "K_out"));
+  if (!idx) return fail(KVC_ERR_INVALID_ARG, "idx is NULL");
+  if ((V == nullptr) != (V_out == nullptr)) return fail(KVC_ERR_INVALID_ARG, "V and V_out must both be given or both NULL");
+  if (V) {
+    KVC_TRY(check_ptr(V, "V"));
+    KVC_TRY(check_ptr(V_out, "V_out"));
+  }
+  uintptr_t k0, k1, v0 = 0, v1 = 0;
+  cache_range(K, *kv, &k0, &k1);
+  if (V) cache_range(V, *kv, &v0, &v1);
+  const uintptr_t osz = (uintptr_t)kv->B * kv->KVH * (uintptr_t)k * kv->D * 2;
+  const uintptr_t ko = reinterpret_cast<uintptr_t>(K_out), vo = reinterpret_cast<uintptr_t>(V_out);
+  if (overlaps(ko, ko + osz, k0, k1) || (V && (overlaps(ko, ko + osz, v0, v1) || overlaps(vo, vo + osz, k0, k1) ||
+                                               overlaps(vo, vo + osz, v0, v1) || overlaps(ko, ko + osz, vo, vo + osz))))
+    return fail(KVC_ERR_INVALID_ARG, "kvc_compact_kv: outputs overlap inputs");
+  return cuda_status(launch_compact(K, V, *kv, idx, k, K_out, V_out, (cudaStream_t)stream), "kvc_compact_kv launch");
+}
+
+kvc_status kvc_compress_prefill(const kvc_bf16* q_win, const kvc_bf16* K, const kvc_bf16* V,
+                                const kvc_kv_desc* kv, int32_t w, float scale,
+                                kvc_head_reduce reduce, int32_t k, int32_t protect_tail,
+                                float* scores, int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out,
+                                void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_TRY(check_desc(kv, "kvc_compress_prefill"));
+  if (k < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill: k must be >= 1");
+  if (protect_tail < 0 || protect_tail > k || protect_tail > w)
+    return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill: need 0 <= protect_tail <= min(k, w)");
+  KVC_TRY(kvc_window_scores(q_win, K, kv, w, scale, 1, nullptr, reduce, scores, ws, ws_bytes, stream));
+  KVC_TRY(kvc_topk_select(scores, kv->B, kv->KVH, kv->S, k, protect_tail, nullptr, 1, idx, nullptr, 0, stream));
+  return kvc_compact_kv(K, V, kv, idx, k, K_out, V_out, stream);
+}
+
+kvc_status kvc_write_slots(const kvc_bf16* k_new, const kvc_bf16* v_new, const int32_t* slot,
+                           kvc_bf16* K, kvc_bf16* V, const kvc_kv_desc* kv, kvc_stream_t stream) {
+  KVC_TRY(check_desc(kv, "kvc_write_slots"));
+  KVC_TRY(check_ptr(k_new, "k_new"));
+  KVC_TRY(check_ptr(K, "K"));
+  if (!slot) return fail(KVC_ERR_INVALID_ARG, "slot is NULL");
+  if ((v_new == nullptr) != (V == nullptr)) return fail(KVC_ERR_INVALID_ARG, "v_new and V must both be given or both NULL");
+  if (V) {
+    KVC_TRY(check_ptr(v_new, "v_new"));
+    KVC_TRY(check_ptr(V, "V"));
+  }
+  return cuda_status(launch_write_slots(k_new, v_new, slot, K, V, *kv, (cudaStream_t)stream), "kvc_write_slots launch");
+}
+
+kvc_status kvc_tova_decode_step(const kvc_bf16* q_new, const kvc_bf16* k_new,
+                                const kvc_bf16* v_new, kvc_bf16* K, kvc_bf16* V,
+                                const kvc_kv_desc* kv, float scale, int32_t* free_slot,
+                                float* scores, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_TRY(check_desc(kv, "kvc_tova_decode_step"));
+  if (!free_slot) return fail(KVC_ERR_INVALID_ARG, "free_slot is NULL");
+  KVC_TRY(check_ptr(scores, "scores"));
+  KVC_TRY(check_ws(ws, ws_bytes, scores_workspace(*kv, 1, KVC_REDUCE_ALL_HEADS), "kvc_tova_decode_step"));
+  KVC_TRY(kvc_write_slots(k_new, v_new, free_slot, K, V, kv, stream));
+  KVC_TRY(kvc_window_scores(q_new, K, kv, 1, scale, 0, nullptr, KVC_REDUCE_ALL_HEADS, scores, ws, ws_bytes, stream));
+  return kvc_topk_select(scores, kv->B, kv->KVH, kv->S, 1, 0, nullptr, 0, free_slot, nullptr, 0, stream);
+}
+
+kvc_status kvc_scissorhands_init(kvc_sh_state* st, int32_t n_live, kvc_stream_t stream) {
+  KVC_TRY(check_sh(st));
+  if (n_live < 0 || n_live > st->cap) return fail(KVC_ERR_INVALID_ARG, "scissorhands_init: n_live in [0, cap]");
+  st->t = 0;
+  st->n_free = st->cap - n_live;
+  return cuda_status(launch_sh_init(*st, n_live, (cudaStream_t)stream), "kvc_scissorhands_init launch");
+}
+
+kvc_status kvc_scissorhands_update_from_probs(kvc_sh_state* st, const float* p, kvc_stream_t stream) {
+  KVC_TRY(check_sh(st));
+  KVC_TRY(check_ptr(p, "p"));
+  const kvc_status s = cuda_status(launch_sh_record(*st, p, (cudaStream_t)stream), "scissorhands record launch");
+  if (s == KVC_OK) st->t += 1;
+  return s;
+}
+
+kvc_status kvc_scissorhands_update(kvc_sh_state* st, const kvc_bf16* q_new, const kvc_bf16* k_new,
+                                   const kvc_bf16* v_new, kvc_bf16* K, kvc_bf16* V,
+                                   const kvc_kv_desc* kv, float scale, float* probs, void* ws,
+                                   size_t ws_bytes, kvc_stream_t stream) {
+  KVC_TRY(check_sh(st));
+  KVC_TRY(check_desc(kv, "kvc_scissorhands_update"));
+  if (kv->B != st->B || kv->KVH != st->KVH || kv->S != st->cap)
+    return fail(KVC_ERR_INVALID_ARG, "scissorhands_update: cache shape does not match the state");
+  if (st->n_free <= 0) return fail(KVC_ERR_INVALID_ARG, "scissorhands_update: no free slot (evict first)");
+  KVC_TRY(check_ptr(q_new, "q_new"));
+  KVC_TRY(check_ptr(k_new, "k_new"));
+  KVC_TRY(check_ptr(K, "K"));
+  KVC_TRY(check_ptr(probs, "probs"));
+  if ((v_new == nullptr) != (V == nullptr)) return fail(KVC_ERR_INVALID_ARG, "v_new and V must both be given or both NULL");
+  KVC_TRY(check_ws(ws, ws_bytes, scores_workspace(*kv, 1, KVC_REDUCE_GQA_GROUP), "kvc_scissorhands_update"));
+  KVC_TRY(cuda_status(launch_sh_insert(*st, k_new, v_new, K, V, *kv, (cudaStream_t)stream), "scissorhands insert launch"));
+  st->n_free -= 1;
+  KVC_TRY(kvc_window_scores(q_new, K, kv, 1, scale, 0, st->live, KVC_REDUCE_GQA_GROUP, probs, ws, ws_bytes, stream));
+  return kvc_scissorhands_update_from_probs(st, probs, stream);
+}
+
+kvc_status kvc_scissorhands_evict(kvc_sh_state* st, int32_t m, int32_t* evicted, kvc_stream_t stream) {
+  KVC_TRY(check_sh(st));
+  if (m < 1 || m > st->cap) return fail(KVC_ERR_INVALID_ARG, "scissorhands_evict: m in [1, cap]");
+  if (st->t < 1) return fail(KVC_ERR_INVALID_ARG, "scissorhands_evict: no step recorded yet");
+  if (!evicted) return fail(KVC_ERR_INVALID_ARG, "evicted is NULL");
+  const kvc_status s = cuda_status(launch_sh_evict(*st, m, evicted, (cudaStream_t)stream), "scissorhands evict launch");
+  if (s == KVC_OK) st->n_free = std::min(st->cap, st->n_free + m);
+  return s;
+}
+
+kvc_status kvc_channel_score(const kvc_bf16* q_win, int32_t w, const kvc_bf16* K,
+                             const kvc_kv_desc* kv, const int32_t* idx, int32_t k, float* cs,
+                             void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_TRY(check_desc(kv, "kvc_channel_score"));
+  if (w < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_score: w must be >= 1");
+  if (idx && k < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_score: k must be >= 1 with idx");
+  KVC_TRY(check_ptr(q_win, "q_win"));
+  KVC_TRY(check_ptr(K, "K"));
+  if (!cs) return fail(KVC_ERR_INVALID_ARG, "cs is NULL");
+  KVC_TRY(check_ws(ws, ws_bytes, channel_score_workspace(*kv, idx ? k : 0, idx != nullptr), "kvc_channel_score"));
+  return cuda_status(launch_channel_score(q_win, w, K, *kv, idx, idx ? k : 0, cs, ws, (cudaStream_t)stream),
+                     "kvc_channel_score launch");
+}
+
+kvc_status kvc_channel_prune(const float* cs, const kvc_bf16* K, const kvc_kv_desc* kv,
+                             int32_t C, int32_t zero_mode, int32_t* ch_idx, kvc_bf16* K_out,
+                             kvc_stream_t stream) {
+  KVC_TRY(check_desc(kv, "kvc_channel_prune"));
+  if (C < 1 || C > kv->D) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune: need 1 <= C <= D");
+  if (!zero_mode && C % 8) return fail(KVC_ERR_UNSUPPORTED, "kvc_channel_prune: compact mode needs C %% 8 == 0");
+  if (!cs || !ch_idx) return fail(KVC_ERR_INVALID_ARG, "cs and ch_idx must be given");
+  KVC_TRY(check_ptr(K, "K"));
+  KVC_TRY(check_ptr(K_out, "K_out"));
+  uintptr_t k0, k1;
+  cache_range(K, *kv, &k0, &k1);
+  const uintptr_t ko = reinterpret_cast<uintptr_t>(K_out);
+  const uintptr_t osz = (uintptr_t)kv->B * kv->KVH * (uintptr_t)kv->S * (zero_mode ? kv->D : C) * 2;
+  if (zero_mode) {
+    const bool dense = kv->stride_s == kv->D && kv->stride_h == kv->S * kv->D && kv->stride_b == kv->KVH * kv->S * kv->D;
+    if (!(ko == k0 && dense) && overlaps(ko, ko + osz, k0, k1))
+      return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune: K_out overlaps K (in place needs K_out == K, dense)");
+  } else if (overlaps(ko, ko + osz, k0, k1)) {
+    return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune: K_out overlaps K");
+  }
+  return cuda_status(launch_channel_prune(cs, K, *kv, C, zero_mode ? 1 : 0, ch_idx, K_out, (cudaStream_t)stream),
+                     "kvc_channel_prune launch");
+}
+
+kvc_status kvc_get_device_status(kvc_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e, "kvc_get_device_status sync");
+  cudaError_t (*takers[])(unsigned int*) = {take_status_scores, take_status_select, take_status_gather,
+                                            take_status_scissorhands};
+  unsigned int first = 0u;
+  for (auto fn : takers) {
+    unsigned int v = 0u;
+    e = fn(&v);
+    if (e != cudaSuccess) return cuda_status(e, "kvc_get_device_status read");
+    if (first == 0u) first = v;
+  }
+  if (first != 0u) return fail((kvc_status)first, "device status: %s", kvc_status_string((kvc_status)first));
+  return KVC_OK;
+}
+
+}  // extern "C"

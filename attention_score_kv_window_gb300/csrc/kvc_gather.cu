@@ -1,0 +1,336 @@
+// Memory-bound row movers: K/V gather-compaction, slot writes, and the ThinK key-channel
+// score and pruning ("Add ThinK_Press", kvpress PR 18).  All rows are moved as 16-byte
+// vectors (8 bf16); grids are sized in multiples of the SM count and grid-stride.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+namespace {
+
+__device__ __forceinline__ uint4 ld16(const uint16_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+__device__ __forceinline__ void st16(uint16_t* p, uint4 v) { __stcs(reinterpret_cast<uint4*>(p), v); }
+
+// ----------------------------------------------------------------------------------------
+// compaction: Ko[b,kvh,t] = K[b,kvh,idx[b,kvh,t]] (V likewise); -1 -> zero row
+// ----------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) k_compact(const uint16_t* __restrict__ K,
+                                                 const uint16_t* __restrict__ V, int64_t sb,
+                                                 int64_t sh, int64_t ss, int KVH, int64_t S,
+                                                 const int32_t* __restrict__ idx, int k,
+                                                 int64_t rows, uint16_t* __restrict__ Ko,
+                                                 uint16_t* __restrict__ Vo) {
+  constexpr int TPR = D / 8;  // 16-byte chunks per row
+  constexpr int U = 4;        // chunks in flight per thread
+  const int64_t total = rows * TPR;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t x0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x0 < total; x0 += stride * U) {
+    uint4 kv[U], vv[U];
+    int64_t orow[U];
+    int cc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t x = x0 + (int64_t)u * stride;
+      orow[u] = -1;
+      kv[u] = make_uint4(0, 0, 0, 0);
+      vv[u] = kv[u];
+      if (x < total) {
+        const int64_t row = x / TPR;
+        cc[u] = (int)(x % TPR);
+        orow[u] = row;
+        const int32_t j = __ldg(idx + row);
+        if (j >= 0 && j < S) {
+          const int64_t bk = row / k;
+          const int64_t b = bk / KVH, kvh = bk % KVH;
+          const int64_t off = b * sb + kvh * sh + (int64_t)j * ss + cc[u] * 8;
+          kv[u] = ld16(K + off);
+          if (V) vv[u] = ld16(V + off);
+        } else if (j >= S || j < -1) {
+          set_device_status(KVC_ERR_DEVICE_BOUNDS);
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (orow[u] >= 0) {
+        st16(Ko + orow[u] * D + cc[u] * 8, kv[u]);
+        if (Vo) st16(Vo + orow[u] * D + cc[u] * 8, vv[u]);
+      }
+    }
+  }
+}
+
+template <int D>
+__global__ void k_write_slots(const uint16_t* __restrict__ kn, const uint16_t* __restrict__ vn,
+                              const int32_t* __restrict__ slot, uint16_t* K, uint16_t* V, int64_t sb,
+                              int64_t sh, int64_t ss, int KVH, int64_t S, int rows) {
+  constexpr int TPR = D / 8;
+  const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= rows * TPR) return;
+  const int row = x / TPR, c = x % TPR;
+  const int32_t j = slot[row];
+  if (j < 0 || j >= S) {
+    set_device_status(KVC_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const int64_t b = row / KVH, kvh = row % KVH;
+  const int64_t off = b * sb + kvh * sh + (int64_t)j * ss + c * 8;
+  *reinterpret_cast<uint4*>(K + off) = ld16(kn + (int64_t)row * D + c * 8);
+  if (V) *reinterpret_cast<uint4*>(V + off) = ld16(vn + (int64_t)row * D + c * 8);
+}
+
+// ----------------------------------------------------------------------------------------
+// ThinK channel score: cs = (mean over group of sum_i q^2) * sum_j k^2 (per channel)
+// ----------------------------------------------------------------------------------------
+__device__ __forceinline__ void acc_sq8(float* acc, uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16);
+    const float hi = __uint_as_float(w[i] & 0xffff0000u);
+    acc[2 * i] = fmaf(lo, lo, acc[2 * i]);
+    acc[2 * i + 1] = fmaf(hi, hi, acc[2 * i + 1]);
+  }
+}
+
+// partial key sums over one range of rows: part[split][b*KVH+kvh][D]
+template <int D>
+__global__ void __launch_bounds__(256) k_channel_partial(const uint16_t* __restrict__ K, int64_t sb,
+                                                         int64_t sh, int64_t ss, int64_t S,
+                                                         const int32_t* __restrict__ idx, int k,
+                                                         int64_t nrows, int64_t chunk,
+                                                         float* __restrict__ part, int KVH) {
+  constexpr int TPR = D / 8;
+  constexpr int RPP = 256 / TPR;  // rows per pass
+  __shared__ float red[RPP][D + 1];
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int bk = b * KVH + kvh;
+  const int c = threadIdx.x % TPR, rl = threadIdx.x / TPR;
+  const int64_t r0 = (int64_t)split * chunk, r1 = std::min(nrows, r0 + chunk);
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  const uint16_t* Kb = K + b * sb + kvh * sh;
+  for (int64_t r = r0 + rl; r < r1; r += RPP) {
+    int64_t j = r;
+    if (idx) {
+      j = __ldg(idx + (int64_t)bk * k + r);
+      if (j < 0) continue;
+      if (j >= S) { set_device_status(KVC_ERR_DEVICE_BOUNDS); continue; }
+    }
+    acc_sq8(acc, ld16(Kb + j * ss + c * 8));
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[rl][c * 8 + i] = acc[i];
+  __syncthreads();
+  for (int d = threadIdx.x; d < D; d += 256) {
+    float s = 0.f;
+    for (int q = 0; q < RPP; ++q) s += red[q][d];
+    part[((int64_t)split * gridDim.z * KVH + bk) * D + d] = s;
+  }
+}
+
+__global__ void k_channel_final(const uint16_t* __restrict__ q, int H, int KVH, int w, int D,
+                                const float* __restrict__ part, int nsplit, int B, float* __restrict__ cs) {
+  const int bk = blockIdx.x;
+  const int b = bk / KVH, kvh = bk % KVH;
+  const int G = H / KVH;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float kn = 0.f;
+    for (int s = 0; s < nsplit; ++s) kn += part[((int64_t)s * B * KVH + bk) * D + d];
+    float qn = 0.f;
+    for (int h = kvh * G; h < (kvh + 1) * G; ++h) {
+      const uint16_t* qh = q + ((int64_t)(b * H + h) * w) * D + d;
+      float sh = 0.f;
+      for (int i = 0; i < w; ++i) {
+        const float v = __uint_as_float((uint32_t)qh[(int64_t)i * D] << 16);
+        sh = fmaf(v, v, sh);
+      }
+      qn += sh;
+    }
+    cs[(int64_t)bk * D + d] = (qn / (float)G) * kn;
+  }
+}
+
+// ----------------------------------------------------------------------------------------
+// ThinK channel pruning
+// ----------------------------------------------------------------------------------------
+// keep the C highest channel scores (ties: lower channel), ascending list
+__global__ void k_channel_select(const float* __restrict__ cs, int D, int C, int32_t* __restrict__ ch) {
+  __shared__ float v[128];
+  __shared__ uint32_t wb[4];
+  const int bk = blockIdx.x, d = threadIdx.x;  // blockDim = 128
+  if (d < D) v[d] = cs[(int64_t)bk * D + d];
+  __syncthreads();
+  bool sel = false;
+  if (d < D) {
+    const float x = v[d];
+    int rank = 0;
+    for (int e = 0; e < D; ++e) {
+      const float y = v[e];
+      rank += (y > x) || (y == x && e < d);
+    }
+    sel = rank < C;
+  }
+  const uint32_t bal = __ballot_sync(0xffffffffu, sel);
+  const int lane = d & 31, warp = d >> 5;
+  if (lane == 0) wb[warp] = __popc(bal);
+  __syncthreads();
+  int base = 0;
+  for (int q = 0; q < warp; ++q) base += wb[q];
+  if (sel) ch[(int64_t)bk * C + base + __popc(bal & ((1u << lane) - 1u))] = d;
+}
+
+// compact mode: Ko[b,kvh,t,c] = K[b,kvh,t,ch[c]] — 32 rows per pass staged in shared memory
+template <int D>
+__global__ void __launch_bounds__(256) k_channel_gather(const uint16_t* __restrict__ K, int64_t sb,
+                                                        int64_t sh, int64_t ss, int64_t S, int KVH,
+                                                        const int32_t* __restrict__ ch, int C,
+                                                        uint16_t* __restrict__ Ko) {
+  constexpr int TPR = D / 8, RB = 32;
+  __shared__ __align__(16) uint16_t tile[RB][D + 8];
+  __shared__ int32_t chs[128];
+  const int bk = blockIdx.y;
+  const int64_t b = bk / KVH, kvh = bk % KVH;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) chs[c] = ch[(int64_t)bk * C + c];
+  const uint16_t* Kb = K + b * sb + kvh * sh;
+  uint16_t* Ob = Ko + (int64_t)bk * S * C;
+  const int out_chunks = C / 8;
+  for (int64_t r0 = (int64_t)blockIdx.x * RB; r0 < S; r0 += (int64_t)gridDim.x * RB) {
+    __syncthreads();
+    for (int x = threadIdx.x; x < RB * TPR; x += blockDim.x) {
+      const int r = x / TPR, c = x % TPR;
+      if (r0 + r < S) *reinterpret_cast<uint4*>(&tile[r][c * 8]) = ld16(Kb + (r0 + r) * ss + c * 8);
+    }
+    __syncthreads();
+    for (int x = threadIdx.x; x < RB * out_chunks; x += blockDim.x) {
+      const int r = x / out_chunks, oc = x % out_chunks;
+      if (r0 + r >= S) continue;
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = tile[r][chs[oc * 8 + 2 * i] & (D - 1)];
+        const uint32_t hi = tile[r][chs[oc * 8 + 2 * i + 1] & (D - 1)];
+        w[i] = lo | (hi << 16);
+      }
+      st16(Ob + (r0 + r) * C + oc * 8, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+  }
+}
+
+// zero mode: Ko = K with unselected channels zeroed (Ko dense [B,KVH,S,D]; may equal K)
+template <int D>
+__global__ void __launch_bounds__(256) k_channel_zero(const uint16_t* K, int64_t sb, int64_t sh,
+                                                      int64_t ss, int64_t S, int KVH,
+                                                      const int32_t* __restrict__ ch, int C,
+                                                      uint16_t* Ko) {
+  constexpr int TPR = D / 8;
+  __shared__ uint32_t keepw[4];
+  const int bk = blockIdx.y;
+  const int64_t b = bk / KVH, kvh = bk % KVH;
+  if (threadIdx.x < 4) keepw[threadIdx.x] = 0;
+  __syncthreads();
+  for (int c = threadIdx.x; c < C; c += blockDim.x) {
+    const int d = ch[(int64_t)bk * C + c] & (D - 1);
+    atomicOr(&keepw[d >> 5], 1u << (d & 31));
+  }
+  __syncthreads();
+  const uint16_t* Kb = K + b * sb + kvh * sh;
+  uint16_t* Ob = Ko + (int64_t)bk * S * D;
+  const int64_t total = S * TPR;
+  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = x / TPR;
+    const int c = (int)(x % TPR);
+    uint4 v = *reinterpret_cast<const uint4*>(Kb + r * ss + c * 8);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int d0 = c * 8 + 2 * i, d1 = d0 + 1;
+      if (!((keepw[d0 >> 5] >> (d0 & 31)) & 1u)) w[i] &= 0xffff0000u;
+      if (!((keepw[d1 >> 5] >> (d1 & 31)) & 1u)) w[i] &= 0x0000ffffu;
+    }
+    *reinterpret_cast<uint4*>(Ob + r * D + c * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+int channel_splits(const kvc_kv_desc& kv, int64_t nrows) {
+  const int64_t units = (int64_t)kv.B * kv.KVH;
+  const int64_t target = (int64_t)num_sms() * 4;
+  int64_t ns = std::max<int64_t>(1, (target + units - 1) / units);
+  ns = std::min<int64_t>(ns, std::max<int64_t>(1, nrows / 64));
+  return (int)ns;
+}
+
+}  // namespace
+
+cudaError_t launch_compact(const uint16_t* K, const uint16_t* V, const kvc_kv_desc& kv,
+                           const int32_t* idx, int k, uint16_t* Ko, uint16_t* Vo, cudaStream_t st) {
+  const int64_t rows = (int64_t)kv.B * kv.KVH * k;
+  const int64_t chunks = rows * (kv.D / 8);
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((chunks + 1023) / 1024, (int64_t)num_sms() * 16));
+  if (kv.D == 64)
+    k_compact<64><<<blocks, 256, 0, st>>>(K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, idx, k, rows, Ko, Vo);
+  else
+    k_compact<128><<<blocks, 256, 0, st>>>(K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, idx, k, rows, Ko, Vo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_write_slots(const uint16_t* kn, const uint16_t* vn, const int32_t* slot,
+                               uint16_t* K, uint16_t* V, const kvc_kv_desc& kv, cudaStream_t st) {
+  const int rows = kv.B * kv.KVH;
+  const int n = rows * (kv.D / 8);
+  const int blocks = (n + 255) / 256;
+  if (kv.D == 64)
+    k_write_slots<64><<<blocks, 256, 0, st>>>(kn, vn, slot, K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, rows);
+  else
+    k_write_slots<128><<<blocks, 256, 0, st>>>(kn, vn, slot, K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, rows);
+  return cudaGetLastError();
+}
+
+size_t channel_score_workspace(const kvc_kv_desc& kv, int k, bool has_idx) {
+  const int64_t nrows = has_idx ? k : kv.S;
+  const int ns = channel_splits(kv, nrows);
+  return (size_t)ns * kv.B * kv.KVH * kv.D * sizeof(float);
+}
+
+cudaError_t launch_channel_score(const uint16_t* q, int w, const uint16_t* K, const kvc_kv_desc& kv,
+                                 const int32_t* idx, int k, float* cs, void* ws, cudaStream_t st) {
+  const int64_t nrows = idx ? k : kv.S;
+  const int ns = channel_splits(kv, nrows);
+  const int64_t chunk = (nrows + ns - 1) / ns;
+  float* part = static_cast<float*>(ws);
+  dim3 grid(ns, kv.KVH, kv.B);
+  if (kv.D == 64)
+    k_channel_partial<64><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, idx, k, nrows, chunk, part, kv.KVH);
+  else
+    k_channel_partial<128><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, idx, k, nrows, chunk, part, kv.KVH);
+  k_channel_final<<<kv.B * kv.KVH, 128, 0, st>>>(q, kv.H, kv.KVH, w, kv.D, part, ns, kv.B, cs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_channel_prune(const float* cs, const uint16_t* K, const kvc_kv_desc& kv, int C,
+                                 int zero_mode, int32_t* ch, uint16_t* Ko, cudaStream_t st) {
+  const int rows = kv.B * kv.KVH;
+  k_channel_select<<<rows, 128, 0, st>>>(cs, kv.D, C, ch);
+  const int per = (int)std::max<int64_t>(1, std::min<int64_t>((kv.S + 31) / 32, ((int64_t)num_sms() * 8 + rows - 1) / rows));
+  dim3 grid(per, rows);
+  if (zero_mode) {
+    if (kv.D == 64)
+      k_channel_zero<64><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, kv.KVH, ch, C, Ko);
+    else
+      k_channel_zero<128><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, kv.KVH, ch, C, Ko);
+  } else {
+    if (kv.D == 64)
+      k_channel_gather<64><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, kv.KVH, ch, C, Ko);
+    else
+      k_channel_gather<128><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, kv.KVH, ch, C, Ko);
+  }
+  return cudaGetLastError();
+}
+
+KVC_TU_STATUS(gather)
+
+}  // namespace kvc

@@ -1,0 +1,82 @@
+// Internal declarations shared by the libkvc translation units (not part of the ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvc.h"
+
+namespace kvc {
+
+// Sticky device status: the first kernel that meets a bad index or gives up a bounded wait
+// records its code here; kvc_get_device_status() reads and clears it.  Each translation
+// unit has its own word (no relocatable device code needed); KVC_TU_STATUS(name) defines
+// the host function take_status_<name>() that reads and clears it.
+namespace {
+__device__ unsigned int g_device_status = 0u;
+__device__ __forceinline__ void set_device_status(unsigned int code) {
+  atomicCAS(&g_device_status, 0u, code);
+}
+inline cudaError_t take_tu_status(unsigned int* v) {
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_device_status, sizeof(unsigned int));
+  if (e != cudaSuccess || *v == 0u) return e;
+  const unsigned int z = 0u;
+  return cudaMemcpyToSymbol(g_device_status, &z, sizeof(unsigned int));
+}
+}  // namespace
+#define KVC_TU_STATUS(name) \
+  cudaError_t take_status_##name(unsigned int* v) { return take_tu_status(v); }
+cudaError_t take_status_scores(unsigned int* v);
+cudaError_t take_status_select(unsigned int* v);
+cudaError_t take_status_gather(unsigned int* v);
+cudaError_t take_status_scissorhands(unsigned int* v);
+
+// Host-side helpers
+int num_sms();                      // SM count of the current device (cached per device)
+void set_error(const char* fmt, ...);  // records the thread's last error message
+
+// ----------------------------------------------------------------------------------------
+// window scores (kvc_scores.cu)
+// ----------------------------------------------------------------------------------------
+struct ScoresPlan {
+  int R;         // query rows per (b,kvh): G*w
+  int Rpad;      // padded to the kernel's row tile
+  int nsplit;    // key ranges per (b,kvh)
+  int64_t chunk; // keys per range (multiple of the key tile)
+  size_t part_bytes;   // (m,l) partials
+  size_t group_bytes;  // per-group scores for the all-heads reduction
+};
+ScoresPlan plan_scores(const kvc_kv_desc& kv, int w, int reduce);
+size_t scores_workspace(const kvc_kv_desc& kv, int w, int reduce);
+cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc_kv_desc& kv, int w,
+                                 float scale, int causal, const uint32_t* live, int reduce,
+                                 float* scores, void* ws, cudaStream_t st);
+
+// ----------------------------------------------------------------------------------------
+// selection (kvc_select.cu)
+// ----------------------------------------------------------------------------------------
+cudaError_t launch_topk(const float* scores, int B, int KVH, int64_t S, int k, int protect_tail,
+                        const uint32_t* live, int largest, int32_t* idx, cudaStream_t st);
+cudaError_t launch_sh_evict(const kvc_sh_state& s, int m, int32_t* evicted, cudaStream_t st);
+
+// ----------------------------------------------------------------------------------------
+// gathers (kvc_gather.cu)
+// ----------------------------------------------------------------------------------------
+cudaError_t launch_compact(const uint16_t* K, const uint16_t* V, const kvc_kv_desc& kv,
+                           const int32_t* idx, int k, uint16_t* Ko, uint16_t* Vo, cudaStream_t st);
+cudaError_t launch_write_slots(const uint16_t* kn, const uint16_t* vn, const int32_t* slot,
+                               uint16_t* K, uint16_t* V, const kvc_kv_desc& kv, cudaStream_t st);
+size_t channel_score_workspace(const kvc_kv_desc& kv, int k, bool has_idx);
+cudaError_t launch_channel_score(const uint16_t* q, int w, const uint16_t* K, const kvc_kv_desc& kv,
+                                 const int32_t* idx, int k, float* cs, void* ws, cudaStream_t st);
+cudaError_t launch_channel_prune(const float* cs, const uint16_t* K, const kvc_kv_desc& kv, int C,
+                                 int zero_mode, int32_t* ch, uint16_t* Ko, cudaStream_t st);
+
+// ----------------------------------------------------------------------------------------
+// Scissorhands state kernels (kvc_scissorhands.cu)
+// ----------------------------------------------------------------------------------------
+cudaError_t launch_sh_init(const kvc_sh_state& s, int n_live, cudaStream_t st);
+cudaError_t launch_sh_insert(const kvc_sh_state& s, const uint16_t* kn, const uint16_t* vn,
+                             uint16_t* K, uint16_t* V, const kvc_kv_desc& kv, cudaStream_t st);
+cudaError_t launch_sh_record(const kvc_sh_state& s, const float* p, cudaStream_t st);
+
+}  // namespace kvc

@@ -1,0 +1,575 @@
+// Window-attention token scores: s = scale * q_win K^T, a softmax over the whole sequence,
+// then the sum over window rows of the head-mean probability ("Add TOVA press", SimJeg's
+// shape walk-through; cold-compress PR 11, attention mean-pooled over grouped queries).
+//
+// The [H, w, S] probabilities never reach memory.  Two passes over K per (b, kvh):
+//   pass 1 (queries on the MMA M axis): per query row, running max m and sum l of
+//           exp2(s*log2e - m) over one key range -> partial (m, l) per range;
+//   merge:  per row, combine the ranges -> c_r = M_r + log2(L_r)  (log2-domain normaliser);
+//   pass 2 (keys on the MMA M axis): per key j, sum_r exp2(s_rj*log2e - c_r), times 1/G.
+// Putting keys on M in pass 2 makes the reduction over query rows a per-thread sum plus a
+// 4-lane shuffle, so no cross-warp column reduction is needed.
+//
+// Both passes stage K tiles (64 keys x D) in shared memory with a 3-stage cp.async
+// pipeline and run bf16 mma.sync m16n8k16 with fp32 accumulation.
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+namespace {
+
+constexpr int TK = 64;        // keys per shared-memory tile
+constexpr int NTHREADS = 256; // 8 warps
+constexpr int STAGES = 3;
+constexpr int P1_MAX_ROWS = 256;  // query rows per pass-1 CTA (row groups beyond)
+constexpr int MAX_RPAD = 512;
+
+struct ScoresArgs {
+  const uint16_t* q;
+  const uint16_t* K;
+  int64_t sb, sh, ss;
+  int B, H, KVH, w, G, R, Rpad;
+  int64_t S;
+  int causal;
+  const uint32_t* live;
+  int64_t live_words;
+  float sl2;  // scale * log2(e)
+  int nsplit;
+  int64_t chunk;
+  float2* part;  // [B*KVH][nsplit][Rpad]  (m2, l)
+  float* mrow;   // [B*KVH][Rpad]          M2 + log2(L)  (+inf: no visible key)
+  float* out;    // [B*KVH][S]
+  float out_mul; // 1/G
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ bool live_bit(const uint32_t* lw, int64_t j) {
+  return (__ldg(lw + (j >> 5)) >> (j & 31)) & 1u;
+}
+// last key index row r may see (-1: padded row)
+__device__ __forceinline__ int64_t row_limit(const ScoresArgs& a, int r) {
+  if (r >= a.R) return -1;
+  return a.causal ? (a.S - a.w + (r % a.w)) : (a.S - 1);
+}
+
+// Stage K rows [kt0, kt0+TK) of one (b,kvh) into a shared tile (rows >= kend zero-filled).
+template <int D>
+__device__ __forceinline__ void load_k_tile(uint16_t* dst, const uint16_t* Kb, int64_t ss,
+                                            int64_t kt0, int64_t kend, int tid) {
+  constexpr int P = D + 8, CH = D / 8;
+#pragma unroll
+  for (int c = tid; c < TK * CH; c += NTHREADS) {
+    const int r = c / CH, cc = c % CH;
+    const int64_t j = kt0 + r;
+    const bool ok = j < kend;
+    const uint16_t* src = ok ? (Kb + j * ss + cc * 8) : Kb;
+    cp_async16(smem_u32(dst + r * P + cc * 8), src, ok ? 16 : 0);
+  }
+}
+
+// Stage query rows [row0, row0+rows) of the group (rows >= R zero-filled).
+template <int D>
+__device__ __forceinline__ void load_q_rows(uint16_t* dst, const uint16_t* Qg, int row0, int rows,
+                                            int R, int tid) {
+  constexpr int P = D + 8, CH = D / 8;
+  for (int c = tid; c < rows * CH; c += NTHREADS) {
+    const int r = c / CH, cc = c % CH;
+    const int gr = row0 + r;
+    const bool ok = gr < R;
+    const uint16_t* src = ok ? (Qg + (int64_t)gr * D + cc * 8) : Qg;
+    cp_async16(smem_u32(dst + r * P + cc * 8), src, ok ? 16 : 0);
+  }
+}
+
+// ----------------------------------------------------------------------------------------
+// pass 1: per-row (max, sum) over one key range
+// ----------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(NTHREADS) k_scores_pass1(const ScoresArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int P = D + 8, KS = D / 16;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y % a.KVH, rg = blockIdx.y / a.KVH;
+  const int b = blockIdx.z;
+  const int bk = b * a.KVH + kvh;
+  const int row0 = rg * P1_MAX_ROWS;
+  const int rows = min(P1_MAX_ROWS, a.Rpad - row0);
+  const int n_mt = rows >> 4;
+  const int64_t kbeg = (int64_t)split * a.chunk;
+  const int64_t kend = min(a.S, kbeg + a.chunk);
+  const int ntiles = (int)((kend - kbeg + TK - 1) / TK);
+
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* Ks = Qs + rows * P;
+  float2* mrg = reinterpret_cast<float2*>(Ks + STAGES * TK * P);  // [8][16]
+
+  const uint16_t* Kb = a.K + b * a.sb + kvh * a.sh;
+  const uint16_t* Qg = a.q + ((int64_t)(b * a.H + kvh * a.G) * a.w) * D;
+  const uint32_t* lw = a.live ? a.live + (int64_t)bk * a.live_words : nullptr;
+
+  load_q_rows<D>(Qs, Qg, row0, rows, a.R, tid);
+  cp_async_commit();
+#pragma unroll
+  for (int s = 0; s < STAGES - 1; ++s) {
+    if (s < ntiles) load_k_tile<D>(Ks + s * TK * P, Kb, a.ss, kbeg + (int64_t)s * TK, kend, tid);
+    cp_async_commit();
+  }
+
+  // warp roles: >= 8 m-tiles: each warp owns up to 2 m-tiles and all keys of a tile;
+  // fewer (1, 2 or 4): warps split the tile's 8 key n-tiles into kg groups.
+  int kg, n_my, mt0, mt1, nt_begin;
+  if (n_mt >= 8) {
+    kg = 1; mt0 = warp; mt1 = warp + 8; n_my = (mt1 < n_mt) ? 2 : 1; nt_begin = 0;
+  } else {
+    // kg = largest power of two with n_mt * kg <= 8; warps beyond n_mt * kg stay idle
+    kg = (n_mt == 1) ? 8 : (n_mt == 2 || n_mt == 3) ? 4 - 2 * (n_mt == 3) : (n_mt == 4) ? 2 : 1;
+    mt0 = warp % n_mt; mt1 = mt0; nt_begin = warp / n_mt;
+    n_my = (warp < n_mt * kg) ? 1 : 0;
+  }
+  const int nts = n_my ? 8 / kg : 0;  // n-tiles per warp per key tile
+
+  int64_t lim[2][2];
+  {
+    const int rA0 = row0 + mt0 * 16 + g, rA1 = row0 + mt1 * 16 + g;
+    lim[0][0] = row_limit(a, rA0);
+    lim[0][1] = row_limit(a, rA0 + 8);
+    lim[1][0] = row_limit(a, rA1);
+    lim[1][1] = row_limit(a, rA1 + 8);
+  }
+  float m_run[2][2], l_run[2][2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) { m_run[i][h] = -CUDART_INF_F; l_run[i][h] = 0.f; }
+
+  uint32_t aq[2][KS][4];
+  for (int it = 0; it < ntiles; ++it) {
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();
+    if (it == 0) {
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) {
+        const int mt = mi == 0 ? mt0 : mt1;
+        if (mi < n_my) {
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            const int r = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int c = ks * 16 + ((lane >> 4) & 1) * 8;
+            ldsm_x4(smem_u32(Qs + r * P + c), aq[mi][ks][0], aq[mi][ks][1], aq[mi][ks][2], aq[mi][ks][3]);
+          }
+        }
+      }
+    }
+    {
+      const int nx = it + STAGES - 1;
+      if (nx < ntiles)
+        load_k_tile<D>(Ks + (nx % STAGES) * TK * P, Kb, a.ss, kbeg + (int64_t)nx * TK, kend, tid);
+      cp_async_commit();
+    }
+    const uint16_t* Kt = Ks + (it % STAGES) * TK * P;
+    const int64_t kt0 = kbeg + (int64_t)it * TK;
+    const bool clean = (kt0 + TK <= kend) && (lw == nullptr) && (!a.causal || kt0 + TK - 1 <= a.S - a.w);
+
+    float c[2][8][4];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int nt = nt_begin + q * kg;
+      if (q < nts) {
+#pragma unroll
+        for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) c[mi][q][e] = 0.f;
+#pragma unroll
+        for (int ks2 = 0; ks2 < KS / 2; ++ks2) {
+          uint32_t b0, b1, b2, b3;
+          const int r = nt * 8 + (lane & 7);
+          const int cc = ks2 * 32 + (lane >> 3) * 8;
+          ldsm_x4(smem_u32(Kt + r * P + cc), b0, b1, b2, b3);
+#pragma unroll
+          for (int mi = 0; mi < 2; ++mi) {
+            if (mi < n_my) {
+              mma16816(c[mi][q], aq[mi][2 * ks2], b0, b1);
+              mma16816(c[mi][q], aq[mi][2 * ks2 + 1], b2, b3);
+            }
+          }
+        }
+      }
+    }
+    // online (max, sum) update per owned row
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi) {
+      if (mi < n_my) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          float v[16];
+          float tmax = -CUDART_INF_F;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float x = -CUDART_INF_F;
+              if (q < nts) {
+                x = c[mi][q][2 * hh + e] * a.sl2;
+                if (!clean) {
+                  const int64_t j = kt0 + (nt_begin + q * kg) * 8 + 2 * t + e;
+                  const bool vis = (j < kend) && (j <= lim[mi][hh]) && (lw == nullptr || live_bit(lw, j));
+                  if (!vis) x = -CUDART_INF_F;
+                } else if (lim[mi][hh] < 0) {
+                  x = -CUDART_INF_F;
+                }
+              }
+              v[q * 2 + e] = x;
+              tmax = fmaxf(tmax, x);
+            }
+          }
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+          tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+          const float mnew = fmaxf(m_run[mi][hh], tmax);
+          if (mnew != -CUDART_INF_F) {
+            float s = l_run[mi][hh] * ex2(m_run[mi][hh] - mnew);
+#pragma unroll
+            for (int z = 0; z < 16; ++z) s += ex2(v[z] - mnew);
+            l_run[mi][hh] = s;
+            m_run[mi][hh] = mnew;
+          }
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  // reduce l over the quad (m is already quad-uniform)
+#pragma unroll
+  for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float l = l_run[mi][hh];
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      l_run[mi][hh] = l;
+    }
+  float2* part = a.part + ((int64_t)bk * a.nsplit + split) * a.Rpad;
+  if (kg == 1) {
+    if (t == 0) {
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) {
+        if (mi < n_my) {
+          const int r = row0 + (mi == 0 ? mt0 : mt1) * 16 + g;
+          part[r] = make_float2(m_run[mi][0], l_run[mi][0]);
+          part[r + 8] = make_float2(m_run[mi][1], l_run[mi][1]);
+        }
+      }
+    }
+  } else {
+    __syncthreads();
+    if (t == 0) {
+      mrg[warp * 16 + g] = make_float2(m_run[0][0], l_run[0][0]);
+      mrg[warp * 16 + g + 8] = make_float2(m_run[0][1], l_run[0][1]);
+    }
+    __syncthreads();
+    if (tid < rows) {
+      const int mt = tid >> 4, rr = tid & 15;
+      float M = -CUDART_INF_F;
+      for (int kgi = 0; kgi < kg; ++kgi) {
+        const float2 v = mrg[(kgi * n_mt + mt) * 16 + rr];
+        if (v.y > 0.f) M = fmaxf(M, v.x);
+      }
+      float L = 0.f;
+      for (int kgi = 0; kgi < kg; ++kgi) {
+        const float2 v = mrg[(kgi * n_mt + mt) * 16 + rr];
+        if (v.y > 0.f) L += v.y * ex2(v.x - M);
+      }
+      part[row0 + tid] = make_float2(M, L);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------------------
+// merge: per row, combine the key ranges' partials into one log2-domain normaliser
+// ----------------------------------------------------------------------------------------
+__global__ void k_scores_merge(const ScoresArgs a) {
+  const int bk = blockIdx.x;
+  for (int r = threadIdx.x; r < a.Rpad; r += blockDim.x) {
+    const float2* p = a.part + (int64_t)bk * a.nsplit * a.Rpad + r;
+    float M = -CUDART_INF_F;
+    for (int s = 0; s < a.nsplit; ++s) {
+      const float2 v = p[(int64_t)s * a.Rpad];
+      if (v.y > 0.f) M = fmaxf(M, v.x);
+    }
+    float L = 0.f;
+    for (int s = 0; s < a.nsplit; ++s) {
+      const float2 v = p[(int64_t)s * a.Rpad];
+      if (v.y > 0.f) L += v.y * ex2(v.x - M);
+    }
+    a.mrow[(int64_t)bk * a.Rpad + r] = (L > 0.f) ? (M + log2f(L)) : CUDART_INF_F;
+  }
+}
+
+// ----------------------------------------------------------------------------------------
+// pass 2: per key, sum over query rows of exp2(s*log2e - c_r), times 1/G
+// ----------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(NTHREADS) k_scores_pass2(const ScoresArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int P = D + 8, KS = D / 16;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int bk = b * a.KVH + kvh;
+  const int64_t kbeg = (int64_t)split * a.chunk;
+  const int64_t kend = min(a.S, kbeg + a.chunk);
+  const int ntiles = (int)((kend - kbeg + TK - 1) / TK);
+  const int Rpad = a.Rpad;
+
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* Ks = Qs + Rpad * P;
+  float* cr = reinterpret_cast<float*>(Ks + STAGES * TK * P);  // [Rpad]
+  long long* lim = reinterpret_cast<long long*>(cr + Rpad);    // [Rpad] (8-byte aligned: Rpad%16==0)
+  float* ksum = reinterpret_cast<float*>(lim + Rpad);          // [2][TK]
+
+  const uint16_t* Kb = a.K + b * a.sb + kvh * a.sh;
+  const uint16_t* Qg = a.q + ((int64_t)(b * a.H + kvh * a.G) * a.w) * D;
+  const uint32_t* lw = a.live ? a.live + (int64_t)bk * a.live_words : nullptr;
+
+  load_q_rows<D>(Qs, Qg, 0, Rpad, a.R, tid);
+  cp_async_commit();
+#pragma unroll
+  for (int s = 0; s < STAGES - 1; ++s) {
+    if (s < ntiles) load_k_tile<D>(Ks + s * TK * P, Kb, a.ss, kbeg + (int64_t)s * TK, kend, tid);
+    cp_async_commit();
+  }
+  for (int r = tid; r < Rpad; r += NTHREADS) {
+    cr[r] = a.mrow[(int64_t)bk * Rpad + r];
+    lim[r] = row_limit(a, r);
+  }
+
+  const int km = warp & 3;  // key m-tile (16 keys) inside the 64-key tile
+  const int ch = warp >> 2; // half of the query-row n-tiles
+  const int NT = Rpad >> 3;
+  const int nt_lo = ch * (NT >> 1), nt_hi = nt_lo + (NT >> 1);
+  float* out = a.out + (int64_t)bk * a.S;
+
+  for (int it = 0; it < ntiles; ++it) {
+    cp_async_wait<STAGES - 2>();
+    __syncthreads();
+    {
+      const int nx = it + STAGES - 1;
+      if (nx < ntiles)
+        load_k_tile<D>(Ks + (nx % STAGES) * TK * P, Kb, a.ss, kbeg + (int64_t)nx * TK, kend, tid);
+      cp_async_commit();
+    }
+    const uint16_t* Kt = Ks + (it % STAGES) * TK * P;
+    const int64_t kt0 = kbeg + (int64_t)it * TK;
+    const bool clean = (kt0 + TK <= kend) && (lw == nullptr) && (!a.causal || kt0 + TK - 1 <= a.S - a.w);
+
+    uint32_t ak[KS][4];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int r = km * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int c = ks * 16 + ((lane >> 4) & 1) * 8;
+      ldsm_x4(smem_u32(Kt + r * P + c), ak[ks][0], ak[ks][1], ak[ks][2], ak[ks][3]);
+    }
+    const int64_t jA = kt0 + km * 16 + g, jB = jA + 8;
+    bool visA = true, visB = true;
+    if (!clean) {
+      visA = jA < kend && (lw == nullptr || live_bit(lw, jA));
+      visB = jB < kend && (lw == nullptr || live_bit(lw, jB));
+    }
+    float acc0 = 0.f, acc1 = 0.f;
+    for (int nt = nt_lo; nt < nt_hi; ++nt) {
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks2 = 0; ks2 < KS / 2; ++ks2) {
+        uint32_t b0, b1, b2, b3;
+        const int r = nt * 8 + (lane & 7);
+        const int cc = ks2 * 32 + (lane >> 3) * 8;
+        ldsm_x4(smem_u32(Qs + r * P + cc), b0, b1, b2, b3);
+        mma16816(c, ak[2 * ks2], b0, b1);
+        mma16816(c, ak[2 * ks2 + 1], b2, b3);
+      }
+      const int r0 = nt * 8 + 2 * t;
+      const float c0 = cr[r0], c1 = cr[r0 + 1];
+      if (clean) {
+        acc0 += ex2(fmaf(c[0], a.sl2, -c0)) + ex2(fmaf(c[1], a.sl2, -c1));
+        acc1 += ex2(fmaf(c[2], a.sl2, -c0)) + ex2(fmaf(c[3], a.sl2, -c1));
+      } else {
+        const long long l0 = lim[r0], l1 = lim[r0 + 1];
+        acc0 += ((visA && jA <= l0) ? ex2(fmaf(c[0], a.sl2, -c0)) : 0.f) +
+                ((visA && jA <= l1) ? ex2(fmaf(c[1], a.sl2, -c1)) : 0.f);
+        acc1 += ((visB && jB <= l0) ? ex2(fmaf(c[2], a.sl2, -c0)) : 0.f) +
+                ((visB && jB <= l1) ? ex2(fmaf(c[3], a.sl2, -c1)) : 0.f);
+      }
+    }
+    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 1);
+    acc0 += __shfl_xor_sync(0xffffffffu, acc0, 2);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 1);
+    acc1 += __shfl_xor_sync(0xffffffffu, acc1, 2);
+    if (t == 0) {
+      ksum[ch * TK + km * 16 + g] = acc0;
+      ksum[ch * TK + km * 16 + g + 8] = acc1;
+    }
+    __syncthreads();
+    if (tid < TK) {
+      const int64_t j = kt0 + tid;
+      if (j < kend) out[j] = (ksum[tid] + ksum[TK + tid]) * a.out_mul;
+    }
+  }
+  cp_async_wait<0>();
+}
+
+// all-heads reduction: mean over KV heads of the per-group scores, written to every kvh
+__global__ void k_scores_allheads(const float* __restrict__ grp, float* __restrict__ out, int B,
+                                  int KVH, int64_t S) {
+  const int64_t n = (int64_t)B * S;
+  const float inv = 1.f / (float)KVH;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < n;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = x / S, j = x % S;
+    float s = 0.f;
+    for (int kv = 0; kv < KVH; ++kv) s += grp[(b * KVH + kv) * S + j];
+    s *= inv;
+    for (int kv = 0; kv < KVH; ++kv) out[(b * KVH + kv) * S + j] = s;
+  }
+}
+
+size_t smem_pass1(int D, int rows) { return (size_t)(rows + STAGES * TK) * (D + 8) * 2 + 8 * 16 * sizeof(float2); }
+size_t smem_pass2(int D, int Rpad) {
+  return (size_t)(Rpad + STAGES * TK) * (D + 8) * 2 + (size_t)Rpad * (4 + 8) + 2 * TK * 4;
+}
+
+template <int D>
+cudaError_t set_smem_attrs() {
+  static bool done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(k_scores_pass1<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem_pass1(D, P1_MAX_ROWS));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_scores_pass2<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_pass2(D, MAX_RPAD));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  return e;
+}
+
+template <int D>
+cudaError_t launch_impl(const ScoresArgs& a, int reduce, float* scores, cudaStream_t st) {
+  cudaError_t e = set_smem_attrs<D>();
+  if (e != cudaSuccess) return e;
+  const int n_rg = (a.Rpad + P1_MAX_ROWS - 1) / P1_MAX_ROWS;
+  const int rows1 = std::min(P1_MAX_ROWS, a.Rpad);
+  dim3 g1(a.nsplit, a.KVH * n_rg, a.B);
+  k_scores_pass1<D><<<g1, NTHREADS, smem_pass1(D, rows1), st>>>(a);
+  k_scores_merge<<<a.B * a.KVH, 256, 0, st>>>(a);
+  dim3 g2(a.nsplit, a.KVH, a.B);
+  k_scores_pass2<D><<<g2, NTHREADS, smem_pass2(D, a.Rpad), st>>>(a);
+  if (reduce == KVC_REDUCE_ALL_HEADS) {
+    const int64_t n = (int64_t)a.B * a.S;
+    const int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 8);
+    k_scores_allheads<<<blocks, 256, 0, st>>>(a.out, scores, a.B, a.KVH, a.S);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+ScoresPlan plan_scores(const kvc_kv_desc& kv, int w, int reduce) {
+  ScoresPlan p{};
+  const int G = kv.H / kv.KVH;
+  p.R = G * w;
+  if (p.R <= 16) p.Rpad = 16;
+  else if (p.R <= 32) p.Rpad = 32;
+  else if (p.R <= 64) p.Rpad = 64;
+  else if (p.R <= 128) p.Rpad = 128;
+  else p.Rpad = (p.R + 15) / 16 * 16;
+  // key ranges: enough CTAs to fill the GPU, at least 4 tiles each
+  const int64_t units = (int64_t)kv.B * kv.KVH;
+  const int64_t target = (int64_t)num_sms() * (p.Rpad >= 128 ? 2 : 4);
+  int64_t nsplit = std::max<int64_t>(1, (target + units - 1) / units);
+  int64_t chunk = (kv.S + nsplit - 1) / nsplit;
+  chunk = std::max<int64_t>(4 * TK, (chunk + TK - 1) / TK * TK);
+  nsplit = (kv.S + chunk - 1) / chunk;
+  p.nsplit = (int)nsplit;
+  p.chunk = chunk;
+  p.part_bytes = (size_t)units * nsplit * p.Rpad * sizeof(float2) + (size_t)units * p.Rpad * sizeof(float);
+  p.part_bytes = (p.part_bytes + 255) / 256 * 256;
+  p.group_bytes = reduce == KVC_REDUCE_ALL_HEADS ? (size_t)units * kv.S * sizeof(float) : 0;
+  return p;
+}
+
+size_t scores_workspace(const kvc_kv_desc& kv, int w, int reduce) {
+  const ScoresPlan p = plan_scores(kv, w, reduce);
+  return p.part_bytes + p.group_bytes;
+}
+
+cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc_kv_desc& kv, int w,
+                                 float scale, int causal, const uint32_t* live, int reduce,
+                                 float* scores, void* ws, cudaStream_t st) {
+  const ScoresPlan p = plan_scores(kv, w, reduce);
+  ScoresArgs a{};
+  a.q = q;
+  a.K = K;
+  a.sb = kv.stride_b;
+  a.sh = kv.stride_h;
+  a.ss = kv.stride_s;
+  a.B = kv.B;
+  a.H = kv.H;
+  a.KVH = kv.KVH;
+  a.w = w;
+  a.G = kv.H / kv.KVH;
+  a.R = p.R;
+  a.Rpad = p.Rpad;
+  a.S = kv.S;
+  a.causal = causal;
+  a.live = live;
+  a.live_words = (kv.S + 31) / 32;
+  a.sl2 = scale * 1.4426950408889634f;
+  a.nsplit = p.nsplit;
+  a.chunk = p.chunk;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  a.part = reinterpret_cast<float2*>(base);
+  a.mrow = reinterpret_cast<float*>(base + (size_t)kv.B * kv.KVH * p.nsplit * p.Rpad * sizeof(float2));
+  a.out = reduce == KVC_REDUCE_ALL_HEADS ? reinterpret_cast<float*>(base + p.part_bytes) : scores;
+  a.out_mul = 1.f / (float)a.G;
+  if (kv.D == 64) return launch_impl<64>(a, reduce, scores, st);
+  return launch_impl<128>(a, reduce, scores, st);
+}
+
+KVC_TU_STATUS(scores)
+
+}  // namespace kvc

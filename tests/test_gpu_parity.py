@@ -1,0 +1,381 @@
+"""GPU parity: every C-ABI call against the CPU oracle on the same seeded inputs.
+
+Sizes span several key tiles (64 keys) and split ranges, with ragged tails; tolerances are
+the ones stated for this method: fp32 scores within 1e-3 relative, compaction bit-exact,
+kept sets identical except oracle near-ties (within 1e-3 of the k-th score).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import attention_score_kv_window_gb300 as kvc
+from synth import (Workload, prefill_inputs, decode_step_inputs, random_scores, random_live_mask,
+                   pack_live_bits, normal_bf16)
+from tests.helpers import (dev_bf16, host_bits, dev_i32, dev_u32, assert_scores_close,
+                           assert_selection_matches)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    kvc.load_library()
+    yield
+    assert kvc.kvc_get_device_status() == kvc.KVC_OK
+
+
+def _wl(B, H, KVH, D, S, w, seed=0, **kw):
+    return Workload("t", B=B, H=H, KVH=KVH, D=D, S=S, w=w, k=1, reduce="gqa", seed=seed, **kw)
+
+
+# ----------------------------------------------------------------------------------------
+# window scores
+# ----------------------------------------------------------------------------------------
+
+SCORE_CASES = [
+    # B, H, KVH, D, S, w, causal, reduce
+    (1, 8, 2, 64, 512, 1, True, "all_heads"),
+    (1, 8, 2, 64, 1, 1, True, "gqa"),
+    (2, 4, 4, 64, 7, 7, True, "gqa"),
+    (1, 8, 1, 128, 63, 63, True, "gqa"),
+    (1, 4, 1, 128, 65, 64, True, "gqa"),
+    (1, 16, 2, 128, 129, 64, True, "gqa"),
+    (2, 8, 2, 128, 1000, 64, True, "gqa"),
+    (1, 32, 8, 128, 1000, 64, True, "gqa"),
+    (3, 8, 8, 64, 777, 5, True, "all_heads"),
+    (2, 32, 8, 128, 2049, 1, False, "all_heads"),
+    (1, 4, 1, 64, 300, 128, True, "gqa"),     # R = 512 rows: two pass-1 row groups
+    (1, 12, 4, 128, 333, 48, True, "gqa"),    # R = 144: odd m-tile count
+    (1, 8, 8, 64, 4000, 40, True, "gqa"),     # R = 40
+    (4, 8, 2, 128, 4096, 1, False, "gqa"),
+]
+
+
+@pytest.mark.parametrize("B,H,KVH,D,S,w,causal,reduce", SCORE_CASES)
+def test_window_scores_parity(B, H, KVH, D, S, w, causal, reduce):
+    inp = prefill_inputs(_wl(B, H, KVH, D, S, w, seed=S + w))
+    scale = 1.0 / np.sqrt(D)
+    got = kvc.kvc_window_scores(dev_bf16(inp["q"]), dev_bf16(inp["K"]), scale, causal=causal, reduce=reduce)
+    ref = O.window_scores(inp["q"], inp["K"], scale, causal=causal, reduce=reduce)
+    assert_scores_close(got.cpu().numpy(), ref)
+    # sum over keys equals the window length (each window row's softmax sums to one)
+    np.testing.assert_allclose(got.double().sum(-1).cpu().numpy(), w, rtol=1e-4)
+
+
+@pytest.mark.parametrize("S,p_live", [(256, 0.7), (4096, 0.5), (100, 0.05), (64, 0.0)])
+def test_window_scores_live_mask(S, p_live):
+    B, H, KVH, D = 2, 8, 2, 128
+    inp = prefill_inputs(_wl(B, H, KVH, D, S, 1, seed=7))
+    live = random_live_mask((B, KVH, S), 3, p_live)
+    got = kvc.kvc_window_scores(dev_bf16(inp["q"]), dev_bf16(inp["K"]), 0.1, causal=False,
+                                live_mask=dev_u32(pack_live_bits(live)), reduce="gqa")
+    ref = O.window_scores(inp["q"], inp["K"], 0.1, causal=False, live=live, reduce="gqa")
+    assert_scores_close(got.cpu().numpy(), ref)
+    assert np.all(got.cpu().numpy()[~live] == 0)
+
+
+def test_window_scores_strided_cache():
+    """K as a view with padded slots (stride_s > D, stride_h > S*D)."""
+    B, H, KVH, D, S = 2, 8, 2, 128, 300
+    inp = prefill_inputs(_wl(B, H, KVH, D, S, 16, seed=9))
+    big = torch.zeros((B, KVH, S + 37, D + 64), dtype=torch.bfloat16, device="cuda")
+    big[:, :, :S, :D] = dev_bf16(inp["K"])
+    Kv = big[:, :, :S, :D]
+    got = kvc.kvc_window_scores(dev_bf16(inp["q"]), Kv, 0.09, causal=True, reduce="gqa")
+    ref = O.window_scores(inp["q"], inp["K"], 0.09, causal=True, reduce="gqa")
+    assert_scores_close(got.cpu().numpy(), ref)
+
+
+def test_window_scores_uniform_and_deterministic():
+    B, H, KVH, D, S = 1, 8, 2, 64, 999
+    q = np.zeros((B, H, 1, D), np.uint16)
+    K = normal_bf16((B, KVH, S, D), 5, 2)
+    a = kvc.kvc_window_scores(dev_bf16(q), dev_bf16(K), 0.125, causal=True, reduce="all_heads")
+    np.testing.assert_allclose(a.cpu().numpy(), 1.0 / S, rtol=1e-5)
+    inp = prefill_inputs(_wl(1, 32, 8, 128, 5000, 64, seed=4))
+    runs = [kvc.kvc_window_scores(dev_bf16(inp["q"]), dev_bf16(inp["K"]), 0.088, reduce="gqa") for _ in range(3)]
+    for r in runs[1:]:
+        assert torch.equal(r, runs[0])
+
+
+# ----------------------------------------------------------------------------------------
+# selection
+# ----------------------------------------------------------------------------------------
+
+TOPK_CASES = [
+    # B, KVH, S, k, protect, ties, largest, live_p
+    (1, 2, 512, 256, 0, 0, True, None),
+    (2, 3, 1000, 100, 64, 0, True, None),
+    (2, 3, 1000, 100, 64, 7, True, None),
+    (1, 8, 32768, 4096, 64, 0, True, None),
+    (1, 2, 50000, 999, 0, 50, True, None),      # uncached (global-memory) path
+    (4, 2, 2049, 1, 0, 0, False, None),
+    (4, 2, 2049, 1, 0, 3, False, None),
+    (2, 2, 4096, 64, 0, 5, True, 0.9),
+    (2, 2, 300, 290, 0, 0, True, 0.5),         # fewer eligible than k -> -1 padding
+    (1, 1, 7, 7, 7, 0, True, None),
+    (1, 1, 33, 40, 0, 0, True, None),          # k > S
+    (3, 1, 129, 65, 1, 2, True, None),
+    (2, 2, 777, 13, 0, 1, False, 0.6),
+]
+
+
+@pytest.mark.parametrize("B,KVH,S,k,protect,ties,largest,live_p", TOPK_CASES)
+def test_topk_parity_exact(B, KVH, S, k, protect, ties, largest, live_p):
+    sc = random_scores((B, KVH, S), 100 + S + k, tie_levels=ties)
+    live = None if live_p is None else random_live_mask((B, KVH, S), 11, live_p)
+    got = kvc.kvc_topk_select(torch.from_numpy(sc).cuda(), k, protect_tail=protect,
+                              live_mask=None if live is None else dev_u32(pack_live_bits(live)), largest=largest)
+    ref = O.topk_select(sc, k, protect_tail=protect, live=live, largest=largest)
+    np.testing.assert_array_equal(got.cpu().numpy(), ref)
+
+
+def test_topk_all_equal_scores():
+    sc = np.full((2, 2, 5000), 0.25, np.float32)
+    got = kvc.kvc_topk_select(torch.from_numpy(sc).cuda(), 123)
+    np.testing.assert_array_equal(got.cpu().numpy(), O.topk_select(sc, 123))
+    got = kvc.kvc_topk_select(torch.from_numpy(sc).cuda(), 9, largest=False)
+    np.testing.assert_array_equal(got.cpu().numpy(), O.topk_select(sc, 9, largest=False))
+
+
+# ----------------------------------------------------------------------------------------
+# compaction
+# ----------------------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_compact_bit_exact(D):
+    B, KVH, S, k = 2, 3, 517, 200
+    K = normal_bf16((B, KVH, S, D), 21, 1)
+    V = normal_bf16((B, KVH, S, D), 21, 2)
+    idx = O.topk_select(random_scores((B, KVH, S), 4), k)
+    idx[0, 1, -5:] = -1
+    big = torch.zeros((B, KVH, S + 3, D), dtype=torch.bfloat16, device="cuda")
+    big[:, :, :S] = dev_bf16(K)
+    bigv = torch.zeros_like(big)
+    bigv[:, :, :S] = dev_bf16(V)
+    Ko, Vo = kvc.kvc_compact_kv(big[:, :, :S], bigv[:, :, :S], dev_i32(idx))
+    Kr, Vr = O.compact_kv(K, V, idx)
+    np.testing.assert_array_equal(host_bits(Ko), Kr)
+    np.testing.assert_array_equal(host_bits(Vo), Vr)
+
+
+def test_compact_out_of_range_index_reports_bounds():
+    K = dev_bf16(normal_bf16((1, 1, 10, 64), 1, 1))
+    idx = dev_i32(np.array([[[0, 10, 3]]]))
+    kvc.kvc_compact_kv(K, None, idx)
+    assert kvc.kvc_get_device_status() == kvc.KVC_ERR_DEVICE_BOUNDS
+    assert kvc.kvc_get_device_status() == kvc.KVC_OK  # cleared on read
+
+
+# ----------------------------------------------------------------------------------------
+# fused prefill compression (TOVA / SnapKV)
+# ----------------------------------------------------------------------------------------
+
+PREFILL_CASES = [
+    # B, H, KVH, D, S, w, k, protect, reduce, hh
+    (1, 8, 2, 64, 512, 1, 256, 0, "all_heads", 0.0),
+    (1, 32, 8, 128, 2000, 64, 512, 64, "gqa", 0.01),
+    (2, 16, 4, 128, 1500, 64, 200, 64, "gqa", 0.01),
+    (1, 8, 2, 64, 100, 16, 128, 16, "gqa", 0.0),   # k > S: keep all
+]
+
+
+@pytest.mark.parametrize("B,H,KVH,D,S,w,k,protect,reduce,hh", PREFILL_CASES)
+def test_compress_prefill_parity(B, H, KVH, D, S, w, k, protect, reduce, hh):
+    wl = _wl(B, H, KVH, D, S, w, seed=31, heavy_hitters=hh)
+    inp = prefill_inputs(wl)
+    scale = 1.0 / np.sqrt(D)
+    sc, idx, Ko, Vo = kvc.kvc_compress_prefill(dev_bf16(inp["q"]), dev_bf16(inp["K"]), dev_bf16(inp["V"]), scale, k,
+                                               protect_tail=protect, reduce=reduce)
+    ref = O.window_scores(inp["q"], inp["K"], scale, causal=True, reduce=reduce)
+    assert_scores_close(sc.cpu().numpy(), ref)
+    gi = idx.cpu().numpy()
+    assert_selection_matches(gi, ref, k, protect_tail=protect)
+    if protect:
+        for b in range(B):
+            for kv in range(KVH):
+                assert set(range(S - protect, S)) <= set(gi[b, kv].tolist())
+    # compaction is exact given the chosen indices
+    Kr, Vr = O.compact_kv(inp["K"], inp["V"], gi)
+    np.testing.assert_array_equal(host_bits(Ko), Kr)
+    np.testing.assert_array_equal(host_bits(Vo), Vr)
+
+
+# ----------------------------------------------------------------------------------------
+# TOVA decode (teacher-forced)
+# ----------------------------------------------------------------------------------------
+
+
+def test_tova_decode_steps_teacher_forced():
+    B, H, KVH, D, S, budget = 2, 8, 2, 128, 700, 256
+    wl = Workload("t", B=B, H=H, KVH=KVH, D=D, S=S, w=1, k=budget, reduce="all_heads", causal=False, seed=41)
+    pre = prefill_inputs(wl)
+    scale = 1.0 / np.sqrt(D)
+    st0 = decode_step_inputs(wl, 0)
+    # first step: append, score, keep the budget
+    sc0, idx0, Kc, Vc = O.tova_first_step(pre["K"], pre["V"], st0["q"], st0["k"], st0["v"], scale, budget)
+    Kf = np.concatenate([pre["K"], st0["k"][:, :, None]], axis=2)
+    Vf = np.concatenate([pre["V"], st0["v"][:, :, None]], axis=2)
+    q0 = dev_bf16(st0["q"])[:, :, None, :]
+    g_sc0 = kvc.kvc_window_scores(q0, dev_bf16(Kf), scale, causal=False, reduce="all_heads")
+    assert_scores_close(g_sc0.cpu().numpy(), sc0)
+    g_idx0 = kvc.kvc_topk_select(g_sc0, budget)
+    assert_selection_matches(g_idx0.cpu().numpy(), sc0, budget)
+    # later steps on a (budget+1)-slot cache, fed the same state on both sides
+    Kd = torch.zeros((B, KVH, budget + 1, D), dtype=torch.bfloat16, device="cuda")
+    Vd = torch.zeros_like(Kd)
+    Kd[:] = dev_bf16(Kc)
+    Vd[:] = dev_bf16(Vc)
+    free = np.full((B, KVH), budget, np.int32)
+    near = 0
+    for t in range(1, 9):
+        st = decode_step_inputs(wl, t)
+        fs = dev_i32(free)
+        g_sc = kvc.kvc_tova_decode_step(dev_bf16(st["q"]), dev_bf16(st["k"]), dev_bf16(st["v"]), Kd, Vd, scale, fs)
+        r_sc, r_ev, Kc, Vc = O.tova_decode_step(Kc, Vc, st["q"], st["k"], st["v"], free, scale)
+        np.testing.assert_array_equal(host_bits(Kd), Kc)
+        assert_scores_close(g_sc.cpu().numpy(), r_sc)
+        g_ev = fs.cpu().numpy()
+        assert np.all(g_ev == g_ev[:, :1])
+        for b in range(B):
+            if g_ev[b, 0] != r_ev[b, 0]:
+                a, c = r_sc[b, 0, g_ev[b, 0]], r_sc[b, 0, r_ev[b, 0]]
+                assert abs(a - c) <= 1e-3 * abs(c)
+                near += 1
+        free = r_ev.astype(np.int32)  # teacher forcing: continue from the oracle's choice
+    assert near <= 2
+
+
+# ----------------------------------------------------------------------------------------
+# Scissorhands
+# ----------------------------------------------------------------------------------------
+
+
+def _sh_host(state):
+    live = np.unpackbits(state.live.cpu().numpy().view(np.uint8), bitorder="little").reshape(
+        state.live.shape[0], state.live.shape[1], -1).astype(bool)
+    return (live, state.low_count.cpu().numpy().view(np.uint16).astype(np.int64),
+            state.insert_step.cpu().numpy().astype(np.int64))
+
+
+def test_scissorhands_update_from_probs_and_evict_exact():
+    """Given the same float32 probabilities, flags, counts and evictions are exact
+    (no insertions here: the live set only shrinks by eviction)."""
+    B, KVH, cap, hist, m = 2, 3, 256, 9, 8
+    st = kvc.ScissorhandsState(B, KVH, cap, history=hist)
+    kvc.kvc_scissorhands_init(st, cap)
+    ref = O.Scissorhands(B, KVH, cap, history=hist)
+    ref.prefill(cap)
+    g = np.random.Generator(np.random.PCG64([77]))
+    for step in range(40):
+        keys = ref.live.sum(-1, keepdims=True)
+        p = np.where(ref.live, g.random((B, KVH, cap)) * 2.0 / keys, 0.0).astype(np.float32)
+        if step % 5 == 0:  # values exactly at the threshold are not low (strict <)
+            p[..., :4] = (np.float32(1) / keys.astype(np.float32))[..., 0:1]
+        kvc.kvc_scissorhands_update_from_probs(st, torch.from_numpy(p).cuda())
+        ref.record(p)
+        live, low, ins = _sh_host(st)
+        np.testing.assert_array_equal(live, ref.live)
+        np.testing.assert_array_equal(np.where(live, low, 0), np.where(ref.live, ref.low, 0))
+        if (step + 1) % m == 0:
+            ev = kvc.kvc_scissorhands_evict(st, m)
+            np.testing.assert_array_equal(ev.cpu().numpy(), ref.evict(m))
+    assert st.t == 40
+    assert kvc.kvc_get_device_status() == kvc.KVC_OK
+
+
+def test_scissorhands_full_update_teacher_forced():
+    B, H, KVH, D, cap, hist, m = 2, 8, 2, 128, 512, 400, 32
+    wl = Workload("t", B=B, H=H, KVH=KVH, D=D, S=cap, w=1, k=cap, reduce="gqa", causal=False, seed=51)
+    pre = prefill_inputs(wl)
+    scale = 1.0 / np.sqrt(D)
+    st = kvc.ScissorhandsState(B, KVH, cap, history=hist)
+    kvc.kvc_scissorhands_init(st, cap - m)
+    Kd, Vd = dev_bf16(pre["K"]), dev_bf16(pre["V"])
+    ref = O.Scissorhands(B, KVH, cap, history=hist)
+    ref.prefill(cap - m)
+    Kr, Vr = pre["K"].copy(), pre["V"].copy()
+    near_total = 0
+    for step in range(2 * m):
+        s = decode_step_inputs(wl, step)
+        probs = kvc.kvc_scissorhands_update(st, dev_bf16(s["q"]), dev_bf16(s["k"]), dev_bf16(s["v"]), Kd, Vd, scale)
+        slot = ref.insert()
+        Kr, Vr = O.write_slots(Kr, Vr, s["k"], s["v"], slot)
+        p_ref = O.scissorhands_probs(s["q"], Kr, scale, ref.live)
+        gp = probs.cpu().numpy()
+        assert_scores_close(gp, p_ref)
+        # flags: identical except where p is within 1e-3/keys of the threshold
+        keys = ref.live.sum(-1, keepdims=True)
+        near = np.abs(p_ref - 1.0 / keys) <= 1e-3 / keys
+        bits_ref = O.low_attention_bits(p_ref, ref.live)
+        bits_gpu = O.low_attention_bits(gp, ref.live)
+        assert np.all((bits_ref == bits_gpu) | near)
+        near_total += int((near & ref.live).sum())
+        ref.record(gp)  # teacher forcing on the GPU's probabilities: counts must then be exact
+        live, low, ins = _sh_host(st)
+        np.testing.assert_array_equal(live, ref.live)
+        np.testing.assert_array_equal(np.where(live, low, 0), np.where(ref.live, ref.low, 0))
+        np.testing.assert_array_equal(np.where(live, ins, 0), np.where(ref.live, ref.insert_step, 0))
+        if (step + 1) % m == 0:
+            ev = kvc.kvc_scissorhands_evict(st, m)
+            np.testing.assert_array_equal(ev.cpu().numpy(), ref.evict(m))
+    np.testing.assert_array_equal(host_bits(Kd), Kr)
+
+
+# ----------------------------------------------------------------------------------------
+# ThinK
+# ----------------------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("D,use_idx", [(128, False), (128, True), (64, True)])
+def test_channel_score_parity(D, use_idx):
+    B, H, KVH, S, w, k = 1, 32, 8, 3000, 64, 700
+    wl = _wl(B, H, KVH, D, S, w, seed=61, channel_scales=True)
+    inp = prefill_inputs(wl)
+    idx = O.topk_select(random_scores((B, KVH, S), 62), k) if use_idx else None
+    cs = kvc.kvc_channel_score(dev_bf16(inp["q"]), dev_bf16(inp["K"]), idx=None if idx is None else dev_i32(idx))
+    ref = O.channel_score(inp["q"], inp["K"], kept=idx)
+    assert_scores_close(cs.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("zero_mode", [False, True])
+def test_channel_prune_parity(zero_mode):
+    B, KVH, S, D, C = 2, 4, 1000, 128, 64
+    cs = random_scores((B, KVH, D), 71, tie_levels=40).astype(np.float32)
+    K = normal_bf16((B, KVH, S, D), 72, 1)
+    ch, Ko = kvc.kvc_channel_prune(torch.from_numpy(cs).cuda(), dev_bf16(K), C, zero_mode=zero_mode)
+    r_ch, r_K = O.channel_prune(cs, K, C, zero_mode=zero_mode)
+    np.testing.assert_array_equal(ch.cpu().numpy(), r_ch)
+    np.testing.assert_array_equal(host_bits(Ko), r_K)
+
+
+def test_channel_prune_in_place_zero():
+    B, KVH, S, D, C = 1, 2, 300, 64, 20
+    cs = random_scores((B, KVH, D), 73).astype(np.float32)
+    K = normal_bf16((B, KVH, S, D), 74, 1)
+    Kd = dev_bf16(K)
+    kvc.kvc_channel_prune(torch.from_numpy(cs).cuda(), Kd, C, zero_mode=True, K_out=Kd)
+    np.testing.assert_array_equal(host_bits(Kd), O.channel_prune(cs, K, C, zero_mode=True)[1])
+
+
+# ----------------------------------------------------------------------------------------
+# host validation through the ABI on a live device
+# ----------------------------------------------------------------------------------------
+
+
+def test_invalid_arguments_raise_and_enqueue_nothing():
+    K = dev_bf16(normal_bf16((1, 2, 64, 64), 1, 1))
+    q = dev_bf16(normal_bf16((1, 6, 1, 64), 1, 2))  # H=6 not a multiple of... 6 % 2 == 0 -> ok
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.kvc_window_scores(q, K, 0.1, reduce="gqa", ws=torch.empty(1, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == kvc.KVC_ERR_WORKSPACE
+    with pytest.raises(kvc.KvcError) as e:
+        kvc.kvc_topk_select(torch.zeros((1, 2, 64), device="cuda"), 4, protect_tail=8)
+    assert e.value.status == kvc.KVC_ERR_INVALID_ARG
+    with pytest.raises(kvc.KvcError):
+        kvc.kvc_compact_kv(K, K, dev_i32(np.zeros((1, 2, 4))), K_out=K[:, :, :4].contiguous(), V_out=K[:, :, :4])
+    assert kvc.kvc_get_device_status() == kvc.KVC_OK

@@ -1,0 +1,97 @@
+"""CPU-side checks of the C ABI: the library builds, loads, exports every declared symbol,
+and rejects bad arguments on the host before anything is launched (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_score_kv_window_gb300 as kvc
+from attention_score_kv_window_gb300 import _binding as bnd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvc.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(bnd.LIB_PATH):
+        from attention_score_kv_window_gb300.build import build_library
+        build_library()
+    return kvc.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvc_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("kvc_window_scores", "kvc_topk_select", "kvc_compact_kv", "kvc_scissorhands_update",
+                 "kvc_scissorhands_evict", "kvc_channel_score", "kvc_channel_prune"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in bnd.exported_symbols(), f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    assert kvc.kvc_status_string(0) == "ok"
+    assert "workspace" in kvc.kvc_status_string(kvc.KVC_ERR_WORKSPACE)
+    assert kvc.kvc_version() >= 10000
+
+
+def _desc(B=1, H=8, KVH=2, D=64, S=128):
+    return bnd.KvDesc(B, H, KVH, D, S, KVH * S * D, S * D, D)
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced (validation fails first)
+
+
+def test_host_validation_without_gpu(lib):
+    d = _desc()
+    # head_dim not supported
+    bad = _desc(D=96)
+    assert lib.kvc_window_scores(FAKE, FAKE, ctypes.byref(bad), 1, 0.1, 1, None, 0, FAKE, FAKE, 1 << 30, None) \
+        == kvc.KVC_ERR_UNSUPPORTED
+    # H not a multiple of KVH
+    bad = _desc(H=7)
+    assert lib.kvc_window_scores(FAKE, FAKE, ctypes.byref(bad), 1, 0.1, 1, None, 0, FAKE, FAKE, 1 << 30, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    # window longer than the sequence
+    assert lib.kvc_window_scores(FAKE, FAKE, ctypes.byref(d), 129, 0.1, 1, None, 0, FAKE, FAKE, 1 << 30, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    # null and misaligned pointers
+    assert lib.kvc_window_scores(None, FAKE, ctypes.byref(d), 1, 0.1, 1, None, 0, FAKE, FAKE, 1 << 30, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_window_scores(FAKE + 2, FAKE, ctypes.byref(d), 1, 0.1, 1, None, 0, FAKE, FAKE, 1 << 30, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    assert "aligned" in kvc.load_library().kvc_last_error_message().decode()
+    # protect_tail larger than k, and with evict order
+    assert lib.kvc_topk_select(FAKE, 1, 2, 128, 4, 8, None, 1, FAKE, None, 0, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_topk_select(FAKE, 1, 2, 128, 4, 2, None, 0, FAKE, None, 0, None) == kvc.KVC_ERR_INVALID_ARG
+    # compaction outputs overlapping the inputs
+    assert lib.kvc_compact_kv(FAKE, None, ctypes.byref(d), FAKE, 4, FAKE + 256, None, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    # channel prune: compact mode needs C % 8 == 0
+    assert lib.kvc_channel_prune(FAKE, FAKE, ctypes.byref(d), 12, 0, FAKE, FAKE * 64, None) \
+        == kvc.KVC_ERR_UNSUPPORTED
+    # Scissorhands: capacity must be a multiple of 32; no free slot -> refused
+    st = bnd.ShState(1, 2, 40, 400, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0)
+    assert lib.kvc_scissorhands_init(ctypes.byref(st), 0, None) == kvc.KVC_ERR_INVALID_ARG
+    st = bnd.ShState(1, 2, 128, 400, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0)
+    assert lib.kvc_scissorhands_update(ctypes.byref(st), FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(d), 0.1, FAKE,
+                                       FAKE, 1 << 30, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_scissorhands_evict(ctypes.byref(st), 8, FAKE, None) == kvc.KVC_ERR_INVALID_ARG  # t == 0
+
+
+def test_workspace_size_rules(lib):
+    d = _desc(S=4096, H=32, KVH=8, D=128)
+    assert lib.kvc_workspace_size(bnd.KVC_OP_TOPK_SELECT, ctypes.byref(d), 1, 1) == 0
+    assert lib.kvc_workspace_size(bnd.KVC_OP_WINDOW_SCORES, ctypes.byref(d), 64, 0) > 0
+    assert lib.kvc_workspace_size(bnd.KVC_OP_WINDOW_SCORES, ctypes.byref(d), 5000, 0) == ctypes.c_size_t(-1).value
