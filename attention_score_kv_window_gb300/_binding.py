@@ -56,6 +56,7 @@ _SH = ctypes.POINTER(ShState)
 _SIGNATURES = {
     "kvc_workspace_size": (_SZ, [_I32, _DESC, _I32, _I32]),
     "kvc_window_scores": (_I32, [_P, _P, _DESC, _I32, _F, _I32, _P, _I32, _P, _P, _SZ, _P]),
+    "kvc_window_scores_noalloc": (_I32, [_P, _P, _DESC, _I32, _F, _I32, _P, _I32, _P, _P]),
     "kvc_topk_select": (_I32, [_P, _I32, _I32, _I64, _I32, _I32, _P, _I32, _P, _P, _SZ, _P]),
     "kvc_compact_kv": (_I32, [_P, _P, _DESC, _P, _I32, _P, _P, _P]),
     "kvc_compress_prefill": (_I32, [_P, _P, _P, _DESC, _I32, _F, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -155,6 +156,25 @@ def kvc_window_scores(q_win, K, scale, causal=True, live_mask=None, reduce="gqa"
     _check(lib.kvc_window_scores(_ptr(q_win.contiguous()), _ptr(K), ctypes.byref(desc), w, float(scale),
                                  int(bool(causal)), _ptr(live_mask), REDUCE[reduce], _ptr(scores),
                                  _ptr(ws), nbytes, _stream(stream)))
+    return scores
+
+
+def kvc_window_scores_noalloc(q_win, K, scale, causal=True, live_mask=None, reduce="gqa", scores=None,
+                              stream=None):
+    """kvc_window_scores with the library's fixed device scratch instead of a workspace.
+
+    For callers that may not allocate device memory during the call (their memory is
+    planned by a host runtime).  ``scores`` should be preallocated by such callers; calls
+    sharing a device must not overlap on the GPU (they share the scratch array)."""
+    lib = load_library()
+    _bf16(q_win, "q_win"), _bf16(K, "K")
+    B, H, w, D = q_win.shape
+    desc = kv_desc(K, H)
+    if scores is None:
+        scores = torch.empty((B, K.shape[1], K.shape[2]), dtype=torch.float32, device=K.device)
+    _check(lib.kvc_window_scores_noalloc(_ptr(q_win.contiguous()), _ptr(K), ctypes.byref(desc), w, float(scale),
+                                         int(bool(causal)), _ptr(live_mask), REDUCE[reduce], _ptr(scores),
+                                         _stream(stream)))
     return scores
 
 

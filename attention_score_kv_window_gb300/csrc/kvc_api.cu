@@ -174,6 +174,31 @@ kvc_status kvc_window_scores(const kvc_bf16* q_win, const kvc_bf16* K, const kvc
                      "kvc_window_scores launch");
 }
 
+kvc_status kvc_window_scores_noalloc(const kvc_bf16* q_win, const kvc_bf16* K,
+                                     const kvc_kv_desc* kv, int32_t w, float scale, int32_t causal,
+                                     const uint32_t* live_mask, kvc_head_reduce reduce,
+                                     float* scores, kvc_stream_t stream) {
+  KVC_TRY(check_desc(kv, "kvc_window_scores_noalloc"));
+  KVC_TRY(check_window(kv, w, "kvc_window_scores_noalloc"));
+  KVC_TRY(check_ptr(q_win, "q_win"));
+  KVC_TRY(check_ptr(K, "K"));
+  KVC_TRY(check_ptr(scores, "scores"));
+  if (live_mask && !aligned16(live_mask)) return fail(KVC_ERR_INVALID_ARG, "live_mask not 16-byte aligned");
+  if (reduce != KVC_REDUCE_GQA_GROUP && reduce != KVC_REDUCE_ALL_HEADS)
+    return fail(KVC_ERR_INVALID_ARG, "unknown head reduction");
+  if (!(scale > 0.f) || scale != scale) return fail(KVC_ERR_INVALID_ARG, "scale must be > 0");
+  const size_t need = scores_workspace(*kv, w, reduce);
+  if (need > (size_t)KVC_NOALLOC_SCRATCH_BYTES)
+    return fail(KVC_ERR_UNSUPPORTED,
+                "kvc_window_scores_noalloc: these shapes need %zu bytes of scratch; the fixed array holds %zu",
+                need, (size_t)KVC_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  KVC_TRY(cuda_status(noalloc_scratch(&scratch), "kvc_window_scores_noalloc scratch address"));
+  return cuda_status(launch_window_scores(q_win, K, *kv, w, scale, causal ? 1 : 0, live_mask, reduce,
+                                          scores, scratch, (cudaStream_t)stream),
+                     "kvc_window_scores_noalloc launch");
+}
+
 kvc_status kvc_topk_select(const float* scores, int32_t B, int32_t KVH, int64_t S, int32_t k,
                            int32_t protect_tail, const uint32_t* live_mask, int32_t largest,
                            int32_t* idx, void* ws, size_t ws_bytes, kvc_stream_t stream) {

@@ -47,6 +47,8 @@ struct ScoresPlan {
 };
 ScoresPlan plan_scores(const kvc_kv_desc& kv, int w, int reduce);
 size_t scores_workspace(const kvc_kv_desc& kv, int w, int reduce);
+// device address of the fixed scratch array behind kvc_window_scores_noalloc (per device)
+cudaError_t noalloc_scratch(void** out);
 cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc_kv_desc& kv, int w,
                                  float scale, int causal, const uint32_t* live, int reduce,
                                  float* scores, void* ws, cudaStream_t st);

@@ -17,6 +17,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "kvc_internal.cuh"
 
@@ -568,6 +569,33 @@ cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc
   a.out_mul = 1.f / (float)a.G;
   if (kv.D == 64) return launch_impl<64>(a, reduce, scores, st);
   return launch_impl<128>(a, reduce, scores, st);
+}
+
+// ----------------------------------------------------------------------------------------
+// Fixed scratch for kvc_window_scores_noalloc: a file-scope device array that every GPU
+// which loads the library holds until the process exits.  Host code cannot use the array's
+// name as a device address (it is a host-side stand-in), so the address is looked up once
+// per device with cudaGetSymbolAddress while that device is current, and passed to the
+// kernels like any caller-provided workspace.
+// ----------------------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[KVC_NOALLOC_SCRATCH_BYTES];
+
+cudaError_t noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
 }
 
 KVC_TU_STATUS(scores)

@@ -103,7 +103,36 @@ kvc_status kvc_window_scores(const kvc_bf16* q_win, const kvc_bf16* K, const kvc
                              kvc_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
- * kvc_topk_select — per (b,kvh) row of `scores`, the k chosen token indices, ascending.
+ * kvc_window_scores_noalloc — kvc_window_scores without a caller workspace and without any
+ * device allocation.  The pages have no counterpart: this is a calling convenience.
+ *
+ * Some callers cannot call cudaMalloc or hand over scratch memory: a plugin run inside
+ * another runtime's step whose memory planner owns every device buffer and passes the
+ * plugin only its inputs and outputs, or a latency-critical loop where an allocation (and
+ * the device synchronisation it can imply) is not allowed.  This entry point serves them:
+ * its scratch is one fixed array of KVC_NOALLOC_SCRATCH_BYTES (4 MiB) compiled into the
+ * library as device memory, which every GPU that loads the library holds until the process
+ * exits.  Inputs and outputs are still the caller's, exactly as for kvc_window_scores.
+ *
+ *  - Shapes whose scratch (kvc_workspace_size(KVC_OP_WINDOW_SCORES, ...) for this reduce
+ *    mode) exceeds the fixed size are rejected with KVC_ERR_UNSUPPORTED; nothing is launched.
+ *  - The first call on a device looks up the array's device address (once, with that device
+ *    current); make that first call before any stream capture on the device.
+ *  - All calls on a device share the one array, and it keeps the last call's contents.
+ *    Every scratch element a call reads is written earlier in the same call, so nothing has
+ *    to be cleared; but two calls that overlap on the GPU (different streams, or different
+ *    host threads without ordering) race on the array and corrupt each other's results.
+ *    Serialise them on one stream.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ * ------------------------------------------------------------------------------------- */
+#define KVC_NOALLOC_SCRATCH_BYTES (4u << 20)
+kvc_status kvc_window_scores_noalloc(const kvc_bf16* q_win, const kvc_bf16* K,
+                                     const kvc_kv_desc* kv, int32_t w, float scale, int32_t causal,
+                                     const uint32_t* live_mask, kvc_head_reduce reduce,
+                                     float* scores, kvc_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * kvc_topk_select —per (b,kvh) row of `scores`, the k chosen token indices, ascending.
  * Keeping (largest=1) takes the k highest-ranked eligible tokens; evicting (largest=0) takes
  * the k lowest-ranked.  Ranking: a outranks b iff score_a > score_b, or equal and a < b.
  * protect_tail = w forces the last w positions in (SnapKV keeps the observation window and
