@@ -37,11 +37,45 @@ void set_error(const char* fmt, ...);  // records the thread's last error messag
 // ----------------------------------------------------------------------------------------
 // window scores (kvc_scores.cu)
 // ----------------------------------------------------------------------------------------
+struct ScoresArgs {
+  const uint16_t* q;
+  const uint16_t* K;
+  int64_t sb, sh, ss;
+  int B, H, KVH, w, G, R, Rpad;
+  int64_t S;
+  int causal;
+  const uint32_t* live;
+  int64_t live_words;
+  float sl2;  // scale * log2(e)
+  int nsplit;    // key ranges per (b, kvh)
+  int64_t units; // 128-key units per (b, kvh); range s covers units [s*units/nsplit, (s+1)*units/nsplit)
+  float2* part;  // [B*KVH][nsplit][Rpad]  (m2, l)
+  float* mrow;   // [B*KVH][Rpad]          M2 + log2(L)  (+inf: no visible key)
+  float* out;    // [B*KVH][S]
+  float out_mul; // 1/G
+};
+
+constexpr int KEY_UNIT = 128;
+// keys [*kbeg, *kend) of key range `split` (balanced: ranges differ by at most one unit)
+__host__ __device__ __forceinline__ void key_range(const ScoresArgs& a, int split, int64_t* kbeg, int64_t* kend) {
+  const int64_t u0 = (int64_t)split * a.units / a.nsplit;
+  const int64_t u1 = (int64_t)(split + 1) * a.units / a.nsplit;
+  *kbeg = u0 * KEY_UNIT;
+  const int64_t e = u1 * KEY_UNIT;
+  *kend = e < a.S ? e : a.S;
+}
+
+// tcgen05 (TMEM/TMA) versions of pass 1 and pass 2 (kvc_scores_tc.cu).  tc_supported() tells
+// whether the shapes fit them; the merge step between them is shared with the other path.
+bool tc_supported(const ScoresArgs& a, int D);
+cudaError_t launch_pass1_tc(const ScoresArgs& a, int D, cudaStream_t st);
+cudaError_t launch_pass2_tc(const ScoresArgs& a, int D, cudaStream_t st);
+
 struct ScoresPlan {
   int R;         // query rows per (b,kvh): G*w
   int Rpad;      // padded to the kernel's row tile
   int nsplit;    // key ranges per (b,kvh)
-  int64_t chunk; // keys per range (multiple of the key tile)
+  int64_t units; // 128-key units per (b,kvh)
   size_t part_bytes;   // (m,l) partials
   size_t group_bytes;  // per-group scores for the all-heads reduction
 };

@@ -31,24 +31,6 @@ constexpr int STAGES = 3;
 constexpr int P1_MAX_ROWS = 256;  // query rows per pass-1 CTA (row groups beyond)
 constexpr int MAX_RPAD = 512;
 
-struct ScoresArgs {
-  const uint16_t* q;
-  const uint16_t* K;
-  int64_t sb, sh, ss;
-  int B, H, KVH, w, G, R, Rpad;
-  int64_t S;
-  int causal;
-  const uint32_t* live;
-  int64_t live_words;
-  float sl2;  // scale * log2(e)
-  int nsplit;
-  int64_t chunk;
-  float2* part;  // [B*KVH][nsplit][Rpad]  (m2, l)
-  float* mrow;   // [B*KVH][Rpad]          M2 + log2(L)  (+inf: no visible key)
-  float* out;    // [B*KVH][S]
-  float out_mul; // 1/G
-};
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -132,8 +114,8 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass1(const ScoresArgs a) {
   const int row0 = rg * P1_MAX_ROWS;
   const int rows = min(P1_MAX_ROWS, a.Rpad - row0);
   const int n_mt = rows >> 4;
-  const int64_t kbeg = (int64_t)split * a.chunk;
-  const int64_t kend = min(a.S, kbeg + a.chunk);
+  int64_t kbeg, kend;
+  key_range(a, split, &kbeg, &kend);
   const int ntiles = (int)((kend - kbeg + TK - 1) / TK);
 
   uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);
@@ -352,8 +334,8 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass2(const ScoresArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int bk = b * a.KVH + kvh;
-  const int64_t kbeg = (int64_t)split * a.chunk;
-  const int64_t kend = min(a.S, kbeg + a.chunk);
+  int64_t kbeg, kend;
+  key_range(a, split, &kbeg, &kend);
   const int ntiles = (int)((kend - kbeg + TK - 1) / TK);
   const int Rpad = a.Rpad;
 
@@ -492,13 +474,21 @@ template <int D>
 cudaError_t launch_impl(const ScoresArgs& a, int reduce, float* scores, cudaStream_t st) {
   cudaError_t e = set_smem_attrs<D>();
   if (e != cudaSuccess) return e;
-  const int n_rg = (a.Rpad + P1_MAX_ROWS - 1) / P1_MAX_ROWS;
-  const int rows1 = std::min(P1_MAX_ROWS, a.Rpad);
-  dim3 g1(a.nsplit, a.KVH * n_rg, a.B);
-  k_scores_pass1<D><<<g1, NTHREADS, smem_pass1(D, rows1), st>>>(a);
-  k_scores_merge<<<a.B * a.KVH, 256, 0, st>>>(a);
-  dim3 g2(a.nsplit, a.KVH, a.B);
-  k_scores_pass2<D><<<g2, NTHREADS, smem_pass2(D, a.Rpad), st>>>(a);
+  if (tc_supported(a, D)) {
+    e = launch_pass1_tc(a, D, st);
+    if (e != cudaSuccess) return e;
+    k_scores_merge<<<a.B * a.KVH, 256, 0, st>>>(a);
+    e = launch_pass2_tc(a, D, st);
+    if (e != cudaSuccess) return e;
+  } else {
+    const int n_rg = (a.Rpad + P1_MAX_ROWS - 1) / P1_MAX_ROWS;
+    const int rows1 = std::min(P1_MAX_ROWS, a.Rpad);
+    dim3 g1(a.nsplit, a.KVH * n_rg, a.B);
+    k_scores_pass1<D><<<g1, NTHREADS, smem_pass1(D, rows1), st>>>(a);
+    k_scores_merge<<<a.B * a.KVH, 256, 0, st>>>(a);
+    dim3 g2(a.nsplit, a.KVH, a.B);
+    k_scores_pass2<D><<<g2, NTHREADS, smem_pass2(D, a.Rpad), st>>>(a);
+  }
   if (reduce == KVC_REDUCE_ALL_HEADS) {
     const int64_t n = (int64_t)a.B * a.S;
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 8);
@@ -517,16 +507,17 @@ ScoresPlan plan_scores(const kvc_kv_desc& kv, int w, int reduce) {
   else if (p.R <= 32) p.Rpad = 32;
   else if (p.R <= 64) p.Rpad = 64;
   else if (p.R <= 128) p.Rpad = 128;
+  else if (p.R <= 256) p.Rpad = (p.R + 63) / 64 * 64;
   else p.Rpad = (p.R + 15) / 16 * 16;
-  // key ranges: enough CTAs to fill the GPU, at least 4 tiles each
+  // key ranges of whole 128-key units, balanced: about one wave of CTAs for the tensor-core
+  // shapes (one CTA per SM), four CTAs per SM for the small-row (decode) shapes
   const int64_t units = (int64_t)kv.B * kv.KVH;
-  const int64_t target = (int64_t)num_sms() * (p.Rpad >= 128 ? 2 : 4);
-  int64_t nsplit = std::max<int64_t>(1, (target + units - 1) / units);
-  int64_t chunk = (kv.S + nsplit - 1) / nsplit;
-  chunk = std::max<int64_t>(4 * TK, (chunk + TK - 1) / TK * TK);
-  nsplit = (kv.S + chunk - 1) / chunk;
+  const int64_t target = (int64_t)num_sms() * (p.Rpad >= 64 ? 1 : 4);
+  p.units = (kv.S + KEY_UNIT - 1) / KEY_UNIT;
+  int64_t nsplit = std::max<int64_t>(1, target / units);
+  nsplit = std::min<int64_t>(nsplit, std::max<int64_t>(1, p.units / 2));  // >= 2 units per range
+  nsplit = std::min<int64_t>(nsplit, 65535);
   p.nsplit = (int)nsplit;
-  p.chunk = chunk;
   p.part_bytes = (size_t)units * nsplit * p.Rpad * sizeof(float2) + (size_t)units * p.Rpad * sizeof(float);
   p.part_bytes = (p.part_bytes + 255) / 256 * 256;
   p.group_bytes = reduce == KVC_REDUCE_ALL_HEADS ? (size_t)units * kv.S * sizeof(float) : 0;
@@ -561,7 +552,7 @@ cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc
   a.live_words = (kv.S + 31) / 32;
   a.sl2 = scale * 1.4426950408889634f;
   a.nsplit = p.nsplit;
-  a.chunk = p.chunk;
+  a.units = p.units;
   uint8_t* base = static_cast<uint8_t*>(ws);
   a.part = reinterpret_cast<float2*>(base);
   a.mrow = reinterpret_cast<float*>(base + (size_t)kv.B * kv.KVH * p.nsplit * p.Rpad * sizeof(float2));

@@ -51,6 +51,8 @@ SCORE_CASES = [
     (1, 12, 4, 128, 333, 48, True, "gqa"),    # R = 144: odd m-tile count
     (1, 8, 8, 64, 4000, 40, True, "gqa"),     # R = 40
     (4, 8, 2, 128, 4096, 1, False, "gqa"),
+    (1, 8, 2, 64, 3000, 32, True, "gqa"),     # R = 128: tensor-core path, one query half
+    (2, 32, 8, 128, 5000, 64, False, "all_heads"),
 ]
 
 
