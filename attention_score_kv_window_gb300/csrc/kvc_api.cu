@@ -86,6 +86,7 @@ kvc_status check_sh(const kvc_sh_state* st) {
   if (st->B < 1 || st->KVH < 1 || st->cap < 32 || st->cap % 32)
     return fail(KVC_ERR_INVALID_ARG, "scissorhands: B, KVH >= 1 and cap a positive multiple of 32");
   if (st->history < 1 || st->history > 4096) return fail(KVC_ERR_INVALID_ARG, "scissorhands: history in [1, 4096]");
+  if (st->cap > 40960) return fail(KVC_ERR_UNSUPPORTED, "scissorhands: cap must be <= 40960");
   if (!st->hist || !st->low_count || !st->insert_step || !st->live || !st->slot)
     return fail(KVC_ERR_INVALID_ARG, "scissorhands: a state buffer is NULL");
   if (st->t < 0 || st->t > INT32_MAX) return fail(KVC_ERR_INVALID_ARG, "scissorhands: step counter out of range");
@@ -205,7 +206,7 @@ kvc_status kvc_topk_select(const float* scores, int32_t B, int32_t KVH, int64_t 
   (void)ws;
   (void)ws_bytes;
   if (B < 1 || KVH < 1 || S < 1 || k < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select: B, KVH, S, k must be >= 1");
-  if (S > (int64_t)INT32_MAX - 64) return fail(KVC_ERR_UNSUPPORTED, "kvc_topk_select: S too large");
+  if (S > topk_max_len()) return fail(KVC_ERR_UNSUPPORTED, "kvc_topk_select: S > %lld", (long long)topk_max_len());
   if ((int64_t)B * KVH > 2147483647LL) return fail(KVC_ERR_UNSUPPORTED, "kvc_topk_select: too many rows");
   if (protect_tail < 0 || protect_tail > k || (int64_t)protect_tail > S)
     return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select: need 0 <= protect_tail <= min(k, S)");

@@ -90,6 +90,7 @@ cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc
 // ----------------------------------------------------------------------------------------
 // selection (kvc_select.cu)
 // ----------------------------------------------------------------------------------------
+int64_t topk_max_len();  // longest row kvc_topk_select accepts
 cudaError_t launch_topk(const float* scores, int B, int KVH, int64_t S, int k, int protect_tail,
                         const uint32_t* live, int largest, int32_t* idx, cudaStream_t st);
 cudaError_t launch_sh_evict(const kvc_sh_state& s, int m, int32_t* evicted, cudaStream_t st);

@@ -2,15 +2,19 @@
 // ascending indices.  Ranking: higher key first; on equal keys the lower index first when
 // keeping, the higher index first when evicting (the lowest-ranked token goes first).
 //
-// One 1024-thread CTA per row runs an MSB-first radix select over 32-bit order-preserving
-// keys (4 digits of 8 bits, shared-memory histograms), which yields the k-th key T and how
-// many items equal to T are taken.  A final pass in index order, with two block-wide scans
-// (items equal to T, then chosen items), writes the chosen indices ascending.  Rows of up
-// to 40960 items keep their keys in shared memory between passes; longer rows re-read
-// global memory (they stay in L2).
+// A row is split over a thread-block cluster of up to 8 CTAs (1024 threads each); each CTA
+// loads its slice of keys into shared memory once.  An MSB-first radix select (digits of
+// 11, 11 and 10 bits) builds shared-memory histograms with warp-aggregated atomics, sums
+// them over the cluster through distributed shared memory, and finds the digit holding the
+// k-th item with one block scan; this yields the k-th key T and how many keys equal to T
+// are taken.  The output pass counts, per warp and per CTA, the keys certainly taken (> T)
+// and those equal to T, exchanges the CTA counts over the cluster, and writes every taken
+// index at (taken-for-sure before it) + (taken-equal before it): ascending order, no sort.
+// Cluster barriers are hardware barriers; there are no spin-waits.
 //
 // Users: token top-k for SnapKV/TOVA ("Add TOVA press"; cold-compress PR 11, SnapKV keeps
 // the observation window) and Scissorhands eviction by low-attention fraction.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,9 +25,11 @@
 namespace kvc {
 namespace {
 
+namespace cg = cooperative_groups;
+
 constexpr int SEL_THREADS = 1024;
-constexpr int SEL_ITEMS = 4;                 // consecutive items per thread in the output pass
-constexpr int64_t SEL_CACHE_MAX = 40960;     // rows up to this length cache keys in smem
+constexpr int64_t SLICE_MAX = 40960;  // keys one CTA keeps in shared memory
+constexpr int MAX_CLUSTER = 8;
 
 __device__ __forceinline__ uint32_t float_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -71,10 +77,11 @@ struct FractionKeys {
 };
 
 struct SelShared {
-  uint32_t hist[256];
+  uint32_t hist[2][2048];
   uint32_t warp_a[32];
   uint32_t warp_b[32];
-  uint32_t prefix, remaining, eq_total, n_forced, n_elig, digit_above;
+  uint32_t cta_cnt[4];  // read by the other CTAs of the cluster: forced, eligible, sure, equal
+  uint32_t prefix, remaining, eq_total;
 };
 
 // inclusive block scan of one value per thread (1024 threads); returns inclusive, total in *tot
@@ -104,146 +111,213 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* warp_buf, u
   return base + x;
 }
 
-__device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* warp_buf) {
-  uint32_t tot;
-  block_scan(v, warp_buf, &tot);
-  return tot;
-}
+template <class Fn>
+__device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_t* kc, SelShared& sh,
+                           bool evict_order) {
+  cg::cluster_group cl = cg::this_cluster();
+  const int cs = (int)cl.num_blocks();
+  const int cr = (int)cl.block_rank();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lower = (1u << lane) - 1u;
+  // this CTA's slice [c0, c1) of the row, and this warp's contiguous segment [w0, w1) of it
+  const int64_t per_cta = ((n + (int64_t)cs * 32 - 1) / ((int64_t)cs * 32)) * 32;
+  const int64_t c0 = (int64_t)cr * per_cta;
+  const int64_t c1 = c0 + per_cta < n ? c0 + per_cta : n;
+  const int64_t len = c1 > c0 ? c1 - c0 : 0;
+  const int64_t per_w = ((len + 1023) / 1024) * 32;
+  const int64_t w0 = c0 + (int64_t)warp * per_w;
+  const int64_t w1 = w0 + per_w < c1 ? w0 + per_w : c1;
 
-template <class Fn, bool CACHE>
-__device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_t* kc,
-                           SelShared& sh, bool evict_order) {
-  const int tid = threadIdx.x;
-  // count eligible and forced items; optionally cache keys
-  uint32_t ce = 0, cf = 0;
-  for (int64_t j = tid; j < n; j += SEL_THREADS) {
-    if (fn.forced(j)) ++cf;
-    else if (fn.eligible(j)) ++ce;
-    if (CACHE) kc[j] = fn.key(j);
+  // keys of the slice into shared memory (independent loads, many in flight)
+#pragma unroll 8
+  for (int64_t j = c0 + tid; j < c1; j += SEL_THREADS) kc[j - c0] = fn.key(j);
+
+  // 1. forced / eligible counts over the cluster
+  uint32_t cf = 0, ce = 0;
+  for (int64_t base = w0; base < w1; base += 32) {
+    const int64_t j = base + lane;
+    const bool in = j < w1;
+    const bool f = in && fn.forced(j);
+    const bool e = in && !f && fn.eligible(j);
+    cf += __popc(__ballot_sync(0xffffffffu, f));
+    ce += __popc(__ballot_sync(0xffffffffu, e));
   }
-  const uint32_t n_forced = block_sum(cf, sh.warp_a);
-  const uint32_t n_elig = block_sum(ce, sh.warp_a);
-  const int64_t need = std::max<int64_t>(0, (int64_t)k - (int64_t)n_forced);
-  const bool take_all = (int64_t)n_elig <= need;
-
-  uint32_t T = 0, take_eq = 0, eq_total = 0;
-  if (!take_all && need > 0) {
-    if (tid == 0) { sh.prefix = 0; sh.remaining = (uint32_t)need; }
-    uint32_t mask = 0;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      if (tid < 256) sh.hist[tid] = 0;
-      __syncthreads();
-      const uint32_t prefix = sh.prefix;
-      for (int64_t j = tid; j < n; j += SEL_THREADS) {
-        if (!fn.eligible(j)) continue;
-        const uint32_t key = CACHE ? kc[j] : fn.key(j);
-        if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
-      }
-      __syncthreads();
-      if (tid < 32) {
-        const int lane = tid;
-        uint32_t s = 0;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) s += sh.hist[255 - 8 * lane - q];
-        uint32_t incl = s;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const uint32_t excl = incl - s;
-        const uint32_t rem = sh.remaining;
-        if (excl < rem && rem <= incl) {
-          uint32_t run = excl;
-          for (int q = 0; q < 8; ++q) {
-            const int d = 255 - 8 * lane - q;
-            const uint32_t h = sh.hist[d];
-            if (run + h >= rem) {
-              sh.prefix = prefix | ((uint32_t)d << shift);
-              sh.remaining = rem - run;
-              sh.eq_total = h;
-              break;
-            }
-            run += h;
-          }
-        }
-      }
-      __syncthreads();
-      mask |= 255u << shift;
+  if (lane == 0) {
+    sh.warp_a[warp] = cf;
+    sh.warp_b[warp] = ce;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t a = 0, b = 0;
+    for (int q = 0; q < 32; ++q) {
+      a += sh.warp_a[q];
+      b += sh.warp_b[q];
     }
-    T = sh.prefix;
-    take_eq = sh.remaining;
+    sh.cta_cnt[0] = a;
+    sh.cta_cnt[1] = b;
+  }
+  cl.sync();
+  uint32_t n_forced = 0, n_elig = 0;
+  for (int r = 0; r < cs; ++r) {
+    const SelShared* rs = cl.map_shared_rank(&sh, r);
+    n_forced += rs->cta_cnt[0];
+    n_elig += rs->cta_cnt[1];
+  }
+  const int64_t need = (int64_t)k - (int64_t)n_forced > 0 ? (int64_t)k - (int64_t)n_forced : 0;
+  const bool take_all = (int64_t)n_elig <= need;
+  const bool split_ties = !take_all && need > 0;
+
+  // 2. radix select of the need-th largest eligible key over the cluster
+  uint32_t T = 0, take_eq = 0, eq_total = 0;
+  if (split_ties) {
+    uint32_t prefix = 0, rem = (uint32_t)need, hi_mask = 0;
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const uint32_t nbins = pass == 2 ? 1024u : 2048u;
+      uint32_t* hist = sh.hist[pass & 1];
+      for (uint32_t i = tid; i < nbins; i += SEL_THREADS) hist[i] = 0u;
+      __syncthreads();
+      for (int64_t j0 = 0; j0 < len; j0 += SEL_THREADS) {
+        const int64_t jl = j0 + tid;
+        uint32_t d = 0xffffffffu;
+        if (jl < len && fn.eligible(c0 + jl)) {
+          const uint32_t key = kc[jl];
+          if ((key & hi_mask) == prefix) d = (key >> shift) & (nbins - 1u);
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        if (d != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+      }
+      cl.sync();
+      // this thread's bins, in descending digit order, summed over the cluster
+      const uint32_t bpt = nbins >> 10;
+      uint32_t hb[2] = {0u, 0u};
+      for (int r = 0; r < cs; ++r) {
+        const uint32_t* rh = cl.map_shared_rank(hist, r);
+        for (uint32_t q = 0; q < bpt; ++q) hb[q] += rh[nbins - 1u - (tid * bpt + q)];
+      }
+      const uint32_t hs = hb[0] + hb[1];
+      uint32_t tot;
+      const uint32_t incl = block_scan(hs, sh.warp_a, &tot);
+      const uint32_t excl = incl - hs;
+      if (excl < rem && rem <= incl) {
+        uint32_t run = excl;
+        for (uint32_t q = 0; q < bpt; ++q) {
+          const uint32_t d = nbins - 1u - (tid * bpt + q);
+          if (run + hb[q] >= rem) {
+            sh.prefix = prefix | (d << shift);
+            sh.remaining = rem - run;
+            sh.eq_total = hb[q];
+            break;
+          }
+          run += hb[q];
+        }
+      }
+      __syncthreads();
+      prefix = sh.prefix;
+      rem = sh.remaining;
+      hi_mask |= (nbins - 1u) << shift;
+    }
+    T = prefix;
+    take_eq = rem;
     eq_total = sh.eq_total;
   }
-  // items equal to T are taken in index order when keeping (the first take_eq), and from
-  // the end when evicting (the last take_eq)
+  // keys equal to T: the first take_eq in index order when keeping, the last when evicting
   const uint32_t skip_eq = evict_order ? (eq_total - take_eq) : 0u;
 
-  uint32_t eq_base = 0, out_base = 0;
-  for (int64_t c0 = 0; c0 < n; c0 += (int64_t)SEL_THREADS * SEL_ITEMS) {
-    const int64_t j0 = c0 + (int64_t)tid * SEL_ITEMS;
-    uint8_t f[SEL_ITEMS];  // 1 = taken for sure, 2 = equal to T
-    uint32_t neq = 0;
-#pragma unroll
-    for (int q = 0; q < SEL_ITEMS; ++q) {
-      const int64_t j = j0 + q;
-      f[q] = 0;
-      if (j < n) {
-        if (fn.forced(j)) f[q] = 1;
-        else if (fn.eligible(j)) {
-          if (take_all) f[q] = 1;
-          else if (need > 0) {
-            const uint32_t key = CACHE ? kc[j] : fn.key(j);
-            if (key > T) f[q] = 1;
-            else if (key == T) { f[q] = 2; ++neq; }
-          }
+  // 3. output, ascending
+  uint32_t cd = 0, cq = 0;
+  for (int64_t base = w0; base < w1; base += 32) {
+    const int64_t j = base + lane;
+    bool def = false, eq = false;
+    if (j < w1) {
+      if (fn.forced(j)) def = true;
+      else if (fn.eligible(j)) {
+        if (take_all) def = true;
+        else if (split_ties) {
+          const uint32_t key = kc[j - c0];
+          def = key > T;
+          eq = key == T;
         }
       }
     }
-    uint32_t eq_tot;
-    const uint32_t eq_incl = block_scan(neq, sh.warp_a, &eq_tot);
-    uint32_t er = eq_base + eq_incl - neq;  // equal-rank of this thread's first equal item
-    uint32_t nsel = 0;
-#pragma unroll
-    for (int q = 0; q < SEL_ITEMS; ++q) {
-      if (f[q] == 2) {
-        f[q] = (er >= skip_eq && er < skip_eq + take_eq) ? 1 : 0;
-        ++er;
-      }
-      nsel += f[q];
-    }
-    uint32_t sel_tot;
-    const uint32_t sel_incl = block_scan(nsel, sh.warp_b, &sel_tot);
-    uint32_t pos = out_base + sel_incl - nsel;
-#pragma unroll
-    for (int q = 0; q < SEL_ITEMS; ++q) {
-      if (f[q] == 1) {
-        if (pos < (uint32_t)k) out[pos] = (int32_t)(j0 + q);
-        ++pos;
-      }
-    }
-    eq_base += eq_tot;
-    out_base += sel_tot;
+    cd += __popc(__ballot_sync(0xffffffffu, def));
+    cq += __popc(__ballot_sync(0xffffffffu, eq));
   }
-  for (int64_t p = (int64_t)out_base + tid; p < k; p += SEL_THREADS) out[p] = -1;
+  if (lane == 0) {
+    sh.warp_a[warp] = cd;
+    sh.warp_b[warp] = cq;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t a = 0, b = 0;
+    for (int q = 0; q < 32; ++q) {
+      a += sh.warp_a[q];
+      b += sh.warp_b[q];
+    }
+    sh.cta_cnt[2] = a;
+    sh.cta_cnt[3] = b;
+  }
+  cl.sync();
+  uint32_t d_run = 0, e_run = 0, d_total = 0;
+  for (int r = 0; r < cs; ++r) {
+    const SelShared* rs = cl.map_shared_rank(&sh, r);
+    const uint32_t a = rs->cta_cnt[2], b = rs->cta_cnt[3];
+    if (r < cr) {
+      d_run += a;
+      e_run += b;
+    }
+    d_total += a;
+  }
+  for (int q = 0; q < warp; ++q) {
+    d_run += sh.warp_a[q];
+    e_run += sh.warp_b[q];
+  }
+  for (int64_t base = w0; base < w1; base += 32) {
+    const int64_t j = base + lane;
+    bool def = false, eq = false;
+    if (j < w1) {
+      if (fn.forced(j)) def = true;
+      else if (fn.eligible(j)) {
+        if (take_all) def = true;
+        else if (split_ties) {
+          const uint32_t key = kc[j - c0];
+          def = key > T;
+          eq = key == T;
+        }
+      }
+    }
+    const uint32_t bd = __ballot_sync(0xffffffffu, def);
+    const uint32_t be = __ballot_sync(0xffffffffu, eq);
+    const uint32_t eb = e_run + __popc(be & lower);  // keys equal to T before j
+    const bool take = def || (eq && eb >= skip_eq && eb < skip_eq + take_eq);
+    if (take) {
+      const uint32_t teq = eb <= skip_eq ? 0u : (eb - skip_eq < take_eq ? eb - skip_eq : take_eq);
+      const uint32_t pos = d_run + __popc(bd & lower) + teq;
+      if (pos < (uint32_t)k) out[pos] = (int32_t)j;
+    }
+    d_run += __popc(bd);
+    e_run += __popc(be);
+  }
+  if (cr == 0) {
+    const uint32_t total = d_total + (split_ties ? take_eq : 0u);
+    for (int64_t p = (int64_t)total + tid; p < k; p += SEL_THREADS) out[p] = -1;
+  }
+  cl.sync();  // no CTA leaves while the others may still read its shared memory
 }
 
-template <bool CACHE>
-__global__ void __launch_bounds__(SEL_THREADS) k_topk(const float* __restrict__ scores, int KVH,
-                                                      int64_t S, int k, int protect,
-                                                      const uint32_t* __restrict__ live,
+__global__ void __launch_bounds__(SEL_THREADS) k_topk(const float* __restrict__ scores, int64_t S, int k,
+                                                      int protect, const uint32_t* __restrict__ live,
                                                       int largest, int32_t* __restrict__ idx) {
   extern __shared__ __align__(16) uint32_t kc[];
   __shared__ SelShared sh;
-  const int64_t row = blockIdx.x;
+  const int64_t row = blockIdx.x / cg::this_cluster().num_blocks();
   ScoreKeys fn;
   fn.row = scores + row * S;
   fn.lw = live ? live + row * ((S + 31) / 32) : nullptr;
   fn.S = S;
   fn.protect = protect;
   fn.largest = largest;
-  select_row<ScoreKeys, CACHE>(fn, S, k, idx + row * k, kc, sh, !largest);
+  select_row<ScoreKeys>(fn, S, k, idx + row * k, kc, sh, !largest);
 }
 
 __global__ void __launch_bounds__(SEL_THREADS) k_sh_evict(kvc_sh_state s, int m, int32_t* evicted) {
@@ -258,9 +332,8 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sh_evict(kvc_sh_state s, int m,
   fn.t_last = s.t - 1;
   fn.history = s.history;
   int32_t* out = evicted + row * m;
-  select_row<FractionKeys, true>(fn, s.cap, m, out, kc, sh, false);
-  __syncthreads();
-  // clear the live bits of the evicted slots
+  select_row<FractionKeys>(fn, s.cap, m, out, kc, sh, false);
+  // clear the live bits of the evicted slots (select_row ended with a barrier)
   uint32_t* lw = s.live + row * nw;
   for (int p = threadIdx.x; p < m; p += SEL_THREADS) {
     const int32_t j = out[p];
@@ -268,31 +341,47 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sh_evict(kvc_sh_state s, int m,
   }
 }
 
+int topk_cluster_size(int64_t S) {
+  if (S <= 8192) return 1;
+  return (int)std::min<int64_t>(MAX_CLUSTER, (S + 4095) / 4096);
+}
+
 }  // namespace
+
+int64_t topk_max_len() { return SLICE_MAX * MAX_CLUSTER; }
 
 cudaError_t launch_topk(const float* scores, int B, int KVH, int64_t S, int k, int protect_tail,
                         const uint32_t* live, int largest, int32_t* idx, cudaStream_t st) {
-  const int rows = B * KVH;
-  if (S <= SEL_CACHE_MAX) {
-    const size_t smem = (size_t)S * 4;
-    static bool attr_done[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(k_topk<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)(SEL_CACHE_MAX * 4));
-      if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 64) attr_done[dev] = true;
-    }
-    k_topk<true><<<rows, SEL_THREADS, smem, st>>>(scores, KVH, S, k, protect_tail, live, largest, idx);
-  } else {
-    k_topk<false><<<rows, SEL_THREADS, 0, st>>>(scores, KVH, S, k, protect_tail, live, largest, idx);
+  const int cs = topk_cluster_size(S);
+  const int64_t per_cta = ((S + (int64_t)cs * 32 - 1) / ((int64_t)cs * 32)) * 32;
+  if (per_cta > SLICE_MAX) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)per_cta * 4;
+  static bool attr_done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(SLICE_MAX * 4));
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((int64_t)B * KVH * cs), 1, 1);
+  cfg.blockDim = dim3(SEL_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_topk, scores, S, k, protect_tail, live, largest, idx);
 }
 
 cudaError_t launch_sh_evict(const kvc_sh_state& s, int m, int32_t* evicted, cudaStream_t st) {
   const size_t smem = (size_t)s.cap * 4;
+  if ((int64_t)s.cap > SLICE_MAX) return cudaErrorInvalidValue;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k_sh_evict, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

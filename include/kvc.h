@@ -139,7 +139,8 @@ kvc_status kvc_window_scores_noalloc(const kvc_bf16* q_win, const kvc_bf16* K,
  * compresses only the prefix, cold-compress PR 11); it requires largest=1 and w <= k.
  * Eligible = live (live_mask as above, NULL = all).  If fewer than k are eligible (e.g.
  * k >= S: SnapKV compresses only on overflow), all are returned and the rest of the row is -1.
- *   scores [B,KVH,S] float32 (finite); idx [B,KVH,k] int32 out.  ws: none needed (pass NULL, 0).
+ *   scores [B,KVH,S] float32 (finite), S <= 327680; idx [B,KVH,k] int32 out.  ws: none needed
+ *   (pass NULL, 0).
  * ------------------------------------------------------------------------------------- */
 kvc_status kvc_topk_select(const float* scores, int32_t B, int32_t KVH, int64_t S, int32_t k,
                            int32_t protect_tail, const uint32_t* live_mask, int32_t largest,
@@ -204,7 +205,7 @@ kvc_status kvc_tova_decode_step(const kvc_bf16* q_new, const kvc_bf16* k_new,
  *   slot        [B][KVH] int32 — slot filled by the last insertion
  *   t           host: index of the next recorded step (advanced by each update)
  *   n_free      host: free slots per (b,kvh) (identical for all heads)
- * cap must be a multiple of 32, history in [1, 4096].
+ * cap must be a multiple of 32 and <= 40960, history in [1, 4096].
  * ------------------------------------------------------------------------------------- */
 typedef struct {
   int32_t B, KVH, cap, history;
