@@ -49,11 +49,41 @@ struct ScoresArgs {
   float sl2;  // scale * log2(e)
   int nsplit;    // key ranges per (b, kvh)
   int64_t units; // 128-key units per (b, kvh); range s covers units [s*units/nsplit, (s+1)*units/nsplit)
-  float2* part;  // [B*KVH][nsplit][Rpad]  (m2, l)
+  float2* part;  // [B*KVH][Rpad][nsplit]  (m2, l), see part_index
   float* mrow;   // [B*KVH][Rpad]          M2 + log2(L)  (+inf: no visible key)
   float* out;    // [B*KVH][S]
   float out_mul; // 1/G
 };
+
+// (m, l) partial of query row r from key range `split`: a row's ranges are contiguous
+__host__ __device__ __forceinline__ int64_t part_index(const ScoresArgs& a, int bk, int r, int split) {
+  return ((int64_t)bk * a.Rpad + r) * a.nsplit + split;
+}
+#ifdef __CUDACC__
+// Row r's normaliser over all key ranges, log2 domain: M + log2(L) with M = max m and
+// L = sum l * 2^(m - M); +inf when the row sees no key.  Loads are issued eight at a time.
+__device__ __forceinline__ float merge_row(const ScoresArgs& a, int bk, int r) {
+  const float2* p = a.part + part_index(a, bk, r, 0);
+  float M = -__int_as_float(0x7f800000), Ls = 0.f;
+  for (int s0 = 0; s0 < a.nsplit; s0 += 8) {
+    float2 o[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o[q] = (s0 + q < a.nsplit) ? p[s0 + q] : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (o[q].y > 0.f) {
+        if (o[q].x > M) {
+          Ls = Ls * exp2f(M - o[q].x) + o[q].y;
+          M = o[q].x;
+        } else {
+          Ls += o[q].y * exp2f(o[q].x - M);
+        }
+      }
+    }
+  }
+  return Ls > 0.f ? M + log2f(Ls) : __int_as_float(0x7f800000);
+}
+#endif
 
 constexpr int KEY_UNIT = 128;
 // keys [*kbeg, *kend) of key range `split` (balanced: ranges differ by at most one unit)

@@ -267,15 +267,14 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass1(const ScoresArgs a) {
       l += __shfl_xor_sync(0xffffffffu, l, 2);
       l_run[mi][hh] = l;
     }
-  float2* part = a.part + ((int64_t)bk * a.nsplit + split) * a.Rpad;
   if (kg == 1) {
     if (t == 0) {
 #pragma unroll
       for (int mi = 0; mi < 2; ++mi) {
         if (mi < n_my) {
           const int r = row0 + (mi == 0 ? mt0 : mt1) * 16 + g;
-          part[r] = make_float2(m_run[mi][0], l_run[mi][0]);
-          part[r + 8] = make_float2(m_run[mi][1], l_run[mi][1]);
+          a.part[part_index(a, bk, r, split)] = make_float2(m_run[mi][0], l_run[mi][0]);
+          a.part[part_index(a, bk, r + 8, split)] = make_float2(m_run[mi][1], l_run[mi][1]);
         }
       }
     }
@@ -298,7 +297,7 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass1(const ScoresArgs a) {
         const float2 v = mrg[(kgi * n_mt + mt) * 16 + rr];
         if (v.y > 0.f) L += v.y * ex2(v.x - M);
       }
-      part[row0 + tid] = make_float2(M, L);
+      a.part[part_index(a, bk, row0 + tid, split)] = make_float2(M, L);
     }
   }
 }
@@ -308,20 +307,7 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass1(const ScoresArgs a) {
 // ----------------------------------------------------------------------------------------
 __global__ void k_scores_merge(const ScoresArgs a) {
   const int bk = blockIdx.x;
-  for (int r = threadIdx.x; r < a.Rpad; r += blockDim.x) {
-    const float2* p = a.part + (int64_t)bk * a.nsplit * a.Rpad + r;
-    float M = -CUDART_INF_F;
-    for (int s = 0; s < a.nsplit; ++s) {
-      const float2 v = p[(int64_t)s * a.Rpad];
-      if (v.y > 0.f) M = fmaxf(M, v.x);
-    }
-    float L = 0.f;
-    for (int s = 0; s < a.nsplit; ++s) {
-      const float2 v = p[(int64_t)s * a.Rpad];
-      if (v.y > 0.f) L += v.y * ex2(v.x - M);
-    }
-    a.mrow[(int64_t)bk * a.Rpad + r] = (L > 0.f) ? (M + log2f(L)) : CUDART_INF_F;
-  }
+  for (int r = threadIdx.x; r < a.Rpad; r += blockDim.x) a.mrow[(int64_t)bk * a.Rpad + r] = merge_row(a, bk, r);
 }
 
 // ----------------------------------------------------------------------------------------
@@ -475,9 +461,8 @@ cudaError_t launch_impl(const ScoresArgs& a, int reduce, float* scores, cudaStre
   cudaError_t e = set_smem_attrs<D>();
   if (e != cudaSuccess) return e;
   if (tc_supported(a, D)) {
-    e = launch_pass1_tc(a, D, st);
+    e = launch_pass1_tc(a, D, st);  // pass 2 merges the key-range partials itself
     if (e != cudaSuccess) return e;
-    k_scores_merge<<<a.B * a.KVH, 256, 0, st>>>(a);
     e = launch_pass2_tc(a, D, st);
     if (e != cudaSuccess) return e;
   } else {

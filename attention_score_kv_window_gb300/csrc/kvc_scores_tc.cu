@@ -31,10 +31,10 @@ namespace {
 
 constexpr int TILE = 128;           // keys per tile
 constexpr int STAGES = 4;           // K ring depth
-constexpr int EPI_WARPS = 8;
-constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;
-constexpr int THREADS = 320;
+constexpr int EPI_WARPS = 16;       // 4 per SM sub-partition
+constexpr int PRODUCER_WARP = 16;
+constexpr int MMA_WARP = 17;
+constexpr int THREADS = 576;
 constexpr int QROWS_MAX = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s bound on any single wait
@@ -50,12 +50,12 @@ struct Layout {
   static constexpr uint32_t K = Q + NP * qpanel_bytes();
   static constexpr uint32_t STAGE = NP * kpanel_bytes();
   static constexpr uint32_t BARS = K + STAGES * STAGE;      // 2*STAGES + 5 mbarriers
-  static constexpr uint32_t MISC = BARS + 8 * (2 * STAGES + 5);  // tmem base, abort flag
-  static constexpr uint32_t CR = MISC + 16;                 // float[256]
+  static constexpr uint32_t MISC = (BARS + 8 * (2 * STAGES + 5) + 15) / 16 * 16;  // tmem base, abort flag
+  static constexpr uint32_t CR = MISC + 16;                 // float[256], 16-byte aligned (float4 reads)
   static constexpr uint32_t LIM = CR + 256 * 4;             // int[256]
-  static constexpr uint32_t STAT = LIM + 256 * 4;           // float2[128]
-  static constexpr uint32_t KSUM = STAT + 128 * 8;          // float[2][2][128]
-  static constexpr uint32_t END = KSUM + 2 * 2 * 128 * 4;
+  static constexpr uint32_t STAT = LIM + 256 * 4;           // float2[4][256]
+  static constexpr uint32_t KSUM = STAT + 4 * 256 * 8;      // float[2][4][128]
+  static constexpr uint32_t END = KSUM + 2 * 4 * 128 * 4;
   static constexpr size_t SMEM = END + 1024;                // + alignment slack
 };
 
@@ -160,7 +160,20 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ void named_sync_epilogue() { asm volatile("bar.sync 1, 256;\n" ::: "memory"); }
+__device__ __forceinline__ void named_sync_epilogue() { asm volatile("bar.sync 1, 512;\n" ::: "memory"); }
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane, then wait for the load
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
 
 // 32 consecutive 32-bit TMEM columns of this thread's lane, then wait for the load
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
@@ -204,8 +217,13 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float* v) {
 
 template <int NC>
 __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float* v) {
-  if constexpr (NC == 32) {
+  if constexpr (NC == 16) {
+    tmem_ld16(taddr, v);
+  } else if constexpr (NC == 32) {
     tmem_ld32(taddr, v);
+  } else if constexpr (NC == 48) {
+    tmem_ld32(taddr, v);
+    tmem_ld16(taddr + 32, v + 32);
   } else if constexpr (NC == 64) {
     tmem_ld64(taddr, v);
   } else if constexpr (NC == 96) {
@@ -311,11 +329,39 @@ __device__ __forceinline__ void producer(const Ctx& c, const ScoresArgs& a, cons
 // ----------------------------------------------------------------------------------------
 // pass 1
 // ----------------------------------------------------------------------------------------
+__device__ __forceinline__ float max8(const float* v, int n) {
+  float m[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) m[q] = -CUDART_INF_F;
+  for (int i = 0; i < n; i += 8) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m[q] = fmaxf(m[q], v[i + q]);
+  }
+  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+// sum_i exp2(v_i * sl2 - off) with eight independent accumulators
+template <int NC>
+__device__ __forceinline__ float sum_exp8(const float* v, float sl2, float off) {
+  float s[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) s[q] = 0.f;
+#pragma unroll
+  for (int i = 0; i < NC; i += 8) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s[q] += ex2(fmaf(v[i + q], sl2, -off));
+  }
+  return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+}
+
+// Epilogue warp w reads columns [part*NC, part*NC + NC) of accumulator half h for the query
+// rows of lane quadrant w%4; the row's (max, sum) is then merged over its NPART warps.
 template <int D, int NHALF>
 __global__ void __launch_bounds__(THREADS, 1)
     k_pass1_tc(const ScoresArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ) {
   using L = Layout<D>;
   constexpr int KS = D / 16;
+  constexpr int NPART = 4 / NHALF;        // warps sharing one query row
+  constexpr int NC = TILE / NPART;        // accumulator columns per warp
   extern __shared__ unsigned char smem_raw[];
   const Ctx c = prologue<D>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -357,13 +403,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else {
-    // epilogue: one query row per thread
-    constexpr int NC = NHALF == 2 ? 128 : 64;
+    // epilogue: one query row per thread and warp-part
     const int qd = warp & 3;
-    const int h = NHALF == 2 ? (warp >> 2) : 0;
-    const int c0 = NHALF == 2 ? 0 : (warp >> 2) * 64;
+    const int h = NHALF == 2 ? ((warp >> 2) & 1) : 0;
+    const int part = NHALF == 2 ? (warp >> 3) : (warp >> 2);
+    const int c0 = part * NC;
     const int r = h * 128 + qd * 32 + lane;
     const int lim = row_limit_i(a, r);
+    // (m, l): l = sum exp2(s*log2e - m).  m is a reference, not always the exact max: a tile
+    // is accumulated against the current m unless its sum shows values more than 2^64 above
+    // it, in which case the exact tile max is taken and l rescaled.
     float m = -CUDART_INF_F, l = 0.f;
     float v[NC];
     for (int it = 0; it < ntiles; ++it) {
@@ -375,49 +424,47 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(c.tempty(buf));
-      const int64_t kt0 = kbeg + (int64_t)it * TILE;
-      const bool clean = (kt0 + TILE <= kend) && (!a.causal || kt0 + TILE - 1 <= a.S - a.w) && lim >= 0;
-      float mx = -CUDART_INF_F;
-      if (clean) {
-#pragma unroll
-        for (int i = 0; i < NC; ++i) mx = fmaxf(mx, v[i]);
-      } else {
+      if (lim < 0) continue;
+      const int64_t kt0 = kbeg + (int64_t)it * TILE + c0;
+      const bool clean = (kt0 + NC <= kend) && (!a.causal || kt0 + NC - 1 <= (int64_t)lim);
+      if (!clean) {
 #pragma unroll
         for (int i = 0; i < NC; ++i) {
-          const int64_t j = kt0 + c0 + i;
+          const int64_t j = kt0 + i;
           if (j >= kend || j > lim) v[i] = -CUDART_INF_F;
-          mx = fmaxf(mx, v[i]);
         }
       }
+      if (m != -CUDART_INF_F) {
+        const float t = sum_exp8<NC>(v, a.sl2, m);
+        if (t <= 0x1p64f) {
+          l += t;
+          continue;
+        }
+      }
+      const float mx = max8(v, NC);
       if (mx == -CUDART_INF_F) continue;
       const float mn = fmaxf(m, mx * a.sl2);
-      float s0 = l * ex2(m - mn), s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-      for (int i = 0; i < NC; i += 4) {
-        s0 += ex2(fmaf(v[i], a.sl2, -mn));
-        s1 += ex2(fmaf(v[i + 1], a.sl2, -mn));
-        s2 += ex2(fmaf(v[i + 2], a.sl2, -mn));
-        s3 += ex2(fmaf(v[i + 3], a.sl2, -mn));
-      }
-      l = (s0 + s1) + (s2 + s3);
+      l = l * ex2(m - mn) + sum_exp8<NC>(v, a.sl2, mn);
       m = mn;
     }
-    float2* part = a.part + ((int64_t)bk * a.nsplit + split) * a.Rpad;
-    if (NHALF == 2) {
-      if (r < a.Rpad) part[r] = make_float2(m, l);
-    } else {
-      float2* stat = reinterpret_cast<float2*>(c.base + L::STAT);
-      if (warp >= 4) stat[qd * 32 + lane] = make_float2(m, l);
-      named_sync_epilogue();
-      if (warp < 4) {
-        const float2 o = stat[qd * 32 + lane];
-        float M = -CUDART_INF_F, Lsum = 0.f;
-        if (l > 0.f) M = m;
+    // merge the NPART partial (m, l) of each row
+    float2* stat = reinterpret_cast<float2*>(c.base + L::STAT);
+    stat[part * 256 + r] = make_float2(m, l);
+    named_sync_epilogue();
+    if (part == 0) {
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int q = 0; q < NPART; ++q) {
+        const float2 o = stat[q * 256 + r];
         if (o.y > 0.f) M = fmaxf(M, o.x);
-        if (l > 0.f) Lsum += l * ex2(m - M);
-        if (o.y > 0.f) Lsum += o.y * ex2(o.x - M);
-        if (r < a.Rpad) part[r] = make_float2(M, Lsum);
       }
+      float Lsum = 0.f;
+#pragma unroll
+      for (int q = 0; q < NPART; ++q) {
+        const float2 o = stat[q * 256 + r];
+        if (o.y > 0.f) Lsum += o.y * ex2(o.x - M);
+      }
+      if (r < a.Rpad) a.part[part_index(a, bk, r, split)] = make_float2(M, Lsum);
     }
   }
   teardown<D>(c);
@@ -426,12 +473,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 // ----------------------------------------------------------------------------------------
 // pass 2
 // ----------------------------------------------------------------------------------------
-template <int D, int NH>
+// Epilogue warp w reads, for the 32 keys of lane quadrant w%4, the NQ query-row columns
+// [(w/4)*NQ, (w/4)*NQ + NQ); the four partial key sums are added after a named barrier.
+// The per-row normalisers c_r = M + log2(L) are merged from pass 1's key-range partials in
+// the prologue (no separate merge launch).
+template <int D, int NQ>
 __global__ void __launch_bounds__(THREADS, 1)
     k_pass2_tc(const ScoresArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ) {
   using L = Layout<D>;
   constexpr int KS = D / 16;
-  constexpr int N = 2 * NH;
+  constexpr int N = 4 * NQ;
   extern __shared__ unsigned char smem_raw[];
   const Ctx c = prologue<D>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -469,22 +520,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     __syncwarp();
   } else {
-    // epilogue: one key per thread, half of the query rows per warp
     float* cr = reinterpret_cast<float*>(c.base + L::CR);
     int* limr = reinterpret_cast<int*>(c.base + L::LIM);
     float* ksum = reinterpret_cast<float*>(c.base + L::KSUM);
+    // merge pass 1's key-range partials: c_r = M + log2(L), +inf when the row sees no key
     for (int r = threadIdx.x; r < N; r += EPI_WARPS * 32) {
-      cr[r] = a.mrow[(int64_t)bk * a.Rpad + r];
+      cr[r] = merge_row(a, bk, r);
       limr[r] = row_limit_i(a, r);
     }
     named_sync_epilogue();
-    const int qd = warp & 3, ch = warp >> 2;
+    const int qd = warp & 3, cq = warp >> 2;
     const int kr = qd * 32 + lane;
-    const float* crh = cr + ch * NH;
-    const int* limh = limr + ch * NH;
+    const float* crq = cr + cq * NQ;
+    const int* limq = limr + cq * NQ;
     float* out = a.out + (int64_t)bk * a.S;
     bool dead = false;
-    float v[NH];
+    float v[NQ];
     for (int it = 0; it < ntiles; ++it) {
       const int buf = it & 1;
       const uint32_t bph = (uint32_t)(it >> 1) & 1u;
@@ -493,32 +544,43 @@ __global__ void __launch_bounds__(THREADS, 1)
       float acc = 0.f;
       if (!dead && wait_bar(c.tfull(buf), bph, c.abort_flag)) {
         tc_fence_after();
-        tmem_load_cols<NH>(c.tmem + ((uint32_t)(qd * 32) << 16) + buf * 256 + ch * NH, v);
+        tmem_load_cols<NQ>(c.tmem + ((uint32_t)(qd * 32) << 16) + buf * 256 + cq * NQ, v);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(c.tempty(buf));
         const bool clean = (kt0 + TILE <= kend) && (!a.causal || kt0 + TILE - 1 <= a.S - a.w);
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        float s[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) s[q] = 0.f;
         if (clean) {
 #pragma unroll
-          for (int i = 0; i < NH; i += 4) {
-            s0 += ex2(fmaf(v[i], a.sl2, -crh[i]));
-            s1 += ex2(fmaf(v[i + 1], a.sl2, -crh[i + 1]));
-            s2 += ex2(fmaf(v[i + 2], a.sl2, -crh[i + 2]));
-            s3 += ex2(fmaf(v[i + 3], a.sl2, -crh[i + 3]));
+          for (int i = 0; i < NQ; i += 8) {
+            const float4 c4a = *reinterpret_cast<const float4*>(crq + i);
+            const float4 c4b = *reinterpret_cast<const float4*>(crq + i + 4);
+            s[0] += ex2(fmaf(v[i + 0], a.sl2, -c4a.x));
+            s[1] += ex2(fmaf(v[i + 1], a.sl2, -c4a.y));
+            s[2] += ex2(fmaf(v[i + 2], a.sl2, -c4a.z));
+            s[3] += ex2(fmaf(v[i + 3], a.sl2, -c4a.w));
+            s[4] += ex2(fmaf(v[i + 4], a.sl2, -c4b.x));
+            s[5] += ex2(fmaf(v[i + 5], a.sl2, -c4b.y));
+            s[6] += ex2(fmaf(v[i + 6], a.sl2, -c4b.z));
+            s[7] += ex2(fmaf(v[i + 7], a.sl2, -c4b.w));
           }
         } else if (j < kend) {
 #pragma unroll
-          for (int i = 0; i < NH; ++i)
-            if (j <= limh[i]) s0 += ex2(fmaf(v[i], a.sl2, -crh[i]));
+          for (int i = 0; i < NQ; ++i)
+            if (j <= limq[i]) s[i & 7] += ex2(fmaf(v[i], a.sl2, -crq[i]));
         }
-        acc = (s0 + s1) + (s2 + s3);
+        acc = ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
       } else {
         dead = true;
       }
-      ksum[(buf * 2 + ch) * 128 + kr] = acc;
+      ksum[(buf * 4 + cq) * 128 + kr] = acc;
       named_sync_epilogue();
-      if (ch == 0 && !dead && j < kend) out[j] = (acc + ksum[(buf * 2 + 1) * 128 + kr]) * a.out_mul;
+      if (cq == 0 && !dead && j < kend) {
+        const float* kb = ksum + buf * 4 * 128 + kr;
+        out[j] = ((acc + kb[128]) + (kb[256] + kb[384])) * a.out_mul;
+      }
     }
   }
   teardown<D>(c);
@@ -585,14 +647,14 @@ cudaError_t run_pass1(const ScoresArgs& a, cudaStream_t st, int slot) {
   return cudaGetLastError();
 }
 
-template <int D, int NH>
+template <int D, int NQ>
 cudaError_t run_pass2(const ScoresArgs& a, cudaStream_t st, int slot) {
   CUtensorMap tmK, tmQ;
-  if (!make_maps(a, D, 2 * NH, &tmK, &tmQ)) return cudaErrorInvalidValue;
+  if (!make_maps(a, D, 4 * NQ, &tmK, &tmQ)) return cudaErrorInvalidValue;
   const size_t smem = Layout<D>::SMEM;
-  cudaError_t e = set_smem_once(k_pass2_tc<D, NH>, smem, slot);
+  cudaError_t e = set_smem_once(k_pass2_tc<D, NQ>, smem, slot);
   if (e != cudaSuccess) return e;
-  k_pass2_tc<D, NH><<<dim3(a.nsplit, a.KVH, a.B), THREADS, smem, st>>>(a, tmK, tmQ);
+  k_pass2_tc<D, NQ><<<dim3(a.nsplit, a.KVH, a.B), THREADS, smem, st>>>(a, tmK, tmQ);
   return cudaGetLastError();
 }
 
@@ -616,20 +678,20 @@ cudaError_t launch_pass1_tc(const ScoresArgs& a, int D, cudaStream_t st) {
 }
 
 cudaError_t launch_pass2_tc(const ScoresArgs& a, int D, cudaStream_t st) {
-  const int nh = a.Rpad / 2;
+  const int nq = a.Rpad / 4;
   if (D == 64) {
-    switch (nh) {
-      case 32: return run_pass2<64, 32>(a, st, 4);
-      case 64: return run_pass2<64, 64>(a, st, 5);
-      case 96: return run_pass2<64, 96>(a, st, 6);
-      default: return run_pass2<64, 128>(a, st, 7);
+    switch (nq) {
+      case 16: return run_pass2<64, 16>(a, st, 4);
+      case 32: return run_pass2<64, 32>(a, st, 5);
+      case 48: return run_pass2<64, 48>(a, st, 6);
+      default: return run_pass2<64, 64>(a, st, 7);
     }
   }
-  switch (nh) {
-    case 32: return run_pass2<128, 32>(a, st, 8);
-    case 64: return run_pass2<128, 64>(a, st, 9);
-    case 96: return run_pass2<128, 96>(a, st, 10);
-    default: return run_pass2<128, 128>(a, st, 11);
+  switch (nq) {
+    case 16: return run_pass2<128, 16>(a, st, 8);
+    case 32: return run_pass2<128, 32>(a, st, 9);
+    case 48: return run_pass2<128, 48>(a, st, 10);
+    default: return run_pass2<128, 64>(a, st, 11);
   }
 }
 

@@ -4,13 +4,15 @@
 //
 // A row is split over a thread-block cluster of up to 8 CTAs (1024 threads each); each CTA
 // loads its slice of keys into shared memory once.  An MSB-first radix select (digits of
-// 11, 11 and 10 bits) builds shared-memory histograms with warp-aggregated atomics, sums
-// them over the cluster through distributed shared memory, and finds the digit holding the
-// k-th item with one block scan; this yields the k-th key T and how many keys equal to T
-// are taken.  The output pass counts, per warp and per CTA, the keys certainly taken (> T)
-// and those equal to T, exchanges the CTA counts over the cluster, and writes every taken
-// index at (taken-for-sure before it) + (taken-equal before it): ascending order, no sort.
-// Cluster barriers are hardware barriers; there are no spin-waits.
+// 11, 11 and 10 bits) builds shared-memory histograms with warp-aggregated atomics; each CTA
+// then adds its nonzero bins into every peer's copy of the cluster histogram with remote
+// reductions (pushes do not stall; remote loads would), and after one cluster barrier each
+// CTA finds the digit holding the k-th item locally with one block scan.  This yields the
+// k-th key T and how many keys equal to T are taken.  The output pass counts, per warp and
+// per CTA, the keys certainly taken (> T) and those equal to T, pushes the CTA counts to
+// every peer, and writes every taken index at (taken-for-sure before it) + (taken-equal
+// before it): ascending order, no sort.  Cluster barriers are hardware barriers; there are
+// no spin-waits.
 //
 // Users: token top-k for SnapKV/TOVA ("Add TOVA press"; cold-compress PR 11, SnapKV keeps
 // the observation window) and Scissorhands eviction by low-attention fraction.
@@ -76,11 +78,12 @@ struct FractionKeys {
   }
 };
 
-struct SelShared {
-  uint32_t hist[2][2048];
+struct __align__(16) SelShared {
+  uint32_t hist[2048];                // this CTA's counts for the current digit
+  uint32_t hsum[3][2048];             // cluster sums per digit pass, filled by every CTA's pushes
+  uint32_t cnt_all[MAX_CLUSTER][4];   // counters pushed by each CTA: forced, eligible, sure, equal
   uint32_t warp_a[32];
   uint32_t warp_b[32];
-  uint32_t cta_cnt[4];  // read by the other CTAs of the cluster: forced, eligible, sure, equal
   uint32_t prefix, remaining, eq_total;
 };
 
@@ -111,12 +114,87 @@ __device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* warp_buf, u
   return base + x;
 }
 
+// Writes into the shared memory of CTA `rank` of the cluster.  They do not stall the issuing
+// thread; the next cluster barrier (release/acquire) makes them visible.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, int rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n"
+               : "=r"(ra)
+               : "r"((uint32_t)__cvta_generic_to_shared(local)), "r"(rank));
+  return ra;
+}
+__device__ __forceinline__ void push_add(const uint32_t* local, int rank, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;\n" ::"r"(cluster_addr(local, rank)), "r"(v) : "memory");
+}
+__device__ __forceinline__ void push_v4(const uint32_t* local, int rank, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};\n" ::"r"(cluster_addr(local, rank)), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// Add this CTA's nonzero bins into hsum[pass] of every CTA of the cluster.
+__device__ __forceinline__ void push_bins(SelShared& sh, int pass, uint32_t nbins, int cs) {
+  for (uint32_t b = threadIdx.x; b < nbins; b += SEL_THREADS) {
+    const uint32_t v = sh.hist[b];
+    if (v) {
+      for (int r = 0; r < cs; ++r) push_add(&sh.hsum[pass][b], r, v);
+    }
+  }
+}
+
+// Digit holding the rem-th largest item, from the cluster-summed bins of `pass` (local):
+// one block scan over the bins in descending order; the thread whose bins contain it
+// publishes the new prefix, remainder and tie count.
+__device__ __forceinline__ void find_digit(SelShared& sh, int pass, uint32_t nbins, int shift, uint32_t prefix,
+                                           uint32_t rem) {
+  const uint32_t bpt = nbins >> 10;  // 2 or 1 bins per thread
+  uint32_t hb[2] = {0u, 0u};
+  for (uint32_t q = 0; q < bpt; ++q) hb[q] = sh.hsum[pass][nbins - 1u - (threadIdx.x * bpt + q)];
+  const uint32_t hs = hb[0] + hb[1];
+  uint32_t tot;
+  const uint32_t incl = block_scan(hs, sh.warp_a, &tot);
+  const uint32_t excl = incl - hs;
+  if (excl < rem && rem <= incl) {
+    uint32_t run = excl;
+    for (uint32_t q = 0; q < bpt; ++q) {
+      const uint32_t d = nbins - 1u - (threadIdx.x * bpt + q);
+      if (run + hb[q] >= rem) {
+        sh.prefix = prefix | (d << shift);
+        sh.remaining = rem - run;
+        sh.eq_total = hb[q];
+        break;
+      }
+      run += hb[q];
+    }
+  }
+  __syncthreads();
+}
+
+// per-warp totals of two counters -> this CTA's totals (thread 0)
+__device__ __forceinline__ uint4 cta_totals(SelShared& sh, uint32_t a, uint32_t b, int lane, int warp) {
+  if (lane == 0) {
+    sh.warp_a[warp] = a;
+    sh.warp_b[warp] = b;
+  }
+  __syncthreads();
+  uint4 t = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < 32; ++q) {
+      t.x += sh.warp_a[q];
+      t.y += sh.warp_b[q];
+    }
+  }
+  return t;
+}
+
 template <class Fn>
 __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_t* kc, SelShared& sh,
                            bool evict_order) {
-  cg::cluster_group cl = cg::this_cluster();
-  const int cs = (int)cl.num_blocks();
-  const int cr = (int)cl.block_rank();
+  const int cs = (int)cg::this_cluster().num_blocks();
+  const int cr = (int)cg::this_cluster().block_rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lower = (1u << lane) - 1u;
   // this CTA's slice [c0, c1) of the row, and this warp's contiguous segment [w0, w1) of it
@@ -128,54 +206,63 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
   const int64_t w0 = c0 + (int64_t)warp * per_w;
   const int64_t w1 = w0 + per_w < c1 ? w0 + per_w : c1;
 
-  // keys of the slice into shared memory (independent loads, many in flight)
-#pragma unroll 8
-  for (int64_t j = c0 + tid; j < c1; j += SEL_THREADS) kc[j - c0] = fn.key(j);
-
-  // 1. forced / eligible counts over the cluster
-  uint32_t cf = 0, ce = 0;
-  for (int64_t base = w0; base < w1; base += 32) {
-    const int64_t j = base + lane;
-    const bool in = j < w1;
-    const bool f = in && fn.forced(j);
-    const bool e = in && !f && fn.eligible(j);
-    cf += __popc(__ballot_sync(0xffffffffu, f));
-    ce += __popc(__ballot_sync(0xffffffffu, e));
-  }
-  if (lane == 0) {
-    sh.warp_a[warp] = cf;
-    sh.warp_b[warp] = ce;
+  // 1. one sweep: keys into shared memory, forced / eligible counts, first-digit histogram
+  for (uint32_t i = tid; i < 2048u; i += SEL_THREADS) {
+    sh.hist[i] = 0u;
+    sh.hsum[0][i] = 0u;
+    sh.hsum[1][i] = 0u;
+    sh.hsum[2][i] = 0u;
   }
   __syncthreads();
-  if (tid == 0) {
-    uint32_t a = 0, b = 0;
-    for (int q = 0; q < 32; ++q) {
-      a += sh.warp_a[q];
-      b += sh.warp_b[q];
+  uint32_t cf = 0, ce = 0;
+  for (int64_t j0 = 0; j0 < len; j0 += 4 * SEL_THREADS) {
+    uint32_t key[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t jl = j0 + u * SEL_THREADS + tid;
+      key[u] = jl < len ? fn.key(c0 + jl) : 0u;
     }
-    sh.cta_cnt[0] = a;
-    sh.cta_cnt[1] = b;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t jl = j0 + u * SEL_THREADS + tid;
+      bool f = false, e = false;
+      uint32_t d = 0xffffffffu;
+      if (jl < len) {
+        kc[jl] = key[u];
+        f = fn.forced(c0 + jl);
+        e = !f && fn.eligible(c0 + jl);
+        if (e) d = key[u] >> 21;
+      }
+      cf += __popc(__ballot_sync(0xffffffffu, f));
+      ce += __popc(__ballot_sync(0xffffffffu, e));
+      const uint32_t peers = __match_any_sync(0xffffffffu, d);
+      if (d != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (uint32_t)__popc(peers));
+    }
   }
-  cl.sync();
+  const uint4 tot0 = cta_totals(sh, cf, ce, lane, warp);
+  cluster_barrier();  // every CTA's hsum is zeroed and its first-digit counts are complete
+  if (tid == 0)  // tot0 is valid in thread 0 only
+    for (int r = 0; r < cs; ++r) push_v4(&sh.cnt_all[cr][0], r, tot0);
+  push_bins(sh, 0, 2048u, cs);
+  cluster_barrier();
   uint32_t n_forced = 0, n_elig = 0;
   for (int r = 0; r < cs; ++r) {
-    const SelShared* rs = cl.map_shared_rank(&sh, r);
-    n_forced += rs->cta_cnt[0];
-    n_elig += rs->cta_cnt[1];
+    n_forced += sh.cnt_all[r][0];
+    n_elig += sh.cnt_all[r][1];
   }
   const int64_t need = (int64_t)k - (int64_t)n_forced > 0 ? (int64_t)k - (int64_t)n_forced : 0;
   const bool take_all = (int64_t)n_elig <= need;
   const bool split_ties = !take_all && need > 0;
 
-  // 2. radix select of the need-th largest eligible key over the cluster
+  // 2. radix select of the need-th largest eligible key: digits of 11, 11 and 10 bits
   uint32_t T = 0, take_eq = 0, eq_total = 0;
   if (split_ties) {
-    uint32_t prefix = 0, rem = (uint32_t)need, hi_mask = 0;
-    for (int pass = 0; pass < 3; ++pass) {
-      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-      const uint32_t nbins = pass == 2 ? 1024u : 2048u;
-      uint32_t* hist = sh.hist[pass & 1];
-      for (uint32_t i = tid; i < nbins; i += SEL_THREADS) hist[i] = 0u;
+    find_digit(sh, 0, 2048u, 21, 0u, (uint32_t)need);
+    uint32_t prefix = sh.prefix, rem = sh.remaining, hi_mask = 0x7FFu << 21;
+    for (int pass = 1; pass < 3; ++pass) {
+      const int shift = pass == 1 ? 10 : 0;
+      const uint32_t nbins = pass == 1 ? 2048u : 1024u;
+      for (uint32_t i = tid; i < nbins; i += SEL_THREADS) sh.hist[i] = 0u;
       __syncthreads();
       for (int64_t j0 = 0; j0 < len; j0 += SEL_THREADS) {
         const int64_t jl = j0 + tid;
@@ -185,34 +272,12 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
           if ((key & hi_mask) == prefix) d = (key >> shift) & (nbins - 1u);
         }
         const uint32_t peers = __match_any_sync(0xffffffffu, d);
-        if (d != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
-      }
-      cl.sync();
-      // this thread's bins, in descending digit order, summed over the cluster
-      const uint32_t bpt = nbins >> 10;
-      uint32_t hb[2] = {0u, 0u};
-      for (int r = 0; r < cs; ++r) {
-        const uint32_t* rh = cl.map_shared_rank(hist, r);
-        for (uint32_t q = 0; q < bpt; ++q) hb[q] += rh[nbins - 1u - (tid * bpt + q)];
-      }
-      const uint32_t hs = hb[0] + hb[1];
-      uint32_t tot;
-      const uint32_t incl = block_scan(hs, sh.warp_a, &tot);
-      const uint32_t excl = incl - hs;
-      if (excl < rem && rem <= incl) {
-        uint32_t run = excl;
-        for (uint32_t q = 0; q < bpt; ++q) {
-          const uint32_t d = nbins - 1u - (tid * bpt + q);
-          if (run + hb[q] >= rem) {
-            sh.prefix = prefix | (d << shift);
-            sh.remaining = rem - run;
-            sh.eq_total = hb[q];
-            break;
-          }
-          run += hb[q];
-        }
+        if (d != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (uint32_t)__popc(peers));
       }
       __syncthreads();
+      push_bins(sh, pass, nbins, cs);
+      cluster_barrier();
+      find_digit(sh, pass, nbins, shift, prefix, rem);
       prefix = sh.prefix;
       rem = sh.remaining;
       hi_mask |= (nbins - 1u) << shift;
@@ -243,25 +308,15 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
     cd += __popc(__ballot_sync(0xffffffffu, def));
     cq += __popc(__ballot_sync(0xffffffffu, eq));
   }
-  if (lane == 0) {
-    sh.warp_a[warp] = cd;
-    sh.warp_b[warp] = cq;
-  }
-  __syncthreads();
+  uint4 tot1 = cta_totals(sh, cd, cq, lane, warp);
   if (tid == 0) {
-    uint32_t a = 0, b = 0;
-    for (int q = 0; q < 32; ++q) {
-      a += sh.warp_a[q];
-      b += sh.warp_b[q];
-    }
-    sh.cta_cnt[2] = a;
-    sh.cta_cnt[3] = b;
+    tot1 = make_uint4(tot0.x, tot0.y, tot1.x, tot1.y);
+    for (int r = 0; r < cs; ++r) push_v4(&sh.cnt_all[cr][0], r, tot1);
   }
-  cl.sync();
+  cluster_barrier();
   uint32_t d_run = 0, e_run = 0, d_total = 0;
   for (int r = 0; r < cs; ++r) {
-    const SelShared* rs = cl.map_shared_rank(&sh, r);
-    const uint32_t a = rs->cta_cnt[2], b = rs->cta_cnt[3];
+    const uint32_t a = sh.cnt_all[r][2], b = sh.cnt_all[r][3];
     if (r < cr) {
       d_run += a;
       e_run += b;
@@ -302,7 +357,7 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
     const uint32_t total = d_total + (split_ties ? take_eq : 0u);
     for (int64_t p = (int64_t)total + tid; p < k; p += SEL_THREADS) out[p] = -1;
   }
-  cl.sync();  // no CTA leaves while the others may still read its shared memory
+  // no remote access follows the last cluster barrier, so CTAs may leave independently
 }
 
 __global__ void __launch_bounds__(SEL_THREADS) k_topk(const float* __restrict__ scores, int64_t S, int k,
@@ -333,7 +388,8 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sh_evict(kvc_sh_state s, int m,
   fn.history = s.history;
   int32_t* out = evicted + row * m;
   select_row<FractionKeys>(fn, s.cap, m, out, kc, sh, false);
-  // clear the live bits of the evicted slots (select_row ended with a barrier)
+  __syncthreads();  // the evicted list written by all threads is now visible to the block
+  // clear the live bits of the evicted slots
   uint32_t* lw = s.live + row * nw;
   for (int p = threadIdx.x; p < m; p += SEL_THREADS) {
     const int32_t j = out[p];
@@ -341,9 +397,11 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sh_evict(kvc_sh_state s, int m,
   }
 }
 
+// CTAs per row: a power of two (the histogram exchange splits 1024 or 2048 bins evenly)
 int topk_cluster_size(int64_t S) {
-  if (S <= 8192) return 1;
-  return (int)std::min<int64_t>(MAX_CLUSTER, (S + 4095) / 4096);
+  int cs = 1;
+  while (cs < MAX_CLUSTER && S > (int64_t)cs * 4096) cs *= 2;
+  return cs;
 }
 
 }  // namespace
