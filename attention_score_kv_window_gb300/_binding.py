@@ -72,6 +72,7 @@ _SIGNATURES = {
     "kvc_status_string": (ctypes.c_char_p, [_I32]),
     "kvc_last_error_message": (ctypes.c_char_p, []),
     "kvc_version": (_I32, []),
+    "kvc_launch_count": (_I64, []),
 }
 
 
@@ -119,6 +120,12 @@ def _bf16(t, name):
     if t.dtype != torch.bfloat16:
         raise TypeError(f"{name} must be bfloat16")
     return t
+
+
+def _dense(t, shape, name):
+    """Outputs the library writes densely must be contiguous tensors of exactly this shape."""
+    if tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous tensor of shape {tuple(shape)}")
 
 
 def kv_desc(K: torch.Tensor, H: int) -> KvDesc:
@@ -201,6 +208,9 @@ def kvc_compact_kv(K, V, idx, H=None, K_out=None, V_out=None, stream=None):
         K_out = torch.empty((B, KVH, k, D), dtype=K.dtype, device=K.device)
     if V is not None and V_out is None:
         V_out = torch.empty((B, KVH, k, D), dtype=V.dtype, device=V.device)
+    _dense(K_out, (B, KVH, k, D), "K_out")
+    if V_out is not None:
+        _dense(V_out, (B, KVH, k, D), "V_out")
     _check(lib.kvc_compact_kv(_ptr(K), _ptr(V), ctypes.byref(desc), _ptr(idx.contiguous()), k, _ptr(K_out),
                               _ptr(V_out), _stream(stream)))
     return K_out, V_out
@@ -338,3 +348,8 @@ def kvc_status_string(s: int) -> str:
 
 def kvc_version() -> int:
     return int(load_library().kvc_version())
+
+
+def kvc_launch_count() -> int:
+    """Kernels the library has enqueued since it was loaded (diagnostic counter)."""
+    return int(load_library().kvc_launch_count())

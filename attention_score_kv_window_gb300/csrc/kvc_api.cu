@@ -7,6 +7,7 @@
 #include <stdio.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "kvc_internal.cuh"
@@ -102,6 +103,13 @@ void set_error(const char* fmt, ...) {
   va_end(ap);
 }
 
+static std::atomic<long long> g_launches{0};
+
+cudaError_t launched(int n) {
+  g_launches.fetch_add(n, std::memory_order_relaxed);
+  return cudaGetLastError();
+}
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -120,6 +128,8 @@ using namespace kvc;
 extern "C" {
 
 int32_t kvc_version(void) { return 10000; }
+
+int64_t kvc_launch_count(void) { return (int64_t)g_launches.load(std::memory_order_relaxed); }
 
 const char* kvc_status_string(kvc_status s) {
   switch (s) {

@@ -132,25 +132,34 @@ __global__ void __launch_bounds__(256) k_channel_partial(const uint16_t* __restr
   }
 }
 
-__global__ void k_channel_final(const uint16_t* __restrict__ q, int H, int KVH, int w, int D,
-                                const float* __restrict__ part, int nsplit, int B, float* __restrict__ cs) {
+// one 1024-thread CTA per (b, kvh): thread (grp, d) sums q^2 over every ngrp-th window row of
+// the group and every ngrp-th key-range partial, then the groups are added in shared memory
+__global__ void __launch_bounds__(1024) k_channel_final(const uint16_t* __restrict__ q, int H, int KVH, int w,
+                                                        int D, const float* __restrict__ part, int nsplit, int B,
+                                                        float* __restrict__ cs) {
+  __shared__ float qred[16][128];
+  __shared__ float kred[16][128];
   const int bk = blockIdx.x;
   const int b = bk / KVH, kvh = bk % KVH;
   const int G = H / KVH;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float kn = 0.f;
-    for (int s = 0; s < nsplit; ++s) kn += part[((int64_t)s * B * KVH + bk) * D + d];
-    float qn = 0.f;
-    for (int h = kvh * G; h < (kvh + 1) * G; ++h) {
-      const uint16_t* qh = q + ((int64_t)(b * H + h) * w) * D + d;
-      float sh = 0.f;
-      for (int i = 0; i < w; ++i) {
-        const float v = __uint_as_float((uint32_t)qh[(int64_t)i * D] << 16);
-        sh = fmaf(v, v, sh);
-      }
-      qn += sh;
+  const int d = threadIdx.x % D, grp = threadIdx.x / D, ngrp = blockDim.x / D;
+  const uint16_t* qg = q + ((int64_t)(b * H + kvh * G) * w) * D + d;  // the group's G*w rows are contiguous
+  float sq = 0.f, kn = 0.f;
+  for (int r = grp; r < G * w; r += ngrp) {
+    const float v = __uint_as_float((uint32_t)__ldg(qg + (int64_t)r * D) << 16);
+    sq = fmaf(v, v, sq);
+  }
+  for (int s = grp; s < nsplit; s += ngrp) kn += __ldg(part + ((int64_t)s * B * KVH + bk) * D + d);
+  qred[grp][d] = sq;
+  kred[grp][d] = kn;
+  __syncthreads();
+  if (grp == 0) {
+    float qs = 0.f, ks = 0.f;
+    for (int g2 = 0; g2 < ngrp; ++g2) {
+      qs += qred[g2][d];
+      ks += kred[g2][d];
     }
-    cs[(int64_t)bk * D + d] = (qn / (float)G) * kn;
+    cs[(int64_t)bk * D + d] = (qs / (float)G) * ks;
   }
 }
 
@@ -275,7 +284,7 @@ cudaError_t launch_compact(const uint16_t* K, const uint16_t* V, const kvc_kv_de
     k_compact<64><<<blocks, 256, 0, st>>>(K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, idx, k, rows, Ko, Vo);
   else
     k_compact<128><<<blocks, 256, 0, st>>>(K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, idx, k, rows, Ko, Vo);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 cudaError_t launch_write_slots(const uint16_t* kn, const uint16_t* vn, const int32_t* slot,
@@ -287,7 +296,7 @@ cudaError_t launch_write_slots(const uint16_t* kn, const uint16_t* vn, const int
     k_write_slots<64><<<blocks, 256, 0, st>>>(kn, vn, slot, K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, rows);
   else
     k_write_slots<128><<<blocks, 256, 0, st>>>(kn, vn, slot, K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, rows);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 size_t channel_score_workspace(const kvc_kv_desc& kv, int k, bool has_idx) {
@@ -307,8 +316,8 @@ cudaError_t launch_channel_score(const uint16_t* q, int w, const uint16_t* K, co
     k_channel_partial<64><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, idx, k, nrows, chunk, part, kv.KVH);
   else
     k_channel_partial<128><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, idx, k, nrows, chunk, part, kv.KVH);
-  k_channel_final<<<kv.B * kv.KVH, 128, 0, st>>>(q, kv.H, kv.KVH, w, kv.D, part, ns, kv.B, cs);
-  return cudaGetLastError();
+  k_channel_final<<<kv.B * kv.KVH, 1024, 0, st>>>(q, kv.H, kv.KVH, w, kv.D, part, ns, kv.B, cs);
+  return launched(2);
 }
 
 cudaError_t launch_channel_prune(const float* cs, const uint16_t* K, const kvc_kv_desc& kv, int C,
@@ -328,7 +337,7 @@ cudaError_t launch_channel_prune(const float* cs, const uint16_t* K, const kvc_k
     else
       k_channel_gather<128><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, kv.KVH, ch, C, Ko);
   }
-  return cudaGetLastError();
+  return launched(2);
 }
 
 KVC_TU_STATUS(gather)

@@ -32,6 +32,8 @@ cudaError_t take_status_scissorhands(unsigned int* v);
 
 // Host-side helpers
 int num_sms();                      // SM count of the current device (cached per device)
+// Count n kernels just enqueued (reported by kvc_launch_count) and return the launch status.
+cudaError_t launched(int n);
 void set_error(const char* fmt, ...);  // records the thread's last error message
 
 // ----------------------------------------------------------------------------------------

@@ -122,7 +122,7 @@ cudaError_t launch_sh_init(const kvc_sh_state& s, int n_live, cudaStream_t st) {
   const int64_t n = std::max<int64_t>((int64_t)s.history * rows * (s.cap / 32), rows * s.cap);
   const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 8));
   k_sh_init<<<blocks, 256, 0, st>>>(s, n_live);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 cudaError_t launch_sh_insert(const kvc_sh_state& s, const uint16_t* kn, const uint16_t* vn,
@@ -133,12 +133,12 @@ cudaError_t launch_sh_insert(const kvc_sh_state& s, const uint16_t* kn, const ui
     k_sh_insert<64><<<blocks, 256, 0, st>>>(s, kn, vn, K, V, kv.stride_b, kv.stride_h, kv.stride_s);
   else
     k_sh_insert<128><<<blocks, 256, 0, st>>>(s, kn, vn, K, V, kv.stride_b, kv.stride_h, kv.stride_s);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 cudaError_t launch_sh_record(const kvc_sh_state& s, const float* p, cudaStream_t st) {
   k_sh_record<<<s.B * s.KVH, 256, 0, st>>>(s, p);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 KVC_TU_STATUS(scissorhands)

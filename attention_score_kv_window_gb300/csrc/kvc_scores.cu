@@ -473,11 +473,14 @@ cudaError_t launch_impl(const ScoresArgs& a, int reduce, float* scores, cudaStre
     k_scores_merge<<<a.B * a.KVH, 256, 0, st>>>(a);
     dim3 g2(a.nsplit, a.KVH, a.B);
     k_scores_pass2<D><<<g2, NTHREADS, smem_pass2(D, a.Rpad), st>>>(a);
+    e = launched(3);
+    if (e != cudaSuccess) return e;
   }
   if (reduce == KVC_REDUCE_ALL_HEADS) {
     const int64_t n = (int64_t)a.B * a.S;
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 8);
     k_scores_allheads<<<blocks, 256, 0, st>>>(a.out, scores, a.B, a.KVH, a.S);
+    return launched(1);
   }
   return cudaGetLastError();
 }

@@ -644,7 +644,7 @@ cudaError_t run_pass1(const ScoresArgs& a, cudaStream_t st, int slot) {
   cudaError_t e = set_smem_once(k_pass1_tc<D, NHALF>, smem, slot);
   if (e != cudaSuccess) return e;
   k_pass1_tc<D, NHALF><<<dim3(a.nsplit, a.KVH, a.B), THREADS, smem, st>>>(a, tmK, tmQ);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 template <int D, int NQ>
@@ -655,7 +655,7 @@ cudaError_t run_pass2(const ScoresArgs& a, cudaStream_t st, int slot) {
   cudaError_t e = set_smem_once(k_pass2_tc<D, NQ>, smem, slot);
   if (e != cudaSuccess) return e;
   k_pass2_tc<D, NQ><<<dim3(a.nsplit, a.KVH, a.B), THREADS, smem, st>>>(a, tmK, tmQ);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 }  // namespace

@@ -434,18 +434,19 @@ cudaError_t launch_topk(const float* scores, int B, int KVH, int64_t S, int k, i
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_topk, scores, S, k, protect_tail, live, largest, idx);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_topk, scores, S, k, protect_tail, live, largest, idx);
+  if (e != cudaSuccess) return e;
+  return launched(1);
 }
 
 cudaError_t launch_sh_evict(const kvc_sh_state& s, int m, int32_t* evicted, cudaStream_t st) {
   const size_t smem = (size_t)s.cap * 4;
   if ((int64_t)s.cap > SLICE_MAX) return cudaErrorInvalidValue;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_sh_evict, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  // static (histograms) + dynamic (keys) shared memory exceed the 48 KB default: opt in
+  cudaError_t e = cudaFuncSetAttribute(k_sh_evict, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(SLICE_MAX * 4));
+  if (e != cudaSuccess) return e;
   k_sh_evict<<<s.B * s.KVH, SEL_THREADS, smem, st>>>(s, m, evicted);
-  return cudaGetLastError();
+  return launched(1);
 }
 
 KVC_TU_STATUS(select)

@@ -178,8 +178,286 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------------------
-# our arm
+# our arm: one case per workload; a step is one pass of that workload's hot path
 # ----------------------------------------------------------------------------------------
+
+
+def _source_sha(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel_key, sources):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    source of the kernel (else None: the counters no longer describe this code)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel_key)
+    if not rec or rec.get("source_sha") != _source_sha(sources):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+CSRC = "attention_score_kv_window_gb300/csrc/"
+SCORE_SOURCES = [CSRC + f for f in ("kvc_scores.cu", "kvc_scores_tc.cu", "kvc_internal.cuh")]
+
+
+class Call:
+    def __init__(self, label, fn, nbytes, flops=0.0, bound="hbm", sources=None, kernel_key=None):
+        self.label, self.fn, self.nbytes, self.flops, self.bound = label, fn, nbytes, flops, bound
+        self.sources, self.kernel_key = sources, kernel_key
+        self.times = []
+
+
+class PrefillCase:
+    """Prefill compression of one layer (TOVA or SnapKV; ThinK adds channel score + prune)."""
+
+    def __init__(self, wl, dev, rank, instances):
+        import torch
+        import attention_score_kv_window_gb300 as kvc
+        self.kvc, self.torch = kvc, torch
+        if instances > 1:
+            wl = wl.with_(B=instances)
+        self.wl = wl
+        inp = prefill_inputs(wl, seed=wl.seed + rank)
+        self.host = inp
+
+        def to_dev(u16):
+            return torch.from_numpy(u16.view(np.int16)).view(torch.bfloat16).to(dev)
+
+        q0, K0, V0 = to_dev(inp["q"]), to_dev(inp["K"]), to_dev(inp["V"])
+        self.in_bytes = (q0.numel() + K0.numel() + V0.numel()) * 2
+        self.R = R = max(2, math.ceil(3 * L2_BYTES / self.in_bytes))
+        self.reps = [(q0, K0, V0)] + [(q0.clone(), K0.clone(), V0.clone()) for _ in range(R - 1)]
+        B, KVH, S, D = K0.shape
+        self.B, self.KVH, self.S, self.D = B, KVH, S, D
+        k = self.k = min(wl.k, S)
+        f32, i32, bf = torch.float32, torch.int32, torch.bfloat16
+        self.outs = [(torch.empty((B, KVH, S), dtype=f32, device=dev), torch.empty((B, KVH, k), dtype=i32, device=dev),
+                      torch.empty((B, KVH, k, D), dtype=bf, device=dev), torch.empty((B, KVH, k, D), dtype=bf, device=dev))
+                     for _ in range(R)]
+        lib = kvc.load_library()
+        self.ws = torch.empty(int(lib.kvc_workspace_size(2, kvc.kv_desc(K0, wl.H), wl.w, k)), dtype=torch.uint8,
+                              device=dev)
+        self.tokens_per_step = B * S
+        G = wl.H // wl.KVH
+        sc_bytes = B * KVH * S * D * 2 + B * wl.H * wl.w * D * 2 + B * KVH * S * 4
+        sc_flops = 2 * 2.0 * B * wl.H * wl.w * S * D  # both passes of q_win K^T
+        big_w = wl.w * G > 32
+        self.calls = [
+            Call("window_scores", self._scores, sc_bytes, sc_flops, "tensor" if big_w else "hbm", SCORE_SOURCES,
+                 f"window_scores/{wl.name}/B{B}"),
+            Call("topk", self._topk, B * KVH * S * 4 + B * KVH * k * 4),
+            Call("compact", self._compact, 4 * B * KVH * k * D * 2 + B * KVH * k * 4),
+        ]
+        if wl.C:
+            C = wl.C
+            self.cs = torch.empty((B, KVH, D), dtype=f32, device=dev)
+            self.ch = torch.empty((B, KVH, C), dtype=i32, device=dev)
+            self.Kp = torch.empty((B, KVH, k, C), dtype=bf, device=dev)
+            self.calls += [Call("channel_score", self._cscore, B * KVH * k * D * 2 + B * wl.H * wl.w * D * 2),
+                           Call("channel_prune", self._cprune, B * KVH * k * D * 2 + B * KVH * k * C * 2)]
+
+    def _scores(self, i):
+        q, K, V = self.reps[i % self.R]
+        self.kvc.kvc_window_scores(q, K, self.wl.scale, causal=True, reduce=self.wl.reduce,
+                                   scores=self.outs[i % self.R][0], ws=self.ws)
+
+    def _topk(self, i):
+        sc, idx, _, _ = self.outs[i % self.R]
+        self.kvc.kvc_topk_select(sc, self.k, protect_tail=self.wl.protect_tail, idx=idx)
+
+    def _compact(self, i):
+        q, K, V = self.reps[i % self.R]
+        _, idx, Ko, Vo = self.outs[i % self.R]
+        self.kvc.kvc_compact_kv(K, V, idx, H=self.wl.H, K_out=Ko, V_out=Vo)
+
+    def _cscore(self, i):
+        q, _, _ = self.reps[i % self.R]
+        self.kvc.kvc_channel_score(q, self.outs[i % self.R][2], cs=self.cs)
+
+    def _cprune(self, i):
+        self.kvc.kvc_channel_prune(self.cs, self.outs[i % self.R][2], self.wl.C, ch_idx=self.ch, K_out=self.Kp,
+                                   H=self.wl.H)
+
+    def config(self):
+        wl = self.wl
+        return {"workload": wl.name, "B": self.B, "H": wl.H, "KVH": self.KVH, "D": self.D, "S": self.S, "w": wl.w,
+                "k": self.k, "C": wl.C or None,
+                "l2": f"inputs rotate over {self.R} replicas ({self.R * self.in_bytes / 2**20:.0f} MiB > L2)"}
+
+    def e2e(self, steps, stream, world, dist, dev):
+        """Same step through kvc_compress_prefill with pinned host inputs and outputs."""
+        torch, kvc, wl = self.torch, self.kvc, self.wl
+        inp = self.host
+        hq = torch.from_numpy(inp["q"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        hK = torch.from_numpy(inp["K"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        hV = torch.from_numpy(inp["V"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        B, KVH, k, D = self.B, self.KVH, self.k, self.D
+        h_idx = torch.empty((B, KVH, k), dtype=torch.int32).pin_memory()
+        h_Ko = torch.empty((B, KVH, k, D), dtype=torch.bfloat16).pin_memory()
+        h_Vo = torch.empty((B, KVH, k, D), dtype=torch.bfloat16).pin_memory()
+        dq, dK, dV = self.reps[0]
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dK.copy_(hK, non_blocking=True)
+            dV.copy_(hV, non_blocking=True)
+            sc, idx, Ko, Vo = self.outs[0]
+            kvc.kvc_compress_prefill(dq, dK, dV, wl.scale, k, protect_tail=wl.protect_tail, reduce=wl.reduce,
+                                     out=(sc, idx, Ko, Vo), ws=self.ws)
+            h_idx.copy_(idx, non_blocking=True)
+            h_Ko.copy_(Ko, non_blocking=True)
+            h_Vo.copy_(Vo, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return {"value": self.tokens_per_step * steps * world / (ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int((hq.numel() + hK.numel() + hV.numel()) * 2),
+                "d2h_bytes_per_step": int(h_idx.numel() * 4 + (h_Ko.numel() + h_Vo.numel()) * 2)}
+
+
+class TovaDecodeCase:
+    """TOVA generation: a cache of budget+1 slots; each step writes the new token into the free
+    slot, scores every slot with the new query (mean over all heads), evicts the minimum."""
+
+    def __init__(self, wl, dev, rank, instances):
+        import torch
+        import attention_score_kv_window_gb300 as kvc
+        self.kvc, self.torch, self.wl = kvc, torch, wl
+        B, H, KVH, D, S0, budget = wl.B, wl.H, wl.KVH, wl.D, wl.S, wl.k
+        n = budget + 1
+        self.cache_bytes = B * KVH * n * D * 2
+        self.R = R = max(2, math.ceil(3 * L2_BYTES / self.cache_bytes))
+        g = torch.Generator(device=dev)
+        g.manual_seed(wl.seed + rank)
+        bf = torch.bfloat16
+        self.caches = []
+        for r in range(R):
+            Kf = torch.randn((B, KVH, S0 + 1, D), generator=g, device=dev).to(bf)
+            Vf = torch.randn((B, KVH, S0 + 1, D), generator=g, device=dev).to(bf)
+            q0 = torch.randn((B, H, 1, D), generator=g, device=dev).to(bf)
+            sc = kvc.kvc_window_scores(q0, Kf, wl.scale, causal=False, reduce="all_heads")
+            idx = kvc.kvc_topk_select(sc, budget)
+            Kk, Vk = kvc.kvc_compact_kv(Kf, Vf, idx, H=H)
+            Kc = torch.zeros((B, KVH, n, D), dtype=bf, device=dev)
+            Vc = torch.zeros_like(Kc)
+            Kc[:, :, :budget] = Kk
+            Vc[:, :, :budget] = Vk
+            del Kk, Vk
+            free = torch.full((B, KVH), budget, dtype=torch.int32, device=dev)
+            self.caches.append((Kc, Vc, free, torch.empty((B, KVH, n), dtype=torch.float32, device=dev)))
+            del Kf, Vf
+        self.nq = 64
+        self.q = torch.randn((self.nq, B, H, D), generator=g, device=dev).to(bf)
+        self.kn = torch.randn((self.nq, B, KVH, D), generator=g, device=dev).to(bf)
+        self.vn = torch.randn((self.nq, B, KVH, D), generator=g, device=dev).to(bf)
+        Kc0 = self.caches[0][0]
+        self.ws = torch.empty(int(kvc.load_library().kvc_workspace_size(3, kvc.kv_desc(Kc0, H), 1, 0)),
+                              dtype=torch.uint8, device=dev)
+        self.B, self.KVH, self.S, self.D = B, KVH, n, D
+        self.tokens_per_step = B * n
+        nbytes = B * KVH * n * D * 2 + 2 * B * KVH * D * 2 + 2 * B * KVH * n * 4 + B * H * D * 2
+        self.calls = [Call("tova_decode_step", self._step, nbytes, 2.0 * B * H * n * D, "hbm", SCORE_SOURCES,
+                           f"tova_decode/{wl.name}")]
+
+    def _step(self, i):
+        Kc, Vc, free, sc = self.caches[i % self.R]
+        j = i % self.nq
+        self.kvc.kvc_tova_decode_step(self.q[j], self.kn[j], self.vn[j], Kc, Vc, self.wl.scale, free, scores=sc,
+                                      ws=self.ws)
+
+    def config(self):
+        wl = self.wl
+        return {"workload": wl.name, "B": wl.B, "H": wl.H, "KVH": wl.KVH, "D": wl.D, "slots": self.S,
+                "l2": f"steps rotate over {self.R} caches ({self.R * self.cache_bytes / 2**20:.0f} MiB > L2)"}
+
+    def e2e(self, *a):
+        return None
+
+
+class ScissorhandsCase:
+    """Scissorhands decode: insert, score the new query over the live slots, record the low-
+    attention flags into the 400-step history; evict m slots per head when the cache is full."""
+
+    def __init__(self, wl, dev, rank, instances):
+        import torch
+        import attention_score_kv_window_gb300 as kvc
+        self.kvc, self.torch, self.wl = kvc, torch, wl
+        B, H, KVH, D, cap = wl.B, wl.H, wl.KVH, wl.D, wl.S
+        self.cache_bytes = B * KVH * cap * D * 2
+        self.R = R = max(2, math.ceil(3 * L2_BYTES / self.cache_bytes))
+        g = torch.Generator(device=dev)
+        g.manual_seed(wl.seed + rank)
+        bf = torch.bfloat16
+        self.reps = []
+        for r in range(R):
+            K = torch.randn((B, KVH, cap, D), generator=g, device=dev).to(bf)
+            V = torch.randn((B, KVH, cap, D), generator=g, device=dev).to(bf)
+            st = kvc.ScissorhandsState(B, KVH, cap, history=wl.history, device=dev)
+            kvc.kvc_scissorhands_init(st, wl.prefill_live)
+            self.reps.append((K, V, st, torch.empty((B, KVH, cap), dtype=torch.float32, device=dev),
+                              torch.empty((B, KVH, wl.m), dtype=torch.int32, device=dev)))
+        self.nq = 64
+        self.q = torch.randn((self.nq, B, H, D), generator=g, device=dev).to(bf)
+        self.kn = torch.randn((self.nq, B, KVH, D), generator=g, device=dev).to(bf)
+        self.vn = torch.randn((self.nq, B, KVH, D), generator=g, device=dev).to(bf)
+        self.ws = torch.empty(int(kvc.load_library().kvc_workspace_size(4, kvc.kv_desc(self.reps[0][0], H), 1, 0)),
+                              dtype=torch.uint8, device=dev)
+        self.B, self.KVH, self.S, self.D = B, KVH, cap, D
+        self.tokens_per_step = B * cap
+        upd = (B * KVH * cap * D * 2 + 2 * B * KVH * D * 2 + 2 * B * KVH * cap * 4 + B * KVH * cap * 4
+               + 2 * B * KVH * cap * 2 + 2 * B * KVH * cap // 8 + B * H * D * 2)
+        self.calls = [Call("scissorhands_update", self._update, upd, 2.0 * B * H * cap * D, "hbm", SCORE_SOURCES,
+                           f"scissorhands/{wl.name}"),
+                      Call("scissorhands_evict", self._evict, B * KVH * cap * (2 + 4 + 0.125) + B * KVH * wl.m * 4)]
+        self.evict_steps = 0
+
+    def _update(self, i):
+        K, V, st, probs, ev = self.reps[i % self.R]
+        j = i % self.nq
+        self.kvc.kvc_scissorhands_update(st, self.q[j], self.kn[j], self.vn[j], K, V, self.wl.scale, probs=probs,
+                                         ws=self.ws)
+
+    def _evict(self, i):
+        K, V, st, probs, ev = self.reps[i % self.R]
+        if st.n_free == 0:
+            self.kvc.kvc_scissorhands_evict(st, self.wl.m, evicted=ev)
+
+    def config(self):
+        wl = self.wl
+        return {"workload": wl.name, "B": wl.B, "H": wl.H, "KVH": wl.KVH, "D": wl.D, "cap": wl.S,
+                "history": wl.history, "m": wl.m,
+                "l2": f"steps rotate over {self.R} caches ({self.R * self.cache_bytes / 2**20:.0f} MiB > L2)"}
+
+    def e2e(self, *a):
+        return None
+
+
+def make_case(wl, dev, rank, instances):
+    if wl.name.startswith("tova_decode"):
+        return TovaDecodeCase(wl, dev, rank, instances)
+    if wl.name.startswith("scissorhands"):
+        return ScissorhandsCase(wl, dev, rank, instances)
+    return PrefillCase(wl, dev, rank, instances)
 
 
 def run_ours(args):
@@ -199,42 +477,17 @@ def run_ours(args):
     kvc.load_library()
     wl = WORKLOADS[args.config]
     peaks = _peaks()
-
-    inp = prefill_inputs(wl, seed=wl.seed + rank)
-
-    def to_dev(u16):
-        return torch.from_numpy(u16.view(np.int16)).view(torch.bfloat16).to(dev)
-
-    q0, K0, V0 = to_dev(inp["q"]), to_dev(inp["K"]), to_dev(inp["V"])
-    in_bytes = (q0.numel() + K0.numel() + V0.numel()) * 2
-    R = max(2, math.ceil(3 * L2_BYTES / in_bytes))
-    reps = [(q0, K0, V0)] + [(q0.clone(), K0.clone(), V0.clone()) for _ in range(R - 1)]
-    B, KVH, S, D = K0.shape
-    k = min(wl.k, S)
-    outs = [(torch.empty((B, KVH, S), dtype=torch.float32, device=dev),
-             torch.empty((B, KVH, k), dtype=torch.int32, device=dev),
-             torch.empty((B, KVH, k, D), dtype=torch.bfloat16, device=dev),
-             torch.empty((B, KVH, k, D), dtype=torch.bfloat16, device=dev)) for _ in range(R)]
-    ws_bytes = kvc.load_library().kvc_workspace_size(2, kvc.kv_desc(K0, wl.H), wl.w, k)
-    ws = torch.empty(int(ws_bytes), dtype=torch.uint8, device=dev)
+    case = make_case(wl, dev, rank, args.instances)
     stream = torch.cuda.current_stream()
+    calls = case.calls
 
     def step(i, ev=None):
-        q, K, V = reps[i % R]
-        sc, idx, Ko, Vo = outs[i % R]
+        for c, call in enumerate(calls):
+            if ev is not None:
+                ev[c].record(stream)
+            call.fn(i)
         if ev is not None:
-            ev[0].record(stream)
-        kvc.kvc_window_scores(q, K, wl.scale, causal=True, reduce=wl.reduce, scores=sc, ws=ws)
-        if ev is not None:
-            ev[1].record(stream)
-        kvc.kvc_topk_select(sc, k, protect_tail=wl.protect_tail, idx=idx)
-        if ev is not None:
-            ev[2].record(stream)
-        kvc.kvc_compact_kv(K, V, idx, H=wl.H, K_out=Ko, V_out=Vo)
-        if ev is not None:
-            ev[3].record(stream)
-
-    launches_per_step = 3 + (1 if wl.reduce == "all_heads" else 0) + 1 + 1
+            ev[len(calls)].record(stream)
 
     for i in range(args.warmup):
         step(i)
@@ -242,26 +495,28 @@ def run_ours(args):
     assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
     sampler = ClockSampler(local) if not args.no_clocks else None
+    base = args.warmup
     if sampler:
         sampler.start()
         # keep the GPU busy for a moment so the sampler sees the loaded clock
         t_end = time.time() + 0.5
-        i = 0
         while time.time() < t_end:
-            step(i)
-            i += 1
+            step(base)
+            base += 1
         torch.cuda.synchronize()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    launches0 = kvc.kvc_launch_count()
     start.record(stream)
     for i in range(args.steps):
-        step(i, evs[i])
+        step(base + i, evs[i])
     stop.record(stream)
     torch.cuda.synchronize()
+    launches = kvc.kvc_launch_count() - launches0
     if world > 1:
         dist.barrier()
     ms = start.elapsed_time(stop)
@@ -272,75 +527,36 @@ def run_ours(args):
         ms = float(t.item())
     assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
-    t_scores = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
-    t_topk = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
-    t_compact = float(np.mean([e[2].elapsed_time(e[3]) for e in evs]))
+    kernels = {}
+    for c, call in enumerate(calls):
+        ts = [e[c].elapsed_time(e[c + 1]) for e in evs]
+        t = float(np.mean(ts))
+        kernels[call.label] = {"ms": t, "alg_bytes": call.nbytes, "gbs": call.nbytes / (t / 1e3) / 1e9}
+        if call.flops:
+            kernels[call.label]["tflops"] = call.flops / (t / 1e3) / 1e12
+    dom = max(calls, key=lambda c: kernels[c.label]["ms"])
+    t_dom = kernels[dom.label]["ms"]
+    if dom.bound == "tensor":
+        achieved = dom.flops / (t_dom / 1e3) / 1e12
+        roof = {"kernel": f"kvc_{dom.label}", "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                "peak_source": f"{peaks['source']} bf16 burst (of measured)" if peaks["source"] == "measured"
+                else "fallback bf16"}
+    else:
+        achieved = dom.nbytes / (t_dom / 1e3) / 1e9
+        roof = {"kernel": f"kvc_{dom.label}", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "peak_source": f"{peaks['source']} HBM copy"}
+    roof["traffic"] = _traffic(dom.kernel_key, dom.sources) if dom.kernel_key else None
+    roof["algorithmic_bytes_per_launch"] = dom.nbytes
+    roof["algorithmic_flops_per_launch"] = dom.flops
 
-    tokens_per_step = B * S
-    value = tokens_per_step * args.steps * world / (ms / 1e3)
-
-    # roofline of the dominant call: window scores (two passes over K on the tensor cores)
-    G = wl.H // wl.KVH
-    flops = 2 * 2.0 * B * wl.H * wl.w * S * D  # two passes of q_win K^T (the pass structure the method fixes)
-    achieved_tflops = flops / (t_scores / 1e3) / 1e12
-    roof = {"kernel": "kvc_window_scores (pass 1 + merge + pass 2)", "bound": "tensor",
-            "achieved": achieved_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": achieved_tflops / peaks["bf16_tflops"], "traffic": None,
-            "peak_source": f"{peaks['source']} bf16 burst",
-            "algorithmic_flops_per_launch": flops,
-            "algorithmic_bytes_per_launch": B * KVH * S * D * 2 + B * wl.H * wl.w * D * 2 + B * KVH * S * 4}
-    sc_bytes = roof["algorithmic_bytes_per_launch"]
-    compact_bytes = 4 * B * KVH * k * D * 2 + B * KVH * k * 4
-    kernels = {
-        "window_scores_ms": t_scores,
-        "window_scores_hbm_gbs": sc_bytes / (t_scores / 1e3) / 1e9,
-        "topk_ms": t_topk,
-        "compact_ms": t_compact,
-        "compact_hbm_gbs": compact_bytes / (t_compact / 1e3) / 1e9,
-    }
-
-    # end to end through the public API with host buffers (pinned), copies inside the timed region
-    hq = torch.from_numpy(inp["q"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    hK = torch.from_numpy(inp["K"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    hV = torch.from_numpy(inp["V"].view(np.int16)).view(torch.bfloat16).pin_memory()
-    h_idx = torch.empty((B, KVH, k), dtype=torch.int32).pin_memory()
-    h_Ko = torch.empty((B, KVH, k, D), dtype=torch.bfloat16).pin_memory()
-    h_Vo = torch.empty((B, KVH, k, D), dtype=torch.bfloat16).pin_memory()
-    dq, dK, dV = reps[0]
-    e2e_steps = max(3, min(args.steps, 20))
-
-    def e2e_step(i):
-        dq.copy_(hq, non_blocking=True)
-        dK.copy_(hK, non_blocking=True)
-        dV.copy_(hV, non_blocking=True)
-        sc, idx, Ko, Vo = outs[0]
-        kvc.kvc_compress_prefill(dq, dK, dV, wl.scale, k, protect_tail=wl.protect_tail, reduce=wl.reduce,
-                                 out=(sc, idx, Ko, Vo), ws=ws)
-        h_idx.copy_(idx, non_blocking=True)
-        h_Ko.copy_(Ko, non_blocking=True)
-        h_Vo.copy_(Vo, non_blocking=True)
-
-    e2e_step(0)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": tokens_per_step * e2e_steps * world / (e2e_ms / 1e3), "unit": "tokens/s",
-           "h2d_bytes_per_step": int((hq.numel() + hK.numel() + hV.numel()) * 2),
-           "d2h_bytes_per_step": int(h_idx.numel() * 4 + (h_Ko.numel() + h_Vo.numel()) * 2)}
+    value = case.tokens_per_step * args.steps * world / (ms / 1e3)
+    e2e = case.e2e(max(3, min(args.steps, 20)), stream, world, dist, dev) if not args.no_e2e else None
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and isinstance(case, PrefillCase) \
+            and args.instances <= 1:
         cpu = cpu_baseline(args.config, budget_s=args.cpu_seconds)
 
     if rank == 0:
@@ -348,11 +564,8 @@ def run_ours(args):
             "metric": "kv_tokens_scored_compacted_per_s_per_layer", "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": wl.name, "B": B, "H": wl.H, "KVH": KVH, "D": D, "S": S, "w": wl.w, "k": k,
-                       "l2": f"inputs rotate over {R} replicas ({R * in_bytes / 2**20:.0f} MiB > L2)"},
-            "roofline": roof, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+            "data": "synthetic", "config": case.config(), "roofline": roof, "kernels": kernels,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -365,8 +578,10 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default=SNAPKV_32K.name,
-                    choices=[n for n, w in sorted(WORKLOADS.items()) if w.steps == 0])
+    ap.add_argument("--config", default=SNAPKV_32K.name, choices=sorted(WORKLOADS))
+    ap.add_argument("--instances", type=int, default=1,
+                    help="independent prefill instances batched into one step (e.g. 8192 for TOVA prefill)")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -281,6 +281,10 @@ const char* kvc_last_error_message(void);
 /* Library version: major*10000 + minor*100 + patch. */
 int32_t kvc_version(void);
 
+/* Diagnostics: number of kernels this library has enqueued since it was loaded (all host
+ * threads, all devices).  The difference over a region counts the region's launches. */
+int64_t kvc_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -379,5 +379,9 @@ def test_invalid_arguments_raise_and_enqueue_nothing():
         kvc.kvc_topk_select(torch.zeros((1, 2, 64), device="cuda"), 4, protect_tail=8)
     assert e.value.status == kvc.KVC_ERR_INVALID_ARG
     with pytest.raises(kvc.KvcError):
-        kvc.kvc_compact_kv(K, K, dev_i32(np.zeros((1, 2, 4))), K_out=K[:, :, :4].contiguous(), V_out=K[:, :, :4])
+        # V_out is a dense view into V's own storage: the library refuses the overlap
+        kvc.kvc_compact_kv(K, K, dev_i32(np.zeros((1, 2, 4))), K_out=K[:, :, :4].contiguous(),
+                           V_out=K.view(-1)[:512].view(1, 2, 4, 64))
+    with pytest.raises(ValueError):
+        kvc.kvc_compact_kv(K, K, dev_i32(np.zeros((1, 2, 4))), K_out=K[:, :, :4])  # not dense
     assert kvc.kvc_get_device_status() == kvc.KVC_OK
