@@ -421,6 +421,183 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass2(const ScoresArgs a) {
   cp_async_wait<0>();
 }
 
+// ----------------------------------------------------------------------------------------
+// single-pass kernel for few query rows (R = G*w <= 16: decode steps, TOVA): K is read once.
+// A cluster of CS CTAs splits one (b, kvh)'s keys; each CTA keeps the logits of its slice in
+// shared memory (log2 domain, masked ones -inf), computes per-row (max, sum), pushes them to
+// every peer, and after one cluster barrier merges them and writes its slice's scores.
+// ----------------------------------------------------------------------------------------
+constexpr int SMALL_STAGES = 4;
+constexpr int SMALL_LOGIT_BYTES = 32 * 1024;  // per CTA; keeps two CTAs per SM
+
+size_t smem_small(int D, int R, int64_t per) {
+  return (size_t)(16 + SMALL_STAGES * TK) * (D + 8) * 2 + (size_t)R * per * 4 + 16 * 8 * sizeof(float2) +
+         8 * 16 * sizeof(float2) + 16 * sizeof(float) + 64;
+}
+
+__device__ __forceinline__ uint32_t cluster_addr_s(const void* local, int rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n"
+               : "=r"(ra)
+               : "r"((uint32_t)__cvta_generic_to_shared(local)), "r"(rank));
+  return ra;
+}
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 2) k_scores_small(const ScoresArgs a, int64_t per) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int P = D + 8, KS = D / 16;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  unsigned int cs, cr;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(cs));
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(cr));
+  const int bk = blockIdx.x / cs;
+  const int b = bk / a.KVH, kvh = bk % a.KVH;
+  const int R = a.R;
+  const int64_t kbeg = (int64_t)cr * per;
+  const int64_t kend = min(a.S, kbeg + per);
+  const int ntiles = kend > kbeg ? (int)((kend - kbeg + TK - 1) / TK) : 0;
+
+  uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);
+  uint16_t* Ks = Qs + 16 * P;
+  float* lg = reinterpret_cast<float*>(Ks + SMALL_STAGES * TK * P);          // [R][per]
+  float2* xch = reinterpret_cast<float2*>(lg + (int64_t)R * per);            // [8 ranks][16 rows], pushed by peers
+  float2* red = xch + 8 * 16;                                                // [8 warps][16 rows]
+  float* crow = reinterpret_cast<float*>(red + 8 * 16);                      // [16]
+
+  const uint16_t* Kb = a.K + b * a.sb + kvh * a.sh;
+  const uint16_t* Qg = a.q + ((int64_t)(b * a.H + kvh * a.G) * a.w) * D;
+  const uint32_t* lw = a.live ? a.live + (int64_t)bk * a.live_words : nullptr;
+
+  load_q_rows<D>(Qs, Qg, 0, 16, R, tid);
+  cp_async_commit();
+#pragma unroll
+  for (int s = 0; s < SMALL_STAGES - 1; ++s) {
+    if (s < ntiles) load_k_tile<D>(Ks + s * TK * P, Kb, a.ss, kbeg + (int64_t)s * TK, kend, tid);
+    cp_async_commit();
+  }
+  // row limits of the two rows this lane's accumulator fragment holds
+  const int64_t limA = (g < R) ? (a.causal ? a.S - a.w + (g % a.w) : a.S - 1) : -1;
+  const int64_t limB = (g + 8 < R) ? (a.causal ? a.S - a.w + ((g + 8) % a.w) : a.S - 1) : -1;
+
+  uint32_t aq[KS][4];
+  for (int it = 0; it < ntiles; ++it) {
+    cp_async_wait<SMALL_STAGES - 2>();
+    __syncthreads();
+    if (it == 0) {
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int c = ks * 16 + ((lane >> 4) & 1) * 8;
+        ldsm_x4(smem_u32(Qs + r * P + c), aq[ks][0], aq[ks][1], aq[ks][2], aq[ks][3]);
+      }
+    }
+    {
+      const int nx = it + SMALL_STAGES - 1;
+      if (nx < ntiles)
+        load_k_tile<D>(Ks + (nx % SMALL_STAGES) * TK * P, Kb, a.ss, kbeg + (int64_t)nx * TK, kend, tid);
+      cp_async_commit();
+    }
+    const uint16_t* Kt = Ks + (it % SMALL_STAGES) * TK * P;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks2 = 0; ks2 < KS / 2; ++ks2) {
+      uint32_t b0, b1, b2, b3;
+      const int r = warp * 8 + (lane & 7);
+      const int cc = ks2 * 32 + (lane >> 3) * 8;
+      ldsm_x4(smem_u32(Kt + r * P + cc), b0, b1, b2, b3);
+      mma16816(c, aq[2 * ks2], b0, b1);
+      mma16816(c, aq[2 * ks2 + 1], b2, b3);
+    }
+    const int64_t j0 = kbeg + (int64_t)it * TK + warp * 8 + 2 * t;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int64_t j = j0 + e;
+      const bool in = j < kend;
+      const bool lv = in && (lw == nullptr || live_bit(lw, j));
+      if (g < R && in) lg[(int64_t)g * per + (j - kbeg)] = (lv && j <= limA) ? c[e] * a.sl2 : -CUDART_INF_F;
+      if (g + 8 < R && in) lg[(int64_t)(g + 8) * per + (j - kbeg)] = (lv && j <= limB) ? c[2 + e] * a.sl2 : -CUDART_INF_F;
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // per-row max, then sum of exp2(logit - max), over this CTA's slice
+  const int64_t len = kend > kbeg ? kend - kbeg : 0;
+  float mx[16], sm[16];
+#pragma unroll
+  for (int r = 0; r < 16; ++r) mx[r] = -CUDART_INF_F;
+  for (int64_t j = tid; j < len; j += NTHREADS)
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+      if (r < R) mx[r] = fmaxf(mx[r], lg[(int64_t)r * per + j]);
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    if (r < R) {
+#pragma unroll
+      for (int o = 16; o; o >>= 1) mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], o));
+      if (lane == 0) red[warp * 16 + r].x = mx[r];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    if (r < R) {
+      float m = -CUDART_INF_F;
+      for (int q = 0; q < NTHREADS / 32; ++q) m = fmaxf(m, red[q * 16 + r].x);
+      mx[r] = m;
+      sm[r] = 0.f;
+    }
+  }
+  for (int64_t j = tid; j < len; j += NTHREADS)
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+      if (r < R && mx[r] != -CUDART_INF_F) sm[r] += ex2(lg[(int64_t)r * per + j] - mx[r]);
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    if (r < R) {
+#pragma unroll
+      for (int o = 16; o; o >>= 1) sm[r] += __shfl_xor_sync(0xffffffffu, sm[r], o);
+      if (lane == 0) red[warp * 16 + r].y = sm[r];
+    }
+  }
+  __syncthreads();
+  // this CTA's (m, l) per row, pushed into slot [cr] of every CTA of the cluster
+  if (tid < R) {
+    float l = 0.f;
+    for (int q = 0; q < NTHREADS / 32; ++q) l += red[q * 16 + tid].y;
+    float mm = -CUDART_INF_F;
+    for (int q = 0; q < NTHREADS / 32; ++q) mm = fmaxf(mm, red[q * 16 + tid].x);
+    for (unsigned int p = 0; p < cs; ++p) {
+      const uint32_t ra = cluster_addr_s(&xch[cr * 16 + tid], (int)p);
+      asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(ra), "f"(mm), "f"(l) : "memory");
+    }
+  }
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+  if (tid < R) {
+    float M = -CUDART_INF_F, L = 0.f;
+    for (unsigned int p = 0; p < cs; ++p) {
+      const float2 o = xch[p * 16 + tid];
+      if (o.y > 0.f) M = fmaxf(M, o.x);
+    }
+    for (unsigned int p = 0; p < cs; ++p) {
+      const float2 o = xch[p * 16 + tid];
+      if (o.y > 0.f) L += o.y * ex2(o.x - M);
+    }
+    crow[tid] = L > 0.f ? M + log2f(L) : CUDART_INF_F;
+  }
+  __syncthreads();
+  float* out = a.out + (int64_t)bk * a.S;
+  for (int64_t j = tid; j < len; j += NTHREADS) {
+    float s = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+      if (r < R) s += ex2(lg[(int64_t)r * per + j] - crow[r]);
+    out[kbeg + j] = s * a.out_mul;
+  }
+  // no remote access follows the cluster barrier: CTAs may leave independently
+}
+
 // all-heads reduction: mean over KV heads of the per-group scores, written to every kvh
 __global__ void k_scores_allheads(const float* __restrict__ grp, float* __restrict__ out, int B,
                                   int KVH, int64_t S) {
@@ -452,15 +629,58 @@ cudaError_t set_smem_attrs() {
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k_scores_pass2<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem_pass2(D, MAX_RPAD));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_scores_small<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_small(D, 16, SMALL_LOGIT_BYTES / (16 * 4)) + 1024);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
   return e;
+}
+
+// Cluster size and keys per CTA for the single-pass small-row kernel; 0 when the logits of
+// one (b, kvh) do not fit the shared memory of an 8-CTA cluster.
+int small_cluster(const ScoresArgs& a, int64_t* per_out) {
+  if (a.R > 16) return 0;
+  const int64_t units = (int64_t)a.B * a.KVH;
+  auto per_for = [&](int cs) { return ((a.S + cs - 1) / cs + TK - 1) / TK * TK; };
+  int cs = 1;
+  while (cs <= 8 && (int64_t)a.R * per_for(cs) * 4 > SMALL_LOGIT_BYTES) ++cs;
+  if (cs > 8) return 0;
+  // more CTAs while the GPU is not yet two CTAs per SM deep and slices stay >= 256 keys
+  while (cs < 8 && units * cs < 2 * (int64_t)num_sms() && per_for(cs + 1) >= 256) ++cs;
+  if (units * cs > 2147483647LL) return 0;
+  *per_out = per_for(cs);
+  return cs;
+}
+
+template <int D>
+cudaError_t launch_small(const ScoresArgs& a, int cs, int64_t per, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((int64_t)a.B * a.KVH * cs), 1, 1);
+  cfg.blockDim = dim3(NTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem_small(D, a.R, per);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cs;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_scores_small<D>, a, per);
+  if (e != cudaSuccess) return e;
+  return launched(1);
 }
 
 template <int D>
 cudaError_t launch_impl(const ScoresArgs& a, int reduce, float* scores, cudaStream_t st) {
   cudaError_t e = set_smem_attrs<D>();
   if (e != cudaSuccess) return e;
-  if (tc_supported(a, D)) {
+  int64_t per = 0;
+  const int cs = small_cluster(a, &per);
+  if (cs > 0) {
+    e = launch_small<D>(a, cs, per, st);
+    if (e != cudaSuccess) return e;
+  } else if (tc_supported(a, D)) {
     e = launch_pass1_tc(a, D, st);  // pass 2 merges the key-range partials itself
     if (e != cudaSuccess) return e;
     e = launch_pass2_tc(a, D, st);

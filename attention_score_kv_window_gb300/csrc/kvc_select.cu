@@ -397,6 +397,153 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sh_evict(kvc_sh_state s, int m,
   }
 }
 
+// ----------------------------------------------------------------------------------------
+// Short rows (S <= 4096, many of them: batched prefill instances, decode steps): one
+// 256-thread CTA per row.  Each eligible item becomes the 64-bit composite (key, tie) with
+// tie = ~index when keeping (lower index first) and index when evicting (higher index
+// first), so composites are distinct and their descending order is the ranking.  k == 1 is
+// a block max; otherwise a bitonic sort (descending) in shared memory gives the need-th
+// composite, and every eligible item at or above it is taken, written in index order.
+// ----------------------------------------------------------------------------------------
+constexpr int SHORT_THREADS = 256;
+constexpr int SHORT_MAX = 4096;
+
+__device__ __forceinline__ uint64_t u64max(uint64_t a, uint64_t b) { return a > b ? a : b; }
+
+__global__ void __launch_bounds__(SHORT_THREADS) k_topk_short(const float* __restrict__ scores, int S, int k,
+                                                              int protect, const uint32_t* __restrict__ live,
+                                                              int largest, int32_t* __restrict__ idx) {
+  __shared__ uint64_t ck[SHORT_MAX];
+  __shared__ uint32_t wsum[SHORT_THREADS / 32];
+  __shared__ uint64_t wmax[SHORT_THREADS / 32];
+  __shared__ uint32_t s_nforced, s_nelig;
+  const int64_t row = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  ScoreKeys fn;
+  fn.row = scores + row * (int64_t)S;
+  fn.lw = live ? live + row * (((int64_t)S + 31) / 32) : nullptr;
+  fn.S = S;
+  fn.protect = protect;
+  fn.largest = largest;
+  int32_t* out = idx + row * (int64_t)k;
+  int n2 = 1;
+  while (n2 < S) n2 <<= 1;
+
+  // composites; ineligible and padding items are 0 (below every real composite)
+  uint32_t cf = 0, ce = 0;
+  uint64_t best = 0;
+  for (int j = tid; j < n2; j += SHORT_THREADS) {
+    uint64_t c = 0;
+    if (j < S) {
+      if (fn.forced(j)) ++cf;
+      else if (fn.eligible(j)) {
+        ++ce;
+        c = ((uint64_t)fn.key(j) << 32) | (uint32_t)(largest ? ~(uint32_t)j : (uint32_t)j);
+      }
+    }
+    ck[j] = c;
+    best = u64max(best, c);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    cf += __shfl_xor_sync(0xffffffffu, cf, o);
+    ce += __shfl_xor_sync(0xffffffffu, ce, o);
+    best = u64max(best, __shfl_xor_sync(0xffffffffu, best, o));
+  }
+  if (lane == 0) {
+    wsum[warp] = cf | (ce << 16);  // S <= 4096: both counts fit 16 bits
+    wmax[warp] = best;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t f = 0, e = 0;
+    uint64_t bb = 0;
+    for (int q = 0; q < SHORT_THREADS / 32; ++q) {
+      f += wsum[q] & 0xffffu;
+      e += wsum[q] >> 16;
+      bb = u64max(bb, wmax[q]);
+    }
+    s_nforced = f;
+    s_nelig = e;
+    wmax[0] = bb;
+  }
+  __syncthreads();
+  const int64_t need = (int64_t)k - (int64_t)s_nforced > 0 ? (int64_t)k - (int64_t)s_nforced : 0;
+  const bool take_all = (int64_t)s_nelig <= need;
+  uint64_t thr = 0;  // take eligible items with composite >= thr (0: take all eligible)
+  if (!take_all && need > 0) {
+    if (need == 1) {
+      thr = wmax[0];
+    } else {
+      __syncthreads();
+      for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          for (int i = tid; i < (n2 >> 1); i += SHORT_THREADS) {
+            const int lo = 2 * i - (i & (stride - 1));
+            const int hi = lo + stride;
+            const bool desc = (lo & size) == 0;  // overall descending order
+            const uint64_t x = ck[lo], y = ck[hi];
+            if ((x < y) == desc) {
+              ck[lo] = y;
+              ck[hi] = x;
+            }
+          }
+          __syncthreads();
+        }
+      }
+      thr = ck[need - 1];
+    }
+  }
+  // output in index order: thread t owns a contiguous run of items
+  const int per = (S + SHORT_THREADS - 1) / SHORT_THREADS;
+  const int j0 = tid * per;
+  uint32_t cnt = 0;
+  for (int j = j0; j < j0 + per && j < S; ++j) {
+    bool take = false;
+    if (fn.forced(j)) take = true;
+    else if (fn.eligible(j)) {
+      if (take_all) take = true;
+      else if (need > 0) {
+        const uint64_t c = ((uint64_t)fn.key(j) << 32) | (uint32_t)(largest ? ~(uint32_t)j : (uint32_t)j);
+        take = c >= thr;
+      }
+    }
+    cnt += take;
+  }
+  // exclusive scan of the per-thread counts
+  uint32_t x = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  uint32_t base = 0, total = 0;
+  for (int q = 0; q < SHORT_THREADS / 32; ++q) {
+    if (q < warp) base += wsum[q];
+    total += wsum[q];
+  }
+  uint32_t pos = base + x - cnt;
+  for (int j = j0; j < j0 + per && j < S; ++j) {
+    bool take = false;
+    if (fn.forced(j)) take = true;
+    else if (fn.eligible(j)) {
+      if (take_all) take = true;
+      else if (need > 0) {
+        const uint64_t c = ((uint64_t)fn.key(j) << 32) | (uint32_t)(largest ? ~(uint32_t)j : (uint32_t)j);
+        take = c >= thr;
+      }
+    }
+    if (take) {
+      if (pos < (uint32_t)k) out[pos] = j;
+      ++pos;
+    }
+  }
+  for (int p = (int)total + tid; p < k; p += SHORT_THREADS) out[p] = -1;
+}
+
 // CTAs per row: a power of two (the histogram exchange splits 1024 or 2048 bins evenly)
 int topk_cluster_size(int64_t S) {
   int cs = 1;
@@ -410,6 +557,11 @@ int64_t topk_max_len() { return SLICE_MAX * MAX_CLUSTER; }
 
 cudaError_t launch_topk(const float* scores, int B, int KVH, int64_t S, int k, int protect_tail,
                         const uint32_t* live, int largest, int32_t* idx, cudaStream_t st) {
+  if (S <= SHORT_MAX) {
+    k_topk_short<<<(unsigned)((int64_t)B * KVH), SHORT_THREADS, 0, st>>>(scores, (int)S, k, protect_tail, live,
+                                                                         largest, idx);
+    return launched(1);
+  }
   const int cs = topk_cluster_size(S);
   const int64_t per_cta = ((S + (int64_t)cs * 32 - 1) / ((int64_t)cs * 32)) * 32;
   if (per_cta > SLICE_MAX) return cudaErrorInvalidValue;
