@@ -427,8 +427,8 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass2(const ScoresArgs a) {
 // shared memory (log2 domain, masked ones -inf), computes per-row (max, sum), pushes them to
 // every peer, and after one cluster barrier merges them and writes its slice's scores.
 // ----------------------------------------------------------------------------------------
-constexpr int SMALL_STAGES = 4;
-constexpr int SMALL_LOGIT_BYTES = 32 * 1024;  // per CTA; keeps two CTAs per SM
+constexpr int SMALL_STAGES = 3;
+constexpr int SMALL_LOGIT_BYTES = 16 * 1024;  // per CTA; keeps three CTAs per SM
 
 size_t smem_small(int D, int R, int64_t per) {
   return (size_t)(16 + SMALL_STAGES * TK) * (D + 8) * 2 + (size_t)R * per * 4 + 16 * 8 * sizeof(float2) +
@@ -444,7 +444,7 @@ __device__ __forceinline__ uint32_t cluster_addr_s(const void* local, int rank) 
 }
 
 template <int D>
-__global__ void __launch_bounds__(NTHREADS, 2) k_scores_small(const ScoresArgs a, int64_t per) {
+__global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a, int64_t per) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int P = D + 8, KS = D / 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -646,7 +646,7 @@ int small_cluster(const ScoresArgs& a, int64_t* per_out) {
   while (cs <= 8 && (int64_t)a.R * per_for(cs) * 4 > SMALL_LOGIT_BYTES) ++cs;
   if (cs > 8) return 0;
   // more CTAs while the GPU is not yet two CTAs per SM deep and slices stay >= 256 keys
-  while (cs < 8 && units * cs < 2 * (int64_t)num_sms() && per_for(cs + 1) >= 256) ++cs;
+  while (cs < 8 && units * cs < 3 * (int64_t)num_sms() && per_for(cs + 1) >= 256) ++cs;
   if (units * cs > 2147483647LL) return 0;
   *per_out = per_for(cs);
   return cs;
