@@ -182,6 +182,26 @@ def run_reference(args):
 # ----------------------------------------------------------------------------------------
 
 
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Every rank compresses its own layer (independent units, weak scaling): its own seed."""
+    return base_seed + rank
+
+
+def max_over_ranks(ms: float, world: int, dist, device) -> float:
+    """The job's time is the slowest rank's (no data-path collective: only this reduction)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step: float, steps: int, world: int, ms: float) -> float:
+    """Whole-job rate: units all ranks processed / the max-over-ranks time."""
+    return units_per_rank_step * steps * world / (ms / 1e3)
+
+
 def _source_sha(paths):
     import hashlib
     h = hashlib.sha256()
@@ -224,7 +244,7 @@ class PrefillCase:
         if instances > 1:
             wl = wl.with_(B=instances)
         self.wl = wl
-        inp = prefill_inputs(wl, seed=wl.seed + rank)
+        inp = prefill_inputs(wl, seed=rank_seed(wl.seed, rank))
         self.host = inp
 
         def to_dev(u16):
@@ -325,11 +345,7 @@ class PrefillCase:
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(e0.elapsed_time(e1), world, dist, dev)
         return {"value": self.tokens_per_step * steps * world / (ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int((hq.numel() + hK.numel() + hV.numel()) * 2),
                 "d2h_bytes_per_step": int(h_idx.numel() * 4 + (h_Ko.numel() + h_Vo.numel()) * 2)}
@@ -348,7 +364,7 @@ class TovaDecodeCase:
         self.cache_bytes = B * KVH * n * D * 2
         self.R = R = max(2, math.ceil(3 * L2_BYTES / self.cache_bytes))
         g = torch.Generator(device=dev)
-        g.manual_seed(wl.seed + rank)
+        g.manual_seed(rank_seed(wl.seed, rank))
         bf = torch.bfloat16
         self.caches = []
         for r in range(R):
@@ -406,7 +422,7 @@ class ScissorhandsCase:
         self.cache_bytes = B * KVH * cap * D * 2
         self.R = R = max(2, math.ceil(3 * L2_BYTES / self.cache_bytes))
         g = torch.Generator(device=dev)
-        g.manual_seed(wl.seed + rank)
+        g.manual_seed(rank_seed(wl.seed, rank))
         bf = torch.bfloat16
         self.reps = []
         for r in range(R):
@@ -519,12 +535,8 @@ def run_ours(args):
     launches = kvc.kvc_launch_count() - launches0
     if world > 1:
         dist.barrier()
-    ms = start.elapsed_time(stop)
+    ms = max_over_ranks(start.elapsed_time(stop), world, dist, dev)
     clocks = sampler.stop() if sampler else None
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
     assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
     kernels = {}
@@ -551,7 +563,7 @@ def run_ours(args):
     roof["algorithmic_bytes_per_launch"] = dom.nbytes
     roof["algorithmic_flops_per_launch"] = dom.flops
 
-    value = case.tokens_per_step * args.steps * world / (ms / 1e3)
+    value = job_throughput(case.tokens_per_step, args.steps, world, ms)
     e2e = case.e2e(max(3, min(args.steps, 20)), stream, world, dist, dev) if not args.no_e2e else None
 
     cpu = None
