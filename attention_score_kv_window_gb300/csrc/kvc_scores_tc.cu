@@ -602,7 +602,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_maps(const ScoresArgs& a, int D, int qrows, CUtensorMap* tmK, CUtensorMap* tmQ) {
+bool make_k_map(const ScoresArgs& a, int D, CUtensorMap* tmK) {
   auto enc = encode_fn();
   if (!enc) return false;
   if (a.ss <= 0 || (a.KVH > 1 && a.sh <= 0) || (a.B > 1 && a.sb <= 0)) return false;
@@ -611,18 +611,58 @@ bool make_maps(const ScoresArgs& a, int D, int qrows, CUtensorMap* tmK, CUtensor
                               (cuuint64_t)(a.B > 1 ? a.sb : (int64_t)a.KVH * (a.KVH > 1 ? a.sh : a.S * a.ss)) * 2};
   const cuuint32_t kbox[4] = {64, (cuuint32_t)TILE, 1, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
-  if (enc(tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(a.K), kdims, kstr, kbox, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return false;
+  return enc(tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(a.K), kdims, kstr, kbox, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_q_map(const ScoresArgs& a, int D, int qrows, CUtensorMap* tmQ) {
+  auto enc = encode_fn();
+  if (!enc) return false;
   const cuuint64_t qdims[2] = {(cuuint64_t)D, (cuuint64_t)a.B * a.H * a.w};
   const cuuint64_t qstr[1] = {(cuuint64_t)D * 2};
   const cuuint32_t qbox[2] = {64, (cuuint32_t)qrows};
-  if (enc(tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.q), qdims, qstr, qbox, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return false;
-  return true;
+  const cuuint32_t es[2] = {1, 1};
+  return enc(tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.q), qdims, qstr, qbox, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The three tensor maps of one call (K; the query group for pass 1 and for pass 2).  Encoding
+// costs host microseconds per map, so the last few sets are kept per host thread, keyed on
+// the addresses, shapes and strides they describe.
+struct TcMaps {
+  CUtensorMap k, q1, q2;
+};
+struct MapKey {
+  const void* K;
+  const void* q;
+  int64_t S, ss, sh, sb;
+  int B, H, KVH, w, D, Rpad;
+  bool operator==(const MapKey& o) const {
+    return K == o.K && q == o.q && S == o.S && ss == o.ss && sh == o.sh && sb == o.sb && B == o.B && H == o.H &&
+           KVH == o.KVH && w == o.w && D == o.D && Rpad == o.Rpad;
+  }
+};
+
+const TcMaps* tc_maps(const ScoresArgs& a, int D) {
+  struct Entry {
+    TcMaps maps;
+    MapKey key;
+    bool valid = false, ok = false;
+  };
+  thread_local Entry cache[8];
+  thread_local int next = 0;
+  const MapKey key{a.K, a.q, a.S, a.ss, a.sh, a.sb, a.B, a.H, a.KVH, a.w, D, a.Rpad};
+  for (Entry& e : cache)
+    if (e.valid && e.key == key) return e.ok ? &e.maps : nullptr;
+  Entry& e = cache[next];
+  next = (next + 1) % 8;
+  e.key = key;
+  e.valid = true;
+  e.ok = make_k_map(a, D, &e.maps.k) && make_q_map(a, D, a.Rpad > 128 ? 256 : 128, &e.maps.q1) &&
+         make_q_map(a, D, a.Rpad, &e.maps.q2);
+  return e.ok ? &e.maps : nullptr;
 }
 
 template <typename Kern>
@@ -638,23 +678,23 @@ cudaError_t set_smem_once(Kern k, size_t bytes, int slot) {
 
 template <int D, int NHALF>
 cudaError_t run_pass1(const ScoresArgs& a, cudaStream_t st, int slot) {
-  CUtensorMap tmK, tmQ;
-  if (!make_maps(a, D, NHALF * 128, &tmK, &tmQ)) return cudaErrorInvalidValue;
+  const TcMaps* m = tc_maps(a, D);
+  if (!m) return cudaErrorInvalidValue;
   const size_t smem = Layout<D>::SMEM;
   cudaError_t e = set_smem_once(k_pass1_tc<D, NHALF>, smem, slot);
   if (e != cudaSuccess) return e;
-  k_pass1_tc<D, NHALF><<<dim3(a.nsplit, a.KVH, a.B), THREADS, smem, st>>>(a, tmK, tmQ);
+  k_pass1_tc<D, NHALF><<<dim3(a.nsplit, a.KVH, a.B), THREADS, smem, st>>>(a, m->k, m->q1);
   return launched(1);
 }
 
 template <int D, int NQ>
 cudaError_t run_pass2(const ScoresArgs& a, cudaStream_t st, int slot) {
-  CUtensorMap tmK, tmQ;
-  if (!make_maps(a, D, 4 * NQ, &tmK, &tmQ)) return cudaErrorInvalidValue;
+  const TcMaps* m = tc_maps(a, D);
+  if (!m) return cudaErrorInvalidValue;
   const size_t smem = Layout<D>::SMEM;
   cudaError_t e = set_smem_once(k_pass2_tc<D, NQ>, smem, slot);
   if (e != cudaSuccess) return e;
-  k_pass2_tc<D, NQ><<<dim3(a.nsplit, a.KVH, a.B), THREADS, smem, st>>>(a, tmK, tmQ);
+  k_pass2_tc<D, NQ><<<dim3(a.nsplit, a.KVH, a.B), THREADS, smem, st>>>(a, m->k, m->q2);
   return launched(1);
 }
 
@@ -667,8 +707,7 @@ bool tc_supported(const ScoresArgs& a, int D) {
   if (a.R <= 32 || a.S < TILE) return false;
   if ((int64_t)a.B * a.H * a.w < (a.Rpad > 128 ? 256 : 128)) return false;
   if (a.nsplit > 65535 || a.KVH > 65535 || a.B > 65535) return false;
-  CUtensorMap k1, q1;
-  return make_maps(a, D, a.Rpad > 128 ? 256 : 128, &k1, &q1) && make_maps(a, D, a.Rpad, &k1, &q1);
+  return tc_maps(a, D) != nullptr;
 }
 
 cudaError_t launch_pass1_tc(const ScoresArgs& a, int D, cudaStream_t st) {
