@@ -9,6 +9,8 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "kvc_internal.cuh"
 
@@ -108,6 +110,21 @@ static std::atomic<long long> g_launches{0};
 cudaError_t launched(int n) {
   g_launches.fetch_add(n, std::memory_order_relaxed);
   return cudaGetLastError();
+}
+
+cudaError_t func_attrs_once(const void* fn, int max_dynamic_smem) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({fn, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess && max_dynamic_smem > 48 * 1024)
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic_smem);
+  if (e == cudaSuccess) done.insert({fn, dev});
+  return e;
 }
 
 int num_sms() {

@@ -30,6 +30,11 @@ cudaError_t take_status_select(unsigned int* v);
 cudaError_t take_status_gather(unsigned int* v);
 cudaError_t take_status_scissorhands(unsigned int* v);
 
+// Once per kernel and device: prefer the largest shared-memory carveout (consecutive kernels
+// of a call then do not make the SM change its L1 / shared split) and, above 48 KB, allow
+// `max_dynamic_smem` bytes of dynamic shared memory.  `fn` is the kernel's address.
+cudaError_t func_attrs_once(const void* fn, int max_dynamic_smem);
+
 // Host-side helpers
 int num_sms();                      // SM count of the current device (cached per device)
 // Count n kernels just enqueued (reported by kvc_launch_count) and return the launch status.
@@ -55,6 +60,7 @@ struct ScoresArgs {
   float* mrow;   // [B*KVH][Rpad]          M2 + log2(L)  (+inf: no visible key)
   float* out;    // [B*KVH][S]
   float out_mul; // 1/G
+  unsigned long long* sync;  // fused tensor-core kernel: epoch word + one tag per CTA (may be null)
 };
 
 // (m, l) partial of query row r from key range `split`: a row's ranges are contiguous
@@ -63,14 +69,15 @@ __host__ __device__ __forceinline__ int64_t part_index(const ScoresArgs& a, int 
 }
 #ifdef __CUDACC__
 // Row r's normaliser over all key ranges, log2 domain: M + log2(L) with M = max m and
-// L = sum l * 2^(m - M); +inf when the row sees no key.  Loads are issued eight at a time.
+// L = sum l * 2^(m - M); +inf when the row sees no key.  Loads are issued eight at a time and
+// bypass L1 (other CTAs of the same launch may have written the partials).
 __device__ __forceinline__ float merge_row(const ScoresArgs& a, int bk, int r) {
   const float2* p = a.part + part_index(a, bk, r, 0);
   float M = -__int_as_float(0x7f800000), Ls = 0.f;
   for (int s0 = 0; s0 < a.nsplit; s0 += 8) {
     float2 o[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) o[q] = (s0 + q < a.nsplit) ? p[s0 + q] : make_float2(0.f, 0.f);
+    for (int q = 0; q < 8; ++q) o[q] = (s0 + q < a.nsplit) ? __ldcg(p + s0 + q) : make_float2(0.f, 0.f);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
       if (o[q].y > 0.f) {
@@ -97,11 +104,11 @@ __host__ __device__ __forceinline__ void key_range(const ScoresArgs& a, int spli
   *kend = e < a.S ? e : a.S;
 }
 
-// tcgen05 (TMEM/TMA) versions of pass 1 and pass 2 (kvc_scores_tc.cu).  tc_supported() tells
-// whether the shapes fit them; the merge step between them is shared with the other path.
+// tcgen05 (TMEM/TMA) scoring (kvc_scores_tc.cu).  tc_supported() tells whether the shapes
+// fit it; launch_scores_tc() runs both passes, fused in one cooperative launch when a.sync is
+// set and the grid fits on the GPU at once, else as two launches.
 bool tc_supported(const ScoresArgs& a, int D);
-cudaError_t launch_pass1_tc(const ScoresArgs& a, int D, cudaStream_t st);
-cudaError_t launch_pass2_tc(const ScoresArgs& a, int D, cudaStream_t st);
+cudaError_t launch_scores_tc(const ScoresArgs& a, int D, cudaStream_t st);
 
 struct ScoresPlan {
   int R;         // query rows per (b,kvh): G*w
@@ -109,6 +116,7 @@ struct ScoresPlan {
   int nsplit;    // key ranges per (b,kvh)
   int64_t units; // 128-key units per (b,kvh)
   size_t part_bytes;   // (m,l) partials
+  size_t sync_bytes;   // fused tensor-core kernel: epoch word + one tag per CTA
   size_t group_bytes;  // per-group scores for the all-heads reduction
 };
 ScoresPlan plan_scores(const kvc_kv_desc& kv, int w, int reduce);

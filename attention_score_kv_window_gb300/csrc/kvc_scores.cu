@@ -681,9 +681,7 @@ cudaError_t launch_impl(const ScoresArgs& a, int reduce, float* scores, cudaStre
     e = launch_small<D>(a, cs, per, st);
     if (e != cudaSuccess) return e;
   } else if (tc_supported(a, D)) {
-    e = launch_pass1_tc(a, D, st);  // pass 2 merges the key-range partials itself
-    if (e != cudaSuccess) return e;
-    e = launch_pass2_tc(a, D, st);
+    e = launch_scores_tc(a, D, st);
     if (e != cudaSuccess) return e;
   } else {
     const int n_rg = (a.Rpad + P1_MAX_ROWS - 1) / P1_MAX_ROWS;
@@ -728,13 +726,14 @@ ScoresPlan plan_scores(const kvc_kv_desc& kv, int w, int reduce) {
   p.nsplit = (int)nsplit;
   p.part_bytes = (size_t)units * nsplit * p.Rpad * sizeof(float2) + (size_t)units * p.Rpad * sizeof(float);
   p.part_bytes = (p.part_bytes + 255) / 256 * 256;
+  p.sync_bytes = ((size_t)(1 + units * nsplit) * sizeof(unsigned long long) + 255) / 256 * 256;
   p.group_bytes = reduce == KVC_REDUCE_ALL_HEADS ? (size_t)units * kv.S * sizeof(float) : 0;
   return p;
 }
 
 size_t scores_workspace(const kvc_kv_desc& kv, int w, int reduce) {
   const ScoresPlan p = plan_scores(kv, w, reduce);
-  return p.part_bytes + p.group_bytes;
+  return p.part_bytes + p.sync_bytes + p.group_bytes;
 }
 
 cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc_kv_desc& kv, int w,
@@ -764,7 +763,8 @@ cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc
   uint8_t* base = static_cast<uint8_t*>(ws);
   a.part = reinterpret_cast<float2*>(base);
   a.mrow = reinterpret_cast<float*>(base + (size_t)kv.B * kv.KVH * p.nsplit * p.Rpad * sizeof(float2));
-  a.out = reduce == KVC_REDUCE_ALL_HEADS ? reinterpret_cast<float*>(base + p.part_bytes) : scores;
+  a.sync = reinterpret_cast<unsigned long long*>(base + p.part_bytes);
+  a.out = reduce == KVC_REDUCE_ALL_HEADS ? reinterpret_cast<float*>(base + p.part_bytes + p.sync_bytes) : scores;
   a.out_mul = 1.f / (float)a.G;
   if (kv.D == 64) return launch_impl<64>(a, reduce, scores, st);
   return launch_impl<128>(a, reduce, scores, st);

@@ -2,19 +2,23 @@
 // mma.sync path in kvc_scores.cu ("Add TOVA press": only the last w attention rows; cold-
 // compress PR 11: mean over each KV head's grouped queries), rebuilt around tcgen05.
 //
-// One CTA per (b, kvh, key range), 10 warps:
-//   warp 8  producer: TMA loads of the query group (once) and of 128-key K tiles into a
+// One CTA per (b, kvh, key range), 18 warps:
+//   warp 16 producer: TMA loads of the query group (once) and of 128-key K tiles into a
 //           4-stage shared-memory ring (128-byte swizzle), mbarrier-tracked;
-//   warp 9  MMA issuer: allocates all 512 TMEM columns (two 256-column accumulators) and
+//   warp 17 MMA issuer: allocates all 512 TMEM columns (two 256-column accumulators) and
 //           issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32) from one thread; commits
 //           free the K stage and publish the accumulator;
-//   warps 0-7 epilogue: tcgen05.ld the accumulator, release it, then do the softmax math.
+//   warps 0-15 epilogue: tcgen05.ld the accumulator, release it, then do the softmax math.
 // pass 1: A = query rows (M = 128 per half), B = K tile (N = 128 keys): each epilogue thread
 //         owns one query row, so its running max / sum over keys is thread-local.
 // pass 2: A = K tile (M = 128 keys), B = the query group (N = Rpad rows): each thread owns
-//         one key and sums exp2(s*log2e - c_r) over its half of the query rows.
-// Every mbarrier wait is bounded (%globaltimer); on timeout the kernel records
-// KVC_ERR_TIMEOUT, all roles leave their loops, and TMEM is released before exit.
+//         one key and sums exp2(s*log2e - c_r) over its quarter of the query rows; the three
+//         other quarters reach the key's owner warp through shared memory and an mbarrier.
+// The passes run as two launches, or fused in one cooperative launch: every CTA is resident,
+// a CTA publishes its pass-1 partials and waits for the other key ranges of its (b, kvh),
+// while its MMA warp streams the same key range again for pass 2 without a pause.
+// Every wait is bounded (%globaltimer); on timeout the kernel records KVC_ERR_TIMEOUT, all
+// roles leave their loops, and TMEM is released before exit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -38,6 +42,9 @@ constexpr int THREADS = 576;
 constexpr int QROWS_MAX = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s bound on any single wait
+constexpr int KSLOTS = 4;           // pass-2 key-sum exchange slots per group and quadrant
+// K ring full/empty, two accumulator full/empty pairs, query group, key-sum slots per quadrant
+constexpr int NBARS = 2 * STAGES + 5 + 2 * 4 * KSLOTS;
 
 __host__ __device__ constexpr uint32_t qpanel_bytes() { return QROWS_MAX * 128; }
 __host__ __device__ constexpr uint32_t kpanel_bytes() { return TILE * 128; }
@@ -49,13 +56,13 @@ struct Layout {
   static constexpr uint32_t Q = 0;
   static constexpr uint32_t K = Q + NP * qpanel_bytes();
   static constexpr uint32_t STAGE = NP * kpanel_bytes();
-  static constexpr uint32_t BARS = K + STAGES * STAGE;      // 2*STAGES + 5 mbarriers
-  static constexpr uint32_t MISC = (BARS + 8 * (2 * STAGES + 5) + 15) / 16 * 16;  // tmem base, abort flag
+  static constexpr uint32_t BARS = K + STAGES * STAGE;      // NBARS mbarriers
+  static constexpr uint32_t MISC = (BARS + 8 * NBARS + 15) / 16 * 16;  // tmem base, abort flag
   static constexpr uint32_t CR = MISC + 16;                 // float[256], 16-byte aligned (float4 reads)
   static constexpr uint32_t LIM = CR + 256 * 4;             // int[256]
   static constexpr uint32_t STAT = LIM + 256 * 4;           // float2[4][256]
-  static constexpr uint32_t KSUM = STAT + 4 * 256 * 8;      // float[2][4][128]
-  static constexpr uint32_t END = KSUM + 2 * 4 * 128 * 4;
+  static constexpr uint32_t KSUM = STAT + 4 * 256 * 8;      // float[2][KSLOTS][128]
+  static constexpr uint32_t END = KSUM + 2 * KSLOTS * 128 * 4;
   static constexpr size_t SMEM = END + 1024;                // + alignment slack
 };
 
@@ -75,6 +82,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// non-blocking test of the phase with the given parity
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -249,6 +267,9 @@ struct Ctx {
   __device__ uint32_t tfull(int b) const { return sbase + BARS_OFF + 8 * (2 * STAGES + b); }
   __device__ uint32_t tempty(int b) const { return sbase + BARS_OFF + 8 * (2 * STAGES + 2 + b); }
   __device__ uint32_t qfull() const { return sbase + BARS_OFF + 8 * (2 * STAGES + 4); }
+  __device__ uint32_t kready(int g, int qd, int slot) const {
+    return sbase + BARS_OFF + 8 * (2 * STAGES + 5 + (g * 4 + qd) * KSLOTS + slot);
+  }
   uint32_t BARS_OFF;
 };
 
@@ -269,9 +290,12 @@ __device__ __forceinline__ Ctx prologue(unsigned char* smem_raw) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(c.tfull(b), 1);
-      mbar_init(c.tempty(b), EPI_WARPS);
+      mbar_init(c.tempty(b), EPI_WARPS / 2);
     }
     mbar_init(c.qfull(), 1);
+    for (int g = 0; g < 2; ++g)
+      for (int q = 0; q < 4; ++q)
+        for (int k = 0; k < KSLOTS; ++k) mbar_init(c.kready(g, q, k), 32);
     *c.abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -298,22 +322,23 @@ __device__ __forceinline__ void teardown(const Ctx& c) {
   }
 }
 
-// producer: query group once, then the K ring
+// producer: query group once, then the K ring: `total` tiles, the key range's `ntiles` tiles
+// once per pass
 template <int D>
 __device__ __forceinline__ void producer(const Ctx& c, const ScoresArgs& a, const CUtensorMap* tmK,
                                          const CUtensorMap* tmQ, int qrows, int kvh, int b, int64_t kbeg,
-                                         int ntiles) {
+                                         int ntiles, int total) {
   using L = Layout<D>;
   const int qrow0 = (b * a.H + kvh * a.G) * a.w;
   mbar_expect_tx(c.qfull(), (uint32_t)(L::NP * qrows * 128));
   for (int p = 0; p < L::NP; ++p) tma_load_2d(c.sbase + L::Q + p * qpanel_bytes(), tmQ, p * 64, qrow0, c.qfull());
   int issued = 0;
-  for (int it = 0; it < ntiles; ++it) {
+  for (int it = 0; it < total; ++it) {
     const int s = it % STAGES;
     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
     if (!wait_bar(c.empty(s), ph ^ 1u, c.abort_flag)) break;
     mbar_expect_tx(c.full(s), L::STAGE);
-    const int y = (int)(kbeg + (int64_t)it * TILE);
+    const int y = (int)(kbeg + (int64_t)(it < ntiles ? it : it - ntiles) * TILE);
     for (int p = 0; p < L::NP; ++p)
       tma_load_4d(c.sbase + L::K + s * L::STAGE + p * kpanel_bytes(), tmK, p * 64, y, kvh, b, c.full(s));
     issued = it + 1;
@@ -327,7 +352,7 @@ __device__ __forceinline__ void producer(const Ctx& c, const ScoresArgs& a, cons
 }
 
 // ----------------------------------------------------------------------------------------
-// pass 1
+// softmax helpers
 // ----------------------------------------------------------------------------------------
 __device__ __forceinline__ float max8(const float* v, int n) {
   float m[8];
@@ -339,29 +364,213 @@ __device__ __forceinline__ float max8(const float* v, int n) {
   }
   return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
 }
-// sum_i exp2(v_i * sl2 - off) with eight independent accumulators
+// Packed pairs of fp32 (fma.rn.f32x2 / add.rn.f32x2 issue once for two lanes of work).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t p, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;\n" : "=f"(lo), "=f"(hi) : "l"(p));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t ex2x2(uint64_t y) {
+  float lo, hi;
+  upk2(y, lo, hi);
+  return pk2(ex2(lo), ex2(hi));
+}
+__device__ __forceinline__ float hsum4(const uint64_t* acc) {
+  float lo, hi;
+  upk2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), lo, hi);
+  return lo + hi;
+}
+// sum_i exp2(v_i * sl2 - off) over NC values (NC a multiple of 8), four packed accumulators
 template <int NC>
-__device__ __forceinline__ float sum_exp8(const float* v, float sl2, float off) {
-  float s[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) s[q] = 0.f;
+__device__ __forceinline__ float sum_exp2x(const float* v, float sl2, float off) {
+  const uint64_t SL = pk2(sl2, sl2), OF = pk2(-off, -off);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
   for (int i = 0; i < NC; i += 8) {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) s[q] += ex2(fmaf(v[i + q], sl2, -off));
+    for (int q = 0; q < 4; ++q) acc[q] = add2(acc[q], ex2x2(fma2(pk2(v[i + 2 * q], v[i + 2 * q + 1]), SL, OF)));
   }
-  return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+  return hsum4(acc);
+}
+// sum_i exp2(v_i * sl2 + nc_i) over NC values with per-column offsets nc (16-byte aligned)
+template <int NC>
+__device__ __forceinline__ float sum_exp2x_cols(const float* v, float sl2, const float* nc) {
+  const uint64_t SL = pk2(sl2, sl2);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int i = 0; i < NC; i += 8) {
+    const float4 ca = *reinterpret_cast<const float4*>(nc + i);
+    const float4 cb = *reinterpret_cast<const float4*>(nc + i + 4);
+    acc[0] = add2(acc[0], ex2x2(fma2(pk2(v[i + 0], v[i + 1]), SL, pk2(ca.x, ca.y))));
+    acc[1] = add2(acc[1], ex2x2(fma2(pk2(v[i + 2], v[i + 3]), SL, pk2(ca.z, ca.w))));
+    acc[2] = add2(acc[2], ex2x2(fma2(pk2(v[i + 4], v[i + 5]), SL, pk2(cb.x, cb.y))));
+    acc[3] = add2(acc[3], ex2x2(fma2(pk2(v[i + 6], v[i + 7]), SL, pk2(cb.z, cb.w))));
+  }
+  return hsum4(acc);
 }
 
-// Epilogue warp w reads columns [part*NC, part*NC + NC) of accumulator half h for the query
-// rows of lane quadrant w%4; the row's (max, sum) is then merged over its NPART warps.
-template <int D, int NHALF>
+// ----------------------------------------------------------------------------------------
+// key-range barrier of the fused launch
+// ----------------------------------------------------------------------------------------
+// Workspace words: sync[0] holds an epoch E that advances by one per launch; CTA (b, kvh,
+// split) sets sync[1 + (b*KVH + kvh)*nsplit + split] to tag(E + 1) once its pass-1 partials
+// are stored.  tag() is the splitmix64 output mix (Steele, Lea & Flood, "Fast splittable
+// pseudorandom number generators", OOPSLA 2014): leftover words from any earlier use of the
+// memory equal the current tag only by a 2^-64 chance, so the words need no initialisation.
+__device__ __forceinline__ uint64_t epoch_tag(uint64_t e) {
+  uint64_t z = e + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const unsigned long long* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;\n" ::: "memory"); }
+// One warp waits (bounded) until words [0, n) of `w` all equal `tag`.  With a non-null
+// abort flag the wait also ends when another role of the CTA has given up.
+__device__ __forceinline__ bool warp_wait_tags(const unsigned long long* w, int64_t n, uint64_t tag,
+                                               volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  bool ok = true;
+  const uint64_t t0 = gtimer();
+  for (int64_t i = lane; i < n && ok; i += 32) {
+    while (ld_relaxed_u64(w + i) != tag) {
+      if (abort_flag != nullptr && *abort_flag) {
+        ok = false;
+        break;
+      }
+      if (gtimer() - t0 > WAIT_NS) {
+        if (abort_flag != nullptr) *abort_flag = 1;
+        set_device_status(KVC_ERR_TIMEOUT);
+        ok = false;
+        break;
+      }
+      __nanosleep(32);
+    }
+  }
+  fence_acq_rel_gpu();  // what the tag writers stored before their release is now visible
+  return __all_sync(0xffffffffu, ok);
+}
+
+// (M, L) <- the log2-domain sum of (M, L) and (m2, l2); an empty side has L = 0
+__device__ __forceinline__ void lse2_merge(float& M, float& L, float m2, float l2) {
+  if (!(l2 > 0.f)) return;
+  if (!(L > 0.f)) {
+    M = m2;
+    L = l2;
+  } else if (m2 > M) {
+    L = L * exp2f(M - m2) + l2;
+    M = m2;
+  } else {
+    L += l2 * exp2f(m2 - M);
+  }
+}
+// Pass-2 prologue: nc[r] = -(M + log2 L) over the nsplit key-range partials of row r (-inf
+// when the row sees no key) and the row's causal limit, for r < N2.  TPR consecutive epilogue
+// threads share a row: each loads its strided share of the partials (eight loads in flight),
+// then the TPR results are combined with shuffles.
+template <int N2>
+__device__ __forceinline__ void merge_rows(const ScoresArgs& a, int bk, float* nc, int* lim) {
+  constexpr int TPR = N2 > 128 ? 2 : (N2 > 64 ? 4 : 8);
+  const int r = threadIdx.x / TPR, sub = threadIdx.x % TPR;
+  float M = -CUDART_INF_F, L = 0.f;
+  if (r < N2) {
+    const float2* p = a.part + part_index(a, bk, r, 0);
+    for (int s0 = sub; s0 < a.nsplit; s0 += 8 * TPR) {
+      float2 o[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int sidx = s0 + q * TPR;
+        o[q] = sidx < a.nsplit ? __ldcg(p + sidx) : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) lse2_merge(M, L, o[q].x, o[q].y);
+    }
+  }
+#pragma unroll
+  for (int off = 1; off < TPR; off <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, M, off), l2 = __shfl_xor_sync(0xffffffffu, L, off);
+    lse2_merge(M, L, m2, l2);
+  }
+  if (r < N2 && sub == 0) {
+    nc[r] = L > 0.f ? -(M + log2f(L)) : -CUDART_INF_F;
+    lim[r] = row_limit_i(a, r);
+  }
+}
+
+// Pass-2 chunk: W query-row columns of this thread's key from TMEM (the accumulator is
+// released after the call's last chunk is loaded), masked columns set to -inf, then
+// sum exp2(s*log2e - c_r) with nc = -c_r.
+template <int W>
+__device__ __forceinline__ float pass2_chunk(const Ctx& c, int buf, uint32_t taddr, bool release, const float* nc,
+                                             const int* lim, float sl2, bool clean, int64_t j, int64_t kend) {
+  float v[W];
+  tmem_load_cols<W>(taddr, v);
+  if (release) {
+    tc_fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(c.tempty(buf));
+  }
+  if (!clean) {
+    // limits are loaded unconditionally and applied with selects (a short-circuit test
+    // around the load would make every column a divergent branch)
+    const bool in = j < kend;
+#pragma unroll
+    for (int i = 0; i < W; i += 4) {
+      const int4 l4 = *reinterpret_cast<const int4*>(lim + i);
+      v[i + 0] = (in & (j <= l4.x)) ? v[i + 0] : -CUDART_INF_F;
+      v[i + 1] = (in & (j <= l4.y)) ? v[i + 1] : -CUDART_INF_F;
+      v[i + 2] = (in & (j <= l4.z)) ? v[i + 2] : -CUDART_INF_F;
+      v[i + 3] = (in & (j <= l4.w)) ? v[i + 3] : -CUDART_INF_F;
+    }
+  }
+  return sum_exp2x_cols<W>(v, sl2, nc);
+}
+
+// ----------------------------------------------------------------------------------------
+// the scoring kernel
+// ----------------------------------------------------------------------------------------
+// MODE 1: pass 1 only (key-range partials (m, l) of every query row to a.part);
+// MODE 2: pass 2 only (c_r merged from a.part, column sums to a.out);
+// MODE 3: both, one cooperative launch, with the key-range barrier between them.
+// The epilogue runs as two groups that alternate tiles: warps 0-7 take the tiles landing in
+// accumulator 0, warps 8-15 those in accumulator 1, so one group computes while the other
+// waits for its next tile.  A warp w only reads TMEM lanes of quadrant w%4.
+// Pass 1: warp (g, w8) reads, for the query rows of quadrant w8%4 in half h, NC1 key columns
+// of its group's tiles; a row's (max, sum) is then merged over its NPART1 warps.
+// Pass 2: warp (g, w8) reads, for the 32 keys of quadrant w8%4, the query-row columns
+// [hf*NW, hf*NW + NW) with hf = w8/4; the hf = 1 warp hands its key sums to the hf = 0 warp
+// through a shared-memory slot and an mbarrier, and that warp adds them and stores.
+template <int D, int NHALF, int NQ, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_pass1_tc(const ScoresArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ) {
+    k_scores_tc(const ScoresArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ) {
   using L = Layout<D>;
   constexpr int KS = D / 16;
-  constexpr int NPART = 4 / NHALF;        // warps sharing one query row
-  constexpr int NC = TILE / NPART;        // accumulator columns per warp
+  constexpr bool P1 = (MODE & 1) != 0, P2 = (MODE & 2) != 0;
+  constexpr int N2 = 4 * NQ;                     // pass-2 MMA N: padded query rows
+  constexpr int QROWS = P1 ? NHALF * 128 : N2;   // query rows staged in shared memory
+  constexpr int NPART1 = NHALF == 2 ? 2 : 4;     // pass 1: warps sharing one query row
+  constexpr int NC1 = NHALF == 2 ? TILE : TILE / 2;  // pass 1: key columns per warp and tile
+  constexpr int NW = N2 / 2;                     // pass 2: query-row columns per warp and tile
   extern __shared__ unsigned char smem_raw[];
   const Ctx c = prologue<D>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -370,216 +579,200 @@ __global__ void __launch_bounds__(THREADS, 1)
   int64_t kbeg, kend;
   key_range(a, split, &kbeg, &kend);
   const int ntiles = (int)((kend - kbeg + TILE - 1) / TILE);
+  const int n1 = P1 ? ntiles : 0;
+  const int total = n1 + (P2 ? ntiles : 0);
 
   if (warp == PRODUCER_WARP) {
-    if (lane == 0) producer<D>(c, a, &tmK, &tmQ, NHALF * 128, kvh, b, kbeg, ntiles);
+    if (lane == 0) producer<D>(c, a, &tmK, &tmQ, QROWS, kvh, b, kbeg, ntiles, total);
   } else if (warp == MMA_WARP) {
     if (lane == 0 && wait_bar(c.qfull(), 0, c.abort_flag)) {
       int done = 0;
-      constexpr uint32_t idesc = idesc_bf16(128, TILE);
-      for (int it = 0; it < ntiles; ++it) {
+      // Tile it+1's barriers are tested (without blocking) between the two halves of tile
+      // it's MMAs; only if they were not yet complete does the thread wait after the commits.
+      // Either way no MMA of tile it waits on the epilogue.
+      auto ready = [&](int t) -> bool {
+        return wait_bar(c.tempty(t & 1), ((uint32_t)(t >> 1) & 1u) ^ 1u, c.abort_flag) &&
+               wait_bar(c.full(t % STAGES), (uint32_t)(t / STAGES) & 1u, c.abort_flag);
+      };
+      auto ready_now = [&](int t) -> bool {
+        return mbar_test(c.tempty(t & 1), ((uint32_t)(t >> 1) & 1u) ^ 1u) &&
+               mbar_test(c.full(t % STAGES), (uint32_t)(t / STAGES) & 1u);
+      };
+      // descriptor start addresses advance in 16-byte units (no carry: shared memory < 256 KB)
+      const uint64_t qdesc = sw128_desc(c.sbase + L::Q), kdesc0 = sw128_desc(c.sbase + L::K);
+      bool ok = total > 0 && ready(0);
+      bool next_ready = false;
+      for (int it = 0; ok && it < total; ++it) {
         const int s = it % STAGES, buf = it & 1;
-        const uint32_t ph = (uint32_t)(it / STAGES) & 1u, bph = (uint32_t)(it >> 1) & 1u;
-        if (!wait_bar(c.tempty(buf), bph ^ 1u, c.abort_flag)) break;
-        if (!wait_bar(c.full(s), ph, c.abort_flag)) break;
         tc_fence_after();
+        const uint64_t kdesc = kdesc0 + (uint64_t)((s * L::STAGE) >> 4);
+        const uint32_t d = c.tmem + buf * 256;
+        if (it < n1) {
+          constexpr uint32_t idesc = idesc_bf16(128, TILE);
+          constexpr int NMMA = NHALF * KS;
 #pragma unroll
-        for (int h = 0; h < NHALF; ++h) {
-          const uint32_t d = c.tmem + buf * 256 + h * 128;
+          for (int q = 0; q < NMMA; ++q) {
+            if (q == NMMA / 2) next_ready = it + 1 < total && ready_now(it + 1);
+            const int h = q / KS, ks = q % KS;
+            const uint32_t koff = (ks & 3) * 32;
+            const uint64_t ad = qdesc + (uint64_t)(((ks >> 2) * qpanel_bytes() + h * 128 * 128 + koff) >> 4);
+            const uint64_t bd = kdesc + (uint64_t)(((ks >> 2) * kpanel_bytes() + koff) >> 4);
+            tc_mma(d + h * 128, ad, bd, idesc, ks > 0 ? 1u : 0u);
+          }
+        } else {
+          constexpr uint32_t idesc = idesc_bf16(128, N2);
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) {
+            if (ks == KS / 2) next_ready = it + 1 < total && ready_now(it + 1);
             const uint32_t koff = (ks & 3) * 32;
-            const uint64_t ad = sw128_desc(c.sbase + L::Q + (ks >> 2) * qpanel_bytes() + h * 128 * 128 + koff);
-            const uint64_t bd = sw128_desc(c.sbase + L::K + s * L::STAGE + (ks >> 2) * kpanel_bytes() + koff);
+            const uint64_t ad = kdesc + (uint64_t)(((ks >> 2) * kpanel_bytes() + koff) >> 4);
+            const uint64_t bd = qdesc + (uint64_t)(((ks >> 2) * qpanel_bytes() + koff) >> 4);
             tc_mma(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
           }
         }
         tc_commit(c.empty(s));
         tc_commit(c.tfull(buf));
         done = it + 1;
+        if (it + 1 < total && !next_ready) ok = ready(it + 1);
       }
       // stopped early: let the MMAs already issued finish before TMEM is released
       if (*c.abort_flag && done > 0) drain_bar(c.tfull((done - 1) & 1), (uint32_t)((done - 1) >> 1) & 1u);
     }
     __syncwarp();
   } else {
-    // epilogue: one query row per thread and warp-part
     const int qd = warp & 3;
-    const int h = NHALF == 2 ? ((warp >> 2) & 1) : 0;
-    const int part = NHALF == 2 ? (warp >> 3) : (warp >> 2);
-    const int c0 = part * NC;
-    const int r = h * 128 + qd * 32 + lane;
-    const int lim = row_limit_i(a, r);
-    // (m, l): l = sum exp2(s*log2e - m).  m is a reference, not always the exact max: a tile
-    // is accumulated against the current m unless its sum shows values more than 2^64 above
-    // it, in which case the exact tile max is taken and l rescaled.
-    float m = -CUDART_INF_F, l = 0.f;
-    float v[NC];
-    for (int it = 0; it < ntiles; ++it) {
-      const int buf = it & 1;
-      const uint32_t bph = (uint32_t)(it >> 1) & 1u;
-      if (!wait_bar(c.tfull(buf), bph, c.abort_flag)) break;
-      tc_fence_after();
-      tmem_load_cols<NC>(c.tmem + ((uint32_t)(qd * 32) << 16) + buf * 256 + h * 128 + c0, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(c.tempty(buf));
-      if (lim < 0) continue;
-      const int64_t kt0 = kbeg + (int64_t)it * TILE + c0;
-      const bool clean = (kt0 + NC <= kend) && (!a.causal || kt0 + NC - 1 <= (int64_t)lim);
-      if (!clean) {
-#pragma unroll
-        for (int i = 0; i < NC; ++i) {
-          const int64_t j = kt0 + i;
-          if (j >= kend || j > lim) v[i] = -CUDART_INF_F;
-        }
-      }
-      if (m != -CUDART_INF_F) {
-        const float t = sum_exp8<NC>(v, a.sl2, m);
-        if (t <= 0x1p64f) {
-          l += t;
-          continue;
-        }
-      }
-      const float mx = max8(v, NC);
-      if (mx == -CUDART_INF_F) continue;
-      const float mn = fmaxf(m, mx * a.sl2);
-      l = l * ex2(m - mn) + sum_exp8<NC>(v, a.sl2, mn);
-      m = mn;
+    const int g = warp >> 3, w8 = warp & 7;  // tile group (= accumulator buffer), warp in group
+    uint64_t epoch = 0;
+    if constexpr (MODE == 3) {
+      if (warp == 0) epoch = ld_relaxed_u64(a.sync);
     }
-    // merge the NPART partial (m, l) of each row
-    float2* stat = reinterpret_cast<float2*>(c.base + L::STAT);
-    stat[part * 256 + r] = make_float2(m, l);
-    named_sync_epilogue();
-    if (part == 0) {
-      float M = -CUDART_INF_F;
-#pragma unroll
-      for (int q = 0; q < NPART; ++q) {
-        const float2 o = stat[q * 256 + r];
-        if (o.y > 0.f) M = fmaxf(M, o.x);
-      }
-      float Lsum = 0.f;
-#pragma unroll
-      for (int q = 0; q < NPART; ++q) {
-        const float2 o = stat[q * 256 + r];
-        if (o.y > 0.f) Lsum += o.y * ex2(o.x - M);
-      }
-      if (r < a.Rpad) a.part[part_index(a, bk, r, split)] = make_float2(M, Lsum);
-    }
-  }
-  teardown<D>(c);
-}
-
-// ----------------------------------------------------------------------------------------
-// pass 2
-// ----------------------------------------------------------------------------------------
-// Epilogue warp w reads, for the 32 keys of lane quadrant w%4, the NQ query-row columns
-// [(w/4)*NQ, (w/4)*NQ + NQ); the four partial key sums are added after a named barrier.
-// The per-row normalisers c_r = M + log2(L) are merged from pass 1's key-range partials in
-// the prologue (no separate merge launch).
-template <int D, int NQ>
-__global__ void __launch_bounds__(THREADS, 1)
-    k_pass2_tc(const ScoresArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ) {
-  using L = Layout<D>;
-  constexpr int KS = D / 16;
-  constexpr int N = 4 * NQ;
-  extern __shared__ unsigned char smem_raw[];
-  const Ctx c = prologue<D>(smem_raw);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int bk = b * a.KVH + kvh;
-  int64_t kbeg, kend;
-  key_range(a, split, &kbeg, &kend);
-  const int ntiles = (int)((kend - kbeg + TILE - 1) / TILE);
-
-  if (warp == PRODUCER_WARP) {
-    if (lane == 0) producer<D>(c, a, &tmK, &tmQ, N, kvh, b, kbeg, ntiles);
-  } else if (warp == MMA_WARP) {
-    if (lane == 0 && wait_bar(c.qfull(), 0, c.abort_flag)) {
-      int done = 0;
-      constexpr uint32_t idesc = idesc_bf16(128, N);
-      for (int it = 0; it < ntiles; ++it) {
-        const int s = it % STAGES, buf = it & 1;
-        const uint32_t ph = (uint32_t)(it / STAGES) & 1u, bph = (uint32_t)(it >> 1) & 1u;
-        if (!wait_bar(c.tempty(buf), bph ^ 1u, c.abort_flag)) break;
-        if (!wait_bar(c.full(s), ph, c.abort_flag)) break;
+    if constexpr (P1) {
+      // one query row per thread; the group's tiles, read in 32-column chunks
+      const int h = NHALF == 2 ? (w8 >> 2) : 0;
+      const int part = NHALF == 2 ? g : g * 2 + (w8 >> 2);
+      const int c0 = NHALF == 2 ? 0 : (w8 >> 2) * NC1;
+      const int r = h * 128 + qd * 32 + lane;
+      const int lim = row_limit_i(a, r);
+      // (m, l): l = sum exp2(s*log2e - m).  m is a reference, not always the exact max: a
+      // chunk is accumulated against the current m unless its sum shows values more than
+      // 2^64 above it, in which case the exact chunk max is taken and l rescaled.
+      float m = -CUDART_INF_F, l = 0.f;
+      float v[32];
+      for (int it = g; it < n1; it += 2) {
+        const uint32_t bph = (uint32_t)(it >> 1) & 1u;
+        if (!wait_bar(c.tfull(g), bph, c.abort_flag)) break;
         tc_fence_after();
-        const uint32_t d = c.tmem + buf * 256;
+        const uint32_t taddr = c.tmem + ((uint32_t)(qd * 32) << 16) + g * 256 + h * 128 + c0;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const uint32_t koff = (ks & 3) * 32;
-          const uint64_t ad = sw128_desc(c.sbase + L::K + s * L::STAGE + (ks >> 2) * kpanel_bytes() + koff);
-          const uint64_t bd = sw128_desc(c.sbase + L::Q + (ks >> 2) * qpanel_bytes() + koff);
-          tc_mma(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
-        }
-        tc_commit(c.empty(s));
-        tc_commit(c.tfull(buf));
-        done = it + 1;
-      }
-      if (*c.abort_flag && done > 0) drain_bar(c.tfull((done - 1) & 1), (uint32_t)((done - 1) >> 1) & 1u);
-    }
-    __syncwarp();
-  } else {
-    float* cr = reinterpret_cast<float*>(c.base + L::CR);
-    int* limr = reinterpret_cast<int*>(c.base + L::LIM);
-    float* ksum = reinterpret_cast<float*>(c.base + L::KSUM);
-    // merge pass 1's key-range partials: c_r = M + log2(L), +inf when the row sees no key
-    for (int r = threadIdx.x; r < N; r += EPI_WARPS * 32) {
-      cr[r] = merge_row(a, bk, r);
-      limr[r] = row_limit_i(a, r);
-    }
-    named_sync_epilogue();
-    const int qd = warp & 3, cq = warp >> 2;
-    const int kr = qd * 32 + lane;
-    const float* crq = cr + cq * NQ;
-    const int* limq = limr + cq * NQ;
-    float* out = a.out + (int64_t)bk * a.S;
-    bool dead = false;
-    float v[NQ];
-    for (int it = 0; it < ntiles; ++it) {
-      const int buf = it & 1;
-      const uint32_t bph = (uint32_t)(it >> 1) & 1u;
-      const int64_t kt0 = kbeg + (int64_t)it * TILE;
-      const int64_t j = kt0 + kr;
-      float acc = 0.f;
-      if (!dead && wait_bar(c.tfull(buf), bph, c.abort_flag)) {
-        tc_fence_after();
-        tmem_load_cols<NQ>(c.tmem + ((uint32_t)(qd * 32) << 16) + buf * 256 + cq * NQ, v);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(c.tempty(buf));
-        const bool clean = (kt0 + TILE <= kend) && (!a.causal || kt0 + TILE - 1 <= a.S - a.w);
-        float s[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) s[q] = 0.f;
-        if (clean) {
-#pragma unroll
-          for (int i = 0; i < NQ; i += 8) {
-            const float4 c4a = *reinterpret_cast<const float4*>(crq + i);
-            const float4 c4b = *reinterpret_cast<const float4*>(crq + i + 4);
-            s[0] += ex2(fmaf(v[i + 0], a.sl2, -c4a.x));
-            s[1] += ex2(fmaf(v[i + 1], a.sl2, -c4a.y));
-            s[2] += ex2(fmaf(v[i + 2], a.sl2, -c4a.z));
-            s[3] += ex2(fmaf(v[i + 3], a.sl2, -c4a.w));
-            s[4] += ex2(fmaf(v[i + 4], a.sl2, -c4b.x));
-            s[5] += ex2(fmaf(v[i + 5], a.sl2, -c4b.y));
-            s[6] += ex2(fmaf(v[i + 6], a.sl2, -c4b.z));
-            s[7] += ex2(fmaf(v[i + 7], a.sl2, -c4b.w));
+        for (int ch = 0; ch < NC1 / 32; ++ch) {
+          tmem_ld32(taddr + ch * 32, v);
+          if (ch == NC1 / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(c.tempty(g));
           }
-        } else if (j < kend) {
+          if (lim < 0) continue;
+          const int64_t kt0 = kbeg + (int64_t)it * TILE + c0 + ch * 32;
+          if (!((kt0 + 32 <= kend) && (!a.causal || kt0 + 31 <= (int64_t)lim))) {
+            const int64_t jmax = (kend - 1 < (int64_t)lim ? kend - 1 : (int64_t)lim) - kt0;  // last visible column
 #pragma unroll
-          for (int i = 0; i < NQ; ++i)
-            if (j <= limq[i]) s[i & 7] += ex2(fmaf(v[i], a.sl2, -crq[i]));
+            for (int i = 0; i < 32; ++i) v[i] = (i <= jmax) ? v[i] : -CUDART_INF_F;
+          }
+          if (m != -CUDART_INF_F) {
+            const float t = sum_exp2x<32>(v, a.sl2, m);
+            if (t <= 0x1p64f) {
+              l += t;
+              continue;
+            }
+          }
+          const float mx = max8(v, 32);
+          if (mx == -CUDART_INF_F) continue;
+          const float mn = fmaxf(m, mx * a.sl2);
+          l = l * ex2(m - mn) + sum_exp2x<32>(v, a.sl2, mn);
+          m = mn;
         }
-        acc = ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
-      } else {
-        dead = true;
       }
-      ksum[(buf * 4 + cq) * 128 + kr] = acc;
+      // merge the NPART1 partial (m, l) of each row
+      float2* stat = reinterpret_cast<float2*>(c.base + L::STAT);
+      stat[part * 256 + r] = make_float2(m, l);
       named_sync_epilogue();
-      if (cq == 0 && !dead && j < kend) {
-        const float* kb = ksum + buf * 4 * 128 + kr;
-        out[j] = ((acc + kb[128]) + (kb[256] + kb[384])) * a.out_mul;
+      if (part == 0) {
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int q = 0; q < NPART1; ++q) {
+          const float2 o = stat[q * 256 + r];
+          if (o.y > 0.f) M = fmaxf(M, o.x);
+        }
+        float Lsum = 0.f;
+#pragma unroll
+        for (int q = 0; q < NPART1; ++q) {
+          const float2 o = stat[q * 256 + r];
+          if (o.y > 0.f) Lsum += o.y * ex2(o.x - M);
+        }
+        if (r < a.Rpad) a.part[part_index(a, bk, r, split)] = make_float2(M, Lsum);
+      }
+    }
+    if constexpr (MODE == 3) {
+      // publish this key range's partials, then wait for the other ranges of (b, kvh)
+      named_sync_epilogue();
+      if (warp == 0) {
+        unsigned long long* tags = a.sync + 1 + (int64_t)bk * a.nsplit;
+        const uint64_t tag = epoch_tag(epoch + 1);
+        if (lane == 0) {
+          fence_acq_rel_gpu();  // release: the CTA's partials (ordered by the barrier above)
+          st_relaxed_u64(tags + split, tag);
+        }
+        __syncwarp();
+        warp_wait_tags(tags, a.nsplit, tag, c.abort_flag);
+      }
+      named_sync_epilogue();
+    }
+    if constexpr (P2) {
+      float* ncr = reinterpret_cast<float*>(c.base + L::CR);
+      int* limr = reinterpret_cast<int*>(c.base + L::LIM);
+      merge_rows<N2>(a, bk, ncr, limr);
+      named_sync_epilogue();
+      const int hf = w8 >> 2;
+      const int kr = qd * 32 + lane;
+      const float* ncq = ncr + hf * NW;
+      const int* limq = limr + hf * NW;
+      float* out = a.out + (int64_t)bk * a.S;
+      bool dead = false;
+      const int first = n1 + ((g - n1) & 1);  // this group's first pass-2 tile
+      for (int it = first; it < total; it += 2) {
+        const int u = (it - first) >> 1;       // this group's pass-2 tile count
+        const int64_t kt0 = kbeg + (int64_t)(it - n1) * TILE;
+        const int64_t j = kt0 + kr;
+        float acc = 0.f;
+        if (!dead && wait_bar(c.tfull(g), (uint32_t)(it >> 1) & 1u, c.abort_flag)) {
+          tc_fence_after();
+          const uint32_t taddr = c.tmem + ((uint32_t)(qd * 32) << 16) + g * 256 + hf * NW;
+          const bool clean = (kt0 + TILE <= kend) && (!a.causal || kt0 + TILE - 1 <= a.S - a.w);
+#pragma unroll
+          for (int ch = 0; ch < NW / 32; ++ch)
+            acc += pass2_chunk<32>(c, g, taddr + ch * 32, ch == NW / 32 - 1, ncq + ch * 32, limq + ch * 32, a.sl2,
+                                   clean, j, kend);
+        } else {
+          dead = true;
+        }
+        // Slot u % KSLOTS is written again only KSLOTS group tiles later, after the reader has
+        // released the accumulator of the group's tile u + KSLOTS - 1 (so has read tile u).
+        const int slot = u % KSLOTS;
+        const uint32_t kb = c.kready(g, qd, slot);
+        float* ks = reinterpret_cast<float*>(c.base + L::KSUM) + (g * KSLOTS + slot) * 128 + kr;
+        if (hf != 0) {
+          *ks = acc;
+          mbar_arrive(kb);
+        } else if (wait_bar(kb, (uint32_t)(u / KSLOTS) & 1u, c.abort_flag) && !dead && j < kend) {
+          out[j] = (acc + *ks) * a.out_mul;
+        }
+      }
+    }
+    if constexpr (MODE == 3) {
+      // CTA 0 advances the epoch once every CTA has published (so has read the epoch)
+      if (warp == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+        warp_wait_tags(a.sync + 1, (int64_t)a.B * a.KVH * a.nsplit, epoch_tag(epoch + 1), nullptr);
+        if (lane == 0) st_relaxed_u64(a.sync, epoch + 1);
       }
     }
   }
@@ -665,37 +858,74 @@ const TcMaps* tc_maps(const ScoresArgs& a, int D) {
   return e.ok ? &e.maps : nullptr;
 }
 
-template <typename Kern>
-cudaError_t set_smem_once(Kern k, size_t bytes, int slot) {
-  static bool done[64][16] = {};
+// one launch of the scoring kernel in the given mode; the fused mode is cooperative
+template <int D, int NHALF, int NQ, int MODE>
+cudaError_t run_tc(const ScoresArgs& a, cudaStream_t st) {
+  const TcMaps* m = tc_maps(a, D);
+  if (!m) return cudaErrorInvalidValue;
+  auto kern = k_scores_tc<D, NHALF, NQ, MODE>;
+  const size_t smem = Layout<D>::SMEM;
+  cudaError_t e = func_attrs_once(reinterpret_cast<const void*>(kern), (int)smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(a.nsplit, a.KVH, a.B);
+  if constexpr (MODE != 3) {
+    kern<<<grid, THREADS, smem, st>>>(a, m->k, MODE == 2 ? m->q2 : m->q1);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, a, m->k, m->q1);
+    if (e != cudaSuccess) return e;
+  }
+  return launched(1);
+}
+
+// Whether every CTA of the fused launch can be resident at once (cached per device).
+template <int D, int NHALF, int NQ>
+bool fused_fits(const ScoresArgs& a) {
+  static int occ_cache[64] = {0};  // 0: not yet known, -1: not usable
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && done[dev][slot]) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev][slot] = true;
-  return e;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (occ_cache[dev] == 0) {
+    auto kern = k_scores_tc<D, NHALF, NQ, 3>;
+    const size_t smem = Layout<D>::SMEM;
+    int occ = 0, coop = 0;
+    if (func_attrs_once(reinterpret_cast<const void*>(kern), (int)smem) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, THREADS, smem) != cudaSuccess || !coop ||
+        occ < 1) {
+      cudaGetLastError();
+      occ = -1;
+    }
+    occ_cache[dev] = occ;
+  }
+  return occ_cache[dev] > 0 && (int64_t)a.nsplit * a.KVH * a.B <= (int64_t)occ_cache[dev] * num_sms();
 }
 
-template <int D, int NHALF>
-cudaError_t run_pass1(const ScoresArgs& a, cudaStream_t st, int slot) {
-  const TcMaps* m = tc_maps(a, D);
-  if (!m) return cudaErrorInvalidValue;
-  const size_t smem = Layout<D>::SMEM;
-  cudaError_t e = set_smem_once(k_pass1_tc<D, NHALF>, smem, slot);
+template <int D, int NHALF, int NQ>
+cudaError_t run_scores(const ScoresArgs& a, cudaStream_t st) {
+  if (a.sync != nullptr && fused_fits<D, NHALF, NQ>(a)) return run_tc<D, NHALF, NQ, 3>(a, st);
+  // pass 1 does not depend on NQ, pass 2 not on NHALF
+  const cudaError_t e = run_tc<D, NHALF, 16, 1>(a, st);
   if (e != cudaSuccess) return e;
-  k_pass1_tc<D, NHALF><<<dim3(a.nsplit, a.KVH, a.B), THREADS, smem, st>>>(a, m->k, m->q1);
-  return launched(1);
+  return run_tc<D, 1, NQ, 2>(a, st);
 }
 
-template <int D, int NQ>
-cudaError_t run_pass2(const ScoresArgs& a, cudaStream_t st, int slot) {
-  const TcMaps* m = tc_maps(a, D);
-  if (!m) return cudaErrorInvalidValue;
-  const size_t smem = Layout<D>::SMEM;
-  cudaError_t e = set_smem_once(k_pass2_tc<D, NQ>, smem, slot);
-  if (e != cudaSuccess) return e;
-  k_pass2_tc<D, NQ><<<dim3(a.nsplit, a.KVH, a.B), THREADS, smem, st>>>(a, m->k, m->q2);
-  return launched(1);
+template <int D>
+cudaError_t run_scores_d(const ScoresArgs& a, cudaStream_t st) {
+  switch (a.Rpad) {
+    case 64: return run_scores<D, 1, 16>(a, st);
+    case 128: return run_scores<D, 1, 32>(a, st);
+    case 192: return run_scores<D, 2, 48>(a, st);
+    default: return run_scores<D, 2, 64>(a, st);
+  }
 }
 
 }  // namespace
@@ -710,28 +940,8 @@ bool tc_supported(const ScoresArgs& a, int D) {
   return tc_maps(a, D) != nullptr;
 }
 
-cudaError_t launch_pass1_tc(const ScoresArgs& a, int D, cudaStream_t st) {
-  const bool two = a.Rpad > 128;
-  if (D == 64) return two ? run_pass1<64, 2>(a, st, 0) : run_pass1<64, 1>(a, st, 1);
-  return two ? run_pass1<128, 2>(a, st, 2) : run_pass1<128, 1>(a, st, 3);
-}
-
-cudaError_t launch_pass2_tc(const ScoresArgs& a, int D, cudaStream_t st) {
-  const int nq = a.Rpad / 4;
-  if (D == 64) {
-    switch (nq) {
-      case 16: return run_pass2<64, 16>(a, st, 4);
-      case 32: return run_pass2<64, 32>(a, st, 5);
-      case 48: return run_pass2<64, 48>(a, st, 6);
-      default: return run_pass2<64, 64>(a, st, 7);
-    }
-  }
-  switch (nq) {
-    case 16: return run_pass2<128, 16>(a, st, 8);
-    case 32: return run_pass2<128, 32>(a, st, 9);
-    case 48: return run_pass2<128, 48>(a, st, 10);
-    default: return run_pass2<128, 64>(a, st, 11);
-  }
+cudaError_t launch_scores_tc(const ScoresArgs& a, int D, cudaStream_t st) {
+  return D == 64 ? run_scores_d<64>(a, st) : run_scores_d<128>(a, st);
 }
 
 }  // namespace kvc

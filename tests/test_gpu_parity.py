@@ -53,6 +53,7 @@ SCORE_CASES = [
     (4, 8, 2, 128, 4096, 1, False, "gqa"),
     (1, 8, 2, 64, 3000, 32, True, "gqa"),     # R = 128: tensor-core path, one query half
     (2, 32, 8, 128, 5000, 64, False, "all_heads"),
+    (40, 16, 4, 64, 256, 16, True, "gqa"),    # 160 (b, kvh) > one CTA per SM: two launches
 ]
 
 
@@ -65,6 +66,24 @@ def test_window_scores_parity(B, H, KVH, D, S, w, causal, reduce):
     assert_scores_close(got.cpu().numpy(), ref)
     # sum over keys equals the window length (each window row's softmax sums to one)
     np.testing.assert_allclose(got.double().sum(-1).cpu().numpy(), w, rtol=1e-4)
+
+
+def test_window_scores_shared_workspace_any_content():
+    """One workspace, filled with random bytes first, serves several shapes in turn (different
+    key-range counts per KV head, so the bookkeeping words land on different offsets)."""
+    g = torch.Generator(device="cuda").manual_seed(11)
+    ws = torch.randint(0, 256, (64 << 20,), dtype=torch.uint8, device="cuda", generator=g)
+    shapes = [(1, 32, 8, 128, 32768, 64), (2, 8, 2, 128, 1000, 64), (1, 32, 8, 128, 5000, 64),
+              (1, 8, 8, 64, 4000, 40), (1, 32, 8, 128, 32768, 64)]
+    for i, (B, H, KVH, D, S, w) in enumerate(shapes):
+        inp = prefill_inputs(_wl(B, H, KVH, D, S, w, seed=100 + i))
+        scale = 1.0 / np.sqrt(D)
+        q, K = dev_bf16(inp["q"]), dev_bf16(inp["K"])
+        for _ in range(2):
+            got = kvc.kvc_window_scores(q, K, scale, causal=True, reduce="gqa", ws=ws)
+        ref = O.window_scores(inp["q"], inp["K"], scale, causal=True, reduce="gqa")
+        assert_scores_close(got.cpu().numpy(), ref)
+        assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
 
 @pytest.mark.parametrize("S,p_live", [(256, 0.7), (4096, 0.5), (100, 0.05), (64, 0.0)])
