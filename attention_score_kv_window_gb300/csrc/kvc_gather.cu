@@ -17,6 +17,10 @@ __device__ __forceinline__ void st16(uint16_t* p, uint4 v) { __stcs(reinterpret_
 // ----------------------------------------------------------------------------------------
 // compaction: Ko[b,kvh,t] = K[b,kvh,idx[b,kvh,t]] (V likewise); -1 -> zero row
 // ----------------------------------------------------------------------------------------
+// One warp per 16 output rows: lanes 0-15 load the rows' indices and source offsets once,
+// then every lane issues all of its 16-byte loads for the 16 rows (K and V) before any
+// store, so a warp keeps 16 x 2 x D x 2 bytes of gather in flight.
+constexpr int COMPACT_RPW = 16;  // output rows per warp
 template <int D>
 __global__ void __launch_bounds__(256) k_compact(const uint16_t* __restrict__ K,
                                                  const uint16_t* __restrict__ V, int64_t sb,
@@ -24,41 +28,44 @@ __global__ void __launch_bounds__(256) k_compact(const uint16_t* __restrict__ K,
                                                  const int32_t* __restrict__ idx, int k,
                                                  int64_t rows, uint16_t* __restrict__ Ko,
                                                  uint16_t* __restrict__ Vo) {
-  constexpr int TPR = D / 8;  // 16-byte chunks per row
-  constexpr int U = 4;        // chunks in flight per thread
-  const int64_t total = rows * TPR;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t x0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x0 < total; x0 += stride * U) {
-    uint4 kv[U], vv[U];
-    int64_t orow[U];
-    int cc[U];
+  pdl_wait();
+  pdl_trigger();
+  constexpr int TPR = D / 8;              // 16-byte chunks per row
+  constexpr int RPI = 32 / TPR;           // rows per warp-wide step
+  constexpr int ITER = COMPACT_RPW / RPI; // steps per warp
+  const int lane = threadIdx.x & 31;
+  const int c = lane % TPR;
+  const int64_t warp_g = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r0 = warp_g * COMPACT_RPW; r0 < rows; r0 += nwarps * COMPACT_RPW) {
+    int64_t off = -1;  // lane < 16: source offset of row r0 + lane (-1: zero row)
+    if (lane < COMPACT_RPW && r0 + lane < rows) {
+      const int64_t row = r0 + lane;
+      const int32_t j = __ldg(idx + row);
+      if (j >= 0 && j < S) {
+        const int64_t bk = row / k;
+        off = (bk / KVH) * sb + (bk % KVH) * sh + (int64_t)j * ss;
+      } else if (j >= S || j < -1) {
+        set_device_status(KVC_ERR_DEVICE_BOUNDS);
+      }
+    }
+    uint4 kv[ITER], vv[ITER];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t x = x0 + (int64_t)u * stride;
-      orow[u] = -1;
-      kv[u] = make_uint4(0, 0, 0, 0);
-      vv[u] = kv[u];
-      if (x < total) {
-        const int64_t row = x / TPR;
-        cc[u] = (int)(x % TPR);
-        orow[u] = row;
-        const int32_t j = __ldg(idx + row);
-        if (j >= 0 && j < S) {
-          const int64_t bk = row / k;
-          const int64_t b = bk / KVH, kvh = bk % KVH;
-          const int64_t off = b * sb + kvh * sh + (int64_t)j * ss + cc[u] * 8;
-          kv[u] = ld16(K + off);
-          if (V) vv[u] = ld16(V + off);
-        } else if (j >= S || j < -1) {
-          set_device_status(KVC_ERR_DEVICE_BOUNDS);
-        }
+    for (int it = 0; it < ITER; ++it) {
+      const int64_t o = __shfl_sync(0xffffffffu, off, it * RPI + lane / TPR);
+      kv[it] = make_uint4(0, 0, 0, 0);
+      vv[it] = kv[it];
+      if (o >= 0) {
+        kv[it] = ld16(K + o + c * 8);
+        if (V) vv[it] = ld16(V + o + c * 8);
       }
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (orow[u] >= 0) {
-        st16(Ko + orow[u] * D + cc[u] * 8, kv[u]);
-        if (Vo) st16(Vo + orow[u] * D + cc[u] * 8, vv[u]);
+    for (int it = 0; it < ITER; ++it) {
+      const int64_t row = r0 + it * RPI + lane / TPR;
+      if (row < rows) {
+        st16(Ko + row * D + c * 8, kv[it]);
+        if (Vo) st16(Vo + row * D + c * 8, vv[it]);
       }
     }
   }
@@ -278,12 +285,18 @@ int channel_splits(const kvc_kv_desc& kv, int64_t nrows) {
 cudaError_t launch_compact(const uint16_t* K, const uint16_t* V, const kvc_kv_desc& kv,
                            const int32_t* idx, int k, uint16_t* Ko, uint16_t* Vo, cudaStream_t st) {
   const int64_t rows = (int64_t)kv.B * kv.KVH * k;
-  const int64_t chunks = rows * (kv.D / 8);
-  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((chunks + 1023) / 1024, (int64_t)num_sms() * 16));
+  const int64_t warps = (rows + COMPACT_RPW - 1) / COMPACT_RPW;
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((warps + 7) / 8, (int64_t)num_sms() * 16));
+  cudaLaunchAttribute attrs[2];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(blocks), dim3(256), 0, st, attrs);
+  cudaError_t e;
   if (kv.D == 64)
-    k_compact<64><<<blocks, 256, 0, st>>>(K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, idx, k, rows, Ko, Vo);
+    e = cudaLaunchKernelEx(&cfg, k_compact<64>, K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, idx, k, rows,
+                           Ko, Vo);
   else
-    k_compact<128><<<blocks, 256, 0, st>>>(K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, idx, k, rows, Ko, Vo);
+    e = cudaLaunchKernelEx(&cfg, k_compact<128>, K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, idx, k,
+                           rows, Ko, Vo);
+  if (e != cudaSuccess) return e;
   return launched(1);
 }
 

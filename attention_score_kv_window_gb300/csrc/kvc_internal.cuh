@@ -30,6 +30,39 @@ cudaError_t take_status_select(unsigned int* v);
 cudaError_t take_status_gather(unsigned int* v);
 cudaError_t take_status_scissorhands(unsigned int* v);
 
+// Programmatic dependent launch.  Kernels launched with pdl_config() may start before the
+// previous kernel on the stream has finished; each such kernel calls pdl_wait() before its
+// first global-memory access (it returns once the previous kernel has completed and its
+// writes are visible; it returns at once when there is nothing to wait for).  pdl_trigger()
+// lets the next kernel's launch begin once every CTA of this grid has called it or exited.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+// Launch configuration with programmatic stream serialisation and, when cluster_x > 1, a
+// cluster shape.  `attrs` must outlive the launch call.
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t st, cudaLaunchAttribute* attrs,
+                                     int cluster_x = 1) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  int n = 0;
+  attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = cluster_x;
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = n;
+  return cfg;
+}
+
 // Once per kernel and device: prefer the largest shared-memory carveout (consecutive kernels
 // of a call then do not make the SM change its L1 / shared split) and, above 48 KB, allow
 // `max_dynamic_smem` bytes of dynamic shared memory.  `fn` is the kernel's address.

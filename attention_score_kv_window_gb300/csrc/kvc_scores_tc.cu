@@ -726,6 +726,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         warp_wait_tags(tags, a.nsplit, tag, c.abort_flag);
       }
       named_sync_epilogue();
+      pdl_trigger();  // the next kernel may start launching; it waits for this grid's end
     }
     if constexpr (P2) {
       float* ncr = reinterpret_cast<float*>(c.base + L::CR);

@@ -365,6 +365,8 @@ __global__ void __launch_bounds__(SEL_THREADS) k_topk(const float* __restrict__ 
                                                       int largest, int32_t* __restrict__ idx) {
   extern __shared__ __align__(16) uint32_t kc[];
   __shared__ SelShared sh;
+  pdl_wait();
+  pdl_trigger();
   const int64_t row = blockIdx.x / cg::this_cluster().num_blocks();
   ScoreKeys fn;
   fn.row = scores + row * S;
@@ -378,6 +380,8 @@ __global__ void __launch_bounds__(SEL_THREADS) k_topk(const float* __restrict__ 
 __global__ void __launch_bounds__(SEL_THREADS) k_sh_evict(kvc_sh_state s, int m, int32_t* evicted) {
   extern __shared__ __align__(16) uint32_t kc[];
   __shared__ SelShared sh;
+  pdl_wait();
+  pdl_trigger();
   const int64_t row = blockIdx.x;
   const int64_t nw = s.cap / 32;
   FractionKeys fn;
@@ -417,6 +421,8 @@ __global__ void __launch_bounds__(SHORT_THREADS) k_topk_short(const float* __res
   __shared__ uint32_t wsum[SHORT_THREADS / 32];
   __shared__ uint64_t wmax[SHORT_THREADS / 32];
   __shared__ uint32_t s_nforced, s_nelig;
+  pdl_wait();
+  pdl_trigger();
   const int64_t row = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   ScoreKeys fn;
@@ -558,8 +564,11 @@ int64_t topk_max_len() { return SLICE_MAX * MAX_CLUSTER; }
 cudaError_t launch_topk(const float* scores, int B, int KVH, int64_t S, int k, int protect_tail,
                         const uint32_t* live, int largest, int32_t* idx, cudaStream_t st) {
   if (S <= SHORT_MAX) {
-    k_topk_short<<<(unsigned)((int64_t)B * KVH), SHORT_THREADS, 0, st>>>(scores, (int)S, k, protect_tail, live,
-                                                                         largest, idx);
+    cudaLaunchAttribute attrs[2];
+    const cudaLaunchConfig_t cfg =
+        pdl_config(dim3((unsigned)((int64_t)B * KVH)), dim3(SHORT_THREADS), 0, st, attrs);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_topk_short, scores, (int)S, k, protect_tail, live, largest, idx);
+    if (e != cudaSuccess) return e;
     return launched(1);
   }
   const int cs = topk_cluster_size(S);
@@ -574,18 +583,9 @@ cudaError_t launch_topk(const float* scores, int B, int KVH, int64_t S, int k, i
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((int64_t)B * KVH * cs), 1, 1);
-  cfg.blockDim = dim3(SEL_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaLaunchAttribute attrs[2];
+  const cudaLaunchConfig_t cfg =
+      pdl_config(dim3((unsigned)((int64_t)B * KVH * cs)), dim3(SEL_THREADS), smem, st, attrs, cs);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k_topk, scores, S, k, protect_tail, live, largest, idx);
   if (e != cudaSuccess) return e;
   return launched(1);
@@ -597,7 +597,10 @@ cudaError_t launch_sh_evict(const kvc_sh_state& s, int m, int32_t* evicted, cuda
   // static (histograms) + dynamic (keys) shared memory exceed the 48 KB default: opt in
   cudaError_t e = cudaFuncSetAttribute(k_sh_evict, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(SLICE_MAX * 4));
   if (e != cudaSuccess) return e;
-  k_sh_evict<<<s.B * s.KVH, SEL_THREADS, smem, st>>>(s, m, evicted);
+  cudaLaunchAttribute attrs[2];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)(s.B * s.KVH)), dim3(SEL_THREADS), smem, st, attrs);
+  e = cudaLaunchKernelEx(&cfg, k_sh_evict, s, m, evicted);
+  if (e != cudaSuccess) return e;
   return launched(1);
 }
 
