@@ -75,6 +75,7 @@ template <int D>
 __global__ void k_write_slots(const uint16_t* __restrict__ kn, const uint16_t* __restrict__ vn,
                               const int32_t* __restrict__ slot, uint16_t* K, uint16_t* V, int64_t sb,
                               int64_t sh, int64_t ss, int KVH, int64_t S, int rows) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   constexpr int TPR = D / 8;
   const int x = blockIdx.x * blockDim.x + threadIdx.x;
   if (x >= rows * TPR) return;
@@ -111,6 +112,7 @@ __global__ void __launch_bounds__(256) k_channel_partial(const uint16_t* __restr
                                                          const int32_t* __restrict__ idx, int k,
                                                          int64_t nrows, int64_t chunk,
                                                          float* __restrict__ part, int KVH) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   constexpr int TPR = D / 8;
   constexpr int RPP = 256 / TPR;  // rows per pass
   __shared__ float red[RPP][D + 1];
@@ -144,6 +146,7 @@ __global__ void __launch_bounds__(256) k_channel_partial(const uint16_t* __restr
 __global__ void __launch_bounds__(1024) k_channel_final(const uint16_t* __restrict__ q, int H, int KVH, int w,
                                                         int D, const float* __restrict__ part, int nsplit, int B,
                                                         float* __restrict__ cs) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   __shared__ float qred[16][128];
   __shared__ float kred[16][128];
   const int bk = blockIdx.x;
@@ -175,6 +178,7 @@ __global__ void __launch_bounds__(1024) k_channel_final(const uint16_t* __restri
 // ----------------------------------------------------------------------------------------
 // keep the C highest channel scores (ties: lower channel), ascending list
 __global__ void k_channel_select(const float* __restrict__ cs, int D, int C, int32_t* __restrict__ ch) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   __shared__ float v[128];
   __shared__ uint32_t wb[4];
   const int bk = blockIdx.x, d = threadIdx.x;  // blockDim = 128
@@ -205,6 +209,7 @@ __global__ void __launch_bounds__(256) k_channel_gather(const uint16_t* __restri
                                                         int64_t sh, int64_t ss, int64_t S, int KVH,
                                                         const int32_t* __restrict__ ch, int C,
                                                         uint16_t* __restrict__ Ko) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   constexpr int TPR = D / 8, RB = 32;
   __shared__ __align__(16) uint16_t tile[RB][D + 8];
   __shared__ int32_t chs[128];
@@ -242,6 +247,7 @@ __global__ void __launch_bounds__(256) k_channel_zero(const uint16_t* K, int64_t
                                                       int64_t ss, int64_t S, int KVH,
                                                       const int32_t* __restrict__ ch, int C,
                                                       uint16_t* Ko) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   constexpr int TPR = D / 8;
   __shared__ uint32_t keepw[4];
   const int bk = blockIdx.y;
@@ -305,10 +311,12 @@ cudaError_t launch_write_slots(const uint16_t* kn, const uint16_t* vn, const int
   const int rows = kv.B * kv.KVH;
   const int n = rows * (kv.D / 8);
   const int blocks = (n + 255) / 256;
-  if (kv.D == 64)
-    k_write_slots<64><<<blocks, 256, 0, st>>>(kn, vn, slot, K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, rows);
-  else
-    k_write_slots<128><<<blocks, 256, 0, st>>>(kn, vn, slot, K, V, kv.stride_b, kv.stride_h, kv.stride_s, kv.KVH, kv.S, rows);
+  const cudaError_t e =
+      kv.D == 64 ? launch_pdl(k_write_slots<64>, dim3(blocks), dim3(256), 0, st, kn, vn, slot, K, V, kv.stride_b,
+                              kv.stride_h, kv.stride_s, kv.KVH, kv.S, rows)
+                 : launch_pdl(k_write_slots<128>, dim3(blocks), dim3(256), 0, st, kn, vn, slot, K, V, kv.stride_b,
+                              kv.stride_h, kv.stride_s, kv.KVH, kv.S, rows);
+  if (e != cudaSuccess) return e;
   return launched(1);
 }
 
@@ -325,31 +333,35 @@ cudaError_t launch_channel_score(const uint16_t* q, int w, const uint16_t* K, co
   const int64_t chunk = (nrows + ns - 1) / ns;
   float* part = static_cast<float*>(ws);
   dim3 grid(ns, kv.KVH, kv.B);
-  if (kv.D == 64)
-    k_channel_partial<64><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, idx, k, nrows, chunk, part, kv.KVH);
-  else
-    k_channel_partial<128><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, idx, k, nrows, chunk, part, kv.KVH);
-  k_channel_final<<<kv.B * kv.KVH, 1024, 0, st>>>(q, kv.H, kv.KVH, w, kv.D, part, ns, kv.B, cs);
+  cudaError_t e =
+      kv.D == 64 ? launch_pdl(k_channel_partial<64>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
+                              kv.S, idx, k, nrows, chunk, part, kv.KVH)
+                 : launch_pdl(k_channel_partial<128>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
+                              kv.S, idx, k, nrows, chunk, part, kv.KVH);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(k_channel_final, dim3(kv.B * kv.KVH), dim3(1024), 0, st, q, kv.H, kv.KVH, w, kv.D, part, ns, kv.B, cs);
+  if (e != cudaSuccess) return e;
   return launched(2);
 }
 
 cudaError_t launch_channel_prune(const float* cs, const uint16_t* K, const kvc_kv_desc& kv, int C,
                                  int zero_mode, int32_t* ch, uint16_t* Ko, cudaStream_t st) {
   const int rows = kv.B * kv.KVH;
-  k_channel_select<<<rows, 128, 0, st>>>(cs, kv.D, C, ch);
+  cudaError_t e = launch_pdl(k_channel_select, dim3(rows), dim3(128), 0, st, cs, kv.D, C, ch);
+  if (e != cudaSuccess) return e;
   const int per = (int)std::max<int64_t>(1, std::min<int64_t>((kv.S + 31) / 32, ((int64_t)num_sms() * 8 + rows - 1) / rows));
-  dim3 grid(per, rows);
-  if (zero_mode) {
-    if (kv.D == 64)
-      k_channel_zero<64><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, kv.KVH, ch, C, Ko);
-    else
-      k_channel_zero<128><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, kv.KVH, ch, C, Ko);
-  } else {
-    if (kv.D == 64)
-      k_channel_gather<64><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, kv.KVH, ch, C, Ko);
-    else
-      k_channel_gather<128><<<grid, 256, 0, st>>>(K, kv.stride_b, kv.stride_h, kv.stride_s, kv.S, kv.KVH, ch, C, Ko);
-  }
+  const dim3 grid(per, rows);
+  if (zero_mode)
+    e = kv.D == 64 ? launch_pdl(k_channel_zero<64>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
+                                kv.S, kv.KVH, ch, C, Ko)
+                   : launch_pdl(k_channel_zero<128>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
+                                kv.S, kv.KVH, ch, C, Ko);
+  else
+    e = kv.D == 64 ? launch_pdl(k_channel_gather<64>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
+                                kv.S, kv.KVH, ch, C, Ko)
+                   : launch_pdl(k_channel_gather<128>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h,
+                                kv.stride_s, kv.S, kv.KVH, ch, C, Ko);
+  if (e != cudaSuccess) return e;
   return launched(2);
 }
 

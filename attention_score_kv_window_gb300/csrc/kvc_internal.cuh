@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "kvc.h"
 
 namespace kvc {
@@ -34,7 +36,10 @@ cudaError_t take_status_scissorhands(unsigned int* v);
 // previous kernel on the stream has finished; each such kernel calls pdl_wait() before its
 // first global-memory access (it returns once the previous kernel has completed and its
 // writes are visible; it returns at once when there is nothing to wait for).  pdl_trigger()
-// lets the next kernel's launch begin once every CTA of this grid has called it or exited.
+// lets the next kernel's launch begin once every CTA of this grid has called it or exited;
+// kernels that do not call it release the next one when they exit.  Early triggers pay where
+// the next kernel's CTAs start on SMs this grid leaves free (top-k after scoring, compaction
+// after top-k); in chains of small kernels they only crowd the running grid.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
@@ -61,6 +66,15 @@ inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStr
   cfg.attrs = attrs;
   cfg.numAttrs = n;
   return cfg;
+}
+
+// Launch `kern` with programmatic stream serialisation (see pdl_config).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchAttribute attrs[2];
+  const cudaLaunchConfig_t cfg = pdl_config(grid, block, smem, st, attrs);
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // Once per kernel and device: prefer the largest shared-memory carveout (consecutive kernels

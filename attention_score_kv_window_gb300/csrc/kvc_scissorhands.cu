@@ -13,6 +13,7 @@ namespace kvc {
 namespace {
 
 __global__ void k_sh_init(kvc_sh_state s, int n_live) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   const int64_t rows = (int64_t)s.B * s.KVH;
   const int64_t nw = s.cap / 32;
   const int64_t n_hist = (int64_t)s.history * rows * nw;
@@ -41,6 +42,7 @@ template <int D>
 __global__ void k_sh_insert(kvc_sh_state s, const uint16_t* __restrict__ kn,
                             const uint16_t* __restrict__ vn, uint16_t* K, uint16_t* V, int64_t sb,
                             int64_t sh, int64_t ss) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (row >= s.B * s.KVH) return;
@@ -78,6 +80,7 @@ __global__ void k_sh_insert(kvc_sh_state s, const uint16_t* __restrict__ kn,
 
 // one CTA per (b,kvh): flags of step t into plane t % history, running low counts
 __global__ void __launch_bounds__(256) k_sh_record(kvc_sh_state s, const float* __restrict__ p) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   __shared__ uint32_t red[8];
   const int row = blockIdx.x;
   const int nw = s.cap / 32;
@@ -121,7 +124,8 @@ cudaError_t launch_sh_init(const kvc_sh_state& s, int n_live, cudaStream_t st) {
   const int64_t rows = (int64_t)s.B * s.KVH;
   const int64_t n = std::max<int64_t>((int64_t)s.history * rows * (s.cap / 32), rows * s.cap);
   const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 8));
-  k_sh_init<<<blocks, 256, 0, st>>>(s, n_live);
+  const cudaError_t e = launch_pdl(k_sh_init, dim3(blocks), dim3(256), 0, st, s, n_live);
+  if (e != cudaSuccess) return e;
   return launched(1);
 }
 
@@ -129,15 +133,19 @@ cudaError_t launch_sh_insert(const kvc_sh_state& s, const uint16_t* kn, const ui
                              uint16_t* K, uint16_t* V, const kvc_kv_desc& kv, cudaStream_t st) {
   const int rows = s.B * s.KVH;
   const int blocks = (rows + 7) / 8;
-  if (kv.D == 64)
-    k_sh_insert<64><<<blocks, 256, 0, st>>>(s, kn, vn, K, V, kv.stride_b, kv.stride_h, kv.stride_s);
-  else
-    k_sh_insert<128><<<blocks, 256, 0, st>>>(s, kn, vn, K, V, kv.stride_b, kv.stride_h, kv.stride_s);
+  const cudaError_t e =
+      kv.D == 64
+          ? launch_pdl(k_sh_insert<64>, dim3(blocks), dim3(256), 0, st, s, kn, vn, K, V, kv.stride_b, kv.stride_h,
+                       kv.stride_s)
+          : launch_pdl(k_sh_insert<128>, dim3(blocks), dim3(256), 0, st, s, kn, vn, K, V, kv.stride_b, kv.stride_h,
+                       kv.stride_s);
+  if (e != cudaSuccess) return e;
   return launched(1);
 }
 
 cudaError_t launch_sh_record(const kvc_sh_state& s, const float* p, cudaStream_t st) {
-  k_sh_record<<<s.B * s.KVH, 256, 0, st>>>(s, p);
+  const cudaError_t e = launch_pdl(k_sh_record, dim3(s.B * s.KVH), dim3(256), 0, st, s, p);
+  if (e != cudaSuccess) return e;
   return launched(1);
 }
 

@@ -104,6 +104,7 @@ __device__ __forceinline__ void load_q_rows(uint16_t* dst, const uint16_t* Qg, i
 // ----------------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(NTHREADS) k_scores_pass1(const ScoresArgs a) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int P = D + 8, KS = D / 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -306,6 +307,7 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass1(const ScoresArgs a) {
 // merge: per row, combine the key ranges' partials into one log2-domain normaliser
 // ----------------------------------------------------------------------------------------
 __global__ void k_scores_merge(const ScoresArgs a) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   const int bk = blockIdx.x;
   for (int r = threadIdx.x; r < a.Rpad; r += blockDim.x) a.mrow[(int64_t)bk * a.Rpad + r] = merge_row(a, bk, r);
 }
@@ -315,6 +317,7 @@ __global__ void k_scores_merge(const ScoresArgs a) {
 // ----------------------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(NTHREADS) k_scores_pass2(const ScoresArgs a) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int P = D + 8, KS = D / 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -445,6 +448,7 @@ __device__ __forceinline__ uint32_t cluster_addr_s(const void* local, int rank) 
 
 template <int D>
 __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a, int64_t per) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int P = D + 8, KS = D / 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
@@ -601,6 +605,7 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
 // all-heads reduction: mean over KV heads of the per-group scores, written to every kvh
 __global__ void k_scores_allheads(const float* __restrict__ grp, float* __restrict__ out, int B,
                                   int KVH, int64_t S) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   const int64_t n = (int64_t)B * S;
   const float inv = 1.f / (float)KVH;
   for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < n;
@@ -654,18 +659,9 @@ int small_cluster(const ScoresArgs& a, int64_t* per_out) {
 
 template <int D>
 cudaError_t launch_small(const ScoresArgs& a, int cs, int64_t per, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((int64_t)a.B * a.KVH * cs), 1, 1);
-  cfg.blockDim = dim3(NTHREADS, 1, 1);
-  cfg.dynamicSmemBytes = smem_small(D, a.R, per);
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaLaunchAttribute attrs[2];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((int64_t)a.B * a.KVH * cs)), dim3(NTHREADS),
+                                            smem_small(D, a.R, per), st, attrs, cs);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, k_scores_small<D>, a, per);
   if (e != cudaSuccess) return e;
   return launched(1);
@@ -687,17 +683,21 @@ cudaError_t launch_impl(const ScoresArgs& a, int reduce, float* scores, cudaStre
     const int n_rg = (a.Rpad + P1_MAX_ROWS - 1) / P1_MAX_ROWS;
     const int rows1 = std::min(P1_MAX_ROWS, a.Rpad);
     dim3 g1(a.nsplit, a.KVH * n_rg, a.B);
-    k_scores_pass1<D><<<g1, NTHREADS, smem_pass1(D, rows1), st>>>(a);
-    k_scores_merge<<<a.B * a.KVH, 256, 0, st>>>(a);
-    dim3 g2(a.nsplit, a.KVH, a.B);
-    k_scores_pass2<D><<<g2, NTHREADS, smem_pass2(D, a.Rpad), st>>>(a);
+    e = launch_pdl(k_scores_pass1<D>, g1, dim3(NTHREADS), smem_pass1(D, rows1), st, a);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(k_scores_merge, dim3(a.B * a.KVH), dim3(256), 0, st, a);
+    if (e != cudaSuccess) return e;
+    const dim3 g2(a.nsplit, a.KVH, a.B);
+    e = launch_pdl(k_scores_pass2<D>, g2, dim3(NTHREADS), smem_pass2(D, a.Rpad), st, a);
+    if (e != cudaSuccess) return e;
     e = launched(3);
     if (e != cudaSuccess) return e;
   }
   if (reduce == KVC_REDUCE_ALL_HEADS) {
     const int64_t n = (int64_t)a.B * a.S;
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 8);
-    k_scores_allheads<<<blocks, 256, 0, st>>>(a.out, scores, a.B, a.KVH, a.S);
+    e = launch_pdl(k_scores_allheads, dim3(blocks), dim3(256), 0, st, (const float*)a.out, scores, a.B, a.KVH, a.S);
+    if (e != cudaSuccess) return e;
     return launched(1);
   }
   return cudaGetLastError();

@@ -563,6 +563,7 @@ __device__ __forceinline__ float pass2_chunk(const Ctx& c, int buf, uint32_t tad
 template <int D, int NHALF, int NQ, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     k_scores_tc(const ScoresArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ) {
+  pdl_wait();  // previous kernel on the stream complete and visible
   using L = Layout<D>;
   constexpr int KS = D / 16;
   constexpr bool P1 = (MODE & 1) != 0, P2 = (MODE & 2) != 0;
@@ -726,7 +727,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         warp_wait_tags(tags, a.nsplit, tag, c.abort_flag);
       }
       named_sync_epilogue();
-      pdl_trigger();  // the next kernel may start launching; it waits for this grid's end
+      pdl_trigger();  // the next kernel may begin launching; it waits for this grid's end
     }
     if constexpr (P2) {
       float* ncr = reinterpret_cast<float*>(c.base + L::CR);
@@ -870,7 +871,8 @@ cudaError_t run_tc(const ScoresArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const dim3 grid(a.nsplit, a.KVH, a.B);
   if constexpr (MODE != 3) {
-    kern<<<grid, THREADS, smem, st>>>(a, m->k, MODE == 2 ? m->q2 : m->q1);
+    e = launch_pdl(kern, grid, dim3(THREADS), smem, st, a, m->k, MODE == 2 ? m->q2 : m->q1);
+    if (e != cudaSuccess) return e;
   } else {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
