@@ -9,7 +9,9 @@
  * Conventions (every call):
  *  - Pointers named K, V, q_*, scores, idx, ... are DEVICE pointers owned by the caller.
  *    The library never allocates or frees device memory: callers size scratch buffers with
- *    kvc_workspace_size() and pass them as (ws, ws_bytes).
+ *    kvc_workspace_size() and pass them as (ws, ws_bytes).  A workspace needs no initial
+ *    content (some calls keep bookkeeping words in it that accept any prior bytes); calls
+ *    that may run at the same time on the GPU must not share one.
  *  - bf16 tensors are passed as kvc_bf16 (the raw 16-bit pattern).  Scores are float32,
  *    indices int32.  Unless stated otherwise tensors are dense row-major with the shape in
  *    the comment; K/V caches are described by kvc_kv_desc and may be strided.
