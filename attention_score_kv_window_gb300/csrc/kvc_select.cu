@@ -4,8 +4,8 @@
 //
 // A row is split over a thread-block cluster of up to 8 CTAs (1024 threads each); each CTA
 // loads its slice of keys into shared memory once.  An MSB-first radix select (digits of
-// 11, 11 and 10 bits) builds shared-memory histograms with warp-aggregated atomics; each CTA
-// then adds its nonzero bins into every peer's copy of the cluster histogram with remote
+// 11, 11 and 10 bits) builds shared-memory histograms with shared atomics; each CTA then
+// adds its nonzero bins into every peer's copy of the cluster histogram with remote
 // reductions (pushes do not stall; remote loads would), and after one cluster barrier each
 // CTA finds the digit holding the k-th item locally with one block scan.  This yields the
 // k-th key T and how many keys equal to T are taken.  The output pass counts, per warp and
@@ -87,33 +87,6 @@ struct __align__(16) SelShared {
   uint32_t prefix, remaining, eq_total;
 };
 
-// inclusive block scan of one value per thread (1024 threads); returns inclusive, total in *tot
-__device__ __forceinline__ uint32_t block_scan(uint32_t v, uint32_t* warp_buf, uint32_t* tot) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) warp_buf[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t w = warp_buf[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    warp_buf[lane] = w;
-  }
-  __syncthreads();
-  const uint32_t base = warp ? warp_buf[warp - 1] : 0u;
-  *tot = warp_buf[31];
-  __syncthreads();
-  return base + x;
-}
-
 // Writes into the shared memory of CTA `rank` of the cluster.  They do not stall the issuing
 // thread; the next cluster barrier (release/acquire) makes them visible.
 __device__ __forceinline__ uint32_t cluster_addr(const void* local, int rank) {
@@ -135,27 +108,48 @@ __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
 
-// Add this CTA's nonzero bins into hsum[pass] of every CTA of the cluster.
+// Add this CTA's nonzero bins into hsum[pass] of every CTA of the cluster, and clear the
+// local histogram for the next digit (the next use follows a block barrier).
 __device__ __forceinline__ void push_bins(SelShared& sh, int pass, uint32_t nbins, int cs) {
   for (uint32_t b = threadIdx.x; b < nbins; b += SEL_THREADS) {
     const uint32_t v = sh.hist[b];
     if (v) {
       for (int r = 0; r < cs; ++r) push_add(&sh.hsum[pass][b], r, v);
+      sh.hist[b] = 0u;
     }
   }
 }
+// Histogram one digit per lane (0xffffffff: no item).  A plain shared atomic per item: the
+// hardware serialises equal addresses within a warp more cheaply than grouping the lanes
+// with match.any first.
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t d, int) {
+  if (d != 0xffffffffu) atomicAdd(&hist[d], 1u);
+}
 
-// Digit holding the rem-th largest item, from the cluster-summed bins of `pass` (local):
-// one block scan over the bins in descending order; the thread whose bins contain it
-// publishes the new prefix, remainder and tie count.
+// Digit holding the rem-th largest item, from the cluster-summed bins of `pass` (local).
+// Thread t takes bins in descending order (bpt = 1 or 2 per thread); one warp scan, warp
+// totals through shared memory, and each thread adds the totals of the warps before it
+// (two block barriers).  The thread whose bins contain the item publishes the new prefix,
+// remainder and tie count.
 __device__ __forceinline__ void find_digit(SelShared& sh, int pass, uint32_t nbins, int shift, uint32_t prefix,
                                            uint32_t rem) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t bpt = nbins >> 10;  // 2 or 1 bins per thread
   uint32_t hb[2] = {0u, 0u};
   for (uint32_t q = 0; q < bpt; ++q) hb[q] = sh.hsum[pass][nbins - 1u - (threadIdx.x * bpt + q)];
   const uint32_t hs = hb[0] + hb[1];
-  uint32_t tot;
-  const uint32_t incl = block_scan(hs, sh.warp_a, &tot);
+  uint32_t x = hs;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh.warp_a[warp] = x;
+  __syncthreads();
+  uint32_t before = lane < warp ? sh.warp_a[lane] : 0u;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+  const uint32_t incl = before + x;
   const uint32_t excl = incl - hs;
   if (excl < rem && rem <= incl) {
     uint32_t run = excl;
@@ -235,8 +229,7 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
       }
       cf += __popc(__ballot_sync(0xffffffffu, f));
       ce += __popc(__ballot_sync(0xffffffffu, e));
-      const uint32_t peers = __match_any_sync(0xffffffffu, d);
-      if (d != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (uint32_t)__popc(peers));
+      hist_add(sh.hist, d, lane);
     }
   }
   const uint4 tot0 = cta_totals(sh, cf, ce, lane, warp);
@@ -262,8 +255,7 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
     for (int pass = 1; pass < 3; ++pass) {
       const int shift = pass == 1 ? 10 : 0;
       const uint32_t nbins = pass == 1 ? 2048u : 1024u;
-      for (uint32_t i = tid; i < nbins; i += SEL_THREADS) sh.hist[i] = 0u;
-      __syncthreads();
+      // the local histogram was cleared by the previous push (find_digit ended with a barrier)
       for (int64_t j0 = 0; j0 < len; j0 += SEL_THREADS) {
         const int64_t jl = j0 + tid;
         uint32_t d = 0xffffffffu;
@@ -271,8 +263,7 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
           const uint32_t key = kc[jl];
           if ((key & hi_mask) == prefix) d = (key >> shift) & (nbins - 1u);
         }
-        const uint32_t peers = __match_any_sync(0xffffffffu, d);
-        if (d != 0xffffffffu && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (uint32_t)__popc(peers));
+        hist_add(sh.hist, d, lane);
       }
       __syncthreads();
       push_bins(sh, pass, nbins, cs);
@@ -289,10 +280,13 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
   // keys equal to T: the first take_eq in index order when keeping, the last when evicting
   const uint32_t skip_eq = evict_order ? (eq_total - take_eq) : 0u;
 
-  // 3. output, ascending
+  // 3. output, ascending.  The count pass keeps each 32-item group's two ballots in the digit
+  // histograms of passes 0 and 1 (no peer writes them any more): 4096 words, 64 groups per warp.
+  uint32_t* ballots = &sh.hsum[0][0];
+  const int n_grp = (int)((w1 - w0 + 31) / 32);  // <= ceil(SLICE_MAX / 1024) = 40
   uint32_t cd = 0, cq = 0;
-  for (int64_t base = w0; base < w1; base += 32) {
-    const int64_t j = base + lane;
+  for (int it = 0; it < n_grp; ++it) {
+    const int64_t j = w0 + (int64_t)it * 32 + lane;
     bool def = false, eq = false;
     if (j < w1) {
       if (fn.forced(j)) def = true;
@@ -305,8 +299,13 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
         }
       }
     }
-    cd += __popc(__ballot_sync(0xffffffffu, def));
-    cq += __popc(__ballot_sync(0xffffffffu, eq));
+    const uint32_t bd = __ballot_sync(0xffffffffu, def), be = __ballot_sync(0xffffffffu, eq);
+    if (lane == 0) {
+      ballots[(warp * 64 + it) * 2] = bd;
+      ballots[(warp * 64 + it) * 2 + 1] = be;
+    }
+    cd += __popc(bd);
+    cq += __popc(be);
   }
   uint4 tot1 = cta_totals(sh, cd, cq, lane, warp);
   if (tid == 0) {
@@ -327,22 +326,10 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
     d_run += sh.warp_a[q];
     e_run += sh.warp_b[q];
   }
-  for (int64_t base = w0; base < w1; base += 32) {
-    const int64_t j = base + lane;
-    bool def = false, eq = false;
-    if (j < w1) {
-      if (fn.forced(j)) def = true;
-      else if (fn.eligible(j)) {
-        if (take_all) def = true;
-        else if (split_ties) {
-          const uint32_t key = kc[j - c0];
-          def = key > T;
-          eq = key == T;
-        }
-      }
-    }
-    const uint32_t bd = __ballot_sync(0xffffffffu, def);
-    const uint32_t be = __ballot_sync(0xffffffffu, eq);
+  for (int it = 0; it < n_grp; ++it) {
+    const int64_t j = w0 + (int64_t)it * 32 + lane;
+    const uint32_t bd = ballots[(warp * 64 + it) * 2], be = ballots[(warp * 64 + it) * 2 + 1];
+    const bool def = (bd >> lane) & 1u, eq = (be >> lane) & 1u;
     const uint32_t eb = e_run + __popc(be & lower);  // keys equal to T before j
     const bool take = def || (eq && eb >= skip_eq && eb < skip_eq + take_eq);
     if (take) {
