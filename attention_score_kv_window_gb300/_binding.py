@@ -59,6 +59,7 @@ _SIGNATURES = {
     "kvc_window_scores_noalloc": (_I32, [_P, _P, _DESC, _I32, _F, _I32, _P, _I32, _P, _P]),
     "kvc_topk_select": (_I32, [_P, _I32, _I32, _I64, _I32, _I32, _P, _I32, _P, _P, _SZ, _P]),
     "kvc_compact_kv": (_I32, [_P, _P, _DESC, _P, _I32, _P, _P, _P]),
+    "kvc_topk_compact": (_I32, [_P, _P, _P, _DESC, _I32, _I32, _P, _I32, _P, _P, _P, _P]),
     "kvc_compress_prefill": (_I32, [_P, _P, _P, _DESC, _I32, _F, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "kvc_write_slots": (_I32, [_P, _P, _P, _P, _P, _DESC, _P]),
     "kvc_tova_decode_step": (_I32, [_P, _P, _P, _P, _P, _DESC, _F, _P, _P, _P, _SZ, _P]),
@@ -214,6 +215,31 @@ def kvc_compact_kv(K, V, idx, H=None, K_out=None, V_out=None, stream=None):
     _check(lib.kvc_compact_kv(_ptr(K), _ptr(V), ctypes.byref(desc), _ptr(idx.contiguous()), k, _ptr(K_out),
                               _ptr(V_out), _stream(stream)))
     return K_out, V_out
+
+
+def kvc_topk_compact(scores, K, V, k, protect_tail=0, live_mask=None, largest=True, H=None, idx=None,
+                     K_out=None, V_out=None, stream=None):
+    """Top-k of each scores row and the gather of the chosen K/V rows; returns (idx, K_out, V_out)."""
+    lib = load_library()
+    if scores.dtype != torch.float32:
+        raise TypeError("scores must be float32")
+    B, KVH, S, D = K.shape
+    desc = kv_desc(K, H or KVH)
+    if V is not None and (V.shape != K.shape or V.stride() != K.stride()):
+        raise ValueError("V must have K's shape and strides")
+    if idx is None:
+        idx = torch.empty((B, KVH, k), dtype=torch.int32, device=K.device)
+    if K_out is None:
+        K_out = torch.empty((B, KVH, k, D), dtype=K.dtype, device=K.device)
+    if V is not None and V_out is None:
+        V_out = torch.empty((B, KVH, k, D), dtype=V.dtype, device=V.device)
+    _dense(K_out, (B, KVH, k, D), "K_out")
+    if V_out is not None:
+        _dense(V_out, (B, KVH, k, D), "V_out")
+    _check(lib.kvc_topk_compact(_ptr(scores.contiguous()), _ptr(K), _ptr(V), ctypes.byref(desc), int(k),
+                                int(protect_tail), _ptr(live_mask), int(bool(largest)), _ptr(idx), _ptr(K_out),
+                                _ptr(V_out), _stream(stream)))
+    return idx, K_out, V_out
 
 
 def kvc_compress_prefill(q_win, K, V, scale, k, protect_tail=0, reduce="gqa", out=None, ws=None,

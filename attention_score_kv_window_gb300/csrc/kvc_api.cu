@@ -246,14 +246,14 @@ kvc_status kvc_topk_select(const float* scores, int32_t B, int32_t KVH, int64_t 
                      "kvc_topk_select launch");
 }
 
-kvc_status kvc_compact_kv(const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_desc* kv,
-                          const int32_t* idx, int32_t k, kvc_bf16* K_out, kvc_bf16* V_out,
-                          kvc_stream_t stream) {
-  KVC_TRY(check_desc(kv, "kvc_compact_kv"));
-  if (k < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_compact_kv: k must be >= 1");
+namespace {
+// K/V, the dense outputs K_out/V_out [B,KVH,k,D] and their overlaps, for the gathers
+kvc_status check_gather(const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_desc* kv, int32_t k,
+                        const kvc_bf16* K_out, const kvc_bf16* V_out, const char* who) {
+  KVC_TRY(check_desc(kv, who));
+  if (k < 1) return fail(KVC_ERR_INVALID_ARG, "%s: k must be >= 1", who);
   KVC_TRY(check_ptr(K, "K"));
   KVC_TRY(check_ptr(K_out, "K_out"));
-  if (!idx) return fail(KVC_ERR_INVALID_ARG, "idx is NULL");
   if ((V == nullptr) != (V_out == nullptr)) return fail(KVC_ERR_INVALID_ARG, "V and V_out must both be given or both NULL");
   if (V) {
     KVC_TRY(check_ptr(V, "V"));
@@ -266,8 +266,47 @@ kvc_status kvc_compact_kv(const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_des
   const uintptr_t ko = reinterpret_cast<uintptr_t>(K_out), vo = reinterpret_cast<uintptr_t>(V_out);
   if (overlaps(ko, ko + osz, k0, k1) || (V && (overlaps(ko, ko + osz, v0, v1) || overlaps(vo, vo + osz, k0, k1) ||
                                                overlaps(vo, vo + osz, v0, v1) || overlaps(ko, ko + osz, vo, vo + osz))))
-    return fail(KVC_ERR_INVALID_ARG, "kvc_compact_kv: outputs overlap inputs");
+    return fail(KVC_ERR_INVALID_ARG, "%s: outputs overlap inputs", who);
+  return KVC_OK;
+}
+}  // namespace
+
+kvc_status kvc_compact_kv(const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_desc* kv,
+                          const int32_t* idx, int32_t k, kvc_bf16* K_out, kvc_bf16* V_out,
+                          kvc_stream_t stream) {
+  KVC_TRY(check_gather(K, V, kv, k, K_out, V_out, "kvc_compact_kv"));
+  if (!idx) return fail(KVC_ERR_INVALID_ARG, "idx is NULL");
   return cuda_status(launch_compact(K, V, *kv, idx, k, K_out, V_out, (cudaStream_t)stream), "kvc_compact_kv launch");
+}
+
+kvc_status kvc_topk_compact(const float* scores, const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_desc* kv,
+                            int32_t k, int32_t protect_tail, const uint32_t* live_mask, int32_t largest,
+                            int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out, kvc_stream_t stream) {
+  KVC_TRY(check_gather(K, V, kv, k, K_out, V_out, "kvc_topk_compact"));
+  if (kv->S > topk_max_len()) return fail(KVC_ERR_UNSUPPORTED, "kvc_topk_compact: S > %lld", (long long)topk_max_len());
+  if ((int64_t)kv->B * kv->KVH > 2147483647LL) return fail(KVC_ERR_UNSUPPORTED, "kvc_topk_compact: too many rows");
+  if (protect_tail < 0 || protect_tail > k || (int64_t)protect_tail > kv->S)
+    return fail(KVC_ERR_INVALID_ARG, "kvc_topk_compact: need 0 <= protect_tail <= min(k, S)");
+  if (protect_tail && !largest) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_compact: protect_tail needs largest=1");
+  KVC_TRY(check_ptr(scores, "scores"));
+  if (!idx) return fail(KVC_ERR_INVALID_ARG, "idx is NULL");
+  if (live_mask && !aligned16(live_mask)) return fail(KVC_ERR_INVALID_ARG, "live_mask not 16-byte aligned");
+  // the kernel writes K_out/V_out while other rows are still being selected: no output may
+  // overlap the scores
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(scores), s1 = s0 + (uintptr_t)kv->B * kv->KVH * kv->S * 4;
+  const uintptr_t osz = (uintptr_t)kv->B * kv->KVH * (uintptr_t)k * kv->D * 2;
+  const uintptr_t ko = reinterpret_cast<uintptr_t>(K_out), vo = reinterpret_cast<uintptr_t>(V_out);
+  const uintptr_t i0 = reinterpret_cast<uintptr_t>(idx), i1 = i0 + (uintptr_t)kv->B * kv->KVH * k * 4;
+  if (overlaps(ko, ko + osz, s0, s1) || (V_out && overlaps(vo, vo + osz, s0, s1)) || overlaps(i0, i1, s0, s1) ||
+      overlaps(i0, i1, ko, ko + osz) || (V_out && overlaps(i0, i1, vo, vo + osz)))
+    return fail(KVC_ERR_INVALID_ARG, "kvc_topk_compact: outputs overlap inputs or each other");
+  // two launches chained by programmatic dependent launch: the gather then runs on every SM
+  // (a gather inside the selection grid, on its B*KVH*8 CTAs, measured slower)
+  KVC_TRY(cuda_status(launch_topk(scores, kv->B, kv->KVH, kv->S, k, protect_tail, live_mask, largest ? 1 : 0, idx,
+                                  (cudaStream_t)stream),
+                      "kvc_topk_compact selection launch"));
+  return cuda_status(launch_compact(K, V, *kv, idx, k, K_out, V_out, (cudaStream_t)stream),
+                     "kvc_topk_compact gather launch");
 }
 
 kvc_status kvc_compress_prefill(const kvc_bf16* q_win, const kvc_bf16* K, const kvc_bf16* V,
@@ -280,8 +319,7 @@ kvc_status kvc_compress_prefill(const kvc_bf16* q_win, const kvc_bf16* K, const 
   if (protect_tail < 0 || protect_tail > k || protect_tail > w)
     return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill: need 0 <= protect_tail <= min(k, w)");
   KVC_TRY(kvc_window_scores(q_win, K, kv, w, scale, 1, nullptr, reduce, scores, ws, ws_bytes, stream));
-  KVC_TRY(kvc_topk_select(scores, kv->B, kv->KVH, kv->S, k, protect_tail, nullptr, 1, idx, nullptr, 0, stream));
-  return kvc_compact_kv(K, V, kv, idx, k, K_out, V_out, stream);
+  return kvc_topk_compact(scores, K, V, kv, k, protect_tail, nullptr, 1, idx, K_out, V_out, stream);
 }
 
 kvc_status kvc_write_slots(const kvc_bf16* k_new, const kvc_bf16* v_new, const int32_t* slot,

@@ -186,7 +186,7 @@ __device__ __forceinline__ uint4 cta_totals(SelShared& sh, uint32_t a, uint32_t 
 
 template <class Fn>
 __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_t* kc, SelShared& sh,
-                           bool evict_order) {
+                               bool evict_order) {
   const int cs = (int)cg::this_cluster().num_blocks();
   const int cr = (int)cg::this_cluster().block_rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -322,6 +322,7 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
     }
     d_total += a;
   }
+
   for (int q = 0; q < warp; ++q) {
     d_run += sh.warp_a[q];
     e_run += sh.warp_b[q];
@@ -562,18 +563,12 @@ cudaError_t launch_topk(const float* scores, int B, int KVH, int64_t S, int k, i
   const int64_t per_cta = ((S + (int64_t)cs * 32 - 1) / ((int64_t)cs * 32)) * 32;
   if (per_cta > SLICE_MAX) return cudaErrorInvalidValue;
   const size_t smem = (size_t)per_cta * 4;
-  static bool attr_done[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(SLICE_MAX * 4));
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = true;
-  }
+  cudaError_t e = func_attrs_once(reinterpret_cast<const void*>(k_topk), (int)(SLICE_MAX * 4));
+  if (e != cudaSuccess) return e;
   cudaLaunchAttribute attrs[2];
   const cudaLaunchConfig_t cfg =
       pdl_config(dim3((unsigned)((int64_t)B * KVH * cs)), dim3(SEL_THREADS), smem, st, attrs, cs);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_topk, scores, S, k, protect_tail, live, largest, idx);
+  e = cudaLaunchKernelEx(&cfg, k_topk, scores, S, k, protect_tail, live, largest, idx);
   if (e != cudaSuccess) return e;
   return launched(1);
 }

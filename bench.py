@@ -272,8 +272,7 @@ class PrefillCase:
         self.calls = [
             Call("window_scores", self._scores, sc_bytes, sc_flops, "tensor" if big_w else "hbm", SCORE_SOURCES,
                  f"window_scores/{wl.name}/B{B}"),
-            Call("topk", self._topk, B * KVH * S * 4 + B * KVH * k * 4),
-            Call("compact", self._compact, 4 * B * KVH * k * D * 2 + B * KVH * k * 4),
+            Call("topk_compact", self._topk_compact, B * KVH * S * 4 + 4 * B * KVH * k * D * 2 + B * KVH * k * 4),
         ]
         if wl.C:
             C = wl.C
@@ -288,14 +287,11 @@ class PrefillCase:
         self.kvc.kvc_window_scores(q, K, self.wl.scale, causal=True, reduce=self.wl.reduce,
                                    scores=self.outs[i % self.R][0], ws=self.ws)
 
-    def _topk(self, i):
-        sc, idx, _, _ = self.outs[i % self.R]
-        self.kvc.kvc_topk_select(sc, self.k, protect_tail=self.wl.protect_tail, idx=idx)
-
-    def _compact(self, i):
+    def _topk_compact(self, i):
         q, K, V = self.reps[i % self.R]
-        _, idx, Ko, Vo = self.outs[i % self.R]
-        self.kvc.kvc_compact_kv(K, V, idx, H=self.wl.H, K_out=Ko, V_out=Vo)
+        sc, idx, Ko, Vo = self.outs[i % self.R]
+        self.kvc.kvc_topk_compact(sc, K, V, self.k, protect_tail=self.wl.protect_tail, H=self.wl.H, idx=idx,
+                                  K_out=Ko, V_out=Vo)
 
     def _cscore(self, i):
         q, _, _ = self.reps[i % self.R]

@@ -160,6 +160,18 @@ kvc_status kvc_compact_kv(const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_des
                           kvc_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * kvc_topk_compact — kvc_topk_select followed by kvc_compact_kv of the chosen rows, in one
+ * call (two kernels; the gather starts as the selection ends).
+ *   Arguments as in those two calls: scores [B,KVH,S] float32; K/V described by kv (V may be
+ *   NULL, then V_out too); idx [B,KVH,k] int32 out; K_out/V_out [B,KVH,k,D] dense bf16 out,
+ *   zero rows where idx is -1.  No output may overlap scores, K, V or another output.
+ * ------------------------------------------------------------------------------------- */
+kvc_status kvc_topk_compact(const float* scores, const kvc_bf16* K, const kvc_bf16* V,
+                            const kvc_kv_desc* kv, int32_t k, int32_t protect_tail,
+                            const uint32_t* live_mask, int32_t largest, int32_t* idx,
+                            kvc_bf16* K_out, kvc_bf16* V_out, kvc_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * kvc_compress_prefill — window scores, top-k and compaction in one call (the press applied
  * after the prefill attention of one layer; "Add TOVA press" / cold-compress SnapKV).
  *   scores [B,KVH,S] out (kept for inspection), idx [B,KVH,k] out, K_out/V_out [B,KVH,k,D] out.

@@ -184,6 +184,48 @@ def test_compact_bit_exact(D):
     np.testing.assert_array_equal(host_bits(Vo), Vr)
 
 
+TOPK_COMPACT_CASES = [
+    # B, KVH, S, k, protect, D, ties, largest, live_p, with_v, strided
+    (1, 8, 32768, 4096, 64, 128, 0, True, None, True, False),   # SnapKV layer, full size
+    (2, 3, 10000, 777, 0, 64, 5, True, None, True, True),       # heavy ties, strided cache
+    (1, 2, 5000, 6000, 0, 128, 0, True, None, True, False),     # k > S: -1 padding, zero rows
+    (2, 2, 3000, 100, 0, 64, 0, True, None, True, False),       # short rows: two launches
+    (1, 4, 20000, 1500, 0, 128, 0, False, None, False, False),  # evict order, keys only
+    (1, 2, 12000, 500, 0, 128, 0, True, 0.5, True, False),      # live mask
+    (1, 2, 12000, 9000, 0, 64, 0, True, 0.5, True, False),      # fewer live than k
+]
+
+
+@pytest.mark.parametrize("B,KVH,S,k,protect,D,ties,largest,live_p,with_v,strided", TOPK_COMPACT_CASES)
+def test_topk_compact_exact(B, KVH, S, k, protect, D, ties, largest, live_p, with_v, strided):
+    """Selection and gather in one call: indices equal the oracle's on the same fp32 scores,
+    gathered rows bit-exact, zero rows where the index is -1."""
+    sc = random_scores((B, KVH, S), 300 + S + k, tie_levels=ties)
+    live = None if live_p is None else random_live_mask((B, KVH, S), 12, live_p)
+    K = normal_bf16((B, KVH, S, D), 31, 1)
+    V = normal_bf16((B, KVH, S, D), 31, 2)
+    if strided:
+        big = torch.zeros((B, KVH, S + 5, D), dtype=torch.bfloat16, device="cuda")
+        big[:, :, :S] = dev_bf16(K)
+        bigv = torch.zeros_like(big)
+        bigv[:, :, :S] = dev_bf16(V)
+        Kd, Vd = big[:, :, :S], bigv[:, :, :S]
+    else:
+        Kd, Vd = dev_bf16(K), dev_bf16(V)
+    idx, Ko, Vo = kvc.kvc_topk_compact(torch.from_numpy(sc).cuda(), Kd, Vd if with_v else None, k,
+                                       protect_tail=protect, largest=largest,
+                                       live_mask=None if live is None else dev_u32(pack_live_bits(live)))
+    ref = O.topk_select(sc, k, protect_tail=protect, live=live, largest=largest)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref)
+    Kr, Vr = O.compact_kv(K, V, ref)
+    np.testing.assert_array_equal(host_bits(Ko), Kr)
+    if with_v:
+        np.testing.assert_array_equal(host_bits(Vo), Vr)
+    else:
+        assert Vo is None
+    assert kvc.kvc_get_device_status() == kvc.KVC_OK
+
+
 def test_compact_out_of_range_index_reports_bounds():
     K = dev_bf16(normal_bf16((1, 1, 10, 64), 1, 1))
     idx = dev_i32(np.array([[[0, 10, 3]]]))

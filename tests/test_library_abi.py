@@ -78,6 +78,12 @@ def test_host_validation_without_gpu(lib):
     # compaction outputs overlapping the inputs
     assert lib.kvc_compact_kv(FAKE, None, ctypes.byref(d), FAKE, 4, FAKE + 256, None, None) \
         == kvc.KVC_ERR_INVALID_ARG
+    # fused selection + gather: idx overlapping the scores, and protect_tail in evict order
+    big = FAKE * 64
+    assert lib.kvc_topk_compact(big, FAKE, None, ctypes.byref(d), 4, 0, None, 1, big, FAKE * 128, None, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_topk_compact(big, FAKE, None, ctypes.byref(d), 4, 2, None, 0, FAKE * 256, FAKE * 128, None,
+                                None) == kvc.KVC_ERR_INVALID_ARG
     # channel prune: compact mode needs C % 8 == 0
     assert lib.kvc_channel_prune(FAKE, FAKE, ctypes.byref(d), 12, 0, FAKE, FAKE * 64, None) \
         == kvc.KVC_ERR_UNSUPPORTED
