@@ -90,6 +90,7 @@ kvc_status check_sh(const kvc_sh_state* st) {
     return fail(KVC_ERR_INVALID_ARG, "scissorhands: B, KVH >= 1 and cap a positive multiple of 32");
   if (st->history < 1 || st->history > 4096) return fail(KVC_ERR_INVALID_ARG, "scissorhands: history in [1, 4096]");
   if (st->cap > 40960) return fail(KVC_ERR_UNSUPPORTED, "scissorhands: cap must be <= 40960");
+  if ((int64_t)st->B * st->KVH > 65535) return fail(KVC_ERR_UNSUPPORTED, "scissorhands: B * KVH must be <= 65535");
   if (!st->hist || !st->low_count || !st->insert_step || !st->live || !st->slot)
     return fail(KVC_ERR_INVALID_ARG, "scissorhands: a state buffer is NULL");
   if (st->t < 0 || st->t > INT32_MAX) return fail(KVC_ERR_INVALID_ARG, "scissorhands: step counter out of range");

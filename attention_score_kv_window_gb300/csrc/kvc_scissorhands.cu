@@ -78,11 +78,12 @@ __global__ void k_sh_insert(kvc_sh_state s, const uint16_t* __restrict__ kn,
   }
 }
 
-// one CTA per (b,kvh): flags of step t into plane t % history, running low counts
+// CTA (x, row) flags slots [256x, 256x + 256) of (b,kvh) row `row` for step t into plane
+// t % history and updates their low counts; each CTA counts the row's live keys itself.
 __global__ void __launch_bounds__(256) k_sh_record(kvc_sh_state s, const float* __restrict__ p) {
   pdl_wait();  // previous kernel on the stream complete and visible
   __shared__ uint32_t red[8];
-  const int row = blockIdx.x;
+  const int row = blockIdx.y;
   const int nw = s.cap / 32;
   const uint32_t* lw = s.live + (int64_t)row * nw;
   uint32_t cnt = 0;
@@ -95,27 +96,24 @@ __global__ void __launch_bounds__(256) k_sh_record(kvc_sh_state s, const float* 
   for (int q = 0; q < (int)(blockDim.x >> 5); ++q) keys += red[q];
   // threshold: float32(1) / float32(keys), correctly rounded
   const float thr = __fdiv_rn(1.0f, (float)(keys > 0 ? keys : 1));
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= s.cap) return;  // cap % 32 == 0: whole warps leave together
   const int64_t plane = s.t % s.history;
   uint32_t* hp = s.hist + (plane * s.B * s.KVH + row) * (int64_t)nw;
-  const float* pr = p + (int64_t)row * s.cap;
-  uint16_t* low = s.low_count + (int64_t)row * s.cap;
-  const int32_t* ins = s.insert_step + (int64_t)row * s.cap;
-  const int lane = threadIdx.x & 31;
-  for (int j = threadIdx.x; j < s.cap; j += blockDim.x) {  // cap % 32 == 0: whole warps per word
-    const int wi = j >> 5;
-    const uint32_t lword = lw[wi];
-    const bool live = (lword >> lane) & 1u;
-    const bool flag = live && (pr[j] < thr);
-    const uint32_t bits = __ballot_sync(0xffffffffu, flag);
-    const uint32_t old = hp[wi];
-    if (live) {
-      const bool old_valid = (s.t - (int64_t)ins[j]) >= (int64_t)s.history;
-      const int oldbit = (old_valid && ((old >> lane) & 1u)) ? 1 : 0;
-      low[j] = (uint16_t)((int)low[j] + (flag ? 1 : 0) - oldbit);
-    }
-    __syncwarp();
-    if (lane == 0) hp[wi] = bits;
+  const int64_t x = (int64_t)row * s.cap + j;
+  const int lane = threadIdx.x & 31, wi = j >> 5;
+  const uint32_t lword = lw[wi];
+  const bool live = (lword >> lane) & 1u;
+  const bool flag = live && (p[x] < thr);
+  const uint32_t bits = __ballot_sync(0xffffffffu, flag);
+  const uint32_t old = hp[wi];
+  if (live) {
+    const bool old_valid = (s.t - (int64_t)s.insert_step[x]) >= (int64_t)s.history;
+    const int oldbit = (old_valid && ((old >> lane) & 1u)) ? 1 : 0;
+    s.low_count[x] = (uint16_t)((int)s.low_count[x] + (flag ? 1 : 0) - oldbit);
   }
+  __syncwarp();
+  if (lane == 0) hp[wi] = bits;
 }
 
 }  // namespace
@@ -144,7 +142,7 @@ cudaError_t launch_sh_insert(const kvc_sh_state& s, const uint16_t* kn, const ui
 }
 
 cudaError_t launch_sh_record(const kvc_sh_state& s, const float* p, cudaStream_t st) {
-  const cudaError_t e = launch_pdl(k_sh_record, dim3(s.B * s.KVH), dim3(256), 0, st, s, p);
+  const cudaError_t e = launch_pdl(k_sh_record, dim3((s.cap + 255) / 256, s.B * s.KVH), dim3(256), 0, st, s, p);
   if (e != cudaSuccess) return e;
   return launched(1);
 }

@@ -538,6 +538,47 @@ __global__ void __launch_bounds__(SHORT_THREADS) k_topk_short(const float* __res
   for (int p = (int)total + tid; p < k; p += SHORT_THREADS) out[p] = -1;
 }
 
+// k = 1 without a protected tail (a TOVA decode step evicts one slot per row): one 256-thread
+// CTA per row takes the maximum of the same (key, tie) composites as k_topk_short, so the
+// ranking is identical; -1 when nothing is eligible.  Finite scores give keys >= 1, so every
+// eligible composite is above the empty value 0.
+__global__ void __launch_bounds__(SHORT_THREADS) k_top1(const float* __restrict__ scores, int64_t S,
+                                                        const uint32_t* __restrict__ live, int largest,
+                                                        int32_t* __restrict__ idx) {
+  __shared__ uint64_t wbest[SHORT_THREADS / 32];
+  pdl_wait();
+  pdl_trigger();
+  const int64_t row = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  ScoreKeys fn;
+  fn.row = scores + row * S;
+  fn.lw = live ? live + row * ((S + 31) / 32) : nullptr;
+  fn.S = S;
+  fn.protect = 0;
+  fn.largest = largest;
+  uint64_t best = 0;
+  for (int64_t j0 = 0; j0 < S; j0 += 4 * SHORT_THREADS) {
+    uint64_t c[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t j = j0 + u * SHORT_THREADS + tid;
+      c[u] = 0;
+      if (j < S && fn.eligible(j))
+        c[u] = ((uint64_t)fn.key(j) << 32) | (uint32_t)(largest ? ~(uint32_t)j : (uint32_t)j);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) best = u64max(best, c[u]);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) best = u64max(best, __shfl_xor_sync(0xffffffffu, best, o));
+  if (lane == 0) wbest[warp] = best;
+  __syncthreads();
+  if (tid == 0) {
+    for (int q = 0; q < SHORT_THREADS / 32; ++q) best = u64max(best, wbest[q]);
+    idx[row] = best ? (int32_t)(largest ? ~(uint32_t)best : (uint32_t)best) : -1;
+  }
+}
+
 // CTAs per row: a power of two (the histogram exchange splits 1024 or 2048 bins evenly)
 int topk_cluster_size(int64_t S) {
   int cs = 1;
@@ -551,6 +592,12 @@ int64_t topk_max_len() { return SLICE_MAX * MAX_CLUSTER; }
 
 cudaError_t launch_topk(const float* scores, int B, int KVH, int64_t S, int k, int protect_tail,
                         const uint32_t* live, int largest, int32_t* idx, cudaStream_t st) {
+  if (k == 1 && protect_tail == 0) {
+    const cudaError_t e =
+        launch_pdl(k_top1, dim3((unsigned)((int64_t)B * KVH)), dim3(SHORT_THREADS), 0, st, scores, S, live, largest, idx);
+    if (e != cudaSuccess) return e;
+    return launched(1);
+  }
   if (S <= SHORT_MAX) {
     cudaLaunchAttribute attrs[2];
     const cudaLaunchConfig_t cfg =

@@ -219,7 +219,7 @@ kvc_status kvc_tova_decode_step(const kvc_bf16* q_new, const kvc_bf16* k_new,
  *   slot        [B][KVH] int32 — slot filled by the last insertion
  *   t           host: index of the next recorded step (advanced by each update)
  *   n_free      host: free slots per (b,kvh) (identical for all heads)
- * cap must be a multiple of 32 and <= 40960, history in [1, 4096].
+ * cap must be a multiple of 32 and <= 40960, history in [1, 4096], B * KVH <= 65535.
  * ------------------------------------------------------------------------------------- */
 typedef struct {
   int32_t B, KVH, cap, history;

@@ -141,6 +141,9 @@ TOPK_CASES = [
     (1, 1, 33, 40, 0, 0, True, None),          # k > S
     (3, 1, 129, 65, 1, 2, True, None),
     (2, 2, 777, 13, 0, 1, False, 0.6),
+    (3, 2, 5000, 1, 0, 0, True, 0.5),          # k = 1 (one CTA per row), keep, live mask
+    (2, 3, 70000, 1, 0, 4, False, None),       # k = 1, evict, long rows with ties
+    (1, 2, 100, 1, 0, 0, True, 0.0),           # k = 1, nothing live -> -1
 ]
 
 
