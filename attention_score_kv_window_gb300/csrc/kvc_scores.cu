@@ -650,8 +650,8 @@ int small_cluster(const ScoresArgs& a, int64_t* per_out) {
   int cs = 1;
   while (cs <= 8 && (int64_t)a.R * per_for(cs) * 4 > SMALL_LOGIT_BYTES) ++cs;
   if (cs > 8) return 0;
-  // more CTAs while the GPU is not yet two CTAs per SM deep and slices stay >= 256 keys
-  while (cs < 8 && units * cs < 3 * (int64_t)num_sms() && per_for(cs + 1) >= 256) ++cs;
+  // more CTAs while they still fit one wave (three CTAs per SM) and slices stay >= 256 keys
+  while (cs < 8 && units * (cs + 1) <= 3 * (int64_t)num_sms() && per_for(cs + 1) >= 256) ++cs;
   if (units * cs > 2147483647LL) return 0;
   *per_out = per_for(cs);
   return cs;
