@@ -308,43 +308,84 @@ class PrefillCase:
                 "l2": f"inputs rotate over {self.R} replicas ({self.R * self.in_bytes / 2**20:.0f} MiB > L2)"}
 
     def e2e(self, steps, stream, world, dist, dev):
-        """Same step through kvc_compress_prefill with pinned host inputs and outputs."""
+        """Same step through kvc_compress_prefill with pinned host inputs and outputs.  Steps are
+        pipelined over two device buffer sets: step i+1's host->device copies (the two halves of
+        K and of V each on its own copy stream, q with the last) overlap step i's compute and
+        its device->host read-back (another stream).  Every step moves its full inputs and
+        results."""
         torch, kvc, wl = self.torch, self.kvc, self.wl
         inp = self.host
         hq = torch.from_numpy(inp["q"].view(np.int16)).view(torch.bfloat16).pin_memory()
         hK = torch.from_numpy(inp["K"].view(np.int16)).view(torch.bfloat16).pin_memory()
         hV = torch.from_numpy(inp["V"].view(np.int16)).view(torch.bfloat16).pin_memory()
         B, KVH, k, D = self.B, self.KVH, self.k, self.D
-        h_idx = torch.empty((B, KVH, k), dtype=torch.int32).pin_memory()
-        h_Ko = torch.empty((B, KVH, k, D), dtype=torch.bfloat16).pin_memory()
-        h_Vo = torch.empty((B, KVH, k, D), dtype=torch.bfloat16).pin_memory()
-        dq, dK, dV = self.reps[0]
+        h_out = [(torch.empty((B, KVH, k), dtype=torch.int32).pin_memory(),
+                  torch.empty((B, KVH, k, D), dtype=torch.bfloat16).pin_memory(),
+                  torch.empty((B, KVH, k, D), dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
+        ws2 = torch.empty_like(self.ws)
+        bufs = [(self.reps[0], self.outs[0], self.ws), (self.reps[1], self.outs[1], ws2)]
+        s_up = [torch.cuda.Stream() for _ in range(4)]
+        s_out = torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        in_ready = [[ev() for _ in range(4)] for _ in range(2)]   # inputs of a buffer set uploaded
+        fK, fV = hK.view(-1), hV.view(-1)
+        half = fK.numel() // 2
 
-        def e2e_step():
-            dq.copy_(hq, non_blocking=True)
-            dK.copy_(hK, non_blocking=True)
-            dV.copy_(hV, non_blocking=True)
-            sc, idx, Ko, Vo = self.outs[0]
+        def pieces(dq, dK, dV):  # contiguous halves of the flattened K and V
+            gK, gV = dK.view(-1), dV.view(-1)
+            return (((gK[:half], fK[:half]),), ((gK[half:], fK[half:]),),
+                    ((gV[:half], fV[:half]),), ((gV[half:], fV[half:]), (dq, hq)))
+        comp_done = [ev() for _ in range(2)]          # compute on a buffer set finished
+        out_done = [ev() for _ in range(2)]           # results of a buffer set read back
+        used = [False, False]
+
+        def e2e_step(i):
+            x = i % 2
+            (dq, dK, dV), (sc, idx, Ko, Vo), ws = bufs[x]
+            hi, hKo, hVo = h_out[x]
+            # upload into set x once its previous compute has consumed it
+            for st_, ev_, pairs in zip(s_up, in_ready[x], pieces(dq, dK, dV)):
+                if used[x]:
+                    st_.wait_event(comp_done[x])
+                with torch.cuda.stream(st_):
+                    for d_, h_ in pairs:
+                        d_.copy_(h_, non_blocking=True)
+                ev_.record(st_)
+            for ev_ in in_ready[x]:
+                stream.wait_event(ev_)
+            if used[x]:
+                stream.wait_event(out_done[x])  # its previous results were read back
             kvc.kvc_compress_prefill(dq, dK, dV, wl.scale, k, protect_tail=wl.protect_tail, reduce=wl.reduce,
-                                     out=(sc, idx, Ko, Vo), ws=self.ws)
-            h_idx.copy_(idx, non_blocking=True)
-            h_Ko.copy_(Ko, non_blocking=True)
-            h_Vo.copy_(Vo, non_blocking=True)
+                                     out=(sc, idx, Ko, Vo), ws=ws)
+            comp_done[x].record(stream)
+            s_out.wait_event(comp_done[x])
+            with torch.cuda.stream(s_out):
+                hi.copy_(idx, non_blocking=True)
+                hKo.copy_(Ko, non_blocking=True)
+                hVo.copy_(Vo, non_blocking=True)
+            out_done[x].record(s_out)
+            used[x] = True
 
-        e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(steps):
-            e2e_step()
+        for st_ in s_up + [s_out]:
+            st_.wait_event(e0)
+        for i in range(steps):
+            e2e_step(i)
+        for x in range(2):
+            stream.wait_event(out_done[x])
         e1.record(stream)
         torch.cuda.synchronize()
         ms = max_over_ranks(e0.elapsed_time(e1), world, dist, dev)
         return {"value": self.tokens_per_step * steps * world / (ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int((hq.numel() + hK.numel() + hV.numel()) * 2),
-                "d2h_bytes_per_step": int(h_idx.numel() * 4 + (h_Ko.numel() + h_Vo.numel()) * 2)}
+                "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h_out[0])),
+                "pipeline": "two buffer sets; uploads (four streams), compute and read-back on separate streams"}
 
 
 class TovaDecodeCase:
