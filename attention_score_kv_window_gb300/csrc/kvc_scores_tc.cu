@@ -563,7 +563,6 @@ __device__ __forceinline__ float pass2_chunk(const Ctx& c, int buf, uint32_t tad
 template <int D, int NHALF, int NQ, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     k_scores_tc(const ScoresArgs a, const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmQ) {
-  pdl_wait();  // previous kernel on the stream complete and visible
   using L = Layout<D>;
   constexpr int KS = D / 16;
   constexpr bool P1 = (MODE & 1) != 0, P2 = (MODE & 2) != 0;
@@ -573,7 +572,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int NC1 = NHALF == 2 ? TILE : TILE / 2;  // pass 1: key columns per warp and tile
   constexpr int NW = N2 / 2;                     // pass 2: query-row columns per warp and tile
   extern __shared__ unsigned char smem_raw[];
-  const Ctx c = prologue<D>(smem_raw);
+  const Ctx c = prologue<D>(smem_raw);  // shared memory and TMEM only
+  pdl_wait();  // previous kernel on the stream complete and visible
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int bk = b * a.KVH + kvh;
@@ -879,11 +879,15 @@ cudaError_t run_tc(const ScoresArgs& a, cudaStream_t st) {
     cfg.blockDim = dim3(THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    // cooperative (every CTA resident: the key-range barrier) and programmatic stream
+    // serialisation (the prologue overlaps the previous kernel's tail)
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kern, a, m->k, m->q1);
     if (e != cudaSuccess) return e;
   }
