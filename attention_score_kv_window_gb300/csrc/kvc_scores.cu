@@ -460,7 +460,6 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
   const int R = a.R;
   const int64_t kbeg = (int64_t)cr * per;
   const int64_t kend = min(a.S, kbeg + per);
-  const int ntiles = kend > kbeg ? (int)((kend - kbeg + TK - 1) / TK) : 0;
 
   uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);
   uint16_t* Ks = Qs + 16 * P;
@@ -473,47 +472,62 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
   const uint16_t* Qg = a.q + ((int64_t)(b * a.H + kvh * a.G) * a.w) * D;
   const uint32_t* lw = a.live ? a.live + (int64_t)bk * a.live_words : nullptr;
 
+  // Query rows once (all warps), then each warp streams its own 8-key chunks (chunk c of the
+  // slice goes to warp c % 8) through a private ring of WST stages: no block barrier inside
+  // the key loop, only the warp's own copies and a warp barrier.
   load_q_rows<D>(Qs, Qg, 0, 16, R, tid);
   cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+  uint32_t aq[KS][4];
 #pragma unroll
-  for (int s = 0; s < SMALL_STAGES - 1; ++s) {
-    if (s < ntiles) load_k_tile<D>(Ks + s * TK * P, Kb, a.ss, kbeg + (int64_t)s * TK, kend, tid);
+  for (int ks = 0; ks < KS; ++ks) {
+    const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int c = ks * 16 + ((lane >> 4) & 1) * 8;
+    ldsm_x4(smem_u32(Qs + r * P + c), aq[ks][0], aq[ks][1], aq[ks][2], aq[ks][3]);
+  }
+  constexpr int WST = SMALL_STAGES;       // stages per warp
+  static_assert(8 * WST * 8 == SMALL_STAGES * TK, "per-warp rings fill the K staging area");
+  constexpr int CH = D / 8;               // 16-byte pieces per key row
+  uint16_t* Kw = Ks + warp * WST * 8 * P;
+  const int64_t nchunks = (kend - kbeg + 7) / 8;
+  const int my = nchunks > warp ? (int)((nchunks - warp + 7) / 8) : 0;
+  auto load_chunk = [&](int i, int st) {
+    const int64_t k0 = kbeg + (int64_t)(warp + 8 * i) * 8;
+#pragma unroll
+    for (int c = lane; c < 8 * CH; c += 32) {
+      const int r = c / CH, cc = c % CH;
+      const int64_t j = k0 + r;
+      const bool ok = j < kend;
+      cp_async16(smem_u32(Kw + (st * 8 + r) * P + cc * 8), ok ? (Kb + j * a.ss + cc * 8) : Kb, ok ? 16 : 0);
+    }
+  };
+#pragma unroll
+  for (int st = 0; st < WST - 1; ++st) {
+    if (st < my) load_chunk(st, st);
     cp_async_commit();
   }
   // row limits of the two rows this lane's accumulator fragment holds
   const int64_t limA = (g < R) ? (a.causal ? a.S - a.w + (g % a.w) : a.S - 1) : -1;
   const int64_t limB = (g + 8 < R) ? (a.causal ? a.S - a.w + ((g + 8) % a.w) : a.S - 1) : -1;
-
-  uint32_t aq[KS][4];
-  for (int it = 0; it < ntiles; ++it) {
-    cp_async_wait<SMALL_STAGES - 2>();
-    __syncthreads();
-    if (it == 0) {
-#pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int c = ks * 16 + ((lane >> 4) & 1) * 8;
-        ldsm_x4(smem_u32(Qs + r * P + c), aq[ks][0], aq[ks][1], aq[ks][2], aq[ks][3]);
-      }
-    }
+  for (int i = 0; i < my; ++i) {
+    cp_async_wait<WST - 2>();
+    __syncwarp();  // the chunk's rows, copied by all lanes, are visible; stage (i-1) % WST is free
     {
-      const int nx = it + SMALL_STAGES - 1;
-      if (nx < ntiles)
-        load_k_tile<D>(Ks + (nx % SMALL_STAGES) * TK * P, Kb, a.ss, kbeg + (int64_t)nx * TK, kend, tid);
+      const int nx = i + WST - 1;
+      if (nx < my) load_chunk(nx, nx % WST);
       cp_async_commit();
     }
-    const uint16_t* Kt = Ks + (it % SMALL_STAGES) * TK * P;
+    const uint16_t* Kt = Kw + (i % WST) * 8 * P;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks2 = 0; ks2 < KS / 2; ++ks2) {
       uint32_t b0, b1, b2, b3;
-      const int r = warp * 8 + (lane & 7);
-      const int cc = ks2 * 32 + (lane >> 3) * 8;
-      ldsm_x4(smem_u32(Kt + r * P + cc), b0, b1, b2, b3);
+      ldsm_x4(smem_u32(Kt + (lane & 7) * P + ks2 * 32 + (lane >> 3) * 8), b0, b1, b2, b3);
       mma16816(c, aq[2 * ks2], b0, b1);
       mma16816(c, aq[2 * ks2 + 1], b2, b3);
     }
-    const int64_t j0 = kbeg + (int64_t)it * TK + warp * 8 + 2 * t;
+    const int64_t j0 = kbeg + (int64_t)(warp + 8 * i) * 8 + 2 * t;
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const int64_t j = j0 + e;
