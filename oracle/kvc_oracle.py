@@ -395,6 +395,12 @@ class Scissorhands:
     * ``low[b,kvh,s]``: number of low flags of the slot's current token over its last
       ``n_obs = min(history, t - insert_step + 1)`` observations;
     * ``insert_step``: step at which the slot's token entered (prefill tokens: 0).
+
+    ``t`` counts recordings.  Dense recording calls ``insert`` then ``record`` every decode
+    step.  Sparse recording (suggested in the PR's review thread: look at the attention only
+    every M steps and update numerator and denominator from that step alone) calls ``record``
+    only every M-th step; ``insert_step`` then holds the index of the token's first
+    recording, so ``n_obs`` counts observations, not steps.
     """
 
     def __init__(self, B: int, KVH: int, cap: int, history: int = 400):
@@ -409,15 +415,26 @@ class Scissorhands:
         self.live[..., :n_live] = True
         self.insert_step[..., :n_live] = 0
 
-    def insert(self) -> np.ndarray:
-        """Place the new token in the lowest free slot of every (b, kvh); returns [B, KVH]."""
+    def insert(self, replace=None) -> np.ndarray:
+        """Place the new token in one slot of every (b, kvh); returns the slots [B, KVH].
+
+        ``replace is None``: the lowest free slot.  Otherwise ``replace[b, kvh]`` names a live
+        slot whose token is evicted and overwritten by the new one (the eviction-queue
+        variant: one eviction per step, so no slot is ever left empty).  Either way the slot
+        starts afresh: ``insert_step = t`` (the index of the next recording) and no low
+        flags; the flags its previous token left in the history are ignored by ``record``."""
         slot = np.zeros((self.B, self.KVH), dtype=np.int32)
         for b in range(self.B):
             for kv in range(self.KVH):
-                free = np.nonzero(~self.live[b, kv])[0]
-                if free.size == 0:
-                    raise RuntimeError("no free slot")
-                s = int(free[0])
+                if replace is None:
+                    free = np.nonzero(~self.live[b, kv])[0]
+                    if free.size == 0:
+                        raise RuntimeError("no free slot")
+                    s = int(free[0])
+                else:
+                    s = int(replace[b, kv])
+                    if not (0 <= s < self.cap and self.live[b, kv, s]):
+                        raise RuntimeError("queued slot is not live")
                 slot[b, kv] = s
                 self.live[b, kv, s] = True
                 self.insert_step[b, kv, s] = self.t
@@ -440,18 +457,36 @@ class Scissorhands:
     def n_obs(self) -> np.ndarray:
         return np.minimum(self.history, (self.t - 1) - self.insert_step + 1)
 
-    def evict(self, m: int) -> np.ndarray:
-        """Per (b, kvh), evict the ``m`` live tokens with the highest fraction
-        ``low / n_obs`` (compared exactly; ties: lower slot index first).  Returns the
-        evicted slots ascending [B, KVH, m] (-1 padded)."""
+    def _eviction_order(self, b: int, kv: int) -> np.ndarray:
+        """Live slots of (b, kvh), most evictable first: highest fraction ``low / n_obs``
+        (compared exactly), ties to the lower slot.  A token inserted after the last
+        recording (possible only when recording is sparse) has no observation and no low
+        flag: its fraction reads as 0, like a token never found below uniform attention."""
         rank = fraction_rank_table(self.history)
-        nobs = self.n_obs()
+        nobs = np.maximum(self.n_obs()[b, kv], 1)
+        cand = np.nonzero(self.live[b, kv])[0]
+        r = rank[self.low[b, kv, cand], nobs[cand]].astype(np.float64)
+        return _ranked(cand, r, True)
+
+    def evict(self, m: int) -> np.ndarray:
+        """Bulk eviction: per (b, kvh), evict the ``m`` most evictable live tokens.  Returns
+        the evicted slots ascending [B, KVH, m] (-1 padded); their slots become free."""
         out = np.full((self.B, self.KVH, m), -1, dtype=np.int32)
         for b in range(self.B):
             for kv in range(self.KVH):
-                cand = np.nonzero(self.live[b, kv])[0]
-                r = rank[self.low[b, kv, cand], nobs[b, kv, cand]].astype(np.float64)
-                ev = np.sort(_ranked(cand, r, True)[:m])
+                ev = np.sort(self._eviction_order(b, kv)[:m])
                 out[b, kv, :ev.size] = ev
                 self.live[b, kv, ev] = False
+        return out
+
+    def refill_queue(self, m: int) -> np.ndarray:
+        """Eviction-queue variant (the PR description's change to Scissorhands): per
+        (b, kvh), the ``m`` tokens bulk eviction would take, listed most evictable first,
+        [B, KVH, m] (-1 padded).  Nothing is evicted here: the tokens stay live (and keep
+        being recorded) until a step replaces them, one per step in queue order."""
+        out = np.full((self.B, self.KVH, m), -1, dtype=np.int32)
+        for b in range(self.B):
+            for kv in range(self.KVH):
+                q = self._eviction_order(b, kv)[:m]
+                out[b, kv, :q.size] = q
         return out

@@ -3,6 +3,7 @@
 Every check here is independent of the oracle's own code: closed forms, invariants,
 brute-force loops written separately in this file, or sizes printed on the pages.
 """
+import copy
 import json
 import math
 import os
@@ -321,11 +322,16 @@ class _FullLog:
     def nobs(self):
         return np.minimum(self.history, self.t - self.born)
 
-    def evict_order(self, b, kv, live, m):
+    def queue_order(self, b, kv, live, m):
+        """The m most evictable live slots, most evictable first.  A token with no
+        observation yet (sparse recording) has no low flag: fraction 0."""
         c, n = self.counts(), self.nobs()
         cand = [s for s in range(live.shape[-1]) if live[b, kv, s]]
-        cand.sort(key=lambda s: (-Fraction(int(c[b, kv, s]), int(n[b, kv, s])), s))
-        return sorted(cand[:m])
+        cand.sort(key=lambda s: (-Fraction(int(c[b, kv, s]), max(1, int(n[b, kv, s]))), s))
+        return cand[:m]
+
+    def evict_order(self, b, kv, live, m):
+        return sorted(self.queue_order(b, kv, live, m))
 
 
 def test_circular_history_matches_full_log_and_exact_eviction():
@@ -351,6 +357,92 @@ def test_circular_history_matches_full_log_and_exact_eviction():
             ev = sh.evict(m)
             assert ev.tolist() == exp
             ref.occ[~sh.live] = -1
+
+
+def test_eviction_queue_matches_full_log():
+    """Queue variant: once the cache is full, every m steps the queue is refilled with the
+    m most evictable tokens (most evictable first), and each step's new token replaces the
+    next queued one.  The queue holds the same tokens bulk eviction would take."""
+    B, KVH, cap, hist, m = 2, 2, 32, 7, 4
+    sh = O.Scissorhands(B, KVH, cap, history=hist)
+    sh.prefill(cap - 3)
+    ref = _FullLog((B, KVH, cap), hist)
+    ref.insert_at(sh.live.copy())
+    g = np.random.Generator(np.random.PCG64([29]))
+    queue, pos, refills = None, m, 0
+    for step in range(70):
+        if sh.live.all():
+            if pos == m:
+                exp = [[ref.queue_order(b, kv, sh.live, m) for kv in range(KVH)] for b in range(B)]
+                bulk = copy.deepcopy(sh).evict(m)
+                queue, pos = sh.refill_queue(m), 0
+                refills += 1
+                assert queue.tolist() == exp
+                np.testing.assert_array_equal(np.sort(queue, axis=-1), bulk)
+                assert sh.live.all()  # the queue evicts nothing by itself
+            slot = sh.insert(replace=queue[..., pos])
+            np.testing.assert_array_equal(slot, queue[..., pos])
+            pos += 1
+            hit = np.zeros(sh.live.shape, bool)
+            np.put_along_axis(hit, slot[..., None].astype(np.int64), True, axis=-1)
+            ref.insert_at(hit)
+        else:
+            before = sh.live.copy()
+            sh.insert()
+            ref.insert_at(sh.live & ~before)
+        keys = sh.live.sum(-1, keepdims=True)
+        p = np.where(sh.live, g.random((B, KVH, cap)) * 2.0 / keys, 0.0)
+        ref.record(O.low_attention_bits(p, sh.live))
+        sh.record(p)
+        np.testing.assert_array_equal(np.where(sh.live, sh.low, 0), np.where(sh.live, ref.counts(), 0))
+        np.testing.assert_array_equal(np.where(sh.live, sh.n_obs(), 0), np.where(sh.live, ref.nobs(), 0))
+    assert refills >= 10
+
+
+def test_sparse_recording_matches_full_log():
+    """Sparse recording: every step inserts, only every M-th step records; counts and
+    n_obs are over recordings, and bulk eviction still ranks by exact fractions (tokens
+    not yet observed rank as fraction 0)."""
+    B, KVH, cap, hist, m, M = 2, 2, 32, 5, 4, 3
+    sh = O.Scissorhands(B, KVH, cap, history=hist)
+    sh.prefill(cap - m)
+    ref = _FullLog((B, KVH, cap), hist)
+    ref.insert_at(sh.live.copy())
+    g = np.random.Generator(np.random.PCG64([31]))
+    unobserved = 0
+    for step in range(80):
+        before = sh.live.copy()
+        sh.insert()
+        ref.insert_at(sh.live & ~before)
+        if step % M == 0:
+            keys = sh.live.sum(-1, keepdims=True)
+            p = np.where(sh.live, g.random((B, KVH, cap)) * 2.0 / keys, 0.0)
+            ref.record(O.low_attention_bits(p, sh.live))
+            sh.record(p)
+        assert sh.t == ref.t == step // M + 1
+        np.testing.assert_array_equal(np.where(sh.live, sh.low, 0), np.where(sh.live, ref.counts(), 0))
+        np.testing.assert_array_equal(np.where(sh.live, sh.n_obs(), 0), np.where(sh.live, ref.nobs(), 0))
+        if (step + 1) % m == 0:
+            unobserved += int((sh.live & (sh.n_obs() == 0)).sum())
+            live_before = sh.live.copy()
+            exp = [[ref.evict_order(b, kv, live_before, m) for kv in range(KVH)] for b in range(B)]
+            assert sh.evict(m).tolist() == exp
+            ref.occ[~sh.live] = -1
+    assert unobserved > 0  # the n_obs = 0 reading was exercised
+
+
+def test_unobserved_token_ranks_as_fraction_zero():
+    """A token inserted after the last recording has no observation: its fraction reads as
+    0, tied with observed tokens that were never low, so ties go by slot."""
+    sh = O.Scissorhands(1, 1, 32, history=5)
+    sh.prefill(28)
+    sh.record(np.full((1, 1, 32), 1.0))  # nothing below 1/keys: every fraction is 0
+    assert sh.evict(4).tolist() == [[[0, 1, 2, 3]]]
+    for _ in range(4):
+        sh.insert()  # slots 0..3, not yet observed
+    assert (sh.n_obs()[0, 0, :4] == 0).all() and (sh.n_obs()[0, 0, 4:28] == 1).all()
+    assert sh.refill_queue(6).tolist() == [[[0, 1, 2, 3, 4, 5]]]
+    assert sh.evict(6).tolist() == [[[0, 1, 2, 3, 4, 5]]]
 
 
 # ----------------------------------------------------------------------------------------
