@@ -22,8 +22,9 @@ Sources (page titles and sections of the web pages this method is taken from):
 * "Add ThinK_Press" (kvpress pull request 18): SimJeg's first comment defines the channel
   score as ``sum_{i,j} (q_id * k_jd)^2`` over the 64 window queries and all keys;
   yuhuixu1993's reply gives the factorised form ``query_norm * key_norm``; SimJeg's option
-  list (3a zero the pruned channels, 3b/3c keep a smaller key cache); the thread settles on
-  pruning tokens first, then channels.
+  list (3a zero the pruned channels, 3b a smaller key cache with the zeros added back for
+  decoding, 3c a smaller key cache and an attention that prunes the query too, as the
+  author's reply proposes); the thread settles on pruning tokens first, then channels.
 
 Readings where the pages are silent or garbled are listed in the repository's design notes;
 the ones that decide a number are repeated beside the code below.
@@ -38,7 +39,8 @@ import numpy as np
 __all__ = [
     "as_f64", "visible_mask", "window_softmax", "window_scores", "topk_select", "compact_kv",
     "write_slots", "channel_score", "channel_score_bruteforce", "channel_prune",
-    "compress_prefill", "tova_first_step", "tova_decode_step", "Scissorhands",
+    "compress_prefill", "zero_add_back", "decode_attention", "decode_attention_pruned",
+    "tova_first_step", "tova_decode_step", "Scissorhands",
     "scissorhands_probs", "low_attention_bits", "fraction_rank_table",
 ]
 
@@ -312,6 +314,61 @@ def channel_prune(cs, K, C: int, zero_mode: bool = False):
             else:
                 out[b, kv] = K[b, kv][:, sel]
     return ch, out
+
+
+# ----------------------------------------------------------------------------------------
+# Decoding over the channel-pruned cache ("Add ThinK_Press" options 3b and 3c)
+# ----------------------------------------------------------------------------------------
+
+
+def zero_add_back(Kp, ch, D: int):
+    """Option 3b: the full-width key cache rebuilt from the pruned one, the dropped channels
+    filled with zeros: ``K[b, kvh, j, ch[b, kvh, c]] = Kp[b, kvh, j, c]``, every other channel 0.
+    Values are moved, not converted (bf16 bit patterns stay bit patterns)."""
+    Kp = np.asarray(Kp)
+    ch = np.asarray(ch)
+    B, KVH, S, C = Kp.shape
+    K = np.zeros((B, KVH, S, D), dtype=Kp.dtype)
+    for b in range(B):
+        for kv in range(KVH):
+            for c in range(C):
+                K[b, kv, :, ch[b, kv, c]] = Kp[b, kv, :, c]
+    return K
+
+
+def decode_attention(q, K, V, scale: float, live=None) -> np.ndarray:
+    """Attention of one new query per head over a cache: query head h reads KV head
+    ``h // G``; logits ``s_j = scale * q[b,h,:] . K[b,kvh,j,:]`` over the live slots j,
+    ``p = softmax(s)``, output ``sum_j p_j V[b,kvh,j,:]``.  float64 [B, H, Dv]; a head with no
+    live slot gets zeros."""
+    q, K, V = as_f64(q), as_f64(K), as_f64(V)
+    B, H, _ = q.shape
+    KVH, S = K.shape[1], K.shape[2]
+    G = H // KVH
+    out = np.zeros((B, H, V.shape[-1]))
+    for b in range(B):
+        for h in range(H):
+            kv = h // G
+            vis = np.ones(S, bool) if live is None else np.asarray(live, bool)[b, kv]
+            if not vis.any():
+                continue
+            s = scale * (K[b, kv][vis] @ q[b, h])
+            e = np.exp(s - s.max())
+            out[b, h] = (e / e.sum()) @ V[b, kv][vis]
+    return out
+
+
+def decode_attention_pruned(q, ch, Kp, V, scale: float, live=None) -> np.ndarray:
+    """Option 3c: the query is pruned to the key channels the cache kept,
+    ``q'[b,h,c] = q[b,h,ch[b,kvh,c]]``, and attends the pruned keys directly.  The logits equal
+    those of the full query against the zero-filled keys, so the scale stays that of the full
+    head (``1/sqrt(D)``); values keep all channels."""
+    q = np.asarray(q)
+    ch = np.asarray(ch)
+    B, H, _ = q.shape
+    G = H // ch.shape[1]
+    qp = np.stack([np.stack([q[b, h, ch[b, h // G]] for h in range(H)]) for b in range(B)])
+    return decode_attention(qp, Kp, V, scale, live)
 
 
 # ----------------------------------------------------------------------------------------

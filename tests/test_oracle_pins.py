@@ -238,6 +238,81 @@ def test_think_prune_compact_and_zero():
         np.testing.assert_array_equal(Kz[0, kv][:, exp], K[0, kv][:, exp])
 
 
+def _decode_attention_loops(q, K, V, scale, live=None):
+    """Independent brute force: one new query per head, pure Python loops."""
+    B, H, D = len(q), len(q[0]), len(q[0][0])
+    KVH, S, Dv = len(K[0]), len(K[0][0]), len(V[0][0][0])
+    G = H // KVH
+    out = [[[0.0] * Dv for _ in range(H)] for _ in range(B)]
+    for b in range(B):
+        for h in range(H):
+            kv = h // G
+            js = [j for j in range(S) if live is None or live[b][kv][j]]
+            if not js:
+                continue
+            lg = [scale * sum(q[b][h][d] * K[b][kv][j][d] for d in range(D)) for j in js]
+            mx = max(lg)
+            ex = [math.exp(x - mx) for x in lg]
+            tot = sum(ex)
+            for n, j in enumerate(js):
+                for d in range(Dv):
+                    out[b][h][d] += ex[n] / tot * V[b][kv][j][d]
+    return out
+
+
+def test_decode_attention_by_loops():
+    B, H, KVH, D, S = 2, 4, 2, 6, 7
+    q = bf16_bits_to_f32(normal_bf16((B, H, D), 90, 1)).astype(np.float64)
+    K = bf16_bits_to_f32(normal_bf16((B, KVH, S, D), 90, 2)).astype(np.float64)
+    V = bf16_bits_to_f32(normal_bf16((B, KVH, S, D), 90, 3)).astype(np.float64)
+    live = np.random.Generator(np.random.PCG64([90])).random((B, KVH, S)) < 0.6
+    live[1, 1] = False  # a head group with no live slot attends nothing
+    for lv in (None, live):
+        got = O.decode_attention(_bf16(q), _bf16(K), _bf16(V), 0.4, lv)
+        exp = _decode_attention_loops(q.tolist(), K.tolist(), V.tolist(), 0.4, None if lv is None else lv.tolist())
+        np.testing.assert_allclose(got, np.array(exp), rtol=1e-12, atol=1e-14)
+    assert np.all(O.decode_attention(_bf16(q), _bf16(K), _bf16(V), 0.4, live)[1, 2:] == 0)
+
+
+def test_decode_attention_closed_forms():
+    B, H, KVH, D, S = 1, 4, 2, 8, 9
+    K = normal_bf16((B, KVH, S, D), 91, 2)
+    V = normal_bf16((B, KVH, S, D), 91, 3)
+    Vf = bf16_bits_to_f32(V).astype(np.float64)
+    # a zero query attends uniformly: the mean of the value rows
+    out = O.decode_attention(np.zeros((B, H, D), np.uint16), K, V, 0.3)
+    np.testing.assert_allclose(out[0, 0], Vf[0, 0].mean(0), rtol=1e-13)
+    np.testing.assert_allclose(out[0, 3], Vf[0, 1].mean(0), rtol=1e-13)
+    # one key aligned with a large query takes all the weight
+    Kd = np.zeros((B, KVH, S, D), np.float32)
+    Kd[:, :, 4, 0] = 1.0
+    q = np.zeros((B, H, D), np.float32)
+    q[..., 0] = 64.0
+    out = O.decode_attention(_bf16(q), _bf16(Kd), V, 1.0)
+    np.testing.assert_allclose(out[0, 1], Vf[0, 0, 4], rtol=1e-12)
+    np.testing.assert_allclose(out[0, 2], Vf[0, 1, 4], rtol=1e-12)
+
+
+def test_pruned_query_equals_zero_filled_keys():
+    """Options 3b and 3c give the attention of option 3a: pruning the query to the kept
+    channels (3c) equals attending the zero-filled keys (3b = 3a's cache)."""
+    B, H, KVH, D, S, C = 2, 8, 2, 16, 11, 8
+    q = normal_bf16((B, H, D), 92, 1)
+    K = normal_bf16((B, KVH, S, D), 92, 2)
+    V = normal_bf16((B, KVH, S, D), 92, 3)
+    cs = O.channel_score(normal_bf16((B, H, 4, D), 92, 4), K)
+    ch, Kp = O.channel_prune(cs, K, C)
+    _, Kz = O.channel_prune(cs, K, C, zero_mode=True)
+    np.testing.assert_array_equal(O.zero_add_back(Kp, ch, D), Kz)
+    live = np.random.Generator(np.random.PCG64([92])).random((B, KVH, S)) < 0.7
+    for lv in (None, live):
+        np.testing.assert_allclose(O.decode_attention_pruned(q, ch, Kp, V, 0.25, lv),
+                                   O.decode_attention(q, Kz, V, 0.25, lv), rtol=1e-12, atol=1e-15)
+    # keeping every channel is plain attention
+    full = np.broadcast_to(np.arange(D, dtype=np.int32), (B, KVH, D))
+    np.testing.assert_array_equal(O.decode_attention_pruned(q, full, K, V, 0.25), O.decode_attention(q, K, V, 0.25))
+
+
 def test_page_shapes_and_memory_ratio():
     g = json.load(open(os.path.join(GOLDEN, "page_shapes.json")))
     # TOVA walk-through: scores [batch, num_kv_heads, seq_len]
