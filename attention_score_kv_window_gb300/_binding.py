@@ -67,6 +67,10 @@ _SIGNATURES = {
     "kvc_scissorhands_update_from_probs": (_I32, [_SH, _P, _P]),
     "kvc_scissorhands_update": (_I32, [_SH, _P, _P, _P, _P, _P, _DESC, _F, _P, _P, _SZ, _P]),
     "kvc_scissorhands_evict": (_I32, [_SH, _I32, _P, _P]),
+    "kvc_scissorhands_refill_queue": (_I32, [_SH, _I32, _P, _P]),
+    "kvc_scissorhands_update_queued": (_I32, [_SH, _P, _I32, _I32, _P, _P, _P, _P, _P, _DESC, _F, _P, _P, _SZ,
+                                              _P]),
+    "kvc_scissorhands_insert": (_I32, [_SH, _P, _I32, _I32, _P, _P, _P, _P, _DESC, _P]),
     "kvc_channel_score": (_I32, [_P, _I32, _P, _DESC, _P, _I32, _P, _P, _SZ, _P]),
     "kvc_channel_prune": (_I32, [_P, _P, _DESC, _I32, _I32, _P, _P, _P]),
     "kvc_get_device_status": (_I32, [_P]),
@@ -317,17 +321,45 @@ def kvc_scissorhands_update_from_probs(state: ScissorhandsState, p, stream=None)
 
 
 def kvc_scissorhands_update(state: ScissorhandsState, q_new, k_new, v_new, K, V, scale, probs=None,
-                            ws=None, stream=None):
+                            ws=None, stream=None, queue=None, pos=0):
+    """One decode step: insert (the lowest free slot, or with ``queue`` [B,KVH,m] over slot
+    ``queue[..., pos]``), score the new query over the live slots, record the flags."""
     lib = load_library()
     B, H, D = q_new.shape
     desc = kv_desc(K, H)
     if probs is None:
         probs = torch.empty((B, K.shape[1], K.shape[2]), dtype=torch.float32, device=K.device)
     ws, nbytes = _ws(KVC_OP_SCISSORHANDS_UPDATE, desc, 1, 0, ws, K.device)
-    _check(lib.kvc_scissorhands_update(ctypes.byref(state.c), _ptr(q_new.contiguous()), _ptr(k_new.contiguous()),
-                                       _ptr(v_new.contiguous()), _ptr(K), _ptr(V), ctypes.byref(desc),
-                                       float(scale), _ptr(probs), _ptr(ws), nbytes, _stream(stream)))
+    vp = None if v_new is None else _ptr(v_new.contiguous())
+    if queue is None:
+        _check(lib.kvc_scissorhands_update(ctypes.byref(state.c), _ptr(q_new.contiguous()), _ptr(k_new.contiguous()),
+                                           vp, _ptr(K), _ptr(V), ctypes.byref(desc), float(scale), _ptr(probs),
+                                           _ptr(ws), nbytes, _stream(stream)))
+    else:
+        _check(lib.kvc_scissorhands_update_queued(ctypes.byref(state.c), _ptr(queue.contiguous()), queue.shape[-1],
+                                                  int(pos), _ptr(q_new.contiguous()), _ptr(k_new.contiguous()), vp,
+                                                  _ptr(K), _ptr(V), ctypes.byref(desc), float(scale), _ptr(probs),
+                                                  _ptr(ws), nbytes, _stream(stream)))
     return probs
+
+
+def kvc_scissorhands_insert(state: ScissorhandsState, k_new, v_new, K, V, H, queue=None, pos=0, stream=None):
+    """Insert without recording (sparse recording's unobserved steps); ``queue`` as in
+    kvc_scissorhands_update.  ``H`` is the number of query heads of the cache's layer."""
+    desc = kv_desc(K, H)
+    vp = None if v_new is None else _ptr(v_new.contiguous())
+    qp, m = (None, 0) if queue is None else (_ptr(queue.contiguous()), queue.shape[-1])
+    _check(load_library().kvc_scissorhands_insert(ctypes.byref(state.c), qp, m, int(pos), _ptr(k_new.contiguous()),
+                                                  vp, _ptr(K), _ptr(V), ctypes.byref(desc), _stream(stream)))
+
+
+def kvc_scissorhands_refill_queue(state: ScissorhandsState, m: int, queue=None, stream=None):
+    """Eviction queue [B,KVH,m] int32: the m most evictable live slots, most evictable first."""
+    if queue is None:
+        queue = torch.empty((state.c.B, state.c.KVH, m), dtype=torch.int32, device=state.hist.device)
+    _check(load_library().kvc_scissorhands_refill_queue(ctypes.byref(state.c), int(m), _ptr(queue),
+                                                        _stream(stream)))
+    return queue
 
 
 def kvc_scissorhands_evict(state: ScissorhandsState, m: int, evicted=None, stream=None):

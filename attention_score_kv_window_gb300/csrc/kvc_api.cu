@@ -366,25 +366,79 @@ kvc_status kvc_scissorhands_update_from_probs(kvc_sh_state* st, const float* p, 
   return s;
 }
 
+namespace {
+// Validation shared by the insertion entry points; `queue` (nullable) with m and pos.
+kvc_status check_sh_insert(const kvc_sh_state* st, const int32_t* queue, int32_t m, int32_t pos,
+                           const kvc_bf16* k_new, const kvc_bf16* v_new, const kvc_bf16* K, const kvc_bf16* V,
+                           const kvc_kv_desc* kv, const char* name) {
+  KVC_TRY(check_sh(st));
+  KVC_TRY(check_desc(kv, name));
+  if (kv->B != st->B || kv->KVH != st->KVH || kv->S != st->cap)
+    return fail(KVC_ERR_INVALID_ARG, "%s: cache shape does not match the state", name);
+  if (queue) {
+    if (m < 1 || m > st->cap) return fail(KVC_ERR_INVALID_ARG, "%s: queue length m in [1, cap]", name);
+    if (pos < 0 || pos >= m) return fail(KVC_ERR_INVALID_ARG, "%s: queue position in [0, m)", name);
+  } else if (st->n_free <= 0) {
+    return fail(KVC_ERR_INVALID_ARG, "%s: no free slot (evict first, or give a queue)", name);
+  }
+  KVC_TRY(check_ptr(k_new, "k_new"));
+  KVC_TRY(check_ptr(K, "K"));
+  if ((v_new == nullptr) != (V == nullptr)) return fail(KVC_ERR_INVALID_ARG, "v_new and V must both be given or both NULL");
+  return KVC_OK;
+}
+
+kvc_status sh_insert(kvc_sh_state* st, const int32_t* queue, int32_t m, int32_t pos, const kvc_bf16* k_new,
+                     const kvc_bf16* v_new, kvc_bf16* K, kvc_bf16* V, const kvc_kv_desc* kv, kvc_stream_t stream) {
+  KVC_TRY(cuda_status(launch_sh_insert(*st, queue, m, pos, k_new, v_new, K, V, *kv, (cudaStream_t)stream),
+                      "scissorhands insert launch"));
+  if (!queue) st->n_free -= 1;  // a queued slot is replaced, not filled
+  return KVC_OK;
+}
+
+kvc_status sh_update(kvc_sh_state* st, const int32_t* queue, int32_t m, int32_t pos, const kvc_bf16* q_new,
+                     const kvc_bf16* k_new, const kvc_bf16* v_new, kvc_bf16* K, kvc_bf16* V, const kvc_kv_desc* kv,
+                     float scale, float* probs, void* ws, size_t ws_bytes, kvc_stream_t stream, const char* name) {
+  KVC_TRY(check_sh_insert(st, queue, m, pos, k_new, v_new, K, V, kv, name));
+  KVC_TRY(check_ptr(q_new, "q_new"));
+  KVC_TRY(check_ptr(probs, "probs"));
+  KVC_TRY(check_ws(ws, ws_bytes, scores_workspace(*kv, 1, KVC_REDUCE_GQA_GROUP), name));
+  KVC_TRY(sh_insert(st, queue, m, pos, k_new, v_new, K, V, kv, stream));
+  KVC_TRY(kvc_window_scores(q_new, K, kv, 1, scale, 0, st->live, KVC_REDUCE_GQA_GROUP, probs, ws, ws_bytes, stream));
+  return kvc_scissorhands_update_from_probs(st, probs, stream);
+}
+}  // namespace
+
 kvc_status kvc_scissorhands_update(kvc_sh_state* st, const kvc_bf16* q_new, const kvc_bf16* k_new,
                                    const kvc_bf16* v_new, kvc_bf16* K, kvc_bf16* V,
                                    const kvc_kv_desc* kv, float scale, float* probs, void* ws,
                                    size_t ws_bytes, kvc_stream_t stream) {
+  return sh_update(st, nullptr, 0, 0, q_new, k_new, v_new, K, V, kv, scale, probs, ws, ws_bytes, stream,
+                   "kvc_scissorhands_update");
+}
+
+kvc_status kvc_scissorhands_update_queued(kvc_sh_state* st, const int32_t* queue, int32_t m, int32_t pos,
+                                          const kvc_bf16* q_new, const kvc_bf16* k_new, const kvc_bf16* v_new,
+                                          kvc_bf16* K, kvc_bf16* V, const kvc_kv_desc* kv, float scale,
+                                          float* probs, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  if (!queue) return fail(KVC_ERR_INVALID_ARG, "kvc_scissorhands_update_queued: queue is NULL");
+  return sh_update(st, queue, m, pos, q_new, k_new, v_new, K, V, kv, scale, probs, ws, ws_bytes, stream,
+                   "kvc_scissorhands_update_queued");
+}
+
+kvc_status kvc_scissorhands_insert(kvc_sh_state* st, const int32_t* queue, int32_t m, int32_t pos,
+                                   const kvc_bf16* k_new, const kvc_bf16* v_new, kvc_bf16* K, kvc_bf16* V,
+                                   const kvc_kv_desc* kv, kvc_stream_t stream) {
+  KVC_TRY(check_sh_insert(st, queue, m, pos, k_new, v_new, K, V, kv, "kvc_scissorhands_insert"));
+  return sh_insert(st, queue, m, pos, k_new, v_new, K, V, kv, stream);
+}
+
+kvc_status kvc_scissorhands_refill_queue(kvc_sh_state* st, int32_t m, int32_t* queue, kvc_stream_t stream) {
   KVC_TRY(check_sh(st));
-  KVC_TRY(check_desc(kv, "kvc_scissorhands_update"));
-  if (kv->B != st->B || kv->KVH != st->KVH || kv->S != st->cap)
-    return fail(KVC_ERR_INVALID_ARG, "scissorhands_update: cache shape does not match the state");
-  if (st->n_free <= 0) return fail(KVC_ERR_INVALID_ARG, "scissorhands_update: no free slot (evict first)");
-  KVC_TRY(check_ptr(q_new, "q_new"));
-  KVC_TRY(check_ptr(k_new, "k_new"));
-  KVC_TRY(check_ptr(K, "K"));
-  KVC_TRY(check_ptr(probs, "probs"));
-  if ((v_new == nullptr) != (V == nullptr)) return fail(KVC_ERR_INVALID_ARG, "v_new and V must both be given or both NULL");
-  KVC_TRY(check_ws(ws, ws_bytes, scores_workspace(*kv, 1, KVC_REDUCE_GQA_GROUP), "kvc_scissorhands_update"));
-  KVC_TRY(cuda_status(launch_sh_insert(*st, k_new, v_new, K, V, *kv, (cudaStream_t)stream), "scissorhands insert launch"));
-  st->n_free -= 1;
-  KVC_TRY(kvc_window_scores(q_new, K, kv, 1, scale, 0, st->live, KVC_REDUCE_GQA_GROUP, probs, ws, ws_bytes, stream));
-  return kvc_scissorhands_update_from_probs(st, probs, stream);
+  if (m < 1 || m > st->cap || m > SH_QUEUE_MAX)
+    return fail(KVC_ERR_INVALID_ARG, "scissorhands_refill_queue: m in [1, min(cap, %d)]", SH_QUEUE_MAX);
+  if (st->t < 1) return fail(KVC_ERR_INVALID_ARG, "scissorhands_refill_queue: no step recorded yet");
+  if (!queue) return fail(KVC_ERR_INVALID_ARG, "queue is NULL");
+  return cuda_status(launch_sh_queue(*st, m, queue, (cudaStream_t)stream), "scissorhands queue launch");
 }
 
 kvc_status kvc_scissorhands_evict(kvc_sh_state* st, int32_t m, int32_t* evicted, kvc_stream_t stream) {

@@ -181,6 +181,8 @@ int64_t topk_max_len();  // longest row kvc_topk_select accepts
 cudaError_t launch_topk(const float* scores, int B, int KVH, int64_t S, int k, int protect_tail,
                         const uint32_t* live, int largest, int32_t* idx, cudaStream_t st);
 cudaError_t launch_sh_evict(const kvc_sh_state& s, int m, int32_t* evicted, cudaStream_t st);
+constexpr int SH_QUEUE_MAX = 2048;  // longest eviction queue launch_sh_queue sorts
+cudaError_t launch_sh_queue(const kvc_sh_state& s, int m, int32_t* queue, cudaStream_t st);
 
 // ----------------------------------------------------------------------------------------
 // gathers (kvc_gather.cu)
@@ -199,8 +201,9 @@ cudaError_t launch_channel_prune(const float* cs, const uint16_t* K, const kvc_k
 // Scissorhands state kernels (kvc_scissorhands.cu)
 // ----------------------------------------------------------------------------------------
 cudaError_t launch_sh_init(const kvc_sh_state& s, int n_live, cudaStream_t st);
-cudaError_t launch_sh_insert(const kvc_sh_state& s, const uint16_t* kn, const uint16_t* vn,
-                             uint16_t* K, uint16_t* V, const kvc_kv_desc& kv, cudaStream_t st);
+// queue == null: the lowest free slot; else the new token replaces slot queue[row * qm + qpos]
+cudaError_t launch_sh_insert(const kvc_sh_state& s, const int32_t* queue, int qm, int qpos, const uint16_t* kn,
+                             const uint16_t* vn, uint16_t* K, uint16_t* V, const kvc_kv_desc& kv, cudaStream_t st);
 cudaError_t launch_sh_record(const kvc_sh_state& s, const float* p, cudaStream_t st);
 
 }  // namespace kvc

@@ -1,5 +1,6 @@
 // Scissorhands state kernels (cold-compress PR 11, "Implement Scissorhands KV-cache
-// compression & SnapKV prompt compression"): slot insertion, and the circular history of
+// compression & SnapKV prompt compression"): slot insertion (into a free slot, or over the
+// next token of an eviction queue), and the circular history of
 // "attention < 1/keys" flags kept as bit planes, one plane per step, with a running count
 // of low flags per slot.  Eviction by low-attention fraction lives with the selection code.
 #include <cuda_runtime.h>
@@ -37,11 +38,13 @@ __global__ void k_sh_init(kvc_sh_state s, int n_live) {
   for (int64_t x = x0; x < rows; x += stride) s.slot[x] = -1;
 }
 
-// one warp per (b,kvh): lowest free slot, mark it live, copy the new K/V row into it
+// One warp per (b,kvh): pick the slot (the lowest free one, or with a queue the slot
+// queue[row][pos], whose token is replaced), mark it live with a fresh insert step and no low
+// flags, and copy the new K/V row into it.
 template <int D>
-__global__ void k_sh_insert(kvc_sh_state s, const uint16_t* __restrict__ kn,
-                            const uint16_t* __restrict__ vn, uint16_t* K, uint16_t* V, int64_t sb,
-                            int64_t sh, int64_t ss) {
+__global__ void k_sh_insert(kvc_sh_state s, const int32_t* __restrict__ queue, int qm, int qpos,
+                            const uint16_t* __restrict__ kn, const uint16_t* __restrict__ vn, uint16_t* K,
+                            uint16_t* V, int64_t sb, int64_t sh, int64_t ss) {
   pdl_wait();  // previous kernel on the stream complete and visible
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
@@ -49,20 +52,27 @@ __global__ void k_sh_insert(kvc_sh_state s, const uint16_t* __restrict__ kn,
   const int nw = s.cap / 32;
   uint32_t* lw = s.live + (int64_t)row * nw;
   int found = -1;
-  for (int base = 0; base < nw; base += 32) {
-    const uint32_t w = (base + lane < nw) ? lw[base + lane] : 0xffffffffu;
-    const uint32_t bal = __ballot_sync(0xffffffffu, w != 0xffffffffu);
-    if (bal) {
-      const int f = __ffs(bal) - 1;
-      const uint32_t word = __shfl_sync(0xffffffffu, w, f);
-      found = (base + f) * 32 + (__ffs(~word) - 1);
-      break;
+  if (queue) {
+    const int32_t q = queue[(int64_t)row * qm + qpos];
+    // a queued slot must hold a live token
+    if (q >= 0 && q < s.cap && ((lw[q >> 5] >> (q & 31)) & 1u)) found = q;
+  } else {
+    for (int base = 0; base < nw; base += 32) {
+      const uint32_t w = (base + lane < nw) ? lw[base + lane] : 0xffffffffu;
+      const uint32_t bal = __ballot_sync(0xffffffffu, w != 0xffffffffu);
+      if (bal) {
+        const int f = __ffs(bal) - 1;
+        const uint32_t word = __shfl_sync(0xffffffffu, w, f);
+        found = (base + f) * 32 + (__ffs(~word) - 1);
+        break;
+      }
     }
   }
   if (found < 0) {
     if (lane == 0) set_device_status(KVC_ERR_DEVICE_BOUNDS);
     return;
   }
+  __syncwarp();  // every lane has read the live word before lane 0 may change it
   if (lane == 0) {
     lw[found >> 5] |= 1u << (found & 31);
     s.insert_step[(int64_t)row * s.cap + found] = (int32_t)s.t;
@@ -127,16 +137,16 @@ cudaError_t launch_sh_init(const kvc_sh_state& s, int n_live, cudaStream_t st) {
   return launched(1);
 }
 
-cudaError_t launch_sh_insert(const kvc_sh_state& s, const uint16_t* kn, const uint16_t* vn,
-                             uint16_t* K, uint16_t* V, const kvc_kv_desc& kv, cudaStream_t st) {
+cudaError_t launch_sh_insert(const kvc_sh_state& s, const int32_t* queue, int qm, int qpos, const uint16_t* kn,
+                             const uint16_t* vn, uint16_t* K, uint16_t* V, const kvc_kv_desc& kv, cudaStream_t st) {
   const int rows = s.B * s.KVH;
   const int blocks = (rows + 7) / 8;
   const cudaError_t e =
       kv.D == 64
-          ? launch_pdl(k_sh_insert<64>, dim3(blocks), dim3(256), 0, st, s, kn, vn, K, V, kv.stride_b, kv.stride_h,
-                       kv.stride_s)
-          : launch_pdl(k_sh_insert<128>, dim3(blocks), dim3(256), 0, st, s, kn, vn, K, V, kv.stride_b, kv.stride_h,
-                       kv.stride_s);
+          ? launch_pdl(k_sh_insert<64>, dim3(blocks), dim3(256), 0, st, s, queue, qm, qpos, kn, vn, K, V,
+                       kv.stride_b, kv.stride_h, kv.stride_s)
+          : launch_pdl(k_sh_insert<128>, dim3(blocks), dim3(256), 0, st, s, queue, qm, qpos, kn, vn, K, V,
+                       kv.stride_b, kv.stride_h, kv.stride_s);
   if (e != cudaSuccess) return e;
   return launched(1);
 }

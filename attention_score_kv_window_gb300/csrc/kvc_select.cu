@@ -389,6 +389,58 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sh_evict(kvc_sh_state s, int m,
   }
 }
 
+// Eviction queue: the m slots bulk eviction would take, listed most evictable first (higher
+// fraction key first, ties to the lower slot).  The selection writes them in slot order; the
+// block then re-sorts the m composites (key, ~slot) descending with a bitonic network in the
+// histogram space the selection no longer needs.  Live bits are not touched.
+__global__ void __launch_bounds__(SEL_THREADS) k_sh_queue(kvc_sh_state s, int m, int32_t* queue) {
+  extern __shared__ __align__(16) uint32_t kc[];
+  __shared__ SelShared sh;
+  pdl_wait();
+  const int64_t row = blockIdx.x;
+  FractionKeys fn;
+  fn.low = s.low_count + row * s.cap;
+  fn.ins = s.insert_step + row * s.cap;
+  fn.lw = s.live + row * (s.cap / 32);
+  fn.t_last = s.t - 1;
+  fn.history = s.history;
+  int32_t* out = queue + row * m;
+  select_row<FractionKeys>(fn, s.cap, m, out, kc, sh, false);
+  __syncthreads();  // the slot-ordered list written by all threads is visible to the block
+  static_assert(sizeof(sh.hsum) >= SH_QUEUE_MAX * sizeof(uint64_t), "queue sort buffer");
+  uint64_t* ck = reinterpret_cast<uint64_t*>(&sh.hsum[0][0]);
+  int n2 = 1;
+  while (n2 < m) n2 <<= 1;
+  for (int p = threadIdx.x; p < n2; p += SEL_THREADS) {
+    uint64_t c = 0;  // empty entries (-1) sort last
+    if (p < m) {
+      const int32_t j = out[p];
+      if (j >= 0) c = ((uint64_t)fn.key(j) << 32) | (uint32_t)~(uint32_t)j;
+    }
+    ck[p] = c;
+  }
+  __syncthreads();
+  for (int size = 2; size <= n2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < (n2 >> 1); i += SEL_THREADS) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const uint64_t x = ck[lo], y = ck[hi];
+        if ((x < y) == desc) {
+          ck[lo] = y;
+          ck[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int p = threadIdx.x; p < m; p += SEL_THREADS) {
+    const uint64_t c = ck[p];
+    out[p] = c ? (int32_t)~(uint32_t)c : -1;
+  }
+}
+
 // ----------------------------------------------------------------------------------------
 // Short rows (S <= 4096, many of them: batched prefill instances, decode steps): one
 // 256-thread CTA per row.  Each eligible item becomes the 64-bit composite (key, tie) with
@@ -623,12 +675,23 @@ cudaError_t launch_topk(const float* scores, int B, int KVH, int64_t S, int k, i
 cudaError_t launch_sh_evict(const kvc_sh_state& s, int m, int32_t* evicted, cudaStream_t st) {
   const size_t smem = (size_t)s.cap * 4;
   if ((int64_t)s.cap > SLICE_MAX) return cudaErrorInvalidValue;
-  // static (histograms) + dynamic (keys) shared memory exceed the 48 KB default: opt in
-  cudaError_t e = cudaFuncSetAttribute(k_sh_evict, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(SLICE_MAX * 4));
+  cudaError_t e = func_attrs_once(reinterpret_cast<const void*>(k_sh_evict), (int)(SLICE_MAX * 4));
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attrs[2];
   const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)(s.B * s.KVH)), dim3(SEL_THREADS), smem, st, attrs);
   e = cudaLaunchKernelEx(&cfg, k_sh_evict, s, m, evicted);
+  if (e != cudaSuccess) return e;
+  return launched(1);
+}
+
+cudaError_t launch_sh_queue(const kvc_sh_state& s, int m, int32_t* queue, cudaStream_t st) {
+  const size_t smem = (size_t)s.cap * 4;
+  if ((int64_t)s.cap > SLICE_MAX || m > SH_QUEUE_MAX) return cudaErrorInvalidValue;
+  cudaError_t e = func_attrs_once(reinterpret_cast<const void*>(k_sh_queue), (int)(SLICE_MAX * 4));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attrs[2];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)(s.B * s.KVH)), dim3(SEL_THREADS), smem, st, attrs);
+  e = cudaLaunchKernelEx(&cfg, k_sh_queue, s, m, queue);
   if (e != cudaSuccess) return e;
   return launched(1);
 }

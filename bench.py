@@ -228,9 +228,12 @@ SCORE_SOURCES = [CSRC + f for f in ("kvc_scores.cu", "kvc_scores_tc.cu", "kvc_in
 
 
 class Call:
-    def __init__(self, label, fn, nbytes, flops=0.0, bound="hbm", sources=None, kernel_key=None):
+    """One library call of a step.  ``roofline=True`` names the call whose roofline the line
+    reports (else the call with the largest share of the instrumented step)."""
+
+    def __init__(self, label, fn, nbytes, flops=0.0, bound="hbm", sources=None, kernel_key=None, roofline=False):
         self.label, self.fn, self.nbytes, self.flops, self.bound = label, fn, nbytes, flops, bound
-        self.sources, self.kernel_key = sources, kernel_key
+        self.sources, self.kernel_key, self.roofline = sources, kernel_key, roofline
         self.times = []
 
 
@@ -449,7 +452,10 @@ class TovaDecodeCase:
 
 class ScissorhandsCase:
     """Scissorhands decode: insert, score the new query over the live slots, record the low-
-    attention flags into the 400-step history; evict m slots per head when the cache is full."""
+    attention flags into the 400-step history.  Policies: bulk eviction of m slots per head
+    when the cache is full; or an eviction queue refilled every m steps once the cache is full,
+    each step's token replacing the next queued one.  With record_every = M > 1 only every
+    M-th step scores and records; the other steps only insert."""
 
     def __init__(self, wl, dev, rank, instances):
         import torch
@@ -467,38 +473,80 @@ class ScissorhandsCase:
             V = torch.randn((B, KVH, cap, D), generator=g, device=dev).to(bf)
             st = kvc.ScissorhandsState(B, KVH, cap, history=wl.history, device=dev)
             kvc.kvc_scissorhands_init(st, wl.prefill_live)
-            self.reps.append((K, V, st, torch.empty((B, KVH, cap), dtype=torch.float32, device=dev),
-                              torch.empty((B, KVH, wl.m), dtype=torch.int32, device=dev)))
+            self.reps.append({"K": K, "V": V, "st": st,
+                              "probs": torch.empty((B, KVH, cap), dtype=torch.float32, device=dev),
+                              "ev": torch.empty((B, KVH, wl.m), dtype=torch.int32, device=dev),
+                              "steps": 0, "pos": wl.m})
         self.nq = 64
         self.q = torch.randn((self.nq, B, H, D), generator=g, device=dev).to(bf)
         self.kn = torch.randn((self.nq, B, KVH, D), generator=g, device=dev).to(bf)
         self.vn = torch.randn((self.nq, B, KVH, D), generator=g, device=dev).to(bf)
-        self.ws = torch.empty(int(kvc.load_library().kvc_workspace_size(4, kvc.kv_desc(self.reps[0][0], H), 1, 0)),
+        self.ws = torch.empty(int(kvc.load_library().kvc_workspace_size(4, kvc.kv_desc(self.reps[0]["K"], H), 1, 0)),
                               dtype=torch.uint8, device=dev)
-        self.B, self.KVH, self.S, self.D = B, KVH, cap, D
+        self.B, self.H, self.KVH, self.S, self.D = B, H, KVH, cap, D
         self.tokens_per_step = B * cap
-        upd = (B * KVH * cap * D * 2 + 2 * B * KVH * D * 2 + 2 * B * KVH * cap * 4 + B * KVH * cap * 4
-               + 2 * B * KVH * cap * 2 + 2 * B * KVH * cap // 8 + B * H * D * 2)
+        rows, slots = B * KVH, B * KVH * cap
+        state = 2 * slots * 4 + slots * 4 + 2 * slots * 2 + 2 * slots // 8  # probs, insert steps, counts, flags
+        new_rows = 2 * rows * D * 2
+        upd = slots * D * 2 + new_rows + state + B * H * D * 2
+        rank_bytes = slots * (2 + 4 + 0.125) + rows * wl.m * 4
+        # the roofline is the update's (score + record over the whole cache); under sparse
+        # recording the insert-only steps are tiny, launch-bound kernels
         self.calls = [Call("scissorhands_update", self._update, upd, 2.0 * B * H * cap * D, "hbm", SCORE_SOURCES,
-                           f"scissorhands/{wl.name}"),
-                      Call("scissorhands_evict", self._evict, B * KVH * cap * (2 + 4 + 0.125) + B * KVH * wl.m * 4)]
-        self.evict_steps = 0
+                           f"scissorhands/{wl.name}", roofline=True)]
+        if wl.record_every > 1:
+            self.calls.append(Call("scissorhands_insert", self._insert, 2 * new_rows + slots // 8 + rows * 12))
+        if wl.policy == "queue":
+            self.calls.insert(0, Call("scissorhands_refill_queue", self._refill, rank_bytes))
+        else:
+            self.calls.append(Call("scissorhands_evict", self._evict, rank_bytes))
+
+    def _queue_args(self, rep):
+        if self.wl.policy != "queue" or rep["st"].n_free > 0:
+            return {}
+        return {"queue": rep["ev"], "pos": rep["pos"]}
+
+    def _refill(self, i):
+        rep = self.reps[i % self.R]
+        if rep["st"].n_free > 0 or rep["pos"] < self.wl.m:
+            return False
+        self.kvc.kvc_scissorhands_refill_queue(rep["st"], self.wl.m, queue=rep["ev"])
+        rep["pos"] = 0
+
+    def _advance(self, rep, qa):
+        rep["steps"] += 1
+        if qa:
+            rep["pos"] += 1
 
     def _update(self, i):
-        K, V, st, probs, ev = self.reps[i % self.R]
+        rep = self.reps[i % self.R]
+        if rep["steps"] % self.wl.record_every:
+            return False
         j = i % self.nq
-        self.kvc.kvc_scissorhands_update(st, self.q[j], self.kn[j], self.vn[j], K, V, self.wl.scale, probs=probs,
-                                         ws=self.ws)
+        qa = self._queue_args(rep)
+        self.kvc.kvc_scissorhands_update(rep["st"], self.q[j], self.kn[j], self.vn[j], rep["K"], rep["V"],
+                                         self.wl.scale, probs=rep["probs"], ws=self.ws, **qa)
+        self._advance(rep, qa)
+
+    def _insert(self, i):
+        rep = self.reps[i % self.R]
+        if rep["steps"] % self.wl.record_every == 0:
+            return False
+        j = i % self.nq
+        qa = self._queue_args(rep)
+        self.kvc.kvc_scissorhands_insert(rep["st"], self.kn[j], self.vn[j], rep["K"], rep["V"], self.H, **qa)
+        self._advance(rep, qa)
 
     def _evict(self, i):
-        K, V, st, probs, ev = self.reps[i % self.R]
-        if st.n_free == 0:
-            self.kvc.kvc_scissorhands_evict(st, self.wl.m, evicted=ev)
+        rep = self.reps[i % self.R]
+        if rep["st"].n_free > 0:
+            return False
+        self.kvc.kvc_scissorhands_evict(rep["st"], self.wl.m, evicted=rep["ev"])
 
     def config(self):
         wl = self.wl
         return {"workload": wl.name, "B": wl.B, "H": wl.H, "KVH": wl.KVH, "D": wl.D, "cap": wl.S,
-                "history": wl.history, "m": wl.m,
+                "history": wl.history, "m": wl.m, "policy": wl.policy, "record_every": wl.record_every,
                 "l2": f"steps rotate over {self.R} caches ({self.R * self.cache_bytes / 2**20:.0f} MiB > L2)"}
 
     def e2e(self, *a):
@@ -534,11 +582,17 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     calls = case.calls
 
-    def step(i, ev=None):
+    # a call's fn returns False when it had nothing to do this step (e.g. eviction while
+    # slots are free); its time is averaged over the steps where it ran
+    ran = [[True] * len(calls) for _ in range(args.steps)]
+
+    def step(i, ev=None, r=None):
         for c, call in enumerate(calls):
             if ev is not None:
                 ev[c].record(stream)
-            call.fn(i)
+            did = call.fn(i) is not False
+            if r is not None:
+                r[c] = did
         if ev is not None:
             ev[len(calls)].record(stream)
 
@@ -592,7 +646,7 @@ def run_ours(args):
                 for i in range(args.steps):
                     for c, call in enumerate(calls):
                         evs[i][c].record(cs)
-                        call.fn(base + i)
+                        ran[i][c] = call.fn(base + i) is not False
                     evs[i][len(calls)].record(cs)
         stream.wait_stream(cap)
     if world > 1:
@@ -618,19 +672,29 @@ def run_ours(args):
         graph_timed.replay()
     else:
         for i in range(args.steps):
-            step(base + i, evs[i])
+            step(base + i, evs[i], ran[i])
     torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
     kernels = {}
     for c, call in enumerate(calls):
-        ts = [e[c].elapsed_time(e[c + 1]) for e in evs]
+        ts = [e[c].elapsed_time(e[c + 1]) for e, r in zip(evs, ran) if r[c]]
+        if not ts:
+            continue
         t = float(np.mean(ts))
-        kernels[call.label] = {"ms": t, "alg_bytes": call.nbytes, "gbs": call.nbytes / (t / 1e3) / 1e9}
+        kernels[call.label] = {"ms": t, "calls": len(ts), "alg_bytes": call.nbytes,
+                               "gbs": call.nbytes / (t / 1e3) / 1e9, "share": t * len(ts)}
         if call.flops:
             kernels[call.label]["tflops"] = call.flops / (t / 1e3) / 1e12
-    dom = max(calls, key=lambda c: kernels[c.label]["ms"])
+    total = sum(k["share"] for k in kernels.values())
+    for k in kernels.values():
+        k["share"] = k["share"] / total
+    # the dominant call takes the largest share of the step (unless the case names one); its
+    # roofline is per launch
+    ran_calls = [c for c in calls if c.label in kernels]
+    named = [c for c in ran_calls if c.roofline]
+    dom = named[0] if named else max(ran_calls, key=lambda c: kernels[c.label]["share"])
     t_dom = kernels[dom.label]["ms"]
     if dom.bound == "tensor":
         achieved = dom.flops / (t_dom / 1e3) / 1e12

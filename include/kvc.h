@@ -253,10 +253,41 @@ kvc_status kvc_scissorhands_update(kvc_sh_state* st, const kvc_bf16* q_new, cons
                                    size_t ws_bytes, kvc_stream_t stream);
 
 /* Evict, per (b,kvh), the m live slots with the highest fraction low_count / n_obs of the
- * last recorded step (compared exactly; ties: lower slot first).  evicted [B,KVH,m] int32
+ * last recorded step (compared exactly; ties: lower slot first; a token not yet observed,
+ * n_obs = 0, counts as fraction 0).  evicted [B,KVH,m] int32
  * out, ascending (-1 padded when fewer are live); their live bits are cleared. */
 kvc_status kvc_scissorhands_evict(kvc_sh_state* st, int32_t m, int32_t* evicted,
                                   kvc_stream_t stream);
+
+/* Eviction-queue variant (cold-compress PR 11 description: instead of evicting in bulk every
+ * m steps, refill an eviction queue every m steps and evict one token per step, so no slot is
+ * left empty).  Fill queue [B,KVH,m] int32 with the m live slots that kvc_scissorhands_evict
+ * would take, listed most evictable first (highest fraction low_count / n_obs, compared
+ * exactly; ties: lower slot first), -1 padded when fewer are live.  Nothing is evicted: live
+ * bits are not touched.  1 <= m <= min(cap, 2048); requires st->t >= 1. */
+kvc_status kvc_scissorhands_refill_queue(kvc_sh_state* st, int32_t m, int32_t* queue,
+                                         kvc_stream_t stream);
+
+/* One decode step of the queue variant: as kvc_scissorhands_update, except that the new token
+ * replaces the token in slot queue[b,kvh,pos] (which must be live; otherwise the row is
+ * skipped and KVC_ERR_DEVICE_BOUNDS is recorded for kvc_get_device_status).  n_free is
+ * unchanged.  0 <= pos < m. */
+kvc_status kvc_scissorhands_update_queued(kvc_sh_state* st, const int32_t* queue, int32_t m,
+                                          int32_t pos, const kvc_bf16* q_new,
+                                          const kvc_bf16* k_new, const kvc_bf16* v_new,
+                                          kvc_bf16* K, kvc_bf16* V, const kvc_kv_desc* kv,
+                                          float scale, float* probs, void* ws, size_t ws_bytes,
+                                          kvc_stream_t stream);
+
+/* Insert the new token without recording: the steps between two observations under sparse
+ * recording (the PR review thread's suggestion: look at attention only every M steps; t and
+ * n_obs then count recordings).  queue == NULL: the lowest free slot (requires n_free > 0;
+ * n_free -= 1).  Otherwise the token replaces slot queue[b,kvh,pos] as in
+ * kvc_scissorhands_update_queued.  The slot gets insert_step = t (its first observation is
+ * the next recording) and low_count = 0; the new rows are written to K/V (S == cap). */
+kvc_status kvc_scissorhands_insert(kvc_sh_state* st, const int32_t* queue, int32_t m, int32_t pos,
+                                   const kvc_bf16* k_new, const kvc_bf16* v_new, kvc_bf16* K,
+                                   kvc_bf16* V, const kvc_kv_desc* kv, kvc_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * kvc_channel_score — ThinK key-channel score ("Add ThinK_Press", kvpress PR 18: the

@@ -8,12 +8,13 @@ Random source: numpy's PCG64 bit generator, seeded with a list ``[seed, tag...]`
 every tensor (and every decode step) has its own independent substream.  bf16 values are
 produced by round-to-nearest-even from float32 draws.
 
-The five workloads follow the shapes of the pages' examples:
+The workloads follow the shapes of the pages' examples:
 
 * TOVA prefill (kvpress PR "Add TOVA press", the last-query head-mean score),
 * SnapKV prefill with a 64-query observation window (cold-compress PR #11, SnapKV paragraph),
 * TOVA decode eviction,
-* Scissorhands decode with a 400-step history (cold-compress PR #11),
+* Scissorhands decode with a 400-step history (cold-compress PR #11), with bulk eviction,
+  with the PR's eviction queue, or with flags recorded only every 8th step,
 * ThinK key-channel pruning after SnapKV (kvpress PR "Add ThinK_Press").
 """
 from __future__ import annotations
@@ -79,6 +80,8 @@ class Workload:
     history: int = 0              # Scissorhands history window
     m: int = 0                    # Scissorhands drop amount / eviction period
     prefill_live: int = 0         # Scissorhands: live tokens at the start of decode
+    policy: str = "bulk"          # Scissorhands: "bulk" eviction every m steps, or an eviction "queue"
+    record_every: int = 1         # Scissorhands: record the flags every M-th step (1: every step)
     C: int = 0                    # ThinK kept key channels
     seed: int = 0
     extra: dict = field(default_factory=dict)
@@ -104,10 +107,13 @@ TOVA_DECODE = Workload("tova_decode_b16_c8192_budget2048", B=16, H=32, KVH=8, D=
 SCISSORHANDS = Workload("scissorhands_decode_b8_cap4096", B=8, H=32, KVH=8, D=128, S=4096, w=1,
                         k=4096, reduce="gqa", causal=False, steps=1024, history=400, m=64,
                         prefill_live=4032)
+SCISSORHANDS_QUEUE = SCISSORHANDS.with_(name="scissorhands_queue_decode_b8_cap4096", policy="queue")
+SCISSORHANDS_SPARSE = SCISSORHANDS.with_(name="scissorhands_sparse8_decode_b8_cap4096", record_every=8)
 THINK_128K = Workload("think_snapkv_prefill_s131072", B=1, H=32, KVH=8, D=128, S=131072, w=64,
                       k=8192, reduce="gqa", protect_tail=64, channel_scales=True, C=64)
 
-WORKLOADS = {wl.name: wl for wl in (TOVA_PREFILL, SNAPKV_32K, TOVA_DECODE, SCISSORHANDS, THINK_128K)}
+WORKLOADS = {wl.name: wl for wl in (TOVA_PREFILL, SNAPKV_32K, TOVA_DECODE, SCISSORHANDS, SCISSORHANDS_QUEUE,
+                                    SCISSORHANDS_SPARSE, THINK_128K)}
 
 
 # ----------------------------------------------------------------------------------------

@@ -354,8 +354,13 @@ def test_scissorhands_update_from_probs_and_evict_exact():
     assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
 
-def test_scissorhands_full_update_teacher_forced():
+@pytest.mark.parametrize("policy", ["bulk", "queue", "sparse"])
+def test_scissorhands_full_update_teacher_forced(policy):
+    """Full decode steps through the library.  bulk: evict m every m steps; queue: once full,
+    refill an eviction queue every m steps and replace one queued token per step; sparse:
+    insert every step, score and record only every M-th step (bulk eviction)."""
     B, H, KVH, D, cap, hist, m = 2, 8, 2, 128, 512, 400, 32
+    M = 3 if policy == "sparse" else 1
     wl = Workload("t", B=B, H=H, KVH=KVH, D=D, S=cap, w=1, k=cap, reduce="gqa", causal=False, seed=51)
     pre = prefill_inputs(wl)
     scale = 1.0 / np.sqrt(D)
@@ -365,31 +370,74 @@ def test_scissorhands_full_update_teacher_forced():
     ref = O.Scissorhands(B, KVH, cap, history=hist)
     ref.prefill(cap - m)
     Kr, Vr = pre["K"].copy(), pre["V"].copy()
-    near_total = 0
-    for step in range(2 * m):
+    queue, rq, pos, refills = None, None, m, 0
+    for step in range((3 if policy == "queue" else 2) * m):
         s = decode_step_inputs(wl, step)
-        probs = kvc.kvc_scissorhands_update(st, dev_bf16(s["q"]), dev_bf16(s["k"]), dev_bf16(s["v"]), Kd, Vd, scale)
-        slot = ref.insert()
+        rep = None
+        if policy == "queue" and ref.live.all():
+            if pos == m:
+                queue = kvc.kvc_scissorhands_refill_queue(st, m)
+                rq = ref.refill_queue(m)
+                np.testing.assert_array_equal(queue.cpu().numpy(), rq)
+                pos, refills = 0, refills + 1
+            rep, pos = pos, pos + 1
+        qa = {} if rep is None else {"queue": queue, "pos": rep}
+        record = step % M == 0
+        if record:
+            probs = kvc.kvc_scissorhands_update(st, dev_bf16(s["q"]), dev_bf16(s["k"]), dev_bf16(s["v"]), Kd, Vd,
+                                                scale, **qa)
+        else:
+            kvc.kvc_scissorhands_insert(st, dev_bf16(s["k"]), dev_bf16(s["v"]), Kd, Vd, H, **qa)
+        slot = ref.insert(replace=None if rep is None else rq[..., rep])
+        np.testing.assert_array_equal(st.slot.cpu().numpy(), slot)
         Kr, Vr = O.write_slots(Kr, Vr, s["k"], s["v"], slot)
-        p_ref = O.scissorhands_probs(s["q"], Kr, scale, ref.live)
-        gp = probs.cpu().numpy()
-        assert_scores_close(gp, p_ref)
-        # flags: identical except where p is within 1e-3/keys of the threshold
-        keys = ref.live.sum(-1, keepdims=True)
-        near = np.abs(p_ref - 1.0 / keys) <= 1e-3 / keys
-        bits_ref = O.low_attention_bits(p_ref, ref.live)
-        bits_gpu = O.low_attention_bits(gp, ref.live)
-        assert np.all((bits_ref == bits_gpu) | near)
-        near_total += int((near & ref.live).sum())
-        ref.record(gp)  # teacher forcing on the GPU's probabilities: counts must then be exact
+        if record:
+            p_ref = O.scissorhands_probs(s["q"], Kr, scale, ref.live)
+            gp = probs.cpu().numpy()
+            assert_scores_close(gp, p_ref)
+            # flags: identical except where p is within 1e-3/keys of the threshold
+            keys = ref.live.sum(-1, keepdims=True)
+            near = np.abs(p_ref - 1.0 / keys) <= 1e-3 / keys
+            bits_ref = O.low_attention_bits(p_ref, ref.live)
+            bits_gpu = O.low_attention_bits(gp, ref.live)
+            assert np.all((bits_ref == bits_gpu) | near)
+            ref.record(gp)  # teacher forcing on the GPU's probabilities: counts must then be exact
+        assert st.t == ref.t
         live, low, ins = _sh_host(st)
         np.testing.assert_array_equal(live, ref.live)
         np.testing.assert_array_equal(np.where(live, low, 0), np.where(ref.live, ref.low, 0))
         np.testing.assert_array_equal(np.where(live, ins, 0), np.where(ref.live, ref.insert_step, 0))
-        if (step + 1) % m == 0:
+        if policy != "queue" and (step + 1) % m == 0:
             ev = kvc.kvc_scissorhands_evict(st, m)
             np.testing.assert_array_equal(ev.cpu().numpy(), ref.evict(m))
     np.testing.assert_array_equal(host_bits(Kd), Kr)
+    np.testing.assert_array_equal(host_bits(Vd), Vr)
+    if policy == "queue":
+        assert refills == 2 and st.n_free == 0
+    assert kvc.kvc_get_device_status() == kvc.KVC_OK
+
+
+def test_scissorhands_refill_queue_exact_with_ties():
+    """Refills on states with many equal fractions (short history, few distinct counts):
+    the queue lists the oracle's order exactly, -1 padded when fewer slots are live."""
+    B, KVH, cap, hist = 2, 3, 320, 3
+    st = kvc.ScissorhandsState(B, KVH, cap, history=hist)
+    kvc.kvc_scissorhands_init(st, cap)
+    ref = O.Scissorhands(B, KVH, cap, history=hist)
+    ref.prefill(cap)
+    g = np.random.Generator(np.random.PCG64([83]))
+    for step in range(12):
+        keys = ref.live.sum(-1, keepdims=True)
+        p = np.where(ref.live, g.random((B, KVH, cap)) * 2.0 / keys, 0.0).astype(np.float32)
+        kvc.kvc_scissorhands_update_from_probs(st, torch.from_numpy(p).cuda())
+        ref.record(p)
+        for m in (1, 7, 64, 300):
+            np.testing.assert_array_equal(kvc.kvc_scissorhands_refill_queue(st, m).cpu().numpy(),
+                                          ref.refill_queue(m))
+        if step % 4 == 3:  # shrink the live set so that some queues need padding
+            np.testing.assert_array_equal(kvc.kvc_scissorhands_evict(st, 100).cpu().numpy(), ref.evict(100))
+    assert ref.live.sum(-1).min() < 300
+    assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
 
 # ----------------------------------------------------------------------------------------

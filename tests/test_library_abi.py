@@ -94,6 +94,20 @@ def test_host_validation_without_gpu(lib):
     assert lib.kvc_scissorhands_update(ctypes.byref(st), FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(d), 0.1, FAKE,
                                        FAKE, 1 << 30, None) == kvc.KVC_ERR_INVALID_ARG
     assert lib.kvc_scissorhands_evict(ctypes.byref(st), 8, FAKE, None) == kvc.KVC_ERR_INVALID_ARG  # t == 0
+    # eviction queue: nothing recorded yet; m above the sort limit; position outside the queue
+    assert lib.kvc_scissorhands_refill_queue(ctypes.byref(st), 8, FAKE, None) == kvc.KVC_ERR_INVALID_ARG
+    st1 = bnd.ShState(1, 2, 4096, 400, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 0)
+    assert lib.kvc_scissorhands_refill_queue(ctypes.byref(st1), 4096, FAKE, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_scissorhands_update_queued(ctypes.byref(st), FAKE, 8, 8, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                              ctypes.byref(d), 0.1, FAKE, FAKE, 1 << 30, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_scissorhands_update_queued(ctypes.byref(st), None, 8, 0, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                              ctypes.byref(d), 0.1, FAKE, FAKE, 1 << 30, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    # insertion without a queue needs a free slot (n_free == 0 here)
+    assert lib.kvc_scissorhands_insert(ctypes.byref(st), None, 0, 0, FAKE, FAKE, FAKE, FAKE, ctypes.byref(d),
+                                       None) == kvc.KVC_ERR_INVALID_ARG
+    assert "free slot" in kvc.load_library().kvc_last_error_message().decode()
 
 
 def test_workspace_size_rules(lib):
