@@ -19,7 +19,7 @@ KVC_OK, KVC_ERR_INVALID_ARG, KVC_ERR_UNSUPPORTED, KVC_ERR_CUDA, KVC_ERR_TIMEOUT,
     KVC_ERR_DEVICE_BOUNDS, KVC_ERR_WORKSPACE = range(7)
 KVC_REDUCE_GQA_GROUP, KVC_REDUCE_ALL_HEADS = 0, 1
 (KVC_OP_WINDOW_SCORES, KVC_OP_TOPK_SELECT, KVC_OP_COMPRESS_PREFILL, KVC_OP_TOVA_DECODE_STEP,
- KVC_OP_SCISSORHANDS_UPDATE, KVC_OP_SCISSORHANDS_EVICT, KVC_OP_CHANNEL_SCORE) = range(7)
+ KVC_OP_SCISSORHANDS_UPDATE, KVC_OP_SCISSORHANDS_EVICT, KVC_OP_CHANNEL_SCORE, KVC_OP_DECODE_ATTENTION) = range(8)
 
 REDUCE = {"gqa": KVC_REDUCE_GQA_GROUP, "all_heads": KVC_REDUCE_ALL_HEADS}
 
@@ -73,6 +73,8 @@ _SIGNATURES = {
     "kvc_scissorhands_insert": (_I32, [_SH, _P, _I32, _I32, _P, _P, _P, _P, _DESC, _P]),
     "kvc_channel_score": (_I32, [_P, _I32, _P, _DESC, _P, _I32, _P, _P, _SZ, _P]),
     "kvc_channel_prune": (_I32, [_P, _P, _DESC, _I32, _I32, _P, _P, _P]),
+    "kvc_decode_attention": (_I32, [_P, _P, _P, _DESC, _P, _DESC, _P, _F, _P, _P, _SZ, _P]),
+    "kvc_zero_add_back": (_I32, [_P, _DESC, _P, _P, _DESC, _P]),
     "kvc_get_device_status": (_I32, [_P]),
     "kvc_status_string": (ctypes.c_char_p, [_I32]),
     "kvc_last_error_message": (ctypes.c_char_p, []),
@@ -394,6 +396,34 @@ def kvc_channel_prune(cs, K, C, zero_mode=False, ch_idx=None, K_out=None, H=None
     _check(lib.kvc_channel_prune(_ptr(cs.contiguous()), _ptr(K), ctypes.byref(desc), int(C), int(bool(zero_mode)),
                                  _ptr(ch_idx), _ptr(K_out), _stream(stream)))
     return ch_idx, K_out
+
+
+def kvc_decode_attention(q, K, V, scale, ch=None, live_mask=None, out=None, ws=None, stream=None):
+    """One new query per head ``q`` [B,H,D] over the cache ``K`` [B,KVH,S,Ck] / ``V``
+    [B,KVH,S,D]; ``ch`` [B,KVH,Ck] lists the key channels K kept (None: Ck == D).
+    Returns ``out`` [B,H,D] float32."""
+    lib = load_library()
+    B, H, D = q.shape
+    kd, vd = kv_desc(K, H), kv_desc(V, H)
+    if out is None:
+        out = torch.empty((B, H, D), dtype=torch.float32, device=q.device)
+    ws, nbytes = _ws(KVC_OP_DECODE_ATTENTION, vd, 0, 0, ws, q.device)
+    _check(lib.kvc_decode_attention(_ptr(q.contiguous()), _ptr(None if ch is None else ch.contiguous()), _ptr(K),
+                                    ctypes.byref(kd), _ptr(V), ctypes.byref(vd),
+                                    _ptr(None if live_mask is None else live_mask.contiguous()), float(scale),
+                                    _ptr(out), _ptr(ws), nbytes, _stream(stream)))
+    return out
+
+
+def kvc_zero_add_back(Kp, ch, D, H=None, K_out=None, stream=None):
+    """Option 3b: the [B,KVH,S,D] key cache rebuilt from the pruned ``Kp`` [B,KVH,S,C]."""
+    B, KVH, S, C = Kp.shape
+    if K_out is None:
+        K_out = torch.empty((B, KVH, S, D), dtype=Kp.dtype, device=Kp.device)
+    pd, od = kv_desc(Kp, H or KVH), kv_desc(K_out, H or KVH)
+    _check(load_library().kvc_zero_add_back(_ptr(Kp), ctypes.byref(pd), _ptr(ch.contiguous()), _ptr(K_out),
+                                             ctypes.byref(od), _stream(stream)))
+    return K_out
 
 
 def kvc_get_device_status(stream=None) -> int:

@@ -12,6 +12,7 @@
 #include <set>
 #include <utility>
 
+#include "kvc_decode.cuh"
 #include "kvc_internal.cuh"
 
 namespace kvc {
@@ -179,6 +180,8 @@ size_t kvc_workspace_size(kvc_op op, const kvc_kv_desc* kv, int32_t w, int32_t k
       return scores_workspace(*kv, 1, KVC_REDUCE_ALL_HEADS);
     case KVC_OP_CHANNEL_SCORE:
       return channel_score_workspace(*kv, k, k > 0);
+    case KVC_OP_DECODE_ATTENTION:
+      return plan_decode(*kv).part_bytes;
     default:
       return (size_t)-1;
   }
@@ -489,11 +492,55 @@ kvc_status kvc_channel_prune(const float* cs, const kvc_bf16* K, const kvc_kv_de
                      "kvc_channel_prune launch");
 }
 
+kvc_status kvc_decode_attention(const kvc_bf16* q, const int32_t* ch, const kvc_bf16* K, const kvc_kv_desc* kd,
+                                const kvc_bf16* V, const kvc_kv_desc* vd, const uint32_t* live_mask, float scale,
+                                float* out, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_TRY(check_desc(kd, "kvc_decode_attention (K)"));
+  KVC_TRY(check_desc(vd, "kvc_decode_attention (V)"));
+  if (kd->B != vd->B || kd->H != vd->H || kd->KVH != vd->KVH || kd->S != vd->S)
+    return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attention: K and V descriptors differ in B, H, KVH or S");
+  if (!decode_shape_supported(kd->D, vd->D))
+    return fail(KVC_ERR_UNSUPPORTED, "kvc_decode_attention: kept key channels must be 64 or 128 and <= D");
+  if (!ch && kd->D != vd->D)
+    return fail(KVC_ERR_INVALID_ARG, "kvc_decode_attention: without a channel list K must keep all D channels");
+  if (kd->stride_s != kd->D || vd->stride_s != vd->D)
+    return fail(KVC_ERR_UNSUPPORTED, "kvc_decode_attention: K and V rows must be dense (stride_s == channels)");
+  if ((int64_t)kd->B * kd->KVH > 65535) return fail(KVC_ERR_UNSUPPORTED, "kvc_decode_attention: B * KVH must be <= 65535");
+  KVC_TRY(check_ptr(q, "q"));
+  KVC_TRY(check_ptr(K, "K"));
+  KVC_TRY(check_ptr(V, "V"));
+  KVC_TRY(check_ptr(out, "out"));
+  if (ch && !aligned16(ch)) return fail(KVC_ERR_INVALID_ARG, "ch not 16-byte aligned");
+  if (live_mask && !aligned16(live_mask)) return fail(KVC_ERR_INVALID_ARG, "live_mask not 16-byte aligned");
+  if (!(scale > 0.f) || scale != scale) return fail(KVC_ERR_INVALID_ARG, "scale must be > 0");
+  KVC_TRY(check_ws(ws, ws_bytes, plan_decode(*vd).part_bytes, "kvc_decode_attention"));
+  return cuda_status(launch_decode_attention(q, ch, K, *kd, V, *vd, live_mask, scale, out, ws, (cudaStream_t)stream),
+                     "kvc_decode_attention launch");
+}
+
+kvc_status kvc_zero_add_back(const kvc_bf16* Kp, const kvc_kv_desc* pd, const int32_t* ch, kvc_bf16* K_out,
+                             const kvc_kv_desc* od, kvc_stream_t stream) {
+  KVC_TRY(check_desc(pd, "kvc_zero_add_back (Kp)"));
+  KVC_TRY(check_desc(od, "kvc_zero_add_back (K_out)"));
+  if (pd->B != od->B || pd->KVH != od->KVH || pd->S != od->S)
+    return fail(KVC_ERR_INVALID_ARG, "kvc_zero_add_back: Kp and K_out descriptors differ in B, KVH or S");
+  if (pd->D > od->D) return fail(KVC_ERR_INVALID_ARG, "kvc_zero_add_back: more kept channels than D");
+  if ((int64_t)od->B * od->KVH > 65535) return fail(KVC_ERR_UNSUPPORTED, "kvc_zero_add_back: B * KVH must be <= 65535");
+  KVC_TRY(check_ptr(Kp, "Kp"));
+  KVC_TRY(check_ptr(K_out, "K_out"));
+  KVC_TRY(check_ptr(ch, "ch"));
+  uintptr_t p0, p1, o0, o1;
+  cache_range(Kp, *pd, &p0, &p1);
+  cache_range(K_out, *od, &o0, &o1);
+  if (overlaps(p0, p1, o0, o1)) return fail(KVC_ERR_INVALID_ARG, "kvc_zero_add_back: K_out overlaps Kp");
+  return cuda_status(launch_zero_add_back(Kp, *pd, ch, K_out, *od, (cudaStream_t)stream), "kvc_zero_add_back launch");
+}
+
 kvc_status kvc_get_device_status(kvc_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "kvc_get_device_status sync");
   cudaError_t (*takers[])(unsigned int*) = {take_status_scores, take_status_select, take_status_gather,
-                                            take_status_scissorhands};
+                                            take_status_scissorhands, take_status_decode};
   unsigned int first = 0u;
   for (auto fn : takers) {
     unsigned int v = 0u;

@@ -553,11 +553,60 @@ class ScissorhandsCase:
         return None
 
 
+class DecodeCase:
+    """Decoding over a compressed cache: one new query per head attends the kept tokens; the
+    keys keep C of the D channels ("Add ThinK_Press" option 3c: the query is pruned to them)
+    or all of them (plain attention)."""
+
+    def __init__(self, wl, dev, rank, instances):
+        import torch
+        import attention_score_kv_window_gb300 as kvc
+        self.kvc, self.torch, self.wl = kvc, torch, wl
+        B, H, KVH, D, S, C = wl.B, wl.H, wl.KVH, wl.D, wl.S, wl.C
+        self.cache_bytes = B * KVH * S * (C + D) * 2
+        self.R = R = max(2, math.ceil(3 * L2_BYTES / self.cache_bytes))
+        g = torch.Generator(device=dev)
+        g.manual_seed(rank_seed(wl.seed, rank))
+        bf = torch.bfloat16
+        self.reps = []
+        for r in range(R):
+            K = torch.randn((B, KVH, S, C), generator=g, device=dev).to(bf)
+            V = torch.randn((B, KVH, S, D), generator=g, device=dev).to(bf)
+            ch = None
+            if C < D:  # a kept-channel list per (b, kvh): C distinct channels, ascending
+                ch = torch.sort(torch.rand((B, KVH, D), generator=g, device=dev).argsort(-1)[..., :C], -1)[0]
+                ch = ch.to(torch.int32).contiguous()
+            self.reps.append((K, V, ch))
+        self.nq = 64
+        self.q = torch.randn((self.nq, B, H, D), generator=g, device=dev).to(bf)
+        self.out = torch.empty((B, H, D), dtype=torch.float32, device=dev)
+        vd = kvc.kv_desc(self.reps[0][1], H)
+        self.ws = torch.empty(int(kvc.load_library().kvc_workspace_size(7, vd, 0, 0)), dtype=torch.uint8, device=dev)
+        self.tokens_per_step = B * S
+        nbytes = self.cache_bytes + B * H * D * 2 + B * H * D * 4 + (B * KVH * C * 4 if C < D else 0)
+        self.calls = [Call("decode_attention", self._step, nbytes, 2.0 * B * H * S * (C + D), "hbm")]
+
+    def _step(self, i):
+        K, V, ch = self.reps[i % self.R]
+        self.kvc.kvc_decode_attention(self.q[i % self.nq], K, V, self.wl.scale, ch=ch, out=self.out, ws=self.ws)
+
+    def config(self):
+        wl = self.wl
+        return {"workload": wl.name, "B": wl.B, "H": wl.H, "KVH": wl.KVH, "D": wl.D, "kept_tokens": wl.S,
+                "key_channels": wl.C, "l2": f"steps rotate over {self.R} caches "
+                                            f"({self.R * self.cache_bytes / 2**20:.0f} MiB > L2)"}
+
+    def e2e(self, *a):
+        return None
+
+
 def make_case(wl, dev, rank, instances):
     if wl.name.startswith("tova_decode"):
         return TovaDecodeCase(wl, dev, rank, instances)
     if wl.name.startswith("scissorhands"):
         return ScissorhandsCase(wl, dev, rank, instances)
+    if "decode_b16_s8192" in wl.name:
+        return DecodeCase(wl, dev, rank, instances)
     return PrefillCase(wl, dev, rank, instances)
 
 

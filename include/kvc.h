@@ -72,7 +72,8 @@ typedef enum {
   KVC_OP_TOVA_DECODE_STEP = 3,
   KVC_OP_SCISSORHANDS_UPDATE = 4,
   KVC_OP_SCISSORHANDS_EVICT = 5,
-  KVC_OP_CHANNEL_SCORE = 6
+  KVC_OP_CHANNEL_SCORE = 6,
+  KVC_OP_DECODE_ATTENTION = 7
 } kvc_op;
 
 /* Bytes of scratch the call `op` needs for these shapes on the current device (w: window
@@ -312,6 +313,36 @@ kvc_status kvc_channel_score(const kvc_bf16* q_win, int32_t w, const kvc_bf16* K
 kvc_status kvc_channel_prune(const float* cs, const kvc_bf16* K, const kvc_kv_desc* kv,
                              int32_t C, int32_t zero_mode, int32_t* ch_idx, kvc_bf16* K_out,
                              kvc_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * kvc_decode_attention — attention of one new query per head over a (compressed) cache, the
+ * decoding step that uses ThinK's smaller key cache ("Add ThinK_Press": option 3c prunes the
+ * query to the kept channels, as the author's reply proposes; with ch == NULL it is plain
+ * decoding attention, which option 3b runs after kvc_zero_add_back).  For each (b, h) with
+ * kvh = h / (H / KVH):
+ *   s_j = scale * sum_c q[b,h,ch[b,kvh,c]] * K[b,kvh,j,c]   over live slots j,
+ *   out[b,h,:] = sum_j softmax(s)_j * V[b,kvh,j,:]          (zeros when no slot is live).
+ *   q [B,H,D] bf16, D = vd->D (the full head); scale: the full head's 1/sqrt(D).
+ *   kd: K [B,KVH,S,Ck] bf16 with Ck = kd->D kept channels (64 or 128, <= D), rows dense
+ *       (stride_s == Ck); ch [B,KVH,Ck] int32 kept channel list, or NULL when Ck == D.
+ *   vd: V [B,KVH,S,D] bf16, rows dense; kd and vd agree on B, H, KVH, S.
+ *   live_mask [B,KVH,ceil(S/32)] or NULL; out [B,H,D] float32.
+ *   ws: kvc_workspace_size(KVC_OP_DECODE_ATTENTION, vd, 0, 0).
+ * An entry of ch outside [0, D) counts as a zero query channel and records
+ * KVC_ERR_DEVICE_BOUNDS for kvc_get_device_status.  B * KVH <= 65535.
+ * ------------------------------------------------------------------------------------- */
+kvc_status kvc_decode_attention(const kvc_bf16* q, const int32_t* ch, const kvc_bf16* K,
+                                const kvc_kv_desc* kd, const kvc_bf16* V, const kvc_kv_desc* vd,
+                                const uint32_t* live_mask, float scale, float* out, void* ws,
+                                size_t ws_bytes, kvc_stream_t stream);
+
+/* kvc_zero_add_back — option 3b of "Add ThinK_Press": rebuild the full-width key cache from
+ * the pruned one, K_out[b,kvh,j,ch[b,kvh,c]] = Kp[b,kvh,j,c] and every other channel 0.
+ *   pd: Kp [B,KVH,S,C] (C = pd->D); od: K_out [B,KVH,S,D] (D = od->D >= C); ch [B,KVH,C]
+ *   int32 (as written by kvc_channel_prune).  K_out must not overlap Kp.  Entries of ch
+ *   outside [0, D) are skipped and record KVC_ERR_DEVICE_BOUNDS. */
+kvc_status kvc_zero_add_back(const kvc_bf16* Kp, const kvc_kv_desc* pd, const int32_t* ch,
+                             kvc_bf16* K_out, const kvc_kv_desc* od, kvc_stream_t stream);
 
 /* Synchronize `stream`, then return (and clear) the sticky device status: KVC_OK,
  * KVC_ERR_DEVICE_BOUNDS or KVC_ERR_TIMEOUT.  KVC_ERR_CUDA if the sync itself failed. */

@@ -481,6 +481,87 @@ def test_channel_prune_in_place_zero():
 # ----------------------------------------------------------------------------------------
 
 
+# ----------------------------------------------------------------------------------------
+# Decoding over the channel-pruned cache (ThinK options 3b / 3c)
+# ----------------------------------------------------------------------------------------
+
+
+def _assert_attention_close(got, ref, V):
+    """fp32 attention outputs against the float64 oracle: |g - r| <= 1e-3 |r| + 1e-4 max|V|
+    (outputs are convex combinations of value rows; the absolute term covers cancellation)."""
+    vmax = float(np.abs(O.as_f64(V)).max())
+    assert_scores_close(got, ref, rtol=1e-3, atol=1e-4 * vmax, what="attention")
+
+
+DECODE_CASES = [
+    # B, H, KVH, D, C (kept key channels; C == D: plain attention), S, live fraction
+    (2, 32, 8, 128, 128, 1000, None),   # ragged last tile
+    (2, 32, 8, 128, 64, 3000, None),    # option 3c: pruned query against pruned keys
+    (1, 4, 4, 64, 64, 777, 0.6),        # one head per KV head, dead slots
+    (1, 16, 2, 128, 128, 500, None),    # 8 heads per KV head: two head groups per range
+    (1, 6, 2, 128, 64, 129, 0.9),       # 3 heads per KV head (padded group)
+    (3, 8, 4, 64, 64, 5, None),         # a single partial tile
+    (1, 8, 2, 128, 64, 64, None),       # exactly one tile
+    (1, 8, 2, 128, 64, 40000, 0.5),     # many key ranges
+]
+
+
+@pytest.mark.parametrize("B,H,KVH,D,C,S,p_live", DECODE_CASES)
+def test_decode_attention_parity(B, H, KVH, D, C, S, p_live):
+    seed = B * 1000 + S
+    q = normal_bf16((B, H, D), seed, 1)
+    K = normal_bf16((B, KVH, S, D), seed, 2)
+    V = normal_bf16((B, KVH, S, D), seed, 3)
+    scale = 1.0 / np.sqrt(D)
+    live = None
+    if p_live is not None:
+        live = random_live_mask((B, KVH, S), seed, p_live)
+        live[0, 0, :] = False  # a KV head with no live slot: zeros
+    if C < D:
+        cs = random_scores((B, KVH, D), seed + 1)
+        ch, Kp = O.channel_prune(cs, K, C)
+        ref = O.decode_attention_pruned(q, ch, Kp, V, scale, live)
+        got = kvc.kvc_decode_attention(dev_bf16(q), dev_bf16(Kp), dev_bf16(V), scale, ch=dev_i32(ch),
+                                       live_mask=None if live is None else dev_u32(pack_live_bits(live)))
+    else:
+        ref = O.decode_attention(q, K, V, scale, live)
+        got = kvc.kvc_decode_attention(dev_bf16(q), dev_bf16(K), dev_bf16(V), scale,
+                                       live_mask=None if live is None else dev_u32(pack_live_bits(live)))
+    _assert_attention_close(got.cpu().numpy(), ref, V)
+    if live is not None:
+        assert np.all(got[0, :H // KVH].cpu().numpy() == 0)
+    assert kvc.kvc_get_device_status() == kvc.KVC_OK
+
+
+def test_zero_add_back_bit_exact_and_3b_equals_3c():
+    B, H, KVH, D, C, S = 2, 16, 4, 128, 64, 700
+    q = normal_bf16((B, H, D), 95, 1)
+    K = normal_bf16((B, KVH, S, D), 95, 2)
+    V = normal_bf16((B, KVH, S, D), 95, 3)
+    cs = O.channel_score(normal_bf16((B, H, 8, D), 95, 4), K)
+    ch, Kp = O.channel_prune(cs, K, C)
+    Kz = kvc.kvc_zero_add_back(dev_bf16(Kp), dev_i32(ch), D)
+    np.testing.assert_array_equal(host_bits(Kz), O.zero_add_back(Kp, ch, D))
+    scale = 1.0 / np.sqrt(D)
+    o3b = kvc.kvc_decode_attention(dev_bf16(q), Kz, dev_bf16(V), scale).cpu().numpy()
+    o3c = kvc.kvc_decode_attention(dev_bf16(q), dev_bf16(Kp), dev_bf16(V), scale, ch=dev_i32(ch)).cpu().numpy()
+    ref = O.decode_attention_pruned(q, ch, Kp, V, scale)
+    _assert_attention_close(o3b, ref, V)
+    _assert_attention_close(o3c, ref, V)
+
+
+def test_decode_attention_bad_channel_reports_bounds():
+    B, H, KVH, D, C, S = 1, 4, 2, 128, 64, 100
+    q = dev_bf16(normal_bf16((B, H, D), 96, 1))
+    Kp = dev_bf16(normal_bf16((B, KVH, S, C), 96, 2))
+    V = dev_bf16(normal_bf16((B, KVH, S, D), 96, 3))
+    ch = np.tile(np.arange(C, dtype=np.int32), (B, KVH, 1))
+    ch[0, 1, 5] = 500  # outside [0, D): counted as a zero query channel, reported
+    kvc.kvc_decode_attention(q, Kp, V, 0.1, ch=dev_i32(ch))
+    assert kvc.kvc_get_device_status() == kvc.KVC_ERR_DEVICE_BOUNDS
+    assert kvc.kvc_get_device_status() == kvc.KVC_OK  # read-and-clear
+
+
 def test_invalid_arguments_raise_and_enqueue_nothing():
     K = dev_bf16(normal_bf16((1, 2, 64, 64), 1, 1))
     q = dev_bf16(normal_bf16((1, 6, 1, 64), 1, 2))  # H=6 not a multiple of... 6 % 2 == 0 -> ok

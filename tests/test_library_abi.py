@@ -108,6 +108,22 @@ def test_host_validation_without_gpu(lib):
     assert lib.kvc_scissorhands_insert(ctypes.byref(st), None, 0, 0, FAKE, FAKE, FAKE, FAKE, ctypes.byref(d),
                                        None) == kvc.KVC_ERR_INVALID_ARG
     assert "free slot" in kvc.load_library().kvc_last_error_message().decode()
+    # decoding attention: K keeps 64 of 128 channels but no channel list; K and V disagree on S
+    kd, vd = _desc(D=64, S=128), _desc(D=128, S=128)
+    assert lib.kvc_decode_attention(FAKE, None, FAKE, ctypes.byref(kd), FAKE, ctypes.byref(vd), None, 0.1, FAKE,
+                                    FAKE, 1 << 30, None) == kvc.KVC_ERR_INVALID_ARG
+    vd2 = _desc(D=128, S=64)
+    assert lib.kvc_decode_attention(FAKE, FAKE, FAKE, ctypes.byref(kd), FAKE, ctypes.byref(vd2), None, 0.1, FAKE,
+                                    FAKE, 1 << 30, None) == kvc.KVC_ERR_INVALID_ARG
+    # keys wider than the values, and strided (non-dense) rows are refused
+    assert lib.kvc_decode_attention(FAKE, FAKE, FAKE, ctypes.byref(vd), FAKE, ctypes.byref(kd), None, 0.1, FAKE,
+                                    FAKE, 1 << 30, None) == kvc.KVC_ERR_UNSUPPORTED
+    strided = bnd.KvDesc(1, 8, 2, 128, 128, 2 * 128 * 256, 128 * 256, 256)
+    assert lib.kvc_decode_attention(FAKE, None, FAKE, ctypes.byref(strided), FAKE, ctypes.byref(vd), None, 0.1,
+                                    FAKE, FAKE, 1 << 30, None) == kvc.KVC_ERR_UNSUPPORTED
+    # zero add-back: output overlapping the pruned input
+    assert lib.kvc_zero_add_back(FAKE, ctypes.byref(kd), FAKE * 2, FAKE + 64, ctypes.byref(vd), None) \
+        == kvc.KVC_ERR_INVALID_ARG
 
 
 def test_workspace_size_rules(lib):
