@@ -446,11 +446,12 @@ __device__ __forceinline__ uint32_t cluster_addr_s(const void* local, int rank) 
   return ra;
 }
 
-template <int D>
+template <int D, bool R16>
 __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a, int64_t per) {
   pdl_wait();  // previous kernel on the stream complete and visible
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int P = D + 8, KS = D / 16;
+  constexpr int RM = R16 ? 16 : 8;  // query rows the accumulators can hold
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   unsigned int cs, cr;
   asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(cs));
@@ -460,6 +461,7 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
   const int R = a.R;
   const int64_t kbeg = (int64_t)cr * per;
   const int64_t kend = min(a.S, kbeg + per);
+  const int len = kend > kbeg ? (int)(kend - kbeg) : 0;
 
   uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);
   uint16_t* Ks = Qs + 16 * P;
@@ -489,17 +491,23 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
   constexpr int WST = SMALL_STAGES;       // stages per warp
   static_assert(8 * WST * 8 == SMALL_STAGES * TK, "per-warp rings fill the K staging area");
   constexpr int CH = D / 8;               // 16-byte pieces per key row
-  uint16_t* Kw = Ks + warp * WST * 8 * P;
-  const int64_t nchunks = (kend - kbeg + 7) / 8;
-  const int my = nchunks > warp ? (int)((nchunks - warp + 7) / 8) : 0;
+  constexpr int PPL = 8 * CH / 32;        // pieces per lane per chunk
+  const uint32_t ring = smem_u32(Ks + warp * WST * 8 * P);
+  const int nchunks = (len + 7) / 8;
+  const int my = nchunks > warp ? (nchunks - warp + 7) / 8 : 0;
+  // this lane's pieces of a chunk: rows r0 + RPP * u, the same 16 bytes of each
+  constexpr int RPP = 32 / CH;            // key rows per 32 pieces
+  const int r0 = lane / CH, cc = lane % CH;
+  const uint32_t dlane = (uint32_t)(r0 * P + cc * 8) * 2;
+  const int64_t slane = (int64_t)r0 * a.ss + cc * 8;
   auto load_chunk = [&](int i, int st) {
-    const int64_t k0 = kbeg + (int64_t)(warp + 8 * i) * 8;
+    const int k0 = (warp + 8 * i) * 8;  // slice-relative
+    const uint16_t* src0 = Kb + (kbeg + k0) * a.ss + slane;
+    const uint32_t dst0 = ring + (uint32_t)(st * 8 * P) * 2 + dlane;
 #pragma unroll
-    for (int c = lane; c < 8 * CH; c += 32) {
-      const int r = c / CH, cc = c % CH;
-      const int64_t j = k0 + r;
-      const bool ok = j < kend;
-      cp_async16(smem_u32(Kw + (st * 8 + r) * P + cc * 8), ok ? (Kb + j * a.ss + cc * 8) : Kb, ok ? 16 : 0);
+    for (int u = 0; u < PPL; ++u) {
+      const bool ok = k0 + r0 + RPP * u < len;
+      cp_async16(dst0 + (uint32_t)(RPP * u * P) * 2, ok ? src0 + (int64_t)RPP * u * a.ss : Kb, ok ? 16 : 0);
     }
   };
 #pragma unroll
@@ -507,9 +515,13 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
     if (st < my) load_chunk(st, st);
     cp_async_commit();
   }
-  // row limits of the two rows this lane's accumulator fragment holds
-  const int64_t limA = (g < R) ? (a.causal ? a.S - a.w + (g % a.w) : a.S - 1) : -1;
-  const int64_t limB = (g + 8 < R) ? (a.causal ? a.S - a.w + ((g + 8) % a.w) : a.S - 1) : -1;
+  // row limits of the two rows this lane's accumulator fragment holds (slice-relative)
+  const int64_t limA = (g < R) ? (a.causal ? a.S - a.w + (g % a.w) : a.S - 1) - kbeg : -1;
+  const int64_t limB = (R16 && g + 8 < R) ? (a.causal ? a.S - a.w + ((g + 8) % a.w) : a.S - 1) - kbeg : -1;
+  float* lgA = lg + (int64_t)g * per;
+  float* lgB = lg + (int64_t)(g + 8) * per;
+  // running (max, sum) of rows g and g + 8 over this lane's keys, log2 domain
+  float mA = -CUDART_INF_F, lA = 0.f, mB = -CUDART_INF_F, lB = 0.f;
   for (int i = 0; i < my; ++i) {
     cp_async_wait<WST - 2>();
     __syncwarp();  // the chunk's rows, copied by all lanes, are visible; stage (i-1) % WST is free
@@ -518,74 +530,65 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
       if (nx < my) load_chunk(nx, nx % WST);
       cp_async_commit();
     }
-    const uint16_t* Kt = Kw + (i % WST) * 8 * P;
+    const uint32_t kt = ring + (uint32_t)((i % WST) * 8 * P) * 2;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks2 = 0; ks2 < KS / 2; ++ks2) {
       uint32_t b0, b1, b2, b3;
-      ldsm_x4(smem_u32(Kt + (lane & 7) * P + ks2 * 32 + (lane >> 3) * 8), b0, b1, b2, b3);
+      ldsm_x4(kt + (uint32_t)((lane & 7) * P + ks2 * 32 + (lane >> 3) * 8) * 2, b0, b1, b2, b3);
       mma16816(c, aq[2 * ks2], b0, b1);
       mma16816(c, aq[2 * ks2 + 1], b2, b3);
     }
-    const int64_t j0 = kbeg + (int64_t)(warp + 8 * i) * 8 + 2 * t;
+    const int j0 = (warp + 8 * i) * 8 + 2 * t;  // slice-relative key of c[0]
+    float sA[2], sB[2];
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int64_t j = j0 + e;
-      const bool in = j < kend;
-      const bool lv = in && (lw == nullptr || live_bit(lw, j));
-      if (g < R && in) lg[(int64_t)g * per + (j - kbeg)] = (lv && j <= limA) ? c[e] * a.sl2 : -CUDART_INF_F;
-      if (g + 8 < R && in) lg[(int64_t)(g + 8) * per + (j - kbeg)] = (lv && j <= limB) ? c[2 + e] * a.sl2 : -CUDART_INF_F;
+      const int j = j0 + e;
+      const bool in = j < len;
+      const bool lv = in && (lw == nullptr || live_bit(lw, kbeg + j));
+      sA[e] = (lv && j <= limA) ? c[e] * a.sl2 : -CUDART_INF_F;
+      sB[e] = (lv && j <= limB) ? c[2 + e] * a.sl2 : -CUDART_INF_F;
+      if (g < R && in) lgA[j] = sA[e];
+      if (R16 && g + 8 < R && in) lgB[j] = sB[e];
+    }
+    {
+      const float mn = fmaxf(mA, fmaxf(sA[0], sA[1]));
+      if (mn != -CUDART_INF_F) {
+        lA = lA * ex2(mA - mn) + ex2(sA[0] - mn) + ex2(sA[1] - mn);
+        mA = mn;
+      }
+    }
+    if (R16) {
+      const float mn = fmaxf(mB, fmaxf(sB[0], sB[1]));
+      if (mn != -CUDART_INF_F) {
+        lB = lB * ex2(mB - mn) + ex2(sB[0] - mn) + ex2(sB[1] - mn);
+        mB = mn;
+      }
     }
   }
   cp_async_wait<0>();
-  __syncthreads();
 
-  // per-row max, then sum of exp2(logit - max), over this CTA's slice
-  const int64_t len = kend > kbeg ? kend - kbeg : 0;
-  float mx[16], sm[16];
-#pragma unroll
-  for (int r = 0; r < 16; ++r) mx[r] = -CUDART_INF_F;
-  for (int64_t j = tid; j < len; j += NTHREADS)
-#pragma unroll
-    for (int r = 0; r < 16; ++r)
-      if (r < R) mx[r] = fmaxf(mx[r], lg[(int64_t)r * per + j]);
-#pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    if (r < R) {
-#pragma unroll
-      for (int o = 16; o; o >>= 1) mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], o));
-      if (lane == 0) red[warp * 16 + r].x = mx[r];
+  // rows' (max, sum): the 4 lanes of a row, then the 8 warps, then the cluster's CTAs
+  auto merge2 = [](float& m, float& l, float m2, float l2) {
+    const float mn = fmaxf(m, m2);
+    if (mn != -CUDART_INF_F) {
+      l = l * ex2(m - mn) + l2 * ex2(m2 - mn);
+      m = mn;
     }
+  };
+#pragma unroll
+  for (int o = 1; o < 4; o <<= 1) {
+    merge2(mA, lA, __shfl_xor_sync(0xffffffffu, mA, o), __shfl_xor_sync(0xffffffffu, lA, o));
+    if (R16) merge2(mB, lB, __shfl_xor_sync(0xffffffffu, mB, o), __shfl_xor_sync(0xffffffffu, lB, o));
   }
-  __syncthreads();
-#pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    if (r < R) {
-      float m = -CUDART_INF_F;
-      for (int q = 0; q < NTHREADS / 32; ++q) m = fmaxf(m, red[q * 16 + r].x);
-      mx[r] = m;
-      sm[r] = 0.f;
-    }
+  if (t == 0) {
+    red[warp * 16 + g] = make_float2(mA, lA);
+    red[warp * 16 + g + 8] = make_float2(mB, lB);
   }
-  for (int64_t j = tid; j < len; j += NTHREADS)
-#pragma unroll
-    for (int r = 0; r < 16; ++r)
-      if (r < R && mx[r] != -CUDART_INF_F) sm[r] += ex2(lg[(int64_t)r * per + j] - mx[r]);
-#pragma unroll
-  for (int r = 0; r < 16; ++r) {
-    if (r < R) {
-#pragma unroll
-      for (int o = 16; o; o >>= 1) sm[r] += __shfl_xor_sync(0xffffffffu, sm[r], o);
-      if (lane == 0) red[warp * 16 + r].y = sm[r];
-    }
-  }
-  __syncthreads();
-  // this CTA's (m, l) per row, pushed into slot [cr] of every CTA of the cluster
+  __syncthreads();  // logits and warp partials complete
   if (tid < R) {
-    float l = 0.f;
-    for (int q = 0; q < NTHREADS / 32; ++q) l += red[q * 16 + tid].y;
-    float mm = -CUDART_INF_F;
-    for (int q = 0; q < NTHREADS / 32; ++q) mm = fmaxf(mm, red[q * 16 + tid].x);
+    float mm = -CUDART_INF_F, l = 0.f;
+    for (int q = 0; q < NTHREADS / 32; ++q) merge2(mm, l, red[q * 16 + tid].x, red[q * 16 + tid].y);
     for (unsigned int p = 0; p < cs; ++p) {
       const uint32_t ra = cluster_addr_s(&xch[cr * 16 + tid], (int)p);
       asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(ra), "f"(mm), "f"(l) : "memory");
@@ -596,22 +599,21 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
     float M = -CUDART_INF_F, L = 0.f;
     for (unsigned int p = 0; p < cs; ++p) {
       const float2 o = xch[p * 16 + tid];
-      if (o.y > 0.f) M = fmaxf(M, o.x);
-    }
-    for (unsigned int p = 0; p < cs; ++p) {
-      const float2 o = xch[p * 16 + tid];
-      if (o.y > 0.f) L += o.y * ex2(o.x - M);
+      if (o.y > 0.f) merge2(M, L, o.x, o.y);
     }
     crow[tid] = L > 0.f ? M + log2f(L) : CUDART_INF_F;
   }
   __syncthreads();
-  float* out = a.out + (int64_t)bk * a.S;
-  for (int64_t j = tid; j < len; j += NTHREADS) {
-    float s = 0.f;
+  float* out = a.out + (int64_t)bk * a.S + kbeg;
+  float cv[RM];
 #pragma unroll
-    for (int r = 0; r < 16; ++r)
-      if (r < R) s += ex2(lg[(int64_t)r * per + j] - crow[r]);
-    out[kbeg + j] = s * a.out_mul;
+  for (int r = 0; r < RM; ++r) cv[r] = r < R ? crow[r] : 0.f;
+  for (int j = tid; j < len; j += NTHREADS) {
+    float sc = 0.f;
+#pragma unroll
+    for (int r = 0; r < RM; ++r)
+      if (r < R) sc += ex2(lg[(int64_t)r * per + j] - cv[r]);
+    out[j] = sc * a.out_mul;
   }
   // no remote access follows the cluster barrier: CTAs may leave independently
 }
@@ -649,9 +651,12 @@ cudaError_t set_smem_attrs() {
   e = cudaFuncSetAttribute(k_scores_pass2<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem_pass2(D, MAX_RPAD));
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_scores_small<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem_small(D, 16, SMALL_LOGIT_BYTES / (16 * 4)) + 1024);
-  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+  for (auto kern : {k_scores_small<D, false>, k_scores_small<D, true>}) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_small(D, 16, SMALL_LOGIT_BYTES / (16 * 4)) + 1024);
+    if (e != cudaSuccess) return e;
+  }
+  if (dev >= 0 && dev < 64) done[dev] = true;
   return e;
 }
 
@@ -676,7 +681,7 @@ cudaError_t launch_small(const ScoresArgs& a, int cs, int64_t per, cudaStream_t 
   cudaLaunchAttribute attrs[2];
   const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)((int64_t)a.B * a.KVH * cs)), dim3(NTHREADS),
                                             smem_small(D, a.R, per), st, attrs, cs);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_scores_small<D>, a, per);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, a.R > 8 ? k_scores_small<D, true> : k_scores_small<D, false>, a, per);
   if (e != cudaSuccess) return e;
   return launched(1);
 }
