@@ -590,6 +590,134 @@ __global__ void __launch_bounds__(SHORT_THREADS) k_topk_short(const float* __res
   for (int p = (int)total + tid; p < k; p += SHORT_THREADS) out[p] = -1;
 }
 
+// Rows of at most 32 * NU keys (batched short prefill instances): one warp per row, lane l
+// holding keys l + 32 u in registers.  A radix select over the 32-bit ranking key (four 8-bit
+// digits, a 256-bin histogram per warp in shared memory) finds the need-th key T and how many
+// keys equal to T are taken (the first ones in index order when keeping, the last ones when
+// evicting); the output pass walks u in order and places taken keys with ballots, so the
+// indices come out ascending.
+constexpr int WARP_ROWS_PER_CTA = 8;
+
+template <int NU>
+__global__ void __launch_bounds__(WARP_ROWS_PER_CTA * 32) k_topk_warp(const float* __restrict__ scores, int S, int k,
+                                                                     int protect, const uint32_t* __restrict__ live,
+                                                                     int largest, int32_t* __restrict__ idx,
+                                                                     int64_t rows) {
+  __shared__ uint32_t hist[WARP_ROWS_PER_CTA][256];
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * WARP_ROWS_PER_CTA + warp;
+  if (row >= rows) return;
+  ScoreKeys fn;
+  fn.row = scores + row * (int64_t)S;
+  fn.lw = live ? live + row * (((int64_t)S + 31) / 32) : nullptr;
+  fn.S = S;
+  fn.protect = protect;
+  fn.largest = largest;
+  uint32_t key[NU];
+  uint32_t elig = 0u, forc = 0u;  // bit u: key u of this lane is eligible / forced
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    const int j = lane + 32 * u;
+    key[u] = 0u;
+    if (j < S) {
+      if (fn.forced(j)) forc |= 1u << u;
+      else if (fn.eligible(j)) {
+        elig |= 1u << u;
+        key[u] = fn.key(j);
+      }
+    }
+  }
+  int n_forced = __popc(forc), n_elig = __popc(elig);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    n_forced += __shfl_xor_sync(0xffffffffu, n_forced, o);
+    n_elig += __shfl_xor_sync(0xffffffffu, n_elig, o);
+  }
+  const int need = k - n_forced > 0 ? k - n_forced : 0;
+  const bool take_all = n_elig <= need;
+  uint32_t T = 0u, prefix_mask = 0u;
+  int take_eq = 0, eq_total = 0;
+  if (!take_all && need > 0) {
+    uint32_t* h = hist[warp];
+    int rem = need;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) h[lane * 8 + q] = 0u;
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < NU; ++u)
+        if (((elig >> u) & 1u) && (key[u] & prefix_mask) == T) atomicAdd(&h[(key[u] >> shift) & 255u], 1u);
+      __syncwarp();
+      // lane l scans bins 255 - 8 l ... 248 - 8 l (descending digits)
+      uint32_t hb[8], tot = 0u;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        hb[q] = h[255 - 8 * lane - q];
+        tot += hb[q];
+      }
+      uint32_t incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t excl = incl - tot;
+      const bool mine = excl < (uint32_t)rem && (uint32_t)rem <= incl;
+      uint32_t digit = 0u, above = 0u, inbin = 0u;
+      if (mine) {
+        uint32_t run = excl;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (run + hb[q] >= (uint32_t)rem) {
+            digit = 255u - 8u * lane - q;
+            above = run;
+            inbin = hb[q];
+            break;
+          }
+          run += hb[q];
+        }
+      }
+      const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+      digit = __shfl_sync(0xffffffffu, digit, src);
+      above = __shfl_sync(0xffffffffu, above, src);
+      inbin = __shfl_sync(0xffffffffu, inbin, src);
+      T |= digit << shift;
+      prefix_mask |= 255u << shift;
+      rem -= (int)above;
+      eq_total = (int)inbin;
+      __syncwarp();  // the histogram is read before the next pass clears it
+    }
+    take_eq = rem;
+  }
+  // equal keys: the first take_eq in index order when keeping, the last take_eq when evicting
+  const int skip_eq = largest ? 0 : eq_total - take_eq;
+  const bool split = !take_all && need > 0;
+  int32_t* out = idx + row * (int64_t)k;
+  const uint32_t lower = (1u << lane) - 1u;
+  int pos = 0, eq_seen = 0;
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    const bool f = (forc >> u) & 1u;
+    const bool e = (elig >> u) & 1u;
+    const bool sure = f || (e && (take_all || (split && key[u] > T)));
+    const bool eq = split && e && key[u] == T;
+    const uint32_t be = __ballot_sync(0xffffffffu, eq);
+    const int eb = eq_seen + __popc(be & lower);
+    const bool take = sure || (eq && eb >= skip_eq && eb < skip_eq + take_eq);
+    const uint32_t bt = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const int p = pos + __popc(bt & lower);
+      if (p < k) out[p] = lane + 32 * u;
+    }
+    pos += __popc(bt);
+    eq_seen += __popc(be);
+  }
+  for (int p = pos + lane; p < k; p += 32) out[p] = -1;
+}
+
 // k = 1 without a protected tail (a TOVA decode step evicts one slot per row): one 256-thread
 // CTA per row takes the maximum of the same (key, tie) composites as k_topk_short, so the
 // ranking is identical; -1 when nothing is eligible.  Finite scores give keys >= 1, so every
@@ -647,6 +775,19 @@ cudaError_t launch_topk(const float* scores, int B, int KVH, int64_t S, int k, i
   if (k == 1 && protect_tail == 0) {
     const cudaError_t e =
         launch_pdl(k_top1, dim3((unsigned)((int64_t)B * KVH)), dim3(SHORT_THREADS), 0, st, scores, S, live, largest, idx);
+    if (e != cudaSuccess) return e;
+    return launched(1);
+  }
+  if (S <= 1024) {
+    const int64_t rows = (int64_t)B * KVH;
+    const dim3 grid((unsigned)((rows + WARP_ROWS_PER_CTA - 1) / WARP_ROWS_PER_CTA));
+    const dim3 block(WARP_ROWS_PER_CTA * 32);
+    const int Si = (int)S;
+    cudaError_t e;
+    if (S <= 128) e = launch_pdl(k_topk_warp<4>, grid, block, 0, st, scores, Si, k, protect_tail, live, largest, idx, rows);
+    else if (S <= 256) e = launch_pdl(k_topk_warp<8>, grid, block, 0, st, scores, Si, k, protect_tail, live, largest, idx, rows);
+    else if (S <= 512) e = launch_pdl(k_topk_warp<16>, grid, block, 0, st, scores, Si, k, protect_tail, live, largest, idx, rows);
+    else e = launch_pdl(k_topk_warp<32>, grid, block, 0, st, scores, Si, k, protect_tail, live, largest, idx, rows);
     if (e != cudaSuccess) return e;
     return launched(1);
   }

@@ -144,6 +144,14 @@ TOPK_CASES = [
     (3, 2, 5000, 1, 0, 0, True, 0.5),          # k = 1 (one CTA per row), keep, live mask
     (2, 3, 70000, 1, 0, 4, False, None),       # k = 1, evict, long rows with ties
     (1, 2, 100, 1, 0, 0, True, 0.0),           # k = 1, nothing live -> -1
+    # one warp per row (S <= 1024): 4, 8, 16 and 32 keys per lane
+    (64, 4, 512, 256, 0, 3, True, None),       # many rows, heavy ties
+    (8, 2, 1024, 1000, 20, 0, True, None),
+    (8, 2, 1024, 517, 0, 9, False, 0.7),       # evict with ties and dead slots
+    (5, 3, 200, 100, 32, 4, True, 0.8),
+    (3, 3, 128, 2, 0, 2, False, None),
+    (2, 2, 300, 299, 0, 0, True, None),
+    (1, 1, 1, 1, 0, 0, True, None),
 ]
 
 
