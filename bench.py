@@ -225,6 +225,7 @@ def _traffic(kernel_key, sources):
 
 CSRC = "attention_score_kv_window_gb300/csrc/"
 SCORE_SOURCES = [CSRC + f for f in ("kvc_scores.cu", "kvc_scores_tc.cu", "kvc_internal.cuh")]
+DECODE_SOURCES = [CSRC + f for f in ("kvc_decode.cu", "kvc_decode.cuh")]
 
 
 class Call:
@@ -584,7 +585,8 @@ class DecodeCase:
         self.ws = torch.empty(int(kvc.load_library().kvc_workspace_size(7, vd, 0, 0)), dtype=torch.uint8, device=dev)
         self.tokens_per_step = B * S
         nbytes = self.cache_bytes + B * H * D * 2 + B * H * D * 4 + (B * KVH * C * 4 if C < D else 0)
-        self.calls = [Call("decode_attention", self._step, nbytes, 2.0 * B * H * S * (C + D), "hbm")]
+        self.calls = [Call("decode_attention", self._step, nbytes, 2.0 * B * H * S * (C + D), "hbm", DECODE_SOURCES,
+                           f"decode_attention/{wl.name}")]
 
     def _step(self, i):
         K, V, ch = self.reps[i % self.R]
