@@ -39,7 +39,7 @@ import numpy as np
 __all__ = [
     "as_f64", "visible_mask", "window_softmax", "window_scores", "topk_select", "compact_kv",
     "write_slots", "channel_score", "channel_score_bruteforce", "channel_prune",
-    "compress_prefill", "zero_add_back", "decode_attention", "decode_attention_pruned",
+    "compress_prefill", "value_channel_score", "zero_add_back", "decode_attention", "decode_attention_pruned",
     "tova_first_step", "tova_decode_step", "Scissorhands",
     "scissorhands_probs", "low_attention_bits", "fraction_rank_table",
 ]
@@ -314,6 +314,34 @@ def channel_prune(cs, K, C: int, zero_mode: bool = False):
             else:
                 out[b, kv] = K[b, kv][:, sel]
     return ch, out
+
+
+def value_channel_score(q, Kc, Vc, scale: float, causal: bool = True) -> np.ndarray:
+    """ThinK value-channel score [B, KVH, D] ("Add ThinK_Press" names value pruning without
+    defining it; this is the key score's definition carried over to values).
+
+    The key score sums, over window rows i and kept tokens j, the squared contribution
+    ``(q_id k_jd)^2`` of channel d to the logit s_ij.  Channel d of value row j contributes
+    ``p_ij v_jd`` to output channel d of row i, so the value score is
+    ``cs_v[b,kvh,d] = mean_{h in group} sum_i sum_j (p_hij v_jd)^2``, where ``p`` is the window's
+    attention over the compressed cache ``Kc`` (tokens first, then channels): the window rows
+    are the last w tokens of ``Kc`` (SnapKV keeps them), so the causal rule of the compressed
+    cache is the ordinary one on its own indices."""
+    q = np.asarray(q)
+    Vc = as_f64(Vc)
+    B, H, w, D = q.shape
+    KVH = Vc.shape[1]
+    G = H // KVH
+    p = window_softmax(q, Kc, scale, causal=causal)  # [B, H, w, k]
+    cs = np.zeros((B, KVH, Vc.shape[-1]))
+    for b in range(B):
+        for kv in range(KVH):
+            for h in range(kv * G, (kv + 1) * G):
+                # sum_i sum_j (p_hij v_jd)^2, one (i, j) pair at a time
+                for i in range(w):
+                    cs[b, kv] += ((p[b, h, i][:, None] * Vc[b, kv]) ** 2).sum(axis=0)
+            cs[b, kv] /= G
+    return cs
 
 
 # ----------------------------------------------------------------------------------------

@@ -238,6 +238,52 @@ def test_think_prune_compact_and_zero():
         np.testing.assert_array_equal(Kz[0, kv][:, exp], K[0, kv][:, exp])
 
 
+def test_value_channel_score_by_loops():
+    """The value score against a pure-Python sum over (head, window row, token) with its own
+    causal softmax over the compressed cache."""
+    B, H, KVH, w, k, D = 1, 4, 2, 3, 6, 4
+    q = bf16_bits_to_f32(normal_bf16((B, H, w, D), 97, 1)).astype(np.float64)
+    Kc = bf16_bits_to_f32(normal_bf16((B, KVH, k, D), 97, 2)).astype(np.float64)
+    Vc = bf16_bits_to_f32(normal_bf16((B, KVH, k, D), 97, 3)).astype(np.float64)
+    scale, G = 0.5, H // KVH
+    exp = np.zeros((B, KVH, D))
+    for kv in range(KVH):
+        for h in range(kv * G, (kv + 1) * G):
+            for i in range(w):
+                vis = list(range(k - w + i + 1))  # window row i sits at index k - w + i
+                lg = [scale * sum(q[0, h, i, d] * Kc[0, kv, j, d] for d in range(D)) for j in vis]
+                mx = max(lg)
+                ex = [math.exp(x - mx) for x in lg]
+                tot = sum(ex)
+                for n, j in enumerate(vis):
+                    for d in range(D):
+                        exp[0, kv, d] += (ex[n] / tot * Vc[0, kv, j, d]) ** 2 / G
+    got = O.value_channel_score(_bf16(q), _bf16(Kc), _bf16(Vc), scale)
+    np.testing.assert_allclose(got, exp, rtol=1e-12)
+
+
+def test_value_channel_score_factorises_and_uniform_case():
+    """sum_i sum_j (p_ij v_jd)^2 = sum_j (sum_i p_ij^2) v_jd^2; with a zero query every
+    visible token gets 1/n_i, so the weights have a closed form."""
+    B, H, KVH, w, k, D = 2, 8, 2, 5, 40, 16
+    q = normal_bf16((B, H, w, D), 98, 1)
+    Kc = normal_bf16((B, KVH, k, D), 98, 2)
+    Vc = normal_bf16((B, KVH, k, D), 98, 3)
+    G = H // KVH
+    p = O.window_softmax(q, Kc, 0.3)
+    wj = np.stack([(p[:, kv * G:(kv + 1) * G] ** 2).sum(axis=(1, 2)) / G for kv in range(KVH)], axis=1)
+    V2 = bf16_bits_to_f32(Vc).astype(np.float64) ** 2
+    np.testing.assert_allclose(O.value_channel_score(q, Kc, Vc, 0.3), np.einsum("bkj,bkjd->bkd", wj, V2),
+                               rtol=1e-12)
+    # zero query: row i sees n_i = k - w + i + 1 tokens, each with p = 1/n_i
+    w0 = np.zeros(k)
+    for i in range(w):
+        n = k - w + i + 1
+        w0[:n] += 1.0 / n ** 2
+    np.testing.assert_allclose(O.value_channel_score(np.zeros_like(q), Kc, Vc, 0.3),
+                               np.einsum("j,bkjd->bkd", w0, V2), rtol=1e-12)
+
+
 def _decode_attention_loops(q, K, V, scale, live=None):
     """Independent brute force: one new query per head, pure Python loops."""
     B, H, D = len(q), len(q[0]), len(q[0][0])
