@@ -19,7 +19,8 @@ KVC_OK, KVC_ERR_INVALID_ARG, KVC_ERR_UNSUPPORTED, KVC_ERR_CUDA, KVC_ERR_TIMEOUT,
     KVC_ERR_DEVICE_BOUNDS, KVC_ERR_WORKSPACE = range(7)
 KVC_REDUCE_GQA_GROUP, KVC_REDUCE_ALL_HEADS = 0, 1
 (KVC_OP_WINDOW_SCORES, KVC_OP_TOPK_SELECT, KVC_OP_COMPRESS_PREFILL, KVC_OP_TOVA_DECODE_STEP,
- KVC_OP_SCISSORHANDS_UPDATE, KVC_OP_SCISSORHANDS_EVICT, KVC_OP_CHANNEL_SCORE, KVC_OP_DECODE_ATTENTION) = range(8)
+ KVC_OP_SCISSORHANDS_UPDATE, KVC_OP_SCISSORHANDS_EVICT, KVC_OP_CHANNEL_SCORE, KVC_OP_DECODE_ATTENTION,
+ KVC_OP_VALUE_CHANNEL_SCORE) = range(9)
 
 REDUCE = {"gqa": KVC_REDUCE_GQA_GROUP, "all_heads": KVC_REDUCE_ALL_HEADS}
 
@@ -75,6 +76,7 @@ _SIGNATURES = {
     "kvc_channel_prune": (_I32, [_P, _P, _DESC, _I32, _I32, _P, _P, _P]),
     "kvc_decode_attention": (_I32, [_P, _P, _P, _DESC, _P, _DESC, _P, _F, _P, _P, _SZ, _P]),
     "kvc_zero_add_back": (_I32, [_P, _DESC, _P, _P, _DESC, _P]),
+    "kvc_value_channel_score": (_I32, [_P, _I32, _P, _P, _DESC, _F, _P, _P, _SZ, _P]),
     "kvc_get_device_status": (_I32, [_P]),
     "kvc_status_string": (ctypes.c_char_p, [_I32]),
     "kvc_last_error_message": (ctypes.c_char_p, []),
@@ -413,6 +415,22 @@ def kvc_decode_attention(q, K, V, scale, ch=None, live_mask=None, out=None, ws=N
                                     _ptr(None if live_mask is None else live_mask.contiguous()), float(scale),
                                     _ptr(out), _ptr(ws), nbytes, _stream(stream)))
     return out
+
+
+def kvc_value_channel_score(q_win, Kc, Vc, scale, cs=None, ws=None, stream=None):
+    """ThinK value-channel score [B,KVH,D] over the compressed cache ``Kc``/``Vc`` whose last
+    w tokens are the window rows of ``q_win`` [B,H,w,D]."""
+    lib = load_library()
+    B, H, w, D = q_win.shape
+    desc = kv_desc(Kc, H)
+    if tuple(Vc.stride()) != tuple(Kc.stride()) or Vc.shape != Kc.shape:
+        raise ValueError("Kc and Vc must have the same shape and strides")
+    if cs is None:
+        cs = torch.empty((B, Kc.shape[1], D), dtype=torch.float32, device=Kc.device)
+    ws, nbytes = _ws(KVC_OP_VALUE_CHANNEL_SCORE, desc, w, 0, ws, Kc.device)
+    _check(lib.kvc_value_channel_score(_ptr(q_win.contiguous()), w, _ptr(Kc), _ptr(Vc), ctypes.byref(desc),
+                                       float(scale), _ptr(cs), _ptr(ws), nbytes, _stream(stream)))
+    return cs
 
 
 def kvc_zero_add_back(Kp, ch, D, H=None, K_out=None, stream=None):

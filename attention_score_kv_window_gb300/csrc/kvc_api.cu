@@ -78,6 +78,16 @@ kvc_status check_ws(void* ws, size_t have, size_t need, const char* what) {
     if (_s != KVC_OK) return _s;    \
   } while (0)
 
+// scratch of kvc_value_channel_score, 16-byte aligned pieces: the window-score workspace,
+// one weight per token (at *wts_off), the channel partials (at *part_off)
+size_t value_score_workspace(const kvc_kv_desc& kv, int w, size_t* wts_off = nullptr, size_t* part_off = nullptr) {
+  const size_t a = (scores_workspace(kv, w, KVC_REDUCE_GQA_GROUP) + 15) / 16 * 16;
+  const size_t b = ((size_t)kv.B * kv.KVH * kv.S * sizeof(float) + 15) / 16 * 16;
+  if (wts_off) *wts_off = a;
+  if (part_off) *part_off = a + b;
+  return a + b + channel_score_workspace(kv, 0, false);
+}
+
 kvc_status check_window(const kvc_kv_desc* kv, int32_t w, const char* name) {
   if (w < 1 || (int64_t)w > kv->S) return fail(KVC_ERR_INVALID_ARG, "%s: need 1 <= w <= S", name);
   if ((int64_t)w * (kv->H / kv->KVH) > 512)
@@ -182,6 +192,9 @@ size_t kvc_workspace_size(kvc_op op, const kvc_kv_desc* kv, int32_t w, int32_t k
       return channel_score_workspace(*kv, k, k > 0);
     case KVC_OP_DECODE_ATTENTION:
       return plan_decode(*kv).part_bytes;
+    case KVC_OP_VALUE_CHANNEL_SCORE:
+      if (check_window(kv, w, "kvc_workspace_size") != KVC_OK) return (size_t)-1;
+      return value_score_workspace(*kv, w);
     default:
       return (size_t)-1;
   }
@@ -490,6 +503,31 @@ kvc_status kvc_channel_prune(const float* cs, const kvc_bf16* K, const kvc_kv_de
   }
   return cuda_status(launch_channel_prune(cs, K, *kv, C, zero_mode ? 1 : 0, ch_idx, K_out, (cudaStream_t)stream),
                      "kvc_channel_prune launch");
+}
+
+kvc_status kvc_value_channel_score(const kvc_bf16* q_win, int32_t w, const kvc_bf16* Kc, const kvc_bf16* Vc,
+                                   const kvc_kv_desc* kv, float scale, float* cs, void* ws, size_t ws_bytes,
+                                   kvc_stream_t stream) {
+  KVC_TRY(check_desc(kv, "kvc_value_channel_score"));
+  KVC_TRY(check_window(kv, w, "kvc_value_channel_score"));
+  KVC_TRY(check_ptr(q_win, "q_win"));
+  KVC_TRY(check_ptr(Kc, "Kc"));
+  KVC_TRY(check_ptr(Vc, "Vc"));
+  if (!cs) return fail(KVC_ERR_INVALID_ARG, "cs is NULL");
+  if (!(scale > 0.f) || scale != scale) return fail(KVC_ERR_INVALID_ARG, "scale must be > 0");
+  KVC_TRY(check_ws(ws, ws_bytes, value_score_workspace(*kv, w), "kvc_value_channel_score"));
+  // the window's attention over the compressed cache, squared and summed over the window
+  // rows (mean over the group): one weight per kept token, then the weighted sums of V^2
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  size_t wts_off = 0, part_off = 0;
+  value_score_workspace(*kv, w, &wts_off, &part_off);
+  float* wts = reinterpret_cast<float*>(base + wts_off);
+  void* part = base + part_off;
+  KVC_TRY(cuda_status(launch_window_scores(q_win, Kc, *kv, w, scale, 1, nullptr, KVC_REDUCE_GQA_GROUP, wts, base,
+                                           (cudaStream_t)stream, 2),
+                      "kvc_value_channel_score weights launch"));
+  return cuda_status(launch_weighted_channel_norm(wts, Vc, *kv, cs, part, (cudaStream_t)stream),
+                     "kvc_value_channel_score launch");
 }
 
 kvc_status kvc_decode_attention(const kvc_bf16* q, const int32_t* ch, const kvc_bf16* K, const kvc_kv_desc* kd,

@@ -105,13 +105,15 @@ __device__ __forceinline__ void acc_sq8(float* acc, uint4 v) {
   }
 }
 
-// partial key sums over one range of rows: part[split][b*KVH+kvh][D]
+// partial sums of squares over one range of rows, weighted by wts[b*KVH+kvh][row] when
+// given: part[split][b*KVH+kvh][D]
 template <int D>
 __global__ void __launch_bounds__(256) k_channel_partial(const uint16_t* __restrict__ K, int64_t sb,
                                                          int64_t sh, int64_t ss, int64_t S,
                                                          const int32_t* __restrict__ idx, int k,
                                                          int64_t nrows, int64_t chunk,
-                                                         float* __restrict__ part, int KVH) {
+                                                         float* __restrict__ part, int KVH,
+                                                         const float* __restrict__ wts) {
   pdl_wait();  // previous kernel on the stream complete and visible
   constexpr int TPR = D / 8;
   constexpr int RPP = 256 / TPR;  // rows per pass
@@ -129,7 +131,15 @@ __global__ void __launch_bounds__(256) k_channel_partial(const uint16_t* __restr
       if (j < 0) continue;
       if (j >= S) { set_device_status(KVC_ERR_DEVICE_BOUNDS); continue; }
     }
-    acc_sq8(acc, ld16(Kb + j * ss + c * 8));
+    if (wts) {
+      float t[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      acc_sq8(t, ld16(Kb + j * ss + c * 8));
+      const float wj = __ldg(wts + (int64_t)bk * S + j);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, t[i], acc[i]);
+    } else {
+      acc_sq8(acc, ld16(Kb + j * ss + c * 8));
+    }
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) red[rl][c * 8 + i] = acc[i];
@@ -138,6 +148,17 @@ __global__ void __launch_bounds__(256) k_channel_partial(const uint16_t* __restr
     float s = 0.f;
     for (int q = 0; q < RPP; ++q) s += red[q][d];
     part[((int64_t)split * gridDim.z * KVH + bk) * D + d] = s;
+  }
+}
+
+// cs[b*KVH+kvh][d] = the sum of the key-range partials
+__global__ void __launch_bounds__(256) k_channel_sum(const float* __restrict__ part, int nsplit, int64_t n,
+                                                     float* __restrict__ cs) {
+  pdl_wait();  // previous kernel on the stream complete and visible
+  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (int64_t)gridDim.x * blockDim.x) {
+    float s = 0.f;
+    for (int q = 0; q < nsplit; ++q) s += __ldg(part + (int64_t)q * n + x);
+    cs[x] = s;
   }
 }
 
@@ -306,6 +327,25 @@ cudaError_t launch_compact(const uint16_t* K, const uint16_t* V, const kvc_kv_de
   return launched(1);
 }
 
+cudaError_t launch_weighted_channel_norm(const float* wts, const uint16_t* V, const kvc_kv_desc& kv, float* cs,
+                                         void* ws, cudaStream_t st) {
+  const int ns = channel_splits(kv, kv.S);
+  const int64_t chunk = (kv.S + ns - 1) / ns;
+  float* part = reinterpret_cast<float*>(ws);
+  const dim3 grid(ns, kv.KVH, kv.B);
+  cudaError_t e =
+      kv.D == 64 ? launch_pdl(k_channel_partial<64>, grid, dim3(256), 0, st, V, kv.stride_b, kv.stride_h, kv.stride_s,
+                              kv.S, (const int32_t*)nullptr, 0, kv.S, chunk, part, kv.KVH, wts)
+                 : launch_pdl(k_channel_partial<128>, grid, dim3(256), 0, st, V, kv.stride_b, kv.stride_h, kv.stride_s,
+                              kv.S, (const int32_t*)nullptr, 0, kv.S, chunk, part, kv.KVH, wts);
+  if (e != cudaSuccess) return e;
+  const int64_t n = (int64_t)kv.B * kv.KVH * kv.D;
+  e = launch_pdl(k_channel_sum, dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 1024))),
+                 dim3(256), 0, st, (const float*)part, ns, n, cs);
+  if (e != cudaSuccess) return e;
+  return launched(2);
+}
+
 cudaError_t launch_write_slots(const uint16_t* kn, const uint16_t* vn, const int32_t* slot,
                                uint16_t* K, uint16_t* V, const kvc_kv_desc& kv, cudaStream_t st) {
   const int rows = kv.B * kv.KVH;
@@ -335,9 +375,9 @@ cudaError_t launch_channel_score(const uint16_t* q, int w, const uint16_t* K, co
   dim3 grid(ns, kv.KVH, kv.B);
   cudaError_t e =
       kv.D == 64 ? launch_pdl(k_channel_partial<64>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
-                              kv.S, idx, k, nrows, chunk, part, kv.KVH)
+                              kv.S, idx, k, nrows, chunk, part, kv.KVH, (const float*)nullptr)
                  : launch_pdl(k_channel_partial<128>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
-                              kv.S, idx, k, nrows, chunk, part, kv.KVH);
+                              kv.S, idx, k, nrows, chunk, part, kv.KVH, (const float*)nullptr);
   if (e != cudaSuccess) return e;
   e = launch_pdl(k_channel_final, dim3(kv.B * kv.KVH), dim3(1024), 0, st, q, kv.H, kv.KVH, w, kv.D, part, ns, kv.B, cs);
   if (e != cudaSuccess) return e;

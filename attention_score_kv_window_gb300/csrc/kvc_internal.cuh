@@ -101,6 +101,7 @@ struct ScoresArgs {
   const uint32_t* live;
   int64_t live_words;
   float sl2;  // scale * log2(e)
+  float pw;   // pass 2 sums p^pw over the query rows (1: scores; 2: value-channel weights)
   int nsplit;    // key ranges per (b, kvh)
   int64_t units; // 128-key units per (b, kvh); range s covers units [s*units/nsplit, (s+1)*units/nsplit)
   float2* part;  // [B*KVH][Rpad][nsplit]  (m2, l), see part_index
@@ -172,7 +173,11 @@ size_t scores_workspace(const kvc_kv_desc& kv, int w, int reduce);
 cudaError_t noalloc_scratch(void** out);
 cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc_kv_desc& kv, int w,
                                  float scale, int causal, const uint32_t* live, int reduce,
-                                 float* scores, void* ws, cudaStream_t st);
+                                 float* scores, void* ws, cudaStream_t st, int power = 1);
+// value-channel score: cs[b,kvh,d] = sum_j wts[b,kvh,j] * V[b,kvh,j,d]^2 (kvc_gather.cu); ws holds
+// channel_score_workspace(kv, 0, false) bytes of partials
+cudaError_t launch_weighted_channel_norm(const float* wts, const uint16_t* V, const kvc_kv_desc& kv, float* cs,
+                                         void* ws, cudaStream_t st);
 
 // ----------------------------------------------------------------------------------------
 // selection (kvc_select.cu)

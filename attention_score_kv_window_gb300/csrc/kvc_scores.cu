@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass2(const ScoresArgs a) {
     cp_async_commit();
   }
   for (int r = tid; r < Rpad; r += NTHREADS) {
-    cr[r] = a.mrow[(int64_t)bk * Rpad + r];
+    cr[r] = a.mrow[(int64_t)bk * Rpad + r] * a.pw;
     lim[r] = row_limit(a, r);
   }
 
@@ -396,15 +396,16 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass2(const ScoresArgs a) {
       }
       const int r0 = nt * 8 + 2 * t;
       const float c0 = cr[r0], c1 = cr[r0 + 1];
+      const float sl2p = a.sl2 * a.pw;
       if (clean) {
-        acc0 += ex2(fmaf(c[0], a.sl2, -c0)) + ex2(fmaf(c[1], a.sl2, -c1));
-        acc1 += ex2(fmaf(c[2], a.sl2, -c0)) + ex2(fmaf(c[3], a.sl2, -c1));
+        acc0 += ex2(fmaf(c[0], sl2p, -c0)) + ex2(fmaf(c[1], sl2p, -c1));
+        acc1 += ex2(fmaf(c[2], sl2p, -c0)) + ex2(fmaf(c[3], sl2p, -c1));
       } else {
         const long long l0 = lim[r0], l1 = lim[r0 + 1];
-        acc0 += ((visA && jA <= l0) ? ex2(fmaf(c[0], a.sl2, -c0)) : 0.f) +
-                ((visA && jA <= l1) ? ex2(fmaf(c[1], a.sl2, -c1)) : 0.f);
-        acc1 += ((visB && jB <= l0) ? ex2(fmaf(c[2], a.sl2, -c0)) : 0.f) +
-                ((visB && jB <= l1) ? ex2(fmaf(c[3], a.sl2, -c1)) : 0.f);
+        acc0 += ((visA && jA <= l0) ? ex2(fmaf(c[0], sl2p, -c0)) : 0.f) +
+                ((visA && jA <= l1) ? ex2(fmaf(c[1], sl2p, -c1)) : 0.f);
+        acc1 += ((visB && jB <= l0) ? ex2(fmaf(c[2], sl2p, -c0)) : 0.f) +
+                ((visB && jB <= l1) ? ex2(fmaf(c[3], sl2p, -c1)) : 0.f);
       }
     }
     acc0 += __shfl_xor_sync(0xffffffffu, acc0, 1);
@@ -606,13 +607,14 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
   __syncthreads();
   float* out = a.out + (int64_t)bk * a.S + kbeg;
   float cv[RM];
+  const float pw = a.pw;
 #pragma unroll
-  for (int r = 0; r < RM; ++r) cv[r] = r < R ? crow[r] : 0.f;
+  for (int r = 0; r < RM; ++r) cv[r] = r < R ? crow[r] * pw : 0.f;
   for (int j = tid; j < len; j += NTHREADS) {
     float sc = 0.f;
 #pragma unroll
     for (int r = 0; r < RM; ++r)
-      if (r < R) sc += ex2(lg[(int64_t)r * per + j] - cv[r]);
+      if (r < R) sc += ex2(fmaf(lg[(int64_t)r * per + j], pw, -cv[r]));
     out[j] = sc * a.out_mul;
   }
   // no remote access follows the cluster barrier: CTAs may leave independently
@@ -757,7 +759,7 @@ size_t scores_workspace(const kvc_kv_desc& kv, int w, int reduce) {
 
 cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc_kv_desc& kv, int w,
                                  float scale, int causal, const uint32_t* live, int reduce,
-                                 float* scores, void* ws, cudaStream_t st) {
+                                 float* scores, void* ws, cudaStream_t st, int power) {
   const ScoresPlan p = plan_scores(kv, w, reduce);
   ScoresArgs a{};
   a.q = q;
@@ -777,6 +779,7 @@ cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc
   a.live = live;
   a.live_words = (kv.S + 31) / 32;
   a.sl2 = scale * 1.4426950408889634f;
+  a.pw = (float)power;
   a.nsplit = p.nsplit;
   a.units = p.units;
   uint8_t* base = static_cast<uint8_t*>(ws);

@@ -512,7 +512,7 @@ __device__ __forceinline__ void merge_rows(const ScoresArgs& a, int bk, float* n
     lse2_merge(M, L, m2, l2);
   }
   if (r < N2 && sub == 0) {
-    nc[r] = L > 0.f ? -(M + log2f(L)) : -CUDART_INF_F;
+    nc[r] = L > 0.f ? -(M + log2f(L)) * a.pw : -CUDART_INF_F;
     lim[r] = row_limit_i(a, r);
   }
 }
@@ -752,8 +752,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const bool clean = (kt0 + TILE <= kend) && (!a.causal || kt0 + TILE - 1 <= a.S - a.w);
 #pragma unroll
           for (int ch = 0; ch < NW / 32; ++ch)
-            acc += pass2_chunk<32>(c, g, taddr + ch * 32, ch == NW / 32 - 1, ncq + ch * 32, limq + ch * 32, a.sl2,
-                                   clean, j, kend);
+            acc += pass2_chunk<32>(c, g, taddr + ch * 32, ch == NW / 32 - 1, ncq + ch * 32, limq + ch * 32,
+                                   a.sl2 * a.pw, clean, j, kend);
         } else {
           dead = true;
         }

@@ -285,6 +285,17 @@ class PrefillCase:
             self.Kp = torch.empty((B, KVH, k, C), dtype=bf, device=dev)
             self.calls += [Call("channel_score", self._cscore, B * KVH * k * D * 2 + B * wl.H * wl.w * D * 2),
                            Call("channel_prune", self._cprune, B * KVH * k * D * 2 + B * KVH * k * C * 2)]
+        if wl.extra.get("values"):  # value channels too: score over the compressed cache, then prune
+            C = wl.C
+            self.vcs = torch.empty((B, KVH, D), dtype=f32, device=dev)
+            self.vch = torch.empty((B, KVH, C), dtype=i32, device=dev)
+            self.Vp = torch.empty((B, KVH, k, C), dtype=bf, device=dev)
+            self.vws = torch.empty(int(lib.kvc_workspace_size(8, kvc.kv_desc(self.outs[0][2], wl.H), wl.w, 0)),
+                                   dtype=torch.uint8, device=dev)
+            vflops = 2 * 2.0 * B * wl.H * wl.w * k * D
+            self.calls += [Call("value_channel_score", self._vscore, 2 * B * KVH * k * D * 2 + B * wl.H * wl.w * D * 2,
+                                vflops, "tensor"),
+                           Call("value_channel_prune", self._vprune, B * KVH * k * D * 2 + B * KVH * k * C * 2)]
 
     def _scores(self, i):
         q, K, V = self.reps[i % self.R]
@@ -305,10 +316,19 @@ class PrefillCase:
         self.kvc.kvc_channel_prune(self.cs, self.outs[i % self.R][2], self.wl.C, ch_idx=self.ch, K_out=self.Kp,
                                    H=self.wl.H)
 
+    def _vscore(self, i):
+        q, _, _ = self.reps[i % self.R]
+        _, _, Ko, Vo = self.outs[i % self.R]
+        self.kvc.kvc_value_channel_score(q, Ko, Vo, self.wl.scale, cs=self.vcs, ws=self.vws)
+
+    def _vprune(self, i):
+        self.kvc.kvc_channel_prune(self.vcs, self.outs[i % self.R][3], self.wl.C, ch_idx=self.vch, K_out=self.Vp,
+                                   H=self.wl.H)
+
     def config(self):
         wl = self.wl
         return {"workload": wl.name, "B": self.B, "H": wl.H, "KVH": self.KVH, "D": self.D, "S": self.S, "w": wl.w,
-                "k": self.k, "C": wl.C or None,
+                "k": self.k, "C": wl.C or None, "value_channels_pruned": bool(wl.extra.get("values")),
                 "l2": f"inputs rotate over {self.R} replicas ({self.R * self.in_bytes / 2**20:.0f} MiB > L2)"}
 
     def e2e(self, steps, stream, world, dist, dev):

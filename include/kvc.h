@@ -73,7 +73,8 @@ typedef enum {
   KVC_OP_SCISSORHANDS_UPDATE = 4,
   KVC_OP_SCISSORHANDS_EVICT = 5,
   KVC_OP_CHANNEL_SCORE = 6,
-  KVC_OP_DECODE_ATTENTION = 7
+  KVC_OP_DECODE_ATTENTION = 7,
+  KVC_OP_VALUE_CHANNEL_SCORE = 8
 } kvc_op;
 
 /* Bytes of scratch the call `op` needs for these shapes on the current device (w: window
@@ -313,6 +314,22 @@ kvc_status kvc_channel_score(const kvc_bf16* q_win, int32_t w, const kvc_bf16* K
 kvc_status kvc_channel_prune(const float* cs, const kvc_bf16* K, const kvc_kv_desc* kv,
                              int32_t C, int32_t zero_mode, int32_t* ch_idx, kvc_bf16* K_out,
                              kvc_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * kvc_value_channel_score — ThinK value-channel score ("Add ThinK_Press" names value-cache
+ * pruning without defining it; this carries the key score's definition over to values):
+ *   cs[b,kvh,d] = mean_{h in group} sum_i sum_j (p[b,h,i,j] * Vc[b,kvh,j,d])^2
+ * with p the window's attention over the compressed cache: softmax_j(scale * q_win . Kc_j),
+ * causal with the w window rows as the LAST w tokens of the cache (as kvc_compress_prefill
+ * with protect_tail = w leaves them).  Computed as sum_j wt_j Vc_jd^2 with
+ * wt_j = mean_h sum_i p_hij^2 (the window scores with p squared).
+ *   q_win [B,H,w,D] bf16; Kc, Vc: the compressed cache, both described by kv (S = kept
+ *   tokens); cs [B,KVH,D] float32 out; ws: kvc_workspace_size(KVC_OP_VALUE_CHANNEL_SCORE,
+ *   kv, w, 0).  kvc_channel_prune(cs, Vc, ...) then prunes the value channels.
+ * ------------------------------------------------------------------------------------- */
+kvc_status kvc_value_channel_score(const kvc_bf16* q_win, int32_t w, const kvc_bf16* Kc,
+                                   const kvc_bf16* Vc, const kvc_kv_desc* kv, float scale,
+                                   float* cs, void* ws, size_t ws_bytes, kvc_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * kvc_decode_attention — attention of one new query per head over a (compressed) cache, the

@@ -113,13 +113,15 @@ SCISSORHANDS_SPARSE = SCISSORHANDS.with_(name="scissorhands_sparse8_decode_b8_ca
 THINK_128K = Workload("think_snapkv_prefill_s131072", B=1, H=32, KVH=8, D=128, S=131072, w=64,
                       k=8192, reduce="gqa", protect_tail=64, channel_scales=True, C=64)
 
+# keys and values pruned to 64 channels (value scores over the compressed cache)
+THINK_KV_128K = THINK_128K.with_(name="think_kv_snapkv_prefill_s131072", extra={"values": True})
 # decoding over the cache ThinK + SnapKV leave (8192 kept tokens, 64 of 128 key channels),
 # for a decode batch of 16 such caches; the _full variant attends unpruned keys
 THINK_DECODE = Workload("think_decode_b16_s8192_c64", B=16, H=32, KVH=8, D=128, S=8192, w=1, k=8192,
                         reduce="gqa", causal=False, C=64)
 FULL_DECODE = THINK_DECODE.with_(name="decode_b16_s8192_full", C=128)
 WORKLOADS = {wl.name: wl for wl in (TOVA_PREFILL, SNAPKV_32K, TOVA_DECODE, SCISSORHANDS, SCISSORHANDS_QUEUE,
-                                    SCISSORHANDS_SPARSE, THINK_128K, THINK_DECODE, FULL_DECODE)}
+                                    SCISSORHANDS_SPARSE, THINK_128K, THINK_KV_128K, THINK_DECODE, FULL_DECODE)}
 
 
 # ----------------------------------------------------------------------------------------

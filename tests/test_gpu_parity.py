@@ -489,6 +489,28 @@ def test_channel_prune_in_place_zero():
 # ----------------------------------------------------------------------------------------
 
 
+VALUE_SCORE_CASES = [
+    # B, H, KVH, D, kept tokens, w: the three scoring paths (G*w = 256, 16, 512)
+    (1, 32, 8, 128, 2000, 64),
+    (2, 8, 2, 64, 333, 4),
+    (1, 8, 1, 128, 700, 64),
+]
+
+
+@pytest.mark.parametrize("B,H,KVH,D,k,w", VALUE_SCORE_CASES)
+def test_value_channel_score_parity(B, H, KVH, D, k, w):
+    seed = k + w
+    q = normal_bf16((B, H, w, D), seed, 1)
+    Kc = normal_bf16((B, KVH, k, D), seed, 2)
+    Vc = normal_bf16((B, KVH, k, D), seed, 3)
+    scale = 1.0 / np.sqrt(D)
+    got = kvc.kvc_value_channel_score(dev_bf16(q), dev_bf16(Kc), dev_bf16(Vc), scale).cpu().numpy()
+    assert_scores_close(got, O.value_channel_score(q, Kc, Vc, scale), what="value channel score")
+    # the same scoring kernels with p (not p^2) still give the window scores
+    sc = kvc.kvc_window_scores(dev_bf16(q), dev_bf16(Kc), scale, causal=True, reduce="gqa").cpu().numpy()
+    assert_scores_close(sc, O.window_scores(q, Kc, scale, causal=True, reduce="gqa"))
+
+
 # ----------------------------------------------------------------------------------------
 # Decoding over the channel-pruned cache (ThinK options 3b / 3c)
 # ----------------------------------------------------------------------------------------
