@@ -533,6 +533,8 @@ DECODE_CASES = [
     (3, 8, 4, 64, 64, 5, None),         # a single partial tile
     (1, 8, 2, 128, 64, 64, None),       # exactly one tile
     (1, 8, 2, 128, 64, 40000, 0.5),     # many key ranges
+    (16, 32, 8, 128, 64, 4096, None),   # 128 (b, kvh) rows
+    (16, 32, 8, 128, 128, 4100, 0.5),   # 128 rows, ragged, dead slots
 ]
 
 
