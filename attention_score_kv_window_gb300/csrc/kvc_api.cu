@@ -361,6 +361,17 @@ kvc_status kvc_tova_decode_step(const kvc_bf16* q_new, const kvc_bf16* k_new,
   if (!free_slot) return fail(KVC_ERR_INVALID_ARG, "free_slot is NULL");
   KVC_TRY(check_ptr(scores, "scores"));
   KVC_TRY(check_ws(ws, ws_bytes, scores_workspace(*kv, 1, KVC_REDUCE_ALL_HEADS), "kvc_tova_decode_step"));
+  KVC_TRY(check_ptr(q_new, "q_new"));
+  KVC_TRY(check_ptr(k_new, "k_new"));
+  KVC_TRY(check_ptr(K, "K"));
+  if ((v_new == nullptr) != (V == nullptr)) return fail(KVC_ERR_INVALID_ARG, "v_new and V must both be given or both NULL");
+  if (V) KVC_TRY(check_ptr(v_new, "v_new"));
+  {
+    const cudaError_t e = launch_tova_decode(q_new, k_new, v_new, K, V, *kv, scale, free_slot, scores, ws,
+                                             (cudaStream_t)stream);
+    if (e != cudaErrorNotSupported) return cuda_status(e, "kvc_tova_decode_step launch");
+    // (returned by the planner, not by the runtime: the shapes take the general kernels below)
+  }
   KVC_TRY(kvc_write_slots(k_new, v_new, free_slot, K, V, kv, stream));
   KVC_TRY(kvc_window_scores(q_new, K, kv, 1, scale, 0, nullptr, KVC_REDUCE_ALL_HEADS, scores, ws, ws_bytes, stream));
   return kvc_topk_select(scores, kv->B, kv->KVH, kv->S, 1, 0, nullptr, 0, free_slot, nullptr, 0, stream);

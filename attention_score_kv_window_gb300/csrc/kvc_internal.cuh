@@ -109,6 +109,14 @@ struct ScoresArgs {
   float* out;    // [B*KVH][S]
   float out_mul; // 1/G
   unsigned long long* sync;  // fused tensor-core kernel: epoch word + one tag per CTA (may be null)
+  // Decode step with the new token written on the fly (small-row kernel only; wslot null
+  // otherwise): slot wslot[b*KVH+kvh] holds the new key knew[b*KVH+kvh] (its stale cache row
+  // is never read), and the CTA whose slice holds it stores knew / vnew into Kw / Vw there.
+  const int32_t* wslot;
+  const uint16_t* knew;
+  const uint16_t* vnew;
+  uint16_t* Kw;
+  uint16_t* Vw;
 };
 
 // (m, l) partial of query row r from key range `split`: a row's ranges are contiguous
@@ -174,6 +182,13 @@ cudaError_t noalloc_scratch(void** out);
 cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc_kv_desc& kv, int w,
                                  float scale, int causal, const uint32_t* live, int reduce,
                                  float* scores, void* ws, cudaStream_t st, int power = 1);
+// One TOVA decode step as three kernels: the new token written into slot free_slot[b,kvh]
+// while the small-row kernel scores all slots with it, then the all-heads mean of the group
+// scores fused with the eviction (argmin) that overwrites free_slot.  cudaErrorNotSupported
+// when the shapes need another scoring kernel.
+cudaError_t launch_tova_decode(const uint16_t* q, const uint16_t* knew, const uint16_t* vnew, uint16_t* K, uint16_t* V,
+                               const kvc_kv_desc& kv, float scale, int32_t* free_slot, float* scores, void* ws,
+                               cudaStream_t st);
 // value-channel score: cs[b,kvh,d] = sum_j wts[b,kvh,j] * V[b,kvh,j,d]^2 (kvc_gather.cu); ws holds
 // channel_score_workspace(kv, 0, false) bytes of partials
 cudaError_t launch_weighted_channel_norm(const float* wts, const uint16_t* V, const kvc_kv_desc& kv, float* cs,

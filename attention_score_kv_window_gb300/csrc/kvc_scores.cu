@@ -501,14 +501,33 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
   const int r0 = lane / CH, cc = lane % CH;
   const uint32_t dlane = (uint32_t)(r0 * P + cc * 8) * 2;
   const int64_t slane = (int64_t)r0 * a.ss + cc * 8;
+  // a decode step's new token: its slot (slice-relative) reads the new key instead of the cache
+  int wf = -1;
+  const uint16_t* knew_lane = nullptr;
+  if (a.wslot) {
+    const int32_t f = __ldg(a.wslot + bk);
+    if (f < 0 || f >= a.S) {
+      if (tid == 0 && cr == 0) set_device_status(KVC_ERR_DEVICE_BOUNDS);
+    } else if (f >= kbeg && f < kend) {
+      wf = (int)(f - kbeg);
+      knew_lane = a.knew + (int64_t)bk * D + cc * 8;
+      if (warp == 0 && lane < CH) {  // the cache row for later steps
+        const int64_t off = b * a.sb + kvh * a.sh + (int64_t)f * a.ss + lane * 8;
+        *reinterpret_cast<uint4*>(a.Kw + off) = *reinterpret_cast<const uint4*>(a.knew + (int64_t)bk * D + lane * 8);
+        if (a.Vw) *reinterpret_cast<uint4*>(a.Vw + off) = *reinterpret_cast<const uint4*>(a.vnew + (int64_t)bk * D + lane * 8);
+      }
+    }
+  }
   auto load_chunk = [&](int i, int st) {
     const int k0 = (warp + 8 * i) * 8;  // slice-relative
     const uint16_t* src0 = Kb + (kbeg + k0) * a.ss + slane;
     const uint32_t dst0 = ring + (uint32_t)(st * 8 * P) * 2 + dlane;
 #pragma unroll
     for (int u = 0; u < PPL; ++u) {
-      const bool ok = k0 + r0 + RPP * u < len;
-      cp_async16(dst0 + (uint32_t)(RPP * u * P) * 2, ok ? src0 + (int64_t)RPP * u * a.ss : Kb, ok ? 16 : 0);
+      const int r = k0 + r0 + RPP * u;
+      const bool ok = r < len;
+      const uint16_t* src = ok ? src0 + (int64_t)RPP * u * a.ss : Kb;
+      cp_async16(dst0 + (uint32_t)(RPP * u * P) * 2, r == wf ? knew_lane : src, ok ? 16 : 0);
     }
   };
 #pragma unroll
@@ -636,6 +655,46 @@ __global__ void k_scores_allheads(const float* __restrict__ grp, float* __restri
   }
 }
 
+// TOVA decode: the all-heads mean (as k_scores_allheads) fused with the eviction of the
+// lowest-ranked slot per batch row (lowest score; equal scores: the highest slot), written
+// to slot[b*KVH+kvh] for every kvh.  One CTA per batch row.
+__global__ void __launch_bounds__(1024) k_allheads_evict1(const float* __restrict__ grp, float* __restrict__ out,
+                                                          int KVH, int64_t S, int32_t* __restrict__ slot) {
+  __shared__ unsigned long long wbest[32];
+  pdl_wait();  // previous kernel on the stream complete and visible
+  const int64_t b = blockIdx.x;
+  const float inv = 1.f / (float)KVH;
+  unsigned long long best = 0ull;
+  for (int64_t j = threadIdx.x; j < S; j += blockDim.x) {
+    float s = 0.f;
+    for (int kv = 0; kv < KVH; ++kv) s += grp[(b * KVH + kv) * S + j];
+    s *= inv;
+    for (int kv = 0; kv < KVH; ++kv) out[(b * KVH + kv) * S + j] = s;
+    uint32_t u = __float_as_uint(s);
+    if (u == 0x80000000u) u = 0u;  // -0 ranks as +0
+    const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    // evicting: the composite (~key, slot) is largest for the lowest score, then the highest slot
+    const unsigned long long c = ((unsigned long long)(~key) << 32) | (uint32_t)j;
+    best = c > best ? c : best;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+    best = y > best ? y : best;
+  }
+  if ((threadIdx.x & 31) == 0) wbest[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    best = threadIdx.x < (blockDim.x >> 5) ? wbest[threadIdx.x] : 0ull;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+      best = y > best ? y : best;
+    }
+    for (int kv = threadIdx.x; kv < KVH; kv += 32) slot[b * KVH + kv] = best ? (int32_t)(uint32_t)best : -1;
+  }
+}
+
 size_t smem_pass1(int D, int rows) { return (size_t)(rows + STAGES * TK) * (D + 8) * 2 + 8 * 16 * sizeof(float2); }
 size_t smem_pass2(int D, int Rpad) {
   return (size_t)(Rpad + STAGES * TK) * (D + 8) * 2 + (size_t)Rpad * (4 + 8) + 2 * TK * 4;
@@ -757,9 +816,9 @@ size_t scores_workspace(const kvc_kv_desc& kv, int w, int reduce) {
   return p.part_bytes + p.sync_bytes + p.group_bytes;
 }
 
-cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc_kv_desc& kv, int w,
-                                 float scale, int causal, const uint32_t* live, int reduce,
-                                 float* scores, void* ws, cudaStream_t st, int power) {
+namespace {
+ScoresArgs make_args(const uint16_t* q, const uint16_t* K, const kvc_kv_desc& kv, int w, float scale, int causal,
+                     const uint32_t* live, int reduce, float* scores, void* ws, int power) {
   const ScoresPlan p = plan_scores(kv, w, reduce);
   ScoresArgs a{};
   a.q = q;
@@ -788,8 +847,39 @@ cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc
   a.sync = reinterpret_cast<unsigned long long*>(base + p.part_bytes);
   a.out = reduce == KVC_REDUCE_ALL_HEADS ? reinterpret_cast<float*>(base + p.part_bytes + p.sync_bytes) : scores;
   a.out_mul = 1.f / (float)a.G;
+  return a;
+}
+}  // namespace
+
+cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc_kv_desc& kv, int w,
+                                 float scale, int causal, const uint32_t* live, int reduce,
+                                 float* scores, void* ws, cudaStream_t st, int power) {
+  const ScoresArgs a = make_args(q, K, kv, w, scale, causal, live, reduce, scores, ws, power);
   if (kv.D == 64) return launch_impl<64>(a, reduce, scores, st);
   return launch_impl<128>(a, reduce, scores, st);
+}
+
+cudaError_t launch_tova_decode(const uint16_t* q, const uint16_t* knew, const uint16_t* vnew, uint16_t* K, uint16_t* V,
+                               const kvc_kv_desc& kv, float scale, int32_t* free_slot, float* scores, void* ws,
+                               cudaStream_t st) {
+  ScoresArgs a = make_args(q, K, kv, 1, scale, 0, nullptr, KVC_REDUCE_ALL_HEADS, scores, ws, 1);
+  int64_t per = 0;
+  const int cs = small_cluster(a, &per);
+  if (cs == 0) return cudaErrorNotSupported;
+  a.wslot = free_slot;
+  a.knew = knew;
+  a.vnew = vnew;
+  a.Kw = K;
+  a.Vw = V;
+  cudaError_t e = kv.D == 64 ? set_smem_attrs<64>() : set_smem_attrs<128>();
+  if (e != cudaSuccess) return e;
+  e = kv.D == 64 ? launch_small<64>(a, cs, per, st) : launch_small<128>(a, cs, per, st);
+  if (e != cudaSuccess) return e;
+  const int threads = (int)std::min<int64_t>(1024, std::max<int64_t>(32, (kv.S + 31) / 32 * 32));
+  e = launch_pdl(k_allheads_evict1, dim3(kv.B), dim3(threads), 0, st, (const float*)a.out, scores, kv.KVH, kv.S,
+                 free_slot);
+  if (e != cudaSuccess) return e;
+  return launched(1);
 }
 
 // ----------------------------------------------------------------------------------------

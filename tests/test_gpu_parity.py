@@ -284,8 +284,8 @@ def test_compress_prefill_parity(B, H, KVH, D, S, w, k, protect, reduce, hh):
 # ----------------------------------------------------------------------------------------
 
 
-def test_tova_decode_steps_teacher_forced():
-    B, H, KVH, D, S, budget = 2, 8, 2, 128, 700, 256
+@pytest.mark.parametrize("B,H,KVH,D,S,budget,steps", [(2, 8, 2, 128, 700, 256, 8), (2, 16, 4, 64, 3000, 2048, 4)])
+def test_tova_decode_steps_teacher_forced(B, H, KVH, D, S, budget, steps):
     wl = Workload("t", B=B, H=H, KVH=KVH, D=D, S=S, w=1, k=budget, reduce="all_heads", causal=False, seed=41)
     pre = prefill_inputs(wl)
     scale = 1.0 / np.sqrt(D)
@@ -306,12 +306,13 @@ def test_tova_decode_steps_teacher_forced():
     Vd[:] = dev_bf16(Vc)
     free = np.full((B, KVH), budget, np.int32)
     near = 0
-    for t in range(1, 9):
+    for t in range(1, steps + 1):
         st = decode_step_inputs(wl, t)
         fs = dev_i32(free)
         g_sc = kvc.kvc_tova_decode_step(dev_bf16(st["q"]), dev_bf16(st["k"]), dev_bf16(st["v"]), Kd, Vd, scale, fs)
         r_sc, r_ev, Kc, Vc = O.tova_decode_step(Kc, Vc, st["q"], st["k"], st["v"], free, scale)
         np.testing.assert_array_equal(host_bits(Kd), Kc)
+        np.testing.assert_array_equal(host_bits(Vd), Vc)
         assert_scores_close(g_sc.cpu().numpy(), r_sc)
         g_ev = fs.cpu().numpy()
         assert np.all(g_ev == g_ev[:, :1])
