@@ -429,6 +429,16 @@ kvc_status sh_update(kvc_sh_state* st, const int32_t* queue, int32_t m, int32_t 
   KVC_TRY(check_ptr(q_new, "q_new"));
   KVC_TRY(check_ptr(probs, "probs"));
   KVC_TRY(check_ws(ws, ws_bytes, scores_workspace(*kv, 1, KVC_REDUCE_GQA_GROUP), name));
+  {  // insert, score and record in one launch where the small-row scoring kernel applies
+    const cudaError_t e = launch_sh_update_fused(*st, queue, m, pos, q_new, k_new, v_new, K, V, *kv, scale, probs, ws,
+                                                 (cudaStream_t)stream);
+    if (e != cudaErrorNotSupported) {
+      KVC_TRY(cuda_status(e, "scissorhands update launch"));
+      if (!queue) st->n_free -= 1;
+      st->t += 1;
+      return KVC_OK;
+    }
+  }
   KVC_TRY(sh_insert(st, queue, m, pos, k_new, v_new, K, V, kv, stream));
   KVC_TRY(kvc_window_scores(q_new, K, kv, 1, scale, 0, st->live, KVC_REDUCE_GQA_GROUP, probs, ws, ws_bytes, stream));
   return kvc_scissorhands_update_from_probs(st, probs, stream);

@@ -117,6 +117,12 @@ struct ScoresArgs {
   const uint16_t* vnew;
   uint16_t* Kw;
   uint16_t* Vw;
+  // Scissorhands step fused into the small-row kernel (shs.B > 0): the new token takes the
+  // lowest free slot, or slot queue[(b*KVH+kvh)*qm + qpos] when queue is given, and the
+  // step's low-attention flags are recorded into the state as kvc_scissorhands.cu does.
+  kvc_sh_state shs;
+  const int32_t* queue;
+  int qm, qpos;
 };
 
 // (m, l) partial of query row r from key range `split`: a row's ranges are contiguous
@@ -189,6 +195,11 @@ cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc
 cudaError_t launch_tova_decode(const uint16_t* q, const uint16_t* knew, const uint16_t* vnew, uint16_t* K, uint16_t* V,
                                const kvc_kv_desc& kv, float scale, int32_t* free_slot, float* scores, void* ws,
                                cudaStream_t st);
+// One Scissorhands decode step (insert, score, record) as one small-row kernel launch;
+// cudaErrorNotSupported when the shapes need another scoring kernel.
+cudaError_t launch_sh_update_fused(const kvc_sh_state& s, const int32_t* queue, int qm, int qpos, const uint16_t* q,
+                                   const uint16_t* knew, const uint16_t* vnew, uint16_t* K, uint16_t* V,
+                                   const kvc_kv_desc& kv, float scale, float* probs, void* ws, cudaStream_t st);
 // value-channel score: cs[b,kvh,d] = sum_j wts[b,kvh,j] * V[b,kvh,j,d]^2 (kvc_gather.cu); ws holds
 // channel_score_workspace(kv, 0, false) bytes of partials
 cudaError_t launch_weighted_channel_norm(const float* wts, const uint16_t* V, const kvc_kv_desc& kv, float* cs,

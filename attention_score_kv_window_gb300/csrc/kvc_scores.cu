@@ -504,10 +504,51 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
   // a decode step's new token: its slot (slice-relative) reads the new key instead of the cache
   int wf = -1;
   const uint16_t* knew_lane = nullptr;
-  if (a.wslot) {
-    const int32_t f = __ldg(a.wslot + bk);
+  int keys = 0;  // Scissorhands: live keys once the new token is in
+  if (a.wslot || a.shs.B) {
+    int64_t f = -1;
+    if (a.wslot) {
+      f = __ldg(a.wslot + bk);
+    } else {
+      // every CTA of the row finds the lowest free slot (or reads the queued one) and counts
+      // the live keys; the live words of the row are not written until after the scores
+      __shared__ int s_cnt[NTHREADS / 32], s_free[NTHREADS / 32];
+      const int nw = a.shs.cap / 32;
+      const uint32_t* lwr = a.shs.live + (int64_t)bk * nw;
+      int cnt = 0, ff = 0x7fffffff;
+      for (int x = tid; x < nw; x += NTHREADS) {
+        const uint32_t v = lwr[x];
+        cnt += __popc(v);
+        if (v != 0xffffffffu) ff = min(ff, x * 32 + __ffs(~v) - 1);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        ff = min(ff, __shfl_xor_sync(0xffffffffu, ff, o));
+      }
+      if (lane == 0) {
+        s_cnt[warp] = cnt;
+        s_free[warp] = ff;
+      }
+      __syncthreads();
+      cnt = 0;
+      ff = 0x7fffffff;
+      for (int q = 0; q < NTHREADS / 32; ++q) {
+        cnt += s_cnt[q];
+        ff = min(ff, s_free[q]);
+      }
+      if (a.queue) {
+        f = __ldg(a.queue + (int64_t)bk * a.qm + a.qpos);
+        if (f >= 0 && f < a.S && !((lwr[f >> 5] >> (f & 31)) & 1u)) f = -1;  // a queued slot must be live
+        keys = cnt;
+      } else {
+        f = ff < a.S ? ff : -1;
+        keys = cnt + 1;
+      }
+    }
     if (f < 0 || f >= a.S) {
       if (tid == 0 && cr == 0) set_device_status(KVC_ERR_DEVICE_BOUNDS);
+      if (a.shs.B && keys > 0 && !a.queue) --keys;  // nothing was inserted
     } else if (f >= kbeg && f < kend) {
       wf = (int)(f - kbeg);
       knew_lane = a.knew + (int64_t)bk * D + cc * 8;
@@ -565,7 +606,7 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
     for (int e = 0; e < 2; ++e) {
       const int j = j0 + e;
       const bool in = j < len;
-      const bool lv = in && (lw == nullptr || live_bit(lw, kbeg + j));
+      const bool lv = in && (lw == nullptr || j == wf || live_bit(lw, kbeg + j));
       sA[e] = (lv && j <= limA) ? c[e] * a.sl2 : -CUDART_INF_F;
       sB[e] = (lv && j <= limB) ? c[2 + e] * a.sl2 : -CUDART_INF_F;
       if (g < R && in) lgA[j] = sA[e];
@@ -629,12 +670,41 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
   const float pw = a.pw;
 #pragma unroll
   for (int r = 0; r < RM; ++r) cv[r] = r < R ? crow[r] * pw : 0.f;
+  const float thr = __fdiv_rn(1.0f, (float)(keys > 0 ? keys : 1));  // Scissorhands: float32(1)/float32(keys)
   for (int j = tid; j < len; j += NTHREADS) {
     float sc = 0.f;
 #pragma unroll
     for (int r = 0; r < RM; ++r)
       if (r < R) sc += ex2(fmaf(lg[(int64_t)r * per + j], pw, -cv[r]));
-    out[j] = sc * a.out_mul;
+    const float p = sc * a.out_mul;
+    out[j] = p;
+    if (a.shs.B) {
+      // record: a slice is whole live words (it starts at a multiple of 64 keys and its
+      // length is a multiple of 32), so lane l of a warp holds bit l of word (kbeg + j) / 32
+      const int64_t gj = kbeg + j;
+      const bool fresh = j == wf;
+      const bool live = fresh || live_bit(lw, gj);
+      const bool flag = live && p < thr;
+      const uint32_t bits = __ballot_sync(0xffffffffu, flag);
+      const int64_t nw = a.shs.cap / 32;
+      uint32_t* hp = a.shs.hist + ((a.shs.t % a.shs.history) * a.shs.B * a.shs.KVH + bk) * nw + (gj >> 5);
+      const uint32_t old = *hp;
+      if (live) {
+        const int64_t x = (int64_t)bk * a.shs.cap + gj;
+        const int64_t ins = fresh ? a.shs.t : (int64_t)a.shs.insert_step[x];
+        const int oldbit = ((a.shs.t - ins) >= a.shs.history && ((old >> lane) & 1u)) ? 1 : 0;
+        const int lowv = fresh ? 0 : (int)a.shs.low_count[x];
+        a.shs.low_count[x] = (uint16_t)(lowv + (flag ? 1 : 0) - oldbit);
+        if (fresh) a.shs.insert_step[x] = (int32_t)a.shs.t;
+      }
+      __syncwarp();
+      if (lane == 0) *hp = bits;
+    }
+  }
+  if (a.shs.B && wf >= 0 && tid == 0) {  // the new token's slot is live from the next kernel on
+    const int64_t f = kbeg + wf;
+    atomicOr(a.shs.live + (int64_t)bk * (a.shs.cap / 32) + (f >> 5), 1u << (f & 31));
+    a.shs.slot[bk] = (int32_t)f;
   }
   // no remote access follows the cluster barrier: CTAs may leave independently
 }
@@ -857,6 +927,26 @@ cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc
   const ScoresArgs a = make_args(q, K, kv, w, scale, causal, live, reduce, scores, ws, power);
   if (kv.D == 64) return launch_impl<64>(a, reduce, scores, st);
   return launch_impl<128>(a, reduce, scores, st);
+}
+
+cudaError_t launch_sh_update_fused(const kvc_sh_state& sh, const int32_t* queue, int qm, int qpos, const uint16_t* q,
+                                   const uint16_t* knew, const uint16_t* vnew, uint16_t* K, uint16_t* V,
+                                   const kvc_kv_desc& kv, float scale, float* probs, void* ws, cudaStream_t st) {
+  ScoresArgs a = make_args(q, K, kv, 1, scale, 0, sh.live, KVC_REDUCE_GQA_GROUP, probs, ws, 1);
+  int64_t per = 0;
+  const int cs = small_cluster(a, &per);
+  if (cs == 0 || a.R > 16) return cudaErrorNotSupported;
+  a.shs = sh;
+  a.queue = queue;
+  a.qm = qm;
+  a.qpos = qpos;
+  a.knew = knew;
+  a.vnew = vnew;
+  a.Kw = K;
+  a.Vw = V;
+  cudaError_t e = kv.D == 64 ? set_smem_attrs<64>() : set_smem_attrs<128>();
+  if (e != cudaSuccess) return e;
+  return kv.D == 64 ? launch_small<64>(a, cs, per, st) : launch_small<128>(a, cs, per, st);
 }
 
 cudaError_t launch_tova_decode(const uint16_t* q, const uint16_t* knew, const uint16_t* vnew, uint16_t* K, uint16_t* V,

@@ -541,7 +541,8 @@ class ScissorhandsCase:
 
     def _update(self, i):
         rep = self.reps[i % self.R]
-        if rep["steps"] % self.wl.record_every:
+        rep["record"] = rep["steps"] % self.wl.record_every == 0  # this step scores and records
+        if not rep["record"]:
             return False
         j = i % self.nq
         qa = self._queue_args(rep)
@@ -551,7 +552,7 @@ class ScissorhandsCase:
 
     def _insert(self, i):
         rep = self.reps[i % self.R]
-        if rep["steps"] % self.wl.record_every == 0:
+        if rep["record"]:
             return False
         j = i % self.nq
         qa = self._queue_args(rep)
