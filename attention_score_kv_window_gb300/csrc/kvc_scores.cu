@@ -17,7 +17,9 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "kvc_internal.cuh"
 
@@ -792,18 +794,50 @@ cudaError_t set_smem_attrs() {
 }
 
 // Cluster size and keys per CTA for the single-pass small-row kernel; 0 when the logits of
-// one (b, kvh) do not fit the shared memory of an 8-CTA cluster.
+// one (b, kvh) do not fit the shared memory of an 8-CTA cluster.  Among the sizes whose
+// slices fit, the largest one whose clusters are all resident at once (as the occupancy
+// calculator counts them: GPCs hold whole clusters, so fewer fit than SMs * 3 / size) with
+// slices of at least 256 keys.
+int64_t small_per(const ScoresArgs& a, int cs) { return ((a.S + cs - 1) / cs + TK - 1) / TK * TK; }
+
+template <int D>
+int max_active_clusters(const ScoresArgs& a, int cs) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int, int64_t, bool>, int> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int64_t per = small_per(a, cs);
+  const auto key = std::make_tuple(dev, D, cs, (int64_t)a.R * per, a.R > 8);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchAttribute attrs[2];
+  const cudaLaunchConfig_t cfg =
+      pdl_config(dim3((unsigned)cs), dim3(NTHREADS), smem_small(D, a.R, per), nullptr, attrs, cs);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, a.R > 8 ? k_scores_small<D, true> : k_scores_small<D, false>, &cfg) !=
+      cudaSuccess) {
+    cudaGetLastError();  // clear the query's error; fall back to the SM count rule
+    n = 3 * num_sms() / cs;
+  }
+  cache[key] = n;
+  return n;
+}
+
+template <int D>
 int small_cluster(const ScoresArgs& a, int64_t* per_out) {
   if (a.R > 16) return 0;
   const int64_t units = (int64_t)a.B * a.KVH;
-  auto per_for = [&](int cs) { return ((a.S + cs - 1) / cs + TK - 1) / TK * TK; };
-  int cs = 1;
-  while (cs <= 8 && (int64_t)a.R * per_for(cs) * 4 > SMALL_LOGIT_BYTES) ++cs;
-  if (cs > 8) return 0;
-  // more CTAs while they still fit one wave (three CTAs per SM) and slices stay >= 256 keys
-  while (cs < 8 && units * (cs + 1) <= 3 * (int64_t)num_sms() && per_for(cs + 1) >= 256) ++cs;
-  if (units * cs > 2147483647LL) return 0;
-  *per_out = per_for(cs);
+  if (units * 8 > 2147483647LL) return 0;
+  int cs_min = 1;
+  while (cs_min <= 8 && (int64_t)a.R * small_per(a, cs_min) * 4 > SMALL_LOGIT_BYTES) ++cs_min;
+  if (cs_min > 8) return 0;
+  int cs = cs_min;
+  for (int c = cs_min + 1; c <= 8; ++c) {
+    if (small_per(a, c) < 256) break;
+    if (units <= (int64_t)max_active_clusters<D>(a, c)) cs = c;
+  }
+  *per_out = small_per(a, cs);
   return cs;
 }
 
@@ -822,7 +856,7 @@ cudaError_t launch_impl(const ScoresArgs& a, int reduce, float* scores, cudaStre
   cudaError_t e = set_smem_attrs<D>();
   if (e != cudaSuccess) return e;
   int64_t per = 0;
-  const int cs = small_cluster(a, &per);
+  const int cs = small_cluster<D>(a, &per);
   if (cs > 0) {
     e = launch_small<D>(a, cs, per, st);
     if (e != cudaSuccess) return e;
@@ -934,7 +968,9 @@ cudaError_t launch_sh_update_fused(const kvc_sh_state& sh, const int32_t* queue,
                                    const kvc_kv_desc& kv, float scale, float* probs, void* ws, cudaStream_t st) {
   ScoresArgs a = make_args(q, K, kv, 1, scale, 0, sh.live, KVC_REDUCE_GQA_GROUP, probs, ws, 1);
   int64_t per = 0;
-  const int cs = small_cluster(a, &per);
+  cudaError_t e0 = kv.D == 64 ? set_smem_attrs<64>() : set_smem_attrs<128>();
+  if (e0 != cudaSuccess) return e0;
+  const int cs = kv.D == 64 ? small_cluster<64>(a, &per) : small_cluster<128>(a, &per);
   if (cs == 0 || a.R > 16) return cudaErrorNotSupported;
   a.shs = sh;
   a.queue = queue;
@@ -954,7 +990,9 @@ cudaError_t launch_tova_decode(const uint16_t* q, const uint16_t* knew, const ui
                                cudaStream_t st) {
   ScoresArgs a = make_args(q, K, kv, 1, scale, 0, nullptr, KVC_REDUCE_ALL_HEADS, scores, ws, 1);
   int64_t per = 0;
-  const int cs = small_cluster(a, &per);
+  cudaError_t e0 = kv.D == 64 ? set_smem_attrs<64>() : set_smem_attrs<128>();
+  if (e0 != cudaSuccess) return e0;
+  const int cs = kv.D == 64 ? small_cluster<64>(a, &per) : small_cluster<128>(a, &per);
   if (cs == 0) return cudaErrorNotSupported;
   a.wslot = free_slot;
   a.knew = knew;
