@@ -77,6 +77,7 @@ _SIGNATURES = {
     "kvc_decode_attention": (_I32, [_P, _P, _P, _DESC, _P, _DESC, _P, _F, _P, _P, _SZ, _P]),
     "kvc_zero_add_back": (_I32, [_P, _DESC, _P, _P, _DESC, _P]),
     "kvc_value_channel_score": (_I32, [_P, _I32, _P, _P, _DESC, _F, _P, _P, _SZ, _P]),
+    "kvc_host_device_pointer": (_I32, [_P, ctypes.POINTER(ctypes.c_void_p)]),
     "kvc_get_device_status": (_I32, [_P]),
     "kvc_status_string": (ctypes.c_char_p, [_I32]),
     "kvc_last_error_message": (ctypes.c_char_p, []),
@@ -118,6 +119,23 @@ def _ptr(t) -> int | None:
     if not t.is_cuda:
         raise ValueError("tensor must be on a CUDA device")
     return t.data_ptr()
+
+
+def host_device_pointer(t) -> int:
+    """Device address of a page-locked host tensor (kvc_host_device_pointer)."""
+    out = ctypes.c_void_p()
+    _check(load_library().kvc_host_device_pointer(ctypes.c_void_p(t.data_ptr()), ctypes.byref(out)))
+    return out.value
+
+
+def _vptr(V) -> int | None:
+    """V of the compaction calls: a CUDA tensor, or a page-locked host tensor whose kept rows
+    the compaction kernel reads over the host link."""
+    if V is not None and not V.is_cuda:
+        if not V.is_pinned():
+            raise ValueError("V must be on a CUDA device or in page-locked host memory")
+        return host_device_pointer(V)
+    return _ptr(V)
 
 
 def _stream(stream=None) -> int:
@@ -216,11 +234,11 @@ def kvc_compact_kv(K, V, idx, H=None, K_out=None, V_out=None, stream=None):
     if K_out is None:
         K_out = torch.empty((B, KVH, k, D), dtype=K.dtype, device=K.device)
     if V is not None and V_out is None:
-        V_out = torch.empty((B, KVH, k, D), dtype=V.dtype, device=V.device)
+        V_out = torch.empty((B, KVH, k, D), dtype=V.dtype, device=K.device)
     _dense(K_out, (B, KVH, k, D), "K_out")
     if V_out is not None:
         _dense(V_out, (B, KVH, k, D), "V_out")
-    _check(lib.kvc_compact_kv(_ptr(K), _ptr(V), ctypes.byref(desc), _ptr(idx.contiguous()), k, _ptr(K_out),
+    _check(lib.kvc_compact_kv(_ptr(K), _vptr(V), ctypes.byref(desc), _ptr(idx.contiguous()), k, _ptr(K_out),
                               _ptr(V_out), _stream(stream)))
     return K_out, V_out
 
@@ -240,11 +258,11 @@ def kvc_topk_compact(scores, K, V, k, protect_tail=0, live_mask=None, largest=Tr
     if K_out is None:
         K_out = torch.empty((B, KVH, k, D), dtype=K.dtype, device=K.device)
     if V is not None and V_out is None:
-        V_out = torch.empty((B, KVH, k, D), dtype=V.dtype, device=V.device)
+        V_out = torch.empty((B, KVH, k, D), dtype=V.dtype, device=K.device)
     _dense(K_out, (B, KVH, k, D), "K_out")
     if V_out is not None:
         _dense(V_out, (B, KVH, k, D), "V_out")
-    _check(lib.kvc_topk_compact(_ptr(scores.contiguous()), _ptr(K), _ptr(V), ctypes.byref(desc), int(k),
+    _check(lib.kvc_topk_compact(_ptr(scores.contiguous()), _ptr(K), _vptr(V), ctypes.byref(desc), int(k),
                                 int(protect_tail), _ptr(live_mask), int(bool(largest)), _ptr(idx), _ptr(K_out),
                                 _ptr(V_out), _stream(stream)))
     return idx, K_out, V_out
@@ -267,7 +285,7 @@ def kvc_compress_prefill(q_win, K, V, scale, k, protect_tail=0, reduce="gqa", ou
                torch.empty((B, KVH, k, D), dtype=V.dtype, device=dev))
     scores, idx, K_out, V_out = out
     ws, nbytes = _ws(KVC_OP_COMPRESS_PREFILL, desc, w, k, ws, K.device)
-    _check(lib.kvc_compress_prefill(_ptr(q_win.contiguous()), _ptr(K), _ptr(V), ctypes.byref(desc), w,
+    _check(lib.kvc_compress_prefill(_ptr(q_win.contiguous()), _ptr(K), _vptr(V), ctypes.byref(desc), w,
                                     float(scale), REDUCE[reduce], int(k), int(protect_tail), _ptr(scores),
                                     _ptr(idx), _ptr(K_out), _ptr(V_out), _ptr(ws), nbytes, _stream(stream)))
     return scores, idx, K_out, V_out

@@ -595,6 +595,24 @@ kvc_status kvc_zero_add_back(const kvc_bf16* Kp, const kvc_kv_desc* pd, const in
   return cuda_status(launch_zero_add_back(Kp, *pd, ch, K_out, *od, (cudaStream_t)stream), "kvc_zero_add_back launch");
 }
 
+kvc_status kvc_host_device_pointer(const void* host_ptr, void** dev_ptr) {
+  if (!host_ptr || !dev_ptr) return fail(KVC_ERR_INVALID_ARG, "kvc_host_device_pointer: NULL argument");
+  *dev_ptr = nullptr;
+  cudaPointerAttributes at{};
+  cudaError_t e = cudaPointerGetAttributes(&at, host_ptr);
+  if (e != cudaSuccess || at.type != cudaMemoryTypeHost) {
+    cudaGetLastError();  // the query's own error, if any: not a failure of earlier work
+    return fail(KVC_ERR_INVALID_ARG, "kvc_host_device_pointer: not page-locked host memory");
+  }
+  e = cudaHostGetDevicePointer(dev_ptr, const_cast<void*>(host_ptr), 0);
+  if (e != cudaSuccess || *dev_ptr == nullptr) {
+    cudaGetLastError();
+    *dev_ptr = nullptr;
+    return fail(KVC_ERR_INVALID_ARG, "kvc_host_device_pointer: host memory not mapped for the device");
+  }
+  return KVC_OK;
+}
+
 kvc_status kvc_get_device_status(kvc_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "kvc_get_device_status sync");

@@ -333,10 +333,11 @@ class PrefillCase:
 
     def e2e(self, steps, stream, world, dist, dev):
         """Same step through kvc_compress_prefill with pinned host inputs and outputs.  Steps are
-        pipelined over two device buffer sets: step i+1's host->device copies (the two halves of
-        K and of V each on its own copy stream, q with the last) overlap step i's compute and
-        its device->host read-back (another stream).  Every step moves its full inputs and
-        results."""
+        pipelined over two device buffer sets: step i+1's host->device copies (the four
+        quarters of K each on its own copy stream, q with the last) overlap step i's compute and
+        its device->host read-back (another stream).  V stays in page-locked host memory: the
+        compaction kernel reads the kept rows over the host link (kvc_host_device_pointer), so
+        only those cross it.  Every step moves its inputs and results."""
         torch, kvc, wl = self.torch, self.kvc, self.wl
         inp = self.host
         hq = torch.from_numpy(inp["q"].view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -352,13 +353,13 @@ class PrefillCase:
         s_out = torch.cuda.Stream()
         ev = lambda: torch.cuda.Event()  # noqa: E731
         in_ready = [[ev() for _ in range(4)] for _ in range(2)]   # inputs of a buffer set uploaded
-        fK, fV = hK.view(-1), hV.view(-1)
-        half = fK.numel() // 2
+        fK = hK.view(-1)
+        qn = fK.numel() // 4
 
-        def pieces(dq, dK, dV):  # contiguous halves of the flattened K and V
-            gK, gV = dK.view(-1), dV.view(-1)
-            return (((gK[:half], fK[:half]),), ((gK[half:], fK[half:]),),
-                    ((gV[:half], fV[:half]),), ((gV[half:], fV[half:]), (dq, hq)))
+        def pieces(dq, dK, dV):  # contiguous quarters of the flattened K
+            gK = dK.view(-1)
+            return (((gK[:qn], fK[:qn]),), ((gK[qn:2 * qn], fK[qn:2 * qn]),),
+                    ((gK[2 * qn:3 * qn], fK[2 * qn:3 * qn]),), ((gK[3 * qn:], fK[3 * qn:]), (dq, hq)))
         comp_done = [ev() for _ in range(2)]          # compute on a buffer set finished
         out_done = [ev() for _ in range(2)]           # results of a buffer set read back
         used = [False, False]
@@ -379,7 +380,7 @@ class PrefillCase:
                 stream.wait_event(ev_)
             if used[x]:
                 stream.wait_event(out_done[x])  # its previous results were read back
-            kvc.kvc_compress_prefill(dq, dK, dV, wl.scale, k, protect_tail=wl.protect_tail, reduce=wl.reduce,
+            kvc.kvc_compress_prefill(dq, dK, hV, wl.scale, k, protect_tail=wl.protect_tail, reduce=wl.reduce,
                                      out=(sc, idx, Ko, Vo), ws=ws)
             comp_done[x].record(stream)
             s_out.wait_event(comp_done[x])
@@ -407,9 +408,10 @@ class PrefillCase:
         torch.cuda.synchronize()
         ms = max_over_ranks(e0.elapsed_time(e1), world, dist, dev)
         return {"value": self.tokens_per_step * steps * world / (ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": int((hq.numel() + hK.numel() + hV.numel()) * 2),
+                "h2d_bytes_per_step": int((hq.numel() + hK.numel()) * 2 + B * KVH * k * D * 2),
                 "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in h_out[0])),
-                "pipeline": "two buffer sets; uploads (four streams), compute and read-back on separate streams"}
+                "pipeline": "two buffer sets; K uploads (four streams), compute and read-back on separate "
+                            "streams; V read in place from page-locked host memory, kept rows only"}
 
 
 class TovaDecodeCase:

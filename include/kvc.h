@@ -154,7 +154,9 @@ kvc_status kvc_topk_select(const float* scores, int32_t B, int32_t KVH, int64_t 
  * kvc_compact_kv — gather the kept rows into a dense cache:
  *   K_out[b,kvh,t,:] = K[b,kvh,idx[b,kvh,t],:], same for V; idx -1 writes a zero row.
  *   idx [B,KVH,k] int32 in [-1, S); K_out, V_out [B,KVH,k,D] dense bf16 out.
- *   V and V_out may both be NULL (keys only).  Outputs must not overlap inputs.
+ *   V and V_out may both be NULL (keys only).  Outputs must not overlap inputs.  V may be
+ *   the device address of page-locked host memory (kvc_host_device_pointer): only the kept
+ *   rows are read.
  *   An index >= S is skipped and reported as KVC_ERR_DEVICE_BOUNDS by kvc_get_device_status.
  * ------------------------------------------------------------------------------------- */
 kvc_status kvc_compact_kv(const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_desc* kv,
@@ -360,6 +362,14 @@ kvc_status kvc_decode_attention(const kvc_bf16* q, const int32_t* ch, const kvc_
  *   outside [0, D) are skipped and record KVC_ERR_DEVICE_BOUNDS. */
 kvc_status kvc_zero_add_back(const kvc_bf16* Kp, const kvc_kv_desc* pd, const int32_t* ch,
                              kvc_bf16* K_out, const kvc_kv_desc* od, kvc_stream_t stream);
+
+/* Device address of page-locked (pinned) host memory, for the inputs that may stay on the
+ * host: V of kvc_compact_kv, kvc_topk_compact and kvc_compress_prefill is read only by the
+ * compaction kernel, with plain loads, row by row, so passing this address moves just the
+ * kept rows over the host link instead of uploading all of V.  KVC_ERR_INVALID_ARG when
+ * host_ptr is not page-locked host memory mapped for the current device.  No other pointer
+ * argument of this library may be host memory. */
+kvc_status kvc_host_device_pointer(const void* host_ptr, void** dev_ptr);
 
 /* Synchronize `stream`, then return (and clear) the sticky device status: KVC_OK,
  * KVC_ERR_DEVICE_BOUNDS or KVC_ERR_TIMEOUT.  KVC_ERR_CUDA if the sync itself failed. */

@@ -237,6 +237,23 @@ def test_topk_compact_exact(B, KVH, S, k, protect, D, ties, largest, live_p, wit
     assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
 
+def test_compaction_reads_v_from_page_locked_host_memory():
+    """V may stay in page-locked host memory: the compaction kernel reads the kept rows over
+    the host link; results are bit-identical to a device V."""
+    B, H, KVH, D, S, k = 2, 8, 2, 128, 3000, 700
+    sc = random_scores((B, KVH, S), 71, tie_levels=0)
+    K = normal_bf16((B, KVH, S, D), 71, 2)
+    V = normal_bf16((B, KVH, S, D), 71, 3)
+    hV = torch.from_numpy(V.view(np.int16)).view(torch.bfloat16).pin_memory()
+    idx, Ko, Vo = kvc.kvc_topk_compact(torch.from_numpy(sc).cuda(), dev_bf16(K), hV, k, protect_tail=64, H=H)
+    ref_idx = O.topk_select(sc, k, protect_tail=64)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    rK, rV = O.compact_kv(K, V, ref_idx)
+    np.testing.assert_array_equal(host_bits(Ko), rK)
+    np.testing.assert_array_equal(host_bits(Vo), rV)
+    assert kvc.kvc_get_device_status() == kvc.KVC_OK
+
+
 def test_compact_out_of_range_index_reports_bounds():
     K = dev_bf16(normal_bf16((1, 1, 10, 64), 1, 1))
     idx = dev_i32(np.array([[[0, 10, 3]]]))
