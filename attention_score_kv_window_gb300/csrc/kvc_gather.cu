@@ -124,21 +124,39 @@ __global__ void __launch_bounds__(256) k_channel_partial(const uint16_t* __restr
   const int64_t r0 = (int64_t)split * chunk, r1 = std::min(nrows, r0 + chunk);
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   const uint16_t* Kb = K + b * sb + kvh * sh;
-  for (int64_t r = r0 + rl; r < r1; r += RPP) {
-    int64_t j = r;
-    if (idx) {
-      j = __ldg(idx + (int64_t)bk * k + r);
-      if (j < 0) continue;
-      if (j >= S) { set_device_status(KVC_ERR_DEVICE_BOUNDS); continue; }
-    }
-    if (wts) {
-      float t[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      acc_sq8(t, ld16(Kb + j * ss + c * 8));
-      const float wj = __ldg(wts + (int64_t)bk * S + j);
+  // four rows per thread in flight: their indices first, then their loads
+  constexpr int U = 4;
+  for (int64_t rb = r0 + rl; rb < r1; rb += U * RPP) {
+    int64_t j[U];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, t[i], acc[i]);
-    } else {
-      acc_sq8(acc, ld16(Kb + j * ss + c * 8));
+    for (int u = 0; u < U; ++u) {
+      const int64_t r = rb + (int64_t)u * RPP;
+      j[u] = -1;
+      if (r < r1) {
+        j[u] = idx ? (int64_t)__ldg(idx + (int64_t)bk * k + r) : r;
+        if (j[u] >= S) {
+          set_device_status(KVC_ERR_DEVICE_BOUNDS);
+          j[u] = -1;
+        }
+      }
+    }
+    uint4 v[U];
+    float wj[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      v[u] = j[u] >= 0 ? ld16(Kb + j[u] * ss + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+      wj[u] = (wts && j[u] >= 0) ? __ldg(wts + (int64_t)bk * S + j[u]) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (wts) {
+        float t[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        acc_sq8(t, v[u]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[u], t[i], acc[i]);
+      } else {
+        acc_sq8(acc, v[u]);  // zero rows (index -1 or past the range) add nothing
+      }
     }
   }
 #pragma unroll
@@ -176,11 +194,27 @@ __global__ void __launch_bounds__(1024) k_channel_final(const uint16_t* __restri
   const int d = threadIdx.x % D, grp = threadIdx.x / D, ngrp = blockDim.x / D;
   const uint16_t* qg = q + ((int64_t)(b * H + kvh * G) * w) * D + d;  // the group's G*w rows are contiguous
   float sq = 0.f, kn = 0.f;
-  for (int r = grp; r < G * w; r += ngrp) {
-    const float v = __uint_as_float((uint32_t)__ldg(qg + (int64_t)r * D) << 16);
-    sq = fmaf(v, v, sq);
+  // eight independent loads in flight per step (the rows and partials are strided)
+  for (int r = grp; r < G * w; r += 8 * ngrp) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int rr = r + u * ngrp;
+      v[u] = rr < G * w ? __uint_as_float((uint32_t)__ldg(qg + (int64_t)rr * D) << 16) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) sq = fmaf(v[u], v[u], sq);
   }
-  for (int s = grp; s < nsplit; s += ngrp) kn += __ldg(part + ((int64_t)s * B * KVH + bk) * D + d);
+  for (int s = grp; s < nsplit; s += 8 * ngrp) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int ss = s + u * ngrp;
+      v[u] = ss < nsplit ? __ldg(part + ((int64_t)ss * B * KVH + bk) * D + d) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) kn += v[u];
+  }
   qred[grp][d] = sq;
   kred[grp][d] = kn;
   __syncthreads();

@@ -729,15 +729,24 @@ __global__ void k_scores_allheads(const float* __restrict__ grp, float* __restri
 
 // TOVA decode: the all-heads mean (as k_scores_allheads) fused with the eviction of the
 // lowest-ranked slot per batch row (lowest score; equal scores: the highest slot), written
-// to slot[b*KVH+kvh] for every kvh.  One CTA per batch row.
-__global__ void __launch_bounds__(1024) k_allheads_evict1(const float* __restrict__ grp, float* __restrict__ out,
-                                                          int KVH, int64_t S, int32_t* __restrict__ slot) {
-  __shared__ unsigned long long wbest[32];
+// to slot[b*KVH+kvh] for every kvh.  A cluster of CTAs per batch row splits the slots; each
+// CTA stores its best composite into rank 0's shared memory, and after one cluster barrier
+// rank 0 picks the winner.
+constexpr int EVICT_CLUSTER = 8;
+
+__global__ void __launch_bounds__(256) k_allheads_evict1(const float* __restrict__ grp, float* __restrict__ out,
+                                                         int KVH, int64_t S, int64_t per, int32_t* __restrict__ slot) {
+  __shared__ unsigned long long wbest[8];
+  __shared__ unsigned long long cbest[EVICT_CLUSTER];
   pdl_wait();  // previous kernel on the stream complete and visible
-  const int64_t b = blockIdx.x;
+  unsigned int cs, cr;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(cs));
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(cr));
+  const int64_t b = blockIdx.x / cs;
+  const int64_t j0 = (int64_t)cr * per, j1 = min(S, j0 + per);
   const float inv = 1.f / (float)KVH;
   unsigned long long best = 0ull;
-  for (int64_t j = threadIdx.x; j < S; j += blockDim.x) {
+  for (int64_t j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
     float s = 0.f;
     for (int kv = 0; kv < KVH; ++kv) s += grp[(b * KVH + kv) * S + j];
     s *= inv;
@@ -756,15 +765,21 @@ __global__ void __launch_bounds__(1024) k_allheads_evict1(const float* __restric
   }
   if ((threadIdx.x & 31) == 0) wbest[threadIdx.x >> 5] = best;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    best = threadIdx.x < (blockDim.x >> 5) ? wbest[threadIdx.x] : 0ull;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
-      best = y > best ? y : best;
-    }
-    for (int kv = threadIdx.x; kv < KVH; kv += 32) slot[b * KVH + kv] = best ? (int32_t)(uint32_t)best : -1;
+  if (threadIdx.x == 0) {
+    for (unsigned int q = 1; q < (blockDim.x >> 5); ++q) best = wbest[q] > best ? wbest[q] : best;
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n"
+                 : "=r"(ra)
+                 : "r"((uint32_t)__cvta_generic_to_shared(&cbest[cr])), "r"(0));
+    asm volatile("st.shared::cluster.u64 [%0], %1;\n" ::"r"(ra), "l"(best) : "memory");
   }
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+  if (cr == 0 && threadIdx.x < 32) {
+    unsigned long long w = 0ull;
+    for (unsigned int q = 0; q < cs; ++q) w = cbest[q] > w ? cbest[q] : w;
+    for (int kv = threadIdx.x; kv < KVH; kv += 32) slot[b * KVH + kv] = w ? (int32_t)(uint32_t)w : -1;
+  }
+  // no remote access follows the cluster barrier: CTAs may leave independently
 }
 
 size_t smem_pass1(int D, int rows) { return (size_t)(rows + STAGES * TK) * (D + 8) * 2 + 8 * 16 * sizeof(float2); }
@@ -1003,9 +1018,11 @@ cudaError_t launch_tova_decode(const uint16_t* q, const uint16_t* knew, const ui
   if (e != cudaSuccess) return e;
   e = kv.D == 64 ? launch_small<64>(a, cs, per, st) : launch_small<128>(a, cs, per, st);
   if (e != cudaSuccess) return e;
-  const int threads = (int)std::min<int64_t>(1024, std::max<int64_t>(32, (kv.S + 31) / 32 * 32));
-  e = launch_pdl(k_allheads_evict1, dim3(kv.B), dim3(threads), 0, st, (const float*)a.out, scores, kv.KVH, kv.S,
-                 free_slot);
+  const int ecs = EVICT_CLUSTER;
+  const int64_t eper = (kv.S + ecs - 1) / ecs;
+  cudaLaunchAttribute attrs[2];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)(kv.B * ecs)), dim3(256), 0, st, attrs, ecs);
+  e = cudaLaunchKernelEx(&cfg, k_allheads_evict1, (const float*)a.out, scores, kv.KVH, kv.S, eper, free_slot);
   if (e != cudaSuccess) return e;
   return launched(1);
 }
