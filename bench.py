@@ -19,6 +19,7 @@ import math
 import multiprocessing as mp
 import os
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -55,7 +56,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # the raw samples go to KVC_CLOCKS_DIR when set (kept for inspection), else a temp dir
+        out_dir = os.environ.get("KVC_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"kvc_clocks_gpu{gpu_index}.csv")
 
     def start(self):
         try:
