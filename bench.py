@@ -19,8 +19,8 @@ import math
 import multiprocessing as mp
 import os
 import subprocess
-import tempfile
 import sys
+import tempfile
 import time
 
 import numpy as np
