@@ -433,11 +433,13 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass2(const ScoresArgs a) {
 // shared memory (log2 domain, masked ones -inf), computes per-row (max, sum), pushes them to
 // every peer, and after one cluster barrier merges them and writes its slice's scores.
 // ----------------------------------------------------------------------------------------
-constexpr int SMALL_STAGES = 3;
+// per-warp ring stages of 8-key chunks: 64-channel rows are half as long, so twice the
+// chunks stay in flight for the same bytes
+constexpr int small_stages(int D) { return D == 64 ? 6 : 3; }
 constexpr int SMALL_LOGIT_BYTES = 16 * 1024;  // per CTA; keeps three CTAs per SM
 
 size_t smem_small(int D, int R, int64_t per) {
-  return (size_t)(16 + SMALL_STAGES * TK) * (D + 8) * 2 + (size_t)R * per * 4 + 16 * 8 * sizeof(float2) +
+  return (size_t)(16 + 64 * small_stages(D)) * (D + 8) * 2 + (size_t)R * per * 4 + 16 * 8 * sizeof(float2) +
          8 * 16 * sizeof(float2) + 16 * sizeof(float) + 64;
 }
 
@@ -468,7 +470,8 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
 
   uint16_t* Qs = reinterpret_cast<uint16_t*>(smem);
   uint16_t* Ks = Qs + 16 * P;
-  float* lg = reinterpret_cast<float*>(Ks + SMALL_STAGES * TK * P);          // [R][per]
+  constexpr int WST = small_stages(D);  // stages per warp (8 warps x WST x 8 key rows)
+  float* lg = reinterpret_cast<float*>(Ks + 64 * WST * P);                  // [R][per]
   float2* xch = reinterpret_cast<float2*>(lg + (int64_t)R * per);            // [8 ranks][16 rows], pushed by peers
   float2* red = xch + 8 * 16;                                                // [8 warps][16 rows]
   float* crow = reinterpret_cast<float*>(red + 8 * 16);                      // [16]
@@ -491,8 +494,6 @@ __global__ void __launch_bounds__(NTHREADS, 3) k_scores_small(const ScoresArgs a
     const int c = ks * 16 + ((lane >> 4) & 1) * 8;
     ldsm_x4(smem_u32(Qs + r * P + c), aq[ks][0], aq[ks][1], aq[ks][2], aq[ks][3]);
   }
-  constexpr int WST = SMALL_STAGES;       // stages per warp
-  static_assert(8 * WST * 8 == SMALL_STAGES * TK, "per-warp rings fill the K staging area");
   constexpr int CH = D / 8;               // 16-byte pieces per key row
   constexpr int PPL = 8 * CH / 32;        // pieces per lane per chunk
   const uint32_t ring = smem_u32(Ks + warp * WST * 8 * P);
