@@ -342,6 +342,59 @@ def test_tova_decode_steps_teacher_forced(B, H, KVH, D, S, budget, steps):
     assert near <= 2
 
 
+def test_think_128k_layer_sampled_kv_head():
+    """The ThinK + SnapKV 128K layer at full size, in the launch configuration the benchmark
+    times: every KV head on the GPU, one KV head by the oracle (scores, kept set, compacted
+    rows, channel scores); every row's scores sum to the window length."""
+    from synth import THINK_128K
+    wl = THINK_128K
+    inp = prefill_inputs(wl)
+    G, scale = wl.G, wl.scale
+    q, K, V = dev_bf16(inp["q"]), dev_bf16(inp["K"]), dev_bf16(inp["V"])
+    sc, idx, Ko, Vo = kvc.kvc_compress_prefill(q, K, V, scale, wl.k, protect_tail=wl.protect_tail, reduce="gqa")
+    cs = kvc.kvc_channel_score(q, Ko).cpu().numpy()
+    np.testing.assert_allclose(sc.double().sum(-1).cpu().numpy(), wl.w, rtol=1e-4)
+    kv = 3
+    qh, Kh, Vh = inp["q"][:, kv * G:(kv + 1) * G], inp["K"][:, kv:kv + 1], inp["V"][:, kv:kv + 1]
+    ref = O.window_scores(qh, Kh, scale, causal=True, reduce="gqa")
+    g_sc = sc.cpu().numpy()[:, kv:kv + 1]
+    assert_scores_close(g_sc, ref)
+    g_idx = idx.cpu().numpy()[:, kv:kv + 1]
+    assert_selection_matches(g_idx, ref, wl.k, protect_tail=wl.protect_tail)
+    rK, rV = O.compact_kv(Kh, Vh, g_idx)  # the gather, given the GPU's kept set
+    np.testing.assert_array_equal(host_bits(Ko)[:, kv:kv + 1], rK)
+    np.testing.assert_array_equal(host_bits(Vo)[:, kv:kv + 1], rV)
+    assert_scores_close(cs[:, kv:kv + 1], O.channel_score(qh, Kh, kept=g_idx), what="channel score")
+
+
+def test_tova_decode_full_size_properties():
+    """B 16, 2049 slots (the benchmark's decode shape): each row's scores are a mean of softmax
+    rows (sum 1), identical for every KV head of a batch row, and the evicted slot is their
+    argmin (lowest score; ties: highest slot); the new rows land in the freed slots."""
+    B, H, KVH, D, n = 16, 32, 8, 128, 2049
+    g = torch.Generator(device="cuda").manual_seed(5)
+    K = torch.randn((B, KVH, n, D), generator=g, device="cuda").to(torch.bfloat16)
+    V = torch.randn((B, KVH, n, D), generator=g, device="cuda").to(torch.bfloat16)
+    free = torch.full((B, KVH), n - 1, dtype=torch.int32, device="cuda")
+    for step in range(3):
+        q = torch.randn((B, H, D), generator=g, device="cuda").to(torch.bfloat16)
+        kn = torch.randn((B, KVH, D), generator=g, device="cuda").to(torch.bfloat16)
+        vn = torch.randn((B, KVH, D), generator=g, device="cuda").to(torch.bfloat16)
+        slot = free.clone()
+        sc = kvc.kvc_tova_decode_step(q, kn, vn, K, V, 1.0 / np.sqrt(D), free).cpu().numpy()
+        s = slot.cpu().numpy()
+        for b in range(B):
+            for h in range(KVH):
+                assert torch.equal(K[b, h, s[b, h]], kn[b, h]) and torch.equal(V[b, h, s[b, h]], vn[b, h])
+        np.testing.assert_allclose(sc.astype(np.float64).sum(-1), 1.0, rtol=1e-4)
+        assert np.all(sc == sc[:, :1])
+        ev = free.cpu().numpy()
+        for b in range(B):
+            row = sc[b, 0]
+            exp = max(range(n), key=lambda j: (-row[j], j))
+            assert np.all(ev[b] == exp)
+
+
 # ----------------------------------------------------------------------------------------
 # Scissorhands
 # ----------------------------------------------------------------------------------------
