@@ -433,12 +433,17 @@ def test_scissorhands_update_from_probs_and_evict_exact():
     assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
 
-@pytest.mark.parametrize("policy", ["bulk", "queue", "sparse"])
-def test_scissorhands_full_update_teacher_forced(policy):
+SH_SHAPES = {"g4": (2, 8, 2, 128, 512, 400, 32), "g16_d64": (1, 16, 1, 64, 256, 5, 16)}
+
+
+@pytest.mark.parametrize("policy,shape", [("bulk", "g4"), ("queue", "g4"), ("sparse", "g4"), ("bulk", "g16_d64"),
+                                          ("queue", "g16_d64")])
+def test_scissorhands_full_update_teacher_forced(policy, shape):
     """Full decode steps through the library.  bulk: evict m every m steps; queue: once full,
     refill an eviction queue every m steps and replace one queued token per step; sparse:
-    insert every step, score and record only every M-th step (bulk eviction)."""
-    B, H, KVH, D, cap, hist, m = 2, 8, 2, 128, 512, 400, 32
+    insert every step, score and record only every M-th step (bulk eviction).  g16_d64: 16
+    query rows per KV head (both accumulator halves), 64-channel rows, a short history."""
+    B, H, KVH, D, cap, hist, m = SH_SHAPES[shape]
     M = 3 if policy == "sparse" else 1
     wl = Workload("t", B=B, H=H, KVH=KVH, D=D, S=cap, w=1, k=cap, reduce="gqa", causal=False, seed=51)
     pre = prefill_inputs(wl)
