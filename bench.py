@@ -138,8 +138,29 @@ def cpu_baseline(config: str, budget_s: float = 10.0):
     p.join()
     wl = WORKLOADS[config]
     return {"value": res["value"], "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "cpu": _cpu_model(),
             "sample": f"{res['kv_heads']} KV-head groups of the {wl.name} layer (oracle compress_prefill, "
                       f"float64 numpy, {res['seconds']:.1f} s), scaled to a full layer of {wl.KVH} KV heads"}
+
+
+def _cpu_model() -> str:
+    """The host CPU's model name as the kernel reports it; on Arm the core's part number
+    (0xd4f: Neoverse V2, Grace's core), else the architecture name."""
+    import platform
+    part = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model"):
+                    return line.split(":", 1)[1].strip()
+                if key == "cpu part" and part is None:
+                    part = line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    if part is not None:
+        return f"{platform.machine()} " + ({"0xd4f": "Neoverse V2"}.get(part.lower(), f"cpu part {part}"))
+    return platform.machine()
 
 
 # ----------------------------------------------------------------------------------------
