@@ -105,8 +105,8 @@ class ClockSampler:
 
 
 def _oracle_sample(config: str, budget_s: float, threads: int, q):
-    os.environ.setdefault("OPENBLAS_NUM_THREADS", str(threads))
-    os.environ.setdefault("OMP_NUM_THREADS", str(threads))
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = str(threads)  # before numpy loads its BLAS in this fresh process
     import oracle as O
     wl = WORKLOADS[config]
     inp = prefill_inputs(wl)
@@ -128,17 +128,23 @@ def _oracle_sample(config: str, budget_s: float, threads: int, q):
     q.put({"value": tokens / dt, "seconds": dt, "kv_heads": heads})
 
 
-def cpu_baseline(config: str, budget_s: float = 10.0):
-    threads = os.cpu_count() or 1
+def _oracle_run(config: str, budget_s: float, threads: int) -> dict:
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     p = ctx.Process(target=_oracle_sample, args=(config, budget_s, threads, q))
     p.start()
     res = q.get(timeout=budget_s * 20 + 600)
     p.join()
+    return res
+
+
+def cpu_baseline(config: str, budget_s: float = 10.0):
+    threads = os.cpu_count() or 1
+    res = _oracle_run(config, budget_s, threads)
+    one = _oracle_run(config, budget_s / 2, 1)
     wl = WORKLOADS[config]
     return {"value": res["value"], "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "cpu": _cpu_model(),
+            "single_thread_value": one["value"], "cpu": _cpu_model(),
             "sample": f"{res['kv_heads']} KV-head groups of the {wl.name} layer (oracle compress_prefill, "
                       f"float64 numpy, {res['seconds']:.1f} s), scaled to a full layer of {wl.KVH} KV heads"}
 
