@@ -192,6 +192,23 @@ def test_compact_is_a_row_gather():
     assert np.all(Kc[0, 0, 3] == 0)
 
 
+def test_write_slots_replaces_one_row_per_head():
+    B, KVH, S, D = 2, 3, 9, 4
+    K = normal_bf16((B, KVH, S, D), 23, 1)
+    V = normal_bf16((B, KVH, S, D), 23, 2)
+    kn = normal_bf16((B, KVH, D), 23, 3)
+    vn = normal_bf16((B, KVH, D), 23, 4)
+    slot = np.array([[0, 8, 4], [3, 3, 7]], np.int32)
+    K2, V2 = O.write_slots(K, V, kn, vn, slot)
+    for b in range(B):
+        for kv in range(KVH):
+            for j in range(S):
+                want_k = kn[b, kv] if j == slot[b, kv] else K[b, kv, j]
+                want_v = vn[b, kv] if j == slot[b, kv] else V[b, kv, j]
+                assert K2[b, kv, j].tolist() == want_k.tolist() and V2[b, kv, j].tolist() == want_v.tolist()
+    np.testing.assert_array_equal(K, normal_bf16((B, KVH, S, D), 23, 1))  # inputs are not modified in place
+
+
 # ----------------------------------------------------------------------------------------
 # ThinK
 # ----------------------------------------------------------------------------------------
