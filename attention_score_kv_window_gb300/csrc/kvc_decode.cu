@@ -117,7 +117,8 @@ __device__ __forceinline__ float ex2f(float x) {
 //           V comes in with ldmatrix.trans.
 // Dead or missing keys are zero-filled by the copy (no stale data reaches the products) and
 // masked to -inf before the softmax.  The warps then merge through shared memory into one
-// (m, l, o) partial per head; k_decode_combine merges the key ranges.
+// (m, l, o) partial per head; k_decode_combine merges the key ranges (when a row is one
+// range, the kernel normalises and writes the output itself).
 template <int CK, int D, bool H16>
 __global__ void __launch_bounds__(DaShape<CK, D>::THREADS, 1) k_decode_attn(DecodeArgs a) {
   using Sh = DaShape<CK, D>;
@@ -320,6 +321,10 @@ __global__ void __launch_bounds__(DaShape<CK, D>::THREADS, 1) k_decode_attn(Deco
         lv += e[1] * f;
       }
     }
+    if (a.nsplit == 1) {  // the CTA saw the whole row: normalise here, no combine kernel
+      a.out[((int64_t)b * a.H + (int64_t)kvh * a.G + gh) * D + d] = lv > 0.f ? ov / lv : 0.f;
+      continue;
+    }
     const int64_t pi = ((int64_t)row * a.nsplit + split) * a.G + gh;
     a.po[pi * D + d] = ov;
     if (d == 0) a.pml[pi] = make_float2(M, lv);
@@ -475,6 +480,7 @@ cudaError_t launch_decode_attention(const uint16_t* q, const int32_t* ch, const 
   else if (Ck == 128 && D == 128) e = run_decode<128, 128>(a, grid, st);
   else return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
+  if (p.nsplit == 1) return launched(1);  // rows were not split: already normalised
   const int64_t heads = rows * a.G;
   const dim3 cgrid((unsigned)((heads + 7) / 8));
   e = D == 64 ? launch_pdl(k_decode_combine<64>, cgrid, dim3(256), 0, st, a, heads)
