@@ -72,6 +72,13 @@ def test_host_validation_without_gpu(lib):
     assert lib.kvc_window_scores(FAKE + 2, FAKE, ctypes.byref(d), 1, 0.1, 1, None, 0, FAKE, FAKE, 1 << 30, None) \
         == kvc.KVC_ERR_INVALID_ARG
     assert "aligned" in kvc.load_library().kvc_last_error_message().decode()
+    # empty cache, and a row longer than the selection supports
+    empty = _desc(S=0)
+    assert lib.kvc_window_scores(FAKE, FAKE, ctypes.byref(empty), 1, 0.1, 1, None, 0, FAKE, FAKE, 1 << 30, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_topk_select(FAKE, 1, 1, 0, 4, 0, None, 1, FAKE, None, 0, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_topk_select(FAKE, 1, 1, 8 * 40960 + 1, 4, 0, None, 1, FAKE, None, 0, None) \
+        == kvc.KVC_ERR_UNSUPPORTED
     # protect_tail larger than k, and with evict order
     assert lib.kvc_topk_select(FAKE, 1, 2, 128, 4, 8, None, 1, FAKE, None, 0, None) == kvc.KVC_ERR_INVALID_ARG
     assert lib.kvc_topk_select(FAKE, 1, 2, 128, 4, 2, None, 0, FAKE, None, 0, None) == kvc.KVC_ERR_INVALID_ARG
