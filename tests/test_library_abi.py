@@ -34,6 +34,21 @@ def test_header_declares_the_boundary():
         assert must in names
 
 
+def test_header_is_plain_c(tmp_path):
+    """include/kvc.h compiles as C99 and as C++ (no torch or CUDA headers needed)."""
+    import shutil
+    import subprocess
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    for compiler, std, ext in (("gcc", "-std=c99", "c"), ("g++", "-std=c++17", "cpp")):
+        if shutil.which(compiler) is None:
+            pytest.skip(f"{compiler} not available")
+        src = tmp_path / f"use.{ext}"
+        src.write_text('#include "kvc.h"\nint use(void) { return (int)kvc_version(); }\n')
+        r = subprocess.run([compiler, std, "-Wall", "-Werror", "-pedantic", "-fsyntax-only", "-I", inc, str(src)],
+                           capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
