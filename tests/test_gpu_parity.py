@@ -501,6 +501,41 @@ def test_scissorhands_full_update_teacher_forced(policy, shape):
     assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
 
+def test_scissorhands_resume_from_saved_state():
+    """Checkpoint / resume: the state is plain caller-owned tensors plus two host counters, so
+    copying them out and back in continues the run exactly (same flags, counts, evictions)."""
+    B, KVH, cap, hist, m = 2, 2, 128, 7, 8
+    g = np.random.Generator(np.random.PCG64([61]))
+    probs = [g.random((B, KVH, cap)).astype(np.float32) * np.float32(2.0 / cap) for _ in range(24)]
+    st = kvc.ScissorhandsState(B, KVH, cap, history=hist)
+    kvc.kvc_scissorhands_init(st, cap)
+
+    def run(state, steps):
+        evs = []
+        for i in steps:
+            kvc.kvc_scissorhands_update_from_probs(state, torch.from_numpy(probs[i]).cuda())
+            if (i + 1) % m == 0:
+                evs.append(kvc.kvc_scissorhands_evict(state, m).cpu().numpy())
+        return evs
+
+    run(st, range(12))
+    saved = {n: getattr(st, n).clone() for n in ("hist", "low_count", "insert_step", "live", "slot")}
+    t, n_free = st.c.t, st.c.n_free
+    ev_a = run(st, range(12, 24))
+    after = {n: getattr(st, n).clone() for n in saved}
+    st2 = kvc.ScissorhandsState(B, KVH, cap, history=hist)
+    for n, v in saved.items():
+        getattr(st2, n).copy_(v)
+    st2.c.t, st2.c.n_free = t, n_free
+    ev_b = run(st2, range(12, 24))
+    assert len(ev_a) == len(ev_b) == 2
+    for a, b in zip(ev_a, ev_b):
+        np.testing.assert_array_equal(a, b)
+    for n in saved:
+        assert torch.equal(after[n], getattr(st2, n)), n
+    assert (st.t, st.n_free) == (st2.t, st2.n_free)
+
+
 def test_scissorhands_refill_queue_exact_with_ties():
     """Refills on states with many equal fractions (short history, few distinct counts):
     the queue lists the oracle's order exactly, -1 padded when fewer slots are live."""
