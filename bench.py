@@ -174,35 +174,95 @@ def _cpu_model() -> str:
 # ----------------------------------------------------------------------------------------
 
 
+def _reference_case(wl):
+    """The oracle's version of one workload step on a sample: (step(i), tokens a step of the
+    sample covers, description).  Samples are one KV head (prefill) or one batch row
+    (decode); rates scale to the whole workload by tokens."""
+    import oracle as O
+    from synth import decode_step_inputs, normal_bf16
+    G = wl.G
+    name = wl.name
+    if name.startswith("tova_decode"):
+        n = wl.k + 1
+        Kc = normal_bf16((1, wl.KVH, n, wl.D), wl.seed, 901)
+        Vc = normal_bf16((1, wl.KVH, n, wl.D), wl.seed, 902)
+        st = {"K": Kc, "V": Vc, "free": np.full((1, wl.KVH), wl.k, np.int32)}
+
+        def step(i):
+            x = decode_step_inputs(wl.with_(B=1), i)
+            _, ev, st["K"], st["V"] = O.tova_decode_step(st["K"], st["V"], x["q"], x["k"], x["v"], st["free"],
+                                                         wl.scale)
+            st["free"] = ev.astype(np.int32)
+        return step, n, "one batch row per step (oracle tova_decode_step)"
+    if name.startswith("scissorhands"):
+        cap = wl.S
+        K = normal_bf16((1, wl.KVH, cap, wl.D), wl.seed, 903)
+        sh = O.Scissorhands(1, wl.KVH, cap, history=wl.history)
+        sh.prefill(wl.prefill_live)
+        st = {"K": K, "queue": None, "pos": wl.m, "n": 0}
+
+        def step(i):
+            x = decode_step_inputs(wl.with_(B=1), i)
+            rep = None
+            if wl.policy == "queue" and sh.live.all():
+                if st["pos"] == wl.m:
+                    st["queue"], st["pos"] = sh.refill_queue(wl.m), 0
+                rep = st["queue"][..., st["pos"]]
+                st["pos"] += 1
+            slot = sh.insert(replace=rep)
+            st["K"], _ = O.write_slots(st["K"], st["K"], x["k"], x["k"], slot)
+            if st["n"] % wl.record_every == 0:
+                sh.record(O.scissorhands_probs(x["q"], st["K"], wl.scale, sh.live))
+            st["n"] += 1
+            if wl.policy != "queue" and not (~sh.live).any():
+                sh.evict(wl.m)
+        return step, cap, f"one batch row per step (oracle Scissorhands, {wl.policy} eviction)"
+    if "decode_b16_s8192" in name:
+        q = normal_bf16((1, wl.H, wl.D), wl.seed, 904)
+        Kf = normal_bf16((1, wl.KVH, wl.S, wl.D), wl.seed, 905)
+        V = normal_bf16((1, wl.KVH, wl.S, wl.D), wl.seed, 906)
+        C = wl.C
+        if C < wl.D:
+            ch = np.sort(np.stack([np.random.Generator(np.random.PCG64([wl.seed, 907, kv])).permutation(wl.D)[:C]
+                                   for kv in range(wl.KVH)])[None], axis=-1).astype(np.int32)
+            Kp = np.take_along_axis(Kf, ch[:, :, None, :].astype(np.int64), axis=-1)
+
+            def step(i):
+                O.decode_attention_pruned(q, ch, Kp, V, wl.scale)
+        else:
+            def step(i):
+                O.decode_attention(q, Kf, V, wl.scale)
+        return step, wl.S, "one batch row per step (oracle decode attention)"
+    inp = prefill_inputs(wl)
+
+    def step(i):
+        kv = i % wl.KVH
+        O.compress_prefill(inp["q"][:, kv * G:(kv + 1) * G], inp["K"][:, kv:kv + 1], inp["V"][:, kv:kv + 1],
+                           wl.scale, wl.k, protect_tail=wl.protect_tail, reduce="gqa")
+    return step, wl.B * wl.S / wl.KVH, f"one of {wl.KVH} KV-head groups per step (oracle compress_prefill)"
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     wl = WORKLOADS[args.config]
     threads = os.cpu_count() or 1
-    import oracle as O
-    inp = prefill_inputs(wl)
-    G = wl.G
-
-    def step(i):
-        kv = i % wl.KVH
-        O.compress_prefill(inp["q"][:, kv * G:(kv + 1) * G], inp["K"][:, kv:kv + 1], inp["V"][:, kv:kv + 1],
-                           wl.scale, wl.k, protect_tail=wl.protect_tail, reduce="gqa")
-
+    step, tokens, sample = _reference_case(wl)
     for i in range(args.warmup):
         step(i)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        step(i)
+        step(args.warmup + i)
     dt = time.perf_counter() - t0
-    value = wl.B * wl.S * args.steps / wl.KVH / dt
+    value = tokens * args.steps / dt
     line = {"impl": "reference", "metric": "kv_tokens_scored_compacted_per_s_per_layer", "value": value,
             "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "sample": "one KV head per step"},
+            "config": {"workload": wl.name, "sample": sample},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": f"each step: one of {wl.KVH} KV-head groups of {wl.name}, scaled to a layer"},
+                             "sample": f"{sample}, of {wl.name}, scaled by tokens"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
