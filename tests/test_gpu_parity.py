@@ -433,6 +433,27 @@ def test_scissorhands_update_from_probs_and_evict_exact():
     assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
 
+def test_scissorhands_threshold_counts_live_keys_hand_built():
+    """cold-compress PR 11 (``keys = attn.shape[1]``, flags written to ``[:keys]``): the
+    threshold is 1/(live keys), not 1/capacity.  5 of 32 slots live (slots 0..4); the flags,
+    bit plane and counts expected are written out here, not taken from the oracle."""
+    cap = 32
+    st = kvc.ScissorhandsState(1, 1, cap, history=4)
+    kvc.kvc_scissorhands_init(st, 5)
+    fifth = np.float32(1) / np.float32(5)
+    p = np.zeros((1, 1, cap), np.float32)
+    p[0, 0, :5] = [fifth, np.nextafter(fifth, np.float32(0)), np.float32(0.0625),
+                   np.nextafter(fifth, np.float32(1)), np.float32(0.5)]
+    p[0, 0, 5:] = np.float32(1e-9)  # dead slots: never flagged
+    kvc.kvc_scissorhands_update_from_probs(st, torch.from_numpy(p).cuda())
+    plane0 = st.hist[0, 0, 0, 0].item() & 0xffffffff
+    assert plane0 == 0b00110, bin(plane0)  # slots 1 and 2 are low
+    low = st.low_count.cpu().numpy().view(np.uint16)[0, 0]
+    np.testing.assert_array_equal(low[:5], [0, 1, 1, 0, 0])
+    assert st.t == 1
+    assert kvc.kvc_get_device_status() == kvc.KVC_OK
+
+
 SH_SHAPES = {"g4": (2, 8, 2, 128, 512, 400, 32), "g16_d64": (1, 16, 1, 64, 256, 5, 16)}
 
 

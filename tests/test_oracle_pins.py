@@ -409,6 +409,31 @@ def test_low_flag_threshold_is_strict_float32():
     assert O.low_attention_bits(p, live).tolist() == [[[False, True, False]]]
 
 
+def test_low_flag_threshold_counts_live_keys_not_capacity():
+    """cold-compress PR 11, review of ``cache.py``: ``keys = attn.shape[1]`` is the width of
+    the attention row, and the step's flags are written to ``attn_history[:, :, :keys, ...]``,
+    the slots the query attended.  Uniform attention over those keys is 1/keys, so with
+    5 live slots out of 32 the threshold is float32(1/5), not 1/32.  Expected flags written
+    out by hand: exactly 1/5 is not low; one ulp below 1/5 is low although it is 6x above
+    1/32; dead slots are never flagged whatever their probability."""
+    cap = 32
+    live = np.zeros((1, 1, cap), bool)
+    live[0, 0, [1, 4, 9, 20, 31]] = True
+    fifth = np.float32(1) / np.float32(5)
+    p = np.zeros((1, 1, cap), np.float32)
+    p[0, 0, 1] = fifth                                   # uniform: not low
+    p[0, 0, 4] = np.nextafter(fifth, np.float32(0))     # below uniform, far above 1/cap: low
+    p[0, 0, 9] = np.float32(0.0625)                      # 1/16 < 1/5: low
+    p[0, 0, 20] = np.nextafter(fifth, np.float32(1))    # above uniform: not low
+    p[0, 0, 31] = np.float32(0.5)                        # not low
+    p[0, 0, 0] = np.float32(0.0)                         # dead slots: never low
+    p[0, 0, 2] = np.float32(1e-9)
+    expected = np.zeros((1, 1, cap), bool)
+    expected[0, 0, 4] = True
+    expected[0, 0, 9] = True
+    np.testing.assert_array_equal(O.low_attention_bits(p, live), expected)
+
+
 def test_uniform_attention_sets_no_flag_and_dominant_key_flags_the_rest():
     B, H, KVH, D, cap = 1, 4, 2, 8, 64
     live = np.zeros((B, KVH, cap), bool)
