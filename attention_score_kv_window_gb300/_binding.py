@@ -269,8 +269,9 @@ def kvc_topk_compact(scores, K, V, k, protect_tail=0, live_mask=None, largest=Tr
 
 
 def kvc_compress_prefill(q_win, K, V, scale, k, protect_tail=0, reduce="gqa", out=None, ws=None,
-                         stream=None):
-    """Returns (scores, idx, K_out, V_out)."""
+                         stream=None, keep_scores=True):
+    """Returns (scores, idx, K_out, V_out).  ``keep_scores=False`` (or ``out`` with scores
+    None) leaves the scores unwritten: the call then returns None in their place."""
     lib = load_library()
     B, H, w, D = q_win.shape
     _, KVH, S, _ = K.shape
@@ -279,7 +280,7 @@ def kvc_compress_prefill(q_win, K, V, scale, k, protect_tail=0, reduce="gqa", ou
         raise ValueError("V must have K's shape and strides")
     if out is None:
         dev = K.device
-        out = (torch.empty((B, KVH, S), dtype=torch.float32, device=dev),
+        out = (torch.empty((B, KVH, S), dtype=torch.float32, device=dev) if keep_scores else None,
                torch.empty((B, KVH, k), dtype=torch.int32, device=dev),
                torch.empty((B, KVH, k, D), dtype=K.dtype, device=dev),
                torch.empty((B, KVH, k, D), dtype=V.dtype, device=dev))

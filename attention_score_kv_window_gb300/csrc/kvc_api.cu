@@ -184,7 +184,13 @@ size_t kvc_workspace_size(kvc_op op, const kvc_kv_desc* kv, int32_t w, int32_t k
       return scores_workspace(*kv, w, KVC_REDUCE_ALL_HEADS);
     case KVC_OP_COMPRESS_PREFILL:
       if (check_window(kv, w, "kvc_workspace_size") != KVC_OK) return (size_t)-1;
-      return scores_workspace(*kv, w, KVC_REDUCE_ALL_HEADS);
+      // the fused short-row kernel needs none; otherwise the window-score scratch plus room
+      // for the scores when the caller passes none
+      if (prefill_fused_supported(*kv, w, k, KVC_REDUCE_GQA_GROUP) &&
+          prefill_fused_supported(*kv, w, k, KVC_REDUCE_ALL_HEADS))
+        return 0;
+      return (scores_workspace(*kv, w, KVC_REDUCE_ALL_HEADS) + 255) / 256 * 256 +
+             (size_t)kv->B * kv->KVH * kv->S * sizeof(float);
     case KVC_OP_TOVA_DECODE_STEP:
     case KVC_OP_SCISSORHANDS_UPDATE:
       return scores_workspace(*kv, 1, KVC_REDUCE_ALL_HEADS);
@@ -331,12 +337,50 @@ kvc_status kvc_compress_prefill(const kvc_bf16* q_win, const kvc_bf16* K, const 
                                 kvc_head_reduce reduce, int32_t k, int32_t protect_tail,
                                 float* scores, int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out,
                                 void* ws, size_t ws_bytes, kvc_stream_t stream) {
-  KVC_TRY(check_desc(kv, "kvc_compress_prefill"));
+  const char* who = "kvc_compress_prefill";
+  KVC_TRY(check_desc(kv, who));
   if (k < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill: k must be >= 1");
+  KVC_TRY(check_window(kv, w, who));
   if (protect_tail < 0 || protect_tail > k || protect_tail > w)
     return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill: need 0 <= protect_tail <= min(k, w)");
-  KVC_TRY(kvc_window_scores(q_win, K, kv, w, scale, 1, nullptr, reduce, scores, ws, ws_bytes, stream));
-  return kvc_topk_compact(scores, K, V, kv, k, protect_tail, nullptr, 1, idx, K_out, V_out, stream);
+  if (reduce != KVC_REDUCE_GQA_GROUP && reduce != KVC_REDUCE_ALL_HEADS)
+    return fail(KVC_ERR_INVALID_ARG, "unknown head reduction");
+  if (!(scale > 0.f) || scale != scale) return fail(KVC_ERR_INVALID_ARG, "scale must be > 0");
+  KVC_TRY(check_ptr(q_win, "q_win"));
+  KVC_TRY(check_gather(K, V, kv, k, K_out, V_out, who));
+  if (kv->S > topk_max_len()) return fail(KVC_ERR_UNSUPPORTED, "kvc_compress_prefill: S > %lld", (long long)topk_max_len());
+  KVC_TRY(check_ptr(idx, "idx"));
+  if (scores && !aligned16(scores)) return fail(KVC_ERR_INVALID_ARG, "scores is not 16-byte aligned");
+  {  // no output may overlap another output or an input
+    const uintptr_t osz = (uintptr_t)kv->B * kv->KVH * (uintptr_t)k * kv->D * 2;
+    const uintptr_t ko = reinterpret_cast<uintptr_t>(K_out), vo = reinterpret_cast<uintptr_t>(V_out);
+    const uintptr_t i0 = reinterpret_cast<uintptr_t>(idx), i1 = i0 + (uintptr_t)kv->B * kv->KVH * k * 4;
+    uintptr_t k0, k1, v0 = 0, v1 = 0;
+    cache_range(K, *kv, &k0, &k1);
+    if (V) cache_range(V, *kv, &v0, &v1);
+    if (overlaps(i0, i1, ko, ko + osz) || (V_out && overlaps(i0, i1, vo, vo + osz)) || overlaps(i0, i1, k0, k1) ||
+        (V && overlaps(i0, i1, v0, v1)))
+      return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill: idx overlaps another argument");
+    if (scores) {
+      const uintptr_t s0 = reinterpret_cast<uintptr_t>(scores), s1 = s0 + (uintptr_t)kv->B * kv->KVH * kv->S * 4;
+      if (overlaps(s0, s1, ko, ko + osz) || (V_out && overlaps(s0, s1, vo, vo + osz)) || overlaps(s0, s1, i0, i1) ||
+          overlaps(s0, s1, k0, k1) || (V && overlaps(s0, s1, v0, v1)))
+        return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill: scores overlaps another argument");
+    }
+  }
+  // short rows: one fused kernel (scores, selection and compaction per (b, kvh); no workspace)
+  if (prefill_fused_supported(*kv, w, k, reduce))
+    return cuda_status(launch_prefill_fused(q_win, K, V, *kv, w, scale, reduce, k, protect_tail, scores, idx, K_out,
+                                            V_out, (cudaStream_t)stream),
+                       "kvc_compress_prefill launch");
+  // otherwise: window scores (into `scores`, or into the workspace when scores is NULL), then
+  // selection and compaction
+  const size_t sc_need = (scores_workspace(*kv, w, reduce) + 255) / 256 * 256;
+  const size_t need = scores ? sc_need : sc_need + (size_t)kv->B * kv->KVH * kv->S * sizeof(float);
+  KVC_TRY(check_ws(ws, ws_bytes, need, who));
+  float* sc = scores ? scores : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sc_need);
+  KVC_TRY(kvc_window_scores(q_win, K, kv, w, scale, 1, nullptr, reduce, sc, ws, sc_need, stream));
+  return kvc_topk_compact(sc, K, V, kv, k, protect_tail, nullptr, 1, idx, K_out, V_out, stream);
 }
 
 kvc_status kvc_write_slots(const kvc_bf16* k_new, const kvc_bf16* v_new, const int32_t* slot,

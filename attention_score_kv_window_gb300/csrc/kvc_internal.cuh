@@ -206,6 +206,17 @@ cudaError_t launch_weighted_channel_norm(const float* wts, const uint16_t* V, co
                                          void* ws, cudaStream_t st);
 
 // ----------------------------------------------------------------------------------------
+// fused prefill compression for short rows (kvc_prefill.cu): scores, top-k and compaction of
+// one (b, kvh) per CTA, K read once into shared memory.  Supported when G*w <= 16, the key
+// block fits shared memory (S <= 1024 at 64 channels, 512 at 128), k <= S rounded up to 64
+// and, in all-heads mode, KVH <= 8.  cudaErrorNotSupported otherwise.
+// ----------------------------------------------------------------------------------------
+bool prefill_fused_supported(const kvc_kv_desc& kv, int w, int k, int reduce);
+cudaError_t launch_prefill_fused(const uint16_t* q, const uint16_t* K, const uint16_t* V, const kvc_kv_desc& kv, int w,
+                                 float scale, int reduce, int k, int protect, float* scores, int32_t* idx,
+                                 uint16_t* Ko, uint16_t* Vo, cudaStream_t st);
+
+// ----------------------------------------------------------------------------------------
 // selection (kvc_select.cu)
 // ----------------------------------------------------------------------------------------
 int64_t topk_max_len();  // longest row kvc_topk_select accepts

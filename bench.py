@@ -1,12 +1,14 @@
 """Benchmark: KV tokens scored + compacted per second per layer, with the HBM / tensor roofline.
 
-One step = one pass of the prefill compression hot path over one synthetic layer: window
-scores (two passes over K on tensor cores) -> per-KV-head top-k with the observation window
-protected -> gather-compaction of the kept K/V rows.  Default workload: the SnapKV prefill of
-a Llama-3-8B-shaped layer (batch 1, 32 query / 8 KV heads, head_dim 128, 32768 tokens,
-window 64, keep 4096 per KV head, bf16, 1% heavy-hitter keys).
+One step = one pass of the prefill compression hot path over one synthetic batch: window
+scores -> per-KV-head top-k (the observation window protected for SnapKV) -> gather-compaction
+of the kept K/V rows.  Default workload: TOVA prefill (8 query / 2 KV heads, head_dim 64, 512
+tokens, the last query's attention averaged over all heads, keep 256 per KV head, bf16), run as
+8192 independent instances per step (one layer of 256 requests x 32 layers, or any other set
+of independent prefills of this shape); on this shape the library runs the whole path as one
+fused kernel.  Other workloads: ``--config``.
 
-Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config NAME]
 Multi-GPU (torchrun): every rank compresses its own replica (independent layers, weak scaling,
 no collective on the data path); the timed region is bracketed by barriers and the max over
 ranks is reported.
@@ -29,9 +31,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from synth import WORKLOADS, SNAPKV_32K, prefill_inputs  # noqa: E402
+from synth import WORKLOADS, TOVA_PREFILL, prefill_inputs  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
+# independent instances stacked into one step when --instances is not given: TOVA prefill of a
+# 512-token layer is far too small to measure alone, so the step runs 8192 of them
+DEFAULT_INSTANCES = {TOVA_PREFILL.name: 8192}
 
 
 def _peaks():
@@ -104,49 +109,71 @@ class ClockSampler:
 # ----------------------------------------------------------------------------------------
 
 
-def _oracle_sample(config: str, budget_s: float, threads: int, q):
-    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[var] = str(threads)  # before numpy loads its BLAS in this fresh process
+def _oracle_unit(wl, inp, i):
+    """One unit of oracle work on a prefill workload and the tokens it covers.  All-heads
+    scoring (TOVA) needs every head of an instance: one whole instance per unit.  Group
+    scoring (SnapKV, ThinK): one KV head and its query group per unit, a 1/KVH share of a
+    layer's tokens."""
     import oracle as O
-    wl = WORKLOADS[config]
-    inp = prefill_inputs(wl)
+    if wl.reduce == "all_heads":
+        O.compress_prefill(inp["q"], inp["K"], inp["V"], wl.scale, wl.k, protect_tail=wl.protect_tail,
+                           reduce="all_heads")
+        return wl.B * wl.S
     G = wl.G
+    kv = i % wl.KVH
+    O.compress_prefill(inp["q"][:, kv * G:(kv + 1) * G], inp["K"][:, kv:kv + 1], inp["V"][:, kv:kv + 1],
+                       wl.scale, wl.k, protect_tail=wl.protect_tail, reduce="gqa")
+    return wl.B * wl.S / wl.KVH
+
+
+def _oracle_worker(config: str, budget_s: float, worker: int, q):
+    """One process of the oracle sample: whole units until the time budget is used.  Each
+    worker takes its own instance seed (instances are independent units of work)."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"  # before numpy loads its BLAS in this fresh process
+    wl = WORKLOADS[config]
+    inp = prefill_inputs(wl, seed=wl.seed + worker)
     t0 = time.perf_counter()
-    heads = 0
-    # sample: one KV head (its G query heads, the whole sequence) per iteration
+    tokens, units = 0.0, 0
     while True:
-        kv = heads % wl.KVH
-        qg = inp["q"][:, kv * G:(kv + 1) * G]
-        Kg = inp["K"][:, kv:kv + 1]
-        Vg = inp["V"][:, kv:kv + 1]
-        O.compress_prefill(qg, Kg, Vg, wl.scale, wl.k, protect_tail=wl.protect_tail, reduce="gqa")
-        heads += 1
+        tokens += _oracle_unit(wl, inp, units)
+        units += 1
         if time.perf_counter() - t0 >= budget_s:
             break
-    dt = time.perf_counter() - t0
-    tokens = wl.B * wl.S * heads / wl.KVH  # a layer's tokens are scored once all KV heads are done
-    q.put({"value": tokens / dt, "seconds": dt, "kv_heads": heads})
+    q.put({"tokens": tokens, "seconds": time.perf_counter() - t0, "units": units})
 
 
-def _oracle_run(config: str, budget_s: float, threads: int) -> dict:
+def _oracle_run(config: str, budget_s: float, workers: int) -> dict:
+    """``workers`` spawned processes (no CUDA in them) run the oracle at the same time, each
+    on its own units; the rate is the tokens of all of them over the longest one's time."""
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    p = ctx.Process(target=_oracle_sample, args=(config, budget_s, threads, q))
-    p.start()
-    res = q.get(timeout=budget_s * 20 + 600)
-    p.join()
-    return res
+    ps = [ctx.Process(target=_oracle_worker, args=(config, budget_s, w, q)) for w in range(workers)]
+    for p_ in ps:
+        p_.start()
+    res = [q.get(timeout=budget_s * 20 + 900) for _ in ps]
+    for p_ in ps:
+        p_.join()
+    dt = max(r["seconds"] for r in res)
+    return {"value": sum(r["tokens"] for r in res) / dt, "seconds": dt, "units": sum(r["units"] for r in res)}
 
 
 def cpu_baseline(config: str, budget_s: float = 10.0):
-    threads = os.cpu_count() or 1
-    res = _oracle_run(config, budget_s, threads)
-    one = _oracle_run(config, budget_s / 2, 1)
+    """The oracle (float64 numpy, single-threaded per process) on the host's cores: one process
+    per core, each on its own independent units, and one process alone for the one-core rate."""
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    res = _oracle_run(config, budget_s / 4, cores)
+    one = _oracle_run(config, budget_s, 1)
     wl = WORKLOADS[config]
-    return {"value": res["value"], "unit": "tokens/s", "cores": threads, "kind": "oracle",
+    unit = "whole instances (B 1)" if wl.reduce == "all_heads" else f"KV-head groups (one of {wl.KVH} per layer)"
+    return {"value": res["value"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "single_thread_value": one["value"], "cpu": _cpu_model(),
-            "sample": f"{res['kv_heads']} KV-head groups of the {wl.name} layer (oracle compress_prefill, "
-                      f"float64 numpy, {res['seconds']:.1f} s), scaled to a full layer of {wl.KVH} KV heads"}
+            "sample": f"{res['units']} {unit} of {wl.name} (oracle compress_prefill, float64 numpy) in "
+                      f"{res['seconds']:.1f} s, {cores} processes of one thread each, one per core; "
+                      f"rate scaled to tokens"}
 
 
 def _cpu_model() -> str:
@@ -234,11 +261,13 @@ def _reference_case(wl):
                 O.decode_attention(q, Kf, V, wl.scale)
         return step, wl.S, "one batch row per step (oracle decode attention)"
     inp = prefill_inputs(wl)
+    if wl.reduce == "all_heads":  # all-heads scoring needs a whole instance
+        def step(i):
+            _oracle_unit(wl, inp, i)
+        return step, wl.B * wl.S, "one whole instance (B 1) per step (oracle compress_prefill)"
 
     def step(i):
-        kv = i % wl.KVH
-        O.compress_prefill(inp["q"][:, kv * G:(kv + 1) * G], inp["K"][:, kv:kv + 1], inp["V"][:, kv:kv + 1],
-                           wl.scale, wl.k, protect_tail=wl.protect_tail, reduce="gqa")
+        _oracle_unit(wl, inp, i)
     return step, wl.B * wl.S / wl.KVH, f"one of {wl.KVH} KV-head groups per step (oracle compress_prefill)"
 
 
@@ -247,7 +276,7 @@ def run_reference(args):
     if rank != 0:
         return
     wl = WORKLOADS[args.config]
-    threads = os.cpu_count() or 1
+    threads = 1  # the oracle as it stands: one process, single-threaded numpy loops
     step, tokens, sample = _reference_case(wl)
     for i in range(args.warmup):
         step(i)
@@ -260,7 +289,9 @@ def run_reference(args):
             "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "sample": sample},
+            "config": {"workload": wl.name, "sample": sample,
+                       "instances": args.instances if args.instances is not None
+                       else DEFAULT_INSTANCES.get(wl.name, 1)},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "sample": f"{sample}, of {wl.name}, scaled by tokens"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -316,6 +347,19 @@ def _traffic(kernel_key, sources):
 CSRC = "attention_score_kv_window_gb300/csrc/"
 SCORE_SOURCES = [CSRC + f for f in ("kvc_scores.cu", "kvc_scores_tc.cu", "kvc_internal.cuh")]
 DECODE_SOURCES = [CSRC + f for f in ("kvc_decode.cu", "kvc_decode.cuh")]
+PREFILL_SOURCES = [CSRC + f for f in ("kvc_prefill.cu", "kvc_internal.cuh")]
+
+
+def _sha256_arrays(arrays) -> str:
+    """SHA-256 of the input bytes (numpy arrays, or torch tensors copied to the host), in order:
+    the oracle and the GPU path consume these same bytes."""
+    import hashlib
+    h = hashlib.sha256()
+    for a in arrays:
+        if not isinstance(a, np.ndarray):
+            a = a.detach().cpu().contiguous().view(-1).view(__import__("torch").uint8).numpy()
+        h.update(np.ascontiguousarray(a).view(np.uint8).reshape(-1).data)
+    return h.hexdigest()
 
 
 class Call:
@@ -325,6 +369,7 @@ class Call:
     def __init__(self, label, fn, nbytes, flops=0.0, bound="hbm", sources=None, kernel_key=None, roofline=False):
         self.label, self.fn, self.nbytes, self.flops, self.bound = label, fn, nbytes, flops, bound
         self.sources, self.kernel_key, self.roofline = sources, kernel_key, roofline
+        self.one_pass_flops = None  # tensor-bound scoring: the flops of one pass over K
         self.times = []
 
 
@@ -340,6 +385,7 @@ class PrefillCase:
         self.wl = wl
         inp = prefill_inputs(wl, seed=rank_seed(wl.seed, rank))
         self.host = inp
+        self.inputs_sha256 = _sha256_arrays([inp["q"], inp["K"], inp["V"]])
 
         def to_dev(u16):
             return torch.from_numpy(u16.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -356,18 +402,28 @@ class PrefillCase:
                       torch.empty((B, KVH, k, D), dtype=bf, device=dev), torch.empty((B, KVH, k, D), dtype=bf, device=dev))
                      for _ in range(R)]
         lib = kvc.load_library()
-        self.ws = torch.empty(int(lib.kvc_workspace_size(2, kvc.kv_desc(K0, wl.H), wl.w, k)), dtype=torch.uint8,
-                              device=dev)
+        ws_bytes = int(lib.kvc_workspace_size(2, kvc.kv_desc(K0, wl.H), wl.w, k))
+        # shapes the library runs as one fused kernel need no workspace
+        self.fused = ws_bytes == 0 and not wl.C
+        self.ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         self.tokens_per_step = B * S
         G = wl.H // wl.KVH
+        # the step's algorithmic bytes: K read once, the kept V rows read, the kept K and V rows
+        # written, the window queries and the indices
+        self.step_bytes = B * KVH * D * 2 * (S + 3 * k) + B * wl.H * wl.w * D * 2 + B * KVH * k * 4
         sc_bytes = B * KVH * S * D * 2 + B * wl.H * wl.w * D * 2 + B * KVH * S * 4
-        sc_flops = 2 * 2.0 * B * wl.H * wl.w * S * D  # both passes of q_win K^T
+        sc_flops = 2 * 2.0 * B * wl.H * wl.w * S * D  # both passes of q_win K^T (the two-pass softmax)
         big_w = wl.w * G > 32
-        self.calls = [
-            Call("window_scores", self._scores, sc_bytes, sc_flops, "tensor" if big_w else "hbm", SCORE_SOURCES,
-                 f"window_scores/{wl.name}/B{B}"),
-            Call("topk_compact", self._topk_compact, B * KVH * S * 4 + 4 * B * KVH * k * D * 2 + B * KVH * k * 4),
-        ]
+        if self.fused:
+            self.calls = [Call("compress_prefill", self._compress, self.step_bytes, 2.0 * B * wl.H * wl.w * S * D,
+                               "hbm", PREFILL_SOURCES, f"compress_prefill/{wl.name}/B{B}", roofline=True)]
+        else:
+            self.calls = [
+                Call("window_scores", self._scores, sc_bytes, sc_flops, "tensor" if big_w else "hbm", SCORE_SOURCES,
+                     f"window_scores/{wl.name}/B{B}"),
+                Call("topk_compact", self._topk_compact, B * KVH * S * 4 + 4 * B * KVH * k * D * 2 + B * KVH * k * 4),
+            ]
+            self.calls[0].one_pass_flops = sc_flops / 2
         if wl.C:
             C = wl.C
             self.cs = torch.empty((B, KVH, D), dtype=f32, device=dev)
@@ -386,6 +442,12 @@ class PrefillCase:
             self.calls += [Call("value_channel_score", self._vscore, 2 * B * KVH * k * D * 2 + B * wl.H * wl.w * D * 2,
                                 vflops, "tensor"),
                            Call("value_channel_prune", self._vprune, B * KVH * k * D * 2 + B * KVH * k * C * 2)]
+
+    def _compress(self, i):
+        q, K, V = self.reps[i % self.R]
+        _, idx, Ko, Vo = self.outs[i % self.R]
+        self.kvc.kvc_compress_prefill(q, K, V, self.wl.scale, self.k, protect_tail=self.wl.protect_tail,
+                                      reduce=self.wl.reduce, out=(None, idx, Ko, Vo))
 
     def _scores(self, i):
         q, K, V = self.reps[i % self.R]
@@ -417,9 +479,49 @@ class PrefillCase:
 
     def config(self):
         wl = self.wl
-        return {"workload": wl.name, "B": self.B, "H": wl.H, "KVH": self.KVH, "D": self.D, "S": self.S, "w": wl.w,
-                "k": self.k, "C": wl.C or None, "value_channels_pruned": bool(wl.extra.get("values")),
-                "l2": f"inputs rotate over {self.R} replicas ({self.R * self.in_bytes / 2**20:.0f} MiB > L2)"}
+        c = {"workload": wl.name, "B": self.B, "H": wl.H, "KVH": self.KVH, "D": self.D, "S": self.S, "w": wl.w,
+             "k": self.k, "C": wl.C or None, "value_channels_pruned": bool(wl.extra.get("values")),
+             "l2": f"inputs rotate over {self.R} replicas ({self.R * self.in_bytes / 2**20:.0f} MiB > L2)",
+             "inputs_sha256": self.inputs_sha256, "path": "one fused kernel" if self.fused else "library calls"}
+        if self.B > 1 and WORKLOADS[wl.name].B == 1:
+            c["instances"] = self.B
+            c["instances_note"] = (f"the {wl.name} layer (batch 1) stacked as {self.B} independent instances "
+                                   f"in one call: a single instance is too small to load the GPU (its latency "
+                                   f"is reported as single_instance)")
+        return c
+
+    def single_instance(self, steps):
+        """Latency of one instance of the workload (batch 1) through the same call: ``steps``
+        calls captured in a CUDA graph and replayed, CUDA events around the replay."""
+        torch, kvc, wl = self.torch, self.kvc, self.wl
+        q, K, V = (t[:1] for t in self.reps[0])
+        _, idx, Ko, Vo = (None if t is None else t[:1] for t in self.outs[0])
+        sc = self.outs[0][0][:1]
+        ws = self.ws
+
+        def call():
+            kvc.kvc_compress_prefill(q, K, V, wl.scale, self.k, protect_tail=wl.protect_tail, reduce=wl.reduce,
+                                     out=(None if self.fused else sc, idx, Ko, Vo), ws=None if self.fused else ws)
+        for _ in range(3):
+            call()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(steps):
+                    call()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / steps
+        nbytes = self.step_bytes / self.B
+        return {"ms": ms, "tokens_per_s": self.S / (ms / 1e3), "alg_bytes": nbytes,
+                "gbs": nbytes / (ms / 1e3) / 1e9}
 
     def e2e(self, steps, stream, world, dist, dev):
         """Same step through kvc_compress_prefill with pinned host inputs and outputs.  Steps are
@@ -471,7 +573,7 @@ class PrefillCase:
             if used[x]:
                 stream.wait_event(out_done[x])  # its previous results were read back
             kvc.kvc_compress_prefill(dq, dK, hV, wl.scale, k, protect_tail=wl.protect_tail, reduce=wl.reduce,
-                                     out=(sc, idx, Ko, Vo), ws=ws)
+                                     out=(None if self.fused else sc, idx, Ko, Vo), ws=None if self.fused else ws)
             comp_done[x].record(stream)
             s_out.wait_event(comp_done[x])
             with torch.cuda.stream(s_out):
@@ -544,6 +646,7 @@ class TovaDecodeCase:
                               dtype=torch.uint8, device=dev)
         self.B, self.KVH, self.S, self.D = B, KVH, n, D
         self.tokens_per_step = B * n
+        self.inputs_sha256 = _sha256_arrays([self.caches[0][0], self.caches[0][1], self.q, self.kn, self.vn])
         nbytes = B * KVH * n * D * 2 + 2 * B * KVH * D * 2 + 2 * B * KVH * n * 4 + B * H * D * 2
         self.calls = [Call("tova_decode_step", self._step, nbytes, 2.0 * B * H * n * D, "hbm", SCORE_SOURCES,
                            f"tova_decode/{wl.name}")]
@@ -557,7 +660,8 @@ class TovaDecodeCase:
     def config(self):
         wl = self.wl
         return {"workload": wl.name, "B": wl.B, "H": wl.H, "KVH": wl.KVH, "D": wl.D, "slots": self.S,
-                "l2": f"steps rotate over {self.R} caches ({self.R * self.cache_bytes / 2**20:.0f} MiB > L2)"}
+                "l2": f"steps rotate over {self.R} caches ({self.R * self.cache_bytes / 2**20:.0f} MiB > L2)",
+                "inputs_sha256": self.inputs_sha256, "inputs": "drawn on the device (torch.Generator, seeded)"}
 
     def e2e(self, *a):
         return None
@@ -598,6 +702,7 @@ class ScissorhandsCase:
                               dtype=torch.uint8, device=dev)
         self.B, self.H, self.KVH, self.S, self.D = B, H, KVH, cap, D
         self.tokens_per_step = B * cap
+        self.inputs_sha256 = _sha256_arrays([self.reps[0]["K"], self.reps[0]["V"], self.q, self.kn, self.vn])
         rows, slots = B * KVH, B * KVH * cap
         state = 2 * slots * 4 + slots * 4 + 2 * slots * 2 + 2 * slots // 8  # probs, insert steps, counts, flags
         new_rows = 2 * rows * D * 2
@@ -661,7 +766,8 @@ class ScissorhandsCase:
         wl = self.wl
         return {"workload": wl.name, "B": wl.B, "H": wl.H, "KVH": wl.KVH, "D": wl.D, "cap": wl.S,
                 "history": wl.history, "m": wl.m, "policy": wl.policy, "record_every": wl.record_every,
-                "l2": f"steps rotate over {self.R} caches ({self.R * self.cache_bytes / 2**20:.0f} MiB > L2)"}
+                "l2": f"steps rotate over {self.R} caches ({self.R * self.cache_bytes / 2**20:.0f} MiB > L2)",
+                "inputs_sha256": self.inputs_sha256, "inputs": "drawn on the device (torch.Generator, seeded)"}
 
     def e2e(self, *a):
         return None
@@ -697,6 +803,8 @@ class DecodeCase:
         vd = kvc.kv_desc(self.reps[0][1], H)
         self.ws = torch.empty(int(kvc.load_library().kvc_workspace_size(7, vd, 0, 0)), dtype=torch.uint8, device=dev)
         self.tokens_per_step = B * S
+        r0 = self.reps[0]
+        self.inputs_sha256 = _sha256_arrays([t for t in r0 if t is not None] + [self.q])
         nbytes = self.cache_bytes + B * H * D * 2 + B * H * D * 4 + (B * KVH * C * 4 if C < D else 0)
         self.calls = [Call("decode_attention", self._step, nbytes, 2.0 * B * H * S * (C + D), "hbm", DECODE_SOURCES,
                            f"decode_attention/{wl.name}")]
@@ -709,7 +817,8 @@ class DecodeCase:
         wl = self.wl
         return {"workload": wl.name, "B": wl.B, "H": wl.H, "KVH": wl.KVH, "D": wl.D, "kept_tokens": wl.S,
                 "key_channels": wl.C, "l2": f"steps rotate over {self.R} caches "
-                                            f"({self.R * self.cache_bytes / 2**20:.0f} MiB > L2)"}
+                                            f"({self.R * self.cache_bytes / 2**20:.0f} MiB > L2)",
+                "inputs_sha256": self.inputs_sha256, "inputs": "drawn on the device (torch.Generator, seeded)"}
 
     def e2e(self, *a):
         return None
@@ -742,7 +851,8 @@ def run_ours(args):
     kvc.load_library()
     wl = WORKLOADS[args.config]
     peaks = _peaks()
-    case = make_case(wl, dev, rank, args.instances)
+    instances = args.instances if args.instances is not None else DEFAULT_INSTANCES.get(wl.name, 1)
+    case = make_case(wl, dev, rank, instances)
     stream = torch.cuda.current_stream()
     calls = case.calls
 
@@ -873,14 +983,34 @@ def run_ours(args):
                 "peak_source": f"{peaks['source']} HBM copy"}
     roof["traffic"] = _traffic(dom.kernel_key, dom.sources) if dom.kernel_key else None
     roof["algorithmic_bytes_per_launch"] = dom.nbytes
-    roof["algorithmic_flops_per_launch"] = dom.flops
+    if dom.bound == "tensor":
+        # both passes of the two-pass softmax over K (the probabilities never reach memory);
+        # the frac of the one-pass minimum is given beside it
+        roof["executed_flops_per_launch"] = dom.flops
+        if dom.one_pass_flops:
+            roof["one_pass_flops_per_launch"] = dom.one_pass_flops
+            roof["one_pass_frac"] = dom.one_pass_flops / (t_dom / 1e3) / 1e12 / peaks["bf16_tflops"]
+    else:
+        roof["flops_per_launch"] = dom.flops
+
+    # the whole step against the HBM roofline: its algorithmic bytes over the replayed step time
+    step_bytes = getattr(case, "step_bytes", None)
+    if step_bytes is None:
+        step_bytes = sum(c.nbytes * kernels[c.label]["calls"] / args.steps for c in ran_calls)
+    step_gbs = step_bytes / (ms / args.steps / 1e3) / 1e9
+    step_roof = {"bound": "hbm", "bytes_per_step": step_bytes, "ms_per_step": ms / args.steps,
+                 "achieved": step_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": step_gbs / peaks["hbm_gbs"],
+                 "basis": "algorithmic bytes of the whole step / the step time of the CUDA-graph replay"}
+    single = case.single_instance(50) if isinstance(case, PrefillCase) and case.B > 1 and \
+        WORKLOADS[case.wl.name].B == 1 else None
+    if single is not None:
+        single["frac"] = single["gbs"] / peaks["hbm_gbs"]
 
     value = job_throughput(case.tokens_per_step, args.steps, world, ms)
     e2e = case.e2e(max(3, min(args.steps, 20)), stream, world, dist, dev) if not args.no_e2e else None
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and isinstance(case, PrefillCase) \
-            and args.instances <= 1:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and isinstance(case, PrefillCase):
         cpu = cpu_baseline(args.config, budget_s=args.cpu_seconds)
 
     if rank == 0:
@@ -888,7 +1018,8 @@ def run_ours(args):
             "metric": "kv_tokens_scored_compacted_per_s_per_layer", "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": case.config(), "roofline": roof, "kernels": kernels,
+            "data": "synthetic", "config": case.config(), "roofline": roof, "step_roofline": step_roof,
+            "single_instance": single, "kernels": kernels,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks,
             "timing": {"cuda_graph": graph is not None, "host_enqueue_ms": host_ms,
                        "kernels": "separate replay with an event before every call"},
@@ -904,9 +1035,10 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default=SNAPKV_32K.name, choices=sorted(WORKLOADS))
-    ap.add_argument("--instances", type=int, default=1,
-                    help="independent prefill instances batched into one step (e.g. 8192 for TOVA prefill)")
+    ap.add_argument("--config", default=TOVA_PREFILL.name, choices=sorted(WORKLOADS))
+    ap.add_argument("--instances", type=int, default=None,
+                    help="independent prefill instances batched into one step (default: 8192 for TOVA "
+                         "prefill, 1 otherwise)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the timed steps directly (no CUDA graph)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -176,11 +176,21 @@ kvc_status kvc_topk_compact(const float* scores, const kvc_bf16* K, const kvc_bf
                             kvc_bf16* K_out, kvc_bf16* V_out, kvc_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
- * kvc_compress_prefill — window scores, top-k and compaction in one call (the press applied
- * after the prefill attention of one layer; "Add TOVA press" / cold-compress SnapKV).
- *   scores [B,KVH,S] out (kept for inspection), idx [B,KVH,k] out, K_out/V_out [B,KVH,k,D] out.
- *   Causal window; protect_tail as in kvc_topk_select.
- *   ws: kvc_workspace_size(KVC_OP_COMPRESS_PREFILL, kv, w, k).
+ * kvc_compress_prefill — window scores, top-k and compaction in one call: the press applied
+ * after the prefill attention of one layer.  "Add TOVA press" (kvpress PR 12): score the
+ * cached tokens by the last query rows' attention averaged over heads and keep the best;
+ * cold-compress PR 11 (SnapKV paragraph): keep every token of the observation window and
+ * compress the prefix by the window's attention.
+ *   q_win [B,H,w,D] bf16; K/V described by kv (V may be NULL with V_out NULL: keys only; V
+ *   may be mapped page-locked host memory, see kvc_host_device_pointer).
+ *   scores [B,KVH,S] float32 out, or NULL (not written).  idx [B,KVH,k] int32 out, ascending,
+ *   -1 padded when fewer than k tokens exist.  K_out/V_out [B,KVH,k,D] dense bf16 out, zero
+ *   rows where idx is -1.  Causal window; protect_tail as in kvc_topk_select (<= min(k, w)).
+ *   No output may overlap an input or another output.
+ *   Short rows (G*w <= 16, S <= 1024 at D = 64 or S <= 512 at D = 128, k <= S rounded up to a
+ *   multiple of 64; all-heads mode also KVH <= 8) run as one kernel that reads K once and
+ *   needs no workspace.  Otherwise ws: kvc_workspace_size(KVC_OP_COMPRESS_PREFILL, kv, w, k)
+ *   bytes (k must be the call's k), which include room for the scores when scores is NULL.
  * ------------------------------------------------------------------------------------- */
 kvc_status kvc_compress_prefill(const kvc_bf16* q_win, const kvc_bf16* K, const kvc_bf16* V,
                                 const kvc_kv_desc* kv, int32_t w, float scale,

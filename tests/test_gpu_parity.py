@@ -272,6 +272,14 @@ PREFILL_CASES = [
     (1, 32, 8, 128, 2000, 64, 512, 64, "gqa", 0.01),
     (2, 16, 4, 128, 1500, 64, 200, 64, "gqa", 0.01),
     (1, 8, 2, 64, 100, 16, 128, 16, "gqa", 0.0),   # k > S: keep all
+    # short rows: the fused one-kernel path (G*w <= 16, the key block in shared memory)
+    (3, 8, 2, 64, 500, 1, 256, 0, "all_heads", 0.0),     # ragged S, 2-CTA clusters
+    (2, 8, 8, 64, 1000, 2, 300, 2, "gqa", 0.0),          # G 1, 16 key tiles per warp
+    (2, 16, 4, 128, 300, 4, 100, 4, "gqa", 0.01),        # 16 query rows, 128 channels
+    (2, 32, 8, 128, 64, 1, 16, 0, "all_heads", 0.0),     # 8-CTA clusters, one key tile per warp
+    (1, 8, 2, 64, 40, 2, 64, 2, "all_heads", 0.0),       # k > S: all kept, -1 padded, zero rows
+    (1, 4, 4, 64, 1024, 16, 512, 16, "gqa", 0.01),       # w 16, window protected
+    (4, 16, 8, 64, 777, 2, 513, 0, "gqa", 0.0),          # k not a multiple of 64
 ]
 
 
@@ -294,6 +302,91 @@ def test_compress_prefill_parity(B, H, KVH, D, S, w, k, protect, reduce, hh):
     Kr, Vr = O.compact_kv(inp["K"], inp["V"], gi)
     np.testing.assert_array_equal(host_bits(Ko), Kr)
     np.testing.assert_array_equal(host_bits(Vo), Vr)
+
+
+def test_compress_prefill_fused_options():
+    """The short-row kernel: scores left unwritten give the same selection and compaction bit
+    for bit; a strided cache (a view of a longer one) and V in page-locked host memory give
+    the oracle's rows."""
+    B, H, KVH, D, S, w, k = 2, 8, 2, 64, 512, 1, 256
+    wl = _wl(B, H, KVH, D, S, w, seed=57)
+    inp = prefill_inputs(wl)
+    scale = 1.0 / np.sqrt(D)
+    q, K, V = dev_bf16(inp["q"]), dev_bf16(inp["K"]), dev_bf16(inp["V"])
+    sc, idx, Ko, Vo = kvc.kvc_compress_prefill(q, K, V, scale, k, reduce="all_heads")
+    none, idx2, Ko2, Vo2 = kvc.kvc_compress_prefill(q, K, V, scale, k, reduce="all_heads", keep_scores=False)
+    assert none is None
+    assert torch.equal(idx, idx2) and torch.equal(Ko, Ko2) and torch.equal(Vo, Vo2)
+    # a strided cache: rows 0..S-1 of a longer buffer
+    bigK = torch.zeros((B, KVH, S + 37, D), dtype=torch.bfloat16, device="cuda")
+    bigV = torch.zeros_like(bigK)
+    bigK[:, :, :S] = K
+    bigV[:, :, :S] = V
+    sc3, idx3, Ko3, Vo3 = kvc.kvc_compress_prefill(q, bigK[:, :, :S], bigV[:, :, :S], scale, k, reduce="all_heads")
+    assert torch.equal(sc, sc3) and torch.equal(idx, idx3) and torch.equal(Ko, Ko3) and torch.equal(Vo, Vo3)
+    # V read over the host link
+    hV = torch.from_numpy(inp["V"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    _, idx4, Ko4, Vo4 = kvc.kvc_compress_prefill(q, K, hV, scale, k, reduce="all_heads", keep_scores=False)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, idx4) and torch.equal(Ko, Ko4) and torch.equal(Vo, Vo4)
+    ref = O.window_scores(inp["q"], inp["K"], scale, causal=True, reduce="all_heads")
+    assert_scores_close(sc.cpu().numpy(), ref)
+    gi = idx.cpu().numpy()
+    assert_selection_matches(gi, ref, k)
+    Kr, Vr = O.compact_kv(inp["K"], inp["V"], gi)
+    np.testing.assert_array_equal(host_bits(Ko), Kr)
+    np.testing.assert_array_equal(host_bits(Vo), Vr)
+
+
+def test_tova_prefill_8192_instances_sampled():
+    """TOVA prefill (8 query / 2 KV heads, 64 channels, 512 tokens, keep 256) stacked as 8192
+    independent instances in one call: the benchmark's launch configuration.  All instances
+    on the GPU; a seeded sample of 16 by the oracle (scores, kept set, compacted rows); every
+    instance's scores sum to 1 and are identical for both KV heads (mean over all heads)."""
+    from synth import TOVA_PREFILL
+    wl = TOVA_PREFILL.with_(B=8192)
+    inp = prefill_inputs(wl)
+    q, K, V = dev_bf16(inp["q"]), dev_bf16(inp["K"]), dev_bf16(inp["V"])
+    sc, idx, Ko, Vo = kvc.kvc_compress_prefill(q, K, V, wl.scale, wl.k, reduce="all_heads")
+    g_sc = sc.cpu().numpy()
+    np.testing.assert_allclose(g_sc.astype(np.float64).sum(-1), 1.0, rtol=1e-4)
+    assert np.array_equal(g_sc[:, 0], g_sc[:, 1])
+    g_idx = idx.cpu().numpy()
+    assert np.array_equal(g_idx[:, 0], g_idx[:, 1])
+    hK, hV = host_bits(Ko), host_bits(Vo)
+    sample = np.random.Generator(np.random.PCG64([2024])).choice(wl.B, size=16, replace=False)
+    for b in sample:
+        sl = slice(int(b), int(b) + 1)
+        ref = O.window_scores(inp["q"][sl], inp["K"][sl], wl.scale, causal=True, reduce="all_heads")
+        assert_scores_close(g_sc[sl], ref, what=f"instance {b} scores")
+        assert_selection_matches(g_idx[sl], ref, wl.k)
+        rK, rV = O.compact_kv(inp["K"][sl], inp["V"][sl], g_idx[sl])
+        np.testing.assert_array_equal(hK[sl], rK)
+        np.testing.assert_array_equal(hV[sl], rV)
+
+
+def test_snapkv_32k_layer_sampled_kv_head():
+    """The SnapKV 32K layer (32 query / 8 KV heads, 128 channels, window 64, keep 4096, 1 %
+    heavy hitters) at full size through kvc_compress_prefill, the chain the benchmark times:
+    every KV head on the GPU, one by the oracle (scores, kept set with the window, compacted
+    rows); every row's scores sum to the window length."""
+    from synth import SNAPKV_32K
+    wl = SNAPKV_32K
+    inp = prefill_inputs(wl)
+    G, scale = wl.G, wl.scale
+    q, K, V = dev_bf16(inp["q"]), dev_bf16(inp["K"]), dev_bf16(inp["V"])
+    sc, idx, Ko, Vo = kvc.kvc_compress_prefill(q, K, V, scale, wl.k, protect_tail=wl.protect_tail, reduce="gqa")
+    np.testing.assert_allclose(sc.double().sum(-1).cpu().numpy(), wl.w, rtol=1e-4)
+    kv = 5
+    qh, Kh, Vh = inp["q"][:, kv * G:(kv + 1) * G], inp["K"][:, kv:kv + 1], inp["V"][:, kv:kv + 1]
+    ref = O.window_scores(qh, Kh, scale, causal=True, reduce="gqa")
+    assert_scores_close(sc.cpu().numpy()[:, kv:kv + 1], ref)
+    g_idx = idx.cpu().numpy()[:, kv:kv + 1]
+    assert_selection_matches(g_idx, ref, wl.k, protect_tail=wl.protect_tail)
+    assert set(range(wl.S - wl.w, wl.S)) <= set(g_idx[0, 0].tolist())
+    rK, rV = O.compact_kv(Kh, Vh, g_idx)
+    np.testing.assert_array_equal(host_bits(Ko)[:, kv:kv + 1], rK)
+    np.testing.assert_array_equal(host_bits(Vo)[:, kv:kv + 1], rV)
 
 
 # ----------------------------------------------------------------------------------------
