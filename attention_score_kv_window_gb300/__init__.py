@@ -13,7 +13,7 @@ from ._binding import (  # noqa: F401
     kvc_scissorhands_update_from_probs, kvc_scissorhands_evict, kvc_scissorhands_refill_queue,
     kvc_scissorhands_insert, kvc_channel_score, kvc_channel_prune, kvc_decode_attention, kvc_zero_add_back,
     kvc_value_channel_score,
-    kvc_get_device_status, kvc_status_string, kvc_version, kvc_launch_count,
+    kvc_get_device_status, kvc_status_string, kvc_version, kvc_launch_count, kvc_debug_inject_timeout,
     KVC_OK, KVC_ERR_INVALID_ARG, KVC_ERR_UNSUPPORTED, KVC_ERR_CUDA, KVC_ERR_TIMEOUT,
     KVC_ERR_DEVICE_BOUNDS, KVC_ERR_WORKSPACE,
 )

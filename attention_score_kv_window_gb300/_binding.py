@@ -83,6 +83,7 @@ _SIGNATURES = {
     "kvc_last_error_message": (ctypes.c_char_p, []),
     "kvc_version": (_I32, []),
     "kvc_launch_count": (_I64, []),
+    "kvc_debug_inject_timeout": (_I32, [_I32]),
 }
 
 
@@ -473,6 +474,12 @@ def kvc_status_string(s: int) -> str:
 
 def kvc_version() -> int:
     return int(load_library().kvc_version())
+
+
+def kvc_debug_inject_timeout(armed: bool = True) -> None:
+    """Test hook: the next fused tensor-core scoring launch waits at most 1 ms and leaves out
+    one CTA's key-range arrival, so it times out (see include/kvc.h); False disarms it."""
+    _check(load_library().kvc_debug_inject_timeout(int(bool(armed))))
 
 
 def kvc_launch_count() -> int:

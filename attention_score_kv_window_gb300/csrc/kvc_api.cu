@@ -160,6 +160,11 @@ int32_t kvc_version(void) { return 10000; }
 
 int64_t kvc_launch_count(void) { return (int64_t)g_launches.load(std::memory_order_relaxed); }
 
+kvc_status kvc_debug_inject_timeout(int32_t armed) {
+  inject_scores_timeout(armed);
+  return KVC_OK;
+}
+
 const char* kvc_status_string(kvc_status s) {
   switch (s) {
     case KVC_OK: return "ok";
@@ -660,8 +665,9 @@ kvc_status kvc_host_device_pointer(const void* host_ptr, void** dev_ptr) {
 kvc_status kvc_get_device_status(kvc_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "kvc_get_device_status sync");
-  cudaError_t (*takers[])(unsigned int*) = {take_status_scores, take_status_select, take_status_gather,
-                                            take_status_scissorhands, take_status_decode};
+  cudaError_t (*takers[])(unsigned int*) = {take_status_scores,       take_status_scores_tc, take_status_select,
+                                            take_status_gather,       take_status_scissorhands, take_status_decode,
+                                            take_status_prefill};
   unsigned int first = 0u;
   for (auto fn : takers) {
     unsigned int v = 0u;

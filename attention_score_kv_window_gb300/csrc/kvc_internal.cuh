@@ -31,6 +31,8 @@ cudaError_t take_status_scores(unsigned int* v);
 cudaError_t take_status_select(unsigned int* v);
 cudaError_t take_status_gather(unsigned int* v);
 cudaError_t take_status_scissorhands(unsigned int* v);
+cudaError_t take_status_scores_tc(unsigned int* v);
+cudaError_t take_status_prefill(unsigned int* v);
 
 // Programmatic dependent launch.  Kernels launched with pdl_config() may start before the
 // previous kernel on the stream has finished; each such kernel calls pdl_wait() before its
@@ -109,6 +111,8 @@ struct ScoresArgs {
   float* out;    // [B*KVH][S]
   float out_mul; // 1/G
   unsigned long long* sync;  // fused tensor-core kernel: epoch word + one tag per CTA (may be null)
+  unsigned long long wait_ns;  // tensor-core kernel: bound on any single wait (2 s)
+  int64_t withhold;            // fused tensor-core kernel: CTA whose key-range arrival a test leaves out (-1)
   // Decode step with the new token written on the fly (small-row kernel only; wslot null
   // otherwise): slot wslot[b*KVH+kvh] holds the new key knew[b*KVH+kvh] (its stale cache row
   // is never read), and the CTA whose slice holds it stores knew / vnew into Kw / Vw there.
@@ -170,6 +174,8 @@ __host__ __device__ __forceinline__ void key_range(const ScoresArgs& a, int spli
 // fit it; launch_scores_tc() runs both passes, fused in one cooperative launch when a.sync is
 // set and the grid fits on the GPU at once, else as two launches.
 bool tc_supported(const ScoresArgs& a, int D);
+// kvc_debug_inject_timeout: arm (1) or disarm (0) the timeout test of the next fused launch
+void inject_scores_timeout(int armed);
 cudaError_t launch_scores_tc(const ScoresArgs& a, int D, cudaStream_t st);
 
 struct ScoresPlan {

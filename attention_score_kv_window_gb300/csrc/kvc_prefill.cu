@@ -574,4 +574,6 @@ cudaError_t launch_prefill_fused(const uint16_t* q, const uint16_t* K, const uin
   }
 }
 
+KVC_TU_STATUS(prefill)
+
 }  // namespace kvc

@@ -967,6 +967,8 @@ ScoresArgs make_args(const uint16_t* q, const uint16_t* K, const kvc_kv_desc& kv
   a.sync = reinterpret_cast<unsigned long long*>(base + p.part_bytes);
   a.out = reduce == KVC_REDUCE_ALL_HEADS ? reinterpret_cast<float*>(base + p.part_bytes + p.sync_bytes) : scores;
   a.out_mul = 1.f / (float)a.G;
+  a.wait_ns = 2000000000ull;
+  a.withhold = -1;
   return a;
 }
 }  // namespace

@@ -26,6 +26,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "kvc_internal.cuh"
@@ -41,7 +42,7 @@ constexpr int MMA_WARP = 17;
 constexpr int THREADS = 576;
 constexpr int QROWS_MAX = 256;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s bound on any single wait
+// Every wait is bounded by ScoresArgs::wait_ns (2 s; 1 ms under kvc_debug_inject_timeout).
 constexpr int KSLOTS = 4;           // pass-2 key-sum exchange slots per group and quadrant
 // K ring full/empty, two accumulator full/empty pairs, query group, key-sum slots per quadrant
 constexpr int NBARS = 2 * STAGES + 5 + 2 * 4 * KSLOTS;
@@ -104,15 +105,15 @@ __device__ __forceinline__ uint64_t gtimer() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Bounded wait for the phase with the given parity.  false: timed out (the abort flag is
-// raised and KVC_ERR_TIMEOUT recorded) or another role already aborted.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+// Bounded wait (limit ns) for the phase with the given parity.  false: timed out (the abort
+// flag is raised and KVC_ERR_TIMEOUT recorded) or another role already aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint64_t limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = gtimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (gtimer() - t0 > WAIT_NS) {
+    if (gtimer() - t0 > limit) {
       *abort_flag = 1;
       set_device_status(KVC_ERR_TIMEOUT);
       return false;
@@ -120,10 +121,10 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 // same, ignoring the abort flag (used only to drain copies already in flight at teardown)
-__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity, uint64_t limit) {
   const uint64_t t0 = gtimer();
   while (!mbar_try_wait(bar, parity)) {
-    if (gtimer() - t0 > WAIT_NS) return;
+    if (gtimer() - t0 > limit) return;
   }
 }
 
@@ -262,6 +263,7 @@ struct Ctx {
   uint32_t sbase;
   volatile int* abort_flag;
   uint32_t tmem;
+  uint64_t wait_ns;  // bound on any single wait
   __device__ uint32_t full(int s) const { return sbase + BARS_OFF + 8 * s; }
   __device__ uint32_t empty(int s) const { return sbase + BARS_OFF + 8 * (STAGES + s); }
   __device__ uint32_t tfull(int b) const { return sbase + BARS_OFF + 8 * (2 * STAGES + b); }
@@ -336,7 +338,7 @@ __device__ __forceinline__ void producer(const Ctx& c, const ScoresArgs& a, cons
   for (int it = 0; it < total; ++it) {
     const int s = it % STAGES;
     const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
-    if (!wait_bar(c.empty(s), ph ^ 1u, c.abort_flag)) break;
+    if (!wait_bar(c.empty(s), ph ^ 1u, c.abort_flag, c.wait_ns)) break;
     mbar_expect_tx(c.full(s), L::STAGE);
     const int y = (int)(kbeg + (int64_t)(it < ntiles ? it : it - ntiles) * TILE);
     for (int p = 0; p < L::NP; ++p)
@@ -345,9 +347,9 @@ __device__ __forceinline__ void producer(const Ctx& c, const ScoresArgs& a, cons
   }
   // copies still in flight when the kernel stops early are waited for (bounded) before exit
   if (*c.abort_flag) {
-    drain_bar(c.qfull(), 0);
+    drain_bar(c.qfull(), 0, c.wait_ns);
     for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
-      drain_bar(c.full(it % STAGES), (uint32_t)(it / STAGES) & 1u);
+      drain_bar(c.full(it % STAGES), (uint32_t)(it / STAGES) & 1u, c.wait_ns);
   }
 }
 
@@ -448,7 +450,7 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 // One warp waits (bounded) until words [0, n) of `w` all equal `tag`.  With a non-null
 // abort flag the wait also ends when another role of the CTA has given up.
 __device__ __forceinline__ bool warp_wait_tags(const unsigned long long* w, int64_t n, uint64_t tag,
-                                               volatile int* abort_flag) {
+                                               volatile int* abort_flag, uint64_t limit) {
   const int lane = threadIdx.x & 31;
   bool ok = true;
   const uint64_t t0 = gtimer();
@@ -458,7 +460,7 @@ __device__ __forceinline__ bool warp_wait_tags(const unsigned long long* w, int6
         ok = false;
         break;
       }
-      if (gtimer() - t0 > WAIT_NS) {
+      if (gtimer() - t0 > limit) {
         if (abort_flag != nullptr) *abort_flag = 1;
         set_device_status(KVC_ERR_TIMEOUT);
         ok = false;
@@ -572,7 +574,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int NC1 = NHALF == 2 ? TILE : TILE / 2;  // pass 1: key columns per warp and tile
   constexpr int NW = N2 / 2;                     // pass 2: query-row columns per warp and tile
   extern __shared__ unsigned char smem_raw[];
-  const Ctx c = prologue<D>(smem_raw);  // shared memory and TMEM only
+  Ctx cx = prologue<D>(smem_raw);  // shared memory and TMEM only
+  cx.wait_ns = a.wait_ns;
+  const Ctx& c = cx;
   pdl_wait();  // previous kernel on the stream complete and visible
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -586,14 +590,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == PRODUCER_WARP) {
     if (lane == 0) producer<D>(c, a, &tmK, &tmQ, QROWS, kvh, b, kbeg, ntiles, total);
   } else if (warp == MMA_WARP) {
-    if (lane == 0 && wait_bar(c.qfull(), 0, c.abort_flag)) {
+    if (lane == 0 && wait_bar(c.qfull(), 0, c.abort_flag, c.wait_ns)) {
       int done = 0;
       // Tile it+1's barriers are tested (without blocking) between the two halves of tile
       // it's MMAs; only if they were not yet complete does the thread wait after the commits.
       // Either way no MMA of tile it waits on the epilogue.
       auto ready = [&](int t) -> bool {
-        return wait_bar(c.tempty(t & 1), ((uint32_t)(t >> 1) & 1u) ^ 1u, c.abort_flag) &&
-               wait_bar(c.full(t % STAGES), (uint32_t)(t / STAGES) & 1u, c.abort_flag);
+        return wait_bar(c.tempty(t & 1), ((uint32_t)(t >> 1) & 1u) ^ 1u, c.abort_flag, c.wait_ns) &&
+               wait_bar(c.full(t % STAGES), (uint32_t)(t / STAGES) & 1u, c.abort_flag, c.wait_ns);
       };
       auto ready_now = [&](int t) -> bool {
         return mbar_test(c.tempty(t & 1), ((uint32_t)(t >> 1) & 1u) ^ 1u) &&
@@ -637,7 +641,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (it + 1 < total && !next_ready) ok = ready(it + 1);
       }
       // stopped early: let the MMAs already issued finish before TMEM is released
-      if (*c.abort_flag && done > 0) drain_bar(c.tfull((done - 1) & 1), (uint32_t)((done - 1) >> 1) & 1u);
+      if (*c.abort_flag && done > 0)
+        drain_bar(c.tfull((done - 1) & 1), (uint32_t)((done - 1) >> 1) & 1u, c.wait_ns);
     }
     __syncwarp();
   } else {
@@ -661,7 +666,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       float v[32];
       for (int it = g; it < n1; it += 2) {
         const uint32_t bph = (uint32_t)(it >> 1) & 1u;
-        if (!wait_bar(c.tfull(g), bph, c.abort_flag)) break;
+        if (!wait_bar(c.tfull(g), bph, c.abort_flag, c.wait_ns)) break;
         tc_fence_after();
         const uint32_t taddr = c.tmem + ((uint32_t)(qd * 32) << 16) + g * 256 + h * 128 + c0;
 #pragma unroll
@@ -719,12 +724,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (warp == 0) {
         unsigned long long* tags = a.sync + 1 + (int64_t)bk * a.nsplit;
         const uint64_t tag = epoch_tag(epoch + 1);
-        if (lane == 0) {
+        // (a.withhold: a test of the timeout path names one CTA whose arrival is left out)
+        if (lane == 0 && (int64_t)bk * a.nsplit + split != a.withhold) {
           fence_acq_rel_gpu();  // release: the CTA's partials (ordered by the barrier above)
           st_relaxed_u64(tags + split, tag);
         }
         __syncwarp();
-        warp_wait_tags(tags, a.nsplit, tag, c.abort_flag);
+        warp_wait_tags(tags, a.nsplit, tag, c.abort_flag, c.wait_ns);
       }
       named_sync_epilogue();
       pdl_trigger();  // the next kernel may begin launching; it waits for this grid's end
@@ -746,7 +752,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int64_t kt0 = kbeg + (int64_t)(it - n1) * TILE;
         const int64_t j = kt0 + kr;
         float acc = 0.f;
-        if (!dead && wait_bar(c.tfull(g), (uint32_t)(it >> 1) & 1u, c.abort_flag)) {
+        if (!dead && wait_bar(c.tfull(g), (uint32_t)(it >> 1) & 1u, c.abort_flag, c.wait_ns)) {
           tc_fence_after();
           const uint32_t taddr = c.tmem + ((uint32_t)(qd * 32) << 16) + g * 256 + hf * NW;
           const bool clean = (kt0 + TILE <= kend) && (!a.causal || kt0 + TILE - 1 <= a.S - a.w);
@@ -765,7 +771,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (hf != 0) {
           *ks = acc;
           mbar_arrive(kb);
-        } else if (wait_bar(kb, (uint32_t)(u / KSLOTS) & 1u, c.abort_flag) && !dead && j < kend) {
+        } else if (wait_bar(kb, (uint32_t)(u / KSLOTS) & 1u, c.abort_flag, c.wait_ns) && !dead && j < kend) {
           out[j] = (acc + *ks) * a.out_mul;
         }
       }
@@ -773,7 +779,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if constexpr (MODE == 3) {
       // CTA 0 advances the epoch once every CTA has published (so has read the epoch)
       if (warp == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
-        warp_wait_tags(a.sync + 1, (int64_t)a.B * a.KVH * a.nsplit, epoch_tag(epoch + 1), nullptr);
+        warp_wait_tags(a.sync + 1, (int64_t)a.B * a.KVH * a.nsplit, epoch_tag(epoch + 1), nullptr, c.wait_ns);
         if (lane == 0) st_relaxed_u64(a.sync, epoch + 1);
       }
     }
@@ -860,9 +866,18 @@ const TcMaps* tc_maps(const ScoresArgs& a, int D) {
   return e.ok ? &e.maps : nullptr;
 }
 
+// Armed by kvc_debug_inject_timeout: the next fused launch waits at most 1 ms and leaves out
+// the key-range arrival of its first CTA, so its other CTAs time out (a test of that path).
+std::atomic<int> g_inject_timeout{0};
+
 // one launch of the scoring kernel in the given mode; the fused mode is cooperative
 template <int D, int NHALF, int NQ, int MODE>
-cudaError_t run_tc(const ScoresArgs& a, cudaStream_t st) {
+cudaError_t run_tc(const ScoresArgs& a_in, cudaStream_t st) {
+  ScoresArgs a = a_in;
+  if (MODE == 3 && g_inject_timeout.exchange(0) != 0) {
+    a.wait_ns = 1000000ull;
+    a.withhold = 0;
+  }
   const TcMaps* m = tc_maps(a, D);
   if (!m) return cudaErrorInvalidValue;
   auto kern = k_scores_tc<D, NHALF, NQ, MODE>;
@@ -947,8 +962,12 @@ bool tc_supported(const ScoresArgs& a, int D) {
   return tc_maps(a, D) != nullptr;
 }
 
+void inject_scores_timeout(int armed) { g_inject_timeout.store(armed ? 1 : 0); }
+
 cudaError_t launch_scores_tc(const ScoresArgs& a, int D, cudaStream_t st) {
   return D == 64 ? run_scores_d<64>(a, st) : run_scores_d<128>(a, st);
 }
+
+KVC_TU_STATUS(scores_tc)
 
 }  // namespace kvc

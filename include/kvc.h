@@ -398,6 +398,16 @@ int32_t kvc_version(void);
  * threads, all devices).  The difference over a region counts the region's launches. */
 int64_t kvc_launch_count(void);
 
+/* Diagnostics: a test of the bounded-wait path.  armed = 1: the next fused tensor-core window
+ * scoring launch in this process (kvc_window_scores and the calls built on it, for shapes
+ * with more than 32 query rows per KV head whose CTAs are all resident at once) bounds each
+ * wait by 1 ms instead of 2 s and leaves out the key-range arrival of its first CTA.  The
+ * other CTAs of that (b, kvh) give up their wait, the launch still returns (its scores for
+ * that (b, kvh) are then undefined), and kvc_get_device_status reports KVC_ERR_TIMEOUT.  The
+ * device stays usable: the next call computes normally.  armed = 0 disarms it if no such
+ * launch came.  Never needed outside tests. */
+kvc_status kvc_debug_inject_timeout(int32_t armed);
+
 #ifdef __cplusplus
 }
 #endif
