@@ -121,12 +121,18 @@ kvc_status kvc_window_scores(const kvc_bf16* q_win, const kvc_bf16* K, const kvc
  *  - Shapes whose scratch (kvc_workspace_size(KVC_OP_WINDOW_SCORES, ...) for this reduce
  *    mode) exceeds the fixed size are rejected with KVC_ERR_UNSUPPORTED; nothing is launched.
  *  - The first call on a device looks up the array's device address (once, with that device
- *    current); make that first call before any stream capture on the device.
+ *    current); make that first call before any stream capture on the device.  The address is
+ *    kept per device ordinal for the life of the process: it belongs to the device's primary
+ *    context, so do not call this after cudaDeviceReset on that device, or with another
+ *    context made current through the driver API.
  *  - All calls on a device share the one array, and it keeps the last call's contents.
- *    Every scratch element a call reads is written earlier in the same call, so nothing has
- *    to be cleared; but two calls that overlap on the GPU (different streams, or different
- *    host threads without ordering) race on the array and corrupt each other's results.
- *    Serialise them on one stream.
+ *    Nothing has to be cleared between calls: the (max, sum) partials a call reads are
+ *    written earlier in the same call, and the cross-CTA bookkeeping words of the fused
+ *    tensor-core launch accept any prior content (each launch advances an epoch word and
+ *    tags every arrival with a hash of that epoch, so words left by an earlier call, of any
+ *    shape, are never mistaken for this call's arrivals).  But two calls that overlap on the
+ *    GPU (different streams, or different host threads without ordering) race on the array
+ *    and corrupt each other's results.  Serialise them on one stream.
  *  - Calls no cudaMalloc, cudaFree or other allocating routine.
  * ------------------------------------------------------------------------------------- */
 #define KVC_NOALLOC_SCRATCH_BYTES (4u << 20)
@@ -151,7 +157,10 @@ kvc_status kvc_topk_select(const float* scores, int32_t B, int32_t KVH, int64_t 
                            int32_t* idx, void* ws, size_t ws_bytes, kvc_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
- * kvc_compact_kv — gather the kept rows into a dense cache:
+ * kvc_compact_kv — gather the kept rows into a dense cache.  "Add TOVA press" (SimJeg's
+ * reply): the press runs after the layer's forward pass and only rewrites its KV cache, which
+ * then stays compressed (hassidm's reply); cold-compress PR 11 (SnapKV paragraph): the cache
+ * receives the kept tokens only.  The compressed cache is therefore the kept rows, in order:
  *   K_out[b,kvh,t,:] = K[b,kvh,idx[b,kvh,t],:], same for V; idx -1 writes a zero row.
  *   idx [B,KVH,k] int32 in [-1, S); K_out, V_out [B,KVH,k,D] dense bf16 out.
  *   V and V_out may both be NULL (keys only).  Outputs must not overlap inputs.  V may be
@@ -165,7 +174,10 @@ kvc_status kvc_compact_kv(const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_des
 
 /* ---------------------------------------------------------------------------------------
  * kvc_topk_compact — kvc_topk_select followed by kvc_compact_kv of the chosen rows, in one
- * call (two kernels; the gather starts as the selection ends).
+ * call (two kernels; the gather starts as the selection ends): choosing the tokens a press
+ * keeps per KV head and rewriting the cache to them ("Add TOVA press": the scores are repeated
+ * over the KV heads and each head's cache keeps its best tokens; cold-compress PR 11: SnapKV
+ * keeps the observation window and compresses the prefix).
  *   Arguments as in those two calls: scores [B,KVH,S] float32; K/V described by kv (V may be
  *   NULL, then V_out too); idx [B,KVH,k] int32 out; K_out/V_out [B,KVH,k,D] dense bf16 out,
  *   zero rows where idx is -1.  No output may overlap scores, K, V or another output.
@@ -199,7 +211,11 @@ kvc_status kvc_compress_prefill(const kvc_bf16* q_win, const kvc_bf16* K, const 
                                 void* ws, size_t ws_bytes, kvc_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
- * kvc_write_slots — K[b,kvh,slot[b,kvh],:] = k_new[b,kvh,:] (same for V; V pair may be NULL).
+ * kvc_write_slots — the decode-step insertion into a fixed-size cache: the new token's key and
+ * value rows go into the slot an eviction freed (cold-compress PR 11 description: the eviction
+ * queue evicts one token at each step, so every new token takes an evicted token's slot and no
+ * slot stays empty; a TOVA decode step evicts the lowest-scoring token the same way).
+ *   K[b,kvh,slot[b,kvh],:] = k_new[b,kvh,:] (same for V; V pair may be NULL).
  *   k_new, v_new [B,KVH,D] bf16; slot [B,KVH] int32 in [0, S).  K/V are updated in place.
  * ------------------------------------------------------------------------------------- */
 kvc_status kvc_write_slots(const kvc_bf16* k_new, const kvc_bf16* v_new, const int32_t* slot,

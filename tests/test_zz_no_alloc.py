@@ -42,6 +42,26 @@ def test_noalloc_matches_workspace_call_twice(B, H, KVH, D, S, w, causal, reduce
     assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
 
+def test_noalloc_alternating_shapes_share_the_array():
+    """Calls of different shapes in turn (A, B, A): each call finds the array as the other
+    shape left it (the fused tensor-core launch's bookkeeping words at other offsets) and
+    must still match the workspace call."""
+    runs = []
+    for B, H, KVH, D, S, w, causal, reduce in CASES:
+        wl = Workload("t", B=B, H=H, KVH=KVH, D=D, S=S, w=w, k=1, reduce=reduce, seed=S + 1)
+        inp = prefill_inputs(wl)
+        q, K = dev_bf16(inp["q"]), dev_bf16(inp["K"])
+        ref = kvc.kvc_window_scores(q, K, wl.scale, causal=causal, reduce=reduce).cpu().numpy()
+        runs.append((q, K, wl.scale, causal, reduce, ref))
+    for i in (0, 1, 0, 1):
+        q, K, scale, causal, reduce, ref = runs[i]
+        out = torch.full(ref.shape, -1.0, dtype=torch.float32, device="cuda")
+        kvc.kvc_window_scores_noalloc(q, K, scale, causal=causal, reduce=reduce, scores=out)
+        torch.cuda.synchronize()
+        assert_scores_close(out.cpu().numpy(), ref)
+    assert kvc.kvc_get_device_status() == kvc.KVC_OK
+
+
 def test_noalloc_rejects_shapes_beyond_the_fixed_scratch():
     # 64 batch rows x 8 KV heads x 32768 slots of all-heads partial scores need 64 MiB > 4 MiB
     # (one batch row broadcast with stride 0: the check is on the host, nothing is read)
