@@ -18,7 +18,7 @@ OUT_DIR = os.path.join(PKG, "_lib")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libkvc.so"
 SOURCES = ["kvc_api.cu", "kvc_scores.cu", "kvc_scores_tc.cu", "kvc_select.cu", "kvc_gather.cu",
-           "kvc_scissorhands.cu", "kvc_decode.cu", "kvc_prefill.cu"]
+           "kvc_scissorhands.cu", "kvc_decode.cu", "kvc_prefill.cu", "kvc_scores_stream.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

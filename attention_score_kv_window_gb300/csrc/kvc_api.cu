@@ -667,7 +667,7 @@ kvc_status kvc_get_device_status(kvc_stream_t stream) {
   if (e != cudaSuccess) return cuda_status(e, "kvc_get_device_status sync");
   cudaError_t (*takers[])(unsigned int*) = {take_status_scores,       take_status_scores_tc, take_status_select,
                                             take_status_gather,       take_status_scissorhands, take_status_decode,
-                                            take_status_prefill};
+                                            take_status_prefill,      take_status_scores_stream};
   unsigned int first = 0u;
   for (auto fn : takers) {
     unsigned int v = 0u;

@@ -1,5 +1,6 @@
 // Internal declarations shared by the libkvc translation units (not part of the ABI).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,6 +34,7 @@ cudaError_t take_status_gather(unsigned int* v);
 cudaError_t take_status_scissorhands(unsigned int* v);
 cudaError_t take_status_scores_tc(unsigned int* v);
 cudaError_t take_status_prefill(unsigned int* v);
+cudaError_t take_status_scores_stream(unsigned int* v);
 
 // Programmatic dependent launch.  Kernels launched with pdl_config() may start before the
 // previous kernel on the stream has finished; each such kernel calls pdl_wait() before its
@@ -176,6 +178,10 @@ __host__ __device__ __forceinline__ void key_range(const ScoresArgs& a, int spli
 bool tc_supported(const ScoresArgs& a, int D);
 // kvc_debug_inject_timeout: arm (1) or disarm (0) the timeout test of the next fused launch
 void inject_scores_timeout(int armed);
+// TMA map of a [B, KVH, S, D] bf16 cache: boxes of 64 channels x 128 rows, 128-byte swizzle
+// (row r's 16-byte chunk c of a 64-channel panel lands at chunk c ^ (r & 7)); false when the
+// strides cannot be described
+bool make_cache_tensor_map(const uint16_t* K, const kvc_kv_desc& kv, CUtensorMap* tm);
 cudaError_t launch_scores_tc(const ScoresArgs& a, int D, cudaStream_t st);
 
 struct ScoresPlan {
@@ -201,6 +207,17 @@ cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc
 cudaError_t launch_tova_decode(const uint16_t* q, const uint16_t* knew, const uint16_t* vnew, uint16_t* K, uint16_t* V,
                                const kvc_kv_desc& kv, float scale, int32_t* free_slot, float* scores, void* ws,
                                cudaStream_t st);
+// TMA-streamed decode-step scoring (kvc_scores_stream.cu), one launch each; the new token's
+// rows are written into its slot (free_slot / the Scissorhands slot search) on the way.
+// cudaErrorNotSupported when the shapes do not fit (more than 8 query rows per KV head,
+// head_dim not 64/128, a slice's logits beyond shared memory, strides a tensor map cannot
+// describe).  group_scores: [B*KVH][S] group-mean probabilities.
+cudaError_t launch_decode_scores_stream(const uint16_t* q, const uint16_t* knew, const uint16_t* vnew, uint16_t* K,
+                                        uint16_t* V, const kvc_kv_desc& kv, float scale, const int32_t* free_slot,
+                                        float* group_scores, cudaStream_t st);
+cudaError_t launch_sh_update_stream(const kvc_sh_state& sh, const int32_t* queue, int qm, int qpos, const uint16_t* q,
+                                    const uint16_t* knew, const uint16_t* vnew, uint16_t* K, uint16_t* V,
+                                    const kvc_kv_desc& kv, float scale, float* probs, cudaStream_t st);
 // One Scissorhands decode step (insert, score, record) as one small-row kernel launch;
 // cudaErrorNotSupported when the shapes need another scoring kernel.
 cudaError_t launch_sh_update_fused(const kvc_sh_state& s, const int32_t* queue, int qm, int qpos, const uint16_t* q,

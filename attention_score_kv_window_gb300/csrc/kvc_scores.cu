@@ -984,6 +984,10 @@ cudaError_t launch_window_scores(const uint16_t* q, const uint16_t* K, const kvc
 cudaError_t launch_sh_update_fused(const kvc_sh_state& sh, const int32_t* queue, int qm, int qpos, const uint16_t* q,
                                    const uint16_t* knew, const uint16_t* vnew, uint16_t* K, uint16_t* V,
                                    const kvc_kv_desc& kv, float scale, float* probs, void* ws, cudaStream_t st) {
+  {
+    const cudaError_t es = launch_sh_update_stream(sh, queue, qm, qpos, q, knew, vnew, K, V, kv, scale, probs, st);
+    if (es != cudaErrorNotSupported) return es;
+  }
   ScoresArgs a = make_args(q, K, kv, 1, scale, 0, sh.live, KVC_REDUCE_GQA_GROUP, probs, ws, 1);
   int64_t per = 0;
   cudaError_t e0 = kv.D == 64 ? set_smem_attrs<64>() : set_smem_attrs<128>();
@@ -1007,19 +1011,21 @@ cudaError_t launch_tova_decode(const uint16_t* q, const uint16_t* knew, const ui
                                const kvc_kv_desc& kv, float scale, int32_t* free_slot, float* scores, void* ws,
                                cudaStream_t st) {
   ScoresArgs a = make_args(q, K, kv, 1, scale, 0, nullptr, KVC_REDUCE_ALL_HEADS, scores, ws, 1);
-  int64_t per = 0;
-  cudaError_t e0 = kv.D == 64 ? set_smem_attrs<64>() : set_smem_attrs<128>();
-  if (e0 != cudaSuccess) return e0;
-  const int cs = kv.D == 64 ? small_cluster<64>(a, &per) : small_cluster<128>(a, &per);
-  if (cs == 0) return cudaErrorNotSupported;
-  a.wslot = free_slot;
-  a.knew = knew;
-  a.vnew = vnew;
-  a.Kw = K;
-  a.Vw = V;
-  cudaError_t e = kv.D == 64 ? set_smem_attrs<64>() : set_smem_attrs<128>();
-  if (e != cudaSuccess) return e;
-  e = kv.D == 64 ? launch_small<64>(a, cs, per, st) : launch_small<128>(a, cs, per, st);
+  // group-mean scores into the workspace: the TMA-streamed kernel, else the small-row kernel
+  cudaError_t e = launch_decode_scores_stream(q, knew, vnew, K, V, kv, scale, free_slot, a.out, st);
+  if (e == cudaErrorNotSupported) {
+    int64_t per = 0;
+    e = kv.D == 64 ? set_smem_attrs<64>() : set_smem_attrs<128>();
+    if (e != cudaSuccess) return e;
+    const int cs = kv.D == 64 ? small_cluster<64>(a, &per) : small_cluster<128>(a, &per);
+    if (cs == 0) return cudaErrorNotSupported;
+    a.wslot = free_slot;
+    a.knew = knew;
+    a.vnew = vnew;
+    a.Kw = K;
+    a.Vw = V;
+    e = kv.D == 64 ? launch_small<64>(a, cs, per, st) : launch_small<128>(a, cs, per, st);
+  }
   if (e != cudaSuccess) return e;
   const int ecs = EVICT_CLUSTER;
   const int64_t eper = (kv.S + ecs - 1) / ecs;

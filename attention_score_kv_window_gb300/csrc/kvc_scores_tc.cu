@@ -964,6 +964,18 @@ bool tc_supported(const ScoresArgs& a, int D) {
 
 void inject_scores_timeout(int armed) { g_inject_timeout.store(armed ? 1 : 0); }
 
+bool make_cache_tensor_map(const uint16_t* K, const kvc_kv_desc& kv, CUtensorMap* tm) {
+  ScoresArgs a{};
+  a.K = K;
+  a.S = kv.S;
+  a.ss = kv.stride_s;
+  a.sh = kv.stride_h;
+  a.sb = kv.stride_b;
+  a.B = kv.B;
+  a.KVH = kv.KVH;
+  return make_k_map(a, kv.D, tm);
+}
+
 cudaError_t launch_scores_tc(const ScoresArgs& a, int D, cudaStream_t st) {
   return D == 64 ? run_scores_d<64>(a, st) : run_scores_d<128>(a, st);
 }
