@@ -178,10 +178,10 @@ __host__ __device__ __forceinline__ void key_range(const ScoresArgs& a, int spli
 bool tc_supported(const ScoresArgs& a, int D);
 // kvc_debug_inject_timeout: arm (1) or disarm (0) the timeout test of the next fused launch
 void inject_scores_timeout(int armed);
-// TMA map of a [B, KVH, S, D] bf16 cache: boxes of 64 channels x 128 rows, 128-byte swizzle
-// (row r's 16-byte chunk c of a 64-channel panel lands at chunk c ^ (r & 7)); false when the
-// strides cannot be described
-bool make_cache_tensor_map(const uint16_t* K, const kvc_kv_desc& kv, CUtensorMap* tm);
+// TMA map of a [B, KVH, S, D] bf16 cache: boxes of 64 channels x box_rows rows (<= 256),
+// 128-byte swizzle (row r's 16-byte chunk c of a 64-channel panel lands at chunk c ^ (r & 7));
+// false when the strides cannot be described
+bool make_cache_tensor_map(const uint16_t* K, const kvc_kv_desc& kv, CUtensorMap* tm, int box_rows);
 cudaError_t launch_scores_tc(const ScoresArgs& a, int D, cudaStream_t st);
 
 struct ScoresPlan {

@@ -6,8 +6,10 @@
 // heads; cold-compress PR 11: SnapKV keeps the observation window and compresses the prefix).
 //
 // One CTA per (b, kvh), 8 warps:
-//  1. cp.async copies the whole key block [S, D] into shared memory (16-byte chunks, chunk c
-//     of row r stored at position c ^ (r & 7): ldmatrix of 8 rows is conflict-free).
+//  1. One thread copies the whole key block [S, D] into shared memory with TMA (tensor-map
+//     boxes of 64 channels x up to 256 rows, 128-byte swizzle: 16-byte chunk c of a row's
+//     64-channel panel lands at chunk c ^ (r & 7), so ldmatrix of 8 rows is conflict-free);
+//     the CTA waits on one mbarrier (bounded).
 //  2. Logits on the tensor cores (mma.sync m16n8k16, the G*w <= 16 query rows as M, 8 keys as
 //     N); each warp keeps its keys' logits in registers.
 //  3. Per query row (max, sum) over the whole sequence (registers -> quad -> 8 warps), then
@@ -55,8 +57,40 @@ struct PrefillArgs {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (2 s, %globaltimer) for phase 0 of the key-copy barrier; false on timeout.
+__device__ __forceinline__ bool wait_keys(uint32_t bar) {
+  if (mbar_try_wait(bar, 0)) return true;
+  uint64_t t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (!mbar_try_wait(bar, 0)) {
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > 2000000000ull) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, int w,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      : "memory");
 }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -265,27 +299,27 @@ __device__ __forceinline__ void reduce_level(float* v, int& off, bool& dup, int 
   }
 }
 
-// Copy the key block of unit u = b * KVH + kvh (rows >= S zero-filled) into shared memory,
-// swizzled: chunk c of row r at position c ^ (r & 7).  One commit group.
-template <int D, int NT>
-__device__ __forceinline__ void load_keys(const PrefillArgs& a, int64_t u, uint32_t ks0, int tid) {
-  constexpr int CH = D / 8, SP = 64 * NT;
-  const uint16_t* Kb = a.K + (u / a.KVH) * a.sb + (u % a.KVH) * a.sh;
-  for (int x = tid; x < SP * CH; x += PF_THREADS) {
-    const int r = x / CH, c = x % CH;
-    const bool ok = r < a.S;
-    cp_async16(ks0 + (uint32_t)((r * CH + (c ^ (r & 7))) * 16), ok ? Kb + (int64_t)r * a.ss + c * 8 : Kb, ok ? 16 : 0);
-  }
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
+// Byte offset of 16-byte chunk c of key row r in the staged block of `sp` rows: the rows'
+// 64-channel panels one after another (128-byte rows), chunks swizzled by the row (the layout
+// TMA writes with the 128-byte swizzle).
+__device__ __forceinline__ uint32_t kaddr(int r, int c, int sp) {
+  return (uint32_t)((c >> 3) * sp * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
+
+// rows per TMA box: the staged block is 64 * NT rows
+constexpr int box_rows(int nt) { return 64 * nt < 256 ? 64 * nt : 256; }
 
 // D channels, NT 8-key n-tiles per warp (the key block is padded to 64 * NT rows).  CTA x
 // handles unit (b * KVH + kvh) x; in all-heads mode the KVH CTAs of a batch row form a cluster.
 // (A persistent variant that copies the next unit's keys in during the V gather measured no
 // faster: three CTAs per SM already overlap one CTA's copy with another's compute.)
 template <int D, int NT>
-__global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1) k_prefill_fused(const PrefillArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
+__global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
+    k_prefill_fused(const PrefillArgs a, const __grid_constant__ CUtensorMap tmK) {
+  extern __shared__ unsigned char smem_raw[];
+  // TMA's 128-byte swizzle wants the staged block 1024-byte aligned
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   constexpr int CH = D / 8;        // 16-byte chunks per key row
   constexpr int KS = D / 16;       // k-steps of the MMA
   constexpr int SP = 64 * NT;      // padded key rows
@@ -302,6 +336,7 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1) k_pr
   int32_t* sidx = reinterpret_cast<int32_t*>(exch + (int64_t)cl * SP);     // [SP]
   float2* red = reinterpret_cast<float2*>(sidx + SP);                      // [8 warps][16 rows]
   uint32_t* hist = reinterpret_cast<uint32_t*>(red + 8 * 16);              // [2][256]
+  const uint32_t kbar = smem_u32(hist + 512);                              // the key copy's mbarrier
   const uint32_t ks0 = smem_u32(Ks);
 
   pdl_wait();   // previous kernel on the stream complete and visible
@@ -311,7 +346,17 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1) k_pr
   const int limA = g < a.R ? S - a.w + (g % a.w) : -1;
   const int limB = g + 8 < a.R ? S - a.w + ((g + 8) % a.w) : -1;
 
-  load_keys<D, NT>(a, bk, ks0, tid);
+  bool keys_ok = true;
+  // 1. the key block: one thread issues the TMA boxes (rows >= S arrive zero-filled)
+  if (tid == 0) {
+    mbar_init(kbar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    constexpr int BR = box_rows(NT);
+    mbar_expect_tx(kbar, (uint32_t)(SP * D * 2));
+    for (int p = 0; p < D / 64; ++p)
+      for (int r0 = 0; r0 < SP; r0 += BR)
+        tma_load_4d(ks0 + (uint32_t)(p * SP * 128 + r0 * 128), &tmK, p * 64, r0, (int)kvh, (int)b, kbar);
+  }
   {
 
     // 2. query fragments of the group's R rows (row r = head-in-group * w + window row)
@@ -328,8 +373,9 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1) k_pr
         aq[ks][3] = rB ? ld_q32(Qg + (g + 8) * D + col + 8) : 0u;
       }
     }
-    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-    __syncthreads();
+    __syncthreads();  // the barrier is initialised before anyone waits on it
+    keys_ok = wait_keys(kbar);
+    if (!keys_ok && tid == 0) set_device_status(KVC_ERR_TIMEOUT);
 
     // 3. logits (log2 domain) of this warp's keys, kept in registers
     float c[NT][4];
@@ -343,7 +389,7 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1) k_pr
       for (int ks2 = 0; ks2 < KS / 2; ++ks2) {
         uint32_t b0, b1, b2, b3;
         const int ch = ks2 * 4 + (lane >> 3);
-        ldsm_x4(ks0 + (uint32_t)((r * CH + (ch ^ (r & 7))) * 16), b0, b1, b2, b3);
+        ldsm_x4(ks0 + kaddr(r, ch, SP), b0, b1, b2, b3);
         mma16816(c[nt], aq[2 * ks2], b0, b1);
         mma16816(c[nt], aq[2 * ks2 + 1], b2, b3);
       }
@@ -475,7 +521,7 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1) k_pr
         if (x < total) {
           const int j = sidx[x / CH], cc = x % CH;
           uint4 kv = make_uint4(0u, 0u, 0u, 0u);
-          if (j >= 0) kv = *reinterpret_cast<const uint4*>(Ks + (j * CH + (cc ^ (j & 7))) * 8);
+          if (j >= 0) kv = *reinterpret_cast<const uint4*>(smem + kaddr(j, cc, SP));
           __stcs(reinterpret_cast<uint4*>(Ko + (int64_t)x * 8), kv);
         }
       }
@@ -488,6 +534,8 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1) k_pr
       }
     }
   }
+  // a key copy that did not arrive in time is waited for once more (bounded) before leaving
+  if (!keys_ok && tid == 0) wait_keys(kbar);
 }
 
 int prefill_nt(int D, int64_t S) {
@@ -499,18 +547,52 @@ int prefill_nt(int D, int64_t S) {
 
 size_t prefill_smem(int D, int nt, int cl) {
   const size_t sp = 64 * (size_t)nt;
-  return sp * D * 2 + (size_t)cl * sp * 4 + sp * 4 + 8 * 16 * sizeof(float2) + 2 * 256 * 4;
+  // + the key copy's mbarrier and 1024 bytes for the staged block's alignment
+  return sp * D * 2 + (size_t)cl * sp * 4 + sp * 4 + 8 * 16 * sizeof(float2) + 2 * 256 * 4 + 16 + 1024;
+}
+
+// TMA maps of the caches last used (encoding costs host microseconds), per host thread
+const CUtensorMap* key_map(const uint16_t* K, const kvc_kv_desc& kv, int rows) {
+  struct Entry {
+    CUtensorMap map;
+    const void* K;
+    int64_t S, ss, sh, sb;
+    int B, KVH, D, rows;
+    bool valid = false, ok = false;
+  };
+  thread_local Entry cache[8];
+  thread_local int next = 0;
+  for (Entry& e : cache)
+    if (e.valid && e.K == K && e.S == kv.S && e.ss == kv.stride_s && e.sh == kv.stride_h && e.sb == kv.stride_b &&
+        e.B == kv.B && e.KVH == kv.KVH && e.D == kv.D && e.rows == rows)
+      return e.ok ? &e.map : nullptr;
+  Entry& e = cache[next];
+  next = (next + 1) % 8;
+  e.K = K;
+  e.S = kv.S;
+  e.ss = kv.stride_s;
+  e.sh = kv.stride_h;
+  e.sb = kv.stride_b;
+  e.B = kv.B;
+  e.KVH = kv.KVH;
+  e.D = kv.D;
+  e.rows = rows;
+  e.valid = true;
+  e.ok = make_cache_tensor_map(K, kv, &e.map, rows);
+  return e.ok ? &e.map : nullptr;
 }
 
 template <int D, int NT>
-cudaError_t launch_fused_t(const PrefillArgs& a, int cl, cudaStream_t st) {
+cudaError_t launch_fused_t(const PrefillArgs& a, const kvc_kv_desc& kv, int cl, cudaStream_t st) {
+  const CUtensorMap* tm = key_map(a.K, kv, box_rows(NT));
+  if (!tm) return cudaErrorInvalidValue;
   const size_t smem = prefill_smem(D, NT, cl);
   cudaError_t e = func_attrs_once(reinterpret_cast<const void*>(k_prefill_fused<D, NT>), (int)prefill_smem(D, NT, 8));
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attrs[2];
   const cudaLaunchConfig_t cfg =
       pdl_config(dim3((unsigned)((int64_t)a.B * a.KVH)), dim3(PF_THREADS), smem, st, attrs, cl);
-  e = cudaLaunchKernelEx(&cfg, k_prefill_fused<D, NT>, a);
+  e = cudaLaunchKernelEx(&cfg, k_prefill_fused<D, NT>, a, *tm);
   if (e != cudaSuccess) return e;
   return launched(1);
 }
@@ -559,18 +641,18 @@ cudaError_t launch_prefill_fused(const uint16_t* q, const uint16_t* K, const uin
   const int nt = prefill_nt(kv.D, kv.S);
   if (kv.D == 64) {
     switch (nt) {
-      case 1: return launch_fused_t<64, 1>(a, cl, st);
-      case 2: return launch_fused_t<64, 2>(a, cl, st);
-      case 4: return launch_fused_t<64, 4>(a, cl, st);
-      case 8: return launch_fused_t<64, 8>(a, cl, st);
-      default: return launch_fused_t<64, 16>(a, cl, st);
+      case 1: return launch_fused_t<64, 1>(a, kv, cl, st);
+      case 2: return launch_fused_t<64, 2>(a, kv, cl, st);
+      case 4: return launch_fused_t<64, 4>(a, kv, cl, st);
+      case 8: return launch_fused_t<64, 8>(a, kv, cl, st);
+      default: return launch_fused_t<64, 16>(a, kv, cl, st);
     }
   }
   switch (nt) {
-    case 1: return launch_fused_t<128, 1>(a, cl, st);
-    case 2: return launch_fused_t<128, 2>(a, cl, st);
-    case 4: return launch_fused_t<128, 4>(a, cl, st);
-    default: return launch_fused_t<128, 8>(a, cl, st);
+    case 1: return launch_fused_t<128, 1>(a, kv, cl, st);
+    case 2: return launch_fused_t<128, 2>(a, kv, cl, st);
+    case 4: return launch_fused_t<128, 4>(a, kv, cl, st);
+    default: return launch_fused_t<128, 8>(a, kv, cl, st);
   }
 }
 

@@ -486,7 +486,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_scores_stream(const StreamArg
 template <int D>
 cudaError_t launch_stream_t(const StreamArgs& a, const kvc_kv_desc& kv, int cs, cudaStream_t st) {
   CUtensorMap tm;
-  if (!make_cache_tensor_map(a.Kc, kv, &tm)) return cudaErrorNotSupported;
+  if (!make_cache_tensor_map(a.Kc, kv, &tm, ST_TILE)) return cudaErrorNotSupported;
   const size_t smem = stream_smem<D>(a.G, a.per);
   cudaError_t e = func_attrs_once(reinterpret_cast<const void*>(k_scores_stream<D>), (int)ST_SMEM_MAX);
   if (e != cudaSuccess) return e;

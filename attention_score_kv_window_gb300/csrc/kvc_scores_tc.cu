@@ -964,16 +964,19 @@ bool tc_supported(const ScoresArgs& a, int D) {
 
 void inject_scores_timeout(int armed) { g_inject_timeout.store(armed ? 1 : 0); }
 
-bool make_cache_tensor_map(const uint16_t* K, const kvc_kv_desc& kv, CUtensorMap* tm) {
-  ScoresArgs a{};
-  a.K = K;
-  a.S = kv.S;
-  a.ss = kv.stride_s;
-  a.sh = kv.stride_h;
-  a.sb = kv.stride_b;
-  a.B = kv.B;
-  a.KVH = kv.KVH;
-  return make_k_map(a, kv.D, tm);
+bool make_cache_tensor_map(const uint16_t* K, const kvc_kv_desc& kv, CUtensorMap* tm, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc || box_rows < 1 || box_rows > 256) return false;
+  if (kv.stride_s <= 0 || (kv.KVH > 1 && kv.stride_h <= 0) || (kv.B > 1 && kv.stride_b <= 0)) return false;
+  const int64_t sh = kv.KVH > 1 ? kv.stride_h : kv.S * kv.stride_s;
+  const int64_t sb = kv.B > 1 ? kv.stride_b : (int64_t)kv.KVH * sh;
+  const cuuint64_t dims[4] = {(cuuint64_t)kv.D, (cuuint64_t)kv.S, (cuuint64_t)kv.KVH, (cuuint64_t)kv.B};
+  const cuuint64_t str[3] = {(cuuint64_t)kv.stride_s * 2, (cuuint64_t)sh * 2, (cuuint64_t)sb * 2};
+  const cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(K), dims, str, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t launch_scores_tc(const ScoresArgs& a, int D, cudaStream_t st) {
