@@ -248,11 +248,14 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
   const bool split_ties = !take_all && need > 0;
 
   // 2. radix select of the need-th largest eligible key: digits of 11, 11 and 10 bits
-  uint32_t T = 0, take_eq = 0, eq_total = 0;
+  uint32_t T = 0, take_eq = 0, eq_total = 0, hi_mask = 0xffffffffu;
   if (split_ties) {
     find_digit(sh, 0, 2048u, 21, 0u, (uint32_t)need);
-    uint32_t prefix = sh.prefix, rem = sh.remaining, hi_mask = 0x7FFu << 21;
-    for (int pass = 1; pass < 3; ++pass) {
+    uint32_t prefix = sh.prefix, rem = sh.remaining;
+    hi_mask = 0x7FFu << 21;
+    // once every key of the bin holding the need-th key is taken (the cluster-summed counts
+    // agree in every CTA, so all stop together), the lower digits decide nothing
+    for (int pass = 1; pass < 3 && rem != sh.eq_total; ++pass) {
       const int shift = pass == 1 ? 10 : 0;
       const uint32_t nbins = pass == 1 ? 2048u : 1024u;
       // the local histogram was cleared by the previous push (find_digit ended with a barrier)
@@ -293,7 +296,7 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
       else if (fn.eligible(j)) {
         if (take_all) def = true;
         else if (split_ties) {
-          const uint32_t key = kc[j - c0];
+          const uint32_t key = kc[j - c0] & hi_mask;  // the digits the select decided
           def = key > T;
           eq = key == T;
         }
