@@ -3,16 +3,17 @@
 // keeping, the higher index first when evicting (the lowest-ranked token goes first).
 //
 // A row is split over a thread-block cluster of up to 8 CTAs (1024 threads each); each CTA
-// loads its slice of keys into shared memory once.  An MSB-first radix select (digits of
-// 11, 11 and 10 bits) builds shared-memory histograms with shared atomics; each CTA then
-// adds its nonzero bins into every peer's copy of the cluster histogram with remote
-// reductions (pushes do not stall; remote loads would), and after one cluster barrier each
-// CTA finds the digit holding the k-th item locally with one block scan.  This yields the
-// k-th key T and how many keys equal to T are taken.  The output pass counts, per warp and
-// per CTA, the keys certainly taken (> T) and those equal to T, pushes the CTA counts to
-// every peer, and writes every taken index at (taken-for-sure before it) + (taken-equal
-// before it): ascending order, no sort.  Cluster barriers are hardware barriers; there are
-// no spin-waits.
+// loads its slice of keys into shared memory once.  An MSB-first radix select with 8-bit
+// digits starts below the bits that every candidate shares (the cluster's min and max key
+// have them in common).  Each pass builds a shared-memory histogram with shared atomics, adds
+// the nonzero bins into every peer's copy of the cluster histogram with remote reductions
+// (pushes do not stall; remote loads would), and after one cluster barrier every warp finds
+// the digit holding the k-th item itself.  This yields the k-th key T and how many keys equal
+// to T are taken.  Each CTA's counts of keys taken for sure (> T) and of keys equal to T
+// follow from its own histograms; they are pushed to every peer while the CTA ballots its
+// keys, and every taken index is written at (taken-for-sure before it) + (taken-equal before
+// it): ascending order, no sort.  Cluster barriers are hardware barriers; there are no
+// spin-waits.
 //
 // Users: token top-k for SnapKV/TOVA ("Add TOVA press"; cold-compress PR 11, SnapKV keeps
 // the observation window) and Scissorhands eviction by low-attention fraction.
@@ -79,12 +80,18 @@ struct FractionKeys {
 };
 
 struct __align__(16) SelShared {
-  uint32_t hist[2048];                // this CTA's counts for the current digit
-  uint32_t hsum[3][2048];             // cluster sums per digit pass, filled by every CTA's pushes
-  uint32_t cnt_all[MAX_CLUSTER][4];   // counters pushed by each CTA: forced, eligible, sure, equal
+  uint32_t hist[2][256];  // this CTA's counts for the current digit (two, used alternately)
+  uint32_t hsum[4][256];  // cluster sums per digit pass, filled by every CTA's pushes
+  union {
+    uint32_t ballots[SEL_THREADS / 32][40][2];  // output pass: (sure, equal) ballots per 32-key group
+    uint64_t sortbuf[SH_QUEUE_MAX];            // the eviction queue's re-sort, after the selection
+  };
+  uint32_t cnt_all[MAX_CLUSTER][4];  // per CTA: forced, eligible, min and max eligible key
+  uint32_t out_all[MAX_CLUSTER][2];  // per CTA: keys taken for sure, keys equal to the threshold
   uint32_t warp_a[32];
   uint32_t warp_b[32];
-  uint32_t prefix, remaining, eq_total;
+  uint32_t warp_c[32];
+  uint32_t warp_d[32];
 };
 
 // Writes into the shared memory of CTA `rank` of the cluster.  They do not stall the issuing
@@ -104,89 +111,66 @@ __device__ __forceinline__ void push_v4(const uint32_t* local, int rank, uint4 v
                "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
+__device__ __forceinline__ void push_v2(const uint32_t* local, int rank, uint32_t x, uint32_t y) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};\n" ::"r"(cluster_addr(local, rank)), "r"(x), "r"(y)
+               : "memory");
+}
+// The two halves of a cluster barrier; work placed between them overlaps its latency.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+  cluster_arrive();
+  cluster_wait();
 }
 
-// Add this CTA's nonzero bins into hsum[pass] of every CTA of the cluster, and clear the
-// local histogram for the next digit (the next use follows a block barrier).
-__device__ __forceinline__ void push_bins(SelShared& sh, int pass, uint32_t nbins, int cs) {
-  for (uint32_t b = threadIdx.x; b < nbins; b += SEL_THREADS) {
-    const uint32_t v = sh.hist[b];
-    if (v) {
-      for (int r = 0; r < cs; ++r) push_add(&sh.hsum[pass][b], r, v);
-      sh.hist[b] = 0u;
-    }
-  }
-}
-// Histogram one digit per lane (0xffffffff: no item).  A plain shared atomic per item: the
-// hardware serialises equal addresses within a warp more cheaply than grouping the lanes
-// with match.any first.
-__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t d, int) {
-  if (d != 0xffffffffu) atomicAdd(&hist[d], 1u);
-}
-
-// Digit holding the rem-th largest item, from the cluster-summed bins of `pass` (local).
-// Thread t takes bins in descending order (bpt = 1 or 2 per thread); one warp scan, warp
-// totals through shared memory, and each thread adds the totals of the warps before it
-// (two block barriers).  The thread whose bins contain the item publishes the new prefix,
-// remainder and tie count.
-__device__ __forceinline__ void find_digit(SelShared& sh, int pass, uint32_t nbins, int shift, uint32_t prefix,
-                                           uint32_t rem) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uint32_t bpt = nbins >> 10;  // 2 or 1 bins per thread
-  uint32_t hb[2] = {0u, 0u};
-  for (uint32_t q = 0; q < bpt; ++q) hb[q] = sh.hsum[pass][nbins - 1u - (threadIdx.x * bpt + q)];
-  const uint32_t hs = hb[0] + hb[1];
-  uint32_t x = hs;
+// The digit holding the rem-th largest candidate, from the 256 cluster-summed bins h (every
+// warp scans them itself, so no block barrier follows).  Lane l takes the bins 255 - 8l down
+// to 248 - 8l.  Returns the digit; *above = candidates in higher bins, *in_bin = its count.
+__device__ __forceinline__ uint32_t pick_digit(const uint32_t* h, uint32_t rem, uint32_t* above, uint32_t* in_bin) {
+  const int lane = threadIdx.x & 31;
+  const uint4 a = *reinterpret_cast<const uint4*>(h + 248 - 8 * lane);
+  const uint4 b = *reinterpret_cast<const uint4*>(h + 252 - 8 * lane);
+  const uint32_t hv[8] = {b.w, b.z, b.y, b.x, a.w, a.z, a.y, a.x};  // descending digits
+  uint32_t sum = 0u;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) sum += hv[q];
+  uint32_t incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
   }
-  if (lane == 31) sh.warp_a[warp] = x;
-  __syncthreads();
-  uint32_t before = lane < warp ? sh.warp_a[lane] : 0u;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
-  const uint32_t incl = before + x;
-  const uint32_t excl = incl - hs;
+  const uint32_t excl = incl - sum;
+  uint32_t pick = 0u, run_at = 0u, cnt = 0u;
   if (excl < rem && rem <= incl) {
     uint32_t run = excl;
-    for (uint32_t q = 0; q < bpt; ++q) {
-      const uint32_t d = nbins - 1u - (threadIdx.x * bpt + q);
-      if (run + hb[q] >= rem) {
-        sh.prefix = prefix | (d << shift);
-        sh.remaining = rem - run;
-        sh.eq_total = hb[q];
-        break;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (run < rem && run + hv[q] >= rem) {
+        pick = 255u - 8u * lane - q;
+        run_at = run;
+        cnt = hv[q];
       }
-      run += hb[q];
+      run += hv[q];
     }
   }
-  __syncthreads();
+  const uint32_t src = __ffs(__ballot_sync(0xffffffffu, excl < rem && rem <= incl)) - 1;
+  *above = __shfl_sync(0xffffffffu, run_at, src);
+  *in_bin = __shfl_sync(0xffffffffu, cnt, src);
+  return __shfl_sync(0xffffffffu, pick, src);
 }
 
-// per-warp totals of two counters -> this CTA's totals (thread 0)
-__device__ __forceinline__ uint4 cta_totals(SelShared& sh, uint32_t a, uint32_t b, int lane, int warp) {
-  if (lane == 0) {
-    sh.warp_a[warp] = a;
-    sh.warp_b[warp] = b;
-  }
-  __syncthreads();
-  uint4 t = make_uint4(0u, 0u, 0u, 0u);
-  if (threadIdx.x == 0) {
-    for (int q = 0; q < 32; ++q) {
-      t.x += sh.warp_a[q];
-      t.y += sh.warp_b[q];
-    }
-  }
-  return t;
-}
-
+// One row over the cluster.  Selection: the need-th largest eligible key is found digit by
+// digit (8 bits each, most significant first), starting below the bits that every eligible
+// key shares (the cluster's min and max key have them in common).  A pass histograms the
+// candidates that match the prefix so far into shared memory, adds the nonzero bins into
+// every CTA's cluster sum (remote reductions), and after one cluster barrier every warp
+// scans the sums itself.  The passes stop once every key of the chosen bin is taken.  Each
+// CTA's counts of keys taken for sure and of keys equal to the threshold follow from its own
+// histograms, so the last exchange (those counts) overlaps the local ballot pass.
 template <class Fn>
 __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_t* kc, SelShared& sh,
-                               bool evict_order) {
+                           bool evict_order) {
   const int cs = (int)cg::this_cluster().num_blocks();
   const int cr = (int)cg::this_cluster().block_rank();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -200,15 +184,13 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
   const int64_t w0 = c0 + (int64_t)warp * per_w;
   const int64_t w1 = w0 + per_w < c1 ? w0 + per_w : c1;
 
-  // 1. one sweep: keys into shared memory, forced / eligible counts, first-digit histogram
-  for (uint32_t i = tid; i < 2048u; i += SEL_THREADS) {
-    sh.hist[i] = 0u;
-    sh.hsum[0][i] = 0u;
-    sh.hsum[1][i] = 0u;
-    sh.hsum[2][i] = 0u;
-  }
-  __syncthreads();
-  uint32_t cf = 0, ce = 0;
+  // 0. clear what the peers add into, then announce it (the wait comes after the sweep)
+  for (uint32_t i = tid; i < 4u * 256u; i += SEL_THREADS) (&sh.hsum[0][0])[i] = 0u;
+  if (tid < 256) sh.hist[0][tid] = 0u;
+  cluster_arrive();
+
+  // 1. one sweep: keys into shared memory, forced / eligible counts, min and max eligible key
+  uint32_t cf = 0, ce = 0, kmin = 0xffffffffu, kmax = 0u;
   for (int64_t j0 = 0; j0 < len; j0 += 4 * SEL_THREADS) {
     uint32_t key[4];
 #pragma unroll
@@ -220,72 +202,112 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
     for (int u = 0; u < 4; ++u) {
       const int64_t jl = j0 + u * SEL_THREADS + tid;
       bool f = false, e = false;
-      uint32_t d = 0xffffffffu;
       if (jl < len) {
         kc[jl] = key[u];
         f = fn.forced(c0 + jl);
         e = !f && fn.eligible(c0 + jl);
-        if (e) d = key[u] >> 21;
       }
       cf += __popc(__ballot_sync(0xffffffffu, f));
       ce += __popc(__ballot_sync(0xffffffffu, e));
-      hist_add(sh.hist, d, lane);
+      if (e) {
+        kmin = min(kmin, key[u]);
+        kmax = max(kmax, key[u]);
+      }
     }
   }
-  const uint4 tot0 = cta_totals(sh, cf, ce, lane, warp);
-  cluster_barrier();  // every CTA's hsum is zeroed and its first-digit counts are complete
-  if (tid == 0)  // tot0 is valid in thread 0 only
-    for (int r = 0; r < cs; ++r) push_v4(&sh.cnt_all[cr][0], r, tot0);
-  push_bins(sh, 0, 2048u, cs);
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) {
+    sh.warp_a[warp] = cf;
+    sh.warp_b[warp] = ce;
+    sh.warp_c[warp] = kmin;
+    sh.warp_d[warp] = kmax;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t a = __reduce_add_sync(0xffffffffu, sh.warp_a[lane]);
+    const uint32_t b = __reduce_add_sync(0xffffffffu, sh.warp_b[lane]);
+    const uint32_t lo = __reduce_min_sync(0xffffffffu, sh.warp_c[lane]);
+    const uint32_t hi = __reduce_max_sync(0xffffffffu, sh.warp_d[lane]);
+    cluster_wait();  // every peer has started and cleared its sums
+    if (lane < cs) push_v4(&sh.cnt_all[cr][0], lane, make_uint4(a, b, lo, hi));
+  } else {
+    cluster_wait();
+  }
   cluster_barrier();
   uint32_t n_forced = 0, n_elig = 0;
+  kmin = 0xffffffffu;
+  kmax = 0u;
   for (int r = 0; r < cs; ++r) {
     n_forced += sh.cnt_all[r][0];
     n_elig += sh.cnt_all[r][1];
+    kmin = min(kmin, sh.cnt_all[r][2]);
+    kmax = max(kmax, sh.cnt_all[r][3]);
   }
+  const uint32_t my_forced = sh.cnt_all[cr][0], my_elig = sh.cnt_all[cr][1];
   const int64_t need = (int64_t)k - (int64_t)n_forced > 0 ? (int64_t)k - (int64_t)n_forced : 0;
   const bool take_all = (int64_t)n_elig <= need;
   const bool split_ties = !take_all && need > 0;
 
-  // 2. radix select of the need-th largest eligible key: digits of 11, 11 and 10 bits
-  uint32_t T = 0, take_eq = 0, eq_total = 0, hi_mask = 0xffffffffu;
+  // 2. radix select of the need-th largest eligible key; bits [hi, 32) are common to all
+  int hi = 32 - __clz(kmin ^ kmax);
+  uint32_t mask = hi == 32 ? 0u : ~((1u << hi) - 1u);
+  uint32_t T = kmin & mask, rem = (uint32_t)need, in_bin = n_elig;
+  uint32_t my_above = 0u, my_eq = my_elig;  // this CTA's keys above T's bin and in it
   if (split_ties) {
-    find_digit(sh, 0, 2048u, 21, 0u, (uint32_t)need);
-    uint32_t prefix = sh.prefix, rem = sh.remaining;
-    hi_mask = 0x7FFu << 21;
-    // once every key of the bin holding the need-th key is taken (the cluster-summed counts
-    // agree in every CTA, so all stop together), the lower digits decide nothing
-    for (int pass = 1; pass < 3 && rem != sh.eq_total; ++pass) {
-      const int shift = pass == 1 ? 10 : 0;
-      const uint32_t nbins = pass == 1 ? 2048u : 1024u;
-      // the local histogram was cleared by the previous push (find_digit ended with a barrier)
+#pragma unroll 1
+    for (int pass = 0; hi > 0 && rem != in_bin; ++pass) {
+      const int lo = hi > 8 ? hi - 8 : 0;
+      const uint32_t dmask = (1u << (hi - lo)) - 1u;
+      uint32_t* h = sh.hist[pass & 1];
       for (int64_t j0 = 0; j0 < len; j0 += SEL_THREADS) {
         const int64_t jl = j0 + tid;
-        uint32_t d = 0xffffffffu;
         if (jl < len && fn.eligible(c0 + jl)) {
           const uint32_t key = kc[jl];
-          if ((key & hi_mask) == prefix) d = (key >> shift) & (nbins - 1u);
+          if ((key & mask) == T) atomicAdd(&h[(key >> lo) & dmask], 1u);
         }
-        hist_add(sh.hist, d, lane);
       }
       __syncthreads();
-      push_bins(sh, pass, nbins, cs);
+      // add the nonzero bins into every CTA's sums; clear the other histogram (its last
+      // readers finished before the barrier above) for the next digit
+      for (int i = tid; i < 256 * cs; i += SEL_THREADS) {
+        const uint32_t v = h[i & 255];
+        if (v) push_add(&sh.hsum[pass][i & 255], i >> 8, v);
+      }
+      if (tid < 256) sh.hist[(pass + 1) & 1][tid] = 0u;
       cluster_barrier();
-      find_digit(sh, pass, nbins, shift, prefix, rem);
-      prefix = sh.prefix;
-      rem = sh.remaining;
-      hi_mask |= (nbins - 1u) << shift;
+      uint32_t above, cnt;
+      const uint32_t d = pick_digit(sh.hsum[pass], rem, &above, &cnt);
+      if (warp == 1) {  // this CTA's own keys in the higher bins and in the chosen one
+        uint32_t s = 0u;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t dq = 8u * lane + q;
+          s += dq > d ? h[dq] : 0u;
+        }
+        my_above += __reduce_add_sync(0xffffffffu, s);
+        my_eq = h[d];
+      }
+      T |= d << lo;
+      mask |= dmask << lo;
+      rem -= above;
+      in_bin = cnt;
+      hi = lo;
     }
-    T = prefix;
-    take_eq = rem;
-    eq_total = sh.eq_total;
   }
-  // keys equal to T: the first take_eq in index order when keeping, the last when evicting
+  const uint32_t take_eq = split_ties ? rem : 0u, eq_total = split_ties ? in_bin : 0u;
+  // keys equal to T (under mask): the first take_eq in index order when keeping, the last when
+  // evicting
   const uint32_t skip_eq = evict_order ? (eq_total - take_eq) : 0u;
 
-  // 3. output, ascending.  The count pass keeps each 32-item group's two ballots in the digit
-  // histograms of passes 0 and 1 (no peer writes them any more): 4096 words, 64 groups per warp.
-  uint32_t* ballots = &sh.hsum[0][0];
+  // 3. output, ascending.  Counts to every peer, then the local ballots while the barrier
+  // completes.
+  if (tid == 32) {
+    const uint32_t sure = my_forced + (take_all ? my_elig : (split_ties ? my_above : 0u));
+    const uint32_t eq = split_ties ? my_eq : 0u;
+    for (int r = 0; r < cs; ++r) push_v2(&sh.out_all[cr][0], r, sure, eq);
+  }
+  cluster_arrive();
   const int n_grp = (int)((w1 - w0 + 31) / 32);  // <= ceil(SLICE_MAX / 1024) = 40
   uint32_t cd = 0, cq = 0;
   for (int it = 0; it < n_grp; ++it) {
@@ -296,7 +318,7 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
       else if (fn.eligible(j)) {
         if (take_all) def = true;
         else if (split_ties) {
-          const uint32_t key = kc[j - c0] & hi_mask;  // the digits the select decided
+          const uint32_t key = kc[j - c0] & mask;  // the digits the select decided
           def = key > T;
           eq = key == T;
         }
@@ -304,35 +326,35 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
     }
     const uint32_t bd = __ballot_sync(0xffffffffu, def), be = __ballot_sync(0xffffffffu, eq);
     if (lane == 0) {
-      ballots[(warp * 64 + it) * 2] = bd;
-      ballots[(warp * 64 + it) * 2 + 1] = be;
+      sh.ballots[warp][it][0] = bd;
+      sh.ballots[warp][it][1] = be;
     }
     cd += __popc(bd);
     cq += __popc(be);
   }
-  uint4 tot1 = cta_totals(sh, cd, cq, lane, warp);
-  if (tid == 0) {
-    tot1 = make_uint4(tot0.x, tot0.y, tot1.x, tot1.y);
-    for (int r = 0; r < cs; ++r) push_v4(&sh.cnt_all[cr][0], r, tot1);
+  if (lane == 0) {
+    sh.warp_a[warp] = cd;
+    sh.warp_b[warp] = cq;
   }
-  cluster_barrier();
-  uint32_t d_run = 0, e_run = 0, d_total = 0;
+  __syncthreads();
+  uint32_t d_run = 0, e_run = 0;
+  for (int q = 0; q < warp; ++q) {
+    d_run += sh.warp_a[q];
+    e_run += sh.warp_b[q];
+  }
+  cluster_wait();
+  uint32_t d_total = 0;
   for (int r = 0; r < cs; ++r) {
-    const uint32_t a = sh.cnt_all[r][2], b = sh.cnt_all[r][3];
+    const uint32_t a = sh.out_all[r][0], b = sh.out_all[r][1];
     if (r < cr) {
       d_run += a;
       e_run += b;
     }
     d_total += a;
   }
-
-  for (int q = 0; q < warp; ++q) {
-    d_run += sh.warp_a[q];
-    e_run += sh.warp_b[q];
-  }
   for (int it = 0; it < n_grp; ++it) {
     const int64_t j = w0 + (int64_t)it * 32 + lane;
-    const uint32_t bd = ballots[(warp * 64 + it) * 2], be = ballots[(warp * 64 + it) * 2 + 1];
+    const uint32_t bd = sh.ballots[warp][it][0], be = sh.ballots[warp][it][1];
     const bool def = (bd >> lane) & 1u, eq = (be >> lane) & 1u;
     const uint32_t eb = e_run + __popc(be & lower);  // keys equal to T before j
     const bool take = def || (eq && eb >= skip_eq && eb < skip_eq + take_eq);
@@ -345,7 +367,7 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
     e_run += __popc(be);
   }
   if (cr == 0) {
-    const uint32_t total = d_total + (split_ties ? take_eq : 0u);
+    const uint32_t total = d_total + take_eq;
     for (int64_t p = (int64_t)total + tid; p < k; p += SEL_THREADS) out[p] = -1;
   }
   // no remote access follows the last cluster barrier, so CTAs may leave independently
@@ -410,8 +432,7 @@ __global__ void __launch_bounds__(SEL_THREADS) k_sh_queue(kvc_sh_state s, int m,
   int32_t* out = queue + row * m;
   select_row<FractionKeys>(fn, s.cap, m, out, kc, sh, false);
   __syncthreads();  // the slot-ordered list written by all threads is visible to the block
-  static_assert(sizeof(sh.hsum) >= SH_QUEUE_MAX * sizeof(uint64_t), "queue sort buffer");
-  uint64_t* ck = reinterpret_cast<uint64_t*>(&sh.hsum[0][0]);
+  uint64_t* ck = sh.sortbuf;
   int n2 = 1;
   while (n2 < m) n2 <<= 1;
   for (int p = threadIdx.x; p < n2; p += SEL_THREADS) {

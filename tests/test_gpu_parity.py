@@ -132,7 +132,15 @@ TOPK_CASES = [
     (2, 3, 1000, 100, 64, 0, True, None),
     (2, 3, 1000, 100, 64, 7, True, None),
     (1, 8, 32768, 4096, 64, 0, True, None),
-    (1, 2, 50000, 999, 0, 50, True, None),      # uncached (global-memory) path
+    (1, 2, 50000, 999, 0, 50, True, None),      # 8-CTA cluster, 50 tie levels
+    # cluster rows (S > 4096): evict with ties and dead slots, fewer eligible than k, the
+    # longest row, protected tails with ties and dead slots, k = S - 1
+    (2, 2, 9000, 3000, 0, 2, False, 0.8),
+    (1, 3, 20000, 19000, 100, 0, True, 0.9),
+    (1, 2, 131072, 8192, 64, 0, True, None),
+    (2, 1, 40000, 5000, 32, 3, True, 0.7),
+    (1, 1, 327680, 1000, 0, 0, False, None),
+    (1, 2, 6000, 5999, 0, 0, True, None),
     (4, 2, 2049, 1, 0, 0, False, None),
     (4, 2, 2049, 1, 0, 3, False, None),
     (2, 2, 4096, 64, 0, 5, True, 0.9),
