@@ -108,7 +108,7 @@ struct ScoresArgs {
   float pw;   // pass 2 sums p^pw over the query rows (1: scores; 2: value-channel weights)
   int nsplit;    // key ranges per (b, kvh)
   int64_t units; // 128-key units per (b, kvh); range s covers units [s*units/nsplit, (s+1)*units/nsplit)
-  float2* part;  // [B*KVH][Rpad][nsplit]  (m2, l), see part_index
+  float* part;   // [B*KVH][nsplit][Rpad]  log2-domain log-sum-exp of a key range per query row (-inf: no key)
   float* mrow;   // [B*KVH][Rpad]          M2 + log2(L)  (+inf: no visible key)
   float* out;    // [B*KVH][S]
   float out_mul; // 1/G
@@ -131,29 +131,32 @@ struct ScoresArgs {
   int qm, qpos;
 };
 
-// (m, l) partial of query row r from key range `split`: a row's ranges are contiguous
+// Partial of query row r from key range `split` (m + log2 l over the range's keys): one
+// range's rows are contiguous (a range writes them coalesced; the merge reads whole sectors)
 __host__ __device__ __forceinline__ int64_t part_index(const ScoresArgs& a, int bk, int r, int split) {
-  return ((int64_t)bk * a.Rpad + r) * a.nsplit + split;
+  return ((int64_t)bk * a.nsplit + split) * a.Rpad + r;
 }
 #ifdef __CUDACC__
-// Row r's normaliser over all key ranges, log2 domain: M + log2(L) with M = max m and
-// L = sum l * 2^(m - M); +inf when the row sees no key.  Loads are issued eight at a time and
-// bypass L1 (other CTAs of the same launch may have written the partials).
+// log2-domain log-sum-exp of a key range for one query row, from its running (max, sum)
+__device__ __forceinline__ float range_lse(float m, float l) { return l > 0.f ? m + log2f(l) : -__int_as_float(0x7f800000); }
+// Row r's normaliser over all key ranges, log2 domain: log2 of the sum of 2^lse over the
+// ranges; +inf when the row sees no key.  Loads are issued eight at a time and bypass L1
+// (other CTAs of the same launch may have written the partials).
 __device__ __forceinline__ float merge_row(const ScoresArgs& a, int bk, int r) {
-  const float2* p = a.part + part_index(a, bk, r, 0);
   float M = -__int_as_float(0x7f800000), Ls = 0.f;
   for (int s0 = 0; s0 < a.nsplit; s0 += 8) {
-    float2 o[8];
+    float o[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) o[q] = (s0 + q < a.nsplit) ? __ldcg(p + s0 + q) : make_float2(0.f, 0.f);
+    for (int q = 0; q < 8; ++q)
+      o[q] = (s0 + q < a.nsplit) ? __ldcg(a.part + part_index(a, bk, r, s0 + q)) : -__int_as_float(0x7f800000);
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      if (o[q].y > 0.f) {
-        if (o[q].x > M) {
-          Ls = Ls * exp2f(M - o[q].x) + o[q].y;
-          M = o[q].x;
+      if (o[q] != -__int_as_float(0x7f800000)) {
+        if (o[q] > M) {
+          Ls = Ls * exp2f(M - o[q]) + 1.f;
+          M = o[q];
         } else {
-          Ls += o[q].y * exp2f(o[q].x - M);
+          Ls += exp2f(o[q] - M);
         }
       }
     }

@@ -276,8 +276,8 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass1(const ScoresArgs a) {
       for (int mi = 0; mi < 2; ++mi) {
         if (mi < n_my) {
           const int r = row0 + (mi == 0 ? mt0 : mt1) * 16 + g;
-          a.part[part_index(a, bk, r, split)] = make_float2(m_run[mi][0], l_run[mi][0]);
-          a.part[part_index(a, bk, r + 8, split)] = make_float2(m_run[mi][1], l_run[mi][1]);
+          a.part[part_index(a, bk, r, split)] = range_lse(m_run[mi][0], l_run[mi][0]);
+          a.part[part_index(a, bk, r + 8, split)] = range_lse(m_run[mi][1], l_run[mi][1]);
         }
       }
     }
@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(NTHREADS) k_scores_pass1(const ScoresArgs a) {
         const float2 v = mrg[(kgi * n_mt + mt) * 16 + rr];
         if (v.y > 0.f) L += v.y * ex2(v.x - M);
       }
-      a.part[part_index(a, bk, row0 + tid, split)] = make_float2(M, L);
+      a.part[part_index(a, bk, row0 + tid, split)] = range_lse(M, L);
     }
   }
 }
@@ -924,7 +924,7 @@ ScoresPlan plan_scores(const kvc_kv_desc& kv, int w, int reduce) {
   nsplit = std::min<int64_t>(nsplit, std::max<int64_t>(1, p.units / 2));  // >= 2 units per range
   nsplit = std::min<int64_t>(nsplit, 65535);
   p.nsplit = (int)nsplit;
-  p.part_bytes = (size_t)units * nsplit * p.Rpad * sizeof(float2) + (size_t)units * p.Rpad * sizeof(float);
+  p.part_bytes = (size_t)units * nsplit * p.Rpad * sizeof(float) + (size_t)units * p.Rpad * sizeof(float);
   p.part_bytes = (p.part_bytes + 255) / 256 * 256;
   p.sync_bytes = ((size_t)(1 + units * nsplit) * sizeof(unsigned long long) + 255) / 256 * 256;
   p.group_bytes = reduce == KVC_REDUCE_ALL_HEADS ? (size_t)units * kv.S * sizeof(float) : 0;
@@ -962,8 +962,8 @@ ScoresArgs make_args(const uint16_t* q, const uint16_t* K, const kvc_kv_desc& kv
   a.nsplit = p.nsplit;
   a.units = p.units;
   uint8_t* base = static_cast<uint8_t*>(ws);
-  a.part = reinterpret_cast<float2*>(base);
-  a.mrow = reinterpret_cast<float*>(base + (size_t)kv.B * kv.KVH * p.nsplit * p.Rpad * sizeof(float2));
+  a.part = reinterpret_cast<float*>(base);
+  a.mrow = reinterpret_cast<float*>(base + (size_t)kv.B * kv.KVH * p.nsplit * p.Rpad * sizeof(float));
   a.sync = reinterpret_cast<unsigned long long*>(base + p.part_bytes);
   a.out = reduce == KVC_REDUCE_ALL_HEADS ? reinterpret_cast<float*>(base + p.part_bytes + p.sync_bytes) : scores;
   a.out_mul = 1.f / (float)a.G;

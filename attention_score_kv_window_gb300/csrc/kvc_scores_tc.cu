@@ -407,6 +407,22 @@ __device__ __forceinline__ float sum_exp2x(const float* v, float sl2, float off)
   }
   return hsum4(acc);
 }
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// max of 32 values with three-input max: 16 instructions, depth 4
+__device__ __forceinline__ float max32(const float* v) {
+  float a[12];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) a[i] = max3f(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+  a[10] = v[30];
+  a[11] = v[31];
+  const float b0 = max3f(a[0], a[1], a[2]), b1 = max3f(a[3], a[4], a[5]), b2 = max3f(a[6], a[7], a[8]),
+              b3 = max3f(a[9], a[10], a[11]);
+  return fmaxf(max3f(b0, b1, b2), b3);
+}
 // sum_i exp2(v_i * sl2 + nc_i) over NC values with per-column offsets nc (16-byte aligned)
 template <int NC>
 __device__ __forceinline__ float sum_exp2x_cols(const float* v, float sl2, const float* nc) {
@@ -480,41 +496,72 @@ __device__ __forceinline__ void lse2_merge(float& M, float& L, float m2, float l
     M = m2;
     L = l2;
   } else if (m2 > M) {
-    L = L * exp2f(M - m2) + l2;
+    L = L * ex2(M - m2) + l2;
     M = m2;
   } else {
-    L += l2 * exp2f(m2 - M);
+    L += l2 * ex2(m2 - M);
   }
 }
-// Pass-2 prologue: nc[r] = -(M + log2 L) over the nsplit key-range partials of row r (-inf
-// when the row sees no key) and the row's causal limit, for r < N2.  TPR consecutive epilogue
-// threads share a row: each loads its strided share of the partials (eight loads in flight),
-// then the TPR results are combined with shuffles.
+// Pass-2 prologue: nc[r] = -log2(sum over the nsplit key ranges of 2^lse) for row r (-inf
+// when the row sees no key) and the row's causal limit, for r < N2.  A thread takes four
+// adjacent rows (one 16-byte load per key range: a range's rows are contiguous, so a warp's
+// loads are whole sectors) and every TPR-th range, all its loads in flight at once (up to 8);
+// the TPR threads of a row quad then combine with shuffles.  Every CTA of a (b, kvh) reads
+// the same partials at the same moment, so the bytes per partial matter: one float each.
 template <int N2>
 __device__ __forceinline__ void merge_rows(const ScoresArgs& a, int bk, float* nc, int* lim) {
-  constexpr int TPR = N2 > 128 ? 2 : (N2 > 64 ? 4 : 8);
-  const int r = threadIdx.x / TPR, sub = threadIdx.x % TPR;
-  float M = -CUDART_INF_F, L = 0.f;
-  if (r < N2) {
-    const float2* p = a.part + part_index(a, bk, r, 0);
-    for (int s0 = sub; s0 < a.nsplit; s0 += 8 * TPR) {
-      float2 o[8];
+  constexpr int NQD = N2 / 4;  // row quads
+  constexpr int TPR = NQD >= 64 ? 8 : (NQD >= 48 ? 8 : (NQD >= 32 ? 16 : 32));
+  constexpr int BATCH = 8;
+  static_assert(NQD * TPR <= EPI_WARPS * 32, "row quads x threads per quad fit the epilogue");
+  const int rq = threadIdx.x / TPR, sub = threadIdx.x % TPR;
+  float M[4], L[4];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
+  for (int i = 0; i < 4; ++i) {
+    M[i] = -CUDART_INF_F;
+    L[i] = 0.f;
+  }
+  if (rq < NQD) {
+    for (int s0 = sub; s0 < a.nsplit; s0 += BATCH * TPR) {
+      float4 o[BATCH];
+#pragma unroll
+      for (int q = 0; q < BATCH; ++q) {
         const int sidx = s0 + q * TPR;
-        o[q] = sidx < a.nsplit ? __ldcg(p + sidx) : make_float2(0.f, 0.f);
+        o[q] = sidx < a.nsplit ? __ldcg(reinterpret_cast<const float4*>(a.part + part_index(a, bk, 4 * rq, sidx)))
+                               : make_float4(-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F);
+      }
+      float mx[4] = {M[0], M[1], M[2], M[3]};
+#pragma unroll
+      for (int q = 0; q < BATCH; ++q) {
+        mx[0] = fmaxf(mx[0], o[q].x);
+        mx[1] = fmaxf(mx[1], o[q].y);
+        mx[2] = fmaxf(mx[2], o[q].z);
+        mx[3] = fmaxf(mx[3], o[q].w);
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) lse2_merge(M, L, o[q].x, o[q].y);
+      for (int i = 0; i < 4; ++i) {
+        if (mx[i] == -CUDART_INF_F) continue;
+        float sum = L[i] > 0.f ? L[i] * ex2(M[i] - mx[i]) : 0.f;
+#pragma unroll
+        for (int q = 0; q < BATCH; ++q) {
+          const float v = i == 0 ? o[q].x : (i == 1 ? o[q].y : (i == 2 ? o[q].z : o[q].w));
+          sum += ex2(v - mx[i]);  // 2^-inf = 0 for a range without keys
+        }
+        M[i] = mx[i];
+        L[i] = sum;
+      }
     }
   }
 #pragma unroll
-  for (int off = 1; off < TPR; off <<= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, M, off), l2 = __shfl_xor_sync(0xffffffffu, L, off);
-    lse2_merge(M, L, m2, l2);
-  }
-  if (r < N2 && sub == 0) {
-    nc[r] = L > 0.f ? -(M + log2f(L)) * a.pw : -CUDART_INF_F;
+  for (int off = 1; off < TPR; off <<= 1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      lse2_merge(M[i], L[i], __shfl_xor_sync(0xffffffffu, M[i], off), __shfl_xor_sync(0xffffffffu, L[i], off));
+  if (rq < NQD && sub < 4) {
+    const int r = 4 * rq + sub;
+    const float Mr = sub == 0 ? M[0] : (sub == 1 ? M[1] : (sub == 2 ? M[2] : M[3]));
+    const float Lr = sub == 0 ? L[0] : (sub == 1 ? L[1] : (sub == 2 ? L[2] : L[3]));
+    nc[r] = Lr > 0.f ? -(Mr + log2f(Lr)) * a.pw : -CUDART_INF_F;
     lim[r] = row_limit_i(a, r);
   }
 }
@@ -659,9 +706,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int c0 = NHALF == 2 ? 0 : (w8 >> 2) * NC1;
       const int r = h * 128 + qd * 32 + lane;
       const int lim = row_limit_i(a, r);
-      // (m, l): l = sum exp2(s*log2e - m).  m is a reference, not always the exact max: a
-      // chunk is accumulated against the current m unless its sum shows values more than
-      // 2^64 above it, in which case the exact chunk max is taken and l rescaled.
+      // (m, l): l = sum exp2(s*log2e - m), m the running max, updated every 32-column chunk
+      // (three-input max tree, one rescale of l).  No chunk waits on the previous chunk's
+      // sum, so the next chunk's TMEM load and max overlap this chunk's exponentials.
       float m = -CUDART_INF_F, l = 0.f;
       float v[32];
       for (int it = g; it < n1; it += 2) {
@@ -669,6 +716,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!wait_bar(c.tfull(g), bph, c.abort_flag, c.wait_ns)) break;
         tc_fence_after();
         const uint32_t taddr = c.tmem + ((uint32_t)(qd * 32) << 16) + g * 256 + h * 128 + c0;
+        // last visible column of the tile for this row (rows without keys: lim < 0, none)
+        const int64_t jlast = (kend - 1 < (int64_t)lim ? kend - 1 : (int64_t)lim) - (kbeg + (int64_t)it * TILE + c0);
 #pragma unroll
         for (int ch = 0; ch < NC1 / 32; ++ch) {
           tmem_ld32(taddr + ch * 32, v);
@@ -677,24 +726,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(c.tempty(g));
           }
-          if (lim < 0) continue;
-          const int64_t kt0 = kbeg + (int64_t)it * TILE + c0 + ch * 32;
-          if (!((kt0 + 32 <= kend) && (!a.causal || kt0 + 31 <= (int64_t)lim))) {
-            const int64_t jmax = (kend - 1 < (int64_t)lim ? kend - 1 : (int64_t)lim) - kt0;  // last visible column
+          const int64_t jmax = jlast - ch * 32;
+          if (jmax < 31) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = (i <= jmax) ? v[i] : -CUDART_INF_F;
           }
-          if (m != -CUDART_INF_F) {
-            const float t = sum_exp2x<32>(v, a.sl2, m);
-            if (t <= 0x1p64f) {
-              l += t;
-              continue;
-            }
-          }
-          const float mx = max8(v, 32);
-          if (mx == -CUDART_INF_F) continue;
-          const float mn = fmaxf(m, mx * a.sl2);
-          l = l * ex2(m - mn) + sum_exp2x<32>(v, a.sl2, mn);
+          const float mn = fmaxf(m, max32(v) * a.sl2);
+          const float mref = mn == -CUDART_INF_F ? 0.f : mn;  // all masked so far: sums stay 0
+          l = l * ex2(m - mref) + sum_exp2x<32>(v, a.sl2, mref);
           m = mn;
         }
       }
@@ -715,7 +754,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float2 o = stat[q * 256 + r];
           if (o.y > 0.f) Lsum += o.y * ex2(o.x - M);
         }
-        if (r < a.Rpad) a.part[part_index(a, bk, r, split)] = make_float2(M, Lsum);
+        if (r < a.Rpad) a.part[part_index(a, bk, r, split)] = range_lse(M, Lsum);
       }
     }
     if constexpr (MODE == 3) {
