@@ -34,8 +34,11 @@
 namespace kvc {
 namespace {
 
-constexpr int TILE = 128;           // keys per tile
-constexpr int STAGES = 4;           // K ring depth
+constexpr int TILE = 128;           // keys per accumulator unit of pass 2 (its MMA M)
+constexpr int KT = 256;             // keys per K stage: pass 1's MMA N, two pass-2 units
+constexpr int MAX_STAGES = 4;       // K ring depth: 2 stages of 64 KiB (D = 128), 4 of 32 KiB (D = 64)
+template <int D>
+__host__ __device__ constexpr int ring_stages() { return D == 128 ? 2 : 4; }
 constexpr int EPI_WARPS = 16;       // 4 per SM sub-partition
 constexpr int PRODUCER_WARP = 16;
 constexpr int MMA_WARP = 17;
@@ -45,10 +48,10 @@ constexpr uint32_t TMEM_COLS = 512;
 // Every wait is bounded by ScoresArgs::wait_ns (2 s; 1 ms under kvc_debug_inject_timeout).
 constexpr int KSLOTS = 4;           // pass-2 key-sum exchange slots per group and quadrant
 // K ring full/empty, two accumulator full/empty pairs, query group, key-sum slots per quadrant
-constexpr int NBARS = 2 * STAGES + 5 + 2 * 4 * KSLOTS;
+constexpr int NBARS = 2 * MAX_STAGES + 5 + 2 * 4 * KSLOTS;
 
 __host__ __device__ constexpr uint32_t qpanel_bytes() { return QROWS_MAX * 128; }
-__host__ __device__ constexpr uint32_t kpanel_bytes() { return TILE * 128; }
+__host__ __device__ constexpr uint32_t kpanel_bytes() { return KT * 128; }
 
 // shared-memory layout behind a 1024-byte aligned base
 template <int D>
@@ -56,8 +59,9 @@ struct Layout {
   static constexpr int NP = D / 64;  // 64-element (128-byte) panels along head_dim
   static constexpr uint32_t Q = 0;
   static constexpr uint32_t K = Q + NP * qpanel_bytes();
+  static constexpr int ST = ring_stages<D>();
   static constexpr uint32_t STAGE = NP * kpanel_bytes();
-  static constexpr uint32_t BARS = K + STAGES * STAGE;      // NBARS mbarriers
+  static constexpr uint32_t BARS = K + ST * STAGE;          // NBARS mbarriers
   static constexpr uint32_t MISC = (BARS + 8 * NBARS + 15) / 16 * 16;  // tmem base, abort flag
   static constexpr uint32_t CR = MISC + 16;                 // float[256], 16-byte aligned (float4 reads)
   static constexpr uint32_t LIM = CR + 256 * 4;             // int[256]
@@ -265,12 +269,12 @@ struct Ctx {
   uint32_t tmem;
   uint64_t wait_ns;  // bound on any single wait
   __device__ uint32_t full(int s) const { return sbase + BARS_OFF + 8 * s; }
-  __device__ uint32_t empty(int s) const { return sbase + BARS_OFF + 8 * (STAGES + s); }
-  __device__ uint32_t tfull(int b) const { return sbase + BARS_OFF + 8 * (2 * STAGES + b); }
-  __device__ uint32_t tempty(int b) const { return sbase + BARS_OFF + 8 * (2 * STAGES + 2 + b); }
-  __device__ uint32_t qfull() const { return sbase + BARS_OFF + 8 * (2 * STAGES + 4); }
+  __device__ uint32_t empty(int s) const { return sbase + BARS_OFF + 8 * (MAX_STAGES + s); }
+  __device__ uint32_t tfull(int b) const { return sbase + BARS_OFF + 8 * (2 * MAX_STAGES + b); }
+  __device__ uint32_t tempty(int b) const { return sbase + BARS_OFF + 8 * (2 * MAX_STAGES + 2 + b); }
+  __device__ uint32_t qfull() const { return sbase + BARS_OFF + 8 * (2 * MAX_STAGES + 4); }
   __device__ uint32_t kready(int g, int qd, int slot) const {
-    return sbase + BARS_OFF + 8 * (2 * STAGES + 5 + (g * 4 + qd) * KSLOTS + slot);
+    return sbase + BARS_OFF + 8 * (2 * MAX_STAGES + 5 + (g * 4 + qd) * KSLOTS + slot);
   }
   uint32_t BARS_OFF;
 };
@@ -286,7 +290,7 @@ __device__ __forceinline__ Ctx prologue(unsigned char* smem_raw) {
   c.abort_flag = reinterpret_cast<volatile int*>(c.base + L::MISC + 4);
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < MAX_STAGES; ++s) {
       mbar_init(c.full(s), 1);
       mbar_init(c.empty(s), 1);
     }
@@ -324,8 +328,8 @@ __device__ __forceinline__ void teardown(const Ctx& c) {
   }
 }
 
-// producer: query group once, then the K ring: `total` tiles, the key range's `ntiles` tiles
-// once per pass
+// producer: query group once, then the K ring: `total` stages of KT keys, the key range's
+// `ntiles` stages once per pass
 template <int D>
 __device__ __forceinline__ void producer(const Ctx& c, const ScoresArgs& a, const CUtensorMap* tmK,
                                          const CUtensorMap* tmQ, int qrows, int kvh, int b, int64_t kbeg,
@@ -336,11 +340,11 @@ __device__ __forceinline__ void producer(const Ctx& c, const ScoresArgs& a, cons
   for (int p = 0; p < L::NP; ++p) tma_load_2d(c.sbase + L::Q + p * qpanel_bytes(), tmQ, p * 64, qrow0, c.qfull());
   int issued = 0;
   for (int it = 0; it < total; ++it) {
-    const int s = it % STAGES;
-    const uint32_t ph = (uint32_t)(it / STAGES) & 1u;
+    const int s = it % L::ST;
+    const uint32_t ph = (uint32_t)(it / L::ST) & 1u;
     if (!wait_bar(c.empty(s), ph ^ 1u, c.abort_flag, c.wait_ns)) break;
     mbar_expect_tx(c.full(s), L::STAGE);
-    const int y = (int)(kbeg + (int64_t)(it < ntiles ? it : it - ntiles) * TILE);
+    const int y = (int)(kbeg + (int64_t)(it < ntiles ? it : it - ntiles) * KT);
     for (int p = 0; p < L::NP; ++p)
       tma_load_4d(c.sbase + L::K + s * L::STAGE + p * kpanel_bytes(), tmK, p * 64, y, kvh, b, c.full(s));
     issued = it + 1;
@@ -348,24 +352,14 @@ __device__ __forceinline__ void producer(const Ctx& c, const ScoresArgs& a, cons
   // copies still in flight when the kernel stops early are waited for (bounded) before exit
   if (*c.abort_flag) {
     drain_bar(c.qfull(), 0, c.wait_ns);
-    for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
-      drain_bar(c.full(it % STAGES), (uint32_t)(it / STAGES) & 1u, c.wait_ns);
+    for (int it = (issued > L::ST ? issued - L::ST : 0); it < issued; ++it)
+      drain_bar(c.full(it % L::ST), (uint32_t)(it / L::ST) & 1u, c.wait_ns);
   }
 }
 
 // ----------------------------------------------------------------------------------------
 // softmax helpers
 // ----------------------------------------------------------------------------------------
-__device__ __forceinline__ float max8(const float* v, int n) {
-  float m[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) m[q] = -CUDART_INF_F;
-  for (int i = 0; i < n; i += 8) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) m[q] = fmaxf(m[q], v[i + q]);
-  }
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
-}
 // Packed pairs of fp32 (fma.rn.f32x2 / add.rn.f32x2 issue once for two lanes of work).
 __device__ __forceinline__ uint64_t pk2(float lo, float hi) {
   uint64_t r;
@@ -618,7 +612,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int N2 = 4 * NQ;                     // pass-2 MMA N: padded query rows
   constexpr int QROWS = P1 ? NHALF * 128 : N2;   // query rows staged in shared memory
   constexpr int NPART1 = NHALF == 2 ? 2 : 4;     // pass 1: warps sharing one query row
-  constexpr int NC1 = NHALF == 2 ? TILE : TILE / 2;  // pass 1: key columns per warp and tile
+  constexpr int NC1 = KT / 2;                    // pass 1: key columns per warp and unit
+  constexpr int UPT1 = NHALF;                    // pass-1 units per K stage (one per query half)
   constexpr int NW = N2 / 2;                     // pass 2: query-row columns per warp and tile
   extern __shared__ unsigned char smem_raw[];
   Ctx cx = prologue<D>(smem_raw);  // shared memory and TMEM only
@@ -630,59 +625,71 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int bk = b * a.KVH + kvh;
   int64_t kbeg, kend;
   key_range(a, split, &kbeg, &kend);
-  const int ntiles = (int)((kend - kbeg + TILE - 1) / TILE);
-  const int n1 = P1 ? ntiles : 0;
-  const int total = n1 + (P2 ? ntiles : 0);
+  // Work comes in units, one accumulator (256 TMEM columns) each, alternating between the two
+  // buffers and the two epilogue groups: pass 1 has UPT1 units per K stage (query half h, all
+  // KT keys), pass 2 two (the stage's 128-key halves on M).
+  const int ntiles = (int)((kend - kbeg + KT - 1) / KT);
+  const int n1 = P1 ? ntiles * UPT1 : 0;
+  const int total = n1 + (P2 ? 2 * ntiles : 0);
+  const int nt1 = P1 ? ntiles : 0;  // K stages of pass 1
+  auto unit_stage = [&](int u) -> int { return u < n1 ? u / UPT1 : nt1 + ((u - n1) >> 1); };
+  auto first_of_stage = [&](int u) -> bool { return u < n1 ? (u % UPT1) == 0 : ((u - n1) & 1) == 0; };
+  auto last_of_stage = [&](int u) -> bool { return u < n1 ? (u % UPT1) == UPT1 - 1 : ((u - n1) & 1) == 1; };
 
   if (warp == PRODUCER_WARP) {
-    if (lane == 0) producer<D>(c, a, &tmK, &tmQ, QROWS, kvh, b, kbeg, ntiles, total);
+    if (lane == 0) producer<D>(c, a, &tmK, &tmQ, QROWS, kvh, b, kbeg, ntiles, nt1 + (P2 ? ntiles : 0));
   } else if (warp == MMA_WARP) {
     if (lane == 0 && wait_bar(c.qfull(), 0, c.abort_flag, c.wait_ns)) {
       int done = 0;
-      // Tile it+1's barriers are tested (without blocking) between the two halves of tile
-      // it's MMAs; only if they were not yet complete does the thread wait after the commits.
-      // Either way no MMA of tile it waits on the epilogue.
+      // Unit it+1's barriers are tested (without blocking) halfway through unit it's MMAs;
+      // only if they were not yet complete does the thread wait after the commits.  Either
+      // way no MMA of unit it waits on the epilogue.
       auto ready = [&](int t) -> bool {
+        const int st = unit_stage(t);
         return wait_bar(c.tempty(t & 1), ((uint32_t)(t >> 1) & 1u) ^ 1u, c.abort_flag, c.wait_ns) &&
-               wait_bar(c.full(t % STAGES), (uint32_t)(t / STAGES) & 1u, c.abort_flag, c.wait_ns);
+               (!first_of_stage(t) ||
+                wait_bar(c.full(st % L::ST), (uint32_t)(st / L::ST) & 1u, c.abort_flag, c.wait_ns));
       };
       auto ready_now = [&](int t) -> bool {
+        const int st = unit_stage(t);
         return mbar_test(c.tempty(t & 1), ((uint32_t)(t >> 1) & 1u) ^ 1u) &&
-               mbar_test(c.full(t % STAGES), (uint32_t)(t / STAGES) & 1u);
+               (!first_of_stage(t) || mbar_test(c.full(st % L::ST), (uint32_t)(st / L::ST) & 1u));
       };
       // descriptor start addresses advance in 16-byte units (no carry: shared memory < 256 KB)
       const uint64_t qdesc = sw128_desc(c.sbase + L::Q), kdesc0 = sw128_desc(c.sbase + L::K);
       bool ok = total > 0 && ready(0);
       bool next_ready = false;
       for (int it = 0; ok && it < total; ++it) {
-        const int s = it % STAGES, buf = it & 1;
+        const int s = unit_stage(it) % L::ST, buf = it & 1;
         tc_fence_after();
         const uint64_t kdesc = kdesc0 + (uint64_t)((s * L::STAGE) >> 4);
         const uint32_t d = c.tmem + buf * 256;
         if (it < n1) {
-          constexpr uint32_t idesc = idesc_bf16(128, TILE);
-          constexpr int NMMA = NHALF * KS;
-#pragma unroll
-          for (int q = 0; q < NMMA; ++q) {
-            if (q == NMMA / 2) next_ready = it + 1 < total && ready_now(it + 1);
-            const int h = q / KS, ks = q % KS;
-            const uint32_t koff = (ks & 3) * 32;
-            const uint64_t ad = qdesc + (uint64_t)(((ks >> 2) * qpanel_bytes() + h * 128 * 128 + koff) >> 4);
-            const uint64_t bd = kdesc + (uint64_t)(((ks >> 2) * kpanel_bytes() + koff) >> 4);
-            tc_mma(d + h * 128, ad, bd, idesc, ks > 0 ? 1u : 0u);
-          }
-        } else {
-          constexpr uint32_t idesc = idesc_bf16(128, N2);
+          // query half h (M = 128 rows) against all KT keys of the stage (N = 256)
+          constexpr uint32_t idesc = idesc_bf16(128, KT);
+          const int h = NHALF == 2 ? (it & 1) : 0;
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) {
             if (ks == KS / 2) next_ready = it + 1 < total && ready_now(it + 1);
             const uint32_t koff = (ks & 3) * 32;
-            const uint64_t ad = kdesc + (uint64_t)(((ks >> 2) * kpanel_bytes() + koff) >> 4);
+            const uint64_t ad = qdesc + (uint64_t)(((ks >> 2) * qpanel_bytes() + h * 128 * 128 + koff) >> 4);
+            const uint64_t bd = kdesc + (uint64_t)(((ks >> 2) * kpanel_bytes() + koff) >> 4);
+            tc_mma(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
+          }
+        } else {
+          // the stage's 128-key half kh on M against the query group (N = N2)
+          constexpr uint32_t idesc = idesc_bf16(128, N2);
+          const int kh = (it - n1) & 1;
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            if (ks == KS / 2) next_ready = it + 1 < total && ready_now(it + 1);
+            const uint32_t koff = (ks & 3) * 32;
+            const uint64_t ad = kdesc + (uint64_t)(((ks >> 2) * kpanel_bytes() + kh * TILE * 128 + koff) >> 4);
             const uint64_t bd = qdesc + (uint64_t)(((ks >> 2) * qpanel_bytes() + koff) >> 4);
             tc_mma(d, ad, bd, idesc, ks > 0 ? 1u : 0u);
           }
         }
-        tc_commit(c.empty(s));
+        if (last_of_stage(it)) tc_commit(c.empty(s));
         tc_commit(c.tfull(buf));
         done = it + 1;
         if (it + 1 < total && !next_ready) ok = ready(it + 1);
@@ -700,10 +707,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (warp == 0) epoch = ld_relaxed_u64(a.sync);
     }
     if constexpr (P1) {
-      // one query row per thread; the group's tiles, read in 32-column chunks
-      const int h = NHALF == 2 ? (w8 >> 2) : 0;
-      const int part = NHALF == 2 ? g : g * 2 + (w8 >> 2);
-      const int c0 = NHALF == 2 ? 0 : (w8 >> 2) * NC1;
+      // one query row per thread; the group's units (query half g when NHALF == 2), each
+      // warp taking one half of the KT key columns, read in 32-column chunks
+      const int h = NHALF == 2 ? g : 0;
+      const int part = NHALF == 2 ? (w8 >> 2) : g * 2 + (w8 >> 2);
+      const int c0 = (w8 >> 2) * NC1;
       const int r = h * 128 + qd * 32 + lane;
       const int lim = row_limit_i(a, r);
       // (m, l): l = sum exp2(s*log2e - m), m the running max, updated every 32-column chunk
@@ -715,9 +723,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t bph = (uint32_t)(it >> 1) & 1u;
         if (!wait_bar(c.tfull(g), bph, c.abort_flag, c.wait_ns)) break;
         tc_fence_after();
-        const uint32_t taddr = c.tmem + ((uint32_t)(qd * 32) << 16) + g * 256 + h * 128 + c0;
-        // last visible column of the tile for this row (rows without keys: lim < 0, none)
-        const int64_t jlast = (kend - 1 < (int64_t)lim ? kend - 1 : (int64_t)lim) - (kbeg + (int64_t)it * TILE + c0);
+        const uint32_t taddr = c.tmem + ((uint32_t)(qd * 32) << 16) + g * 256 + c0;
+        // last visible column of the unit for this row (rows without keys: lim < 0, none)
+        const int64_t jlast =
+            (kend - 1 < (int64_t)lim ? kend - 1 : (int64_t)lim) - (kbeg + (int64_t)(it / UPT1) * KT + c0);
 #pragma unroll
         for (int ch = 0; ch < NC1 / 32; ++ch) {
           tmem_ld32(taddr + ch * 32, v);
@@ -849,7 +858,7 @@ bool make_k_map(const ScoresArgs& a, int D, CUtensorMap* tmK) {
   const cuuint64_t kdims[4] = {(cuuint64_t)D, (cuuint64_t)a.S, (cuuint64_t)a.KVH, (cuuint64_t)a.B};
   const cuuint64_t kstr[3] = {(cuuint64_t)a.ss * 2, (cuuint64_t)(a.KVH > 1 ? a.sh : a.S * a.ss) * 2,
                               (cuuint64_t)(a.B > 1 ? a.sb : (int64_t)a.KVH * (a.KVH > 1 ? a.sh : a.S * a.ss)) * 2};
-  const cuuint32_t kbox[4] = {64, (cuuint32_t)TILE, 1, 1};
+  const cuuint32_t kbox[4] = {64, (cuuint32_t)KT, 1, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<uint16_t*>(a.K), kdims, kstr, kbox, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -995,7 +1004,7 @@ bool tc_supported(const ScoresArgs& a, int D) {
   if (D != 64 && D != 128) return false;
   if (a.live != nullptr) return false;
   if (a.Rpad != 64 && a.Rpad != 128 && a.Rpad != 192 && a.Rpad != 256) return false;
-  if (a.R <= 32 || a.S < TILE) return false;
+  if (a.R <= 32 || a.S < KT) return false;
   if ((int64_t)a.B * a.H * a.w < (a.Rpad > 128 ? 256 : 128)) return false;
   if (a.nsplit > 65535 || a.KVH > 65535 || a.B > 65535) return false;
   return tc_maps(a, D) != nullptr;
