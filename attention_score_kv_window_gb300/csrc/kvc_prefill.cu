@@ -5,25 +5,28 @@
 // last w rows of the attention matrix, averaged over query heads and, for TOVA, over all
 // heads; cold-compress PR 11: SnapKV keeps the observation window and compresses the prefix).
 //
-// One CTA per (b, kvh), 8 warps:
-//  1. One thread copies the whole key block [S, D] into shared memory with TMA (tensor-map
+// One CTA per (b, kvh) -- per batch row in all-heads mode (TOVA), whose scores are the mean
+// over every KV head's query group -- 8 warps:
+//  1. One thread copies a head's key block [S, D] into shared memory with TMA (tensor-map
 //     boxes of 64 channels x up to 256 rows, 128-byte swizzle: 16-byte chunk c of a row's
 //     64-channel panel lands at chunk c ^ (r & 7), so ldmatrix of 8 rows is conflict-free);
 //     the CTA waits on one mbarrier (bounded).
 //  2. Logits on the tensor cores (mma.sync m16n8k16, the G*w <= 16 query rows as M, 8 keys as
-//     N); each warp keeps its keys' logits in registers.
+//     N); each warp keeps its keys' logits in registers.  In all-heads mode the next head's
+//     key block is copied in as soon as the logits are out of shared memory.
 //  3. Per query row (max, sum) over the whole sequence (registers -> quad -> 8 warps), then
-//     p = exp2(x - c_r) from the same registers, summed over the group's query rows.
-//  4. All-heads mode (TOVA): a cluster of KVH CTAs (one per KV head of a batch row) pushes its
-//     group-mean scores into every peer's shared memory; after one cluster barrier each CTA
-//     adds them in rank order, so every KV head gets bit-identical scores and selection.
-//  5. The CTA selects the k highest-ranked tokens (radix select over the score bits; ties to
-//     the lower index; the last protect_tail positions forced in) with ascending output.
-//  6. Kept K rows are written from shared memory; kept V rows are read from HBM once.
+//     p = exp2(x - c_r) from the same registers, summed over the group's query rows and added
+//     (head by head, in head order) into the row's scores in shared memory.
+//  4. The CTA selects the k highest-ranked tokens (radix select over the score bits; ties to
+//     the lower index; the last protect_tail positions forced in) with ascending output; in
+//     all-heads mode every KV head of the row gets the same scores and indices.
+//  5. Kept K rows of the last head are written from shared memory, those of earlier heads
+//     read back (from L2: the block passed through it moments before); kept V rows are read
+//     from HBM once.
 //
 // Shared memory holds K of one KV head: 64 KiB for 512 keys of 64 channels, so three CTAs
 // share an SM and one CTA's copy-in overlaps another's compute and write-out.  The only
-// waits are cp.async group waits, block barriers and one hardware cluster barrier.
+// waits are the key copy's mbarrier (bounded) and block barriers.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 #include <stdint.h>
@@ -36,7 +39,7 @@ namespace kvc {
 namespace {
 
 constexpr int PF_THREADS = 256;  // 8 warps
-constexpr int PF_MAX_CLUSTER = 8;
+constexpr int PF_MAX_HEADS = 8;  // KV heads one all-heads CTA scores in turn
 
 struct PrefillArgs {
   const uint16_t* q;
@@ -47,7 +50,8 @@ struct PrefillArgs {
   int S;
   float sl2;     // scale * log2(e)
   float inv_g;   // 1 / G
-  float inv_cl;  // 1 / KVH in all-heads mode, 1 otherwise
+  int nh;        // KV heads per CTA: KVH in all-heads mode, 1 otherwise
+  float inv_nh;  // 1 / nh
   float* scores;  // [B*KVH][S] or null
   int32_t* idx;   // [B*KVH][k]
   uint16_t* Ko;   // [B*KVH][k][D]
@@ -73,12 +77,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait (2 s, %globaltimer) for phase 0 of the key-copy barrier; false on timeout.
-__device__ __forceinline__ bool wait_keys(uint32_t bar) {
-  if (mbar_try_wait(bar, 0)) return true;
+// Bounded wait (2 s, %globaltimer) for the key-copy barrier's phase of the given parity;
+// false on timeout.
+__device__ __forceinline__ bool wait_keys(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0, t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-  while (!mbar_try_wait(bar, 0)) {
+  while (!mbar_try_wait(bar, parity)) {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     if (t - t0 > 2000000000ull) return false;
   }
@@ -118,8 +123,9 @@ __device__ __forceinline__ uint32_t score_key(float f) {
 __device__ __forceinline__ uint32_t ld_q32(const uint16_t* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
 
 // Keep the k highest-ranked of the S scores (a outranks b: higher score, or equal and lower
-// index); positions >= S - protect are forced in.  Score j is the sum of slots[p * SP + j]
-// over the cl slots (times inv_cl when cl > 1), written to scores_out when that is given.
+// index); positions >= S - protect are forced in.  Score j is acc[j] (times mul when nh > 1),
+// written to the nh rows of scores_out (S apart) when that is given; the indices go to the nh
+// rows of gidx (k apart) and to sidx.
 // All PF_THREADS threads; thread t holds keys t + PF_THREADS * u.  An MSB-first radix select
 // over the 32-bit key, starting below the bits every candidate shares (the block's min and max
 // key give them): the scores of a row are close, so most of the 32 bits are settled at once,
@@ -131,8 +137,8 @@ __device__ __forceinline__ uint32_t ld_q32(const uint16_t* p) { return __ldg(rei
 // in the tie bin (one ballot scan for both), so the indices come out ascending.  Fewer than k
 // candidates: all are taken and the rest of the row is -1.  hist: 2 x 256 words.
 template <int KPT>
-__device__ void block_select_keep(const float* slots, int SP, int cl, float inv_cl, float* scores_out, int S, int k,
-                                  int protect, int32_t* sidx, int32_t* gidx, uint32_t* hist) {
+__device__ void block_select_keep(const float* acc, float mul, int nh, float* scores_out, int S, int k, int protect,
+                                  int32_t* sidx, int32_t* gidx, uint32_t* hist) {
   constexpr int NW = PF_THREADS / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   __shared__ uint32_t s_pick[3];  // digit, keys above its bin, keys in its bin
@@ -146,12 +152,10 @@ __device__ void block_select_keep(const float* slots, int SP, int cl, float inv_
     cand[u] = j < S - protect;
     float sc = 0.f;
     if (j < S) {
-      sc = slots[j];
-      if (cl > 1) {
-        for (int p = 1; p < cl; ++p) sc += slots[p * SP + j];
-        sc *= inv_cl;
-      }
-      if (scores_out) scores_out[j] = sc;
+      sc = acc[j];
+      if (nh > 1) sc *= mul;
+      if (scores_out)
+        for (int h = 0; h < nh; ++h) scores_out[(int64_t)h * S + j] = sc;
     }
     key[u] = cand[u] ? score_key(sc) : 0u;
     nf += __popc(__ballot_sync(0xffffffffu, forc[u]));
@@ -267,7 +271,7 @@ __device__ void block_select_keep(const float* slots, int SP, int cl, float inv_
       const uint32_t p = sure_before + (eq_before < rem ? eq_before : rem);
       if (p < (uint32_t)k) {
         sidx[p] = tid + PF_THREADS * u;
-        gidx[p] = tid + PF_THREADS * u;
+        for (int h = 0; h < nh; ++h) gidx[(int64_t)h * k + p] = tid + PF_THREADS * u;
       }
     }
     for (int q = 0; q < NW; ++q) before += tot[u * NW + q];
@@ -275,7 +279,7 @@ __device__ void block_select_keep(const float* slots, int SP, int cl, float inv_
   const uint32_t taken = (before & 0xffffu) + ((before >> 16) < rem ? (before >> 16) : rem);
   for (int p = (int)taken + tid; p < k; p += PF_THREADS) {
     sidx[p] = -1;
-    gidx[p] = -1;
+    for (int h = 0; h < nh; ++h) gidx[(int64_t)h * k + p] = -1;
   }
 }
 
@@ -310,7 +314,8 @@ __device__ __forceinline__ uint32_t kaddr(int r, int c, int sp) {
 constexpr int box_rows(int nt) { return 64 * nt < 256 ? 64 * nt : 256; }
 
 // D channels, NT 8-key n-tiles per warp (the key block is padded to 64 * NT rows).  CTA x
-// handles unit (b * KVH + kvh) x; in all-heads mode the KVH CTAs of a batch row form a cluster.
+// handles the a.nh units (b, kvh) starting at x * a.nh: one in GQA mode, every KV head of
+// batch row x in all-heads mode.
 // (A persistent variant that copies the next unit's keys in during the V gather measured no
 // faster: three CTAs per SM already overlap one CTA's copy with another's compute.)
 template <int D, int NT>
@@ -324,20 +329,25 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
   constexpr int KS = D / 16;       // k-steps of the MMA
   constexpr int SP = 64 * NT;      // padded key rows
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-  unsigned int cl, crank;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(cl));
-  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(crank));
-  const int S = a.S;
-  const int64_t bk = blockIdx.x;
-  const int64_t b = bk / a.KVH, kvh = bk % a.KVH;
+  const int S = a.S, nh = a.nh;
+  const int64_t bk0 = (int64_t)blockIdx.x * nh;  // first unit (b * KVH + kvh) of this CTA
+  const int64_t b = bk0 / a.KVH;
+  const int kvh0 = (int)(bk0 % a.KVH);
 
   uint16_t* Ks = reinterpret_cast<uint16_t*>(smem);                        // [SP][D], swizzled chunks
-  float* exch = reinterpret_cast<float*>(Ks + SP * D);                     // [cl][SP]
-  int32_t* sidx = reinterpret_cast<int32_t*>(exch + (int64_t)cl * SP);     // [SP]
+  float* acc = reinterpret_cast<float*>(Ks + SP * D);                      // [SP] scores, summed over heads
+  int32_t* sidx = reinterpret_cast<int32_t*>(acc + SP);                    // [SP]
   float2* red = reinterpret_cast<float2*>(sidx + SP);                      // [8 warps][16 rows]
   uint32_t* hist = reinterpret_cast<uint32_t*>(red + 8 * 16);              // [2][256]
   const uint32_t kbar = smem_u32(hist + 512);                              // the key copy's mbarrier
   const uint32_t ks0 = smem_u32(Ks);
+  constexpr int BR = box_rows(NT);
+  auto copy_keys = [&](int kvh) {  // one thread: the key block of head kvh, one barrier phase
+    mbar_expect_tx(kbar, (uint32_t)(SP * D * 2));
+    for (int p = 0; p < D / 64; ++p)
+      for (int r0 = 0; r0 < SP; r0 += BR)
+        tma_load_4d(ks0 + (uint32_t)(p * SP * 128 + r0 * 128), &tmK, p * 64, r0, kvh, (int)b, kbar);
+  };
 
   pdl_wait();   // previous kernel on the stream complete and visible
   pdl_trigger();
@@ -346,19 +356,17 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
   const int limA = g < a.R ? S - a.w + (g % a.w) : -1;
   const int limB = g + 8 < a.R ? S - a.w + ((g + 8) % a.w) : -1;
 
-  bool keys_ok = true;
-  // 1. the key block: one thread issues the TMA boxes (rows >= S arrive zero-filled)
+  // 1. the first head's key block: one thread issues the TMA boxes (rows >= S arrive zero-filled)
   if (tid == 0) {
     mbar_init(kbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    constexpr int BR = box_rows(NT);
-    mbar_expect_tx(kbar, (uint32_t)(SP * D * 2));
-    for (int p = 0; p < D / 64; ++p)
-      for (int r0 = 0; r0 < SP; r0 += BR)
-        tma_load_4d(ks0 + (uint32_t)(p * SP * 128 + r0 * 128), &tmK, p * 64, r0, (int)kvh, (int)b, kbar);
+    copy_keys(kvh0);
   }
-  {
-
+  __syncthreads();  // the barrier is initialised before anyone waits on it
+  bool keys_ok = true;
+  int phase = 0;  // key copies waited for so far
+  for (int hh = 0; hh < nh; ++hh) {
+    const int kvh = kvh0 + hh;
     // 2. query fragments of the group's R rows (row r = head-in-group * w + window row)
     const uint16_t* Qg = a.q + (b * a.H + kvh * a.G) * (int64_t)a.w * D;
     uint32_t aq[KS][4];
@@ -373,9 +381,12 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
         aq[ks][3] = rB ? ld_q32(Qg + (g + 8) * D + col + 8) : 0u;
       }
     }
-    __syncthreads();  // the barrier is initialised before anyone waits on it
-    keys_ok = wait_keys(kbar);
-    if (!keys_ok && tid == 0) set_device_status(KVC_ERR_TIMEOUT);
+    keys_ok = __syncthreads_and(wait_keys(kbar, (uint32_t)(phase & 1)) ? 1 : 0) != 0;
+    ++phase;
+    if (!keys_ok) {  // (the same decision in every thread)
+      if (tid == 0) set_device_status(KVC_ERR_TIMEOUT);
+      break;
+    }
 
     // 3. logits (log2 domain) of this warp's keys, kept in registers
     float c[NT][4];
@@ -398,6 +409,15 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
         const int j = key0 + 2 * t + e;
         c[nt][e] = j <= limA ? c[nt][e] * a.sl2 : -CUDART_INF_F;
         c[nt][2 + e] = j <= limB ? c[nt][2 + e] * a.sl2 : -CUDART_INF_F;
+      }
+    }
+    if (hh + 1 < nh) {
+      // every warp's keys are in registers: the next head's block may overwrite the stage
+      // (the generic-proxy reads above are ordered before the copy by the barrier and fence)
+      __syncthreads();
+      if (tid == 0) {
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        copy_keys(kvh + 1);
       }
     }
 
@@ -429,6 +449,7 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
       merge2(mA, lA, __shfl_xor_sync(0xffffffffu, mA, o), __shfl_xor_sync(0xffffffffu, lA, o));
       merge2(mB, lB, __shfl_xor_sync(0xffffffffu, mB, o), __shfl_xor_sync(0xffffffffu, lB, o));
     }
+    // (the previous head's readers of red passed the barrier at this head's key wait)
     if (t == 0) {
       red[warp * 16 + g] = make_float2(mA, lA);
       red[warp * 16 + g + 8] = make_float2(mB, lB);
@@ -453,7 +474,7 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
     //    8 g's (lane bits 2..4) as a transpose-reduce: at each level a lane keeps half of its
     //    values and adds the partner's copy of that half, so the 2 * NT sums of a lane take
     //    14 shuffles (NT = 8) instead of 48, and every lane ends with its own keys; those are
-    //    pushed into slot `crank` of every CTA of the cluster
+    //    added into the row's scores (each key has one owner lane: no two lanes write it)
     constexpr int NV = 2 * NT;  // value m = 2 * nt + e: key (warp * NT + nt) * 8 + 2t + e
     float v[NV];
 #pragma unroll
@@ -469,73 +490,85 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
     constexpr int NF = NV >= 8 ? NV / 8 : 1;  // sums left in this lane: values off .. off + NF - 1
     if (!dup) {
 #pragma unroll
-      for (int i = 0; i < NF; i += (NF >= 2 ? 2 : 1)) {
+      for (int i = 0; i < NF; ++i) {
         const int m = off + i;
         const int j = (warp * NT + (m >> 1)) * 8 + 2 * t + (m & 1);
-        float* dst = exch + (int64_t)crank * SP + j;
-        for (unsigned int p = 0; p < cl; ++p) {
-          const uint32_t la = smem_u32(dst);
-          uint32_t ra = la;
-          if (cl > 1) asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(ra) : "r"(la), "r"(p));
-          if (NF >= 2)
-            asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(ra), "f"(v[i] * a.inv_g),
-                         "f"(v[i + (NF >= 2 ? 1 : 0)] * a.inv_g)
-                         : "memory");
-          else
-            asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(ra), "f"(v[i] * a.inv_g) : "memory");
-        }
-      }
-    }
-    if (cl > 1) {
-      asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-    } else {
-      __syncthreads();
-    }
-    // 6. selection (all threads), ascending indices to shared memory and the output; the final
-    //    scores are the slots summed in rank order (identical in every CTA of the cluster).  No
-    //    remote access follows the cluster barrier.
-    block_select_keep<(64 * NT + PF_THREADS - 1) / PF_THREADS>(exch, SP, (int)cl, a.inv_cl,
-                                                                a.scores ? a.scores + bk * S : nullptr, S, a.k,
-                                                                a.protect, sidx, a.idx + bk * a.k, hist);
-    __syncthreads();
-
-    // 7. kept rows: V from HBM (a batch's loads issued before K is written from shared memory,
-    //    then the V stores)
-    const uint16_t* Vb = a.V ? a.V + b * a.sb + kvh * a.sh : nullptr;
-    uint16_t* Ko = a.Ko + bk * a.k * (int64_t)D;
-    uint16_t* Vo = a.Vo ? a.Vo + bk * a.k * (int64_t)D : nullptr;
-    const int total = a.k * CH;
-    constexpr int BATCH = 8;
-    for (int base = 0; base < total; base += PF_THREADS * BATCH) {
-      uint4 vv[BATCH];
-#pragma unroll
-      for (int u = 0; u < BATCH; ++u) {
-        const int x = base + u * PF_THREADS + tid;
-        const int j = x < total ? sidx[x / CH] : -1;
-        vv[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (Vb && j >= 0) vv[u] = __ldg(reinterpret_cast<const uint4*>(Vb + (int64_t)j * a.ss + (x % CH) * 8));
-      }
-#pragma unroll
-      for (int u = 0; u < BATCH; ++u) {
-        const int x = base + u * PF_THREADS + tid;
-        if (x < total) {
-          const int j = sidx[x / CH], cc = x % CH;
-          uint4 kv = make_uint4(0u, 0u, 0u, 0u);
-          if (j >= 0) kv = *reinterpret_cast<const uint4*>(smem + kaddr(j, cc, SP));
-          __stcs(reinterpret_cast<uint4*>(Ko + (int64_t)x * 8), kv);
-        }
-      }
-      if (Vo) {
-#pragma unroll
-        for (int u = 0; u < BATCH; ++u) {
-          const int x = base + u * PF_THREADS + tid;
-          if (x < total) __stcs(reinterpret_cast<uint4*>(Vo + (int64_t)x * 8), vv[u]);
-        }
+        const float gm = v[i] * a.inv_g;
+        acc[j] = hh == 0 ? gm : acc[j] + gm;
       }
     }
   }
-  // a key copy that did not arrive in time is waited for once more (bounded) before leaving
-  if (!keys_ok && tid == 0) wait_keys(kbar);
+  if (keys_ok) {
+    __syncthreads();  // every head's scores are in acc
+    // 6. selection (all threads), ascending indices to shared memory and to every head's output
+    block_select_keep<(64 * NT + PF_THREADS - 1) / PF_THREADS>(acc, a.inv_nh, nh,
+                                                                a.scores ? a.scores + bk0 * S : nullptr, S, a.k,
+                                                                a.protect, sidx, a.idx + bk0 * a.k, hist);
+    __syncthreads();
+
+    // 7. kept rows of every head: V from HBM, K of the last head from shared memory and of the
+    //    earlier heads from global memory (a batch's loads issued before the stores)
+    const int total = a.k * CH;
+    for (int hh = 0; hh < nh; ++hh) {
+      const int kvh = kvh0 + hh;
+      const uint16_t* Vb = a.V ? a.V + b * a.sb + kvh * a.sh : nullptr;
+      uint16_t* Ko = a.Ko + (bk0 + hh) * a.k * (int64_t)D;
+      uint16_t* Vo = a.Vo ? a.Vo + (bk0 + hh) * a.k * (int64_t)D : nullptr;
+      if (hh == nh - 1) {
+        constexpr int BATCH = 8;
+        for (int base = 0; base < total; base += PF_THREADS * BATCH) {
+          uint4 vv[BATCH];
+#pragma unroll
+          for (int u = 0; u < BATCH; ++u) {
+            const int x = base + u * PF_THREADS + tid;
+            const int j = x < total ? sidx[x / CH] : -1;
+            vv[u] = make_uint4(0u, 0u, 0u, 0u);
+            if (Vb && j >= 0) vv[u] = __ldg(reinterpret_cast<const uint4*>(Vb + (int64_t)j * a.ss + (x % CH) * 8));
+          }
+#pragma unroll
+          for (int u = 0; u < BATCH; ++u) {
+            const int x = base + u * PF_THREADS + tid;
+            if (x < total) {
+              const int j = sidx[x / CH], cc = x % CH;
+              uint4 kv = make_uint4(0u, 0u, 0u, 0u);
+              if (j >= 0) kv = *reinterpret_cast<const uint4*>(smem + kaddr(j, cc, SP));
+              __stcs(reinterpret_cast<uint4*>(Ko + (int64_t)x * 8), kv);
+              if (Vo) __stcs(reinterpret_cast<uint4*>(Vo + (int64_t)x * 8), vv[u]);
+            }
+          }
+        }
+      } else {
+        const uint16_t* Kb = a.K + b * a.sb + kvh * a.sh;
+        constexpr int BATCH = 4;
+        for (int base = 0; base < total; base += PF_THREADS * BATCH) {
+          uint4 vv[BATCH], kk[BATCH];
+#pragma unroll
+          for (int u = 0; u < BATCH; ++u) {
+            const int x = base + u * PF_THREADS + tid;
+            const int j = x < total ? sidx[x / CH] : -1;
+            vv[u] = make_uint4(0u, 0u, 0u, 0u);
+            kk[u] = vv[u];
+            if (j >= 0) {
+              const int64_t o = (int64_t)j * a.ss + (x % CH) * 8;
+              kk[u] = __ldg(reinterpret_cast<const uint4*>(Kb + o));
+              if (Vb) vv[u] = __ldg(reinterpret_cast<const uint4*>(Vb + o));
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < BATCH; ++u) {
+            const int x = base + u * PF_THREADS + tid;
+            if (x < total) {
+              __stcs(reinterpret_cast<uint4*>(Ko + (int64_t)x * 8), kk[u]);
+              if (Vo) __stcs(reinterpret_cast<uint4*>(Vo + (int64_t)x * 8), vv[u]);
+            }
+          }
+        }
+      }
+    }
+  } else if (tid == 0) {
+    // a key copy that did not arrive in time is waited for once more (bounded) before leaving
+    wait_keys(kbar, (uint32_t)((phase - 1) & 1));
+  }
 }
 
 int prefill_nt(int D, int64_t S) {
@@ -545,10 +578,10 @@ int prefill_nt(int D, int64_t S) {
   return 0;
 }
 
-size_t prefill_smem(int D, int nt, int cl) {
+size_t prefill_smem(int D, int nt) {
   const size_t sp = 64 * (size_t)nt;
   // + the key copy's mbarrier and 1024 bytes for the staged block's alignment
-  return sp * D * 2 + (size_t)cl * sp * 4 + sp * 4 + 8 * 16 * sizeof(float2) + 2 * 256 * 4 + 16 + 1024;
+  return sp * D * 2 + sp * 4 + sp * 4 + 8 * 16 * sizeof(float2) + 2 * 256 * 4 + 16 + 1024;
 }
 
 // TMA maps of the caches last used (encoding costs host microseconds), per host thread
@@ -583,15 +616,15 @@ const CUtensorMap* key_map(const uint16_t* K, const kvc_kv_desc& kv, int rows) {
 }
 
 template <int D, int NT>
-cudaError_t launch_fused_t(const PrefillArgs& a, const kvc_kv_desc& kv, int cl, cudaStream_t st) {
+cudaError_t launch_fused_t(const PrefillArgs& a, const kvc_kv_desc& kv, cudaStream_t st) {
   const CUtensorMap* tm = key_map(a.K, kv, box_rows(NT));
   if (!tm) return cudaErrorInvalidValue;
-  const size_t smem = prefill_smem(D, NT, cl);
-  cudaError_t e = func_attrs_once(reinterpret_cast<const void*>(k_prefill_fused<D, NT>), (int)prefill_smem(D, NT, 8));
+  const size_t smem = prefill_smem(D, NT);
+  cudaError_t e = func_attrs_once(reinterpret_cast<const void*>(k_prefill_fused<D, NT>), (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attrs[2];
   const cudaLaunchConfig_t cfg =
-      pdl_config(dim3((unsigned)((int64_t)a.B * a.KVH)), dim3(PF_THREADS), smem, st, attrs, cl);
+      pdl_config(dim3((unsigned)((int64_t)a.B * a.KVH / a.nh)), dim3(PF_THREADS), smem, st, attrs);
   e = cudaLaunchKernelEx(&cfg, k_prefill_fused<D, NT>, a, *tm);
   if (e != cudaSuccess) return e;
   return launched(1);
@@ -602,12 +635,11 @@ cudaError_t launch_fused_t(const PrefillArgs& a, const kvc_kv_desc& kv, int cl, 
 bool prefill_fused_supported(const kvc_kv_desc& kv, int w, int k, int reduce) {
   const int G = kv.H / kv.KVH;
   if ((int64_t)G * w > 16) return false;
-  const int cl = reduce == KVC_REDUCE_ALL_HEADS ? kv.KVH : 1;
-  if (cl > PF_MAX_CLUSTER) return false;
+  if (reduce == KVC_REDUCE_ALL_HEADS && kv.KVH > PF_MAX_HEADS) return false;
   const int nt = prefill_nt(kv.D, kv.S);
   if (nt == 0 || (int64_t)k > 64 * (int64_t)nt) return false;
   if ((int64_t)kv.B * kv.KVH > 2147483647LL) return false;
-  return prefill_smem(kv.D, nt, cl) <= 227 * 1024;
+  return prefill_smem(kv.D, nt) <= 227 * 1024;
 }
 
 cudaError_t launch_prefill_fused(const uint16_t* q, const uint16_t* K, const uint16_t* V, const kvc_kv_desc& kv, int w,
@@ -632,8 +664,8 @@ cudaError_t launch_prefill_fused(const uint16_t* q, const uint16_t* K, const uin
   a.S = (int)kv.S;
   a.sl2 = scale * 1.4426950408889634f;
   a.inv_g = 1.f / (float)a.G;
-  const int cl = reduce == KVC_REDUCE_ALL_HEADS ? kv.KVH : 1;
-  a.inv_cl = 1.f / (float)cl;
+  a.nh = reduce == KVC_REDUCE_ALL_HEADS ? kv.KVH : 1;
+  a.inv_nh = 1.f / (float)a.nh;
   a.scores = scores;
   a.idx = idx;
   a.Ko = Ko;
@@ -641,18 +673,18 @@ cudaError_t launch_prefill_fused(const uint16_t* q, const uint16_t* K, const uin
   const int nt = prefill_nt(kv.D, kv.S);
   if (kv.D == 64) {
     switch (nt) {
-      case 1: return launch_fused_t<64, 1>(a, kv, cl, st);
-      case 2: return launch_fused_t<64, 2>(a, kv, cl, st);
-      case 4: return launch_fused_t<64, 4>(a, kv, cl, st);
-      case 8: return launch_fused_t<64, 8>(a, kv, cl, st);
-      default: return launch_fused_t<64, 16>(a, kv, cl, st);
+      case 1: return launch_fused_t<64, 1>(a, kv, st);
+      case 2: return launch_fused_t<64, 2>(a, kv, st);
+      case 4: return launch_fused_t<64, 4>(a, kv, st);
+      case 8: return launch_fused_t<64, 8>(a, kv, st);
+      default: return launch_fused_t<64, 16>(a, kv, st);
     }
   }
   switch (nt) {
-    case 1: return launch_fused_t<128, 1>(a, kv, cl, st);
-    case 2: return launch_fused_t<128, 2>(a, kv, cl, st);
-    case 4: return launch_fused_t<128, 4>(a, kv, cl, st);
-    default: return launch_fused_t<128, 8>(a, kv, cl, st);
+    case 1: return launch_fused_t<128, 1>(a, kv, st);
+    case 2: return launch_fused_t<128, 2>(a, kv, st);
+    case 4: return launch_fused_t<128, 4>(a, kv, st);
+    default: return launch_fused_t<128, 8>(a, kv, st);
   }
 }
 
