@@ -89,13 +89,33 @@ __device__ __forceinline__ bool wait_keys(uint32_t bar, uint32_t parity) {
   }
   return true;
 }
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, int w,
-                                            uint32_t bar) {
+// L2 eviction policies: a key block that is read again after the selection (earlier heads of
+// an all-heads row) stays in L2 ahead of data read once (the last head's block, the kept V
+// rows and the read-back itself)
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, int w,
+                                                 uint32_t bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
-      "[%6];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6], %7;\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
       : "memory");
+}
+__device__ __forceinline__ uint4 ld_once(const void* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
 }
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -344,9 +364,10 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
   constexpr int BR = box_rows(NT);
   auto copy_keys = [&](int kvh) {  // one thread: the key block of head kvh, one barrier phase
     mbar_expect_tx(kbar, (uint32_t)(SP * D * 2));
+    const uint64_t pol = kvh < kvh0 + nh - 1 ? l2_policy_evict_last() : l2_policy_evict_first();
     for (int p = 0; p < D / 64; ++p)
       for (int r0 = 0; r0 < SP; r0 += BR)
-        tma_load_4d(ks0 + (uint32_t)(p * SP * 128 + r0 * 128), &tmK, p * 64, r0, kvh, (int)b, kbar);
+        tma_load_4d_hint(ks0 + (uint32_t)(p * SP * 128 + r0 * 128), &tmK, p * 64, r0, kvh, (int)b, kbar, pol);
   };
 
   pdl_wait();   // previous kernel on the stream complete and visible
@@ -509,6 +530,7 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
     // 7. kept rows of every head: V from HBM, K of the last head from shared memory and of the
     //    earlier heads from global memory (a batch's loads issued before the stores)
     const int total = a.k * CH;
+    const uint64_t once = l2_policy_evict_first();
     for (int hh = 0; hh < nh; ++hh) {
       const int kvh = kvh0 + hh;
       const uint16_t* Vb = a.V ? a.V + b * a.sb + kvh * a.sh : nullptr;
@@ -523,7 +545,7 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
             const int x = base + u * PF_THREADS + tid;
             const int j = x < total ? sidx[x / CH] : -1;
             vv[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (Vb && j >= 0) vv[u] = __ldg(reinterpret_cast<const uint4*>(Vb + (int64_t)j * a.ss + (x % CH) * 8));
+            if (Vb && j >= 0) vv[u] = ld_once(Vb + (int64_t)j * a.ss + (x % CH) * 8, once);
           }
 #pragma unroll
           for (int u = 0; u < BATCH; ++u) {
@@ -550,8 +572,8 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
             kk[u] = vv[u];
             if (j >= 0) {
               const int64_t o = (int64_t)j * a.ss + (x % CH) * 8;
-              kk[u] = __ldg(reinterpret_cast<const uint4*>(Kb + o));
-              if (Vb) vv[u] = __ldg(reinterpret_cast<const uint4*>(Vb + o));
+              kk[u] = ld_once(Kb + o, once);
+              if (Vb) vv[u] = ld_once(Vb + o, once);
             }
           }
 #pragma unroll
