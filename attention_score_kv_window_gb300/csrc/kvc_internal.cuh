@@ -218,6 +218,11 @@ cudaError_t launch_tova_decode(const uint16_t* q, const uint16_t* knew, const ui
 cudaError_t launch_decode_scores_stream(const uint16_t* q, const uint16_t* knew, const uint16_t* vnew, uint16_t* K,
                                         uint16_t* V, const kvc_kv_desc& kv, float scale, const int32_t* free_slot,
                                         float* group_scores, cudaStream_t st);
+// A whole TOVA decode step in one streamed kernel (scores, all-heads mean, eviction) when the
+// head clusters fit; cudaErrorNotSupported otherwise.
+cudaError_t launch_tova_step_stream(const uint16_t* q, const uint16_t* knew, const uint16_t* vnew, uint16_t* K,
+                                    uint16_t* V, const kvc_kv_desc& kv, float scale, int32_t* free_slot, float* scores,
+                                    cudaStream_t st);
 cudaError_t launch_sh_update_stream(const kvc_sh_state& sh, const int32_t* queue, int qm, int qpos, const uint16_t* q,
                                     const uint16_t* knew, const uint16_t* vnew, uint16_t* K, uint16_t* V,
                                     const kvc_kv_desc& kv, float scale, float* probs, cudaStream_t st);

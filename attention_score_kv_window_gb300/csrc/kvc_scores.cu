@@ -1010,6 +1010,11 @@ cudaError_t launch_sh_update_fused(const kvc_sh_state& sh, const int32_t* queue,
 cudaError_t launch_tova_decode(const uint16_t* q, const uint16_t* knew, const uint16_t* vnew, uint16_t* K, uint16_t* V,
                                const kvc_kv_desc& kv, float scale, int32_t* free_slot, float* scores, void* ws,
                                cudaStream_t st) {
+  // the whole step in one kernel where its head clusters fit
+  {
+    const cudaError_t e1 = launch_tova_step_stream(q, knew, vnew, K, V, kv, scale, free_slot, scores, st);
+    if (e1 != cudaErrorNotSupported) return e1;
+  }
   ScoresArgs a = make_args(q, K, kv, 1, scale, 0, nullptr, KVC_REDUCE_ALL_HEADS, scores, ws, 1);
   // group-mean scores into the workspace: the TMA-streamed kernel, else the small-row kernel
   cudaError_t e = launch_decode_scores_stream(q, knew, vnew, K, V, kv, scale, free_slot, a.out, st);

@@ -1,10 +1,13 @@
 // Decode-step scoring streamed by TMA: one new query per head (G query rows per KV head,
 // G <= 8) against every slot of the cache, the new token written into its slot on the way.
-// Used for a TOVA decode step ("Add TOVA press": the last query's attention; the mean over all
-// heads and the eviction follow in a second small kernel) and a Scissorhands update
-// (cold-compress PR 11: attention mean-pooled over the grouped queries, "attention < 1/keys"
-// flags recorded into the circular history).  A cluster of CTAs splits one (b, kvh)'s slots
-// and exchanges the per-row (max, sum); with one CTA per (b, kvh) there is no cluster.
+// Used for a TOVA decode step ("Add TOVA press": the last query's attention, averaged over all
+// heads; the lowest-scored slot is evicted) and a Scissorhands update (cold-compress PR 11:
+// attention mean-pooled over the grouped queries, "attention < 1/keys" flags recorded into the
+// circular history).  Either a cluster of CTAs splits one (b, kvh)'s slots and exchanges the
+// per-row (max, sum), or (TOVA, one CTA per (b, kvh)) the KVH CTAs of a batch row form the
+// cluster: each keeps its head's probabilities in shared memory, every CTA averages a slice of
+// slots over the heads through distributed shared memory and offers its eviction candidate to
+// rank 0, which writes the evicted slot for every head: the whole step is one kernel.
 //
 // CTA: warp 8 is the producer (one thread issues TMA loads of 128-slot tiles, both 64-channel
 // panels, 128-byte swizzle, into a ring of mbarrier-tracked stages, 128 KiB in flight);
@@ -22,6 +25,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "kvc_internal.cuh"
 
@@ -37,12 +41,19 @@ constexpr uint64_t ST_WAIT_NS = 2000000000ull;
 constexpr int ST_LG_PAD = 4;                       // logit row stride = slots + 4 (spreads banks)
 constexpr size_t ST_SMEM_MAX = 220 * 1024;         // dynamic shared memory limit requested
 
+// default ring depth (128 / 96 KiB in flight), and the shallower ring that lets two CTAs of
+// the head cluster share an SM (64 / 48 KiB)
 template <int D>
+constexpr int ring_deep() { return D == 128 ? 4 : 6; }
+template <int D>
+constexpr int ring_shallow() { return D == 128 ? 2 : 3; }
+
+template <int D, int NS_ = ring_deep<D>()>
 struct StreamLayout {
   static constexpr int NP = D / 64;                          // 64-channel panels
   static constexpr uint32_t PANEL = ST_TILE * 128;           // bytes
   static constexpr uint32_t STAGE = NP * PANEL;
-  static constexpr int NS = D == 128 ? 4 : 6;                // ring depth: 128 / 96 KiB
+  static constexpr int NS = NS_;                             // ring depth
   static constexpr uint32_t BARS = NS * STAGE;               // full[NS], empty[NS]
   static constexpr uint32_t MISC = BARS + 16 * NS;           // abort flag, slot, keys
   static constexpr uint32_t RED = MISC + 64;                 // float2 [8 warps][8 rows]
@@ -50,9 +61,9 @@ struct StreamLayout {
   static constexpr uint32_t LG = XCH + 8 * ST_RMAX * 8;      // float [G][per + pad]
 };
 
-template <int D>
+template <int D, int NS = ring_deep<D>()>
 size_t stream_smem(int G, int per) {
-  return StreamLayout<D>::LG + (size_t)G * (per + ST_LG_PAD) * 4 + 1024;
+  return StreamLayout<D, NS>::LG + (size_t)G * (per + ST_LG_PAD) * 4 + 1024;
 }
 
 struct StreamArgs {
@@ -60,6 +71,7 @@ struct StreamArgs {
   int B, H, KVH, G;    // G query rows per KV head
   int S;               // slots
   int per;             // slots per CTA (a multiple of 128)
+  int split;           // CTAs per (b, kvh) (a cluster when > 1)
   float sl2;           // scale * log2(e)
   float inv_g;
   const uint32_t* live;  // [B*KVH][S/32] live words, or null (every slot live)
@@ -70,7 +82,9 @@ struct StreamArgs {
   uint16_t* Kc;          // the cache, written at the new token's slot
   uint16_t* Vc;
   int64_t sb, sh, ss;
-  float* out;            // [B*KVH][S]: group-mean probabilities
+  float* out;            // [B*KVH][S]: group-mean probabilities (unless allh_out is given)
+  float* allh_out;       // TOVA in one kernel: [B*KVH][S] all-heads mean (cluster = the KVH heads)
+  int32_t* allh_slot;    //   and the evicted slot per (b, kvh) (may alias wslot)
   kvc_sh_state shs;      // Scissorhands step (shs.B > 0)
   const int32_t* queue;
   int qm, qpos;
@@ -174,10 +188,12 @@ __device__ __forceinline__ void merge2(float& m, float& l, float m2, float l2) {
   }
 }
 
-// The cluster = the CTAs of one (b, kvh), each over `per` slots (no cluster with one CTA).
-template <int D>
-__global__ void __launch_bounds__(ST_THREADS, 1) k_scores_stream(const StreamArgs a, const __grid_constant__ CUtensorMap tmK) {
-  using L = StreamLayout<D>;
+// The cluster = the a.split CTAs of one (b, kvh), each over `per` slots, or (a.allh_out) the
+// KVH CTAs of one batch row.
+template <int D, int NS = ring_deep<D>()>
+__global__ void __launch_bounds__(ST_THREADS, NS == ring_shallow<D>() ? 2 : 1)
+    k_scores_stream(const StreamArgs a, const __grid_constant__ CUtensorMap tmK) {
+  using L = StreamLayout<D, NS>;
   constexpr int KS = D / 16;
   constexpr int CH = D / 8;  // 16-byte pieces per row
   extern __shared__ unsigned char smem_raw[];
@@ -196,9 +212,11 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_scores_stream(const StreamArg
   auto full = [&](int s) { return sbase + L::BARS + 8u * s; };
   auto empty = [&](int s) { return sbase + L::BARS + 8u * (L::NS + s); };
 
-  const int64_t bk = blockIdx.x / cs;
+  const int split = a.split;
+  const unsigned int sr = split > 1 ? cr : 0u;  // this CTA's slice of the row
+  const int64_t bk = blockIdx.x / split;
   const int b = (int)(bk / a.KVH), kvh = (int)(bk % a.KVH);
-  const int kbeg = (int)cr * a.per;
+  const int kbeg = (int)sr * a.per;
   const int kend = min(a.S, kbeg + a.per);
   const int len = kend > kbeg ? kend - kbeg : 0;
   const int ntiles = (len + ST_TILE - 1) / ST_TILE;
@@ -265,7 +283,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_scores_stream(const StreamArg
         keys = cnt + 1;
       }
       if (f < 0 || f >= a.S) {
-        if (cr == 0) set_device_status(KVC_ERR_DEVICE_BOUNDS);
+        if (sr == 0) set_device_status(KVC_ERR_DEVICE_BOUNDS);
         if (keys > 0 && !a.queue) --keys;  // nothing was inserted
         f = -1;
       }
@@ -275,7 +293,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_scores_stream(const StreamArg
   } else if (tid == 0) {
     int f = a.wslot ? __ldg(a.wslot + bk) : -1;
     if (a.wslot && (f < 0 || f >= a.S)) {
-      if (cr == 0) set_device_status(KVC_ERR_DEVICE_BOUNDS);
+      if (sr == 0) set_device_status(KVC_ERR_DEVICE_BOUNDS);
       f = -1;
     }
     s_slot[0] = f;
@@ -391,18 +409,18 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_scores_stream(const StreamArg
   float M = -CUDART_INF_F, Ls = 0.f;
   if (tid < R) {
     for (int q = 0; q < ST_CWARPS; ++q) merge2(M, Ls, red[q * ST_RMAX + tid].x, red[q * ST_RMAX + tid].y);
-    if (cs > 1) {
+    if (split > 1) {
       for (unsigned int p = 0; p < cs; ++p) {
         const uint32_t ra = map_rank(su32(&xch[cr * ST_RMAX + tid]), p);
         asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};\n" ::"r"(ra), "f"(M), "f"(Ls) : "memory");
       }
     }
   }
-  if (cs > 1) cluster_sync();
+  if (split > 1) cluster_sync();
   float* crow = reinterpret_cast<float*>(red);  // the merged normalisers (red is no longer read)
   __syncthreads();
   if (tid < R) {
-    if (cs > 1) {
+    if (split > 1) {
       M = -CUDART_INF_F;
       Ls = 0.f;
       for (unsigned int p = 0; p < cs; ++p) {
@@ -455,7 +473,10 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_scores_stream(const StreamArg
       for (int r = 0; r < ST_RMAX; ++r)
         if (r < R && in) sc += ex2(lg[r * lgs + j] - cv[r]);
       const float p = sc * a.inv_g;
-      if (in) a.out[bk * a.S + kbeg + j] = p;
+      if (in) {
+        if (a.allh_out) lg[j] = p;  // (row 0 of column j: read above by this thread only)
+        else a.out[bk * a.S + kbeg + j] = p;
+      }
       if (a.shs.B) {
         // record: lane l holds bit l of live word (kbeg + j0) / 32
         const int64_t gj = kbeg + j;
@@ -480,22 +501,111 @@ __global__ void __launch_bounds__(ST_THREADS, 1) k_scores_stream(const StreamArg
     atomicOr(a.shs.live + bk * nwl + (fslot >> 5), 1u << (fslot & 31));
     a.shs.slot[bk] = fslot;
   }
-  // no remote access follows the cluster barrier
+  if (a.allh_out) {
+    // TOVA eviction: slot j's score is the mean over the KV heads of their group-mean
+    // probabilities (each head's row 0 of lg, read through the cluster); the evicted slot has
+    // the lowest score, then the highest index (composite (~key, slot), largest wins)
+    __shared__ unsigned long long wbest[ST_THREADS / 32], cbest[8];
+    cluster_sync();  // every head's probabilities are in its CTA
+    const int KV = (int)cs;
+    const int per2 = (a.S + KV - 1) / KV;
+    const int j0 = (int)cr * per2, j1 = min(a.S, j0 + per2);
+    const float inv = 1.f / (float)KV;
+    const int64_t row0 = (int64_t)b * KV;
+    unsigned long long best = 0ull;
+    for (int j = j0 + tid; j < j1; j += ST_THREADS) {
+      const uint32_t la = su32(lg + j);
+      float sm = 0.f;
+      for (int h = 0; h < KV; ++h) {
+        float v;
+        asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(map_rank(la, (unsigned)h)) : "memory");
+        sm += v;
+      }
+      sm *= inv;
+      for (int h = 0; h < KV; ++h) a.allh_out[(row0 + h) * a.S + j] = sm;
+      uint32_t u = __float_as_uint(sm);
+      if (u == 0x80000000u) u = 0u;  // -0 ranks as +0
+      const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+      const unsigned long long c = ((unsigned long long)(~key) << 32) | (uint32_t)j;
+      best = c > best ? c : best;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const unsigned long long y = __shfl_xor_sync(0xffffffffu, best, o);
+      best = y > best ? y : best;
+    }
+    if (lane == 0) wbest[warp] = best;
+    __syncthreads();
+    if (tid == 0) {
+      for (int q = 1; q < ST_THREADS / 32; ++q) best = wbest[q] > best ? wbest[q] : best;
+      asm volatile("st.shared::cluster.u64 [%0], %1;\n" ::"r"(map_rank(su32(&cbest[cr]), 0u)), "l"(best) : "memory");
+    }
+    cluster_sync();  // (also: no CTA leaves while a peer may still read its probabilities)
+    if (cr == 0 && tid < 32) {
+      unsigned long long w = 0ull;
+      for (int q = 0; q < KV; ++q) w = cbest[q] > w ? cbest[q] : w;
+      for (int h = tid; h < KV; h += 32) a.allh_slot[row0 + h] = w ? (int32_t)(uint32_t)w : -1;
+    }
+  }
+  // no remote access follows the last cluster barrier
 }
 
-template <int D>
-cudaError_t launch_stream_t(const StreamArgs& a, const kvc_kv_desc& kv, int cs, cudaStream_t st) {
+// a.split CTAs per (b, kvh); the cluster is a.split CTAs, or the KVH heads in the TOVA mode
+template <int D, int NS = ring_deep<D>()>
+cudaError_t launch_stream_t(const StreamArgs& a, const kvc_kv_desc& kv, cudaStream_t st) {
   CUtensorMap tm;
   if (!make_cache_tensor_map(a.Kc, kv, &tm, ST_TILE)) return cudaErrorNotSupported;
-  const size_t smem = stream_smem<D>(a.G, a.per);
-  cudaError_t e = func_attrs_once(reinterpret_cast<const void*>(k_scores_stream<D>), (int)ST_SMEM_MAX);
+  const size_t smem = stream_smem<D, NS>(a.G, a.per);
+  cudaError_t e = func_attrs_once(reinterpret_cast<const void*>(k_scores_stream<D, NS>), (int)ST_SMEM_MAX);
   if (e != cudaSuccess) return e;
   const int64_t units = (int64_t)kv.B * kv.KVH;
+  const int cl = a.allh_out ? kv.KVH : a.split;
   cudaLaunchAttribute attrs[2];
-  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)(units * cs)), dim3(ST_THREADS), smem, st, attrs, cs);
-  e = cudaLaunchKernelEx(&cfg, k_scores_stream<D>, a, tm);
+  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)(units * a.split)), dim3(ST_THREADS), smem, st, attrs, cl);
+  e = cudaLaunchKernelEx(&cfg, k_scores_stream<D, NS>, a, tm);
   if (e != cudaSuccess) return e;
   return launched(1);
+}
+
+// Whether every head cluster of a one-kernel TOVA step is resident at once (clusters of KVH
+// CTAs with the shallow ring, up to two CTAs per SM); cached per device and shape.
+template <int D>
+bool allh_clusters_fit(int KVH, int B, size_t smem) {
+  constexpr int NS = ring_shallow<D>();
+  struct Entry {
+    int dev, KVH;
+    size_t smem;
+    int n;
+  };
+  static std::mutex mu;
+  static Entry cache[16];
+  static int used = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i)
+    if (cache[i].dev == dev && cache[i].KVH == KVH && cache[i].smem == smem) return cache[i].n >= B;
+  auto kern = k_scores_stream<D, NS>;
+  int n = 0;
+  if (func_attrs_once(reinterpret_cast<const void*>(kern), (int)ST_SMEM_MAX) == cudaSuccess) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = KVH;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)KVH);
+    cfg.blockDim = dim3(ST_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+  }
+  if (used < 16) cache[used++] = Entry{dev, KVH, smem, n};
+  return n >= B;
 }
 
 // CTAs per (b, kvh): about one per SM over all rows, at most 8, every slice at least one
@@ -553,9 +663,31 @@ cudaError_t launch_decode_scores_stream(const uint16_t* q, const uint16_t* knew,
   if (cs == 0) return cudaErrorNotSupported;
   StreamArgs a = base_args(q, knew, vnew, K, V, kv, scale);
   a.per = per;
+  a.split = cs;
   a.wslot = free_slot;
   a.out = group_scores;
-  return kv.D == 64 ? launch_stream_t<64>(a, kv, cs, st) : launch_stream_t<128>(a, kv, cs, st);
+  return kv.D == 64 ? launch_stream_t<64>(a, kv, st) : launch_stream_t<128>(a, kv, st);
+}
+
+cudaError_t launch_tova_step_stream(const uint16_t* q, const uint16_t* knew, const uint16_t* vnew, uint16_t* K,
+                                    uint16_t* V, const kvc_kv_desc& kv, float scale, int32_t* free_slot, float* scores,
+                                    cudaStream_t st) {
+  if (!stream_shape_ok(kv) || kv.KVH > 8 || kv.KVH < 2) return cudaErrorNotSupported;
+  int per = 0;
+  if (stream_cluster(kv, &per) != 1) return cudaErrorNotSupported;  // one CTA per (b, kvh) only
+  const int G = kv.H / kv.KVH;
+  const size_t smem = kv.D == 64 ? stream_smem<64, ring_shallow<64>()>(G, per) : stream_smem<128, ring_shallow<128>()>(G, per);
+  if (smem > ST_SMEM_MAX) return cudaErrorNotSupported;
+  const bool fits = kv.D == 64 ? allh_clusters_fit<64>(kv.KVH, kv.B, smem) : allh_clusters_fit<128>(kv.KVH, kv.B, smem);
+  if (!fits) return cudaErrorNotSupported;
+  StreamArgs a = base_args(q, knew, vnew, K, V, kv, scale);
+  a.per = per;
+  a.split = 1;
+  a.wslot = free_slot;
+  a.allh_out = scores;
+  a.allh_slot = free_slot;
+  return kv.D == 64 ? launch_stream_t<64, ring_shallow<64>()>(a, kv, st)
+                    : launch_stream_t<128, ring_shallow<128>()>(a, kv, st);
 }
 
 cudaError_t launch_sh_update_stream(const kvc_sh_state& sh, const int32_t* queue, int qm, int qpos, const uint16_t* q,
@@ -567,6 +699,7 @@ cudaError_t launch_sh_update_stream(const kvc_sh_state& sh, const int32_t* queue
   if (cs == 0) return cudaErrorNotSupported;
   StreamArgs a = base_args(q, knew, vnew, K, V, kv, scale);
   a.per = per;
+  a.split = cs;
   a.live = sh.live;
   a.live_words = kv.S / 32;
   a.out = probs;
@@ -574,7 +707,7 @@ cudaError_t launch_sh_update_stream(const kvc_sh_state& sh, const int32_t* queue
   a.queue = queue;
   a.qm = qm;
   a.qpos = qpos;
-  return kv.D == 64 ? launch_stream_t<64>(a, kv, cs, st) : launch_stream_t<128>(a, kv, cs, st);
+  return kv.D == 64 ? launch_stream_t<64>(a, kv, st) : launch_stream_t<128>(a, kv, st);
 }
 
 KVC_TU_STATUS(scores_stream)
