@@ -348,6 +348,7 @@ CSRC = "attention_score_kv_window_gb300/csrc/"
 SCORE_SOURCES = [CSRC + f for f in ("kvc_scores.cu", "kvc_scores_tc.cu", "kvc_internal.cuh")]
 DECODE_SOURCES = [CSRC + f for f in ("kvc_decode.cu", "kvc_decode.cuh")]
 PREFILL_SOURCES = [CSRC + f for f in ("kvc_prefill.cu", "kvc_internal.cuh")]
+STREAM_SOURCES = [CSRC + f for f in ("kvc_scores.cu", "kvc_scores_stream.cu", "kvc_internal.cuh")]
 
 
 def _sha256_arrays(arrays) -> str:
@@ -648,7 +649,7 @@ class TovaDecodeCase:
         self.tokens_per_step = B * n
         self.inputs_sha256 = _sha256_arrays([self.caches[0][0], self.caches[0][1], self.q, self.kn, self.vn])
         nbytes = B * KVH * n * D * 2 + 2 * B * KVH * D * 2 + 2 * B * KVH * n * 4 + B * H * D * 2
-        self.calls = [Call("tova_decode_step", self._step, nbytes, 2.0 * B * H * n * D, "hbm", SCORE_SOURCES,
+        self.calls = [Call("tova_decode_step", self._step, nbytes, 2.0 * B * H * n * D, "hbm", STREAM_SOURCES,
                            f"tova_decode/{wl.name}")]
 
     def _step(self, i):
@@ -710,7 +711,7 @@ class ScissorhandsCase:
         rank_bytes = slots * (2 + 4 + 0.125) + rows * wl.m * 4
         # the roofline is the update's (score + record over the whole cache); under sparse
         # recording the insert-only steps are tiny, launch-bound kernels
-        self.calls = [Call("scissorhands_update", self._update, upd, 2.0 * B * H * cap * D, "hbm", SCORE_SOURCES,
+        self.calls = [Call("scissorhands_update", self._update, upd, 2.0 * B * H * cap * D, "hbm", STREAM_SOURCES,
                            f"scissorhands/{wl.name}", roofline=True)]
         if wl.record_every > 1:
             self.calls.append(Call("scissorhands_insert", self._insert, 2 * new_rows + slots // 8 + rows * 12))
