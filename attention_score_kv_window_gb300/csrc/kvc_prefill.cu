@@ -51,6 +51,7 @@ struct PrefillArgs {
   float sl2;     // scale * log2(e)
   float inv_g;   // 1 / G
   int nh;        // KV heads per CTA: KVH in all-heads mode, 1 otherwise
+  bool v_device;  // V is device memory (not page-locked host memory read in place)
   float inv_nh;  // 1 / nh
   float* scores;  // [B*KVH][S] or null
   int32_t* idx;   // [B*KVH][k]
@@ -110,7 +111,10 @@ __device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
       : "memory");
 }
-__device__ __forceinline__ uint4 ld_once(const void* p, uint64_t policy) {
+// a row read once: device memory with the evict-first policy, page-locked host memory (read in
+// place over the host link) with a plain non-coherent load
+__device__ __forceinline__ uint4 ld_once(const void* p, uint64_t policy, bool device) {
+  if (!device) return __ldg(reinterpret_cast<const uint4*>(p));
   uint4 v;
   asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;\n"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -545,7 +549,7 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
             const int x = base + u * PF_THREADS + tid;
             const int j = x < total ? sidx[x / CH] : -1;
             vv[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (Vb && j >= 0) vv[u] = ld_once(Vb + (int64_t)j * a.ss + (x % CH) * 8, once);
+            if (Vb && j >= 0) vv[u] = ld_once(Vb + (int64_t)j * a.ss + (x % CH) * 8, once, a.v_device);
           }
 #pragma unroll
           for (int u = 0; u < BATCH; ++u) {
@@ -572,8 +576,8 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
             kk[u] = vv[u];
             if (j >= 0) {
               const int64_t o = (int64_t)j * a.ss + (x % CH) * 8;
-              kk[u] = ld_once(Kb + o, once);
-              if (Vb) vv[u] = ld_once(Vb + o, once);
+              kk[u] = ld_once(Kb + o, once, true);
+              if (Vb) vv[u] = ld_once(Vb + o, once, a.v_device);
             }
           }
 #pragma unroll
@@ -692,6 +696,12 @@ cudaError_t launch_prefill_fused(const uint16_t* q, const uint16_t* K, const uin
   a.idx = idx;
   a.Ko = Ko;
   a.Vo = V ? Vo : nullptr;
+  a.v_device = true;
+  if (V) {
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, V) == cudaSuccess) a.v_device = pa.type == cudaMemoryTypeDevice;
+    else cudaGetLastError();
+  }
   const int nt = prefill_nt(kv.D, kv.S);
   if (kv.D == 64) {
     switch (nt) {
