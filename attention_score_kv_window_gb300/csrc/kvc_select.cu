@@ -7,8 +7,8 @@
 // digits starts below the bits that every candidate shares (the cluster's min and max key
 // have them in common).  Each pass builds a shared-memory histogram with shared atomics, adds
 // the nonzero bins into every peer's copy of the cluster histogram with remote reductions
-// (pushes do not stall; remote loads would), and after one cluster barrier every warp finds
-// the digit holding the k-th item itself.  This yields the k-th key T and how many keys equal
+// (pushes do not stall; remote loads would), and after one cluster barrier one warp finds
+// the digit holding the k-th item and a block barrier hands it to the others.  This yields the k-th key T and how many keys equal
 // to T are taken.  Each CTA's counts of keys taken for sure (> T) and of keys equal to T
 // follow from its own histograms; they are pushed to every peer while the CTA ballots its
 // keys, and every taken index is written at (taken-for-sure before it) + (taken-equal before
@@ -92,6 +92,7 @@ struct __align__(16) SelShared {
   uint32_t warp_b[32];
   uint32_t warp_c[32];
   uint32_t warp_d[32];
+  uint32_t pick[3];  // the pass's digit, keys in higher bins, keys in its bin (warp 0 -> all)
 };
 
 // Writes into the shared memory of CTA `rank` of the cluster.  They do not stall the issuing
@@ -123,9 +124,9 @@ __device__ __forceinline__ void cluster_barrier() {
   cluster_wait();
 }
 
-// The digit holding the rem-th largest candidate, from the 256 cluster-summed bins h (every
-// warp scans them itself, so no block barrier follows).  Lane l takes the bins 255 - 8l down
-// to 248 - 8l.  Returns the digit; *above = candidates in higher bins, *in_bin = its count.
+// The digit holding the rem-th largest candidate, from the 256 cluster-summed bins h (one
+// warp).  Lane l takes the bins 255 - 8l down to 248 - 8l.  Returns the digit; *above =
+// candidates in higher bins, *in_bin = its count.
 __device__ __forceinline__ uint32_t pick_digit(const uint32_t* h, uint32_t rem, uint32_t* above, uint32_t* in_bin) {
   const int lane = threadIdx.x & 31;
   const uint4 a = *reinterpret_cast<const uint4*>(h + 248 - 8 * lane);
@@ -164,8 +165,11 @@ __device__ __forceinline__ uint32_t pick_digit(const uint32_t* h, uint32_t rem, 
 // digit (8 bits each, most significant first), starting below the bits that every eligible
 // key shares (the cluster's min and max key have them in common).  A pass histograms the
 // candidates that match the prefix so far into shared memory, adds the nonzero bins into
-// every CTA's cluster sum (remote reductions), and after one cluster barrier every warp
-// scans the sums itself.  The passes stop once every key of the chosen bin is taken.  Each
+// every CTA's cluster sum (remote reductions), and after one cluster barrier warp 0 scans
+// the sums and a block barrier passes the digit on (every warp scanning them itself cost more
+// in issue slots than the barrier).  One plain shared atomic per candidate: grouping a warp's
+// equal digits with match.any first measured 2.5-4x slower even on the concentrated first
+// digit.  The passes stop once every key of the chosen bin is taken.  Each
 // CTA's counts of keys taken for sure and of keys equal to the threshold follow from its own
 // histograms, so the last exchange (those counts) overlaps the local ballot pass.
 template <class Fn>
@@ -191,15 +195,16 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
 
   // 1. one sweep: keys into shared memory, forced / eligible counts, min and max eligible key
   uint32_t cf = 0, ce = 0, kmin = 0xffffffffu, kmax = 0u;
-  for (int64_t j0 = 0; j0 < len; j0 += 4 * SEL_THREADS) {
-    uint32_t key[4];
+  constexpr int KB = 4;  // keys per thread whose loads are in flight together
+  for (int64_t j0 = 0; j0 < len; j0 += KB * SEL_THREADS) {
+    uint32_t key[KB];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < KB; ++u) {
       const int64_t jl = j0 + u * SEL_THREADS + tid;
       key[u] = jl < len ? fn.key(c0 + jl) : 0u;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < KB; ++u) {
       const int64_t jl = j0 + u * SEL_THREADS + tid;
       bool f = false, e = false;
       if (jl < len) {
@@ -253,19 +258,21 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
   int hi = 32 - __clz(kmin ^ kmax);
   uint32_t mask = hi == 32 ? 0u : ~((1u << hi) - 1u);
   uint32_t T = kmin & mask, rem = (uint32_t)need, in_bin = n_elig;
-  uint32_t my_above = 0u, my_eq = my_elig;  // this CTA's keys above T's bin and in it
+  uint32_t my_above = 0u, my_eq = my_elig;  // this CTA's keys above T's bin and in it (thread 0)
   if (split_ties) {
 #pragma unroll 1
     for (int pass = 0; hi > 0 && rem != in_bin; ++pass) {
       const int lo = hi > 8 ? hi - 8 : 0;
       const uint32_t dmask = (1u << (hi - lo)) - 1u;
       uint32_t* h = sh.hist[pass & 1];
-      for (int64_t j0 = 0; j0 < len; j0 += SEL_THREADS) {
+      for (int64_t j0 = 0; j0 < len; j0 += SEL_THREADS) {  // (warp-uniform trip count)
         const int64_t jl = j0 + tid;
+        uint32_t dg = 0xffffffffu;  // this lane's digit, or none
         if (jl < len && fn.eligible(c0 + jl)) {
           const uint32_t key = kc[jl];
-          if ((key & mask) == T) atomicAdd(&h[(key >> lo) & dmask], 1u);
+          if ((key & mask) == T) dg = (key >> lo) & dmask;
         }
+        if (dg != 0xffffffffu) atomicAdd(&h[dg], 1u);
       }
       __syncthreads();
       // add the nonzero bins into every CTA's sums; clear the other histogram (its last
@@ -276,9 +283,10 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
       }
       if (tid < 256) sh.hist[(pass + 1) & 1][tid] = 0u;
       cluster_barrier();
-      uint32_t above, cnt;
-      const uint32_t d = pick_digit(sh.hsum[pass], rem, &above, &cnt);
-      if (warp == 1) {  // this CTA's own keys in the higher bins and in the chosen one
+      if (warp == 0) {
+        uint32_t above, cnt;
+        const uint32_t d = pick_digit(sh.hsum[pass], rem, &above, &cnt);
+        // this CTA's own keys in the higher bins and in the chosen one
         uint32_t s = 0u;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -287,7 +295,14 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
         }
         my_above += __reduce_add_sync(0xffffffffu, s);
         my_eq = h[d];
+        if (lane == 0) {
+          sh.pick[0] = d;
+          sh.pick[1] = above;
+          sh.pick[2] = cnt;
+        }
       }
+      __syncthreads();
+      const uint32_t d = sh.pick[0], above = sh.pick[1], cnt = sh.pick[2];
       T |= d << lo;
       mask |= dmask << lo;
       rem -= above;
@@ -302,7 +317,7 @@ __device__ void select_row(const Fn& fn, int64_t n, int k, int32_t* out, uint32_
 
   // 3. output, ascending.  Counts to every peer, then the local ballots while the barrier
   // completes.
-  if (tid == 32) {
+  if (tid == 0) {
     const uint32_t sure = my_forced + (take_all ? my_elig : (split_ties ? my_above : 0u));
     const uint32_t eq = split_ties ? my_eq : 0u;
     for (int r = 0; r < cs; ++r) push_v2(&sh.out_all[cr][0], r, sure, eq);
