@@ -288,6 +288,11 @@ PREFILL_CASES = [
     (1, 8, 2, 64, 40, 2, 64, 2, "all_heads", 0.0),       # k > S: all kept, -1 padded, zero rows
     (1, 4, 4, 64, 1024, 16, 512, 16, "gqa", 0.01),       # w 16, window protected
     (4, 16, 8, 64, 777, 2, 513, 0, "gqa", 0.0),          # k not a multiple of 64
+    # all-heads rows scored head by head in one CTA: 4 heads of 128 channels, 8 heads of 64
+    # channels over 16 key tiles per warp, 3 heads with every token kept
+    (2, 16, 4, 128, 512, 2, 200, 2, "all_heads", 0.01),
+    (1, 16, 8, 64, 1000, 1, 300, 1, "all_heads", 0.0),
+    (3, 12, 3, 64, 333, 4, 333, 4, "all_heads", 0.0),
 ]
 
 
