@@ -565,7 +565,7 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
         }
       } else {
         const uint16_t* Kb = a.K + b * a.sb + kvh * a.sh;
-        constexpr int BATCH = 4;
+        constexpr int BATCH = 8;
         for (int base = 0; base < total; base += PF_THREADS * BATCH) {
           uint4 vv[BATCH], kk[BATCH];
 #pragma unroll
