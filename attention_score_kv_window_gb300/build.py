@@ -51,7 +51,7 @@ def build_library(verbose: bool = False, ptxas_info: bool = False) -> str:
         objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
     lib = os.path.join(OUT_DIR, LIB_NAME)
     tmp = lib + ".tmp"
-    cmd = [nvcc_path(), "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static"]
+    cmd = [nvcc_path(), "-shared", "-o", tmp] + objs + ARCH + ["-cudart", "static", "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

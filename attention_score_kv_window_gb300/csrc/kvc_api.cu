@@ -2,6 +2,7 @@
 // stream.  Every entry point validates on the host before enqueuing anything and reports
 // failures as kvc_status codes; no exception crosses the boundary.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -19,6 +20,15 @@ namespace kvc {
 
 namespace {
 thread_local char t_err[512] = {0};
+
+// An NVTX range named after the entry point around each call, so that a timeline tool shows
+// which library call enqueued which kernels.  Without a tool attached a push/pop is a call
+// through an empty function pointer.
+struct NvtxScope {
+  explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+  ~NvtxScope() { nvtxRangePop(); }
+};
+#define KVC_RANGE() NvtxScope kvc_nvtx_scope_(__func__)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -161,6 +171,7 @@ int32_t kvc_version(void) { return 10000; }
 int64_t kvc_launch_count(void) { return (int64_t)g_launches.load(std::memory_order_relaxed); }
 
 kvc_status kvc_debug_inject_timeout(int32_t armed) {
+  KVC_RANGE();
   inject_scores_timeout(armed);
   return KVC_OK;
 }
@@ -215,6 +226,7 @@ kvc_status kvc_window_scores(const kvc_bf16* q_win, const kvc_bf16* K, const kvc
                              int32_t w, float scale, int32_t causal, const uint32_t* live_mask,
                              kvc_head_reduce reduce, float* scores, void* ws, size_t ws_bytes,
                              kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_desc(kv, "kvc_window_scores"));
   KVC_TRY(check_window(kv, w, "kvc_window_scores"));
   KVC_TRY(check_ptr(q_win, "q_win"));
@@ -234,6 +246,7 @@ kvc_status kvc_window_scores_noalloc(const kvc_bf16* q_win, const kvc_bf16* K,
                                      const kvc_kv_desc* kv, int32_t w, float scale, int32_t causal,
                                      const uint32_t* live_mask, kvc_head_reduce reduce,
                                      float* scores, kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_desc(kv, "kvc_window_scores_noalloc"));
   KVC_TRY(check_window(kv, w, "kvc_window_scores_noalloc"));
   KVC_TRY(check_ptr(q_win, "q_win"));
@@ -258,6 +271,7 @@ kvc_status kvc_window_scores_noalloc(const kvc_bf16* q_win, const kvc_bf16* K,
 kvc_status kvc_topk_select(const float* scores, int32_t B, int32_t KVH, int64_t S, int32_t k,
                            int32_t protect_tail, const uint32_t* live_mask, int32_t largest,
                            int32_t* idx, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_RANGE();
   (void)ws;
   (void)ws_bytes;
   if (B < 1 || KVH < 1 || S < 1 || k < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_select: B, KVH, S, k must be >= 1");
@@ -302,6 +316,7 @@ kvc_status check_gather(const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_desc*
 kvc_status kvc_compact_kv(const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_desc* kv,
                           const int32_t* idx, int32_t k, kvc_bf16* K_out, kvc_bf16* V_out,
                           kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_gather(K, V, kv, k, K_out, V_out, "kvc_compact_kv"));
   if (!idx) return fail(KVC_ERR_INVALID_ARG, "idx is NULL");
   return cuda_status(launch_compact(K, V, *kv, idx, k, K_out, V_out, (cudaStream_t)stream), "kvc_compact_kv launch");
@@ -310,6 +325,7 @@ kvc_status kvc_compact_kv(const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_des
 kvc_status kvc_topk_compact(const float* scores, const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_desc* kv,
                             int32_t k, int32_t protect_tail, const uint32_t* live_mask, int32_t largest,
                             int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out, kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_gather(K, V, kv, k, K_out, V_out, "kvc_topk_compact"));
   if (kv->S > topk_max_len()) return fail(KVC_ERR_UNSUPPORTED, "kvc_topk_compact: S > %lld", (long long)topk_max_len());
   if ((int64_t)kv->B * kv->KVH > 2147483647LL) return fail(KVC_ERR_UNSUPPORTED, "kvc_topk_compact: too many rows");
@@ -342,6 +358,7 @@ kvc_status kvc_compress_prefill(const kvc_bf16* q_win, const kvc_bf16* K, const 
                                 kvc_head_reduce reduce, int32_t k, int32_t protect_tail,
                                 float* scores, int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out,
                                 void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_RANGE();
   const char* who = "kvc_compress_prefill";
   KVC_TRY(check_desc(kv, who));
   if (k < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill: k must be >= 1");
@@ -390,6 +407,7 @@ kvc_status kvc_compress_prefill(const kvc_bf16* q_win, const kvc_bf16* K, const 
 
 kvc_status kvc_write_slots(const kvc_bf16* k_new, const kvc_bf16* v_new, const int32_t* slot,
                            kvc_bf16* K, kvc_bf16* V, const kvc_kv_desc* kv, kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_desc(kv, "kvc_write_slots"));
   KVC_TRY(check_ptr(k_new, "k_new"));
   KVC_TRY(check_ptr(K, "K"));
@@ -406,6 +424,7 @@ kvc_status kvc_tova_decode_step(const kvc_bf16* q_new, const kvc_bf16* k_new,
                                 const kvc_bf16* v_new, kvc_bf16* K, kvc_bf16* V,
                                 const kvc_kv_desc* kv, float scale, int32_t* free_slot,
                                 float* scores, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_desc(kv, "kvc_tova_decode_step"));
   if (!free_slot) return fail(KVC_ERR_INVALID_ARG, "free_slot is NULL");
   KVC_TRY(check_ptr(scores, "scores"));
@@ -427,6 +446,7 @@ kvc_status kvc_tova_decode_step(const kvc_bf16* q_new, const kvc_bf16* k_new,
 }
 
 kvc_status kvc_scissorhands_init(kvc_sh_state* st, int32_t n_live, kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_sh(st));
   if (n_live < 0 || n_live > st->cap) return fail(KVC_ERR_INVALID_ARG, "scissorhands_init: n_live in [0, cap]");
   st->t = 0;
@@ -435,6 +455,7 @@ kvc_status kvc_scissorhands_init(kvc_sh_state* st, int32_t n_live, kvc_stream_t 
 }
 
 kvc_status kvc_scissorhands_update_from_probs(kvc_sh_state* st, const float* p, kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_sh(st));
   KVC_TRY(check_ptr(p, "p"));
   const kvc_status s = cuda_status(launch_sh_record(*st, p, (cudaStream_t)stream), "scissorhands record launch");
@@ -498,6 +519,7 @@ kvc_status kvc_scissorhands_update(kvc_sh_state* st, const kvc_bf16* q_new, cons
                                    const kvc_bf16* v_new, kvc_bf16* K, kvc_bf16* V,
                                    const kvc_kv_desc* kv, float scale, float* probs, void* ws,
                                    size_t ws_bytes, kvc_stream_t stream) {
+  KVC_RANGE();
   return sh_update(st, nullptr, 0, 0, q_new, k_new, v_new, K, V, kv, scale, probs, ws, ws_bytes, stream,
                    "kvc_scissorhands_update");
 }
@@ -506,6 +528,7 @@ kvc_status kvc_scissorhands_update_queued(kvc_sh_state* st, const int32_t* queue
                                           const kvc_bf16* q_new, const kvc_bf16* k_new, const kvc_bf16* v_new,
                                           kvc_bf16* K, kvc_bf16* V, const kvc_kv_desc* kv, float scale,
                                           float* probs, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_RANGE();
   if (!queue) return fail(KVC_ERR_INVALID_ARG, "kvc_scissorhands_update_queued: queue is NULL");
   return sh_update(st, queue, m, pos, q_new, k_new, v_new, K, V, kv, scale, probs, ws, ws_bytes, stream,
                    "kvc_scissorhands_update_queued");
@@ -514,11 +537,13 @@ kvc_status kvc_scissorhands_update_queued(kvc_sh_state* st, const int32_t* queue
 kvc_status kvc_scissorhands_insert(kvc_sh_state* st, const int32_t* queue, int32_t m, int32_t pos,
                                    const kvc_bf16* k_new, const kvc_bf16* v_new, kvc_bf16* K, kvc_bf16* V,
                                    const kvc_kv_desc* kv, kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_sh_insert(st, queue, m, pos, k_new, v_new, K, V, kv, "kvc_scissorhands_insert"));
   return sh_insert(st, queue, m, pos, k_new, v_new, K, V, kv, stream);
 }
 
 kvc_status kvc_scissorhands_refill_queue(kvc_sh_state* st, int32_t m, int32_t* queue, kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_sh(st));
   if (m < 1 || m > st->cap || m > SH_QUEUE_MAX)
     return fail(KVC_ERR_INVALID_ARG, "scissorhands_refill_queue: m in [1, min(cap, %d)]", SH_QUEUE_MAX);
@@ -528,6 +553,7 @@ kvc_status kvc_scissorhands_refill_queue(kvc_sh_state* st, int32_t m, int32_t* q
 }
 
 kvc_status kvc_scissorhands_evict(kvc_sh_state* st, int32_t m, int32_t* evicted, kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_sh(st));
   if (m < 1 || m > st->cap) return fail(KVC_ERR_INVALID_ARG, "scissorhands_evict: m in [1, cap]");
   if (st->t < 1) return fail(KVC_ERR_INVALID_ARG, "scissorhands_evict: no step recorded yet");
@@ -540,6 +566,7 @@ kvc_status kvc_scissorhands_evict(kvc_sh_state* st, int32_t m, int32_t* evicted,
 kvc_status kvc_channel_score(const kvc_bf16* q_win, int32_t w, const kvc_bf16* K,
                              const kvc_kv_desc* kv, const int32_t* idx, int32_t k, float* cs,
                              void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_desc(kv, "kvc_channel_score"));
   if (w < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_score: w must be >= 1");
   if (idx && k < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_score: k must be >= 1 with idx");
@@ -554,6 +581,7 @@ kvc_status kvc_channel_score(const kvc_bf16* q_win, int32_t w, const kvc_bf16* K
 kvc_status kvc_channel_prune(const float* cs, const kvc_bf16* K, const kvc_kv_desc* kv,
                              int32_t C, int32_t zero_mode, int32_t* ch_idx, kvc_bf16* K_out,
                              kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_desc(kv, "kvc_channel_prune"));
   if (C < 1 || C > kv->D) return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune: need 1 <= C <= D");
   if (!zero_mode && C % 8) return fail(KVC_ERR_UNSUPPORTED, "kvc_channel_prune: compact mode needs C %% 8 == 0");
@@ -578,6 +606,7 @@ kvc_status kvc_channel_prune(const float* cs, const kvc_bf16* K, const kvc_kv_de
 kvc_status kvc_value_channel_score(const kvc_bf16* q_win, int32_t w, const kvc_bf16* Kc, const kvc_bf16* Vc,
                                    const kvc_kv_desc* kv, float scale, float* cs, void* ws, size_t ws_bytes,
                                    kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_desc(kv, "kvc_value_channel_score"));
   KVC_TRY(check_window(kv, w, "kvc_value_channel_score"));
   KVC_TRY(check_ptr(q_win, "q_win"));
@@ -603,6 +632,7 @@ kvc_status kvc_value_channel_score(const kvc_bf16* q_win, int32_t w, const kvc_b
 kvc_status kvc_decode_attention(const kvc_bf16* q, const int32_t* ch, const kvc_bf16* K, const kvc_kv_desc* kd,
                                 const kvc_bf16* V, const kvc_kv_desc* vd, const uint32_t* live_mask, float scale,
                                 float* out, void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_desc(kd, "kvc_decode_attention (K)"));
   KVC_TRY(check_desc(vd, "kvc_decode_attention (V)"));
   if (kd->B != vd->B || kd->H != vd->H || kd->KVH != vd->KVH || kd->S != vd->S)
@@ -628,6 +658,7 @@ kvc_status kvc_decode_attention(const kvc_bf16* q, const int32_t* ch, const kvc_
 
 kvc_status kvc_zero_add_back(const kvc_bf16* Kp, const kvc_kv_desc* pd, const int32_t* ch, kvc_bf16* K_out,
                              const kvc_kv_desc* od, kvc_stream_t stream) {
+  KVC_RANGE();
   KVC_TRY(check_desc(pd, "kvc_zero_add_back (Kp)"));
   KVC_TRY(check_desc(od, "kvc_zero_add_back (K_out)"));
   if (pd->B != od->B || pd->KVH != od->KVH || pd->S != od->S)
@@ -645,6 +676,7 @@ kvc_status kvc_zero_add_back(const kvc_bf16* Kp, const kvc_kv_desc* pd, const in
 }
 
 kvc_status kvc_host_device_pointer(const void* host_ptr, void** dev_ptr) {
+  KVC_RANGE();
   if (!host_ptr || !dev_ptr) return fail(KVC_ERR_INVALID_ARG, "kvc_host_device_pointer: NULL argument");
   *dev_ptr = nullptr;
   cudaPointerAttributes at{};
@@ -663,6 +695,7 @@ kvc_status kvc_host_device_pointer(const void* host_ptr, void** dev_ptr) {
 }
 
 kvc_status kvc_get_device_status(kvc_stream_t stream) {
+  KVC_RANGE();
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_status(e, "kvc_get_device_status sync");
   cudaError_t (*takers[])(unsigned int*) = {take_status_scores,       take_status_scores_tc, take_status_select,
