@@ -106,14 +106,18 @@ __device__ __forceinline__ void acc_sq8(float* acc, uint4 v) {
 }
 
 // partial sums of squares over one range of rows, weighted by wts[b*KVH+kvh][row] when
-// given: part[split][b*KVH+kvh][D]
+// given: part[split][b*KVH+kvh][D].  With q given, the CTA also sums q^2 over its share of the
+// group's window rows (rows split, split + nsplit, ...): qpart[split][b*KVH+kvh][D], so that
+// the final step reads two partials per split and nothing else.
 template <int D>
 __global__ void __launch_bounds__(256) k_channel_partial(const uint16_t* __restrict__ K, int64_t sb,
                                                          int64_t sh, int64_t ss, int64_t S,
                                                          const int32_t* __restrict__ idx, int k,
                                                          int64_t nrows, int64_t chunk,
                                                          float* __restrict__ part, int KVH,
-                                                         const float* __restrict__ wts) {
+                                                         const float* __restrict__ wts,
+                                                         const uint16_t* __restrict__ q, int H, int w,
+                                                         float* __restrict__ qpart) {
   pdl_wait();  // previous kernel on the stream complete and visible
   constexpr int TPR = D / 8;
   constexpr int RPP = 256 / TPR;  // rows per pass
@@ -164,8 +168,32 @@ __global__ void __launch_bounds__(256) k_channel_partial(const uint16_t* __restr
   __syncthreads();
   for (int d = threadIdx.x; d < D; d += 256) {
     float s = 0.f;
-    for (int q = 0; q < RPP; ++q) s += red[q][d];
+    for (int rr = 0; rr < RPP; ++rr) s += red[rr][d];
     part[((int64_t)split * gridDim.z * KVH + bk) * D + d] = s;
+  }
+  if (q == nullptr) return;
+  // the group's G*w window rows are contiguous: [b][kvh*G .. kvh*G + G)[w][D]
+  const int G = H / KVH, nq = G * w, ns = gridDim.x;
+  const uint16_t* qg = q + ((int64_t)(b * H + kvh * G) * w) * D;
+  float qa[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int r0 = split + rl * ns; r0 < nq; r0 += U * RPP * ns) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int r = r0 + u * RPP * ns;
+      v[u] = r < nq ? ld16(qg + (int64_t)r * D + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc_sq8(qa, v[u]);
+  }
+  __syncthreads();  // red is reused
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[rl][c * 8 + i] = qa[i];
+  __syncthreads();
+  for (int d = threadIdx.x; d < D; d += 256) {
+    float s = 0.f;
+    for (int rr = 0; rr < RPP; ++rr) s += red[rr][d];
+    qpart[((int64_t)split * gridDim.z * KVH + bk) * D + d] = s;
   }
 }
 
@@ -180,40 +208,33 @@ __global__ void __launch_bounds__(256) k_channel_sum(const float* __restrict__ p
   }
 }
 
-// one 1024-thread CTA per (b, kvh): thread (grp, d) sums q^2 over every ngrp-th window row of
-// the group and every ngrp-th key-range partial, then the groups are added in shared memory
-__global__ void __launch_bounds__(1024) k_channel_final(const uint16_t* __restrict__ q, int H, int KVH, int w,
-                                                        int D, const float* __restrict__ part, int nsplit, int B,
-                                                        float* __restrict__ cs) {
+// one CTA per (b, kvh): thread (grp, d) adds every ngrp-th split's key and query partials of
+// channel d, all of its loads in flight at once; the groups are then added in shared memory
+// in group order, and cs = (query sum / G) * key sum
+__global__ void __launch_bounds__(1024) k_channel_final(const float* __restrict__ part,
+                                                        const float* __restrict__ qpart, int nsplit, int B,
+                                                        int KVH, int G, int D, float* __restrict__ cs) {
   pdl_wait();  // previous kernel on the stream complete and visible
   __shared__ float qred[16][128];
   __shared__ float kred[16][128];
   const int bk = blockIdx.x;
-  const int b = bk / KVH, kvh = bk % KVH;
-  const int G = H / KVH;
   const int d = threadIdx.x % D, grp = threadIdx.x / D, ngrp = blockDim.x / D;
-  const uint16_t* qg = q + ((int64_t)(b * H + kvh * G) * w) * D + d;  // the group's G*w rows are contiguous
-  float sq = 0.f, kn = 0.f;
-  // eight independent loads in flight per step (the rows and partials are strided)
-  for (int r = grp; r < G * w; r += 8 * ngrp) {
-    float v[8];
+  constexpr int BATCH = 16;
+  float kn = 0.f, sq = 0.f;
+  for (int s0 = grp; s0 < nsplit; s0 += BATCH * ngrp) {
+    float kv[BATCH], qv[BATCH];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int rr = r + u * ngrp;
-      v[u] = rr < G * w ? __uint_as_float((uint32_t)__ldg(qg + (int64_t)rr * D) << 16) : 0.f;
+    for (int u = 0; u < BATCH; ++u) {
+      const int sp = s0 + u * ngrp;
+      const int64_t o = ((int64_t)sp * B * KVH + bk) * D + d;
+      kv[u] = sp < nsplit ? __ldg(part + o) : 0.f;
+      qv[u] = sp < nsplit ? __ldg(qpart + o) : 0.f;
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) sq = fmaf(v[u], v[u], sq);
-  }
-  for (int s = grp; s < nsplit; s += 8 * ngrp) {
-    float v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int ss = s + u * ngrp;
-      v[u] = ss < nsplit ? __ldg(part + ((int64_t)ss * B * KVH + bk) * D + d) : 0.f;
+    for (int u = 0; u < BATCH; ++u) {
+      kn += kv[u];
+      sq += qv[u];
     }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) kn += v[u];
   }
   qred[grp][d] = sq;
   kred[grp][d] = kn;
@@ -369,9 +390,11 @@ cudaError_t launch_weighted_channel_norm(const float* wts, const uint16_t* V, co
   const dim3 grid(ns, kv.KVH, kv.B);
   cudaError_t e =
       kv.D == 64 ? launch_pdl(k_channel_partial<64>, grid, dim3(256), 0, st, V, kv.stride_b, kv.stride_h, kv.stride_s,
-                              kv.S, (const int32_t*)nullptr, 0, kv.S, chunk, part, kv.KVH, wts)
+                              kv.S, (const int32_t*)nullptr, 0, kv.S, chunk, part, kv.KVH, wts,
+                              (const uint16_t*)nullptr, 0, 0, (float*)nullptr)
                  : launch_pdl(k_channel_partial<128>, grid, dim3(256), 0, st, V, kv.stride_b, kv.stride_h, kv.stride_s,
-                              kv.S, (const int32_t*)nullptr, 0, kv.S, chunk, part, kv.KVH, wts);
+                              kv.S, (const int32_t*)nullptr, 0, kv.S, chunk, part, kv.KVH, wts,
+                              (const uint16_t*)nullptr, 0, 0, (float*)nullptr);
   if (e != cudaSuccess) return e;
   const int64_t n = (int64_t)kv.B * kv.KVH * kv.D;
   e = launch_pdl(k_channel_sum, dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 1024))),
@@ -394,10 +417,11 @@ cudaError_t launch_write_slots(const uint16_t* kn, const uint16_t* vn, const int
   return launched(1);
 }
 
+// key partials, then query partials: [2][nsplit][B*KVH][D] floats
 size_t channel_score_workspace(const kvc_kv_desc& kv, int k, bool has_idx) {
   const int64_t nrows = has_idx ? k : kv.S;
   const int ns = channel_splits(kv, nrows);
-  return (size_t)ns * kv.B * kv.KVH * kv.D * sizeof(float);
+  return 2 * (size_t)ns * kv.B * kv.KVH * kv.D * sizeof(float);
 }
 
 cudaError_t launch_channel_score(const uint16_t* q, int w, const uint16_t* K, const kvc_kv_desc& kv,
@@ -406,14 +430,16 @@ cudaError_t launch_channel_score(const uint16_t* q, int w, const uint16_t* K, co
   const int ns = channel_splits(kv, nrows);
   const int64_t chunk = (nrows + ns - 1) / ns;
   float* part = static_cast<float*>(ws);
+  float* qpart = part + (size_t)ns * kv.B * kv.KVH * kv.D;
   dim3 grid(ns, kv.KVH, kv.B);
   cudaError_t e =
       kv.D == 64 ? launch_pdl(k_channel_partial<64>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
-                              kv.S, idx, k, nrows, chunk, part, kv.KVH, (const float*)nullptr)
+                              kv.S, idx, k, nrows, chunk, part, kv.KVH, (const float*)nullptr, q, kv.H, w, qpart)
                  : launch_pdl(k_channel_partial<128>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
-                              kv.S, idx, k, nrows, chunk, part, kv.KVH, (const float*)nullptr);
+                              kv.S, idx, k, nrows, chunk, part, kv.KVH, (const float*)nullptr, q, kv.H, w, qpart);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(k_channel_final, dim3(kv.B * kv.KVH), dim3(1024), 0, st, q, kv.H, kv.KVH, w, kv.D, part, ns, kv.B, cs);
+  e = launch_pdl(k_channel_final, dim3(kv.B * kv.KVH), dim3(1024), 0, st, (const float*)part, (const float*)qpart, ns,
+                 kv.B, kv.KVH, kv.H / kv.KVH, kv.D, cs);
   if (e != cudaSuccess) return e;
   return launched(2);
 }
