@@ -140,6 +140,10 @@ TOPK_CASES = [
     (1, 2, 131072, 8192, 64, 0, True, None),
     (2, 1, 40000, 5000, 32, 3, True, 0.7),
     (1, 1, 327680, 1000, 0, 0, False, None),
+    # long rows (8-CTA clusters of 8-25K keys each): live masks, ties, k close to S
+    (2, 1, 100000, 5000, 32, 3, True, 0.7),
+    (1, 2, 70000, 69000, 0, 0, True, None),
+    (1, 1, 200000, 100, 0, 50, False, 0.5),
     (1, 2, 6000, 5999, 0, 0, True, None),
     (4, 2, 2049, 1, 0, 0, False, None),
     (4, 2, 2049, 1, 0, 3, False, None),
