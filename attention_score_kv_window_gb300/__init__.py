@@ -7,8 +7,8 @@ the GPU; the first call loads the library and raises if it has not been built.
 from ._binding import (  # noqa: F401
     KvcError, KvDesc, ShState, ScissorhandsState, LIB_PATH, exported_symbols, load_library, kv_desc,
     host_device_pointer,
-    kvc_window_scores, kvc_window_scores_noalloc, kvc_topk_select, kvc_compact_kv, kvc_topk_compact,
-    kvc_compress_prefill, kvc_write_slots,
+    kvc_window_scores, kvc_window_scores_noalloc, kvc_topk_select, kvc_compact_kv, kvc_topk_compact, kvc_topk_compact_channels,
+    kvc_compress_prefill, kvc_compress_prefill_channels, kvc_write_slots,
     kvc_tova_decode_step, kvc_scissorhands_init, kvc_scissorhands_update,
     kvc_scissorhands_update_from_probs, kvc_scissorhands_evict, kvc_scissorhands_refill_queue,
     kvc_scissorhands_insert, kvc_channel_score, kvc_channel_prune, kvc_decode_attention, kvc_zero_add_back,

@@ -20,7 +20,7 @@ KVC_OK, KVC_ERR_INVALID_ARG, KVC_ERR_UNSUPPORTED, KVC_ERR_CUDA, KVC_ERR_TIMEOUT,
 KVC_REDUCE_GQA_GROUP, KVC_REDUCE_ALL_HEADS = 0, 1
 (KVC_OP_WINDOW_SCORES, KVC_OP_TOPK_SELECT, KVC_OP_COMPRESS_PREFILL, KVC_OP_TOVA_DECODE_STEP,
  KVC_OP_SCISSORHANDS_UPDATE, KVC_OP_SCISSORHANDS_EVICT, KVC_OP_CHANNEL_SCORE, KVC_OP_DECODE_ATTENTION,
- KVC_OP_VALUE_CHANNEL_SCORE) = range(9)
+ KVC_OP_VALUE_CHANNEL_SCORE, KVC_OP_COMPRESS_PREFILL_CHANNELS, KVC_OP_TOPK_COMPACT_CHANNELS) = range(11)
 
 REDUCE = {"gqa": KVC_REDUCE_GQA_GROUP, "all_heads": KVC_REDUCE_ALL_HEADS}
 
@@ -61,7 +61,11 @@ _SIGNATURES = {
     "kvc_topk_select": (_I32, [_P, _I32, _I32, _I64, _I32, _I32, _P, _I32, _P, _P, _SZ, _P]),
     "kvc_compact_kv": (_I32, [_P, _P, _DESC, _P, _I32, _P, _P, _P]),
     "kvc_topk_compact": (_I32, [_P, _P, _P, _DESC, _I32, _I32, _P, _I32, _P, _P, _P, _P]),
+    "kvc_topk_compact_channels": (_I32, [_P, _P, _P, _DESC, _I32, _I32, _P, _I32, _P, _P, _P, _P, _I32, _P, _P, _SZ,
+                                         _P]),
     "kvc_compress_prefill": (_I32, [_P, _P, _P, _DESC, _I32, _F, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "kvc_compress_prefill_channels": (_I32, [_P, _P, _P, _DESC, _I32, _F, _I32, _I32, _I32, _P, _P, _P, _P, _P, _P,
+                                             _SZ, _P]),
     "kvc_write_slots": (_I32, [_P, _P, _P, _P, _P, _DESC, _P]),
     "kvc_tova_decode_step": (_I32, [_P, _P, _P, _P, _P, _DESC, _F, _P, _P, _P, _SZ, _P]),
     "kvc_scissorhands_init": (_I32, [_SH, _I32, _P]),
@@ -269,6 +273,37 @@ def kvc_topk_compact(scores, K, V, k, protect_tail=0, live_mask=None, largest=Tr
     return idx, K_out, V_out
 
 
+def kvc_topk_compact_channels(scores, K, V, k, q_win, protect_tail=0, live_mask=None, largest=True, idx=None,
+                              K_out=None, V_out=None, cs=None, ws=None, stream=None):
+    """kvc_topk_compact plus ThinK's key-channel scores of the kept keys (summed by the
+    compaction; ``q_win`` [B,H,w,D] the window queries).  Returns (idx, K_out, V_out, cs)."""
+    lib = load_library()
+    if scores.dtype != torch.float32:
+        raise TypeError("scores must be float32")
+    B, KVH, S, D = K.shape
+    H, w = q_win.shape[1], q_win.shape[2]
+    desc = kv_desc(K, H)
+    if V is not None and (V.shape != K.shape or V.stride() != K.stride()):
+        raise ValueError("V must have K's shape and strides")
+    if idx is None:
+        idx = torch.empty((B, KVH, k), dtype=torch.int32, device=K.device)
+    if K_out is None:
+        K_out = torch.empty((B, KVH, k, D), dtype=K.dtype, device=K.device)
+    if V is not None and V_out is None:
+        V_out = torch.empty((B, KVH, k, D), dtype=V.dtype, device=K.device)
+    _dense(K_out, (B, KVH, k, D), "K_out")
+    if V_out is not None:
+        _dense(V_out, (B, KVH, k, D), "V_out")
+    if cs is None:
+        cs = torch.empty((B, KVH, D), dtype=torch.float32, device=K.device)
+    ws, nbytes = _ws(KVC_OP_TOPK_COMPACT_CHANNELS, desc, 0, k, ws, K.device)
+    _check(lib.kvc_topk_compact_channels(_ptr(scores.contiguous()), _ptr(K), _vptr(V), ctypes.byref(desc), int(k),
+                                         int(protect_tail), _ptr(live_mask), int(bool(largest)), _ptr(idx),
+                                         _ptr(K_out), _ptr(V_out), _ptr(q_win.contiguous()), int(w), _ptr(cs),
+                                         _ptr(ws), nbytes, _stream(stream)))
+    return idx, K_out, V_out, cs
+
+
 def kvc_compress_prefill(q_win, K, V, scale, k, protect_tail=0, reduce="gqa", out=None, ws=None,
                          stream=None, keep_scores=True):
     """Returns (scores, idx, K_out, V_out).  ``keep_scores=False`` (or ``out`` with scores
@@ -291,6 +326,33 @@ def kvc_compress_prefill(q_win, K, V, scale, k, protect_tail=0, reduce="gqa", ou
                                     float(scale), REDUCE[reduce], int(k), int(protect_tail), _ptr(scores),
                                     _ptr(idx), _ptr(K_out), _ptr(V_out), _ptr(ws), nbytes, _stream(stream)))
     return scores, idx, K_out, V_out
+
+
+def kvc_compress_prefill_channels(q_win, K, V, scale, k, protect_tail=0, reduce="gqa", out=None, cs=None, ws=None,
+                                  stream=None, keep_scores=True):
+    """kvc_compress_prefill plus ThinK's key-channel scores of the kept keys, summed by the
+    compaction.  Returns (scores, idx, K_out, V_out, cs) with cs [B,KVH,D] float32."""
+    lib = load_library()
+    B, H, w, D = q_win.shape
+    _, KVH, S, _ = K.shape
+    desc = kv_desc(K, H)
+    if V is not None and (V.shape != K.shape or V.stride() != K.stride()):
+        raise ValueError("V must have K's shape and strides")
+    dev = K.device
+    if out is None:
+        out = (torch.empty((B, KVH, S), dtype=torch.float32, device=dev) if keep_scores else None,
+               torch.empty((B, KVH, k), dtype=torch.int32, device=dev),
+               torch.empty((B, KVH, k, D), dtype=K.dtype, device=dev),
+               torch.empty((B, KVH, k, D), dtype=K.dtype, device=dev) if V is not None else None)
+    scores, idx, K_out, V_out = out
+    if cs is None:
+        cs = torch.empty((B, KVH, D), dtype=torch.float32, device=dev)
+    ws, nbytes = _ws(KVC_OP_COMPRESS_PREFILL_CHANNELS, desc, w, k, ws, dev)
+    _check(lib.kvc_compress_prefill_channels(_ptr(q_win.contiguous()), _ptr(K), _vptr(V), ctypes.byref(desc), w,
+                                             float(scale), REDUCE[reduce], int(k), int(protect_tail), _ptr(scores),
+                                             _ptr(idx), _ptr(K_out), _ptr(V_out), _ptr(cs), _ptr(ws), nbytes,
+                                             _stream(stream)))
+    return scores, idx, K_out, V_out, cs
 
 
 def kvc_write_slots(k_new, v_new, slot, K, V, H=None, stream=None):

@@ -198,6 +198,13 @@ size_t kvc_workspace_size(kvc_op op, const kvc_kv_desc* kv, int32_t w, int32_t k
     case KVC_OP_WINDOW_SCORES:
       if (check_window(kv, w, "kvc_workspace_size") != KVC_OK) return (size_t)-1;
       return scores_workspace(*kv, w, KVC_REDUCE_ALL_HEADS);
+    case KVC_OP_TOPK_COMPACT_CHANNELS:
+      if (check_desc(kv, "kvc_workspace_size") != KVC_OK || k < 1) return (size_t)-1;
+      return compact_channels_workspace(*kv, k);
+    case KVC_OP_COMPRESS_PREFILL_CHANNELS:
+      if (check_window(kv, w, "kvc_workspace_size") != KVC_OK) return (size_t)-1;
+      return (scores_workspace(*kv, w, KVC_REDUCE_ALL_HEADS) + 255) / 256 * 256 +
+             ((size_t)kv->B * kv->KVH * kv->S * sizeof(float) + 255) / 256 * 256 + compact_channels_workspace(*kv, k);
     case KVC_OP_COMPRESS_PREFILL:
       if (check_window(kv, w, "kvc_workspace_size") != KVC_OK) return (size_t)-1;
       // the fused short-row kernel needs none; otherwise the window-score scratch plus room
@@ -322,16 +329,25 @@ kvc_status kvc_compact_kv(const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_des
   return cuda_status(launch_compact(K, V, *kv, idx, k, K_out, V_out, (cudaStream_t)stream), "kvc_compact_kv launch");
 }
 
-kvc_status kvc_topk_compact(const float* scores, const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_desc* kv,
-                            int32_t k, int32_t protect_tail, const uint32_t* live_mask, int32_t largest,
-                            int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out, kvc_stream_t stream) {
-  KVC_RANGE();
-  KVC_TRY(check_gather(K, V, kv, k, K_out, V_out, "kvc_topk_compact"));
-  if (kv->S > topk_max_len()) return fail(KVC_ERR_UNSUPPORTED, "kvc_topk_compact: S > %lld", (long long)topk_max_len());
-  if ((int64_t)kv->B * kv->KVH > 2147483647LL) return fail(KVC_ERR_UNSUPPORTED, "kvc_topk_compact: too many rows");
+// kvc_topk_compact, and with channel_scores also ThinK's key-channel scores of the kept keys
+// (kvc_topk_compact_channels)
+static kvc_status topk_compact_impl(const char* who, const float* scores, const kvc_bf16* K, const kvc_bf16* V,
+                                    const kvc_kv_desc* kv, int32_t k, int32_t protect_tail,
+                                    const uint32_t* live_mask, int32_t largest, int32_t* idx, kvc_bf16* K_out,
+                                    kvc_bf16* V_out, const kvc_bf16* q_win, int32_t w, float* channel_scores,
+                                    void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_TRY(check_gather(K, V, kv, k, K_out, V_out, who));
+  if (kv->S > topk_max_len()) return fail(KVC_ERR_UNSUPPORTED, "%s: S > %lld", who, (long long)topk_max_len());
+  if ((int64_t)kv->B * kv->KVH > 2147483647LL) return fail(KVC_ERR_UNSUPPORTED, "%s: too many rows", who);
   if (protect_tail < 0 || protect_tail > k || (int64_t)protect_tail > kv->S)
-    return fail(KVC_ERR_INVALID_ARG, "kvc_topk_compact: need 0 <= protect_tail <= min(k, S)");
-  if (protect_tail && !largest) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_compact: protect_tail needs largest=1");
+    return fail(KVC_ERR_INVALID_ARG, "%s: need 0 <= protect_tail <= min(k, S)", who);
+  if (protect_tail && !largest) return fail(KVC_ERR_INVALID_ARG, "%s: protect_tail needs largest=1", who);
+  if (channel_scores) {
+    if (w < 1) return fail(KVC_ERR_INVALID_ARG, "%s: w must be >= 1", who);
+    KVC_TRY(check_ptr(q_win, "q_win"));
+    if (!aligned16(channel_scores)) return fail(KVC_ERR_INVALID_ARG, "channel_scores is not 16-byte aligned");
+    KVC_TRY(check_ws(ws, ws_bytes, compact_channels_workspace(*kv, k), who));
+  }
   KVC_TRY(check_ptr(scores, "scores"));
   if (!idx) return fail(KVC_ERR_INVALID_ARG, "idx is NULL");
   if (live_mask && !aligned16(live_mask)) return fail(KVC_ERR_INVALID_ARG, "live_mask not 16-byte aligned");
@@ -343,36 +359,69 @@ kvc_status kvc_topk_compact(const float* scores, const kvc_bf16* K, const kvc_bf
   const uintptr_t i0 = reinterpret_cast<uintptr_t>(idx), i1 = i0 + (uintptr_t)kv->B * kv->KVH * k * 4;
   if (overlaps(ko, ko + osz, s0, s1) || (V_out && overlaps(vo, vo + osz, s0, s1)) || overlaps(i0, i1, s0, s1) ||
       overlaps(i0, i1, ko, ko + osz) || (V_out && overlaps(i0, i1, vo, vo + osz)))
-    return fail(KVC_ERR_INVALID_ARG, "kvc_topk_compact: outputs overlap inputs or each other");
+    return fail(KVC_ERR_INVALID_ARG, "%s: outputs overlap inputs or each other", who);
+  if (channel_scores) {
+    const uintptr_t c0 = reinterpret_cast<uintptr_t>(channel_scores), c1 = c0 + (uintptr_t)kv->B * kv->KVH * kv->D * 4;
+    uintptr_t k0, k1;
+    cache_range(K, *kv, &k0, &k1);
+    if (overlaps(c0, c1, s0, s1) || overlaps(c0, c1, ko, ko + osz) || (V_out && overlaps(c0, c1, vo, vo + osz)) ||
+        overlaps(c0, c1, i0, i1) || overlaps(c0, c1, k0, k1))
+      return fail(KVC_ERR_INVALID_ARG, "%s: channel_scores overlaps another argument", who);
+  }
   // two launches chained by programmatic dependent launch: the gather then runs on every SM
   // (a gather inside the selection grid, on its B*KVH*8 CTAs, measured slower)
   KVC_TRY(cuda_status(launch_topk(scores, kv->B, kv->KVH, kv->S, k, protect_tail, live_mask, largest ? 1 : 0, idx,
                                   (cudaStream_t)stream),
-                      "kvc_topk_compact selection launch"));
-  return cuda_status(launch_compact(K, V, *kv, idx, k, K_out, V_out, (cudaStream_t)stream),
-                     "kvc_topk_compact gather launch");
+                      "selection launch"));
+  if (channel_scores)
+    return cuda_status(launch_compact_channels(K, V, *kv, idx, k, K_out, V_out, q_win, w, channel_scores, ws,
+                                               (cudaStream_t)stream),
+                       "gather launch");
+  return cuda_status(launch_compact(K, V, *kv, idx, k, K_out, V_out, (cudaStream_t)stream), "gather launch");
 }
 
-kvc_status kvc_compress_prefill(const kvc_bf16* q_win, const kvc_bf16* K, const kvc_bf16* V,
-                                const kvc_kv_desc* kv, int32_t w, float scale,
-                                kvc_head_reduce reduce, int32_t k, int32_t protect_tail,
-                                float* scores, int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out,
-                                void* ws, size_t ws_bytes, kvc_stream_t stream) {
+kvc_status kvc_topk_compact(const float* scores, const kvc_bf16* K, const kvc_bf16* V, const kvc_kv_desc* kv,
+                            int32_t k, int32_t protect_tail, const uint32_t* live_mask, int32_t largest,
+                            int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out, kvc_stream_t stream) {
   KVC_RANGE();
-  const char* who = "kvc_compress_prefill";
+  return topk_compact_impl("kvc_topk_compact", scores, K, V, kv, k, protect_tail, live_mask, largest, idx, K_out,
+                           V_out, nullptr, 0, nullptr, nullptr, 0, stream);
+}
+
+kvc_status kvc_topk_compact_channels(const float* scores, const kvc_bf16* K, const kvc_bf16* V,
+                                     const kvc_kv_desc* kv, int32_t k, int32_t protect_tail,
+                                     const uint32_t* live_mask, int32_t largest, int32_t* idx, kvc_bf16* K_out,
+                                     kvc_bf16* V_out, const kvc_bf16* q_win, int32_t w, float* channel_scores,
+                                     void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_RANGE();
+  if (!channel_scores) return fail(KVC_ERR_INVALID_ARG, "kvc_topk_compact_channels: channel_scores is NULL");
+  KVC_TRY(check_desc(kv, "kvc_topk_compact_channels"));
+  return topk_compact_impl("kvc_topk_compact_channels", scores, K, V, kv, k, protect_tail, live_mask, largest, idx,
+                           K_out, V_out, q_win, w, channel_scores, ws, ws_bytes, stream);
+}
+
+// kvc_compress_prefill, and with channel_scores also ThinK's key-channel scores of the kept
+// keys, summed by the compaction as it reads them (kvc_compress_prefill_channels)
+static kvc_status compress_prefill_impl(const char* who, const kvc_bf16* q_win, const kvc_bf16* K,
+                                        const kvc_bf16* V, const kvc_kv_desc* kv, int32_t w, float scale,
+                                        kvc_head_reduce reduce, int32_t k, int32_t protect_tail, float* scores,
+                                        int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out, float* channel_scores,
+                                        void* ws, size_t ws_bytes, kvc_stream_t stream) {
   KVC_TRY(check_desc(kv, who));
-  if (k < 1) return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill: k must be >= 1");
+  if (k < 1) return fail(KVC_ERR_INVALID_ARG, "%s: k must be >= 1", who);
   KVC_TRY(check_window(kv, w, who));
   if (protect_tail < 0 || protect_tail > k || protect_tail > w)
-    return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill: need 0 <= protect_tail <= min(k, w)");
+    return fail(KVC_ERR_INVALID_ARG, "%s: need 0 <= protect_tail <= min(k, w)", who);
   if (reduce != KVC_REDUCE_GQA_GROUP && reduce != KVC_REDUCE_ALL_HEADS)
     return fail(KVC_ERR_INVALID_ARG, "unknown head reduction");
   if (!(scale > 0.f) || scale != scale) return fail(KVC_ERR_INVALID_ARG, "scale must be > 0");
   KVC_TRY(check_ptr(q_win, "q_win"));
   KVC_TRY(check_gather(K, V, kv, k, K_out, V_out, who));
-  if (kv->S > topk_max_len()) return fail(KVC_ERR_UNSUPPORTED, "kvc_compress_prefill: S > %lld", (long long)topk_max_len());
+  if (kv->S > topk_max_len()) return fail(KVC_ERR_UNSUPPORTED, "%s: S > %lld", who, (long long)topk_max_len());
   KVC_TRY(check_ptr(idx, "idx"));
   if (scores && !aligned16(scores)) return fail(KVC_ERR_INVALID_ARG, "scores is not 16-byte aligned");
+  if (channel_scores && !aligned16(channel_scores))
+    return fail(KVC_ERR_INVALID_ARG, "channel_scores is not 16-byte aligned");
   {  // no output may overlap another output or an input
     const uintptr_t osz = (uintptr_t)kv->B * kv->KVH * (uintptr_t)k * kv->D * 2;
     const uintptr_t ko = reinterpret_cast<uintptr_t>(K_out), vo = reinterpret_cast<uintptr_t>(V_out);
@@ -382,27 +431,61 @@ kvc_status kvc_compress_prefill(const kvc_bf16* q_win, const kvc_bf16* K, const 
     if (V) cache_range(V, *kv, &v0, &v1);
     if (overlaps(i0, i1, ko, ko + osz) || (V_out && overlaps(i0, i1, vo, vo + osz)) || overlaps(i0, i1, k0, k1) ||
         (V && overlaps(i0, i1, v0, v1)))
-      return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill: idx overlaps another argument");
+      return fail(KVC_ERR_INVALID_ARG, "%s: idx overlaps another argument", who);
     if (scores) {
       const uintptr_t s0 = reinterpret_cast<uintptr_t>(scores), s1 = s0 + (uintptr_t)kv->B * kv->KVH * kv->S * 4;
       if (overlaps(s0, s1, ko, ko + osz) || (V_out && overlaps(s0, s1, vo, vo + osz)) || overlaps(s0, s1, i0, i1) ||
           overlaps(s0, s1, k0, k1) || (V && overlaps(s0, s1, v0, v1)))
-        return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill: scores overlaps another argument");
+        return fail(KVC_ERR_INVALID_ARG, "%s: scores overlaps another argument", who);
+    }
+    if (channel_scores) {
+      const uintptr_t c0 = reinterpret_cast<uintptr_t>(channel_scores),
+                      c1 = c0 + (uintptr_t)kv->B * kv->KVH * kv->D * 4;
+      const uintptr_t s0 = reinterpret_cast<uintptr_t>(scores), s1 = s0 + (uintptr_t)kv->B * kv->KVH * kv->S * 4;
+      if (overlaps(c0, c1, ko, ko + osz) || (V_out && overlaps(c0, c1, vo, vo + osz)) || overlaps(c0, c1, i0, i1) ||
+          overlaps(c0, c1, k0, k1) || (V && overlaps(c0, c1, v0, v1)) || (scores && overlaps(c0, c1, s0, s1)))
+        return fail(KVC_ERR_INVALID_ARG, "%s: channel_scores overlaps another argument", who);
     }
   }
   // short rows: one fused kernel (scores, selection and compaction per (b, kvh); no workspace)
-  if (prefill_fused_supported(*kv, w, k, reduce))
+  if (!channel_scores && prefill_fused_supported(*kv, w, k, reduce))
     return cuda_status(launch_prefill_fused(q_win, K, V, *kv, w, scale, reduce, k, protect_tail, scores, idx, K_out,
                                             V_out, (cudaStream_t)stream),
                        "kvc_compress_prefill launch");
   // otherwise: window scores (into `scores`, or into the workspace when scores is NULL), then
-  // selection and compaction
+  // selection and compaction; the channel partials follow the scores in the workspace
   const size_t sc_need = (scores_workspace(*kv, w, reduce) + 255) / 256 * 256;
-  const size_t need = scores ? sc_need : sc_need + (size_t)kv->B * kv->KVH * kv->S * sizeof(float);
+  const size_t sc_room = ((size_t)kv->B * kv->KVH * kv->S * sizeof(float) + 255) / 256 * 256;
+  const size_t need = sc_need + (scores ? 0 : sc_room) + (channel_scores ? compact_channels_workspace(*kv, k) : 0);
   KVC_TRY(check_ws(ws, ws_bytes, need, who));
   float* sc = scores ? scores : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sc_need);
   KVC_TRY(kvc_window_scores(q_win, K, kv, w, scale, 1, nullptr, reduce, sc, ws, sc_need, stream));
-  return kvc_topk_compact(sc, K, V, kv, k, protect_tail, nullptr, 1, idx, K_out, V_out, stream);
+  if (!channel_scores) return kvc_topk_compact(sc, K, V, kv, k, protect_tail, nullptr, 1, idx, K_out, V_out, stream);
+  const size_t used = sc_need + (scores ? 0 : sc_room);
+  return topk_compact_impl(who, sc, K, V, kv, k, protect_tail, nullptr, 1, idx, K_out, V_out, q_win, w,
+                           channel_scores, static_cast<uint8_t*>(ws) + used, ws_bytes - used, stream);
+}
+
+kvc_status kvc_compress_prefill(const kvc_bf16* q_win, const kvc_bf16* K, const kvc_bf16* V,
+                                const kvc_kv_desc* kv, int32_t w, float scale,
+                                kvc_head_reduce reduce, int32_t k, int32_t protect_tail,
+                                float* scores, int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out,
+                                void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  KVC_RANGE();
+  return compress_prefill_impl("kvc_compress_prefill", q_win, K, V, kv, w, scale, reduce, k, protect_tail, scores,
+                               idx, K_out, V_out, nullptr, ws, ws_bytes, stream);
+}
+
+kvc_status kvc_compress_prefill_channels(const kvc_bf16* q_win, const kvc_bf16* K, const kvc_bf16* V,
+                                         const kvc_kv_desc* kv, int32_t w, float scale,
+                                         kvc_head_reduce reduce, int32_t k, int32_t protect_tail,
+                                         float* scores, int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out,
+                                         float* channel_scores, void* ws, size_t ws_bytes,
+                                         kvc_stream_t stream) {
+  KVC_RANGE();
+  if (!channel_scores) return fail(KVC_ERR_INVALID_ARG, "kvc_compress_prefill_channels: channel_scores is NULL");
+  return compress_prefill_impl("kvc_compress_prefill_channels", q_win, K, V, kv, w, scale, reduce, k, protect_tail,
+                               scores, idx, K_out, V_out, channel_scores, ws, ws_bytes, stream);
 }
 
 kvc_status kvc_write_slots(const kvc_bf16* k_new, const kvc_bf16* v_new, const int32_t* slot,

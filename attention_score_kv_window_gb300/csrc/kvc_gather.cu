@@ -105,6 +105,108 @@ __device__ __forceinline__ void acc_sq8(float* acc, uint4 v) {
   }
 }
 
+// Query half of the ThinK channel score, one share: the CTA (split of nsplit) of KV head (b,
+// kvh) sums q^2 per channel over the group's window rows split, split + nsplit, ... (the G*w
+// rows are contiguous: [b][kvh*G .. kvh*G + G)[w][D]) and stores qpart[split][b*KVH+kvh][D].
+// 256 threads, TPR per row; red is the caller's [256/TPR][D+1] reduction array, free on entry.
+template <int D>
+__device__ __forceinline__ void q_sq_partial(const uint16_t* __restrict__ q, int H, int w, int KVH, int b, int kvh,
+                                             int split, int nsplit, int nbk, float (*red)[D + 1],
+                                             float* __restrict__ qpart) {
+  constexpr int TPR = D / 8, RPP = 256 / TPR, U = 4;
+  const int c = threadIdx.x % TPR, rl = threadIdx.x / TPR;
+  const int G = H / KVH, nq = G * w;
+  const uint16_t* qg = q + ((int64_t)(b * H + kvh * G) * w) * D;
+  float qa[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int r0 = split + rl * nsplit; r0 < nq; r0 += U * RPP * nsplit) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int r = r0 + u * RPP * nsplit;
+      v[u] = r < nq ? ld16(qg + (int64_t)r * D + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc_sq8(qa, v[u]);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[rl][c * 8 + i] = qa[i];
+  __syncthreads();
+  const int bk = b * KVH + kvh;
+  for (int d = threadIdx.x; d < D; d += 256) {
+    float sum = 0.f;
+    for (int rr = 0; rr < RPP; ++rr) sum += red[rr][d];
+    qpart[((int64_t)split * nbk + bk) * D + d] = sum;
+  }
+}
+
+// Compaction of one (b, kvh)'s kept rows, chunk by chunk (grid: nsplit x B*KVH), that also
+// sums the squares of every kept key per channel: ThinK's key-channel norms come from the
+// compaction's own read of the kept K rows ("Add ThinK_Press": sum_j k_jd^2 over the kept
+// tokens), so no later call reads K_out again.  Each CTA stores its partial sums
+// kpart[split][b*KVH+kvh][D] and the query half of the score (q_sq_partial); warps move 16
+// rows at a time as in k_compact.  Sums are in a fixed order: runs are bit-identical.
+template <int D>
+__global__ void __launch_bounds__(256) k_compact_ksq(const uint16_t* __restrict__ K,
+                                                     const uint16_t* __restrict__ V, int64_t sb, int64_t sh,
+                                                     int64_t ss, int KVH, int64_t S,
+                                                     const int32_t* __restrict__ idx, int k, int64_t chunk,
+                                                     uint16_t* __restrict__ Ko, uint16_t* __restrict__ Vo,
+                                                     float* __restrict__ kpart, const uint16_t* __restrict__ q,
+                                                     int H, int w, float* __restrict__ qpart) {
+  pdl_wait();
+  constexpr int TPR = D / 8, RPI = 32 / TPR, ITER = COMPACT_RPW / RPI, RPP = 256 / TPR;
+  __shared__ float red[RPP][D + 1];
+  const int split = blockIdx.x, bk = blockIdx.y;
+  const int b = bk / KVH, kvh = bk % KVH;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, c = lane % TPR;
+  const int64_t r_beg = (int64_t)split * chunk, r_end = std::min<int64_t>(k, r_beg + chunk);
+  const int64_t row0 = (int64_t)bk * k;  // this (b, kvh)'s first output row
+  const uint16_t* Kb = K + (int64_t)b * sb + (int64_t)kvh * sh;
+  const uint16_t* Vb = V ? V + (int64_t)b * sb + (int64_t)kvh * sh : nullptr;
+  pdl_trigger();
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  for (int64_t r0 = r_beg + (int64_t)warp * COMPACT_RPW; r0 < r_end; r0 += 8 * COMPACT_RPW) {
+    int64_t off = -1;  // lane < 16: source offset of row r0 + lane (-1: zero row)
+    if (lane < COMPACT_RPW && r0 + lane < r_end) {
+      const int32_t j = __ldg(idx + row0 + r0 + lane);
+      if (j >= 0 && j < S) off = (int64_t)j * ss;
+      else if (j >= S || j < -1) set_device_status(KVC_ERR_DEVICE_BOUNDS);
+    }
+    uint4 kv[ITER], vv[ITER];
+#pragma unroll
+    for (int it = 0; it < ITER; ++it) {
+      const int64_t o = __shfl_sync(0xffffffffu, off, it * RPI + lane / TPR);
+      kv[it] = make_uint4(0, 0, 0, 0);
+      vv[it] = kv[it];
+      if (o >= 0) {
+        kv[it] = ld16(Kb + o + c * 8);
+        if (Vb) vv[it] = ld16(Vb + o + c * 8);
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < ITER; ++it) {
+      const int64_t r = r0 + it * RPI + lane / TPR;
+      if (r < r_end) {
+        st16(Ko + (row0 + r) * D + c * 8, kv[it]);
+        if (Vo) st16(Vo + (row0 + r) * D + c * 8, vv[it]);
+      }
+      acc_sq8(acc, kv[it]);  // zero rows add nothing
+    }
+  }
+  // lanes with the same channel block: reduce in shared memory (slot = warp x RPI + lane / TPR)
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[warp * RPI + lane / TPR][c * 8 + i] = acc[i];
+  __syncthreads();
+  const int nbk = gridDim.y;
+  for (int d = threadIdx.x; d < D; d += 256) {
+    float sum = 0.f;
+    for (int rr = 0; rr < RPP; ++rr) sum += red[rr][d];
+    kpart[((int64_t)split * nbk + bk) * D + d] = sum;
+  }
+  __syncthreads();  // red is reused
+  q_sq_partial<D>(q, H, w, KVH, b, kvh, split, gridDim.x, nbk, red, qpart);
+}
+
 // partial sums of squares over one range of rows, weighted by wts[b*KVH+kvh][row] when
 // given: part[split][b*KVH+kvh][D].  With q given, the CTA also sums q^2 over its share of the
 // group's window rows (rows split, split + nsplit, ...): qpart[split][b*KVH+kvh][D], so that
@@ -172,29 +274,8 @@ __global__ void __launch_bounds__(256) k_channel_partial(const uint16_t* __restr
     part[((int64_t)split * gridDim.z * KVH + bk) * D + d] = s;
   }
   if (q == nullptr) return;
-  // the group's G*w window rows are contiguous: [b][kvh*G .. kvh*G + G)[w][D]
-  const int G = H / KVH, nq = G * w, ns = gridDim.x;
-  const uint16_t* qg = q + ((int64_t)(b * H + kvh * G) * w) * D;
-  float qa[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int r0 = split + rl * ns; r0 < nq; r0 += U * RPP * ns) {
-    uint4 v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int r = r0 + u * RPP * ns;
-      v[u] = r < nq ? ld16(qg + (int64_t)r * D + c * 8) : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) acc_sq8(qa, v[u]);
-  }
   __syncthreads();  // red is reused
-#pragma unroll
-  for (int i = 0; i < 8; ++i) red[rl][c * 8 + i] = qa[i];
-  __syncthreads();
-  for (int d = threadIdx.x; d < D; d += 256) {
-    float s = 0.f;
-    for (int rr = 0; rr < RPP; ++rr) s += red[rr][d];
-    qpart[((int64_t)split * gridDim.z * KVH + bk) * D + d] = s;
-  }
+  q_sq_partial<D>(q, H, w, KVH, b, kvh, split, gridDim.x, gridDim.z * KVH, red, qpart);
 }
 
 // cs[b*KVH+kvh][d] = the sum of the key-range partials
@@ -437,6 +518,31 @@ cudaError_t launch_channel_score(const uint16_t* q, int w, const uint16_t* K, co
                               kv.S, idx, k, nrows, chunk, part, kv.KVH, (const float*)nullptr, q, kv.H, w, qpart)
                  : launch_pdl(k_channel_partial<128>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
                               kv.S, idx, k, nrows, chunk, part, kv.KVH, (const float*)nullptr, q, kv.H, w, qpart);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(k_channel_final, dim3(kv.B * kv.KVH), dim3(1024), 0, st, (const float*)part, (const float*)qpart, ns,
+                 kv.B, kv.KVH, kv.H / kv.KVH, kv.D, cs);
+  if (e != cudaSuccess) return e;
+  return launched(2);
+}
+
+// key partials, then query partials, of the compaction that also scores the key channels
+size_t compact_channels_workspace(const kvc_kv_desc& kv, int k) {
+  return 2 * (size_t)channel_splits(kv, k) * kv.B * kv.KVH * kv.D * sizeof(float);
+}
+
+cudaError_t launch_compact_channels(const uint16_t* K, const uint16_t* V, const kvc_kv_desc& kv, const int32_t* idx,
+                                    int k, uint16_t* Ko, uint16_t* Vo, const uint16_t* q, int w, float* cs, void* ws,
+                                    cudaStream_t st) {
+  const int ns = channel_splits(kv, k);
+  const int64_t chunk = (k + ns - 1) / ns;
+  float* part = static_cast<float*>(ws);
+  float* qpart = part + (size_t)ns * kv.B * kv.KVH * kv.D;
+  const dim3 grid(ns, kv.B * kv.KVH);
+  cudaError_t e =
+      kv.D == 64 ? launch_pdl(k_compact_ksq<64>, grid, dim3(256), 0, st, K, V, kv.stride_b, kv.stride_h, kv.stride_s,
+                              kv.KVH, kv.S, idx, k, chunk, Ko, Vo, part, q, kv.H, w, qpart)
+                 : launch_pdl(k_compact_ksq<128>, grid, dim3(256), 0, st, K, V, kv.stride_b, kv.stride_h, kv.stride_s,
+                              kv.KVH, kv.S, idx, k, chunk, Ko, Vo, part, q, kv.H, w, qpart);
   if (e != cudaSuccess) return e;
   e = launch_pdl(k_channel_final, dim3(kv.B * kv.KVH), dim3(1024), 0, st, (const float*)part, (const float*)qpart, ns,
                  kv.B, kv.KVH, kv.H / kv.KVH, kv.D, cs);

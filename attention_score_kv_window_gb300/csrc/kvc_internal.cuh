@@ -265,6 +265,12 @@ cudaError_t launch_compact(const uint16_t* K, const uint16_t* V, const kvc_kv_de
 cudaError_t launch_write_slots(const uint16_t* kn, const uint16_t* vn, const int32_t* slot,
                                uint16_t* K, uint16_t* V, const kvc_kv_desc& kv, cudaStream_t st);
 size_t channel_score_workspace(const kvc_kv_desc& kv, int k, bool has_idx);
+// compaction (as launch_compact) that also writes the ThinK key-channel scores cs [B,KVH,D] of
+// the kept keys; ws: compact_channels_workspace(kv, k) bytes
+size_t compact_channels_workspace(const kvc_kv_desc& kv, int k);
+cudaError_t launch_compact_channels(const uint16_t* K, const uint16_t* V, const kvc_kv_desc& kv, const int32_t* idx,
+                                    int k, uint16_t* Ko, uint16_t* Vo, const uint16_t* q, int w, float* cs, void* ws,
+                                    cudaStream_t st);
 cudaError_t launch_channel_score(const uint16_t* q, int w, const uint16_t* K, const kvc_kv_desc& kv,
                                  const int32_t* idx, int k, float* cs, void* ws, cudaStream_t st);
 cudaError_t launch_channel_prune(const float* cs, const uint16_t* K, const kvc_kv_desc& kv, int C,

@@ -426,12 +426,19 @@ class PrefillCase:
             ]
             self.calls[0].one_pass_flops = sc_flops / 2
         if wl.C:
+            # ThinK: the compaction also sums the kept keys' squares per channel (the key half of
+            # the channel score comes from the same read of the kept K rows); then the prune
             C = wl.C
             self.cs = torch.empty((B, KVH, D), dtype=f32, device=dev)
             self.ch = torch.empty((B, KVH, C), dtype=i32, device=dev)
             self.Kp = torch.empty((B, KVH, k, C), dtype=bf, device=dev)
-            self.calls += [Call("channel_score", self._cscore, B * KVH * k * D * 2 + B * wl.H * wl.w * D * 2),
-                           Call("channel_prune", self._cprune, B * KVH * k * D * 2 + B * KVH * k * C * 2)]
+            self.cws = torch.empty(int(lib.kvc_workspace_size(10, kvc.kv_desc(K0, wl.H), 0, k)), dtype=torch.uint8,
+                                   device=dev)
+            assert not self.fused
+            tc = self.calls[1]
+            self.calls[1] = Call("topk_compact_channels", self._topk_compact_ch,
+                                 tc.nbytes + B * wl.H * wl.w * D * 2 + B * KVH * D * 4)
+            self.calls += [Call("channel_prune", self._cprune, B * KVH * k * D * 2 + B * KVH * k * C * 2)]
         if wl.extra.get("values"):  # value channels too: score over the compressed cache, then prune
             C = wl.C
             self.vcs = torch.empty((B, KVH, D), dtype=f32, device=dev)
@@ -461,9 +468,11 @@ class PrefillCase:
         self.kvc.kvc_topk_compact(sc, K, V, self.k, protect_tail=self.wl.protect_tail, H=self.wl.H, idx=idx,
                                   K_out=Ko, V_out=Vo)
 
-    def _cscore(self, i):
-        q, _, _ = self.reps[i % self.R]
-        self.kvc.kvc_channel_score(q, self.outs[i % self.R][2], cs=self.cs)
+    def _topk_compact_ch(self, i):
+        q, K, V = self.reps[i % self.R]
+        sc, idx, Ko, Vo = self.outs[i % self.R]
+        self.kvc.kvc_topk_compact_channels(sc, K, V, self.k, q, protect_tail=self.wl.protect_tail, idx=idx, K_out=Ko,
+                                           V_out=Vo, cs=self.cs, ws=self.cws)
 
     def _cprune(self, i):
         self.kvc.kvc_channel_prune(self.cs, self.outs[i % self.R][2], self.wl.C, ch_idx=self.ch, K_out=self.Kp,

@@ -74,7 +74,9 @@ typedef enum {
   KVC_OP_SCISSORHANDS_EVICT = 5,
   KVC_OP_CHANNEL_SCORE = 6,
   KVC_OP_DECODE_ATTENTION = 7,
-  KVC_OP_VALUE_CHANNEL_SCORE = 8
+  KVC_OP_VALUE_CHANNEL_SCORE = 8,
+  KVC_OP_COMPRESS_PREFILL_CHANNELS = 9,
+  KVC_OP_TOPK_COMPACT_CHANNELS = 10
 } kvc_op;
 
 /* Bytes of scratch the call `op` needs for these shapes on the current device (w: window
@@ -188,6 +190,23 @@ kvc_status kvc_topk_compact(const float* scores, const kvc_bf16* K, const kvc_bf
                             kvc_bf16* K_out, kvc_bf16* V_out, kvc_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
+ * kvc_topk_compact_channels — kvc_topk_compact, and ThinK's key-channel scores of the kept
+ * keys ("Add ThinK_Press", kvpress PR 18: the group's window queries' squared norm per channel,
+ * averaged over the group's heads, times the kept keys' squared norm per channel; as
+ * kvc_channel_score with idx = the kept rows).  The compaction sums the kept keys' squares as
+ * it reads them, so K_out is not read again; one small kernel then forms the scores.
+ *   Arguments as kvc_topk_compact, plus q_win [B,H,w,D] bf16 (the window queries, kv.H heads)
+ *   and channel_scores [B,KVH,D] float32 out (16-byte aligned, overlapping no other argument).
+ *   ws: kvc_workspace_size(KVC_OP_TOPK_COMPACT_CHANNELS, kv, 0, k) bytes, any content.  Rows
+ *   whose index is -1 add nothing to the key norms.
+ * ------------------------------------------------------------------------------------- */
+kvc_status kvc_topk_compact_channels(const float* scores, const kvc_bf16* K, const kvc_bf16* V,
+                                     const kvc_kv_desc* kv, int32_t k, int32_t protect_tail,
+                                     const uint32_t* live_mask, int32_t largest, int32_t* idx, kvc_bf16* K_out,
+                                     kvc_bf16* V_out, const kvc_bf16* q_win, int32_t w, float* channel_scores,
+                                     void* ws, size_t ws_bytes, kvc_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
  * kvc_compress_prefill — window scores, top-k and compaction in one call: the press applied
  * after the prefill attention of one layer.  "Add TOVA press" (kvpress PR 12): score the
  * cached tokens by the last query rows' attention averaged over heads and keep the best;
@@ -209,6 +228,27 @@ kvc_status kvc_compress_prefill(const kvc_bf16* q_win, const kvc_bf16* K, const 
                                 kvc_head_reduce reduce, int32_t k, int32_t protect_tail,
                                 float* scores, int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out,
                                 void* ws, size_t ws_bytes, kvc_stream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * kvc_compress_prefill_channels — kvc_compress_prefill, and ThinK's key-channel scores of the
+ * kept keys ("Add ThinK_Press", kvpress PR 18: the channel score is the window queries'
+ * squared norm per channel, averaged over the group's heads, times the kept keys' squared
+ * norm per channel, as in kvc_channel_score with idx = the kept rows).  The key norms are
+ * summed by the compaction while it reads the kept K rows (kvc_topk_compact_channels), so
+ * K_out is not read again.
+ *   Arguments as kvc_compress_prefill, plus channel_scores [B,KVH,D] float32 out (16-byte
+ *   aligned, not NULL, overlapping no other argument).  Always takes the multi-kernel path
+ *   (window scores, top-k, compaction with the channel sums, one small final kernel).
+ *   ws: kvc_workspace_size(KVC_OP_COMPRESS_PREFILL_CHANNELS, kv, w, k) bytes (k must be the
+ *   call's k), including room for the scores when scores is NULL.  Rows whose index is -1
+ *   (fewer than k tokens) add nothing to the key norms.
+ * ------------------------------------------------------------------------------------- */
+kvc_status kvc_compress_prefill_channels(const kvc_bf16* q_win, const kvc_bf16* K, const kvc_bf16* V,
+                                         const kvc_kv_desc* kv, int32_t w, float scale,
+                                         kvc_head_reduce reduce, int32_t k, int32_t protect_tail,
+                                         float* scores, int32_t* idx, kvc_bf16* K_out, kvc_bf16* V_out,
+                                         float* channel_scores, void* ws, size_t ws_bytes,
+                                         kvc_stream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * kvc_write_slots — the decode-step insertion into a fixed-size cache: the new token's key and

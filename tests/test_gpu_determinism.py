@@ -138,6 +138,14 @@ def test_scissorhands_repeatable(policy):
     _same(runs)
 
 
+def test_compress_prefill_channels_repeatable():
+    """Compaction with the kept keys' channel sums (per-CTA partials in a fixed order)."""
+    B, H, KVH, D, S, w, k = 1, 32, 8, 128, 32768, 64, 4096
+    inp = prefill_inputs(_wl(B, H, KVH, D, S, w, seed=91))
+    q, K, V = dev_bf16(inp["q"]), dev_bf16(inp["K"]), dev_bf16(inp["V"])
+    _same([kvc.kvc_compress_prefill_channels(q, K, V, 0.088, k, protect_tail=w) for _ in range(RUNS)])
+
+
 def test_channel_paths_repeatable():
     """Channel scores (query rows by kept keys), channel prune, value-channel scores."""
     B, H, KVH, D, S, w, k, C = 2, 32, 8, 128, 4096, 64, 1024, 64

@@ -461,8 +461,9 @@ def test_think_128k_layer_sampled_kv_head():
     inp = prefill_inputs(wl)
     G, scale = wl.G, wl.scale
     q, K, V = dev_bf16(inp["q"]), dev_bf16(inp["K"]), dev_bf16(inp["V"])
-    sc, idx, Ko, Vo = kvc.kvc_compress_prefill(q, K, V, scale, wl.k, protect_tail=wl.protect_tail, reduce="gqa")
-    cs = kvc.kvc_channel_score(q, Ko).cpu().numpy()
+    sc, idx, Ko, Vo, cs = kvc.kvc_compress_prefill_channels(q, K, V, scale, wl.k, protect_tail=wl.protect_tail,
+                                                            reduce="gqa")
+    cs = cs.cpu().numpy()
     np.testing.assert_allclose(sc.double().sum(-1).cpu().numpy(), wl.w, rtol=1e-4)
     kv = 3
     qh, Kh, Vh = inp["q"][:, kv * G:(kv + 1) * G], inp["K"][:, kv:kv + 1], inp["V"][:, kv:kv + 1]
@@ -704,6 +705,37 @@ def test_channel_score_parity(D, use_idx):
     cs = kvc.kvc_channel_score(dev_bf16(inp["q"]), dev_bf16(inp["K"]), idx=None if idx is None else dev_i32(idx))
     ref = O.channel_score(inp["q"], inp["K"], kept=idx)
     assert_scores_close(cs.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("B,H,KVH,D,S,w,k,protect,reduce", [
+    (1, 32, 8, 128, 3000, 64, 700, 64, "gqa"),    # several chunks per KV head, ragged last chunk
+    (2, 8, 2, 64, 2500, 32, 1000, 32, "gqa"),
+    (2, 16, 4, 128, 2049, 1, 512, 0, "all_heads"),
+    (1, 4, 1, 64, 300, 16, 290, 16, "gqa"),      # fewer eligible tokens than k: -1 rows add nothing
+])
+def test_compress_prefill_channels_parity(B, H, KVH, D, S, w, k, protect, reduce):
+    """The compaction that also sums the kept keys' squares: the same kept set and compacted
+    rows as kvc_compress_prefill (bit for bit), and ThinK's channel scores of the kept keys
+    against the oracle's closed form on the GPU's kept set."""
+    wl = _wl(B, H, KVH, D, S, w, seed=S + k, channel_scales=True)
+    inp = prefill_inputs(wl)
+    q, K, V = dev_bf16(inp["q"]), dev_bf16(inp["K"]), dev_bf16(inp["V"])
+    scale = 1.0 / np.sqrt(D)
+    sc, idx, Ko, Vo = kvc.kvc_compress_prefill(q, K, V, scale, k, protect_tail=protect, reduce=reduce)
+    sc2, idx2, Ko2, Vo2, cs = kvc.kvc_compress_prefill_channels(q, K, V, scale, k, protect_tail=protect, reduce=reduce)
+    assert torch.equal(sc.view(torch.int32), sc2.view(torch.int32))
+    assert torch.equal(idx, idx2)
+    assert torch.equal(Ko, Ko2) and torch.equal(Vo, Vo2)
+    g_idx = idx2.cpu().numpy()
+    assert_scores_close(cs.cpu().numpy(), O.channel_score(inp["q"], inp["K"], kept=g_idx), what="channel score")
+    # the separate call over the compacted keys agrees to fp32 rounding (other summation order)
+    cs_sep = kvc.kvc_channel_score(q, Ko2).cpu().numpy()
+    np.testing.assert_allclose(cs.cpu().numpy(), cs_sep, rtol=1e-5, atol=1e-6 * float(np.abs(cs_sep).max()))
+    # scores not kept: room for them comes from the workspace
+    none, idx3, Ko3, Vo3, cs3 = kvc.kvc_compress_prefill_channels(q, K, V, scale, k, protect_tail=protect, reduce=reduce,
+                                                                  keep_scores=False)
+    assert none is None and torch.equal(idx3, idx2) and torch.equal(Ko3, Ko2)
+    assert torch.equal(cs3.view(torch.int32), cs.view(torch.int32))
 
 
 @pytest.mark.parametrize("zero_mode", [False, True])
