@@ -3,13 +3,14 @@
 // compress PR 11: mean over each KV head's grouped queries), rebuilt around tcgen05.
 //
 // One CTA per (b, kvh, key range), 18 warps:
-//   warp 16 producer: TMA loads of the query group (once) and of 128-key K tiles into a
-//           4-stage shared-memory ring (128-byte swizzle), mbarrier-tracked;
+//   warp 16 producer: TMA loads of the query group (once) and of 256-key K stages into a
+//           2-stage (D = 128) or 4-stage (D = 64) shared-memory ring (128-byte swizzle),
+//           mbarrier-tracked;
 //   warp 17 MMA issuer: allocates all 512 TMEM columns (two 256-column accumulators) and
 //           issues tcgen05.mma kind::f16 (bf16 x bf16 -> fp32) from one thread; commits
 //           free the K stage and publish the accumulator;
 //   warps 0-15 epilogue: tcgen05.ld the accumulator, release it, then do the softmax math.
-// pass 1: A = query rows (M = 128 per half), B = K tile (N = 128 keys): each epilogue thread
+// pass 1: A = query rows (M = 128 per half), B = K stage (N = 256 keys): each epilogue thread
 //         owns one query row, so its running max / sum over keys is thread-local.
 // pass 2: A = K tile (M = 128 keys), B = the query group (N = Rpad rows): each thread owns
 //         one key and sums exp2(s*log2e - c_r) over its quarter of the query rows; the three
