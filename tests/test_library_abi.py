@@ -106,6 +106,24 @@ def test_host_validation_without_gpu(lib):
         == kvc.KVC_ERR_INVALID_ARG
     assert lib.kvc_topk_compact(big, FAKE, None, ctypes.byref(d), 4, 2, None, 0, FAKE * 256, FAKE * 128, None,
                                 None) == kvc.KVC_ERR_INVALID_ARG
+    # compaction with the key-channel sums: no channel_scores, a misaligned one, one that
+    # overlaps the indices, and a workspace too small
+    cws = lib.kvc_workspace_size(bnd.KVC_OP_TOPK_COMPACT_CHANNELS, ctypes.byref(d), 0, 4)
+    assert cws > 0
+    assert lib.kvc_topk_compact_channels(big, FAKE, None, ctypes.byref(d), 4, 0, None, 1, FAKE * 256, FAKE * 128,
+                                         None, FAKE * 512, 1, None, FAKE * 1024, cws, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_topk_compact_channels(big, FAKE, None, ctypes.byref(d), 4, 0, None, 1, FAKE * 256, FAKE * 128,
+                                         None, FAKE * 512, 1, FAKE * 768 + 4, FAKE * 1024, cws, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_topk_compact_channels(big, FAKE, None, ctypes.byref(d), 4, 0, None, 1, FAKE * 256, FAKE * 128,
+                                         None, FAKE * 512, 1, FAKE * 256, FAKE * 1024, cws, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_topk_compact_channels(big, FAKE, None, ctypes.byref(d), 4, 0, None, 1, FAKE * 256, FAKE * 128,
+                                         None, FAKE * 512, 1, FAKE * 768, FAKE * 1024, cws - 16, None) \
+        == kvc.KVC_ERR_WORKSPACE
+    assert lib.kvc_compress_prefill_channels(FAKE * 512, FAKE, None, ctypes.byref(d), 1, 0.1, 1, 4, 0, None,
+                                             FAKE * 256, FAKE * 128, None, None, FAKE * 1024, 1 << 30, None) \
+        == kvc.KVC_ERR_INVALID_ARG
     # channel prune: compact mode needs C % 8 == 0
     assert lib.kvc_channel_prune(FAKE, FAKE, ctypes.byref(d), 12, 0, FAKE, FAKE * 64, None) \
         == kvc.KVC_ERR_UNSUPPORTED
@@ -153,3 +171,10 @@ def test_workspace_size_rules(lib):
     assert lib.kvc_workspace_size(bnd.KVC_OP_TOPK_SELECT, ctypes.byref(d), 1, 1) == 0
     assert lib.kvc_workspace_size(bnd.KVC_OP_WINDOW_SCORES, ctypes.byref(d), 64, 0) > 0
     assert lib.kvc_workspace_size(bnd.KVC_OP_WINDOW_SCORES, ctypes.byref(d), 5000, 0) == ctypes.c_size_t(-1).value
+    # the channel-summing compaction: room for the key and query partials; the fused prefill
+    # entry adds the window-score scratch and the scores
+    ch = lib.kvc_workspace_size(bnd.KVC_OP_TOPK_COMPACT_CHANNELS, ctypes.byref(d), 0, 512)
+    assert ch > 0 and ch % (2 * 8 * 128 * 4) == 0
+    assert lib.kvc_workspace_size(bnd.KVC_OP_TOPK_COMPACT_CHANNELS, ctypes.byref(d), 0, 0) == ctypes.c_size_t(-1).value
+    assert lib.kvc_workspace_size(bnd.KVC_OP_COMPRESS_PREFILL_CHANNELS, ctypes.byref(d), 64, 512) >= \
+        ch + lib.kvc_workspace_size(bnd.KVC_OP_WINDOW_SCORES, ctypes.byref(d), 64, 0)
