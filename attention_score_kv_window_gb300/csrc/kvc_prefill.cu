@@ -382,6 +382,16 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
       for (int r0 = 0; r0 < SP; r0 += BR)
         tma_load_4d_hint(ks0 + (uint32_t)(p * SP * 128 + r0 * 128), &tmK, p * 64, r0, kvh, (int)b, kbar, pol);
   };
+  // The next head's key block, requested into L2 (evict-last) one copy ahead, so that its copy
+  // (issued once the stage is free) is an L2 hit and the CTA keeps more reads in flight.  Only
+  // with V in device memory: when the kept V rows come over the host link the pinned blocks
+  // slowed the whole pipeline, and without the evict-last hint the prefetch gained nothing.
+  auto prefetch_keys = [&](int kvh) {
+    if (kvh >= kvh0 + nh || !a.v_device) return;
+    const uint64_t keep = l2_policy_evict_last();
+    for (int p = 0; p < D / 64; ++p)
+      for (int r0 = 0; r0 < SP; r0 += BR) tma_prefetch_4d_hint(&tmK, p * 64, r0, kvh, (int)b, keep);
+  };
 
   pdl_wait();   // previous kernel on the stream complete and visible
   pdl_trigger();
@@ -390,21 +400,13 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
   const int limA = g < a.R ? S - a.w + (g % a.w) : -1;
   const int limB = g + 8 < a.R ? S - a.w + ((g + 8) % a.w) : -1;
 
-  // 1. the first head's key block: one thread issues the TMA boxes (rows >= S arrive zero-filled);
-  // the later heads' blocks are requested into L2 at once (evict-last), so their copies (issued
-  // once the stage is free) are L2 hits and the CTA keeps more of its reads in flight.  Only
-  // with V in device memory: when the kept V rows come over the host link the pinned blocks
-  // slowed the whole pipeline, and without the evict-last hint the prefetch gained nothing.
+  // 1. the first head's key block: one thread issues the TMA boxes (rows >= S arrive zero-filled)
+  // and requests the second head's block into L2
   if (tid == 0) {
     mbar_init(kbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     copy_keys(kvh0);
-    if (nh > 1 && a.v_device) {
-      const uint64_t keep = l2_policy_evict_last();
-      for (int hh = 1; hh < nh; ++hh)
-        for (int p = 0; p < D / 64; ++p)
-          for (int r0 = 0; r0 < SP; r0 += BR) tma_prefetch_4d_hint(&tmK, p * 64, r0, kvh0 + hh, (int)b, keep);
-    }
+    prefetch_keys(kvh0 + 1);
   }
   __syncthreads();  // the barrier is initialised before anyone waits on it
   bool keys_ok = true;
@@ -462,6 +464,7 @@ __global__ void __launch_bounds__(PF_THREADS, (D == 64 && NT <= 8) ? 3 : 1)
       if (tid == 0) {
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         copy_keys(kvh + 1);
+        prefetch_keys(kvh + 2);
       }
     }
 
