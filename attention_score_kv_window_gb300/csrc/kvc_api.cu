@@ -336,6 +336,8 @@ static kvc_status topk_compact_impl(const char* who, const float* scores, const 
                                     const uint32_t* live_mask, int32_t largest, int32_t* idx, kvc_bf16* K_out,
                                     kvc_bf16* V_out, const kvc_bf16* q_win, int32_t w, float* channel_scores,
                                     void* ws, size_t ws_bytes, kvc_stream_t stream) {
+  if (channel_scores && (int64_t)kv->B * kv->KVH > 65535)  // (kv checked by the caller)
+    return fail(KVC_ERR_UNSUPPORTED, "%s: B * KVH > 65535 with channel scores", who);
   KVC_TRY(check_gather(K, V, kv, k, K_out, V_out, who));
   if (kv->S > topk_max_len()) return fail(KVC_ERR_UNSUPPORTED, "%s: S > %lld", who, (long long)topk_max_len());
   if ((int64_t)kv->B * kv->KVH > 2147483647LL) return fail(KVC_ERR_UNSUPPORTED, "%s: too many rows", who);

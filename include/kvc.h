@@ -198,7 +198,8 @@ kvc_status kvc_topk_compact(const float* scores, const kvc_bf16* K, const kvc_bf
  *   Arguments as kvc_topk_compact, plus q_win [B,H,w,D] bf16 (the window queries, kv.H heads)
  *   and channel_scores [B,KVH,D] float32 out (16-byte aligned, overlapping no other argument).
  *   ws: kvc_workspace_size(KVC_OP_TOPK_COMPACT_CHANNELS, kv, 0, k) bytes, any content.  Rows
- *   whose index is -1 add nothing to the key norms.
+ *   whose index is -1 add nothing to the key norms.  B * KVH <= 65535 (else
+ *   KVC_ERR_UNSUPPORTED).
  * ------------------------------------------------------------------------------------- */
 kvc_status kvc_topk_compact_channels(const float* scores, const kvc_bf16* K, const kvc_bf16* V,
                                      const kvc_kv_desc* kv, int32_t k, int32_t protect_tail,

@@ -121,6 +121,10 @@ def test_host_validation_without_gpu(lib):
     assert lib.kvc_topk_compact_channels(big, FAKE, None, ctypes.byref(d), 4, 0, None, 1, FAKE * 256, FAKE * 128,
                                          None, FAKE * 512, 1, FAKE * 768, FAKE * 1024, cws - 16, None) \
         == kvc.KVC_ERR_WORKSPACE
+    wide = _desc(B=40000, H=8, KVH=2)
+    assert lib.kvc_topk_compact_channels(big, FAKE, None, ctypes.byref(wide), 4, 0, None, 1, FAKE * 256, FAKE * 128,
+                                         None, FAKE * 512, 1, FAKE * 768, FAKE * 1024, 1 << 40, None) \
+        == kvc.KVC_ERR_UNSUPPORTED
     assert lib.kvc_compress_prefill_channels(FAKE * 512, FAKE, None, ctypes.byref(d), 1, 0.1, 1, 4, 0, None,
                                              FAKE * 256, FAKE * 128, None, None, FAKE * 1024, 1 << 30, None) \
         == kvc.KVC_ERR_INVALID_ARG
