@@ -310,6 +310,35 @@ __global__ void __launch_bounds__(ST_THREADS, NS == ring_shallow<D>() ? 2 : 1)
     if (a.Vc) *reinterpret_cast<uint4*>(a.Vc + off) = *reinterpret_cast<const uint4*>(a.vnew + bk * D + lane * 8);
   }
 
+  // Scissorhands (deep ring, one CTA per SM): the history state of this thread's first NPRE
+  // output-pass iterations is loaded now, so its latency runs under the stream instead of
+  // stalling the output pass (the kernel writes that state only in the output pass)
+  constexpr bool PRE = NS != ring_shallow<D>();
+  constexpr int OB = 4, NPRE = PRE ? 2 : 1;
+  const int64_t nwl = a.shs.cap / 32;
+  uint32_t pre_l[NPRE][OB], pre_h[NPRE][OB];
+  int32_t pre_i[NPRE][OB];
+  uint32_t pre_w[NPRE][OB];
+  if (PRE && a.shs.B) {
+    const int64_t plane = ((a.shs.t % a.shs.history) * a.shs.B * a.shs.KVH + bk) * nwl;
+#pragma unroll
+    for (int it = 0; it < NPRE; ++it)
+#pragma unroll
+      for (int u = 0; u < OB; ++u) {
+        const int j0 = warp * 32 + it * OB * ST_THREADS + u * ST_THREADS;
+        pre_l[it][u] = pre_h[it][u] = pre_w[it][u] = 0u;
+        pre_i[it][u] = 0;
+        if (j0 < len) {
+          const int64_t gj = kbeg + j0 + lane;
+          const int64_t x = bk * a.shs.cap + gj;
+          pre_l[it][u] = a.shs.live[bk * nwl + (gj >> 5)];
+          pre_h[it][u] = a.shs.hist[plane + (gj >> 5)];
+          pre_i[it][u] = a.shs.insert_step[x];
+          pre_w[it][u] = a.shs.low_count[x];
+        }
+      }
+  }
+
   if (warp == ST_PRODUCER) {
     if (lane == 0) {
       for (int it = issued; it < ntiles; ++it) {
@@ -439,13 +468,23 @@ __global__ void __launch_bounds__(ST_THREADS, NS == ring_shallow<D>() ? 2 : 1)
   // slots: a slice starts at a multiple of 128, and a Scissorhands row is whole live words).
   // The Scissorhands state of OB iterations is loaded before any is used (the loads overlap).
   const float thr = __fdiv_rn(1.0f, (float)(keys > 0 ? keys : 1));  // Scissorhands: float32(1)/float32(keys)
-  const int64_t nwl = a.shs.cap / 32;
-  constexpr int OB = 4;
-  for (int jb = warp * 32; jb < len; jb += OB * ST_THREADS) {
+  for (int jb = warp * 32, oit = 0; jb < len; jb += OB * ST_THREADS, ++oit) {
     uint32_t lword[OB], hword[OB];
     int32_t insv[OB];
     uint16_t lowv[OB];
-    if (a.shs.B) {
+    if (PRE && a.shs.B && oit < NPRE) {
+#pragma unroll
+      for (int it = 0; it < NPRE; ++it)
+        if (it == oit) {
+#pragma unroll
+          for (int u = 0; u < OB; ++u) {
+            lword[u] = pre_l[it][u];
+            hword[u] = pre_h[it][u];
+            insv[u] = pre_i[it][u];
+            lowv[u] = (uint16_t)pre_w[it][u];
+          }
+        }
+    } else if (a.shs.B) {
 #pragma unroll
       for (int u = 0; u < OB; ++u) {
         const int j0 = jb + u * ST_THREADS;
