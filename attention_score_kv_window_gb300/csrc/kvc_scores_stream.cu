@@ -244,6 +244,19 @@ __global__ void __launch_bounds__(ST_THREADS, NS == ring_shallow<D>() ? 2 : 1)
     }
   }
 
+  // B operand of the consumer warps: query row g (< R), channels ks*16 + 2t4 (+1) and + 8,
+  // loaded before the slot search so that the loads overlap it
+  const uint16_t* qg = a.q + ((int64_t)b * a.H + (int64_t)kvh * a.G) * D;  // the group's query rows
+  uint32_t bq[KS][2];
+  if (warp != ST_PRODUCER) {
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const bool rv = g < R;
+      bq[ks][0] = rv ? __ldg(reinterpret_cast<const uint32_t*>(qg + (int64_t)g * D + ks * 16 + 2 * t4)) : 0u;
+      bq[ks][1] = rv ? __ldg(reinterpret_cast<const uint32_t*>(qg + (int64_t)g * D + ks * 16 + 8 + 2 * t4)) : 0u;
+    }
+  }
+
   // the new token: its slot (TOVA: given; Scissorhands: the lowest free slot, or the queued
   // one) and, Scissorhands, the live keys once it is in
   if (a.shs.B) {
@@ -303,7 +316,6 @@ __global__ void __launch_bounds__(ST_THREADS, NS == ring_shallow<D>() ? 2 : 1)
   const int fslot = s_slot[0];
   const int keys = s_slot[1];
   const int wf = (fslot >= kbeg && fslot < kend) ? fslot - kbeg : -1;  // slice-relative
-  const uint16_t* qg = a.q + ((int64_t)b * a.H + (int64_t)kvh * a.G) * D;  // the group's query rows
   if (wf >= 0 && warp == 0 && lane < CH) {  // the cache rows for later steps
     const int64_t off = (int64_t)b * a.sb + (int64_t)kvh * a.sh + (int64_t)fslot * a.ss + lane * 8;
     *reinterpret_cast<uint4*>(a.Kc + off) = *reinterpret_cast<const uint4*>(a.knew + bk * D + lane * 8);
@@ -355,14 +367,6 @@ __global__ void __launch_bounds__(ST_THREADS, NS == ring_shallow<D>() ? 2 : 1)
           drain_bar(full(it % L::NS), (uint32_t)(it / L::NS) & 1u);
     }
   } else {
-    // B operand: query row g (< R), channels ks*16 + 2t4 (+1) and + 8
-    uint32_t bq[KS][2];
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      const bool rv = g < R;
-      bq[ks][0] = rv ? __ldg(reinterpret_cast<const uint32_t*>(qg + (int64_t)g * D + ks * 16 + 2 * t4)) : 0u;
-      bq[ks][1] = rv ? __ldg(reinterpret_cast<const uint32_t*>(qg + (int64_t)g * D + ks * 16 + 8 + 2 * t4)) : 0u;
-    }
     const int r0 = 2 * t4, r1 = r0 + 1;
     const bool v0 = r0 < R, v1 = r1 < R;
     const uint32_t* lw = a.live ? a.live + bk * a.live_words : nullptr;
