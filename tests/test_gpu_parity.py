@@ -809,6 +809,7 @@ DECODE_CASES = [
     (1, 8, 2, 128, 64, 40000, 0.5),     # many key ranges
     (16, 32, 8, 128, 64, 4096, None),   # 128 (b, kvh) rows
     (16, 32, 8, 128, 128, 4100, 0.5),   # 128 rows, ragged, dead slots
+    (2, 32, 8, 128, 64, 40000, 0.5),    # 16 rows over all SMs: up to 11 pieces per row
 ]
 
 
