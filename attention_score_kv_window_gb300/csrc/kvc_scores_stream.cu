@@ -222,6 +222,10 @@ __global__ void __launch_bounds__(ST_THREADS, NS == ring_shallow<D>() ? 2 : 1)
   const int ntiles = (len + ST_TILE - 1) / ST_TILE;
   const int R = a.G;
 
+  // the key tensor map's descriptor fetched while the barriers are set up and the previous
+  // kernel finishes (it is a launch parameter, not an output of that kernel)
+  if (warp == ST_PRODUCER && lane == 0)
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
   if (tid == 0) {
     for (int s = 0; s < L::NS; ++s) {
       mbar_init(full(s), 1);
@@ -558,12 +562,17 @@ __global__ void __launch_bounds__(ST_THREADS, NS == ring_shallow<D>() ? 2 : 1)
     unsigned long long best = 0ull;
     for (int j = j0 + tid; j < j1; j += ST_THREADS) {
       const uint32_t la = su32(lg + j);
-      float sm = 0.f;
-      for (int h = 0; h < KV; ++h) {
-        float v;
-        asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(map_rank(la, (unsigned)h)) : "memory");
-        sm += v;
+      // all heads' loads issued before the first add (KV <= 8), summed in head order
+      float v[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        v[h] = 0.f;
+        if (h < KV) asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v[h]) : "r"(map_rank(la, (unsigned)h)));
       }
+      float sm = 0.f;
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        if (h < KV) sm += v[h];
       sm *= inv;
       for (int h = 0; h < KV; ++h) a.allh_out[(row0 + h) * a.S + j] = sm;
       uint32_t u = __float_as_uint(sm);

@@ -37,6 +37,12 @@ namespace {
 
 constexpr int TILE = 128;           // keys per accumulator unit of pass 2 (its MMA M)
 constexpr int KT = 256;             // keys per K stage: pass 1's MMA N, two pass-2 units
+// K bytes over all CTAs that pass 1 marks to stay in L2 for pass 2 (of the 126 MB L2; the
+// rest holds what is streamed through once, the partials and the scores)
+constexpr int64_t L2_KEEP_BYTES = 80ll << 20;
+// the range's K stage that pass 2 reads i-th: the stages in reverse order, so that it starts
+// with those pass 1 read last
+__device__ __forceinline__ int pass2_stage(int ntiles, int i) { return ntiles - 1 - i; }
 constexpr int MAX_STAGES = 4;       // K ring depth: 2 stages of 64 KiB (D = 128), 4 of 32 KiB (D = 64)
 template <int D>
 __host__ __device__ constexpr int ring_stages() { return D == 128 ? 2 : 4; }
@@ -139,13 +145,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
           "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// one K box with an L2 eviction policy (createpolicy below)
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* tm, int x, int y, int z, int w,
-                                            uint32_t bar) {
+                                            uint32_t bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
-      "[%6];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6], %7;\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
       : "memory");
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
@@ -334,20 +351,31 @@ __device__ __forceinline__ void teardown(const Ctx& c) {
 template <int D>
 __device__ __forceinline__ void producer(const Ctx& c, const ScoresArgs& a, const CUtensorMap* tmK,
                                          const CUtensorMap* tmQ, int qrows, int kvh, int b, int64_t kbeg,
-                                         int ntiles, int total) {
+                                         int ntiles, int nt1, int total) {
   using L = Layout<D>;
   const int qrow0 = (b * a.H + kvh * a.G) * a.w;
   mbar_expect_tx(c.qfull(), (uint32_t)(L::NP * qrows * 128));
   for (int p = 0; p < L::NP; ++p) tma_load_2d(c.sbase + L::Q + p * qpanel_bytes(), tmQ, p * 64, qrow0, c.qfull());
+  // Pass 1 reads the range's stages in order, pass 2 in reverse (pass2_stage).  The last
+  // `keep` stages of pass 1, the first that pass 2 reads, are loaded with the L2 evict-last
+  // policy, all other loads with evict-first: where K is larger than L2, the part of it that
+  // L2 can hold is still there when pass 2 starts instead of the part read longest ago.
+  const int64_t ctas = (int64_t)gridDim.x * gridDim.y * gridDim.z;
+  const int64_t fit = L2_KEEP_BYTES / (ctas * (int64_t)L::STAGE);
+  const int keep = fit < ntiles ? (int)fit : ntiles;
+  const uint64_t pol_keep = l2_evict_last(), pol_once = l2_evict_first();
   int issued = 0;
   for (int it = 0; it < total; ++it) {
     const int s = it % L::ST;
     const uint32_t ph = (uint32_t)(it / L::ST) & 1u;
     if (!wait_bar(c.empty(s), ph ^ 1u, c.abort_flag, c.wait_ns)) break;
     mbar_expect_tx(c.full(s), L::STAGE);
-    const int y = (int)(kbeg + (int64_t)(it < ntiles ? it : it - ntiles) * KT);
+    const bool p2 = it >= nt1;
+    const int t = p2 ? pass2_stage(ntiles, it - nt1) : it;
+    const int y = (int)(kbeg + (int64_t)t * KT);
+    const uint64_t pol = !p2 && t >= ntiles - keep ? pol_keep : pol_once;
     for (int p = 0; p < L::NP; ++p)
-      tma_load_4d(c.sbase + L::K + s * L::STAGE + p * kpanel_bytes(), tmK, p * 64, y, kvh, b, c.full(s));
+      tma_load_4d(c.sbase + L::K + s * L::STAGE + p * kpanel_bytes(), tmK, p * 64, y, kvh, b, c.full(s), pol);
     issued = it + 1;
   }
   // copies still in flight when the kernel stops early are waited for (bounded) before exit
@@ -617,6 +645,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int UPT1 = NHALF;                    // pass-1 units per K stage (one per query half)
   constexpr int NW = N2 / 2;                     // pass 2: query-row columns per warp and tile
   extern __shared__ unsigned char smem_raw[];
+  // both tensor maps' descriptors fetched during the prologue and the wait for the previous
+  // kernel (they are launch parameters, not outputs of that kernel)
+  if (threadIdx.x == PRODUCER_WARP * 32) {
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
+  }
   Ctx cx = prologue<D>(smem_raw);  // shared memory and TMEM only
   cx.wait_ns = a.wait_ns;
   const Ctx& c = cx;
@@ -638,7 +672,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto last_of_stage = [&](int u) -> bool { return u < n1 ? (u % UPT1) == UPT1 - 1 : ((u - n1) & 1) == 1; };
 
   if (warp == PRODUCER_WARP) {
-    if (lane == 0) producer<D>(c, a, &tmK, &tmQ, QROWS, kvh, b, kbeg, ntiles, nt1 + (P2 ? ntiles : 0));
+    if (lane == 0) producer<D>(c, a, &tmK, &tmQ, QROWS, kvh, b, kbeg, ntiles, nt1, nt1 + (P2 ? ntiles : 0));
   } else if (warp == MMA_WARP) {
     if (lane == 0 && wait_bar(c.qfull(), 0, c.abort_flag, c.wait_ns)) {
       int done = 0;
@@ -798,7 +832,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int first = n1 + ((g - n1) & 1);  // this group's first pass-2 tile
       for (int it = first; it < total; it += 2) {
         const int u = (it - first) >> 1;       // this group's pass-2 tile count
-        const int64_t kt0 = kbeg + (int64_t)(it - n1) * TILE;
+        const int64_t kt0 = kbeg + (int64_t)pass2_stage(ntiles, (it - n1) >> 1) * KT + ((it - n1) & 1) * TILE;
         const int64_t j = kt0 + kr;
         float acc = 0.f;
         if (!dead && wait_bar(c.tfull(g), (uint32_t)(it >> 1) & 1u, c.abort_flag, c.wait_ns)) {
