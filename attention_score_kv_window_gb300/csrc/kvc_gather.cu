@@ -333,12 +333,15 @@ __global__ void __launch_bounds__(1024) k_channel_final(const float* __restrict_
 // ----------------------------------------------------------------------------------------
 // ThinK channel pruning
 // ----------------------------------------------------------------------------------------
-// keep the C highest channel scores (ties: lower channel), ascending list
-__global__ void k_channel_select(const float* __restrict__ cs, int D, int C, int32_t* __restrict__ ch) {
-  pdl_wait();  // previous kernel on the stream complete and visible
+// The C highest channel scores of row bk (ties: the lower channel), as an ascending channel list
+// in chs (shared memory).  Every CTA of the row takes the same decision from the same scores, so
+// the list needs no launch of its own; the row's first CTA also writes it to ch.  Threads
+// d < D (D <= 128) rank channel d; the block has at least D threads.
+__device__ __forceinline__ void select_channels(const float* __restrict__ cs, int bk, int D, int C, int32_t* chs,
+                                                int32_t* __restrict__ ch) {
   __shared__ float v[128];
   __shared__ uint32_t wb[4];
-  const int bk = blockIdx.x, d = threadIdx.x;  // blockDim = 128
+  const int d = threadIdx.x;
   if (d < D) v[d] = cs[(int64_t)bk * D + d];
   __syncthreads();
   bool sel = false;
@@ -351,39 +354,60 @@ __global__ void k_channel_select(const float* __restrict__ cs, int D, int C, int
     }
     sel = rank < C;
   }
-  const uint32_t bal = __ballot_sync(0xffffffffu, sel);
   const int lane = d & 31, warp = d >> 5;
-  if (lane == 0) wb[warp] = __popc(bal);
+  const uint32_t bal = __ballot_sync(0xffffffffu, sel);
+  if (lane == 0 && warp < 4) wb[warp] = __popc(bal);
   __syncthreads();
-  int base = 0;
-  for (int q = 0; q < warp; ++q) base += wb[q];
-  if (sel) ch[(int64_t)bk * C + base + __popc(bal & ((1u << lane) - 1u))] = d;
+  if (sel) {
+    int base = 0;
+    for (int q = 0; q < warp; ++q) base += wb[q];
+    const int pos = base + __popc(bal & ((1u << lane) - 1u));
+    chs[pos] = d;
+    if (blockIdx.x == 0) ch[(int64_t)bk * C + pos] = d;
+  }
+  __syncthreads();
 }
 
-// compact mode: Ko[b,kvh,t,c] = K[b,kvh,t,ch[c]] — 32 rows per pass staged in shared memory
+// compact mode: ch = the selected channels, Ko[b,kvh,t,c] = K[b,kvh,t,ch[c]] — 64 rows per
+// pass staged in shared memory.  Each thread's 16-byte loads of a pass are in flight together,
+// the first pass's during the channel selection and each next pass's during this pass's stores.
 template <int D>
-__global__ void __launch_bounds__(256) k_channel_gather(const uint16_t* __restrict__ K, int64_t sb,
-                                                        int64_t sh, int64_t ss, int64_t S, int KVH,
-                                                        const int32_t* __restrict__ ch, int C,
+__global__ void __launch_bounds__(256) k_channel_gather(const float* __restrict__ cs, const uint16_t* __restrict__ K,
+                                                        int64_t sb, int64_t sh, int64_t ss, int64_t S, int KVH,
+                                                        int32_t* __restrict__ ch, int C,
                                                         uint16_t* __restrict__ Ko) {
   pdl_wait();  // previous kernel on the stream complete and visible
-  constexpr int TPR = D / 8, RB = 32;
+  constexpr int NT = 256, TPR = D / 8, RB = 64, LPT = RB * TPR / NT;
+  static_assert(LPT * NT == RB * TPR, "whole rows per pass");
   __shared__ __align__(16) uint16_t tile[RB][D + 8];
   __shared__ int32_t chs[128];
+  const int tid = threadIdx.x;
   const int bk = blockIdx.y;
   const int64_t b = bk / KVH, kvh = bk % KVH;
-  for (int c = threadIdx.x; c < C; c += blockDim.x) chs[c] = ch[(int64_t)bk * C + c];
   const uint16_t* Kb = K + b * sb + kvh * sh;
   uint16_t* Ob = Ko + (int64_t)bk * S * C;
+  const int64_t step = (int64_t)gridDim.x * RB;
+  uint4 buf[LPT];
+  auto load = [&](int64_t r0) {
+#pragma unroll
+    for (int u = 0; u < LPT; ++u) {
+      const int x = u * NT + tid, r = x / TPR, c = x % TPR;
+      buf[u] = r0 + r < S ? ld16(Kb + (r0 + r) * ss + c * 8) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  int64_t r0 = (int64_t)blockIdx.x * RB;
+  if (r0 < S) load(r0);
+  select_channels(cs, bk, D, C, chs, ch);  // (ends with a block barrier)
   const int out_chunks = C / 8;
-  for (int64_t r0 = (int64_t)blockIdx.x * RB; r0 < S; r0 += (int64_t)gridDim.x * RB) {
-    __syncthreads();
-    for (int x = threadIdx.x; x < RB * TPR; x += blockDim.x) {
-      const int r = x / TPR, c = x % TPR;
-      if (r0 + r < S) *reinterpret_cast<uint4*>(&tile[r][c * 8]) = ld16(Kb + (r0 + r) * ss + c * 8);
+  for (; r0 < S; r0 += step) {
+#pragma unroll
+    for (int u = 0; u < LPT; ++u) {
+      const int x = u * NT + tid, r = x / TPR, c = x % TPR;
+      *reinterpret_cast<uint4*>(&tile[r][c * 8]) = buf[u];
     }
     __syncthreads();
-    for (int x = threadIdx.x; x < RB * out_chunks; x += blockDim.x) {
+    if (r0 + step < S) load(r0 + step);
+    for (int x = tid; x < RB * out_chunks; x += NT) {
       const int r = x / out_chunks, oc = x % out_chunks;
       if (r0 + r >= S) continue;
       uint32_t w[4];
@@ -395,24 +419,25 @@ __global__ void __launch_bounds__(256) k_channel_gather(const uint16_t* __restri
       }
       st16(Ob + (r0 + r) * C + oc * 8, make_uint4(w[0], w[1], w[2], w[3]));
     }
+    __syncthreads();  // the tile is rewritten next pass
   }
 }
 
 // zero mode: Ko = K with unselected channels zeroed (Ko dense [B,KVH,S,D]; may equal K)
 template <int D>
-__global__ void __launch_bounds__(256) k_channel_zero(const uint16_t* K, int64_t sb, int64_t sh,
-                                                      int64_t ss, int64_t S, int KVH,
-                                                      const int32_t* __restrict__ ch, int C,
-                                                      uint16_t* Ko) {
+__global__ void __launch_bounds__(256) k_channel_zero(const float* __restrict__ cs, const uint16_t* K, int64_t sb,
+                                                      int64_t sh, int64_t ss, int64_t S, int KVH,
+                                                      int32_t* __restrict__ ch, int C, uint16_t* Ko) {
   pdl_wait();  // previous kernel on the stream complete and visible
   constexpr int TPR = D / 8;
   __shared__ uint32_t keepw[4];
+  __shared__ int32_t chs[128];
   const int bk = blockIdx.y;
   const int64_t b = bk / KVH, kvh = bk % KVH;
   if (threadIdx.x < 4) keepw[threadIdx.x] = 0;
-  __syncthreads();
+  select_channels(cs, bk, D, C, chs, ch);  // (ends with a block barrier)
   for (int c = threadIdx.x; c < C; c += blockDim.x) {
-    const int d = ch[(int64_t)bk * C + c] & (D - 1);
+    const int d = chs[c];
     atomicOr(&keepw[d >> 5], 1u << (d & 31));
   }
   __syncthreads();
@@ -553,22 +578,21 @@ cudaError_t launch_compact_channels(const uint16_t* K, const uint16_t* V, const 
 cudaError_t launch_channel_prune(const float* cs, const uint16_t* K, const kvc_kv_desc& kv, int C,
                                  int zero_mode, int32_t* ch, uint16_t* Ko, cudaStream_t st) {
   const int rows = kv.B * kv.KVH;
-  cudaError_t e = launch_pdl(k_channel_select, dim3(rows), dim3(128), 0, st, cs, kv.D, C, ch);
-  if (e != cudaSuccess) return e;
-  const int per = (int)std::max<int64_t>(1, std::min<int64_t>((kv.S + 31) / 32, ((int64_t)num_sms() * 8 + rows - 1) / rows));
+  cudaError_t e;
+  const int per = (int)std::max<int64_t>(1, std::min<int64_t>((kv.S + 63) / 64, ((int64_t)num_sms() * 8 + rows - 1) / rows));
   const dim3 grid(per, rows);
   if (zero_mode)
-    e = kv.D == 64 ? launch_pdl(k_channel_zero<64>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
+    e = kv.D == 64 ? launch_pdl(k_channel_zero<64>, grid, dim3(256), 0, st, cs, K, kv.stride_b, kv.stride_h, kv.stride_s,
                                 kv.S, kv.KVH, ch, C, Ko)
-                   : launch_pdl(k_channel_zero<128>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
+                   : launch_pdl(k_channel_zero<128>, grid, dim3(256), 0, st, cs, K, kv.stride_b, kv.stride_h, kv.stride_s,
                                 kv.S, kv.KVH, ch, C, Ko);
   else
-    e = kv.D == 64 ? launch_pdl(k_channel_gather<64>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h, kv.stride_s,
+    e = kv.D == 64 ? launch_pdl(k_channel_gather<64>, grid, dim3(256), 0, st, cs, K, kv.stride_b, kv.stride_h, kv.stride_s,
                                 kv.S, kv.KVH, ch, C, Ko)
-                   : launch_pdl(k_channel_gather<128>, grid, dim3(256), 0, st, K, kv.stride_b, kv.stride_h,
+                   : launch_pdl(k_channel_gather<128>, grid, dim3(256), 0, st, cs, K, kv.stride_b, kv.stride_h,
                                 kv.stride_s, kv.S, kv.KVH, ch, C, Ko);
   if (e != cudaSuccess) return e;
-  return launched(2);
+  return launched(1);
 }
 
 KVC_TU_STATUS(gather)
