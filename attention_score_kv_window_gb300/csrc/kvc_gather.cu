@@ -278,14 +278,33 @@ __global__ void __launch_bounds__(256) k_channel_partial(const uint16_t* __restr
   q_sq_partial<D>(q, H, w, KVH, b, kvh, split, gridDim.x, gridDim.z * KVH, red, qpart);
 }
 
-// cs[b*KVH+kvh][d] = the sum of the key-range partials
-__global__ void __launch_bounds__(256) k_channel_sum(const float* __restrict__ part, int nsplit, int64_t n,
-                                                     float* __restrict__ cs) {
+// cs[b*KVH+kvh][d] = the sum of the key-range partials: one CTA per (b, kvh), thread (grp, d)
+// adding every ngrp-th range with its loads in flight at once, the groups then added in
+// shared memory in group order
+__global__ void __launch_bounds__(1024) k_channel_sum(const float* __restrict__ part, int nsplit, int rows, int D,
+                                                      float* __restrict__ cs) {
   pdl_wait();  // previous kernel on the stream complete and visible
-  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n; x += (int64_t)gridDim.x * blockDim.x) {
-    float s = 0.f;
-    for (int q = 0; q < nsplit; ++q) s += __ldg(part + (int64_t)q * n + x);
-    cs[x] = s;
+  __shared__ float red[16][128];
+  const int bk = blockIdx.x;
+  const int d = threadIdx.x % D, grp = threadIdx.x / D, ngrp = blockDim.x / D;
+  constexpr int BATCH = 16;
+  float acc = 0.f;
+  for (int s0 = grp; s0 < nsplit; s0 += BATCH * ngrp) {
+    float v[BATCH];
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int sp = s0 + u * ngrp;
+      v[u] = sp < nsplit ? __ldg(part + ((int64_t)sp * rows + bk) * D + d) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) acc += v[u];
+  }
+  red[grp][d] = acc;
+  __syncthreads();
+  if (grp == 0) {
+    float t = 0.f;
+    for (int g2 = 0; g2 < ngrp; ++g2) t += red[g2][d];
+    cs[(int64_t)bk * D + d] = t;
   }
 }
 
@@ -460,9 +479,13 @@ __global__ void __launch_bounds__(256) k_channel_zero(const float* __restrict__ 
   }
 }
 
-int channel_splits(const kvc_kv_desc& kv, int64_t nrows) {
+// Row ranges per (b, kvh) for the channel sums: about per_sm CTAs per SM over all units, at
+// least 64 rows each.  Measured best on the ThinK 128K shapes: 2 for the compaction (fewer,
+// longer CTAs overlap their stores with the next rows' loads), 8 for the weighted value sums.
+constexpr int SPLITS_COMPACT = 2, SPLITS_PLAIN = 4, SPLITS_WEIGHTED = 8;
+int channel_splits(const kvc_kv_desc& kv, int64_t nrows, int per_sm) {
   const int64_t units = (int64_t)kv.B * kv.KVH;
-  const int64_t target = (int64_t)num_sms() * 4;
+  const int64_t target = (int64_t)num_sms() * per_sm;
   int64_t ns = std::max<int64_t>(1, (target + units - 1) / units);
   ns = std::min<int64_t>(ns, std::max<int64_t>(1, nrows / 64));
   return (int)ns;
@@ -490,7 +513,11 @@ cudaError_t launch_compact(const uint16_t* K, const uint16_t* V, const kvc_kv_de
 
 cudaError_t launch_weighted_channel_norm(const float* wts, const uint16_t* V, const kvc_kv_desc& kv, float* cs,
                                          void* ws, cudaStream_t st) {
-  const int ns = channel_splits(kv, kv.S);
+  const int ns = channel_splits(kv, kv.S, SPLITS_WEIGHTED);
+  // the caller's scratch is channel_score_workspace(kv, 0, false) bytes: 2 x ceil(4 x SMs /
+  // units) partials per unit, never fewer than ceil(8 x SMs / units)
+  if ((size_t)ns * kv.B * kv.KVH * kv.D * sizeof(float) > channel_score_workspace(kv, 0, false))
+    return cudaErrorInvalidValue;
   const int64_t chunk = (kv.S + ns - 1) / ns;
   float* part = reinterpret_cast<float*>(ws);
   const dim3 grid(ns, kv.KVH, kv.B);
@@ -502,9 +529,8 @@ cudaError_t launch_weighted_channel_norm(const float* wts, const uint16_t* V, co
                               kv.S, (const int32_t*)nullptr, 0, kv.S, chunk, part, kv.KVH, wts,
                               (const uint16_t*)nullptr, 0, 0, (float*)nullptr);
   if (e != cudaSuccess) return e;
-  const int64_t n = (int64_t)kv.B * kv.KVH * kv.D;
-  e = launch_pdl(k_channel_sum, dim3((unsigned)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 1024))),
-                 dim3(256), 0, st, (const float*)part, ns, n, cs);
+  const int rows = kv.B * kv.KVH;
+  e = launch_pdl(k_channel_sum, dim3((unsigned)rows), dim3(1024), 0, st, (const float*)part, ns, rows, kv.D, cs);
   if (e != cudaSuccess) return e;
   return launched(2);
 }
@@ -526,14 +552,14 @@ cudaError_t launch_write_slots(const uint16_t* kn, const uint16_t* vn, const int
 // key partials, then query partials: [2][nsplit][B*KVH][D] floats
 size_t channel_score_workspace(const kvc_kv_desc& kv, int k, bool has_idx) {
   const int64_t nrows = has_idx ? k : kv.S;
-  const int ns = channel_splits(kv, nrows);
+  const int ns = channel_splits(kv, nrows, SPLITS_PLAIN);
   return 2 * (size_t)ns * kv.B * kv.KVH * kv.D * sizeof(float);
 }
 
 cudaError_t launch_channel_score(const uint16_t* q, int w, const uint16_t* K, const kvc_kv_desc& kv,
                                  const int32_t* idx, int k, float* cs, void* ws, cudaStream_t st) {
   const int64_t nrows = idx ? k : kv.S;
-  const int ns = channel_splits(kv, nrows);
+  const int ns = channel_splits(kv, nrows, SPLITS_PLAIN);
   const int64_t chunk = (nrows + ns - 1) / ns;
   float* part = static_cast<float*>(ws);
   float* qpart = part + (size_t)ns * kv.B * kv.KVH * kv.D;
@@ -552,13 +578,13 @@ cudaError_t launch_channel_score(const uint16_t* q, int w, const uint16_t* K, co
 
 // key partials, then query partials, of the compaction that also scores the key channels
 size_t compact_channels_workspace(const kvc_kv_desc& kv, int k) {
-  return 2 * (size_t)channel_splits(kv, k) * kv.B * kv.KVH * kv.D * sizeof(float);
+  return 2 * (size_t)channel_splits(kv, k, SPLITS_COMPACT) * kv.B * kv.KVH * kv.D * sizeof(float);
 }
 
 cudaError_t launch_compact_channels(const uint16_t* K, const uint16_t* V, const kvc_kv_desc& kv, const int32_t* idx,
                                     int k, uint16_t* Ko, uint16_t* Vo, const uint16_t* q, int w, float* cs, void* ws,
                                     cudaStream_t st) {
-  const int ns = channel_splits(kv, k);
+  const int ns = channel_splits(kv, k, SPLITS_COMPACT);
   const int64_t chunk = (k + ns - 1) / ns;
   float* part = static_cast<float*>(ws);
   float* qpart = part + (size_t)ns * kv.B * kv.KVH * kv.D;
