@@ -684,6 +684,12 @@ kvc_status kvc_channel_prune(const float* cs, const kvc_bf16* K, const kvc_kv_de
   } else if (overlaps(ko, ko + osz, k0, k1)) {
     return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune: K_out overlaps K");
   }
+  // every CTA of a row reads the row's scores and its keys while the row's first CTA writes
+  // the channel list, so the list may share no bytes with cs, K or K_out
+  const uintptr_t c0 = reinterpret_cast<uintptr_t>(ch_idx), c1 = c0 + (uintptr_t)kv->B * kv->KVH * C * 4;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(cs), s1 = s0 + (uintptr_t)kv->B * kv->KVH * kv->D * 4;
+  if (overlaps(c0, c1, s0, s1) || overlaps(c0, c1, k0, k1) || overlaps(c0, c1, ko, ko + osz))
+    return fail(KVC_ERR_INVALID_ARG, "kvc_channel_prune: ch_idx overlaps cs, K or K_out");
   return cuda_status(launch_channel_prune(cs, K, *kv, C, zero_mode ? 1 : 0, ch_idx, K_out, (cudaStream_t)stream),
                      "kvc_channel_prune launch");
 }

@@ -379,6 +379,7 @@ kvc_status kvc_channel_score(const kvc_bf16* q_win, int32_t w, const kvc_bf16* K
  *                ThinK_Press" options 3b/3c).
  *   zero_mode 1: K_out [B,KVH,S,D] dense = K with the other channels zeroed (option 3a);
  *                K_out may equal K when K is dense (in place).
+ *   cs [B,KVH,D] float32.  ch_idx shares no bytes with cs, K or K_out (KVC_ERR_INVALID_ARG).
  * ------------------------------------------------------------------------------------- */
 kvc_status kvc_channel_prune(const float* cs, const kvc_bf16* K, const kvc_kv_desc* kv,
                              int32_t C, int32_t zero_mode, int32_t* ch_idx, kvc_bf16* K_out,

@@ -128,9 +128,17 @@ def test_host_validation_without_gpu(lib):
     assert lib.kvc_compress_prefill_channels(FAKE * 512, FAKE, None, ctypes.byref(d), 1, 0.1, 1, 4, 0, None,
                                              FAKE * 256, FAKE * 128, None, None, FAKE * 1024, 1 << 30, None) \
         == kvc.KVC_ERR_INVALID_ARG
-    # channel prune: compact mode needs C % 8 == 0
+    # channel prune: compact mode needs C % 8 == 0; the channel list may not overlap the scores,
+    # the keys or the pruned keys
     assert lib.kvc_channel_prune(FAKE, FAKE, ctypes.byref(d), 12, 0, FAKE, FAKE * 64, None) \
         == kvc.KVC_ERR_UNSUPPORTED
+    assert lib.kvc_channel_prune(FAKE * 512, FAKE, ctypes.byref(d), 16, 0, FAKE * 512 + 64, FAKE * 64, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_channel_prune(FAKE * 512, FAKE, ctypes.byref(d), 16, 0, FAKE + 256, FAKE * 64, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_channel_prune(FAKE * 512, FAKE, ctypes.byref(d), 16, 0, FAKE * 64 + 256, FAKE * 64, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    assert "ch_idx overlaps" in kvc.load_library().kvc_last_error_message().decode()
     # Scissorhands: capacity must be a multiple of 32; no free slot -> refused
     st = bnd.ShState(1, 2, 40, 400, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0)
     assert lib.kvc_scissorhands_init(ctypes.byref(st), 0, None) == kvc.KVC_ERR_INVALID_ARG
