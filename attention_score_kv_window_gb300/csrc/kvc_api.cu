@@ -706,6 +706,15 @@ kvc_status kvc_value_channel_score(const kvc_bf16* q_win, int32_t w, const kvc_b
   if (!cs) return fail(KVC_ERR_INVALID_ARG, "cs is NULL");
   if (!(scale > 0.f) || scale != scale) return fail(KVC_ERR_INVALID_ARG, "scale must be > 0");
   KVC_TRY(check_ws(ws, ws_bytes, value_score_workspace(*kv, w), "kvc_value_channel_score"));
+  {  // cs is written while the partials in ws are read, and must leave the caches intact
+    const uintptr_t c0 = reinterpret_cast<uintptr_t>(cs), c1 = c0 + (uintptr_t)kv->B * kv->KVH * kv->D * 4;
+    const uintptr_t w0 = reinterpret_cast<uintptr_t>(ws), w1 = w0 + value_score_workspace(*kv, w);
+    uintptr_t k0, k1, v0, v1;
+    cache_range(Kc, *kv, &k0, &k1);
+    cache_range(Vc, *kv, &v0, &v1);
+    if (overlaps(c0, c1, w0, w1) || overlaps(c0, c1, k0, k1) || overlaps(c0, c1, v0, v1))
+      return fail(KVC_ERR_INVALID_ARG, "kvc_value_channel_score: cs overlaps ws, Kc or Vc");
+  }
   // the window's attention over the compressed cache, squared and summed over the window
   // rows (mean over the group): one weight per kept token, then the weighted sums of V^2
   uint8_t* base = static_cast<uint8_t*>(ws);

@@ -139,6 +139,14 @@ def test_host_validation_without_gpu(lib):
     assert lib.kvc_channel_prune(FAKE * 512, FAKE, ctypes.byref(d), 16, 0, FAKE * 64 + 256, FAKE * 64, None) \
         == kvc.KVC_ERR_INVALID_ARG
     assert "ch_idx overlaps" in kvc.load_library().kvc_last_error_message().decode()
+    # value-channel scores: cs may not overlap the workspace or the caches
+    vws = lib.kvc_workspace_size(bnd.KVC_OP_VALUE_CHANNEL_SCORE, ctypes.byref(d), 4, 0)
+    assert vws > 0
+    assert lib.kvc_value_channel_score(FAKE * 512, 4, FAKE, FAKE * 64, ctypes.byref(d), ctypes.c_float(0.1),
+                                       FAKE * 1024 + 256, FAKE * 1024, vws, None) == kvc.KVC_ERR_INVALID_ARG
+    assert lib.kvc_value_channel_score(FAKE * 512, 4, FAKE, FAKE * 64, ctypes.byref(d), ctypes.c_float(0.1),
+                                       FAKE * 64 + 512, FAKE * 1024, vws, None) == kvc.KVC_ERR_INVALID_ARG
+    assert "cs overlaps" in kvc.load_library().kvc_last_error_message().decode()
     # Scissorhands: capacity must be a multiple of 32; no free slot -> refused
     st = bnd.ShState(1, 2, 40, 400, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0)
     assert lib.kvc_scissorhands_init(ctypes.byref(st), 0, None) == kvc.KVC_ERR_INVALID_ARG
