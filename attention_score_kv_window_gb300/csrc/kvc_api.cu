@@ -74,6 +74,16 @@ kvc_status check_ptr(const void* p, const char* what) {
   return KVC_OK;
 }
 
+// An output [out, out + out_bytes) may share no byte with any of the n input ranges [lo, hi)
+// (a range with lo == hi is absent).
+kvc_status check_out_apart(const void* out, size_t out_bytes, const uintptr_t (*in)[2], int n, const char* what) {
+  const uintptr_t o0 = reinterpret_cast<uintptr_t>(out), o1 = o0 + out_bytes;
+  for (int i = 0; i < n; ++i)
+    if (in[i][0] != in[i][1] && overlaps(o0, o1, in[i][0], in[i][1]))
+      return fail(KVC_ERR_INVALID_ARG, "%s overlaps an input or the workspace", what);
+  return KVC_OK;
+}
+
 kvc_status check_ws(void* ws, size_t have, size_t need, const char* what) {
   if (need == 0) return KVC_OK;
   if (!ws || have < need)
@@ -243,7 +253,17 @@ kvc_status kvc_window_scores(const kvc_bf16* q_win, const kvc_bf16* K, const kvc
   if (reduce != KVC_REDUCE_GQA_GROUP && reduce != KVC_REDUCE_ALL_HEADS)
     return fail(KVC_ERR_INVALID_ARG, "unknown head reduction");
   if (!(scale > 0.f) || scale != scale) return fail(KVC_ERR_INVALID_ARG, "scale must be > 0");
-  KVC_TRY(check_ws(ws, ws_bytes, scores_workspace(*kv, w, reduce), "kvc_window_scores"));
+  const size_t need = scores_workspace(*kv, w, reduce);
+  KVC_TRY(check_ws(ws, ws_bytes, need, "kvc_window_scores"));
+  {
+    uintptr_t in[3][2];
+    cache_range(K, *kv, &in[0][0], &in[0][1]);
+    in[1][0] = reinterpret_cast<uintptr_t>(q_win);
+    in[1][1] = in[1][0] + (uintptr_t)kv->B * kv->H * w * kv->D * 2;
+    in[2][0] = reinterpret_cast<uintptr_t>(ws);
+    in[2][1] = need ? in[2][0] + need : in[2][0];
+    KVC_TRY(check_out_apart(scores, (size_t)kv->B * kv->KVH * kv->S * 4, in, 3, "kvc_window_scores: scores"));
+  }
   return cuda_status(launch_window_scores(q_win, K, *kv, w, scale, causal ? 1 : 0, live_mask, reduce,
                                           scores, ws, (cudaStream_t)stream),
                      "kvc_window_scores launch");
@@ -268,6 +288,14 @@ kvc_status kvc_window_scores_noalloc(const kvc_bf16* q_win, const kvc_bf16* K,
     return fail(KVC_ERR_UNSUPPORTED,
                 "kvc_window_scores_noalloc: these shapes need %zu bytes of scratch; the fixed array holds %zu",
                 need, (size_t)KVC_NOALLOC_SCRATCH_BYTES);
+  {
+    uintptr_t in[2][2];
+    cache_range(K, *kv, &in[0][0], &in[0][1]);
+    in[1][0] = reinterpret_cast<uintptr_t>(q_win);
+    in[1][1] = in[1][0] + (uintptr_t)kv->B * kv->H * w * kv->D * 2;
+    KVC_TRY(check_out_apart(scores, (size_t)kv->B * kv->KVH * kv->S * 4, in, 2,
+                            "kvc_window_scores_noalloc: scores"));
+  }
   void* scratch = nullptr;
   KVC_TRY(cuda_status(noalloc_scratch(&scratch), "kvc_window_scores_noalloc scratch address"));
   return cuda_status(launch_window_scores(q_win, K, *kv, w, scale, causal ? 1 : 0, live_mask, reduce,
@@ -658,7 +686,19 @@ kvc_status kvc_channel_score(const kvc_bf16* q_win, int32_t w, const kvc_bf16* K
   KVC_TRY(check_ptr(q_win, "q_win"));
   KVC_TRY(check_ptr(K, "K"));
   if (!cs) return fail(KVC_ERR_INVALID_ARG, "cs is NULL");
-  KVC_TRY(check_ws(ws, ws_bytes, channel_score_workspace(*kv, idx ? k : 0, idx != nullptr), "kvc_channel_score"));
+  const size_t need = channel_score_workspace(*kv, idx ? k : 0, idx != nullptr);
+  KVC_TRY(check_ws(ws, ws_bytes, need, "kvc_channel_score"));
+  {
+    uintptr_t in[4][2];
+    cache_range(K, *kv, &in[0][0], &in[0][1]);
+    in[1][0] = reinterpret_cast<uintptr_t>(q_win);
+    in[1][1] = in[1][0] + (uintptr_t)kv->B * kv->H * w * kv->D * 2;
+    in[2][0] = reinterpret_cast<uintptr_t>(ws);
+    in[2][1] = in[2][0] + need;
+    in[3][0] = reinterpret_cast<uintptr_t>(idx);
+    in[3][1] = idx ? in[3][0] + (uintptr_t)kv->B * kv->KVH * k * 4 : in[3][0];
+    KVC_TRY(check_out_apart(cs, (size_t)kv->B * kv->KVH * kv->D * 4, in, 4, "kvc_channel_score: cs"));
+  }
   return cuda_status(launch_channel_score(q_win, w, K, *kv, idx, idx ? k : 0, cs, ws, (cudaStream_t)stream),
                      "kvc_channel_score launch");
 }
@@ -751,7 +791,20 @@ kvc_status kvc_decode_attention(const kvc_bf16* q, const int32_t* ch, const kvc_
   if (ch && !aligned16(ch)) return fail(KVC_ERR_INVALID_ARG, "ch not 16-byte aligned");
   if (live_mask && !aligned16(live_mask)) return fail(KVC_ERR_INVALID_ARG, "live_mask not 16-byte aligned");
   if (!(scale > 0.f) || scale != scale) return fail(KVC_ERR_INVALID_ARG, "scale must be > 0");
-  KVC_TRY(check_ws(ws, ws_bytes, plan_decode(*vd).part_bytes, "kvc_decode_attention"));
+  const size_t need = plan_decode(*vd).part_bytes;
+  KVC_TRY(check_ws(ws, ws_bytes, need, "kvc_decode_attention"));
+  {
+    uintptr_t in[5][2];
+    cache_range(K, *kd, &in[0][0], &in[0][1]);
+    cache_range(V, *vd, &in[1][0], &in[1][1]);
+    in[2][0] = reinterpret_cast<uintptr_t>(q);
+    in[2][1] = in[2][0] + (uintptr_t)vd->B * vd->H * vd->D * 2;
+    in[3][0] = reinterpret_cast<uintptr_t>(ws);
+    in[3][1] = in[3][0] + need;
+    in[4][0] = reinterpret_cast<uintptr_t>(ch);
+    in[4][1] = ch ? in[4][0] + (uintptr_t)kd->B * kd->KVH * kd->D * 4 : in[4][0];
+    KVC_TRY(check_out_apart(out, (size_t)vd->B * vd->H * vd->D * 4, in, 5, "kvc_decode_attention: out"));
+  }
   return cuda_status(launch_decode_attention(q, ch, K, *kd, V, *vd, live_mask, scale, out, ws, (cudaStream_t)stream),
                      "kvc_decode_attention launch");
 }

@@ -184,6 +184,23 @@ def test_host_validation_without_gpu(lib):
     # zero add-back: output overlapping the pruned input
     assert lib.kvc_zero_add_back(FAKE, ctypes.byref(kd), FAKE * 2, FAKE + 64, ctypes.byref(vd), None) \
         == kvc.KVC_ERR_INVALID_ARG
+    # outputs that share bytes with an input or the workspace: the scores with K, q or the
+    # workspace; the channel scores with their workspace; decoding's output with V
+    M = FAKE * 256  # q at M, K at 2M, the workspace at 4M, outputs elsewhere unless overlapped
+    wsz = lib.kvc_workspace_size(bnd.KVC_OP_WINDOW_SCORES, ctypes.byref(d), 4, 0)
+    for out in (2 * M + 1024, M + 16, 4 * M + 32):
+        assert lib.kvc_window_scores(M, 2 * M, ctypes.byref(d), 4, 0.1, 1, None, 0, out, 4 * M, wsz, None) \
+            == kvc.KVC_ERR_INVALID_ARG
+        assert "scores overlaps" in kvc.load_library().kvc_last_error_message().decode()
+    assert lib.kvc_window_scores_noalloc(M, 2 * M, ctypes.byref(d), 4, 0.1, 1, None, 0, 2 * M + 1024, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    csz = lib.kvc_workspace_size(bnd.KVC_OP_CHANNEL_SCORE, ctypes.byref(d), 4, 0)
+    assert lib.kvc_channel_score(M, 4, 2 * M, ctypes.byref(d), None, 0, 4 * M + 64, 4 * M, csz, None) \
+        == kvc.KVC_ERR_INVALID_ARG
+    assert "cs overlaps" in kvc.load_library().kvc_last_error_message().decode()
+    assert lib.kvc_decode_attention(M, None, 2 * M, ctypes.byref(vd), 3 * M, ctypes.byref(vd), None, 0.1,
+                                    3 * M + 4096, 4 * M, 1 << 30, None) == kvc.KVC_ERR_INVALID_ARG
+    assert "out overlaps" in kvc.load_library().kvc_last_error_message().decode()
 
 
 def test_workspace_size_rules(lib):
