@@ -738,11 +738,16 @@ def test_compress_prefill_channels_parity(B, H, KVH, D, S, w, k, protect, reduce
     assert torch.equal(cs3.view(torch.int32), cs.view(torch.int32))
 
 
+@pytest.mark.parametrize("B,KVH,S,D,C", [
+    (2, 4, 1000, 128, 64),    # one 64-row pass per CTA, ragged last pass
+    (1, 8, 40000, 64, 32),    # several passes per CTA (the next pass's loads in flight), D = 64
+    (2, 4, 20011, 128, 8),    # ~2 passes per CTA, ragged tail, few channels kept
+    (1, 2, 777, 128, 120),    # nearly all channels kept
+])
 @pytest.mark.parametrize("zero_mode", [False, True])
-def test_channel_prune_parity(zero_mode):
-    B, KVH, S, D, C = 2, 4, 1000, 128, 64
-    cs = random_scores((B, KVH, D), 71, tie_levels=40).astype(np.float32)
-    K = normal_bf16((B, KVH, S, D), 72, 1)
+def test_channel_prune_parity(zero_mode, B, KVH, S, D, C):
+    cs = random_scores((B, KVH, D), 71 + S, tie_levels=40).astype(np.float32)
+    K = normal_bf16((B, KVH, S, D), 72 + S, 1)
     ch, Ko = kvc.kvc_channel_prune(torch.from_numpy(cs).cuda(), dev_bf16(K), C, zero_mode=zero_mode)
     r_ch, r_K = O.channel_prune(cs, K, C, zero_mode=zero_mode)
     np.testing.assert_array_equal(ch.cpu().numpy(), r_ch)
