@@ -773,6 +773,7 @@ VALUE_SCORE_CASES = [
     (1, 32, 8, 128, 2000, 64),
     (2, 8, 2, 64, 333, 4),
     (1, 8, 1, 128, 700, 64),
+    (1, 32, 8, 128, 8192, 64),  # the ThinK 128K layer's compressed cache (the bench's launch shape)
 ]
 
 
