@@ -565,11 +565,14 @@ def test_scissorhands_threshold_counts_live_keys_hand_built():
     assert kvc.kvc_get_device_status() == kvc.KVC_OK
 
 
-SH_SHAPES = {"g4": (2, 8, 2, 128, 512, 400, 32), "g16_d64": (1, 16, 1, 64, 256, 5, 16)}
+SH_SHAPES = {"g4": (2, 8, 2, 128, 512, 400, 32), "g16_d64": (1, 16, 1, 64, 256, 5, 16),
+             # 64 (b, kvh) rows of 8192 slots: two CTAs per row of 4096 slots each, so the output
+             # pass runs more iterations than it loads the history state for ahead of the stream
+             "long": (8, 8, 8, 128, 8192, 400, 8)}
 
 
 @pytest.mark.parametrize("policy,shape", [("bulk", "g4"), ("queue", "g4"), ("sparse", "g4"), ("bulk", "g16_d64"),
-                                          ("queue", "g16_d64")])
+                                          ("queue", "g16_d64"), ("bulk", "long"), ("queue", "long")])
 def test_scissorhands_full_update_teacher_forced(policy, shape):
     """Full decode steps through the library.  bulk: evict m every m steps; queue: once full,
     refill an eviction queue every m steps and replace one queued token per step; sparse:
