@@ -411,7 +411,12 @@ def test_snapkv_32k_layer_sampled_kv_head():
 # ----------------------------------------------------------------------------------------
 
 
-@pytest.mark.parametrize("B,H,KVH,D,S,budget,steps", [(2, 8, 2, 128, 700, 256, 8), (2, 16, 4, 64, 3000, 2048, 4)])
+@pytest.mark.parametrize("B,H,KVH,D,S,budget,steps", [
+    (2, 8, 2, 128, 700, 256, 8), (2, 16, 4, 64, 3000, 2048, 4),
+    # B x KVH above half the SM count: one CTA per (b, kvh) and the step is one kernel (head
+    # clusters of KVH CTAs average over the heads and evict); the first is the benchmark's shape
+    (16, 32, 8, 128, 2100, 2048, 3), (40, 8, 2, 128, 1100, 1000, 3), (20, 16, 4, 64, 900, 777, 3),
+])
 def test_tova_decode_steps_teacher_forced(B, H, KVH, D, S, budget, steps):
     wl = Workload("t", B=B, H=H, KVH=KVH, D=D, S=S, w=1, k=budget, reduce="all_heads", causal=False, seed=41)
     pre = prefill_inputs(wl)
@@ -436,7 +441,11 @@ def test_tova_decode_steps_teacher_forced(B, H, KVH, D, S, budget, steps):
     for t in range(1, steps + 1):
         st = decode_step_inputs(wl, t)
         fs = dev_i32(free)
-        g_sc = kvc.kvc_tova_decode_step(dev_bf16(st["q"]), dev_bf16(st["k"]), dev_bf16(st["v"]), Kd, Vd, scale, fs)
+        qd, kd, vd = dev_bf16(st["q"]), dev_bf16(st["k"]), dev_bf16(st["v"])
+        n0 = kvc.kvc_launch_count()
+        g_sc = kvc.kvc_tova_decode_step(qd, kd, vd, Kd, Vd, scale, fs)
+        if 2 * B * KVH > torch.cuda.get_device_properties(0).multi_processor_count:
+            assert kvc.kvc_launch_count() - n0 == 1  # the one-kernel step
         r_sc, r_ev, Kc, Vc = O.tova_decode_step(Kc, Vc, st["q"], st["k"], st["v"], free, scale)
         np.testing.assert_array_equal(host_bits(Kd), Kc)
         np.testing.assert_array_equal(host_bits(Vd), Vc)
@@ -449,7 +458,7 @@ def test_tova_decode_steps_teacher_forced(B, H, KVH, D, S, budget, steps):
                 assert abs(a - c) <= 1e-3 * abs(c)
                 near += 1
         free = r_ev.astype(np.int32)  # teacher forcing: continue from the oracle's choice
-    assert near <= 2
+    assert near <= max(2, B * steps // 8)
 
 
 def test_think_128k_layer_sampled_kv_head():
